@@ -1,0 +1,295 @@
+// CPU oracle for the SparCML sparse-reduction hot path.
+//
+// TEST INFRASTRUCTURE ONLY. This file is the plain, slow, obviously correct
+// statement of what the hot path computes. Only the test-suite, the smoke
+// check and the benchmark's CPU-baseline leg may load it. It shares no code,
+// header, table or constant generator with the CUDA library.
+//
+// Source: "SparCML: High-Performance Sparse Communication for Machine
+// Learning" (Renggli, Ashkboos, Aghagolzadeh, Alistarh, Hoefler), as
+// summarised section by section on its abstract page:
+//   §2.2   Top-k SGD keeps the k largest-magnitude components per node and
+//          carries the rest forward (error feedback); quantisation Q is an
+//          element-wise stochastic operator with zero-mean noise.
+//   §4     each node carries its unapplied components as a residual.
+//   §5.1   sparse streams of index-value pairs, dense once fill-in passes a
+//          threshold delta.
+//   §5.2   reduction with any coordinate-wise associative op that has a
+//          neutral element (here: fp32 sum, neutral element +0.0).
+//   §6     stochastic QSGD quantisation in buckets with one full-precision
+//          scale per bucket.
+//   App. A floor(N/P)-style partitions with the remainder in the last part.
+//
+// Readings where the summary is silent (each one is also listed in the
+// design notes): ties at the Top-k boundary go to the lowest index; exactly
+// k_s = floor(n_s * k_num / k_den) entries are kept per segment even if some
+// are zero; streams are strictly ascending; the sum runs over nodes in
+// ascending order starting from +0.0f; the result is dense iff
+// U * dens_den > N * dens_num; the 4-bit code is sign<<3 | level with 7
+// levels of the bucket's max |v|; the rounding draw is SplitMix64 keyed by
+// (seed, node, index).
+//
+// Status codes returned (0 = OK): 1 invalid argument, 3 capacity exceeded,
+// 4 bad stream (index out of range or not strictly ascending).
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <utility>
+#include <vector>
+
+namespace {
+
+enum { OK = 0, INVALID = 1, CAPACITY = 3, BAD_STREAM = 4 };
+
+// Magnitude ordering key: the IEEE-754 bit pattern of |x|. For non-negative
+// floats the unsigned bit pattern orders like the value.
+uint32_t magnitude_key(float x) {
+  uint32_t u;
+  std::memcpy(&u, &x, sizeof u);
+  return u & 0x7fffffffu;
+}
+
+// SplitMix64 (Steele, Lea and Flood, "Fast splittable pseudorandom number
+// generators", OOPSLA 2014; the 64-bit finaliser from Vigna's splitmix64):
+// advance the state by the golden-ratio increment, then mix it.
+uint64_t splitmix64(uint64_t x) {
+  uint64_t z = x + 0x9e3779b97f4a7c15ULL;
+  z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ULL;
+  z = (z ^ (z >> 27)) * 0x94d049bb133111ebULL;
+  return z ^ (z >> 31);
+}
+
+uint64_t segment_k(uint64_t n_s, uint64_t k_num, uint64_t k_den) {
+  return n_s * k_num / k_den;  // floor(d * n_s) with d = k_num / k_den
+}
+
+}  // namespace
+
+extern "C" {
+
+uint64_t oracle_splitmix64(uint64_t x) { return splitmix64(x); }
+
+// Per-node Top-k with error feedback (§2.2, §4), segment by segment.
+//   grad, residual: [P][N] fp32 row-major; residual is updated in place.
+//   Segments of one node: [s*seg_len, min((s+1)*seg_len, N)).
+//   k_s = floor(n_s * k_num / k_den).
+//   out_idx/out_val: [P][cap]; node p's stream is written ascending at
+//   p*cap; out_nnz[p] = sum of k_s.
+int oracle_topk_ef(const float* grad, float* residual, int32_t P, uint64_t N,
+                   uint64_t seg_len, uint64_t k_num, uint64_t k_den,
+                   uint32_t* out_idx, float* out_val, uint32_t* out_nnz,
+                   uint64_t cap) {
+  if (P <= 0 || N == 0 || N > 0xffffffffULL || seg_len == 0 || k_den == 0 ||
+      k_num > k_den || k_den > 0xffffffffULL)
+    return INVALID;
+  uint64_t total_k = 0;
+  for (uint64_t b = 0; b < N; b += seg_len)
+    total_k += segment_k(std::min(seg_len, N - b), k_num, k_den);
+  if (total_k > cap) return CAPACITY;
+
+  std::vector<float> acc(N);
+  std::vector<std::pair<uint32_t, uint32_t>> keyed;  // (key, index)
+  std::vector<uint32_t> chosen;
+  for (int32_t p = 0; p < P; ++p) {
+    const float* g = grad + (uint64_t)p * N;
+    float* r = residual + (uint64_t)p * N;
+    // Error feedback: the accumulated gradient is residual + new gradient.
+    for (uint64_t i = 0; i < N; ++i) acc[i] = r[i] + g[i];
+    uint64_t written = 0;
+    for (uint64_t b = 0; b < N; b += seg_len) {
+      const uint64_t n_s = std::min(seg_len, N - b);
+      const uint64_t k_s = segment_k(n_s, k_num, k_den);
+      keyed.clear();
+      for (uint64_t i = b; i < b + n_s; ++i)
+        keyed.emplace_back(magnitude_key(acc[i]), (uint32_t)i);
+      // Largest magnitude first; among equal magnitudes the lower index first.
+      std::sort(keyed.begin(), keyed.end(),
+                [](const std::pair<uint32_t, uint32_t>& a,
+                   const std::pair<uint32_t, uint32_t>& c) {
+                  if (a.first != c.first) return a.first > c.first;
+                  return a.second < c.second;
+                });
+      chosen.clear();
+      for (uint64_t j = 0; j < k_s; ++j) chosen.push_back(keyed[j].second);
+      std::sort(chosen.begin(), chosen.end());
+      for (uint32_t i : chosen) {
+        out_idx[(uint64_t)p * cap + written] = i;
+        out_val[(uint64_t)p * cap + written] = acc[i];
+        ++written;
+      }
+      // Transmitted components leave the residual; the rest stay in it.
+      for (uint32_t i : chosen) acc[i] = 0.0f;
+    }
+    for (uint64_t i = 0; i < N; ++i) r[i] = acc[i];
+    out_nnz[p] = (uint32_t)written;
+  }
+  return OK;
+}
+
+// Select entries with |x| > thr (thr = 0 keeps the nonzeros), ascending.
+// If a node has more than cap such entries, the first cap are kept and
+// CAPACITY is returned; out_nnz[p] = min(count, cap).
+int oracle_pack(const float* x, int32_t P, uint64_t N, float thr, uint32_t* out_idx,
+                float* out_val, uint32_t* out_nnz, uint64_t cap) {
+  if (P <= 0 || N > 0xffffffffULL || !(thr >= 0.0f)) return INVALID;
+  int status = OK;
+  for (int32_t p = 0; p < P; ++p) {
+    uint64_t n = 0;
+    for (uint64_t i = 0; i < N; ++i) {
+      const float v = x[(uint64_t)p * N + i];
+      if (std::fabs(v) > thr) {
+        if (n < cap) {
+          out_idx[(uint64_t)p * cap + n] = (uint32_t)i;
+          out_val[(uint64_t)p * cap + n] = v;
+        }
+        ++n;
+      }
+    }
+    if (n > cap) status = CAPACITY;
+    out_nnz[p] = (uint32_t)std::min<uint64_t>(n, cap);
+  }
+  return status;
+}
+
+// 4-bit stochastic quantisation of each node's stream values (§2.2, §6).
+// Buckets are runs of `bucket` consecutive stream entries (the last one may
+// be short). scale = max |v| over the bucket. With r = (|v| / scale) * 7 in
+// fp32, the level is floor(r) rounded up with probability frac(r), the draw
+// being u = (h >> 40) * 2^-24 for h = sm(sm(sm(seed) ^ node) ^ index).
+// Code = (v < 0 ? 8 : 0) | level; two codes per byte, even entry in the low
+// nibble. codes: [P][ceil(cap/2)], scales: [P][ceil(cap/bucket)].
+int oracle_quantize4(const uint32_t* idx, const float* val, const uint32_t* nnz,
+                     int32_t P, uint64_t cap, uint32_t bucket, uint64_t seed,
+                     uint8_t* codes, float* scales) {
+  if (P <= 0 || bucket == 0 || cap == 0) return INVALID;
+  const uint64_t code_stride = (cap + 1) / 2;
+  const uint64_t scale_stride = (cap + bucket - 1) / bucket;
+  const uint64_t seed_mix = splitmix64(seed);
+  for (int32_t p = 0; p < P; ++p) {
+    if (nnz[p] > cap) return INVALID;
+    const uint64_t node_mix = splitmix64(seed_mix ^ (uint64_t)(uint32_t)p);
+    const uint32_t* ip = idx + (uint64_t)p * cap;
+    const float* vp = val + (uint64_t)p * cap;
+    uint8_t* cp = codes + (uint64_t)p * code_stride;
+    for (uint64_t b0 = 0; b0 < nnz[p]; b0 += bucket) {
+      const uint64_t b1 = std::min<uint64_t>(b0 + bucket, nnz[p]);
+      float scale = 0.0f;
+      for (uint64_t j = b0; j < b1; ++j) scale = std::max(scale, std::fabs(vp[j]));
+      scales[(uint64_t)p * scale_stride + b0 / bucket] = scale;
+      for (uint64_t j = b0; j < b1; ++j) {
+        const float v = vp[j];
+        uint32_t level = 0;
+        if (scale > 0.0f) {
+          const float r = (std::fabs(v) / scale) * 7.0f;
+          const float f = std::floor(r);
+          const float frac = r - f;
+          const uint64_t h = splitmix64(node_mix ^ (uint64_t)ip[j]);
+          const float u = (float)(h >> 40) * (1.0f / 16777216.0f);
+          level = (uint32_t)f + (u < frac ? 1u : 0u);
+          if (level > 7) level = 7;
+        }
+        const uint8_t code = (uint8_t)((v < 0.0f ? 8u : 0u) | level);
+        uint8_t& byte = cp[j / 2];
+        if ((j & 1) == 0)
+          byte = (uint8_t)((byte & 0xf0) | code);
+        else
+          byte = (uint8_t)((byte & 0x0f) | (code << 4));
+      }
+    }
+  }
+  return OK;
+}
+
+// Inverse of the 4-bit code: v = +-(level / 7) * scale, level 0 -> +0.0f.
+int oracle_dequantize4(const uint8_t* codes, const float* scales, const uint32_t* nnz,
+                       int32_t P, uint64_t cap, uint32_t bucket, float* val_out) {
+  if (P <= 0 || bucket == 0 || cap == 0) return INVALID;
+  const uint64_t code_stride = (cap + 1) / 2;
+  const uint64_t scale_stride = (cap + bucket - 1) / bucket;
+  float level_value[8];
+  for (int l = 0; l < 8; ++l) level_value[l] = (float)l / 7.0f;
+  for (int32_t p = 0; p < P; ++p) {
+    if (nnz[p] > cap) return INVALID;
+    for (uint64_t j = 0; j < nnz[p]; ++j) {
+      const uint8_t byte = codes[(uint64_t)p * code_stride + j / 2];
+      const uint32_t code = (j & 1) ? (byte >> 4) : (byte & 0x0f);
+      const uint32_t level = code & 7u;
+      const float scale = scales[(uint64_t)p * scale_stride + j / bucket];
+      float v = 0.0f;
+      if (level != 0) {
+        v = level_value[level] * scale;
+        if (code & 8u) v = -v;
+      }
+      val_out[(uint64_t)p * cap + j] = v;
+    }
+  }
+  return OK;
+}
+
+// Sum-reduction of P sparse streams (§5.2) with the dense switch (§5.1,
+// §5.3.3). The sum for an index runs over the nodes that hold it, in
+// ascending node order, starting from +0.0f. U = size of the index union.
+// Dense iff U * dens_den > N * dens_num; then out_dense[N] holds the sums
+// and +0.0f elsewhere. Otherwise out_idx/out_val hold the U sums ascending
+// (out_cap must be >= U). out_nnz = U in both cases.
+int oracle_sparse_reduce(const uint32_t* idx, const float* val, const uint32_t* nnz,
+                         int32_t P, uint64_t cap, uint64_t N, uint32_t dens_num,
+                         uint32_t dens_den, uint32_t* out_idx, float* out_val,
+                         uint64_t out_cap, float* out_dense, uint64_t* out_nnz,
+                         int32_t* out_is_dense) {
+  if (P <= 0 || N == 0 || N > 0xffffffffULL || dens_den == 0) return INVALID;
+  std::map<uint32_t, float> sum;
+  for (int32_t p = 0; p < P; ++p) {
+    if (nnz[p] > cap) return INVALID;
+    for (uint64_t j = 0; j < nnz[p]; ++j) {
+      const uint32_t i = idx[(uint64_t)p * cap + j];
+      if (i >= N) return BAD_STREAM;
+      if (j > 0 && i <= idx[(uint64_t)p * cap + j - 1]) return BAD_STREAM;
+      const float v = val[(uint64_t)p * cap + j];
+      auto it = sum.find(i);
+      if (it == sum.end())
+        sum.emplace(i, 0.0f + v);
+      else
+        it->second = it->second + v;
+    }
+  }
+  const uint64_t U = sum.size();
+  const bool dense = U * (uint64_t)dens_den > N * (uint64_t)dens_num;
+  *out_nnz = U;
+  *out_is_dense = dense ? 1 : 0;
+  if (dense) {
+    for (uint64_t i = 0; i < N; ++i) out_dense[i] = 0.0f;
+    for (const auto& kv : sum) out_dense[kv.first] = kv.second;
+  } else {
+    if (U > out_cap) return CAPACITY;
+    uint64_t j = 0;
+    for (const auto& kv : sum) {
+      out_idx[j] = kv.first;
+      out_val[j] = kv.second;
+      ++j;
+    }
+  }
+  return OK;
+}
+
+// Scatter each node's stream into a dense [P][N] vector, +0.0f elsewhere.
+int oracle_densify(const uint32_t* idx, const float* val, const uint32_t* nnz, int32_t P,
+                   uint64_t cap, uint64_t N, float* dense) {
+  if (P <= 0 || N > 0xffffffffULL) return INVALID;
+  for (int32_t p = 0; p < P; ++p) {
+    if (nnz[p] > cap) return INVALID;
+    float* d = dense + (uint64_t)p * N;
+    for (uint64_t i = 0; i < N; ++i) d[i] = 0.0f;
+    for (uint64_t j = 0; j < nnz[p]; ++j) {
+      const uint32_t i = idx[(uint64_t)p * cap + j];
+      if (i >= N) return BAD_STREAM;
+      d[i] = val[(uint64_t)p * cap + j];
+    }
+  }
+  return OK;
+}
+
+}  // extern "C"

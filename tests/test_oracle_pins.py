@@ -1,0 +1,396 @@
+"""Pins of the CPU oracle against what the SparCML pages and mathematics fix.
+
+No GPU. Each test checks the oracle against something other than itself:
+brute force on tiny inputs, closed forms, invariants, published known-answer
+values. A plausible slip in the oracle (a dropped term, a wrong sign or index,
+a flipped tie-break, a transposed operand) breaks at least one of these.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from top_gradient_compression_gb300 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+GOLDEN_RATIO_INC = 0x9E3779B97F4A7C15
+M64 = (1 << 64) - 1
+
+
+def keys(x):
+    return np.asarray(x, np.float32).view(np.uint32) & np.uint32(0x7FFFFFFF)
+
+
+# --------------------------------------------------------------------------
+# SplitMix64: published known-answer vector (Rosetta Code, seed 1234567).
+# --------------------------------------------------------------------------
+def test_splitmix64_known_answer_vector():
+    with open(os.path.join(GOLDEN, "splitmix64_seed1234567.txt")) as f:
+        expect = [int(l) for l in f if l.strip() and not l.startswith("#")]
+    assert len(expect) == 5
+    state = 1234567
+    for e in expect:
+        # one generator step: output = finaliser(state + increment)
+        assert oracle.splitmix64(state) == e
+        state = (state + GOLDEN_RATIO_INC) & M64
+
+
+# --------------------------------------------------------------------------
+# Top-k with error feedback (§2.2, §4).
+# --------------------------------------------------------------------------
+def brute_topk(acc_seg, k):
+    """O(n^2) definition: i is kept iff fewer than k entries beat it, where j
+    beats i when |acc_j| > |acc_i|, or they are equal and j < i."""
+    kk = keys(acc_seg).astype(np.int64)
+    n = len(kk)
+    keep = []
+    for i in range(n):
+        beaten_by = sum(1 for j in range(n) if kk[j] > kk[i] or (kk[j] == kk[i] and j < i))
+        if beaten_by < k:
+            keep.append(i)
+    return keep
+
+
+def tie_heavy(rng, shape):
+    pool = np.array([0.0, -0.0, 1.0, -1.0, 2.0, -2.0, 0.5, -0.5, 3.0], np.float32)
+    return pool[rng.integers(0, len(pool), size=shape)]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_topk_brute_force_all_k_tiny(seed):
+    rng = np.random.default_rng(seed)
+    P = int(rng.integers(1, 6))
+    N = int(rng.integers(1, 41))
+    grad = tie_heavy(rng, (P, N)) if seed % 2 else rng.standard_normal((P, N)).astype(np.float32)
+    res0 = tie_heavy(rng, (P, N)) * np.float32(0.25)
+    for k in range(0, N + 1):
+        res = res0.copy()
+        idx, val, nnz = oracle.topk_ef(grad, res, seg_len=N, k_num=k, k_den=N, cap=N + 1)
+        acc = res0 + grad
+        for p in range(P):
+            want = brute_topk(acc[p], k)
+            assert nnz[p] == k
+            assert list(idx[p, :k]) == want
+            assert np.array_equal(val[p, :k].view(np.uint32), acc[p, want].view(np.uint32))
+
+
+@pytest.mark.parametrize("N,seg_len,k_num,k_den", [(50, 16, 3, 8), (37, 5, 2, 5), (64, 64, 1, 100),
+                                                    (33, 1, 1, 1), (40, 7, 0, 3)])
+def test_topk_segments_brute_force(N, seg_len, k_num, k_den):
+    rng = np.random.default_rng(N * 7 + seg_len)
+    P = 3
+    grad = tie_heavy(rng, (P, N))
+    res = np.zeros((P, N), np.float32)
+    idx, val, nnz = oracle.topk_ef(grad, res, seg_len, k_num, k_den, cap=N)
+    for p in range(P):
+        want = []
+        for b in range(0, N, seg_len):
+            n_s = min(seg_len, N - b)
+            k_s = n_s * k_num // k_den  # App. A style: last segment takes the remainder
+            want += [b + i for i in brute_topk(grad[p, b:b + n_s], k_s)]
+        assert int(nnz[p]) == len(want)
+        assert list(idx[p, :len(want)]) == want
+
+
+def test_topk_k_equals_n_keeps_everything_and_zero_keeps_nothing():
+    rng = np.random.default_rng(3)
+    g = rng.standard_normal((2, 17)).astype(np.float32)
+    r = np.zeros_like(g)
+    idx, val, nnz = oracle.topk_ef(g, r, 17, 1, 1)
+    assert list(nnz) == [17, 17] and (idx[:, :17] == np.arange(17)).all()
+    assert not r.any()
+    r = np.zeros_like(g)
+    idx, val, nnz = oracle.topk_ef(g, r, 17, 0, 1)
+    assert list(nnz) == [0, 0] and np.array_equal(r, g)
+
+
+def test_topk_floor_rounding_of_k_matches_tiny_workload():
+    # 1% of 65,536 per node is 655 entries: k_s is floor(d * n_s).
+    assert oracle.segment_ks(65_536, 65_536, 1, 100) == [655]
+    ks = oracle.segment_ks(25_557_032, 100_000, 1, 1000)
+    assert len(ks) == 256 and ks[:-1] == [100] * 255 and ks[-1] == 57
+
+
+@pytest.mark.parametrize("steps", [1, 4])
+def test_error_feedback_invariant_transmitted_plus_residual_is_accumulated(steps):
+    """§2.2/§4: what is not sent stays in the residual, bit for bit."""
+    P, N = 3, 3000
+    res = np.zeros((P, N), np.float32)
+    for t in range(steps):
+        g = W.normal_grad(P, N, 1.0, 100 + t).numpy()
+        acc = res + g  # fp32 round-to-nearest add
+        idx, val, nnz = oracle.topk_ef(g, res, 500, 1, 50)
+        for p in range(P):
+            sel = idx[p, :nnz[p]]
+            assert np.all(np.diff(sel.astype(np.int64)) > 0)
+            sent = np.zeros(N, np.float32)
+            sent[sel] = val[p, :nnz[p]]
+            assert np.array_equal((sent + res[p]).view(np.uint32), acc[p].view(np.uint32))
+            assert not res[p, sel].view(np.uint32).any()  # +0.0 exactly
+            # every kept magnitude >= every dropped one inside each segment
+            for b in range(0, N, 500):
+                m = np.zeros(N, bool)
+                m[sel] = True
+                seg = slice(b, b + 500)
+                kept = keys(acc[p, seg][m[seg]])
+                drop = keys(acc[p, seg][~m[seg]])
+                assert kept.min() >= drop.max()
+
+
+# --------------------------------------------------------------------------
+# Sparse sum-reduction (§5.2) and dense switch (§5.1, §5.3.3).
+# --------------------------------------------------------------------------
+def brute_dense_sum(idx, val, nnz, N):
+    out = np.zeros(N, np.float32)  # neutral element +0.0
+    for p in range(idx.shape[0]):
+        d = np.zeros(N, np.float32)
+        d[idx[p, :nnz[p]]] = val[p, :nnz[p]]
+        out = out + d
+    return out
+
+
+def random_streams(rng, P, N, maxk, tie_vals=False):
+    cap = maxk
+    idx = np.zeros((P, cap), np.uint32)
+    val = np.zeros((P, cap), np.float32)
+    nnz = np.zeros(P, np.uint32)
+    for p in range(P):
+        k = int(rng.integers(0, maxk + 1))
+        sel = np.sort(rng.choice(N, size=k, replace=False))
+        idx[p, :k] = sel
+        val[p, :k] = tie_heavy(rng, k) if tie_vals else rng.standard_normal(k).astype(np.float32)
+        nnz[p] = k
+    return idx, val, nnz
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_reduce_equals_brute_force_dense_sum(seed):
+    rng = np.random.default_rng(1000 + seed)
+    P = int(rng.integers(1, 9))
+    N = int(rng.integers(1, 200))
+    idx, val, nnz = random_streams(rng, P, N, min(N, 60), tie_vals=seed % 2 == 1)
+    r = oracle.sparse_reduce(idx, val, nnz, N)
+    want = brute_dense_sum(idx, val, nnz, N)
+    union = set()
+    for p in range(P):
+        union |= set(idx[p, :nnz[p]].tolist())
+    assert r["nnz"] == len(union)
+    assert r["is_dense"] == (4 * len(union) > N)
+    if r["is_dense"]:
+        assert np.array_equal(r["dense"].view(np.uint32), want.view(np.uint32))
+    else:
+        assert list(r["idx"]) == sorted(union)
+        assert np.array_equal(r["val"].view(np.uint32), want[sorted(union)].view(np.uint32))
+
+
+def test_reduce_size_bounds_disjoint_and_identical():
+    N, P, k = 4096, 8, 100
+    rng = np.random.default_rng(5)
+    perm = rng.permutation(N)[: P * k].reshape(P, k)
+    idx = np.sort(perm, axis=1).astype(np.uint32)
+    val = rng.standard_normal((P, k)).astype(np.float32)
+    nnz = np.full(P, k, np.uint32)
+    r = oracle.sparse_reduce(idx, val, nnz, N)
+    assert r["nnz"] == P * k  # App. B: union bound tight for disjoint sets (allgather)
+    same = np.tile(idx[:1], (P, 1))
+    r2 = oracle.sparse_reduce(same, val, nnz, N)
+    assert r2["nnz"] == k  # §5.3.1: full overlap keeps k items
+    for P2 in (1, 3, 16):
+        i2, v2, n2 = uniform_small = W.uniform_streams(P2, N, 300, 77)
+        assert oracle.sparse_reduce(i2, v2, n2, N)["nnz"] <= min(N, P2 * 300)
+
+
+def test_dense_switch_exactly_at_quarter():
+    N = 64
+    for U, dense in ((16, False), (17, True)):
+        idx = np.arange(U, dtype=np.uint32)[None, :]
+        val = np.ones((1, U), np.float32)
+        r = oracle.sparse_reduce(idx, val, np.array([U], np.uint32), N)
+        assert r["nnz"] == U and r["is_dense"] == dense
+        if dense:
+            assert r["dense"][:U].tolist() == [1.0] * U and not r["dense"][U:].any()
+
+
+def test_reduce_signed_zero_and_cancellation_keep_structural_support():
+    idx = np.array([[3, 5], [3, 5]], np.uint32)
+    val = np.array([[-0.0, 2.5], [-0.0, -2.5]], np.float32)
+    r = oracle.sparse_reduce(idx, val, np.array([2, 2], np.uint32), 1000)
+    assert r["nnz"] == 2 and list(r["idx"]) == [3, 5]
+    assert r["val"].view(np.uint32).tolist() == [0, 0]  # +0.0 both (sum from +0.0)
+
+
+def test_reduce_rejects_bad_streams():
+    with pytest.raises(oracle.OracleError):
+        oracle.sparse_reduce(np.array([[4, 2]], np.uint32), np.ones((1, 2), np.float32),
+                             np.array([2], np.uint32), 10)
+    with pytest.raises(oracle.OracleError):
+        oracle.sparse_reduce(np.array([[4, 10]], np.uint32), np.ones((1, 2), np.float32),
+                             np.array([2], np.uint32), 10)
+
+
+@pytest.mark.parametrize("P,dnum,dden", [(2, 1, 100), (8, 1, 100), (8, 10, 100), (32, 5, 100)])
+def test_density_law_uniform_indices(P, dnum, dden):
+    """App. B.1 / uniform model: E[U]/N = 1 - (1 - d)^P for k = dN distinct indices."""
+    N = 1 << 18
+    k = N * dnum // dden
+    idx, val, nnz = W.uniform_streams(P, N, k, 900 + P)
+    r = oracle.sparse_reduce(idx, val, nnz, N)
+    d = k / N
+    q = 1 - (1 - d) ** P
+    assert abs(r["nnz"] / N - q) <= 6 * math.sqrt(q * (1 - q) / N)
+    assert r["is_dense"] == (4 * r["nnz"] > N)
+
+
+def test_density_law_small_n_mean_over_seeds():
+    """Figure 7's setting (N = 512): mean union size over seeds follows the closed form."""
+    N, P, k, M = 512, 8, 32, 300
+    us = []
+    for s in range(M):
+        idx, val, nnz = W.uniform_streams(P, N, k, 5000 + s)
+        us.append(oracle.sparse_reduce(idx, val, nnz, N)["nnz"])
+    q = 1 - (1 - k / N) ** P
+    sd = math.sqrt(N * q * (1 - q))
+    assert abs(np.mean(us) - N * q) <= 6 * sd / math.sqrt(M)
+    assert max(us) <= min(N, P * k)
+
+
+# --------------------------------------------------------------------------
+# 4-bit stochastic quantisation (§2.2, §6).
+# --------------------------------------------------------------------------
+def unpack(codes, n):
+    lo = codes & 0x0F
+    hi = codes >> 4
+    out = np.empty(codes.shape[:-1] + (codes.shape[-1] * 2,), np.uint8)
+    out[..., 0::2] = lo
+    out[..., 1::2] = hi
+    return out[..., :n]
+
+
+def test_quantizer_bounds_levels_signs_and_max_entry():
+    rng = np.random.default_rng(11)
+    P, cap, bucket = 3, 1300, 512
+    val = (rng.laplace(size=(P, cap)) * 1e-3).astype(np.float32)
+    idx = np.tile(np.arange(cap, dtype=np.uint32) * 3, (P, 1))
+    nnz = np.array([1300, 1025, 7], np.uint32)
+    codes, scales = oracle.quantize4(idx, val, nnz, bucket, seed=42)
+    deq = oracle.dequantize4(codes, scales, nnz, cap, bucket)
+    cl = unpack(codes, cap)
+    for p in range(P):
+        n = int(nnz[p])
+        for b0 in range(0, n, bucket):
+            b1 = min(b0 + bucket, n)
+            v = val[p, b0:b1]
+            s = scales[p, b0 // bucket]
+            assert s == np.abs(v).max()
+            lv = cl[p, b0:b1] & 7
+            sg = cl[p, b0:b1] >> 3
+            assert np.array_equal(sg, (v < 0).astype(np.uint8))
+            for j in range(len(v)):
+                r = Fraction(float(abs(v[j]))) / Fraction(float(s)) * 7
+                assert math.floor(r - Fraction(1, 10**5)) <= lv[j] <= math.ceil(r + Fraction(1, 10**5))
+            assert np.all(np.abs(deq[p, b0:b1].astype(np.float64) - v) <= s / 7 * (1 + 1e-6))
+            m = int(np.argmax(np.abs(v)))
+            assert deq[p, b0 + m] == v[m]  # the bucket maximum is exact (level 7)
+
+
+def test_quantizer_zero_bucket_gives_positive_zeros():
+    idx = np.arange(10, dtype=np.uint32)[None]
+    val = np.array([[0.0, -0.0] * 5], np.float32)
+    codes, scales = oracle.quantize4(idx, val, np.array([10], np.uint32), 4, seed=1)
+    assert not scales.any() and not codes.any()
+    deq = oracle.dequantize4(codes, scales, np.array([10], np.uint32), 10, 4)
+    assert not deq.view(np.uint32).any()
+
+
+def test_quantizer_rounds_up_with_probability_frac():
+    """r = 2.25 for every entry: about a quarter round up to level 3."""
+    n = 40000
+    val = np.full((1, n), 2.25, np.float32)
+    val[0, 0] = 7.0  # bucket scale 7 => r = |v| exactly
+    idx = np.arange(n, dtype=np.uint32)[None]
+    codes, _ = oracle.quantize4(idx, val, np.array([n], np.uint32), n, seed=9)
+    lv = unpack(codes, n)[0, 1:] & 7
+    assert set(np.unique(lv).tolist()) <= {2, 3}
+    frac_up = np.mean(lv == 3)
+    assert abs(frac_up - 0.25) <= 6 * math.sqrt(0.25 * 0.75 / (n - 1))
+
+
+def test_quantizer_is_unbiased_over_seeds():
+    """§2.2: zero-mean quantisation noise, E[Q(v)] = v."""
+    rng = np.random.default_rng(2)
+    n, M = 64, 3000
+    val = rng.standard_normal((1, n)).astype(np.float32)
+    idx = np.arange(n, dtype=np.uint32)[None] * 11
+    nnz = np.array([n], np.uint32)
+    acc = np.zeros(n)
+    for s in range(M):
+        c, sc = oracle.quantize4(idx, val, nnz, n, seed=s * 7919 + 1)
+        acc += oracle.dequantize4(c, sc, nnz, n, n)[0]
+    scale = np.abs(val).max()
+    sd = scale / 14  # level spacing scale/7, Bernoulli sd <= 1/2 of it
+    assert np.all(np.abs(acc / M - val[0]) <= 6 * sd / math.sqrt(M) + 1e-7)
+
+
+def test_quantizer_draw_depends_only_on_seed_node_index():
+    rng = np.random.default_rng(4)
+    n = 512
+    val = rng.standard_normal((2, n)).astype(np.float32)
+    val[:, 0] = 10.0  # same scale in both nodes
+    idx = np.tile(np.arange(n, dtype=np.uint32), (2, 1))
+    nnz = np.array([n, n], np.uint32)
+    c1, _ = oracle.quantize4(idx, val, nnz, n, seed=5)
+    val2 = val.copy()
+    val2[:, 1:] = val[:, 1:][:, ::-1]  # move other entries around
+    c2, _ = oracle.quantize4(idx, val2, nnz, n, seed=5)
+    l1, l2 = unpack(c1, n), unpack(c2, n)
+    # entry j of val2 equals entry (n - j) of val: different index, so its draw may differ,
+    # but the unchanged entry 0 and its code are fixed
+    assert l1[0, 0] == l2[0, 0] == 7
+    # same values, same (node, index) => same code whatever the other entries are
+    val3 = val.copy()
+    val3[0, 2:] *= 0.5
+    c3, _ = oracle.quantize4(idx, val3, nnz, n, seed=5)
+    assert unpack(c3, n)[0, 1] == l1[0, 1]
+    # a different node key changes some draws
+    c4, _ = oracle.quantize4(idx[::-1].copy(), val[::-1].copy(), nnz, n, seed=5)
+    assert not np.array_equal(unpack(c4, n)[1], l1[0])
+
+
+# --------------------------------------------------------------------------
+# Pack and densify (§5.1).
+# --------------------------------------------------------------------------
+def test_pack_and_densify_round_trip():
+    rng = np.random.default_rng(8)
+    P, N = 4, 999
+    x = rng.standard_normal((P, N)).astype(np.float32)
+    x[rng.random((P, N)) < 0.7] = 0.0
+    x[0, 5] = -0.0
+    idx, val, nnz, st = oracle.pack(x, 0.0, N)
+    assert st == oracle.OK
+    d = oracle.densify(idx, val, nnz, N)
+    assert np.array_equal(d, x)
+    for p in range(P):
+        assert int(nnz[p]) == sum(1 for i in range(N) if abs(float(x[p, i])) > 0.0)
+    idx2, val2, nnz2, st2 = oracle.pack(x, 0.5, N)
+    for p in range(P):
+        sel = idx2[p, :nnz2[p]]
+        assert np.all(np.abs(x[p, sel]) > 0.5)
+        rest = np.setdiff1d(np.arange(N), sel)
+        assert np.all(np.abs(x[p, rest]) <= 0.5)
+    _, _, nnz3, st3 = oracle.pack(x, 0.0, 5)
+    assert st3 == oracle.CAPACITY and list(nnz3) == [5] * P
+
+
+def test_reduce_single_node_is_densify():
+    rng = np.random.default_rng(9)
+    N = 100
+    idx = np.sort(rng.choice(N, size=90, replace=False)).astype(np.uint32)[None]
+    val = rng.standard_normal((1, 90)).astype(np.float32)
+    nnz = np.array([90], np.uint32)
+    r = oracle.sparse_reduce(idx, val, nnz, N)
+    d = oracle.densify(idx, val, nnz, N)[0]
+    assert r["is_dense"]
+    assert np.array_equal((d + np.float32(0)).view(np.uint32), r["dense"].view(np.uint32))
