@@ -1,0 +1,478 @@
+#!/usr/bin/env python3
+"""Benchmark of the SparCML-style sparse-reduction hot path on GB300.
+
+One step = one error-feedback step of the whole path for P emulated nodes:
+Top-k with residual (guess, stream and select kernels), packing into
+{uint32 index, fp32 value} streams, and the sparse sum-reduce with the dense
+switch (tile and fix-up kernels). The default workload is the ResNet-50-sized
+one: P=8 nodes of N=25,557,032 fp32 gradients, Top-k 0.1% per 100,000-entry
+layer block. ``value`` is the gradient input consumed per second
+(P * N * 4 bytes per step) with inputs resident in HBM; ``e2e`` is the same
+metric with every step's gradients copied in from pinned host memory and the
+reduced result copied back.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs an independent replica on its own GPU (the
+path has no cross-GPU exchange); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-reduce step input GB/s and elems/s at 1 GB300; % of HBM peak (ncu)"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["resnet50", "asr"], default="resnet50")
+    ap.add_argument("--e2e-steps", type=int, default=40)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-segments", type=int, default=48,
+                    help="segments per node in the bounded CPU-baseline sample")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# ranks
+# ---------------------------------------------------------------------------
+class Ranks:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = False
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend=backend)
+            self.pg = True
+
+    def device(self):
+        return torch.device("cuda", self.local) if torch.cuda.is_available() else torch.device("cpu")
+
+    def barrier(self):
+        if self.pg:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max(self, x: float) -> float:
+        return reduce_max(x, self.pg, self.device())
+
+    def close(self):
+        if self.pg:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+def reduce_max(x: float, pg: bool, device) -> float:
+    """Max of a float over all ranks (identity without a process group)."""
+    if not pg:
+        return float(x)
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, device):
+        self.samples = []
+        self.proc = None
+        try:
+            ident = str(device.index)
+            try:
+                u = torch.cuda.get_device_properties(device).uuid
+                ident = "GPU-" + str(u) if not str(u).startswith("GPU-") else str(u)
+            except Exception:
+                pass
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+                 "-i", ident, "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.samples.append((time.time(), parts))
+
+    def window(self, t0, t1):
+        return [p for (t, p) in self.samples if t0 <= t <= t1]
+
+    def summary(self, t0, t1):
+        w = self.window(t0, t1)
+        if not w:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in w if num(p[0]) is not None]
+        mx = [num(p[1]) for p in w if num(p[1]) is not None]
+        reasons = sorted({self.REASONS[i] for p in w for i in range(4)
+                          if p[3 + i].lower().startswith("active")})
+        pw = [num(p[2]) for p in w if num(p[2]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(w),
+                "power_w_max": max(pw) if pw else None}
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+def workload_spec(name):
+    from top_gradient_compression_gb300 import workloads as W
+    if name == "resnet50":
+        c = W.RESNET50
+        return dict(name="resnet50", P=c["P"], N=c["N"], seg_len=c["seg_len"], k_num=c["k_num"],
+                    k_den=c["k_den"], quant=False,
+                    desc=("ResNet-50-sized EF step: P=8 nodes x N=25,557,032 fp32, Top-k 0.1% per "
+                          "100,000-entry layer block with error feedback, sparse sum-reduce with "
+                          "dense switch at 25%"),
+                    gen=lambda t, dev: W.resnet50_grads(t, device=dev),
+                    data="synthetic: N(0, sigma_b^2), sigma_b log-uniform in [1e-4, 1e-1] per "
+                         "100k-entry block (seeded torch generator on device)")
+    c = W.ASR
+    return dict(name="asr", P=c["P"], N=c["N"], seg_len=c["seg_len"], k_num=c["k_num"],
+                k_den=c["k_den"], quant=True, bucket=c["bucket"],
+                desc=("LSTM/ASR-like EF step: P=16 x N=67,108,864 fp32, Top-k 1%, 4-bit "
+                      "stochastic quantisation in buckets of 512, fused dequantise + sparse reduce"),
+                gen=lambda t, dev: W.asr_grads(t, device=dev),
+                data="synthetic: Laplace(0, 1e-3) (seeded torch generator on device)")
+
+
+def file_sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def load_traffic(kernel, src):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current source of the kernel (else None)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+        e = t[kernel]
+        if e.get("source_sha") != file_sha(src):
+            return None
+        return e
+    except Exception:
+        return None
+
+
+def hbm_peak():
+    try:
+        with open(PEAKS_FILE) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle as it stands, on a bounded sample
+# ---------------------------------------------------------------------------
+def cpu_sample_run(spec, grads_host, nseg, steps):
+    """Oracle Top-k+EF and reduce over the first nseg segments of every node for
+    `steps` EF steps. Returns (seconds, bytes of gradient input processed)."""
+    import oracle
+    P, L = spec["P"], spec["seg_len"]
+    n = min(spec["N"], nseg * L)
+    res = np.zeros((P, n), np.float32)
+    t0 = time.perf_counter()
+    for s in range(steps):
+        g = grads_host[s % len(grads_host)][:, :n]
+        g = np.ascontiguousarray(g)
+        oi, ov, on = oracle.topk_ef(g, res, L, spec["k_num"], spec["k_den"])
+        if spec["quant"]:
+            from top_gradient_compression_gb300 import workloads as W
+            codes, scales = oracle.quantize4(oi, ov, on, spec["bucket"], W.quant_seed(s))
+            ov = oracle.dequantize4(codes, scales, on, oi.shape[1], spec["bucket"])
+        oracle.sparse_reduce(oi, ov, on, n)
+    dt = time.perf_counter() - t0
+    return dt, P * n * 4 * steps, n
+
+
+def run_reference(args, ranks):
+    """--impl reference: the CPU oracle timed on host cores (rank 0 only)."""
+    if ranks.rank != 0:
+        return
+    from top_gradient_compression_gb300 import workloads as W
+    spec = workload_spec(args.workload)
+    P, L = spec["P"], spec["seg_len"]
+    nseg = 1
+    n = min(spec["N"], nseg * L)
+    grads = [spec["gen"](0, "cpu")[:, :n].numpy().copy()]
+    import oracle
+    res = np.zeros((P, n), np.float32)
+
+    def step(s):
+        oi, ov, on = oracle.topk_ef(grads[0], res, L, spec["k_num"], spec["k_den"])
+        if spec["quant"]:
+            c, sc = oracle.quantize4(oi, ov, on, spec["bucket"], W.quant_seed(s))
+            ov = oracle.dequantize4(c, sc, on, oi.shape[1], spec["bucket"])
+        oracle.sparse_reduce(oi, ov, on, n)
+
+    for s in range(args.warmup):
+        step(s)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        step(s)
+    dt = time.perf_counter() - t0
+    v = P * n * 4 * args.steps / dt / 1e9
+    sample = (f"oracle (1 thread): {nseg} segment(s) of {L} entries per node x {P} nodes "
+              f"= {P * n:,} gradient entries per step")
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s",
+            "elems_per_s": P * n * args.steps / dt, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": spec["data"], "config": {"workload": spec["desc"], "sample": sample},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our path
+# ---------------------------------------------------------------------------
+def run_ours(args, ranks):
+    from top_gradient_compression_gb300 import api, workloads as W
+    dev = ranks.device()
+    if dev.type != "cuda":
+        raise RuntimeError("bench.py --impl ours needs a CUDA device")
+    torch.cuda.set_device(dev)
+    spec = workload_spec(args.workload)
+    P, N, L, kn, kd = spec["P"], spec["N"], spec["seg_len"], spec["k_num"], spec["k_den"]
+    NB = 3 if spec["name"] == "resnet50" else 2  # distinct gradient batches, cycled
+    grads = [spec["gen"](t, dev) for t in range(NB)]
+    res = torch.zeros((P, N), device=dev)
+    cap = api.segment_k_total(N, L, kn, kd)
+    tk_out = (torch.empty((P, cap), dtype=torch.int32, device=dev),
+              torch.empty((P, cap), dtype=torch.float32, device=dev),
+              torch.empty((P,), dtype=torch.int32, device=dev))
+    tk_ws = api.workspace(api.topk_ef_workspace_size(P, N, L, kn, kd), dev)
+    rd_ws = api.workspace(api.reduce_workspace_size(P, N), dev)
+    rd_out = api.reduce_out(N, dev)
+    if spec["quant"]:
+        bucket = spec["bucket"]
+        codes = torch.zeros((P, (cap + 1) // 2), dtype=torch.uint8, device=dev)
+        scales = torch.zeros((P, (cap + bucket - 1) // bucket), device=dev)
+        qstat = api.status_word(dev)
+
+    K, Wm = args.steps, args.warmup
+    ev_tk = [api.make_events(4) for _ in range(K)]
+    ev_rd = [api.make_events(3) for _ in range(K)]
+    ev_q = [api.make_events(2) for _ in range(K)] if spec["quant"] else None
+
+    def step(i, grad, timed=False):
+        api.topk_ef(grad, res, L, kn, kd, out=tk_out, ws=tk_ws,
+                    events=ev_tk[i] if timed else None)
+        if spec["quant"]:
+            if timed:
+                ev_q[i][0].record()
+            api.quantize4(tk_out[0], tk_out[1], tk_out[2], bucket, W.quant_seed(i), codes=codes,
+                          scales=scales, status=qstat)
+            if timed:
+                ev_q[i][1].record()
+            api.sparse_reduce_q4(tk_out[0], codes, scales, tk_out[2], bucket, N, out=rd_out,
+                                 ws=rd_ws)
+        else:
+            api.sparse_reduce(tk_out[0], tk_out[1], tk_out[2], N, out=rd_out, ws=rd_ws,
+                              events=ev_rd[i] if timed else None)
+
+    for i in range(Wm):
+        step(i, grads[i % NB])
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev)
+    time.sleep(1.0)  # let nvidia-smi start sampling
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = api.launch_count()
+    ranks.barrier()
+    torch.cuda.synchronize()
+    t_host0 = time.time()
+    ev0.record()
+    for i in range(K):
+        step(i, grads[i % NB], timed=True)
+    ev1.record()
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    ranks.barrier()
+    launches = api.launch_count() - launches0
+    ms_local = ev0.elapsed_time(ev1) / K
+    clk = clocks.summary(t_host0, t_host1)
+    clocks.stop()
+    for word in (tk_ws, rd_ws):
+        st = api.get_status(word)
+        if st != 0:
+            raise RuntimeError(f"device status {api.STATUS.get(st, st)} after the timed steps")
+    ms = ranks.max(ms_local)
+
+    def mean_ms(evs, a, b):
+        return float(np.mean([e[a].elapsed_time(e[b]) for e in evs]))
+    kern = {"topk_guess": mean_ms(ev_tk, 0, 1), "topk_stream": mean_ms(ev_tk, 1, 2),
+            "topk_select": mean_ms(ev_tk, 2, 3)}
+    if spec["quant"]:
+        kern["quantize4"] = mean_ms(ev_q, 0, 1)
+    else:
+        kern["reduce_tile"] = mean_ms(ev_rd, 0, 1)
+        kern["reduce_fixup"] = mean_ms(ev_rd, 1, 2)
+
+    U = int(rd_out.nnz.item())
+    is_dense = bool(rd_out.is_dense.item())
+    sum_nnz = int(tk_out[2].sum().item())
+    in_bytes_step = P * N * 4
+    value = ranks.world * in_bytes_step / (ms * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+    stream_bytes = 12 * P * N  # read grad + residual, write residual
+    achieved = stream_bytes / (kern["topk_stream"] * 1e-3) / 1e9
+    traffic = load_traffic("topk_stream_kernel",
+                           os.path.join(ROOT, "top_gradient_compression_gb300", "csrc",
+                                        "topk_ef.cu"))
+    reduce_in = 8 * sum_nnz if not spec["quant"] else sum_nnz // 2 + 4 * P * ((cap + 511) // 512) + 4 * sum_nnz
+
+    # ---- end to end: pinned host gradients in, reduced result out, every step
+    e2e = None
+    if args.e2e_steps > 0:
+        hg = [torch.empty((P, N), dtype=torch.float32, pin_memory=True) for _ in range(2)]
+        for b in range(2):
+            hg[b].copy_(grads[b])
+        dgrad = torch.empty((P, N), device=dev)
+        cap_out = rd_out.idx.numel()
+        h_idx = torch.empty(cap_out, dtype=torch.int32, pin_memory=True)
+        h_val = torch.empty(cap_out, dtype=torch.float32, pin_memory=True)
+        h_dense = torch.empty(N, dtype=torch.float32, pin_memory=True)
+        h_small = torch.empty(2, dtype=torch.int32, pin_memory=True)
+        small = torch.empty(2, dtype=torch.int32, device=dev)
+        d2h = 0
+        E = args.e2e_steps
+        for i in range(2):  # warm-up of the copy path
+            dgrad.copy_(hg[i % 2], non_blocking=True)
+            step(i, dgrad)
+        torch.cuda.synchronize()
+        ranks.barrier()
+        t0 = time.perf_counter()
+        for i in range(E):
+            dgrad.copy_(hg[i % 2], non_blocking=True)
+            step(i, dgrad)
+            small[0:1].copy_(rd_out.nnz)
+            small[1:2].copy_(rd_out.is_dense)
+            h_small.copy_(small, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+            u, dn = int(h_small[0]), int(h_small[1])
+            if dn:
+                h_dense.copy_(rd_out.dense, non_blocking=True)
+                d2h += 8 + 4 * N
+            else:
+                h_idx[:u].copy_(rd_out.idx[:u], non_blocking=True)
+                h_val[:u].copy_(rd_out.val[:u], non_blocking=True)
+                d2h += 8 + 8 * u
+            torch.cuda.current_stream().synchronize()
+        dt = ranks.max(time.perf_counter() - t0)
+        e2e = {"value": ranks.world * in_bytes_step * E / dt / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": in_bytes_step, "d2h_bytes_per_step": d2h // E,
+               "ms_per_step": dt / E * 1e3, "steps": E}
+        del hg, dgrad
+
+    # ---- CPU baseline (rank 0, single GPU only)
+    cpu = None
+    if not args.no_cpu_baseline and ranks.world == 1:
+        nseg = min(args.cpu_segments, (N + L - 1) // L)
+        n = min(N, nseg * L)
+        gh = [grads[b][:, :n].cpu().numpy() for b in range(min(2, NB))]
+        dt, nbytes, _ = cpu_sample_run(spec, gh, nseg, 2)
+        cpu = {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": (f"first {nseg} segments ({n:,} entries) of each of the {P} nodes, 2 EF "
+                          f"steps of Top-k + reduce; {nbytes / 4:,.0f} gradient entries in "
+                          f"{dt:.1f} s on one host core")}
+
+    if ranks.rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s",
+        "elems_per_s": ranks.world * P * N / (ms * 1e-3),
+        "n_gpus": ranks.world, "steps": K, "warmup": Wm, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": spec["data"],
+        "config": {"workload": spec["desc"], "P": P, "N": N, "seg_len": L,
+                   "k_per_node": cap, "units": "value = P*N*4 gradient bytes per step / time",
+                   "l2": "inputs larger than L2 (3 x 818 MB gradient batches + 818 MB residual), "
+                         "no flush",
+                   "parallelism": f"replicas x{ranks.world} (no cross-GPU exchange)"},
+        "roofline": {"bound": "hbm", "kernel": "topk_stream_kernel",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": stream_bytes,
+                     "traffic": None if traffic is None else traffic["dram_bytes_per_launch"],
+                     "launch_ms": kern["topk_stream"]},
+        "kernels_ms": kern,
+        "reduce": {"input_bytes": reduce_in, "sum_nnz": sum_nnz, "U": U, "is_dense": is_dense,
+                   "input_GBps": reduce_in / ((kern.get("reduce_tile", 0) +
+                                               kern.get("reduce_fixup", 0)) * 1e-3) / 1e9
+                   if not spec["quant"] else None},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    ranks = Ranks()
+    try:
+        if args.impl == "reference":
+            run_reference(args, ranks)
+        else:
+            run_ours(args, ranks)
+    finally:
+        ranks.close()
+
+
+if __name__ == "__main__":
+    main()

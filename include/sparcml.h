@@ -1,0 +1,231 @@
+/*
+ * sparcml.h - C ABI of the GB300 (sm_103a) sparse-reduction hot path.
+ *
+ * The operations follow "SparCML: High-Performance Sparse Communication for
+ * Machine Learning" (Renggli, Ashkboos, Aghagolzadeh, Alistarh, Hoefler):
+ * P data-parallel nodes each hold a fp32 gradient of N entries. Each node
+ * keeps its k largest-magnitude components and carries the rest forward as
+ * a residual (Top-k with error feedback, §2.2 and §4), sends them as a
+ * sparse stream of index-value pairs (§5.1), optionally quantised to 4 bits
+ * with stochastic rounding (§2.2, §6), and the P streams are sum-reduced
+ * (§5.2) into a sparse result that switches to a dense fp32 vector once its
+ * fill-in passes a threshold (§5.1, §5.3.3). Here the P nodes are slices of
+ * one GPU's memory and the "network" is the reduce kernel.
+ *
+ * Conventions shared by every entry point:
+ *   - Layout. A node-major batch of P vectors of N fp32 values is one
+ *     row-major [P][N] array: node p starts at element p*N. A batch of P
+ *     sparse streams is idx uint32 [P][cap], val float [P][cap] and nnz
+ *     uint32 [P]: node p's entries are idx[p*cap + j], val[p*cap + j] for
+ *     j < nnz[p], with idx strictly ascending and < N (node-local indices).
+ *   - Memory. Every array argument is DEVICE memory owned by the caller,
+ *     except where a parameter says "host". The library never allocates,
+ *     frees or keeps device memory between calls: scratch space comes from
+ *     the caller as a workspace (`ws`, `ws_bytes`), sized by the matching
+ *     *_workspace_size function. A workspace may be reused by later calls
+ *     but not by two calls in flight at the same time.
+ *   - Streams. `stream` is a cudaStream_t (NULL = legacy default stream).
+ *     All work is enqueued on it and the call returns without waiting:
+ *     the calls are non-blocking in the sense of §7 (MPI-3 style
+ *     non-blocking collectives). Only sparcml_get_status synchronises.
+ *   - Errors. A return value other than SPARCML_OK means nothing was
+ *     enqueued (bad argument, workspace too small, capacity too small) or
+ *     a CUDA launch failed (SPARCML_ERR_CUDA). Problems found on the device
+ *     (an index out of range or out of order, a selection that does not
+ *     fit, a wait that ran out) never trap: the first one is recorded in a
+ *     device status word (the first 4 bytes of the workspace, or the
+ *     explicit `status` pointer) and read back by sparcml_get_status.
+ *   - Limits. 1 <= P <= 65535, 1 <= N <= 2^32 - 1 (indices are uint32).
+ *
+ * Results are deterministic: the same inputs give the same bits on every
+ * run (fixed summation order, no floating-point atomics).
+ */
+#ifndef SPARCML_H
+#define SPARCML_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum sparcml_status {
+  SPARCML_OK = 0,
+  SPARCML_ERR_INVALID_ARG = 1, /* bad pointer, size or parameter           */
+  SPARCML_ERR_WORKSPACE = 2,   /* ws_bytes below the *_workspace_size     */
+  SPARCML_ERR_CAPACITY = 3,    /* an output does not fit its capacity     */
+  SPARCML_ERR_BAD_STREAM = 4,  /* index >= N, or not strictly ascending   */
+  SPARCML_ERR_TIMEOUT = 6,     /* a bounded device-side wait ran out      */
+  SPARCML_ERR_CUDA = 7         /* a CUDA runtime call or launch failed    */
+};
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* sparcml_status_string(int status);
+
+/* Number of GPU kernels this library has launched in this process so far
+ * (all devices, all threads). Lets a caller count the kernels inside a
+ * timed region. */
+uint64_t sparcml_launch_count(void);
+
+/* Synchronises `stream`, then returns the first device-detected error
+ * recorded in the status word at `status_word` (a workspace pointer, or the
+ * explicit status pointer given to densify/quantize/dequantize) and resets
+ * it to SPARCML_OK. Returns SPARCML_ERR_CUDA if synchronisation fails. */
+int sparcml_get_status(void* status_word, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Top-k selection with error feedback, fused with packing (§2.2, §4, §5.1;
+ * layer-wise sparsification of §8.4 via segments; last segment takes the
+ * remainder as in App. A).
+ *
+ * For every node p and every element i:
+ *     acc = residual[p][i] + grad[p][i]            (one fp32 add, RN)
+ * Each node is cut into segments [s*seg_len, min((s+1)*seg_len, N)) of
+ * length n_s; segment s keeps exactly k_s = floor(n_s * k_num / k_den)
+ * entries: those with the largest |acc|, comparing the bit patterns of
+ * |acc| as unsigned integers, ties going to the lowest index. The kept
+ * entries are written to node p's stream in ascending index order
+ * (segment after segment), with val = acc; out_nnz[p] = sum of k_s.
+ * residual[p][i] becomes +0.0f at kept entries and acc everywhere else.
+ *
+ *   grad      [P][N] fp32, read only.
+ *   residual  [P][N] fp32, read and overwritten in place (the EF state).
+ *   seg_len   segment length, >= 1 (values >= N mean one segment per node).
+ *   k_num, k_den  density d = k_num / k_den, 0 <= k_num <= k_den < 2^32.
+ *   out_idx, out_val  [P][cap]; out_nnz [P].  cap >= sum of k_s, else
+ *             SPARCML_ERR_CAPACITY.
+ *   ws        >= sparcml_topk_ef_workspace_size(P, N, seg_len, k_num, k_den)
+ *             bytes, 256-byte aligned.
+ * Non-finite inputs are not rejected; NaN has the largest magnitude key.
+ * ------------------------------------------------------------------------ */
+size_t sparcml_topk_ef_workspace_size(int32_t P, uint64_t N, uint64_t seg_len,
+                                      uint32_t k_num, uint32_t k_den);
+int sparcml_topk_ef(const float* grad, float* residual, int32_t P, uint64_t N,
+                    uint64_t seg_len, uint32_t k_num, uint32_t k_den,
+                    uint32_t* out_idx, float* out_val, uint32_t* out_nnz,
+                    uint64_t cap, void* ws, size_t ws_bytes, void* stream);
+
+/* Same as sparcml_topk_ef, plus a profiling hook: `events` is a host array
+ * of 4 cudaEvent_t (entries may be NULL; the array itself may be NULL),
+ * recorded on `stream` before the guess kernel, before the stream kernel,
+ * before the select kernel and after it, so a caller can time each kernel
+ * with CUDA events on the launching stream. */
+int sparcml_topk_ef_traced(const float* grad, float* residual, int32_t P, uint64_t N,
+                           uint64_t seg_len, uint32_t k_num, uint32_t k_den,
+                           uint32_t* out_idx, float* out_val, uint32_t* out_nnz,
+                           uint64_t cap, void* ws, size_t ws_bytes, void* stream,
+                           void* const* events);
+
+/* ------------------------------------------------------------------------
+ * Pack a naturally sparse dense batch into streams (§5.1): node p's stream
+ * holds every i with |x[p][i]| > thr, ascending (thr = 0 keeps nonzeros;
+ * -0.0 is not kept). thr must be >= 0 and not NaN.
+ * If a node has more than cap such entries, its first cap (lowest indices)
+ * are written, out_nnz[p] = cap and SPARCML_ERR_CAPACITY is recorded in the
+ * workspace status word.
+ *   x [P][N] fp32;  out_* as above;  ws >= sparcml_pack_workspace_size(P, N).
+ * ------------------------------------------------------------------------ */
+size_t sparcml_pack_workspace_size(int32_t P, uint64_t N);
+int sparcml_pack(const float* x, int32_t P, uint64_t N, float thr, uint32_t* out_idx,
+                 float* out_val, uint32_t* out_nnz, uint64_t cap, void* ws,
+                 size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * 4-bit stochastic quantisation of stream values (QSGD-style, §2.2 and §6;
+ * the pages give 2/4/8-bit outputs and buckets with one full-precision
+ * scale each).
+ *
+ * Node p's entries are cut into buckets of `bucket` consecutive stream
+ * entries (the last may be short). scale = max |val| over the bucket (fp32).
+ * For each entry with value v and index i:
+ *     r     = (|v| / scale) * 7            (fp32, RN, no contraction)
+ *     level = floor(r) + (u < r - floor(r)),  clamped to 7;  level = 0 if
+ *             scale == 0
+ *     u     = (h >> 40) * 2^-24,  h = sm(sm(sm(seed) ^ p) ^ i)
+ * where sm(x) is one SplitMix64 output for state x (x + 0x9e3779b97f4a7c15
+ * through the SplitMix64 finaliser). code = (v < 0 ? 8 : 0) | level, two
+ * codes per byte, the even entry in the low nibble.
+ *   idx, val, nnz  input streams [P][cap], [P][cap], [P].
+ *   bucket   entries per bucket, even, >= 2.
+ *   codes    [P][ceil(cap/2)] bytes: bytes past ceil(nnz[p]/2) untouched.
+ *   scales   [P][ceil(cap/bucket)] fp32: entries past the last bucket
+ *            untouched.
+ *   status   device int32 status word (may be NULL): records
+ *            SPARCML_ERR_CAPACITY if some nnz[p] > cap (that node is
+ *            treated as having cap entries).
+ * ------------------------------------------------------------------------ */
+int sparcml_quantize4(const uint32_t* idx, const float* val, const uint32_t* nnz,
+                      int32_t P, uint64_t cap, uint32_t bucket, uint64_t seed,
+                      uint8_t* codes, float* scales, int32_t* status, void* stream);
+
+/* Inverse map: val_out[p][j] = (code & 8 ? -1 : 1) * (level / 7.0f) * scale,
+ * with level / 7.0f rounded to fp32 first and level 0 giving +0.0f.
+ * val_out [P][cap]; entries past nnz[p] untouched. */
+int sparcml_dequantize4(const uint8_t* codes, const float* scales, const uint32_t* nnz,
+                        int32_t P, uint64_t cap, uint32_t bucket, float* val_out,
+                        int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Sparse sum-reduction of P streams with the adaptive dense switch
+ * (§5.2 sum with neutral element 0; §5.1 / §5.3.3 switch to dense; the
+ * result size U is the size of the index union, App. B).
+ *
+ * For every index i in the union of the P streams:
+ *     out[i] = ((+0.0f + v_p0) + v_p1) + ...   over the nodes p0 < p1 < ...
+ *              that hold i, in ascending node order (fp32 RN adds).
+ * U = number of distinct indices. The result is dense iff
+ *     U * dens_den > N * dens_num          (dens_num/dens_den = 1/4: > 25%)
+ * Sparse result: out_idx/out_val [0, U) ascending; out_dense untouched.
+ * Dense result: out_dense [N] holds out[i], +0.0f where no node has i;
+ * out_idx/out_val hold unspecified values.
+ * *out_nnz = U and *out_is_dense = 0/1 in both cases (device scalars).
+ *   out_cap  capacity of out_idx/out_val, >= floor(N * dens_num / dens_den)
+ *            (enough for any sparse result).
+ *   ws       >= sparcml_sparse_reduce_workspace_size(P, N) bytes.
+ * Streams must be strictly ascending with indices < N; otherwise
+ * SPARCML_ERR_BAD_STREAM is recorded in the workspace and the outputs are
+ * unspecified (all memory accesses stay in bounds).
+ * ------------------------------------------------------------------------ */
+size_t sparcml_sparse_reduce_workspace_size(int32_t P, uint64_t N);
+int sparcml_sparse_reduce(const uint32_t* idx, const float* val, const uint32_t* nnz,
+                          int32_t P, uint64_t cap, uint64_t N, uint32_t dens_num,
+                          uint32_t dens_den, uint32_t* out_idx, float* out_val,
+                          uint64_t out_cap, float* out_dense, uint32_t* out_nnz,
+                          int32_t* out_is_dense, void* ws, size_t ws_bytes, void* stream);
+
+/* Same as sparcml_sparse_reduce, plus a profiling hook: `events` is a host
+ * array of 3 cudaEvent_t (entries may be NULL), recorded on `stream` before
+ * the tile kernel, between it and the dense fix-up kernel, and after. */
+int sparcml_sparse_reduce_traced(const uint32_t* idx, const float* val, const uint32_t* nnz,
+                                 int32_t P, uint64_t cap, uint64_t N, uint32_t dens_num,
+                                 uint32_t dens_den, uint32_t* out_idx, float* out_val,
+                                 uint64_t out_cap, float* out_dense, uint32_t* out_nnz,
+                                 int32_t* out_is_dense, void* ws, size_t ws_bytes, void* stream,
+                                 void* const* events);
+
+/* Same reduction, with each stream's values given in the 4-bit form of
+ * sparcml_quantize4 (codes, scales, bucket) and decoded on load exactly as
+ * sparcml_dequantize4 does. Bit-identical to dequantize4 followed by
+ * sparcml_sparse_reduce. */
+int sparcml_sparse_reduce_q4(const uint32_t* idx, const uint8_t* codes, const float* scales,
+                             const uint32_t* nnz, int32_t P, uint64_t cap, uint32_t bucket,
+                             uint64_t N, uint32_t dens_num, uint32_t dens_den,
+                             uint32_t* out_idx, float* out_val, uint64_t out_cap,
+                             float* out_dense, uint32_t* out_nnz, int32_t* out_is_dense,
+                             void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Densify (§5.1 representation switch): dense[p][i] = val of node p's
+ * entry with index i, +0.0f where the stream has none. dense [P][N].
+ * Entries with idx >= N are skipped and SPARCML_ERR_BAD_STREAM is recorded
+ * in *status (may be NULL). Duplicate indices: one of them wins.
+ * ------------------------------------------------------------------------ */
+int sparcml_densify(const uint32_t* idx, const float* val, const uint32_t* nnz, int32_t P,
+                    uint64_t cap, uint64_t N, float* dense, int32_t* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARCML_H */

@@ -1,0 +1,196 @@
+"""GPU parity of the sparse sum-reduce with the dense switch (SparCML §5.1-§5.3,
+App. B), of pack, densify and the 4-bit quantiser (§2.2, §6), against the oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from top_gradient_compression_gb300 import api, workloads as W
+
+from gpu_helpers import DEV, bits, check_reduce, streams_to_dev, u32
+
+pytestmark = pytest.mark.gpu
+
+
+def rand_streams(rng, P, N, maxk, cap=None):
+    cap = max(maxk, 1) if cap is None else cap
+    idx = np.zeros((P, cap), np.uint32)
+    val = np.zeros((P, cap), np.float32)
+    nnz = np.zeros(P, np.uint32)
+    for p in range(P):
+        k = int(rng.integers(0, maxk + 1))
+        idx[p, :k] = np.sort(rng.choice(N, size=k, replace=False))
+        val[p, :k] = rng.standard_normal(k).astype(np.float32)
+        nnz[p] = k
+    return idx, val, nnz
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_reduce_random(seed):
+    rng = np.random.default_rng(seed)
+    P = int(rng.integers(1, 12))
+    N = int(rng.choice([1, 7, 1000, 8192, 8193, 3 * 8192 + 7, 100_003]))
+    maxk = int(min(N, rng.choice([1, 50, 3000, 30_000])))
+    idx, val, nnz = rand_streams(rng, P, N, maxk)
+    check_reduce(idx, val, nnz, N, repeat=2)
+
+
+def test_reduce_all_empty_and_single_entry():
+    N = 100_000
+    idx = np.zeros((3, 4), np.uint32)
+    check_reduce(idx, np.zeros((3, 4), np.float32), np.zeros(3, np.uint32), N)
+    idx[1, 0] = N - 1
+    r = check_reduce(idx, np.ones((3, 4), np.float32), np.array([0, 1, 0], np.uint32), N)
+    assert r["nnz"] == 1
+
+
+@pytest.mark.parametrize("N", [64, 8192 * 4, 8192 * 4 + 4])
+def test_reduce_switch_exactly_at_quarter(N):
+    for extra, dense in ((0, False), (1, True)):
+        U = N // 4 + extra
+        rng = np.random.default_rng(N + extra)
+        sel = np.sort(rng.choice(N, size=U, replace=False)).astype(np.uint32)
+        # spread the union over 3 nodes so no single node decides it
+        parts = np.array_split(sel, 3)
+        cap = max(len(x) for x in parts)
+        idx = np.zeros((3, cap), np.uint32)
+        val = np.zeros((3, cap), np.float32)
+        nnz = np.zeros(3, np.uint32)
+        for p, part in enumerate(parts):
+            idx[p, :len(part)] = part
+            val[p, :len(part)] = rng.standard_normal(len(part))
+            nnz[p] = len(part)
+        r = check_reduce(idx, val, nnz, N)
+        assert r["nnz"] == U and r["is_dense"] == dense
+
+
+def test_reduce_dense_paths():
+    rng = np.random.default_rng(11)
+    N = 200_000
+    # (a) one node alone is above the threshold: dense from the first tile
+    idx, val, nnz = W.uniform_streams(3, N, 60_000, 21)
+    check_reduce(idx, val, nnz, N, repeat=2)
+    # (b) every node small, the union crosses 25% part-way: leading tiles are fixed up
+    idx, val, nnz = W.uniform_streams(16, N, 4_000, 22)
+    r = check_reduce(idx, val, nnz, N, repeat=2)
+    assert r["is_dense"]
+
+
+@pytest.mark.parametrize("P,dnum,dden", [(2, 1, 1000), (4, 10, 100), (8, 5, 100), (32, 1, 100)])
+def test_reduce_density_sweep_cells_exact(P, dnum, dden):
+    idx, val, nnz = W.sweep_streams(P, dnum, dden)
+    check_reduce(idx, val, nnz, W.SWEEP_N)
+
+
+def test_reduce_density_sweep_all_cells_follow_the_closed_form():
+    """All 24 (P, d) cells at N = 4,194,304: U/N tracks 1 - (1 - d)^P (App. B.1) and
+    the result is dense exactly when 4U > N."""
+    N = W.SWEEP_N
+    for P in W.SWEEP_P:
+        for dnum, dden in W.SWEEP_D:
+            idx, val, nnz = W.sweep_streams(P, dnum, dden)
+            di, dv, dn = streams_to_dev(idx, val, nnz)
+            out = api.sparse_reduce(di, dv, dn, N)
+            U = int(out.nnz.item())
+            d = (N * dnum // dden) / N
+            q = 1 - (1 - d) ** P
+            assert abs(U / N - q) <= 6 * math.sqrt(q * (1 - q) / N) + 1e-12, (P, dnum, dden)
+            assert bool(out.is_dense.item()) == (4 * U > N)
+            assert U <= min(N, P * (N * dnum // dden))
+
+
+def test_reduce_logreg_workload_exact():
+    idx, val, nnz = W.logreg_streams()
+    r = check_reduce(idx, val, nnz, W.LOGREG["N"], repeat=2)
+    assert not r["is_dense"]
+
+
+def test_reduce_detects_bad_streams():
+    N = 50_000
+    cases = [np.array([[5, 3, 9, 0]], np.uint32),        # not ascending
+             np.array([[5, 5, 9, 0]], np.uint32),        # duplicate
+             np.array([[5, 9, N, 0]], np.uint32),        # index out of range
+             np.array([[9000, 20, 30000, 40000]], np.uint32)]  # out of order across tiles
+    nn = [3, 3, 3, 4]
+    for idx, n in zip(cases, nn):
+        di, dv, dn = streams_to_dev(idx, np.ones((1, 4), np.float32), np.array([n], np.uint32))
+        ws = api.workspace(api.reduce_workspace_size(1, N), DEV)
+        api.sparse_reduce(di, dv, dn, N, ws=ws)
+        assert api.get_status(ws) == api.STATUS_CODE["SPARCML_ERR_BAD_STREAM"]
+        assert api.get_status(ws) == 0  # reading clears it
+
+
+def test_pack_parity_and_capacity():
+    rng = np.random.default_rng(2)
+    P, N = 3, 100_003
+    x = rng.standard_normal((P, N)).astype(np.float32)
+    x[rng.random((P, N)) < 0.9] = 0.0
+    x[0, 1] = -0.0
+    xd = torch.from_numpy(x).to(DEV)
+    for thr, cap in ((0.0, N), (1.5, N), (0.0, 5000)):
+        oi, ov, on, ost = oracle.pack(x, thr, cap)
+        idx, val, nnz, ws = api.pack(xd, thr, cap)
+        st = api.get_status(ws)
+        assert st == (api.STATUS_CODE["SPARCML_ERR_CAPACITY"] if ost else 0)
+        assert np.array_equal(u32(nnz), on)
+        for p in range(P):
+            n = int(on[p])
+            assert np.array_equal(u32(idx)[p, :n], oi[p, :n])
+            assert np.array_equal(bits(val.cpu().numpy()[p, :n]), bits(ov[p, :n]))
+
+
+def test_densify_parity():
+    rng = np.random.default_rng(4)
+    P, N = 4, 9999
+    idx, val, nnz = rand_streams(rng, P, N, 3000)
+    di, dv, dn = streams_to_dev(idx, val, nnz)
+    got = api.densify(di, dv, dn, N)
+    assert np.array_equal(bits(got.cpu().numpy()), bits(oracle.densify(idx, val, nnz, N)))
+
+
+def test_quantize_dequantize_parity():
+    rng = np.random.default_rng(6)
+    P, cap, bucket = 3, 2000, 512
+    val = (rng.laplace(size=(P, cap)) * 1e-3).astype(np.float32)
+    val[1, 600:700] = 0.0  # a partly zero bucket
+    val[2, :] = 0.0        # an all-zero node
+    idx = np.sort(rng.choice(1 << 24, size=(P, cap), replace=False), axis=1).astype(np.uint32)
+    nnz = np.array([2000, 1025, 7], np.uint32)
+    for seed in (0, 123456789, 2**63 + 5):
+        oc, osc = oracle.quantize4(idx, val, nnz, bucket, seed)
+        di, dv, dn = streams_to_dev(idx, val, nnz)
+        codes, scales = api.quantize4(di, dv, dn, bucket, seed)
+        gc, gs = codes.cpu().numpy(), scales.cpu().numpy()
+        for p in range(P):
+            n = int(nnz[p])
+            lo_o, hi_o = oc[p] & 15, oc[p] >> 4
+            lo_g, hi_g = gc[p] & 15, gc[p] >> 4
+            assert np.array_equal(lo_g[: (n + 1) // 2], lo_o[: (n + 1) // 2])
+            assert np.array_equal(hi_g[: n // 2], hi_o[: n // 2])
+            nb = (n + bucket - 1) // bucket
+            assert np.array_equal(bits(gs[p, :nb]), bits(osc[p, :nb]))
+        od = oracle.dequantize4(oc, osc, nnz, cap, bucket)
+        gd = api.dequantize4(codes, scales, dn, cap, bucket).cpu().numpy()
+        for p in range(P):
+            n = int(nnz[p])
+            assert np.array_equal(bits(gd[p, :n]), bits(od[p, :n]))
+
+
+def test_reduce_q4_equals_dequantize_then_reduce():
+    rng = np.random.default_rng(8)
+    P, N, k, bucket = 6, 300_000, 20_000, 512
+    idx, val, nnz = W.uniform_streams(P, N, k, 31, std=1e-3)
+    nnz[2] = 12_345
+    seed = W.quant_seed(0)
+    oc, osc = oracle.quantize4(idx, val, nnz, bucket, seed)
+    deq = oracle.dequantize4(oc, osc, nnz, k, bucket)
+    ref = oracle.sparse_reduce(idx, deq, nnz, N)
+    di, dv, dn = streams_to_dev(idx, val, nnz)
+    codes, scales = api.quantize4(di, dv, dn, bucket, seed)
+    out = api.sparse_reduce_q4(di, codes, scales, dn, bucket, N)
+    U = int(out.nnz.item())
+    assert U == ref["nnz"] and bool(out.is_dense.item()) == ref["is_dense"]
+    assert np.array_equal(u32(out.idx[:U]), ref["idx"])
+    assert np.array_equal(bits(out.val[:U].cpu().numpy()), bits(ref["val"]))

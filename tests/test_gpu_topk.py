@@ -1,0 +1,126 @@
+"""GPU parity of Top-k with error feedback (SparCML §2.2, §4, §8.4) against the
+oracle: indices, nnz, values and the residual must match bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from top_gradient_compression_gb300 import api, workloads as W
+
+from gpu_helpers import DEV, bits, check_topk_steps, u32
+
+pytestmark = pytest.mark.gpu
+
+
+def make(dist, P, N, seed):
+    rng = np.random.default_rng(seed)
+    if dist == "normal":
+        return rng.standard_normal((P, N)).astype(np.float32)
+    if dist == "laplace":
+        return (rng.laplace(size=(P, N)) * 1e-3).astype(np.float32)
+    if dist == "ties":  # a handful of magnitudes: large equal-key groups at the boundary
+        pool = np.array([0.0, -0.0, 1.0, -1.0, 2.0, -2.0, 0.5, -0.5, 3.0], np.float32)
+        return pool[rng.integers(0, len(pool), size=(P, N))]
+    if dist == "const":  # one magnitude everywhere: every entry ties
+        return np.where(rng.random((P, N)) < 0.5, 1.5, -1.5).astype(np.float32)
+    raise ValueError(dist)
+
+
+def test_tiny_workload_three_steps():
+    c = W.TINY
+    grads = [W.tiny_grads(t).numpy() for t in range(c["steps"])]
+    check_topk_steps(grads, c["seg_len"], c["k_num"], c["k_den"])
+
+
+@pytest.mark.parametrize("P,N,seg_len,k_num,k_den,dist", [
+    (3, 1001, 100, 3, 100, "normal"),          # node bases not 16-byte aligned
+    (2, 50_000, 7_000, 1, 50, "ties"),          # ragged segments, heavy ties
+    (1, 3 * 8192 + 5, 8192, 1, 10, "normal"),   # chunk-sized segments + ragged tail
+    (2, 40, 1, 1, 1, "normal"),                 # segment length 1, k = n
+    (2, 1000, 1000, 0, 1, "normal"),            # k = 0
+    (2, 777, 777, 1, 1, "ties"),                # k = n with ties
+    (1, 1 << 21, 1 << 21, 1, 100, "normal"),    # one long segment: 4-CTA cluster
+    (2, 4_194_304, 4_194_304, 1, 100, "laplace"),  # 8-CTA cluster
+    (2, 300_000, 100_000, 1, 1000, "normal"),   # layer-sized segments, k = 100
+    (4, 65_536, 65_536, 30, 100, "ties"),       # dense selection (30%)
+    (2, 20_000, 20_000, 1, 100, "const"),       # all keys equal: lowest indices win
+])
+def test_topk_shapes(P, N, seg_len, k_num, k_den, dist):
+    grads = [make(dist, P, N, s) for s in range(2)]
+    check_topk_steps(grads, seg_len, k_num, k_den)
+
+
+def test_topk_const_keeps_lowest_indices():
+    P, N = 2, 100_000  # sampled segment, every key equal: candidate slots overflow
+    g = make("const", P, N, 7)
+    res = torch.zeros((P, N), device=DEV)
+    idx, val, nnz = api.topk_ef(torch.from_numpy(g).to(DEV), res, N, 1, 100)
+    k = N // 100
+    assert (u32(idx)[:, :k] == np.arange(k)).all()
+    check_topk_steps([g], N, 1, 100)
+
+
+def test_topk_sample_overestimates_then_falls_back():
+    """Large values only where the guess pass samples: too few candidates, so the
+    select pass re-reads the segment. The result is still exact."""
+    P, N = 1, 1 << 20
+    n_runs, run = 256, 32
+    g = (np.random.default_rng(3).standard_normal((P, N)) * 0.01).astype(np.float32)
+    for i in range(n_runs):
+        st = (i * (N - run) // (n_runs - 1)) & ~(run - 1)
+        g[0, st:st + run] = 10.0 + i
+    check_topk_steps([g], N, 1, 100)  # k = 10,485 > 8,192 sampled entries
+
+
+def test_topk_nonzero_initial_residual():
+    rng = np.random.default_rng(5)
+    P, N = 3, 70_000
+    res0 = rng.standard_normal((P, N)).astype(np.float32)
+    grads = [rng.standard_normal((P, N)).astype(np.float32) for _ in range(3)]
+    check_topk_steps(grads, 30_000, 1, 100, res0=res0)
+
+
+def test_topk_deterministic_and_capacity_checked():
+    P, N = 2, 100_000
+    g = torch.from_numpy(make("normal", P, N, 1)).to(DEV)
+    r1 = torch.zeros_like(g)
+    r2 = torch.zeros_like(g)
+    a = api.topk_ef(g, r1, N, 1, 100)
+    b = api.topk_ef(g, r2, N, 1, 100)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1]) and torch.equal(r1, r2)
+    with pytest.raises(api.SparcmlError):
+        small = (torch.empty((P, 10), dtype=torch.int32, device=DEV),
+                 torch.empty((P, 10), device=DEV), torch.empty(P, dtype=torch.int32, device=DEV))
+        api.topk_ef(g, r1, N, 1, 100, out=small)
+
+
+@pytest.mark.slow
+def test_resnet50_workload_sampled_segments_ten_steps():
+    """Full ResNet-50-sized workload (P=8, N=25,557,032, 256 layer blocks, k=0.1%)
+    through the same calls the benchmark times; the oracle checks a sample of
+    (node, segment) pairs over all 10 EF steps (segments are independent)."""
+    c = W.RESNET50
+    P, N, L = c["P"], c["N"], c["seg_len"]
+    picks = [(0, 0), (0, 137), (5, 1), (7, 255), (3, 200)]
+    res_g = torch.zeros((P, N), device=DEV)
+    ws = api.workspace(api.topk_ef_workspace_size(P, N, L, c["k_num"], c["k_den"]), DEV)
+    res_o = {pk: np.zeros((1, min(L, N - pk[1] * L)), np.float32) for pk in picks}
+    for t in range(c["steps"]):
+        g = W.resnet50_grads(t, device=DEV)
+        idx, val, nnz = api.topk_ef(g, res_g, L, c["k_num"], c["k_den"], ws=ws)
+        assert api.get_status(ws) == 0
+        gi, gv, gr = u32(idx), bits(val.cpu().numpy()), None
+        for (p, s) in picks:
+            lo, n = s * L, res_o[(p, s)].shape[1]
+            gs = g[p, lo:lo + n].cpu().numpy()[None]
+            oi, ov, on = oracle.topk_ef(gs, res_o[(p, s)], n, c["k_num"], c["k_den"])
+            k = int(on[0])
+            off = s * (L * c["k_num"] // c["k_den"])
+            assert np.array_equal(gi[p, off:off + k], oi[0, :k] + lo)
+            assert np.array_equal(gv[p, off:off + k], bits(ov[0, :k]))
+            assert np.array_equal(bits(res_g[p, lo:lo + n].cpu().numpy()), bits(res_o[(p, s)][0]))
+        assert (u32(nnz) == api.segment_k_total(N, L, c["k_num"], c["k_den"])).all()
+    # every node's stream is strictly ascending and inside [0, N)
+    for p in range(P):
+        s = gi[p, :int(u32(nnz)[p])].astype(np.int64)
+        assert (np.diff(s) > 0).all() and s[-1] < N

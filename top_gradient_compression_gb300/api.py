@@ -1,0 +1,276 @@
+"""Python binding of the C ABI (include/sparcml.h): argument marshalling only.
+
+Every function takes torch CUDA tensors, checks dtype/shape/contiguity,
+passes raw device pointers and the current CUDA stream to libsparcml.so and
+returns without synchronising. All computation happens in the library's
+kernels; there is no fallback path.
+
+Stream layout (SparCML §5.1 sparse streams): ``idx`` int32 [P, cap] (read as
+uint32 by the library), ``val`` float32 [P, cap], ``nnz`` int32 [P].
+"""
+from __future__ import annotations
+
+import ctypes as C
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+
+OK = 0
+STATUS = {0: "SPARCML_OK", 1: "SPARCML_ERR_INVALID_ARG", 2: "SPARCML_ERR_WORKSPACE",
+          3: "SPARCML_ERR_CAPACITY", 4: "SPARCML_ERR_BAD_STREAM", 6: "SPARCML_ERR_TIMEOUT",
+          7: "SPARCML_ERR_CUDA"}
+STATUS_CODE = {v: k for k, v in STATUS.items()}
+
+
+class SparcmlError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn}: {_lib.load().sparcml_status_string(code).decode()} ({code})")
+        self.code = code
+
+
+def _check(fn: str, code: int):
+    if code != OK:
+        raise SparcmlError(fn, code)
+
+
+def _cuda(t: torch.Tensor, dtype, name: str, ndim: int | None = None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+    return t.data_ptr()
+
+
+def _opt_ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def workspace(nbytes: int, device) -> torch.Tensor:
+    """Caller-owned scratch for one library call (256-byte aligned by torch's allocator)."""
+    ws = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    assert ws.data_ptr() % 256 == 0
+    ws[:4].zero_()  # status word
+    return ws
+
+
+def status_word(device) -> torch.Tensor:
+    return torch.zeros(64, dtype=torch.int32, device=device)
+
+
+def make_events(n: int, stream=None) -> list:
+    """CUDA events usable by the *_traced entry points (each recorded once so the
+    underlying cudaEvent_t exists)."""
+    s = torch.cuda.current_stream() if stream is None else stream
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for e in evs:
+        e.record(s)
+    return evs
+
+
+def _event_array(events):
+    if events is None:
+        return None
+    arr = (C.c_void_p * len(events))(*[e.cuda_event for e in events])
+    return arr
+
+
+def launch_count() -> int:
+    return int(_lib.load().sparcml_launch_count())
+
+
+def get_status(word: torch.Tensor, stream=None) -> int:
+    """Synchronise the stream, return and clear the first device-side error."""
+    return int(_lib.load().sparcml_get_status(word.data_ptr(), _stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+# Top-k with error feedback (§2.2, §4) fused with packing (§5.1).
+# ---------------------------------------------------------------------------
+def topk_ef_workspace_size(P: int, N: int, seg_len: int, k_num: int, k_den: int) -> int:
+    return int(_lib.load().sparcml_topk_ef_workspace_size(P, N, seg_len, k_num, k_den))
+
+
+def segment_k_total(N: int, seg_len: int, k_num: int, k_den: int) -> int:
+    L = min(seg_len, N)
+    nseg = (N + L - 1) // L
+    return (nseg - 1) * (L * k_num // k_den) + (N - (nseg - 1) * L) * k_num // k_den
+
+
+def topk_ef(grad: torch.Tensor, residual: torch.Tensor, seg_len: int, k_num: int, k_den: int,
+            out=None, ws: torch.Tensor | None = None, stream=None, events=None):
+    """Returns (idx int32 [P, cap], val float32 [P, cap], nnz int32 [P]); residual is updated.
+    ``events``: optional 4 CUDA events (see make_events) recorded around the three kernels."""
+    gp = _cuda(grad, torch.float32, "grad", 2)
+    rp = _cuda(residual, torch.float32, "residual", 2)
+    if residual.shape != grad.shape:
+        raise ValueError("grad and residual shapes differ")
+    P, N = grad.shape
+    if out is None:
+        cap = max(segment_k_total(N, seg_len, k_num, k_den), 1)
+        out = (torch.empty((P, cap), dtype=torch.int32, device=grad.device),
+               torch.empty((P, cap), dtype=torch.float32, device=grad.device),
+               torch.empty((P,), dtype=torch.int32, device=grad.device))
+    idx, val, nnz = out
+    ip = _cuda(idx, torch.int32, "out_idx", 2)
+    vp = _cuda(val, torch.float32, "out_val", 2)
+    np_ = _cuda(nnz, torch.int32, "out_nnz", 1)
+    cap = idx.shape[1]
+    if ws is None:
+        ws = workspace(topk_ef_workspace_size(P, N, seg_len, k_num, k_den), grad.device)
+    lib = _lib.load()
+    if events is None:
+        _check("sparcml_topk_ef", lib.sparcml_topk_ef(
+            gp, rp, P, N, seg_len, k_num, k_den, ip, vp, np_, cap, ws.data_ptr(), ws.numel(),
+            _stream(stream)))
+    else:
+        assert len(events) == 4
+        _check("sparcml_topk_ef_traced", lib.sparcml_topk_ef_traced(
+            gp, rp, P, N, seg_len, k_num, k_den, ip, vp, np_, cap, ws.data_ptr(), ws.numel(),
+            _stream(stream), _event_array(events)))
+    return idx, val, nnz
+
+
+# ---------------------------------------------------------------------------
+# Pack (§5.1).
+# ---------------------------------------------------------------------------
+def pack_workspace_size(P: int, N: int) -> int:
+    return int(_lib.load().sparcml_pack_workspace_size(P, N))
+
+
+def pack(x: torch.Tensor, thr: float, cap: int, out=None, ws=None, stream=None):
+    xp = _cuda(x, torch.float32, "x", 2)
+    P, N = x.shape
+    if out is None:
+        out = (torch.empty((P, cap), dtype=torch.int32, device=x.device),
+               torch.empty((P, cap), dtype=torch.float32, device=x.device),
+               torch.empty((P,), dtype=torch.int32, device=x.device))
+    idx, val, nnz = out
+    if ws is None:
+        ws = workspace(pack_workspace_size(P, N), x.device)
+    _check("sparcml_pack", _lib.load().sparcml_pack(
+        xp, P, N, float(thr), _cuda(idx, torch.int32, "out_idx", 2),
+        _cuda(val, torch.float32, "out_val", 2), _cuda(nnz, torch.int32, "out_nnz", 1),
+        idx.shape[1], ws.data_ptr(), ws.numel(), _stream(stream)))
+    return idx, val, nnz, ws
+
+
+# ---------------------------------------------------------------------------
+# 4-bit stochastic quantisation (§2.2, §6).
+# ---------------------------------------------------------------------------
+def quantize4(idx, val, nnz, bucket: int, seed: int, codes=None, scales=None, status=None,
+              stream=None):
+    P, cap = val.shape
+    if codes is None:
+        codes = torch.zeros((P, (cap + 1) // 2), dtype=torch.uint8, device=val.device)
+    if scales is None:
+        scales = torch.zeros((P, (cap + bucket - 1) // bucket), dtype=torch.float32,
+                             device=val.device)
+    _check("sparcml_quantize4", _lib.load().sparcml_quantize4(
+        _cuda(idx, torch.int32, "idx", 2), _cuda(val, torch.float32, "val", 2),
+        _cuda(nnz, torch.int32, "nnz", 1), P, cap, bucket, seed & (2**64 - 1),
+        _cuda(codes, torch.uint8, "codes", 2), _cuda(scales, torch.float32, "scales", 2),
+        _opt_ptr(status), _stream(stream)))
+    return codes, scales
+
+
+def dequantize4(codes, scales, nnz, cap: int, bucket: int, out=None, status=None, stream=None):
+    P = codes.shape[0]
+    if out is None:
+        out = torch.zeros((P, cap), dtype=torch.float32, device=codes.device)
+    _check("sparcml_dequantize4", _lib.load().sparcml_dequantize4(
+        _cuda(codes, torch.uint8, "codes", 2), _cuda(scales, torch.float32, "scales", 2),
+        _cuda(nnz, torch.int32, "nnz", 1), P, cap, bucket,
+        _cuda(out, torch.float32, "val_out", 2), _opt_ptr(status), _stream(stream)))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Sparse sum-reduce with the dense switch (§5.1-§5.3).
+# ---------------------------------------------------------------------------
+@dataclass
+class ReduceOut:
+    idx: torch.Tensor        # int32 [out_cap]; first nnz entries valid when sparse
+    val: torch.Tensor        # float32 [out_cap]
+    dense: torch.Tensor      # float32 [N]; valid when is_dense
+    nnz: torch.Tensor        # int32 [1] device scalar: U
+    is_dense: torch.Tensor   # int32 [1] device scalar
+
+
+def reduce_workspace_size(P: int, N: int) -> int:
+    return int(_lib.load().sparcml_sparse_reduce_workspace_size(P, N))
+
+
+def reduce_out(N: int, device, dens_num: int = 1, dens_den: int = 4) -> ReduceOut:
+    cap = max(N * dens_num // dens_den, 1)
+    return ReduceOut(torch.empty(cap, dtype=torch.int32, device=device),
+                     torch.empty(cap, dtype=torch.float32, device=device),
+                     torch.empty(N, dtype=torch.float32, device=device),
+                     torch.zeros(1, dtype=torch.int32, device=device),
+                     torch.zeros(1, dtype=torch.int32, device=device))
+
+
+def _reduce_out_ptrs(o: ReduceOut):
+    return (_cuda(o.idx, torch.int32, "out_idx", 1), _cuda(o.val, torch.float32, "out_val", 1),
+            o.idx.numel(), _cuda(o.dense, torch.float32, "out_dense", 1),
+            _cuda(o.nnz, torch.int32, "out_nnz"), _cuda(o.is_dense, torch.int32, "out_is_dense"))
+
+
+def sparse_reduce(idx, val, nnz, N: int, dens_num: int = 1, dens_den: int = 4,
+                  out: ReduceOut | None = None, ws=None, stream=None, events=None) -> ReduceOut:
+    """``events``: optional 3 CUDA events recorded around the two kernels."""
+    P, cap = idx.shape
+    if out is None:
+        out = reduce_out(N, idx.device, dens_num, dens_den)
+    if ws is None:
+        ws = workspace(reduce_workspace_size(P, N), idx.device)
+    oi, ov, ocap, od, on, odn = _reduce_out_ptrs(out)
+    args = (_cuda(idx, torch.int32, "idx", 2), _cuda(val, torch.float32, "val", 2),
+            _cuda(nnz, torch.int32, "nnz", 1), P, cap, N, dens_num, dens_den, oi, ov, ocap, od,
+            on, odn, ws.data_ptr(), ws.numel(), _stream(stream))
+    lib = _lib.load()
+    if events is None:
+        _check("sparcml_sparse_reduce", lib.sparcml_sparse_reduce(*args))
+    else:
+        assert len(events) == 3
+        _check("sparcml_sparse_reduce_traced",
+               lib.sparcml_sparse_reduce_traced(*args, _event_array(events)))
+    return out
+
+
+def sparse_reduce_q4(idx, codes, scales, nnz, bucket: int, N: int, dens_num: int = 1,
+                     dens_den: int = 4, out: ReduceOut | None = None, ws=None,
+                     stream=None) -> ReduceOut:
+    P, cap = idx.shape
+    if out is None:
+        out = reduce_out(N, idx.device, dens_num, dens_den)
+    if ws is None:
+        ws = workspace(reduce_workspace_size(P, N), idx.device)
+    oi, ov, ocap, od, on, odn = _reduce_out_ptrs(out)
+    _check("sparcml_sparse_reduce_q4", _lib.load().sparcml_sparse_reduce_q4(
+        _cuda(idx, torch.int32, "idx", 2), _cuda(codes, torch.uint8, "codes", 2),
+        _cuda(scales, torch.float32, "scales", 2), _cuda(nnz, torch.int32, "nnz", 1), P, cap,
+        bucket, N, dens_num, dens_den, oi, ov, ocap, od, on, odn, ws.data_ptr(), ws.numel(),
+        _stream(stream)))
+    return out
+
+
+def densify(idx, val, nnz, N: int, out=None, status=None, stream=None):
+    P, cap = idx.shape
+    if out is None:
+        out = torch.empty((P, N), dtype=torch.float32, device=idx.device)
+    _check("sparcml_densify", _lib.load().sparcml_densify(
+        _cuda(idx, torch.int32, "idx", 2), _cuda(val, torch.float32, "val", 2),
+        _cuda(nnz, torch.int32, "nnz", 1), P, cap, N, _cuda(out, torch.float32, "dense", 2),
+        _opt_ptr(status), _stream(stream)))
+    return out

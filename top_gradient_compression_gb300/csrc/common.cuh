@@ -1,0 +1,104 @@
+// Shared device helpers of the sm_103a sparse-reduction library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sparcml.h"
+
+namespace sparcml {
+
+// Count of kernels launched by the library (see sparcml_launch_count).
+void note_launches(uint64_t n);
+
+// Record the first device-side error in a status word (never traps).
+__device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
+  if (status != nullptr) atomicCAS(status, 0, code);
+}
+
+// Magnitude key: IEEE bit pattern of |x|, ordered like |x| for non-NaN x.
+__device__ __forceinline__ uint32_t mag_key(float x) {
+  return __float_as_uint(x) & 0x7fffffffu;
+}
+
+__device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm volatile("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// Exclusive prefix over the warp of a small per-lane count c (0 <= c < 8),
+// in lane order, from three ballots.
+__device__ __forceinline__ uint32_t warp_excl_small(uint32_t c, uint32_t* total) {
+  const uint32_t b0 = __ballot_sync(0xffffffffu, c & 1u);
+  const uint32_t b1 = __ballot_sync(0xffffffffu, c & 2u);
+  const uint32_t b2 = __ballot_sync(0xffffffffu, c & 4u);
+  const uint32_t lt = lanemask_lt();
+  *total = __popc(b0) + 2u * __popc(b1) + 4u * __popc(b2);
+  return __popc(b0 & lt) + 2u * __popc(b1 & lt) + 4u * __popc(b2 & lt);
+}
+
+__device__ __forceinline__ uint32_t warp_incl_sum(uint32_t v) {
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, v, d);
+    if (lane_id() >= (uint32_t)d) v += t;
+  }
+  return v;
+}
+
+__device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+  return v;
+}
+
+// Block-wide exclusive scan of one uint32 per thread. `scratch` holds at
+// least 33 words of shared memory. Returns the exclusive prefix; *total gets
+// the block sum. Contains two __syncthreads().
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* scratch,
+                                                    uint32_t* total) {
+  const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+  const uint32_t nwarps = (blockDim.x + 31) >> 5;
+  const uint32_t incl = warp_incl_sum(v);
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t w = lane < nwarps ? scratch[lane] : 0u;
+    const uint32_t wi = warp_incl_sum(w);
+    scratch[lane] = wi - w;
+    if (lane == 31) scratch[32] = wi;
+  }
+  __syncthreads();
+  *total = scratch[32];
+  return scratch[warp] + incl - v;
+}
+
+// Histogram increment with warp aggregation: lanes that hit the same bin
+// in one step add once, which keeps skewed key distributions from
+// serialising on one shared-memory word.
+__device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin, bool active) {
+  const uint32_t am = __ballot_sync(0xffffffffu, active);
+  if (!active) return;
+  const uint32_t peers = __match_any_sync(am, bin);
+  const uint32_t leader = __ffs(peers) - 1;
+  if (lane_id() == leader) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+}
+
+// SplitMix64 (Steele, Lea and Flood, OOPSLA 2014): the output for state x.
+__device__ __forceinline__ uint64_t splitmix64(uint64_t x) {
+  uint64_t z = x + 0x9e3779b97f4a7c15ull;
+  z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+  z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+  return z ^ (z >> 31);
+}
+
+inline int launch_status() {
+  return cudaGetLastError() == cudaSuccess ? SPARCML_OK : SPARCML_ERR_CUDA;
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace sparcml

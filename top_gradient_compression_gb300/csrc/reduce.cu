@@ -1,0 +1,407 @@
+// Sparse sum-reduction of P streams with the adaptive dense switch, sm_103a.
+//
+// "SparCML: High-Performance Sparse Communication for Machine Learning",
+// §5.2 (allreduce of sparse vectors with a coordinate-wise associative op
+// that has a neutral element: here fp32 sum, neutral +0.0), §5.3.2 (the
+// split phase routes index ranges to owners: here each CTA owns a tile of
+// the index space), §5.1 / §5.3.3 (switch to a dense representation once
+// fill-in passes the threshold delta), App. B (the result size is the size
+// of the union of the contributed index sets).
+//
+// One pass over the input, no sort, no floating-point atomics:
+//
+//  tile kernel   (one CTA per tile of kTile consecutive indices, tiles taken
+//                in index order through a ticket). The CTA binary-searches
+//                each node's sub-range for its tile, then adds the nodes'
+//                entries into a shared-memory fp32 accumulator node by node
+//                in ascending node order (indices are unique within a node,
+//                so no two threads of one node touch the same word) and sets
+//                a presence bitmap. Its union count is chained to the
+//                previous tiles with a decoupled look-back (Merrill and
+//                Garland, 2016) to get the tile's output offset. A tile whose
+//                inclusive count still fits the sparse capacity writes its
+//                entries ascending (bitmap + prefix popcount); once the
+//                running count passes floor(N * num / den) the result is
+//                certainly dense and the tile writes its dense slice.
+//  fix-up kernel (one CTA per tile) runs only if the final result is dense:
+//                the leading tiles that were written sparse are turned into
+//                their dense slices (zeros, then a scatter of their entries).
+//
+// Every wait on a predecessor is bounded; on expiry the kernel records
+// SPARCML_ERR_TIMEOUT and carries on, so a bad input can never hang the GPU.
+
+#include "common.cuh"
+
+namespace sparcml {
+namespace {
+
+constexpr uint32_t kTile = 8192;  // indices per tile
+constexpr uint32_t kWords = kTile / 32;
+constexpr uint32_t kReduceThreads = 512;
+constexpr uint32_t kUnroll = 4;
+constexpr int32_t kMaxReduceP = 4096;
+constexpr unsigned long long kFlagAgg = 1ull << 62;
+constexpr unsigned long long kFlagInc = 2ull << 62;
+constexpr uint32_t kSpinLimit = 1u << 21;
+
+struct ReduceArgs {
+  const uint32_t* idx;
+  const float* val;
+  const uint8_t* codes;
+  const float* scales;
+  const uint32_t* nnz;
+  uint64_t cap;
+  uint64_t code_stride;
+  uint64_t scale_stride;
+  uint32_t bucket;
+  int32_t P;
+  uint32_t N;
+  uint32_t ntiles;
+  uint32_t cap_sparse;  // floor(N * num / den): largest sparse result
+  uint32_t* out_idx;
+  float* out_val;
+  float* out_dense;
+  uint32_t* out_nnz;
+  int32_t* out_is_dense;
+  uint32_t* ticket;
+  unsigned long long* tile_state;
+  uint2* tile_info;  // (offset, count | dense << 31)
+  int32_t* status;
+};
+
+__device__ __forceinline__ uint32_t lower_bound_u32(const uint32_t* a, uint32_t n, uint32_t x) {
+  uint32_t lo = 0, hi = n;
+  while (lo < hi) {
+    const uint32_t mid = lo + ((hi - lo) >> 1);
+    if (a[mid] < x) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+// Value of entry j of node p: fp32 as stored, or decoded from 4 bits.
+template <bool Q4>
+__device__ __forceinline__ float load_value(const ReduceArgs& a, uint32_t p, uint32_t j) {
+  if constexpr (!Q4) {
+    return a.val[(uint64_t)p * a.cap + j];
+  } else {
+    const uint8_t byte = a.codes[(uint64_t)p * a.code_stride + (j >> 1)];
+    const uint32_t code = (j & 1) ? (byte >> 4) : (byte & 15u);
+    const uint32_t level = code & 7u;
+    if (level == 0) return 0.0f;
+    const float scale = a.scales[(uint64_t)p * a.scale_stride + j / a.bucket];
+    const float v = __fmul_rn(__fdiv_rn((float)level, 7.0f), scale);
+    return (code & 8u) ? -v : v;
+  }
+}
+
+template <bool Q4>
+__global__ void __launch_bounds__(kReduceThreads)
+reduce_tile_kernel(ReduceArgs a) {
+  extern __shared__ __align__(16) uint32_t dyn[];
+  float* acc = reinterpret_cast<float*>(dyn);
+  uint32_t* bm = dyn + kTile;
+  uint32_t* lo = bm + kWords;
+  uint32_t* hi = lo + a.P;
+  __shared__ uint32_t scratch[34];
+  __shared__ uint32_t bc[4];
+  const uint32_t t = threadIdx.x;
+
+  if (t == 0) {
+    bc[0] = atomicAdd(a.ticket, 1u);
+    bc[1] = 0;
+  }
+  for (uint32_t w = t; w < kTile / 4; w += blockDim.x)
+    reinterpret_cast<float4*>(acc)[w] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (uint32_t w = t; w < kWords; w += blockDim.x) bm[w] = 0;
+  __syncthreads();
+  const uint32_t tile = bc[0];
+  const uint32_t tile_lo = tile * kTile;
+  const uint32_t tile_n = min(kTile, a.N - tile_lo);
+  const bool last = tile == a.ntiles - 1;
+
+  // Each node's sub-range [lo, hi) of entries with tile_lo <= idx < tile_hi.
+  for (int32_t p = t; p < a.P; p += blockDim.x) {
+    uint32_t n = a.nnz[p];
+    if (n > a.cap) {
+      set_status(a.status, SPARCML_ERR_CAPACITY);
+      n = (uint32_t)a.cap;
+    }
+    const uint32_t* ip = a.idx + (uint64_t)p * a.cap;
+    const uint32_t l = lower_bound_u32(ip, n, tile_lo);
+    uint32_t h = lower_bound_u32(ip, n, tile_lo + tile_n);
+    if (last && h < n) set_status(a.status, SPARCML_ERR_BAD_STREAM);  // idx >= N
+    if (h < l) {
+      set_status(a.status, SPARCML_ERR_BAD_STREAM);
+      h = l;
+    }
+    lo[p] = l;
+    hi[p] = h;
+    atomicMax(&bc[1], n);  // U >= max nnz: dense for certain if above the cap
+  }
+  __syncthreads();
+  const bool dense_certain = bc[1] > a.cap_sparse;
+
+  // Accumulate node by node, in ascending node order.
+  const uint32_t lane = lane_id();
+  for (int32_t p = 0; p < a.P; ++p) {
+    const uint32_t l = lo[p], h = hi[p];
+    const uint32_t* ip = a.idx + (uint64_t)p * a.cap;
+    for (uint32_t j0 = l; j0 < h; j0 += blockDim.x * kUnroll) {
+      uint32_t iv[kUnroll];
+      float vv[kUnroll];
+#pragma unroll
+      for (uint32_t u = 0; u < kUnroll; ++u) {
+        const uint32_t j = j0 + u * blockDim.x + t;
+        iv[u] = j < h ? ip[j] : 0u;
+        vv[u] = j < h ? load_value<Q4>(a, p, j) : 0.0f;
+      }
+#pragma unroll
+      for (uint32_t u = 0; u < kUnroll; ++u) {
+        const uint32_t j = j0 + u * blockDim.x + t;
+        // Predecessor index: the previous lane holds entry j - 1.
+        uint32_t prev = __shfl_up_sync(0xffffffffu, iv[u], 1);
+        if (lane == 0 && j < h && j > 0) prev = ip[j - 1];
+        if (j < h) {
+          const uint32_t off = iv[u] - tile_lo;
+          if (off < tile_n && (j == 0 || prev < iv[u])) {
+            acc[off] = __fadd_rn(acc[off], vv[u]);
+            atomicOr(&bm[off >> 5], 1u << (off & 31));
+          } else {
+            set_status(a.status, SPARCML_ERR_BAD_STREAM);
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+
+  // Union count of the tile.
+  uint32_t c = 0;
+  for (uint32_t w = t; w < kWords; w += blockDim.x) c += __popc(bm[w]);
+  uint32_t count;
+  block_excl_scan(c, scratch, &count);
+
+  // Decoupled look-back for the tile's exclusive offset.
+  if (t == 0) {
+    unsigned long long* st = a.tile_state;
+    uint32_t excl = 0;
+    if (tile == 0) {
+      atomicExch(&st[0], kFlagInc | count);
+    } else {
+      atomicExch(&st[tile], kFlagAgg | count);
+      int64_t j = (int64_t)tile - 1;
+      uint32_t spins = 0, backoff = 32;
+      while (j >= 0) {
+        const unsigned long long s = *reinterpret_cast<volatile unsigned long long*>(&st[j]);
+        const unsigned long long flag = s & (3ull << 62);
+        if (flag == 0) {
+          if (++spins > kSpinLimit) {
+            set_status(a.status, SPARCML_ERR_TIMEOUT);
+            break;
+          }
+          __nanosleep(backoff);
+          backoff = min(backoff * 2, 1024u);
+          continue;
+        }
+        excl += (uint32_t)s;
+        if (flag == kFlagInc) break;
+        --j;
+      }
+      atomicExch(&st[tile], kFlagInc | (excl + count));
+    }
+    bc[2] = excl;
+  }
+  __syncthreads();
+  const uint32_t excl = bc[2];
+  const uint32_t incl = excl + count;
+  const bool dense = dense_certain || incl > a.cap_sparse;
+
+  if (dense) {
+    float* od = a.out_dense + tile_lo;
+    const bool vec = (reinterpret_cast<uintptr_t>(od) & 15) == 0;
+    const uint32_t nv = vec ? tile_n / 4 : 0;
+    for (uint32_t w = t; w < nv; w += blockDim.x)
+      reinterpret_cast<float4*>(od)[w] = reinterpret_cast<const float4*>(acc)[w];
+    for (uint32_t x = nv * 4 + t; x < tile_n; x += blockDim.x) od[x] = acc[x];
+  } else {
+    // Ascending compaction: one bitmap word per thread, prefix of popcounts.
+    const uint32_t word = t < kWords ? bm[t] : 0u;
+    uint32_t tot;
+    uint32_t pos = excl + block_excl_scan(__popc(word), scratch, &tot);
+    uint32_t bits = word;
+    while (bits) {
+      const uint32_t b = __ffs(bits) - 1;
+      bits &= bits - 1;
+      const uint32_t off = t * 32 + b;
+      a.out_idx[pos] = tile_lo + off;
+      a.out_val[pos] = acc[off];
+      ++pos;
+    }
+  }
+  if (t == 0) {
+    a.tile_info[tile] = make_uint2(excl, count | (dense ? 0x80000000u : 0u));
+    if (last) {
+      *a.out_nnz = incl;
+      *a.out_is_dense = dense ? 1 : 0;
+    }
+  }
+}
+
+// Dense result: rewrite the leading tiles that were emitted sparse.
+__global__ void __launch_bounds__(256)
+reduce_fixup_kernel(const int32_t* __restrict__ is_dense, const uint2* __restrict__ tile_info,
+                    const uint32_t* __restrict__ out_idx, const float* __restrict__ out_val,
+                    float* __restrict__ out_dense, uint32_t N) {
+  if (*is_dense == 0) return;
+  const uint2 info = tile_info[blockIdx.x];
+  if (info.y & 0x80000000u) return;
+  const uint32_t tile_lo = blockIdx.x * kTile;
+  const uint32_t tile_n = min(kTile, N - tile_lo);
+  for (uint32_t x = threadIdx.x; x < tile_n; x += blockDim.x) out_dense[tile_lo + x] = 0.0f;
+  __syncthreads();
+  for (uint32_t e = threadIdx.x; e < info.y; e += blockDim.x) {
+    const uint32_t i = out_idx[info.x + e];
+    if (i - tile_lo < tile_n) out_dense[i] = out_val[info.x + e];
+  }
+}
+
+struct ReduceLayout {
+  size_t ticket, state, info, total;
+};
+
+ReduceLayout reduce_layout(uint64_t N) {
+  const size_t ntiles = (N + kTile - 1) / kTile;
+  ReduceLayout l;
+  l.ticket = 64;
+  l.state = 256;
+  l.info = align_up(l.state + 8 * ntiles, 256);
+  l.total = align_up(l.info + 8 * ntiles, 256);
+  return l;
+}
+
+template <bool Q4>
+int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
+                  void* const* events) {
+  auto mark = [&](int i) {
+    if (events && events[i]) cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s);
+  };
+  const ReduceLayout l = reduce_layout(a.N);
+  if (ws_bytes < l.total) return SPARCML_ERR_WORKSPACE;
+  char* w = static_cast<char*>(ws);
+  a.status = reinterpret_cast<int32_t*>(w);
+  a.ticket = reinterpret_cast<uint32_t*>(w + l.ticket);
+  a.tile_state = reinterpret_cast<unsigned long long*>(w + l.state);
+  a.tile_info = reinterpret_cast<uint2*>(w + l.info);
+  // Clear the ticket and the look-back states (the status word is kept).
+  if (cudaMemsetAsync(w + l.ticket, 0, l.info - l.ticket, s) != cudaSuccess)
+    return SPARCML_ERR_CUDA;
+  const size_t smem = (kTile + kWords + 2 * (size_t)a.P) * sizeof(uint32_t);
+  if (cudaFuncSetAttribute(reduce_tile_kernel<Q4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return SPARCML_ERR_CUDA;
+  mark(0);
+  reduce_tile_kernel<Q4><<<a.ntiles, kReduceThreads, smem, s>>>(a);
+  if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
+  mark(1);
+  reduce_fixup_kernel<<<a.ntiles, 256, 0, s>>>(a.out_is_dense, a.tile_info, a.out_idx,
+                                               a.out_val, a.out_dense, a.N);
+  if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
+  mark(2);
+  note_launches(2);
+  return SPARCML_OK;
+}
+
+int check_reduce_args(const uint32_t* idx, const uint32_t* nnz, int32_t P, uint64_t cap,
+                      uint64_t N, uint32_t dens_num, uint32_t dens_den, uint32_t* out_idx,
+                      float* out_val, uint64_t out_cap, float* out_dense, uint32_t* out_nnz,
+                      int32_t* out_is_dense, void* ws) {
+  if (!idx || !nnz || !out_idx || !out_val || !out_dense || !out_nnz || !out_is_dense || !ws)
+    return SPARCML_ERR_INVALID_ARG;
+  if (P < 1 || P > kMaxReduceP || N < 1 || N > 0xffffffffull || cap > 0xffffffffull ||
+      dens_den < 1 || dens_num > dens_den)
+    return SPARCML_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return SPARCML_ERR_INVALID_ARG;
+  if (out_cap < N * dens_num / dens_den) return SPARCML_ERR_CAPACITY;
+  return SPARCML_OK;
+}
+
+}  // namespace
+}  // namespace sparcml
+
+using namespace sparcml;
+
+extern "C" size_t sparcml_sparse_reduce_workspace_size(int32_t P, uint64_t N) {
+  if (P < 1 || P > kMaxReduceP || N < 1 || N > 0xffffffffull) return 0;
+  return reduce_layout(N).total;
+}
+
+extern "C" int sparcml_sparse_reduce_traced(const uint32_t* idx, const float* val,
+                                            const uint32_t* nnz, int32_t P, uint64_t cap,
+                                            uint64_t N, uint32_t dens_num, uint32_t dens_den,
+                                            uint32_t* out_idx, float* out_val, uint64_t out_cap,
+                                            float* out_dense, uint32_t* out_nnz,
+                                            int32_t* out_is_dense, void* ws, size_t ws_bytes,
+                                            void* stream, void* const* events) {
+  const int st = check_reduce_args(idx, nnz, P, cap, N, dens_num, dens_den, out_idx, out_val,
+                                   out_cap, out_dense, out_nnz, out_is_dense, ws);
+  if (st != SPARCML_OK) return st;
+  if (!val) return SPARCML_ERR_INVALID_ARG;
+  ReduceArgs a = {};
+  a.idx = idx;
+  a.val = val;
+  a.nnz = nnz;
+  a.cap = cap;
+  a.P = P;
+  a.N = (uint32_t)N;
+  a.ntiles = (uint32_t)((N + kTile - 1) / kTile);
+  a.cap_sparse = (uint32_t)(N * dens_num / dens_den);
+  a.out_idx = out_idx;
+  a.out_val = out_val;
+  a.out_dense = out_dense;
+  a.out_nnz = out_nnz;
+  a.out_is_dense = out_is_dense;
+  return launch_reduce<false>(a, ws, ws_bytes, static_cast<cudaStream_t>(stream), events);
+}
+
+extern "C" int sparcml_sparse_reduce(const uint32_t* idx, const float* val, const uint32_t* nnz,
+                                     int32_t P, uint64_t cap, uint64_t N, uint32_t dens_num,
+                                     uint32_t dens_den, uint32_t* out_idx, float* out_val,
+                                     uint64_t out_cap, float* out_dense, uint32_t* out_nnz,
+                                     int32_t* out_is_dense, void* ws, size_t ws_bytes,
+                                     void* stream) {
+  return sparcml_sparse_reduce_traced(idx, val, nnz, P, cap, N, dens_num, dens_den, out_idx,
+                                      out_val, out_cap, out_dense, out_nnz, out_is_dense, ws,
+                                      ws_bytes, stream, nullptr);
+}
+
+extern "C" int sparcml_sparse_reduce_q4(const uint32_t* idx, const uint8_t* codes,
+                                        const float* scales, const uint32_t* nnz, int32_t P,
+                                        uint64_t cap, uint32_t bucket, uint64_t N,
+                                        uint32_t dens_num, uint32_t dens_den, uint32_t* out_idx,
+                                        float* out_val, uint64_t out_cap, float* out_dense,
+                                        uint32_t* out_nnz, int32_t* out_is_dense, void* ws,
+                                        size_t ws_bytes, void* stream) {
+  const int st = check_reduce_args(idx, nnz, P, cap, N, dens_num, dens_den, out_idx, out_val,
+                                   out_cap, out_dense, out_nnz, out_is_dense, ws);
+  if (st != SPARCML_OK) return st;
+  if (!codes || !scales || bucket < 2 || (bucket & 1) || cap < 1) return SPARCML_ERR_INVALID_ARG;
+  ReduceArgs a = {};
+  a.idx = idx;
+  a.codes = codes;
+  a.scales = scales;
+  a.nnz = nnz;
+  a.cap = cap;
+  a.code_stride = (cap + 1) / 2;
+  a.scale_stride = (cap + bucket - 1) / bucket;
+  a.bucket = bucket;
+  a.P = P;
+  a.N = (uint32_t)N;
+  a.ntiles = (uint32_t)((N + kTile - 1) / kTile);
+  a.cap_sparse = (uint32_t)(N * dens_num / dens_den);
+  a.out_idx = out_idx;
+  a.out_val = out_val;
+  a.out_dense = out_dense;
+  a.out_nnz = out_nnz;
+  a.out_is_dense = out_is_dense;
+  return launch_reduce<true>(a, ws, ws_bytes, static_cast<cudaStream_t>(stream), nullptr);
+}
