@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--workload", choices=["resnet50", "asr"], default="resnet50")
     ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--nodes", type=int, default=0,
+                    help="override P (smaller device footprint for profiling captures)")
     ap.add_argument("--cpu-segments", type=int, default=48,
                     help="segments per node in the bounded CPU-baseline sample")
     return ap.parse_args()
@@ -287,6 +289,11 @@ def run_ours(args, ranks):
         raise RuntimeError("bench.py --impl ours needs a CUDA device")
     torch.cuda.set_device(dev)
     spec = workload_spec(args.workload)
+    if args.nodes:
+        spec["P"] = args.nodes
+        spec["desc"] += f" [P overridden to {args.nodes}]"
+        gen = spec["gen"]
+        spec["gen"] = lambda t, d: gen(t, d)[: args.nodes].contiguous()
     P, N, L, kn, kd = spec["P"], spec["N"], spec["seg_len"], spec["k_num"], spec["k_den"]
     NB = 3 if spec["name"] == "resnet50" else 2  # distinct gradient batches, cycled
     grads = [spec["gen"](t, dev) for t in range(NB)]

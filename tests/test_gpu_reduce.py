@@ -178,19 +178,23 @@ def test_quantize_dequantize_parity():
             assert np.array_equal(bits(gd[p, :n]), bits(od[p, :n]))
 
 
-def test_reduce_q4_equals_dequantize_then_reduce():
-    rng = np.random.default_rng(8)
-    P, N, k, bucket = 6, 300_000, 20_000, 512
+@pytest.mark.parametrize("k,dense", [(5_000, False), (20_000, True)])
+def test_reduce_q4_equals_dequantize_then_reduce(k, dense):
+    P, N, bucket = 6, 300_000, 512
     idx, val, nnz = W.uniform_streams(P, N, k, 31, std=1e-3)
-    nnz[2] = 12_345
+    nnz[2] = k // 2 + 345
     seed = W.quant_seed(0)
     oc, osc = oracle.quantize4(idx, val, nnz, bucket, seed)
     deq = oracle.dequantize4(oc, osc, nnz, k, bucket)
     ref = oracle.sparse_reduce(idx, deq, nnz, N)
+    assert ref["is_dense"] == dense
     di, dv, dn = streams_to_dev(idx, val, nnz)
     codes, scales = api.quantize4(di, dv, dn, bucket, seed)
     out = api.sparse_reduce_q4(di, codes, scales, dn, bucket, N)
     U = int(out.nnz.item())
     assert U == ref["nnz"] and bool(out.is_dense.item()) == ref["is_dense"]
-    assert np.array_equal(u32(out.idx[:U]), ref["idx"])
-    assert np.array_equal(bits(out.val[:U].cpu().numpy()), bits(ref["val"]))
+    if dense:
+        assert np.array_equal(bits(out.dense.cpu().numpy()), bits(ref["dense"]))
+    else:
+        assert np.array_equal(u32(out.idx[:U]), ref["idx"])
+        assert np.array_equal(bits(out.val[:U].cpu().numpy()), bits(ref["val"]))

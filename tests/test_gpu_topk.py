@@ -124,3 +124,42 @@ def test_resnet50_workload_sampled_segments_ten_steps():
     for p in range(P):
         s = gi[p, :int(u32(nnz)[p])].astype(np.int64)
         assert (np.diff(s) > 0).all() and s[-1] < N
+
+
+@pytest.mark.slow
+def test_asr_workload_node0_three_steps_then_quantised_reduce():
+    """Full LSTM/ASR-like workload (P=16, N=67,108,864, one segment per node,
+    k=1%, Laplace(0, 1e-3)): node 0's Top-k+EF is checked against the oracle for
+    all 3 steps; then every node's stream is 4-bit quantised (buckets of 512)
+    and reduced with the fused dequantising reduce, checked against the oracle
+    quantiser, dequantiser and map-based sum on the same streams."""
+    c = W.ASR
+    P, N, L = c["P"], c["N"], c["seg_len"]
+    res_g = torch.zeros((P, N), device=DEV)
+    res_o = np.zeros((1, N), np.float32)
+    ws = api.workspace(api.topk_ef_workspace_size(P, N, L, c["k_num"], c["k_den"]), DEV)
+    for t in range(c["steps"]):
+        g = W.asr_grads(t, device=DEV)
+        idx, val, nnz = api.topk_ef(g, res_g, L, c["k_num"], c["k_den"], ws=ws)
+        assert api.get_status(ws) == 0
+        g0 = g[0:1].cpu().numpy()
+        del g
+        oi, ov, on = oracle.topk_ef(g0, res_o, L, c["k_num"], c["k_den"])
+        k = int(on[0])
+        assert k == N // 100 and (u32(nnz) == k).all()
+        assert np.array_equal(u32(idx[0]), oi[0, :k])
+        assert np.array_equal(bits(val[0].cpu().numpy()), bits(ov[0, :k]))
+        assert np.array_equal(bits(res_g[0].cpu().numpy()), bits(res_o[0]))
+    bucket, seed = c["bucket"], W.quant_seed(c["steps"] - 1)
+    codes, scales = api.quantize4(idx, val, nnz, bucket, seed)
+    hi, hv, hn = u32(idx), val.cpu().numpy(), u32(nnz)
+    oc, osc = oracle.quantize4(hi, hv, hn, bucket, seed)
+    assert np.array_equal(codes.cpu().numpy(), oc)  # k is even: every nibble is valid
+    assert np.array_equal(bits(scales.cpu().numpy()), bits(osc))
+    deq = oracle.dequantize4(oc, osc, hn, hi.shape[1], bucket)
+    ref = oracle.sparse_reduce(hi, deq, hn, N)
+    out = api.sparse_reduce_q4(idx, codes, scales, nnz, bucket, N)
+    U = int(out.nnz.item())
+    assert U == ref["nnz"] and not ref["is_dense"] and not bool(out.is_dense.item())
+    assert np.array_equal(u32(out.idx[:U]), ref["idx"])
+    assert np.array_equal(bits(out.val[:U].cpu().numpy()), bits(ref["val"]))
