@@ -216,6 +216,35 @@ int sparcml_sparse_reduce_q4(const uint32_t* idx, const uint8_t* codes, const fl
                              void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Allocation-free sparse reduce. The paper has no counterpart: this entry
+ * point exists for callers of this library that cannot allocate device
+ * memory where they reduce (a plug-in inside a host framework that owns all
+ * device memory through its own pool, or a latency-critical path where a
+ * cudaMalloc would synchronise the device), so they cannot provide the
+ * workspace that sparcml_sparse_reduce needs.
+ *
+ * Same arguments and results as sparcml_sparse_reduce, without ws/ws_bytes.
+ * Its scratch is one fixed array compiled into the library (262,400 bytes,
+ * enough for N <= SPARCML_NOALLOC_MAX_N); every GPU that loads the library
+ * holds it until the process exits. The call allocates and frees nothing.
+ *   - N > SPARCML_NOALLOC_MAX_N returns SPARCML_ERR_WORKSPACE and enqueues
+ *     nothing.
+ *   - Device-side errors go to *status (device int32, may be NULL).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the array: calls whose work can overlap on the GPU
+ *     (different streams, different host threads) race and must be
+ *     serialised by the caller. Each call clears what must start at zero.
+ * ------------------------------------------------------------------------ */
+#define SPARCML_NOALLOC_MAX_N (1ull << 27)
+int sparcml_sparse_reduce_noalloc(const uint32_t* idx, const float* val, const uint32_t* nnz,
+                                  int32_t P, uint64_t cap, uint64_t N, uint32_t dens_num,
+                                  uint32_t dens_den, uint32_t* out_idx, float* out_val,
+                                  uint64_t out_cap, float* out_dense, uint32_t* out_nnz,
+                                  int32_t* out_is_dense, int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------
  * Densify (§5.1 representation switch): dense[p][i] = val of node p's
  * entry with index i, +0.0f where the stream has none. dense [P][N].
  * Entries with idx >= N are skipped and SPARCML_ERR_BAD_STREAM is recorded

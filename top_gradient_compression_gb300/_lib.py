@@ -46,6 +46,9 @@ SIGNATURES = {
     "sparcml_sparse_reduce_q4": (C.c_int, [vp, vp, vp, vp, C.c_int32, C.c_uint64, C.c_uint32,
                                            C.c_uint64, C.c_uint32, C.c_uint32, vp, vp,
                                            C.c_uint64, vp, vp, vp, vp, C.c_size_t, vp]),
+    "sparcml_sparse_reduce_noalloc": (C.c_int, [vp, vp, vp, C.c_int32, C.c_uint64, C.c_uint64,
+                                                C.c_uint32, C.c_uint32, vp, vp, C.c_uint64, vp,
+                                                vp, vp, vp, vp]),
     "sparcml_densify": (C.c_int, [vp, vp, vp, C.c_int32, C.c_uint64, C.c_uint64, vp, vp, vp]),
 }
 

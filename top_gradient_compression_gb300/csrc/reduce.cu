@@ -405,3 +405,107 @@ extern "C" int sparcml_sparse_reduce_q4(const uint32_t* idx, const uint8_t* code
   a.out_is_dense = out_is_dense;
   return launch_reduce<true>(a, ws, ws_bytes, static_cast<cudaStream_t>(stream), nullptr);
 }
+
+// ---------------------------------------------------------------------------
+// Allocation-free sparse reduce (the paper has no counterpart).
+//
+// For callers that cannot allocate device memory where they reduce: a plug-in
+// inside a host framework that owns all device memory through its own pool,
+// or a latency-critical path where cudaMalloc would synchronise the device.
+// The reduce's scratch (ticket, look-back words, per-tile records) then comes
+// from one fixed array compiled into this file. Every GPU that loads the
+// library holds that array until the process exits. All calls share it, so
+// calls whose work overlaps on the GPU race; the array keeps the last call's
+// contents and each call clears the words that must start at zero.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace sparcml {
+namespace {
+constexpr uint64_t kNoAllocMaxN = SPARCML_NOALLOC_MAX_N;
+constexpr size_t kNoAllocTiles = (kNoAllocMaxN + kTile - 1) / kTile;  // 16,384
+constexpr size_t kNoAllocStateOff = 256;
+constexpr size_t kNoAllocInfoOff = kNoAllocStateOff + 8 * kNoAllocTiles;
+constexpr size_t kNoAllocBytes = kNoAllocInfoOff + 8 * kNoAllocTiles;  // 262,400 B
+constexpr int kNoAllocMaxDevices = 64;
+}  // namespace
+}  // namespace sparcml
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[sparcml::kNoAllocBytes];
+
+namespace sparcml {
+namespace {
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on the current device. The first call
+// on a device looks it up (cudaGetSymbolAddress, no allocation) and keeps it.
+int noalloc_scratch(char** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices)
+    return SPARCML_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return SPARCML_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = static_cast<char*>(g_noalloc_ptr[dev]);
+  return SPARCML_OK;
+}
+}  // namespace
+}  // namespace sparcml
+
+extern "C" int sparcml_sparse_reduce_noalloc(const uint32_t* idx, const float* val,
+                                             const uint32_t* nnz, int32_t P, uint64_t cap,
+                                             uint64_t N, uint32_t dens_num, uint32_t dens_den,
+                                             uint32_t* out_idx, float* out_val, uint64_t out_cap,
+                                             float* out_dense, uint32_t* out_nnz,
+                                             int32_t* out_is_dense, int32_t* status,
+                                             void* stream) {
+  if (!idx || !val || !nnz || !out_idx || !out_val || !out_dense || !out_nnz || !out_is_dense)
+    return SPARCML_ERR_INVALID_ARG;
+  if (P < 1 || P > kMaxReduceP || N < 1 || N > 0xffffffffull || cap > 0xffffffffull ||
+      dens_den < 1 || dens_num > dens_den)
+    return SPARCML_ERR_INVALID_ARG;
+  if (N > kNoAllocMaxN) return SPARCML_ERR_WORKSPACE;  // beyond the fixed scratch
+  if (out_cap < N * dens_num / dens_den) return SPARCML_ERR_CAPACITY;
+  char* scratch = nullptr;
+  const int st = noalloc_scratch(&scratch);
+  if (st != SPARCML_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ReduceArgs a = {};
+  a.idx = idx;
+  a.val = val;
+  a.nnz = nnz;
+  a.cap = cap;
+  a.P = P;
+  a.N = (uint32_t)N;
+  a.ntiles = (uint32_t)((N + kTile - 1) / kTile);
+  a.cap_sparse = (uint32_t)(N * dens_num / dens_den);
+  a.out_idx = out_idx;
+  a.out_val = out_val;
+  a.out_dense = out_dense;
+  a.out_nnz = out_nnz;
+  a.out_is_dense = out_is_dense;
+  a.status = status;
+  a.ticket = reinterpret_cast<uint32_t*>(scratch + 64);
+  a.tile_state = reinterpret_cast<unsigned long long*>(scratch + kNoAllocStateOff);
+  a.tile_info = reinterpret_cast<uint2*>(scratch + kNoAllocInfoOff);
+  // The ticket and this call's look-back words must start at zero.
+  if (cudaMemsetAsync(scratch + 64, 0, kNoAllocStateOff - 64 + 8 * (size_t)a.ntiles, s) !=
+      cudaSuccess)
+    return SPARCML_ERR_CUDA;
+  const size_t smem = (kTile + kWords + 2 * (size_t)a.P) * sizeof(uint32_t);
+  if (cudaFuncSetAttribute(reduce_tile_kernel<false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return SPARCML_ERR_CUDA;
+  reduce_tile_kernel<false><<<a.ntiles, kReduceThreads, smem, s>>>(a);
+  if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
+  reduce_fixup_kernel<<<a.ntiles, 256, 0, s>>>(a.out_is_dense, a.tile_info, a.out_idx,
+                                               a.out_val, a.out_dense, a.N);
+  if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
+  note_launches(2);
+  return SPARCML_OK;
+}
