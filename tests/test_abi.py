@@ -105,3 +105,13 @@ def test_segment_k_total_matches_the_oracle_rule():
     for N, L, kn, kd in [(65_536, 65_536, 1, 100), (25_557_032, 100_000, 1, 1000), (1001, 7, 3, 8),
                          (10, 100, 1, 1), (33, 1, 1, 2)]:
         assert api.segment_k_total(N, L, kn, kd) == sum(oracle.segment_ks(N, L, kn, kd))
+
+
+def test_binding_arity_matches_the_header():
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    decls = re.findall(r"\b(sparcml_\w+)\s*\(([^)]*)\)\s*;", text)
+    assert decls
+    for name, params in decls:
+        params = params.strip()
+        n = 0 if params in ("", "void") else len(params.split(","))
+        assert len(_lib.SIGNATURES[name][1]) == n, name
