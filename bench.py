@@ -366,7 +366,7 @@ def run_ours(args, ranks):
     if spec["quant"]:
         kern["quantize4"] = mean_ms(ev_q, 0, 1)
     else:
-        kern["reduce_tile"] = mean_ms(ev_rd, 0, 1)
+        kern["reduce_split_tile"] = mean_ms(ev_rd, 0, 1)
         kern["reduce_fixup"] = mean_ms(ev_rd, 1, 2)
 
     U = int(rd_out.nnz.item())
@@ -458,7 +458,7 @@ def run_ours(args, ranks):
                      "launch_ms": kern["topk_stream"]},
         "kernels_ms": kern,
         "reduce": {"input_bytes": reduce_in, "sum_nnz": sum_nnz, "U": U, "is_dense": is_dense,
-                   "input_GBps": reduce_in / ((kern.get("reduce_tile", 0) +
+                   "input_GBps": reduce_in / ((kern.get("reduce_split_tile", 0) +
                                                kern.get("reduce_fixup", 0)) * 1e-3) / 1e9
                    if not spec["quant"] else None},
         "cpu_baseline": cpu,

@@ -37,8 +37,8 @@ namespace {
 
 constexpr uint32_t kTile = 8192;  // indices per tile
 constexpr uint32_t kWords = kTile / 32;
-constexpr uint32_t kReduceThreads = 512;
-constexpr uint32_t kUnroll = 4;
+constexpr uint32_t kReduceThreads = 256;
+constexpr uint32_t kUnroll = 8;
 constexpr int32_t kMaxReduceP = 4096;
 constexpr unsigned long long kFlagAgg = 1ull << 62;
 constexpr unsigned long long kFlagInc = 2ull << 62;
@@ -66,6 +66,7 @@ struct ReduceArgs {
   uint32_t* ticket;
   unsigned long long* tile_state;
   uint2* tile_info;  // (offset, count | dense << 31)
+  const uint32_t* split;  // [(ntiles + 1) * P] node sub-range starts per tile
   int32_t* status;
 };
 
@@ -94,14 +95,32 @@ __device__ __forceinline__ float load_value(const ReduceArgs& a, uint32_t p, uin
   }
 }
 
-template <bool Q4>
+// Where each node's entries for tile t start: split[t * P + p] =
+// lower_bound(idx_p, t * kTile) for t < ntiles and lower_bound(idx_p, N) for
+// t = ntiles. One thread per (tile boundary, node); all searches run at once
+// and the upper levels of every search hit L2.
+__global__ void __launch_bounds__(256)
+reduce_split_kernel(const uint32_t* __restrict__ idx, const uint32_t* __restrict__ nnz,
+                    int32_t P, uint64_t cap, uint32_t N, uint32_t ntiles,
+                    uint32_t* __restrict__ split) {
+  const uint64_t e = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= (uint64_t)(ntiles + 1) * P) return;
+  const uint32_t t = (uint32_t)(e / P), p = (uint32_t)(e % P);
+  const uint32_t n = (uint32_t)min((uint64_t)nnz[p], cap);
+  const uint32_t x = t == ntiles ? N : t * kTile;
+  split[e] = lower_bound_u32(idx + (uint64_t)p * cap, n, x);
+}
+
+// TABLE: node sub-ranges come from reduce_split_kernel's table; otherwise the
+// CTA binary-searches them itself (no table in the scratch).
+template <bool Q4, bool TABLE = false>
 __global__ void __launch_bounds__(kReduceThreads)
 reduce_tile_kernel(ReduceArgs a) {
   extern __shared__ __align__(16) uint32_t dyn[];
   float* acc = reinterpret_cast<float*>(dyn);
   uint32_t* bm = dyn + kTile;
-  uint32_t* lo = bm + kWords;
-  uint32_t* hi = lo + a.P;
+  uint32_t* lo = bm + kWords;  // [P] first entry of each node in this tile
+  uint32_t* pre = lo + a.P;    // [P + 1] exclusive prefix of the nodes' entry counts
   __shared__ uint32_t scratch[34];
   __shared__ uint32_t bc[4];
   const uint32_t t = threadIdx.x;
@@ -119,60 +138,109 @@ reduce_tile_kernel(ReduceArgs a) {
   const uint32_t tile_n = min(kTile, a.N - tile_lo);
   const bool last = tile == a.ntiles - 1;
 
-  // Each node's sub-range [lo, hi) of entries with tile_lo <= idx < tile_hi.
+  // Each node's sub-range [lo, hi) of entries with tile_lo <= idx < tile_lo + tile_n.
   for (int32_t p = t; p < a.P; p += blockDim.x) {
     uint32_t n = a.nnz[p];
     if (n > a.cap) {
       set_status(a.status, SPARCML_ERR_CAPACITY);
       n = (uint32_t)a.cap;
     }
-    const uint32_t* ip = a.idx + (uint64_t)p * a.cap;
-    const uint32_t l = lower_bound_u32(ip, n, tile_lo);
-    uint32_t h = lower_bound_u32(ip, n, tile_lo + tile_n);
+    uint32_t l, h;
+    if constexpr (TABLE) {
+      l = a.split[(uint64_t)tile * a.P + p];
+      h = a.split[(uint64_t)(tile + 1) * a.P + p];
+    } else {
+      const uint32_t* ip = a.idx + (uint64_t)p * a.cap;
+      l = lower_bound_u32(ip, n, tile_lo);
+      h = lower_bound_u32(ip, n, tile_lo + tile_n);
+    }
     if (last && h < n) set_status(a.status, SPARCML_ERR_BAD_STREAM);  // idx >= N
     if (h < l) {
       set_status(a.status, SPARCML_ERR_BAD_STREAM);
       h = l;
     }
     lo[p] = l;
-    hi[p] = h;
+    pre[p] = h - l;
     atomicMax(&bc[1], n);  // U >= max nnz: dense for certain if above the cap
   }
   __syncthreads();
+  uint32_t E = 0;  // entries of the tile, all nodes
+  for (int32_t base = 0; base < a.P; base += blockDim.x) {
+    const int32_t p = base + (int32_t)t;
+    const uint32_t c = p < a.P ? pre[p] : 0u;
+    uint32_t tot;
+    const uint32_t ex = block_excl_scan(c, scratch, &tot);
+    if (p < a.P) pre[p] = E + ex;
+    E += tot;
+    __syncthreads();
+  }
+  if (t == 0) pre[a.P] = E;
+  __syncthreads();
   const bool dense_certain = bc[1] > a.cap_sparse;
 
-  // Accumulate node by node, in ascending node order.
+  // Node of flattened entry v: the largest p with pre[p] <= v.
+  auto node_of = [&](uint32_t v) {
+    uint32_t l = 0, h = (uint32_t)a.P;  // pre[l] <= v < pre[h]
+    while (h - l > 1) {
+      const uint32_t m = (l + h) >> 1;
+      if (pre[m] <= v) l = m; else h = m;
+    }
+    return l;
+  };
+
+  // Accumulate. Entries are taken in node-major order, kUnroll * blockDim at
+  // a time (all loads in flight together); the adds of one batch then run
+  // node by node, a barrier after each node that has entries in the batch,
+  // so every index sees its nodes in ascending order.
   const uint32_t lane = lane_id();
-  for (int32_t p = 0; p < a.P; ++p) {
-    const uint32_t l = lo[p], h = hi[p];
-    const uint32_t* ip = a.idx + (uint64_t)p * a.cap;
-    for (uint32_t j0 = l; j0 < h; j0 += blockDim.x * kUnroll) {
-      uint32_t iv[kUnroll];
-      float vv[kUnroll];
+  const uint32_t batch = blockDim.x * kUnroll;
+  for (uint32_t c0 = 0; c0 < E; c0 += batch) {
+    uint32_t iv[kUnroll], pv[kUnroll];
+    float vv[kUnroll];
 #pragma unroll
-      for (uint32_t u = 0; u < kUnroll; ++u) {
-        const uint32_t j = j0 + u * blockDim.x + t;
-        iv[u] = j < h ? ip[j] : 0u;
-        vv[u] = j < h ? load_value<Q4>(a, p, j) : 0.0f;
+    for (uint32_t u = 0; u < kUnroll; ++u) {
+      const uint32_t v = c0 + u * blockDim.x + t;
+      iv[u] = 0;
+      vv[u] = 0.0f;
+      pv[u] = 0xffffffffu;
+      if (v < E) {
+        const uint32_t p = node_of(v);
+        const uint32_t j = lo[p] + (v - pre[p]);
+        iv[u] = a.idx[(uint64_t)p * a.cap + j];
+        vv[u] = load_value<Q4>(a, p, j);
+        pv[u] = p;
       }
+    }
 #pragma unroll
-      for (uint32_t u = 0; u < kUnroll; ++u) {
-        const uint32_t j = j0 + u * blockDim.x + t;
-        // Predecessor index: the previous lane holds entry j - 1.
-        uint32_t prev = __shfl_up_sync(0xffffffffu, iv[u], 1);
-        if (lane == 0 && j < h && j > 0) prev = ip[j - 1];
-        if (j < h) {
-          const uint32_t off = iv[u] - tile_lo;
-          if (off < tile_n && (j == 0 || prev < iv[u])) {
-            acc[off] = __fadd_rn(acc[off], vv[u]);
-            atomicOr(&bm[off >> 5], 1u << (off & 31));
-          } else {
-            set_status(a.status, SPARCML_ERR_BAD_STREAM);
-          }
+    for (uint32_t u = 0; u < kUnroll; ++u) {
+      const uint32_t v = c0 + u * blockDim.x + t;
+      // Strictly ascending check against entry j - 1 of the same node: the
+      // previous lane holds it unless this is a warp's or a node's first entry.
+      uint32_t prev = __shfl_up_sync(0xffffffffu, iv[u], 1);
+      if (v < E) {
+        const uint32_t p = pv[u];
+        const uint32_t j = lo[p] + (v - pre[p]);
+        if ((lane == 0 || v == pre[p]) && j > 0) prev = a.idx[(uint64_t)p * a.cap + j - 1];
+        if (!((j == 0 || prev < iv[u]) && iv[u] - tile_lo < tile_n)) {
+          set_status(a.status, SPARCML_ERR_BAD_STREAM);
+          pv[u] = 0xffffffffu;  // skip it
         }
       }
     }
-    __syncthreads();
+    const uint32_t c1 = min(c0 + batch, E);
+    const uint32_t p_first = node_of(c0), p_last = node_of(c1 - 1);
+    for (uint32_t p = p_first; p <= p_last; ++p) {
+      if (pre[p + 1] == pre[p]) continue;  // no entries: no barrier needed
+#pragma unroll
+      for (uint32_t u = 0; u < kUnroll; ++u) {
+        if (pv[u] == p) {
+          const uint32_t off = iv[u] - tile_lo;
+          acc[off] = __fadd_rn(acc[off], vv[u]);
+          atomicOr(&bm[off >> 5], 1u << (off & 31));
+        }
+      }
+      __syncthreads();
+    }
   }
 
   // Union count of the tile.
@@ -266,16 +334,17 @@ reduce_fixup_kernel(const int32_t* __restrict__ is_dense, const uint2* __restric
 }
 
 struct ReduceLayout {
-  size_t ticket, state, info, total;
+  size_t ticket, state, info, split, total;
 };
 
-ReduceLayout reduce_layout(uint64_t N) {
+ReduceLayout reduce_layout(int32_t P, uint64_t N) {
   const size_t ntiles = (N + kTile - 1) / kTile;
   ReduceLayout l;
   l.ticket = 64;
   l.state = 256;
   l.info = align_up(l.state + 8 * ntiles, 256);
-  l.total = align_up(l.info + 8 * ntiles, 256);
+  l.split = align_up(l.info + 8 * ntiles, 256);
+  l.total = align_up(l.split + 4 * (ntiles + 1) * (size_t)P, 256);
   return l;
 }
 
@@ -285,29 +354,35 @@ int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
   auto mark = [&](int i) {
     if (events && events[i]) cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s);
   };
-  const ReduceLayout l = reduce_layout(a.N);
+  const ReduceLayout l = reduce_layout(a.P, a.N);
   if (ws_bytes < l.total) return SPARCML_ERR_WORKSPACE;
   char* w = static_cast<char*>(ws);
   a.status = reinterpret_cast<int32_t*>(w);
   a.ticket = reinterpret_cast<uint32_t*>(w + l.ticket);
   a.tile_state = reinterpret_cast<unsigned long long*>(w + l.state);
   a.tile_info = reinterpret_cast<uint2*>(w + l.info);
+  uint32_t* split = reinterpret_cast<uint32_t*>(w + l.split);
+  a.split = split;
   // Clear the ticket and the look-back states (the status word is kept).
   if (cudaMemsetAsync(w + l.ticket, 0, l.info - l.ticket, s) != cudaSuccess)
     return SPARCML_ERR_CUDA;
-  const size_t smem = (kTile + kWords + 2 * (size_t)a.P) * sizeof(uint32_t);
-  if (cudaFuncSetAttribute(reduce_tile_kernel<Q4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
+  const size_t smem = (kTile + kWords + 2 * (size_t)a.P + 1) * sizeof(uint32_t);
+  if (cudaFuncSetAttribute(reduce_tile_kernel<Q4, true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return SPARCML_ERR_CUDA;
   mark(0);
-  reduce_tile_kernel<Q4><<<a.ntiles, kReduceThreads, smem, s>>>(a);
+  const uint64_t nsplit = (uint64_t)(a.ntiles + 1) * a.P;
+  reduce_split_kernel<<<(unsigned)((nsplit + 255) / 256), 256, 0, s>>>(a.idx, a.nnz, a.P, a.cap,
+                                                                      a.N, a.ntiles, split);
+  if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
+  reduce_tile_kernel<Q4, true><<<a.ntiles, kReduceThreads, smem, s>>>(a);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   mark(1);
   reduce_fixup_kernel<<<a.ntiles, 256, 0, s>>>(a.out_is_dense, a.tile_info, a.out_idx,
                                                a.out_val, a.out_dense, a.N);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   mark(2);
-  note_launches(2);
+  note_launches(3);
   return SPARCML_OK;
 }
 
@@ -332,7 +407,7 @@ using namespace sparcml;
 
 extern "C" size_t sparcml_sparse_reduce_workspace_size(int32_t P, uint64_t N) {
   if (P < 1 || P > kMaxReduceP || N < 1 || N > 0xffffffffull) return 0;
-  return reduce_layout(N).total;
+  return reduce_layout(P, N).total;
 }
 
 extern "C" int sparcml_sparse_reduce_traced(const uint32_t* idx, const float* val,
@@ -497,7 +572,7 @@ extern "C" int sparcml_sparse_reduce_noalloc(const uint32_t* idx, const float* v
   if (cudaMemsetAsync(scratch + 64, 0, kNoAllocStateOff - 64 + 8 * (size_t)a.ntiles, s) !=
       cudaSuccess)
     return SPARCML_ERR_CUDA;
-  const size_t smem = (kTile + kWords + 2 * (size_t)a.P) * sizeof(uint32_t);
+  const size_t smem = (kTile + kWords + 2 * (size_t)a.P + 1) * sizeof(uint32_t);
   if (cudaFuncSetAttribute(reduce_tile_kernel<false>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return SPARCML_ERR_CUDA;

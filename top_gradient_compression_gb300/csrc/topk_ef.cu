@@ -48,10 +48,13 @@ namespace {
 constexpr uint32_t kChunk = 8192;         // entries per stream-pass CTA
 constexpr uint32_t kStreamThreads = 256;  // 8 warps x 1024 entries
 constexpr uint32_t kRounds = kChunk / (kStreamThreads * 4);  // float4 rounds per warp
-constexpr uint32_t kSampleMax = 8192;
+constexpr uint32_t kSampleMax = 8192;     // sample of a long segment
+constexpr uint32_t kSampleShort = 2048;   // sample of a layer-sized segment
+constexpr uint32_t kShortSegment = 1u << 18;
 constexpr uint32_t kRun = 32;
 constexpr uint32_t kGuessThreads = 256;
-constexpr uint32_t kSelectThreads = 512;
+constexpr uint32_t kSelectThreads = 256;
+constexpr uint32_t kSmallCands = 4096;  // candidates a select CTA keeps in shared memory
 constexpr uint32_t kWin = 1024;  // chunks per window in the select pass
 constexpr uint32_t kNone = 0xffffffffu;
 
@@ -153,27 +156,46 @@ topk_guess_kernel(const float* __restrict__ grad, const float* __restrict__ resi
   const float* gp = grad + base;
   const float* rp = residual + base;
 
-  uint32_t S, r;
+  // Sample size: all of a short segment; else runs of 32 consecutive entries
+  // (one 128-byte line per array per run), fewer for layer-sized segments
+  // whose candidate sets are small anyway.
   const bool exact = n <= kSampleMax;
+  const uint32_t S = exact ? n : (n <= kShortSegment ? kSampleShort : kSampleMax);
+  uint32_t r;
   if (exact) {
-    S = n;
     r = k;
   } else {
-    S = kSampleMax;
     const double lam = (double)k * (double)S / (double)n;
     const double rr = ceil(lam + 4.0 * sqrt(lam) + 8.0);
     r = rr >= (double)S ? S : (uint32_t)rr;
   }
-  const uint32_t nruns = kSampleMax / kRun;
-  for (uint32_t i = t; i < S; i += blockDim.x) {
-    uint32_t pos = i;
-    if (!exact) {
-      const uint32_t run = i / kRun;
-      const uint64_t st = ((uint64_t)run * (n - kRun) / (nruns - 1)) & ~(uint64_t)(kRun - 1);
-      pos = (uint32_t)st + (i % kRun);
+  if (exact) {
+#pragma unroll 4
+    for (uint32_t i = t; i < S; i += blockDim.x) keys[i] = mag_key(__fadd_rn(rp[i], gp[i]));
+  } else {
+    // Warp w loads runs w, w + 8, ...: 4 runs (8 coalesced lines) in flight per lane.
+    const uint32_t nruns = S / kRun, lane = lane_id(), warp = t >> 5, nw = blockDim.x >> 5;
+    for (uint32_t r0 = warp; r0 < nruns; r0 += 4 * nw) {
+      float a[4], b[4];
+#pragma unroll
+      for (uint32_t q = 0; q < 4; ++q) {
+        const uint32_t run = r0 + q * nw;
+        a[q] = b[q] = 0.0f;
+        if (run < nruns) {
+          const uint32_t st =
+              (uint32_t)(((uint64_t)run * (n - kRun) / (nruns - 1)) & ~(uint64_t)(kRun - 1));
+          a[q] = rp[st + lane];
+          b[q] = gp[st + lane];
+        }
+      }
+#pragma unroll
+      for (uint32_t q = 0; q < 4; ++q) {
+        const uint32_t run = r0 + q * nw;
+        if (run < nruns) keys[run * kRun + lane] = mag_key(__fadd_rn(a[q], b[q]));
+      }
     }
-    keys[i] = mag_key(__fadd_rn(rp[pos], gp[pos]));
   }
+  __syncthreads();
   // Two radix digits (bits 30..20, then 19..9) of the r-th largest key.
   uint32_t prefix = 0, rem = r;
   for (int d = 0; d < 2; ++d) {
@@ -337,7 +359,7 @@ struct SelectShared {
 // Exclusive prefix of the candidate counts of chunks [c0, c0 + nw) into
 // sh.wpre[0..nw]; returns the window total.
 __device__ uint32_t load_window(SelectShared& sh, const uint32_t* cc, uint32_t nw) {
-  const uint32_t per = (kWin + kSelectThreads - 1) / kSelectThreads;  // 2
+  const uint32_t per = (kWin + kSelectThreads - 1) / kSelectThreads;
   const uint32_t t = threadIdx.x;
   uint32_t v[per], sum = 0;
 #pragma unroll
@@ -394,6 +416,76 @@ topk_select_kernel(SelectArgs a) {
       (uint32_t)min((uint64_t)seg_start + (uint64_t)(cb - c_first) * kChunk, seg_end);
   float* rp = a.residual + (uint64_t)p * g.N;
   const uint64_t node_chunk0 = (uint64_t)p * g.nchunk;
+
+  // Fast path: one CTA owns the segment and all its candidates fit in shared
+  // memory. They are read from global memory once, in index order; the
+  // radix select and the ordered compaction then run on the shared copy.
+  if (CS == 1 && !raw && ms <= kWin && a.seg_cnt[gs] <= kSmallCands) {
+    extern __shared__ uint32_t dsm[];
+    uint32_t* s_idx = dsm;
+    float* s_val = reinterpret_cast<float*>(dsm + kSmallCands);
+    const uint32_t M = load_window(sh, a.chunk_cnt + node_chunk0 + c_first, ms);
+    for (uint32_t v = t; v < M; v += blockDim.x) {
+      const uint32_t w = window_chunk(sh, ms, v);
+      const uint64_t slot = (node_chunk0 + c_first + w) * g.slot + (v - sh.wpre[w]);
+      s_idx[v] = a.cand_idx[slot];
+      s_val[v] = a.cand_val[slot];
+    }
+    __syncthreads();
+    const uint32_t shifts[3] = {20, 9, 0};
+    const uint32_t widths[3] = {11, 11, 9};
+    uint32_t prefix = 0, rem = k;
+    for (int d = 0; d < 3; ++d) {
+      const uint32_t shift = shifts[d], nb = 1u << widths[d], hi_shift = shift + widths[d];
+      for (uint32_t b = t; b < nb; b += blockDim.x) sh.hist[b] = 0;
+      __syncthreads();
+      for (uint32_t v0 = 0; v0 < M; v0 += blockDim.x) {
+        const uint32_t v = v0 + t;
+        const uint32_t key = v < M ? mag_key(s_val[v]) : 0u;
+        const bool match = v < M && (d == 0 || (key >> hi_shift) == prefix);
+        hist_add(sh.hist, (key >> shift) & (nb - 1), match);
+      }
+      __syncthreads();
+      find_from_top(sh.hist, nb, rem, sh.scratch, sh.res);
+      uint32_t b = sh.res[0];
+      if (b == kNone) {
+        set_status(a.status, SPARCML_ERR_BAD_STREAM);
+        b = 0;
+      } else {
+        rem -= sh.res[1];
+      }
+      prefix = (prefix << widths[d]) | b;
+    }
+    const uint32_t T = prefix, tie_take = rem;
+    const uint64_t out0 = (uint64_t)p * g.cap + (uint64_t)s * g.k_full;
+    uint32_t run_gt = 0, run_eq = 0;
+    for (uint32_t v0 = 0; v0 < M; v0 += blockDim.x) {
+      const uint32_t v = v0 + t;
+      const float x = v < M ? s_val[v] : 0.0f;
+      const uint32_t key = mag_key(x);
+      const bool gt = v < M && key > T;
+      const bool eq = v < M && key == T;
+      uint32_t tot;
+      const uint32_t ex =
+          block_excl_scan((gt ? 1u : 0u) | (eq ? 0x10000u : 0u), sh.scratch, &tot);
+      const uint32_t e_gt = run_gt + (ex & 0xffffu), e_eq = run_eq + (ex >> 16);
+      if (gt || (eq && e_eq < tie_take)) {
+        const uint32_t pos = e_gt + min(e_eq, tie_take);
+        if (pos < k) {
+          const uint32_t i = s_idx[v];
+          a.out_idx[out0 + pos] = i;
+          a.out_val[out0 + pos] = x;
+          rp[i] = 0.0f;
+        } else {
+          set_status(a.status, SPARCML_ERR_BAD_STREAM);
+        }
+      }
+      run_gt += tot & 0xffffu;
+      run_eq += tot >> 16;
+      __syncthreads();
+    }
+    return;
+  }
 
   // Visit every candidate of this CTA as (index, value), window by window.
   // `ordered` passes see them in ascending index order, blockDim at a time.
@@ -617,7 +709,7 @@ extern "C" int sparcml_topk_ef_traced(const float* grad, float* residual, int32_
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((uint64_t)P * g.nseg * CS), 1, 1);
   cfg.blockDim = dim3(kSelectThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = 2 * kSmallCands * sizeof(uint32_t);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -626,6 +718,9 @@ extern "C" int sparcml_topk_ef_traced(const float* grad, float* residual, int32_
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)cfg.dynamicSmemBytes) != cudaSuccess)
+    return SPARCML_ERR_CUDA;
   if (cudaLaunchKernelEx(&cfg, topk_select_kernel, a) != cudaSuccess) return SPARCML_ERR_CUDA;
   mark(3);
   note_launches(3);
