@@ -64,7 +64,7 @@ def test_topk_sample_overestimates_then_falls_back():
     """Large values only where the guess pass samples: too few candidates, so the
     select pass re-reads the segment. The result is still exact."""
     P, N = 1, 1 << 20
-    n_runs, run = 256, 32
+    n_runs, run = 32, 256  # the guess pass reads 32 runs of 256 entries of a long segment
     g = (np.random.default_rng(3).standard_normal((P, N)) * 0.01).astype(np.float32)
     for i in range(n_runs):
         st = (i * (N - run) // (n_runs - 1)) & ~(run - 1)

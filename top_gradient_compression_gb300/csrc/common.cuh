@@ -11,6 +11,10 @@ namespace sparcml {
 // Count of kernels launched by the library (see sparcml_launch_count).
 void note_launches(uint64_t n);
 
+// Raise a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device; the runtime call is made once per (device, kernel, size).
+bool ensure_smem(const void* func, size_t bytes);
+
 // Record the first device-side error in a status word (never traps).
 __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
   if (status != nullptr) atomicCAS(status, 0, code);
@@ -93,6 +97,32 @@ __device__ __forceinline__ uint64_t splitmix64(uint64_t x) {
   z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
   z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
   return z ^ (z >> 31);
+}
+
+// L2 eviction-priority hints (PTX createpolicy / .L2::cache_hint). Data that
+// a later kernel of the same step reads back (candidates, streams) is stored
+// evict-last so the multi-GB streaming pass does not flush it from L2.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void st_keep(uint32_t* ptr, uint32_t v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.u32 [%0], %1, %2;" ::"l"(ptr), "r"(v), "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ void st_keep(float* ptr, float v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(ptr), "f"(v), "l"(pol)
+               : "memory");
+}
+
+// Asynchronous 4-byte global -> shared copy (no register round trip).
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
+  const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 inline int launch_status() {

@@ -7,6 +7,9 @@
 
 #include <algorithm>
 #include <atomic>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "common.cuh"
 
@@ -148,6 +151,21 @@ size_t pack_chunk_array_bytes(int32_t P, uint64_t N) {
 }  // namespace
 
 void note_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+bool ensure_smem(const void* func, size_t bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, size_t> done;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  size_t& have = done[{dev, func}];
+  if (have >= bytes) return true;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+      cudaSuccess)
+    return false;
+  have = bytes;
+  return true;
+}
 
 }  // namespace sparcml
 

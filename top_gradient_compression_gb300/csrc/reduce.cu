@@ -97,18 +97,33 @@ __device__ __forceinline__ float load_value(const ReduceArgs& a, uint32_t p, uin
 
 // Where each node's entries for tile t start: split[t * P + p] =
 // lower_bound(idx_p, t * kTile) for t < ntiles and lower_bound(idx_p, N) for
-// t = ntiles. One thread per (tile boundary, node); all searches run at once
-// and the upper levels of every search hit L2.
+// t = ntiles. One warp per (tile boundary, node): each round probes 32
+// evenly spaced entries and keeps the bracket, narrowing the range 33-fold
+// per memory round trip instead of 2-fold.
 __global__ void __launch_bounds__(256)
 reduce_split_kernel(const uint32_t* __restrict__ idx, const uint32_t* __restrict__ nnz,
                     int32_t P, uint64_t cap, uint32_t N, uint32_t ntiles,
                     uint32_t* __restrict__ split) {
-  const uint64_t e = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (e >= (uint64_t)(ntiles + 1) * P) return;
-  const uint32_t t = (uint32_t)(e / P), p = (uint32_t)(e % P);
+  const uint64_t w = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (w >= (uint64_t)(ntiles + 1) * P) return;  // warp-uniform
+  const uint32_t lane = lane_id();
+  const uint32_t t = (uint32_t)(w / P), p = (uint32_t)(w % P);
   const uint32_t n = (uint32_t)min((uint64_t)nnz[p], cap);
   const uint32_t x = t == ntiles ? N : t * kTile;
-  split[e] = lower_bound_u32(idx + (uint64_t)p * cap, n, x);
+  const uint32_t* a = idx + (uint64_t)p * cap;
+  uint32_t lo = 0, hi = n;  // the answer lies in [lo, hi]
+  while (hi - lo > 32) {
+    const uint32_t span = hi - lo;
+    const uint32_t pos = lo + (uint32_t)((uint64_t)span * (lane + 1) / 33);
+    const uint32_t c = __popc(__ballot_sync(0xffffffffu, a[pos] < x));
+    const uint32_t nlo = c ? lo + (uint32_t)((uint64_t)span * c / 33) + 1 : lo;
+    const uint32_t nhi = c < 32 ? lo + (uint32_t)((uint64_t)span * (c + 1) / 33) : hi;
+    lo = nlo;
+    hi = nhi;
+  }
+  const uint32_t pos = lo + lane;
+  const uint32_t c = __popc(__ballot_sync(0xffffffffu, pos < hi && a[pos] < x));
+  if (lane == 0) split[w] = lo + c;
 }
 
 // TABLE: node sub-ranges come from reduce_split_kernel's table; otherwise the
@@ -249,35 +264,43 @@ reduce_tile_kernel(ReduceArgs a) {
   uint32_t count;
   block_excl_scan(c, scratch, &count);
 
-  // Decoupled look-back for the tile's exclusive offset.
-  if (t == 0) {
+  // Decoupled look-back for the tile's exclusive offset, one warp wide: each
+  // round reads the states of the 32 nearest predecessors at once and sums
+  // back to the nearest inclusive prefix.
+  if (t < 32) {
     unsigned long long* st = a.tile_state;
     uint32_t excl = 0;
     if (tile == 0) {
-      atomicExch(&st[0], kFlagInc | count);
+      if (t == 0) atomicExch(&st[0], kFlagInc | count);
     } else {
-      atomicExch(&st[tile], kFlagAgg | count);
-      int64_t j = (int64_t)tile - 1;
+      if (t == 0) atomicExch(&st[tile], kFlagAgg | count);
+      int64_t base = (int64_t)tile - 1;
       uint32_t spins = 0, backoff = 32;
-      while (j >= 0) {
-        const unsigned long long s = *reinterpret_cast<volatile unsigned long long*>(&st[j]);
-        const unsigned long long flag = s & (3ull << 62);
-        if (flag == 0) {
+      while (true) {
+        const int64_t j = base - (int64_t)lane;
+        const unsigned long long sv =
+            j >= 0 ? *reinterpret_cast<volatile unsigned long long*>(&st[j]) : (2ull << 62);
+        const unsigned long long flag = sv & (3ull << 62);
+        const uint32_t inc = __ballot_sync(0xffffffffu, flag == kFlagInc);
+        const uint32_t notready = __ballot_sync(0xffffffffu, flag == 0);
+        const uint32_t upto = inc ? (uint32_t)(__ffs(inc) - 1) : 31u;  // lanes 0..upto count
+        const uint32_t need = upto == 31 ? 0xffffffffu : ((2u << upto) - 1u);
+        if (notready & need) {
           if (++spins > kSpinLimit) {
-            set_status(a.status, SPARCML_ERR_TIMEOUT);
+            if (t == 0) set_status(a.status, SPARCML_ERR_TIMEOUT);
             break;
           }
           __nanosleep(backoff);
           backoff = min(backoff * 2, 1024u);
           continue;
         }
-        excl += (uint32_t)s;
-        if (flag == kFlagInc) break;
-        --j;
+        excl += warp_sum(lane <= upto ? (uint32_t)sv : 0u);
+        if (inc) break;
+        base -= 32;
       }
-      atomicExch(&st[tile], kFlagInc | (excl + count));
+      if (t == 0) atomicExch(&st[tile], kFlagInc | (excl + count));
     }
-    bc[2] = excl;
+    if (t == 0) bc[2] = excl;
   }
   __syncthreads();
   const uint32_t excl = bc[2];
@@ -367,13 +390,12 @@ int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
   if (cudaMemsetAsync(w + l.ticket, 0, l.info - l.ticket, s) != cudaSuccess)
     return SPARCML_ERR_CUDA;
   const size_t smem = (kTile + kWords + 2 * (size_t)a.P + 1) * sizeof(uint32_t);
-  if (cudaFuncSetAttribute(reduce_tile_kernel<Q4, true>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+  if (!ensure_smem(reinterpret_cast<const void*>(reduce_tile_kernel<Q4, true>), smem))
     return SPARCML_ERR_CUDA;
   mark(0);
-  const uint64_t nsplit = (uint64_t)(a.ntiles + 1) * a.P;
-  reduce_split_kernel<<<(unsigned)((nsplit + 255) / 256), 256, 0, s>>>(a.idx, a.nnz, a.P, a.cap,
-                                                                      a.N, a.ntiles, split);
+  const uint64_t nsplit = (uint64_t)(a.ntiles + 1) * a.P;  // one warp each
+  reduce_split_kernel<<<(unsigned)((nsplit * 32 + 255) / 256), 256, 0, s>>>(
+      a.idx, a.nnz, a.P, a.cap, a.N, a.ntiles, split);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   reduce_tile_kernel<Q4, true><<<a.ntiles, kReduceThreads, smem, s>>>(a);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
@@ -573,8 +595,7 @@ extern "C" int sparcml_sparse_reduce_noalloc(const uint32_t* idx, const float* v
       cudaSuccess)
     return SPARCML_ERR_CUDA;
   const size_t smem = (kTile + kWords + 2 * (size_t)a.P + 1) * sizeof(uint32_t);
-  if (cudaFuncSetAttribute(reduce_tile_kernel<false>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+  if (!ensure_smem(reinterpret_cast<const void*>(reduce_tile_kernel<false>), smem))
     return SPARCML_ERR_CUDA;
   reduce_tile_kernel<false><<<a.ntiles, kReduceThreads, smem, s>>>(a);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;

@@ -47,11 +47,13 @@ namespace {
 
 constexpr uint32_t kChunk = 8192;         // entries per stream-pass CTA
 constexpr uint32_t kStreamThreads = 256;  // 8 warps x 1024 entries
-constexpr uint32_t kRounds = kChunk / (kStreamThreads * 4);  // float4 rounds per warp
+constexpr uint32_t kWarpsPerChunk = kStreamThreads / 32;
+constexpr uint32_t kSub = kChunk / kWarpsPerChunk;            // entries per warp: 1,024
+constexpr uint32_t kRounds = kSub / (32 * 4);                  // float4 rounds per warp
 constexpr uint32_t kSampleMax = 8192;     // sample of a long segment
-constexpr uint32_t kSampleShort = 2048;   // sample of a layer-sized segment
+constexpr uint32_t kSampleShort = 4096;   // sample of a layer-sized segment
 constexpr uint32_t kShortSegment = 1u << 18;
-constexpr uint32_t kRun = 32;
+constexpr uint32_t kRun = 256;  // consecutive entries per sample run (1 KB per array)
 constexpr uint32_t kGuessThreads = 256;
 constexpr uint32_t kSelectThreads = 256;
 constexpr uint32_t kSmallCands = 4096;  // candidates a select CTA keeps in shared memory
@@ -69,7 +71,7 @@ struct Geo {
   uint32_t nchunk;   // chunks per node
   uint32_t k_full;   // k of a full segment
   uint32_t k_last;   // k of the last segment
-  uint32_t slot;     // candidate slot capacity per chunk
+  uint32_t slot;     // candidate slot capacity per warp sub-chunk
   int32_t P;
 };
 
@@ -123,23 +125,25 @@ __device__ void find_from_top(const uint32_t* h, uint32_t nbins, uint32_t r, uin
 }
 
 // ---------------------------------------------------------------------------
-// 1. guess: one CTA per (node, segment).
+// 1. guess: one CTA per (node, segment). The sample keys stay in registers
+// (KPT per thread); G = the r-th largest sample key with its low 15 bits
+// cleared, found bit by bit (16 block-wide counts, no histogram).
 // ---------------------------------------------------------------------------
+template <uint32_t KPT>
 __global__ void __launch_bounds__(kGuessThreads)
 topk_guess_kernel(const float* __restrict__ grad, const float* __restrict__ residual, Geo g,
                   uint32_t* __restrict__ guess, uint32_t* __restrict__ seg_cnt,
                   uint32_t* __restrict__ seg_flag, uint32_t* __restrict__ out_nnz,
-                  uint32_t total_k) {
-  __shared__ uint32_t keys[kSampleMax];
-  __shared__ uint32_t hist[2048];
-  __shared__ uint32_t scratch[34];
-  __shared__ uint32_t res[2];
+                  uint32_t total_k, uint32_t* __restrict__ todo_cnt) {
+  constexpr uint32_t kWarps = kGuessThreads / 32;
+  __shared__ uint32_t wsum[2][kWarps];
 
   const uint32_t gs = blockIdx.x;
   const uint32_t p = gs / g.nseg, s = gs % g.nseg;
   const uint32_t n = seg_n(g, s), k = seg_k(g, s);
-  const uint32_t t = threadIdx.x;
+  const uint32_t t = threadIdx.x, lane = lane_id(), warp = t >> 5;
   if (t == 0) {
+    if (gs == 0) *todo_cnt = 0;
     seg_cnt[gs] = 0;
     seg_flag[gs] = 0;
     if (s == 0) out_nnz[p] = total_k;
@@ -156,9 +160,9 @@ topk_guess_kernel(const float* __restrict__ grad, const float* __restrict__ resi
   const float* gp = grad + base;
   const float* rp = residual + base;
 
-  // Sample size: all of a short segment; else runs of 32 consecutive entries
-  // (one 128-byte line per array per run), fewer for layer-sized segments
-  // whose candidate sets are small anyway.
+  // Sample: all of a segment of at most kSampleMax entries; else runs of kRun
+  // consecutive entries (1 KB per array: whole DRAM bursts), fewer for
+  // layer-sized segments whose candidate sets are small anyway.
   const bool exact = n <= kSampleMax;
   const uint32_t S = exact ? n : (n <= kShortSegment ? kSampleShort : kSampleMax);
   uint32_t r;
@@ -169,89 +173,160 @@ topk_guess_kernel(const float* __restrict__ grad, const float* __restrict__ resi
     const double rr = ceil(lam + 4.0 * sqrt(lam) + 8.0);
     r = rr >= (double)S ? S : (uint32_t)rr;
   }
+  // All sample loads are issued before any is used.
+  uint32_t pos[KPT];
+  bool ok[KPT];
   if (exact) {
-#pragma unroll 4
-    for (uint32_t i = t; i < S; i += blockDim.x) keys[i] = mag_key(__fadd_rn(rp[i], gp[i]));
+#pragma unroll
+    for (uint32_t q = 0; q < KPT; ++q) {
+      pos[q] = t + q * kGuessThreads;
+      ok[q] = pos[q] < S;
+    }
   } else {
-    // Warp w loads runs w, w + 8, ...: 4 runs (8 coalesced lines) in flight per lane.
-    const uint32_t nruns = S / kRun, lane = lane_id(), warp = t >> 5, nw = blockDim.x >> 5;
-    for (uint32_t r0 = warp; r0 < nruns; r0 += 4 * nw) {
-      float a[4], b[4];
+    // Runs of kRun consecutive entries spread evenly over the segment; warp w
+    // reads runs w * (KPT / kLinesPerRun) + ..., each as kRun / 32 coalesced
+    // 128-byte lines per array.
+    const uint32_t nruns = S / kRun;
+    constexpr uint32_t kLinesPerRun = kRun / 32;
 #pragma unroll
-      for (uint32_t q = 0; q < 4; ++q) {
-        const uint32_t run = r0 + q * nw;
-        a[q] = b[q] = 0.0f;
-        if (run < nruns) {
-          const uint32_t st =
-              (uint32_t)(((uint64_t)run * (n - kRun) / (nruns - 1)) & ~(uint64_t)(kRun - 1));
-          a[q] = rp[st + lane];
-          b[q] = gp[st + lane];
-        }
-      }
+    for (uint32_t q = 0; q < KPT; q += kLinesPerRun) {
+      const uint32_t run = warp * (KPT / kLinesPerRun) + q / kLinesPerRun;
+      const uint32_t st =
+          run < nruns
+              ? (uint32_t)(((uint64_t)run * (n - kRun) / (nruns - 1)) & ~(uint64_t)(kRun - 1))
+              : 0u;
 #pragma unroll
-      for (uint32_t q = 0; q < 4; ++q) {
-        const uint32_t run = r0 + q * nw;
-        if (run < nruns) keys[run * kRun + lane] = mag_key(__fadd_rn(a[q], b[q]));
+      for (uint32_t l = 0; l < kLinesPerRun; ++l) {
+        pos[q + l] = st + l * 32 + lane;
+        ok[q + l] = run < nruns;
       }
     }
   }
-  __syncthreads();
-  // Two radix digits (bits 30..20, then 19..9) of the r-th largest key.
-  uint32_t prefix = 0, rem = r;
-  for (int d = 0; d < 2; ++d) {
-    const uint32_t shift = d == 0 ? 20 : 9;
-    for (uint32_t b = t; b < 2048; b += blockDim.x) hist[b] = 0;
-    __syncthreads();
-    const uint32_t iters = (S + blockDim.x - 1) / blockDim.x;
-    for (uint32_t it = 0; it < iters; ++it) {
-      const uint32_t i = it * blockDim.x + t;
-      const bool valid = i < S;
-      const uint32_t key = valid ? keys[i] : 0;
-      const bool match = valid && (d == 0 || (key >> 20) == prefix);
-      hist_add(hist, (key >> shift) & 2047u, match);
-    }
-    __syncthreads();
-    find_from_top(hist, 2048, rem, scratch, res);
-    const uint32_t b = res[0] == kNone ? 0 : res[0];
-    rem -= res[0] == kNone ? 0 : res[1];
-    prefix = d == 0 ? b : ((prefix << 11) | b);
-    __syncthreads();
+  float ra[KPT], ga[KPT];
+#pragma unroll
+  for (uint32_t q = 0; q < KPT; ++q) {
+    ra[q] = ok[q] ? rp[pos[q]] : 0.0f;
+    ga[q] = ok[q] ? gp[pos[q]] : 0.0f;
   }
-  if (t == 0) guess[gs] = prefix << 9;
+  uint32_t key[KPT];
+#pragma unroll
+  for (uint32_t q = 0; q < KPT; ++q) key[q] = ok[q] ? mag_key(__fadd_rn(ra[q], ga[q])) : kNone;
+  // Bitwise radix select on the 2^15 grid: the largest G with at least r
+  // sample keys >= G, i.e. the r-th largest key with its low 15 bits cleared.
+  uint32_t G = 0;
+#pragma unroll 1
+  for (int bit = 30; bit >= 15; --bit) {
+    const uint32_t trial = G | (1u << bit);
+    uint32_t c = 0;
+#pragma unroll
+    for (uint32_t q = 0; q < KPT; ++q) c += (key[q] != kNone && key[q] >= trial) ? 1u : 0u;
+    c = warp_sum(c);
+    uint32_t* ws = wsum[bit & 1];  // double-buffered: one barrier per bit
+    if (lane == 0) ws[warp] = c;
+    __syncthreads();
+    uint32_t tot = 0;
+#pragma unroll
+    for (uint32_t w = 0; w < kWarps; ++w) tot += ws[w];
+    if (tot >= r) G = trial;
+  }
+  const uint32_t prefix = G >> 15;
+  if (t == 0) guess[gs] = prefix << 15;
+}
+
+// Layer-sized segments (kSampleMax < n <= kShortSegment): one warp per
+// segment, no block barrier. The 2,048-entry sample (8 runs of kRun) sits in
+// registers, 64 keys per lane; G is the same function of the sample as in
+// topk_guess_kernel (the r-th largest key with its low 15 bits cleared).
+constexpr uint32_t kWarpSample = 2048;
+constexpr uint32_t kWarpKeys = kWarpSample / 32;
+
+__global__ void __launch_bounds__(kGuessThreads)
+topk_guess_warp_kernel(const float* __restrict__ grad, const float* __restrict__ residual, Geo g,
+                       uint32_t* __restrict__ guess, uint32_t* __restrict__ seg_cnt,
+                       uint32_t* __restrict__ seg_flag, uint32_t* __restrict__ out_nnz,
+                       uint32_t total_k, uint32_t* __restrict__ todo_cnt) {
+  const uint32_t lane = lane_id();
+  const uint32_t gs = blockIdx.x * (kGuessThreads / 32) + (threadIdx.x >> 5);
+  if (gs >= (uint32_t)g.P * g.nseg) return;  // warp-uniform
+  const uint32_t p = gs / g.nseg, s = gs % g.nseg;
+  const uint32_t n = seg_n(g, s), k = seg_k(g, s);
+  if (lane == 0) {
+    if (gs == 0) *todo_cnt = 0;
+    seg_cnt[gs] = 0;
+    seg_flag[gs] = 0;
+    if (s == 0) out_nnz[p] = total_k;
+  }
+  if (k == 0 || k >= n) {
+    if (lane == 0) guess[gs] = k == 0 ? kNone : 0u;
+    return;
+  }
+  const uint64_t base = (uint64_t)p * g.N + (uint64_t)s * g.L;
+  const float* gp = grad + base;
+  const float* rp = residual + base;
+  constexpr uint32_t nruns = kWarpSample / kRun, kLines = kRun / 32, kBatchRuns = 2;
+  const double lam = (double)k * (double)kWarpSample / (double)n;
+  const double rr = ceil(lam + 4.0 * sqrt(lam) + 8.0);
+  const uint32_t r = rr >= (double)kWarpSample ? kWarpSample : (uint32_t)rr;
+  uint32_t key[kWarpKeys];
+#pragma unroll
+  for (uint32_t r0 = 0; r0 < nruns; r0 += kBatchRuns) {
+    float a[kBatchRuns * kLines], b[kBatchRuns * kLines];
+#pragma unroll
+    for (uint32_t q = 0; q < kBatchRuns * kLines; ++q) {
+      const uint32_t run = r0 + q / kLines;
+      // n <= kShortSegment, so run * (n - kRun) fits in 32 bits
+      const uint32_t i = ((run * (n - kRun) / (nruns - 1)) & ~(kRun - 1)) + (q % kLines) * 32 + lane;
+      a[q] = rp[i];
+      b[q] = gp[i];
+    }
+#pragma unroll
+    for (uint32_t q = 0; q < kBatchRuns * kLines; ++q)
+      key[r0 * kLines + q] = mag_key(__fadd_rn(a[q], b[q]));
+  }
+  uint32_t G = 0;
+#pragma unroll 1
+  for (int bit = 30; bit >= 15; --bit) {
+    const uint32_t trial = G | (1u << bit);
+    uint32_t c = 0;
+#pragma unroll
+    for (uint32_t q = 0; q < kWarpKeys; ++q) c += key[q] >= trial ? 1u : 0u;
+    if (warp_sum(c) >= r) G = trial;
+  }
+  if (lane == 0) guess[gs] = G;
 }
 
 // ---------------------------------------------------------------------------
 // 2. stream: one CTA per chunk of kChunk entries (a chunk never crosses a
-// segment boundary). Warp w owns the contiguous entries
-// [start + 1024 w, start + 1024 (w + 1)), read as kRounds rounds of 32 float4.
+// segment boundary). Warp w owns the contiguous sub-chunk of kSub entries
+// [start + kSub w, start + kSub (w + 1)), read as kRounds rounds of 32 float4,
+// and compacts its candidates in index order straight from registers into its
+// own sub-slot: no barrier, no second read.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kStreamThreads)
 topk_stream_kernel(const float* __restrict__ grad, float* __restrict__ residual, Geo g,
                    const uint32_t* __restrict__ guess, uint32_t* __restrict__ seg_cnt,
-                   uint32_t* __restrict__ seg_flag, uint32_t* __restrict__ chunk_cnt,
+                   uint32_t* __restrict__ seg_flag, uint32_t* __restrict__ sub_cnt,
                    uint32_t* __restrict__ cand_idx, float* __restrict__ cand_val) {
-  __shared__ uint32_t warp_tot[kStreamThreads / 32];
   const uint32_t gc = blockIdx.x;
   const uint32_t p = gc / g.nchunk, c = gc % g.nchunk;
   uint32_t s, j;
   chunk_pos(g, c, &s, &j);
+  const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
   const uint32_t seg_start = s * g.L;
-  const uint32_t start = seg_start + j * kChunk;
-  const uint32_t nn = min(kChunk, seg_start + seg_n(g, s) - start);  // entries in this chunk
+  const uint64_t start64 = (uint64_t)seg_start + (uint64_t)j * kChunk + warp * kSub;
+  const uint64_t seg_end = (uint64_t)seg_start + seg_n(g, s);
+  const uint32_t nn = start64 < seg_end ? (uint32_t)min((uint64_t)kSub, seg_end - start64) : 0u;
+  const uint32_t start = nn ? (uint32_t)start64 : 0u;  // this warp's first entry
   const uint32_t G = guess[p * g.nseg + s];
   const float* gp = grad + (uint64_t)p * g.N + start;
   float* rp = residual + (uint64_t)p * g.N + start;
   const bool aligned =
       ((reinterpret_cast<uintptr_t>(gp) | reinterpret_cast<uintptr_t>(rp)) & 15) == 0;
 
-  const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
-  uint32_t mask = 0;  // bit 4t+q: entry q of round t is a candidate
-
-  // Phase A: load, accumulate, write back, flag candidates.
   float4 gv[kRounds], rv[kRounds];
 #pragma unroll
   for (uint32_t t = 0; t < kRounds; ++t) {
-    const uint32_t e0 = 4 * (warp * (kRounds * 32) + t * 32 + lane);  // chunk-local
+    const uint32_t e0 = 4 * (t * 32 + lane);  // sub-chunk local
     if (aligned && e0 + 4 <= nn) {
       gv[t] = __ldcs(reinterpret_cast<const float4*>(gp + e0));
       rv[t] = *reinterpret_cast<const float4*>(rp + e0);
@@ -267,66 +342,50 @@ topk_stream_kernel(const float* __restrict__ grad, float* __restrict__ residual,
       rv[t] = make_float4(b[0], b[1], b[2], b[3]);
     }
   }
+  const uint64_t sub = (uint64_t)gc * kWarpsPerChunk + warp;
+  const uint64_t slot0 = sub * g.slot;
+  uint32_t run = 0;  // candidates so far in this sub-chunk (warp-uniform)
 #pragma unroll
   for (uint32_t t = 0; t < kRounds; ++t) {
-    const uint32_t e0 = 4 * (warp * (kRounds * 32) + t * 32 + lane);
+    const uint32_t e0 = 4 * (t * 32 + lane);
     float4 a;
     a.x = __fadd_rn(rv[t].x, gv[t].x);
     a.y = __fadd_rn(rv[t].y, gv[t].y);
     a.z = __fadd_rn(rv[t].z, gv[t].z);
     a.w = __fadd_rn(rv[t].w, gv[t].w);
     const float av[4] = {a.x, a.y, a.z, a.w};
+    uint32_t bits = 0;
     if (aligned && e0 + 4 <= nn) {
       *reinterpret_cast<float4*>(rp + e0) = a;
 #pragma unroll
-      for (uint32_t q = 0; q < 4; ++q) mask |= (mag_key(av[q]) >= G ? 1u : 0u) << (4 * t + q);
+      for (uint32_t q = 0; q < 4; ++q) bits |= (mag_key(av[q]) >= G ? 1u : 0u) << q;
     } else {
 #pragma unroll
       for (uint32_t q = 0; q < 4; ++q)
         if (e0 + q < nn) {
           rp[e0 + q] = av[q];
-          mask |= (mag_key(av[q]) >= G ? 1u : 0u) << (4 * t + q);
+          bits |= (mag_key(av[q]) >= G ? 1u : 0u) << q;
         }
     }
-  }
-  const uint32_t my = __popc(mask);
-  const uint32_t wsum = warp_sum(my);
-  if (lane == 0) warp_tot[warp] = wsum;
-  __syncthreads();
-  uint32_t base = 0, total = 0;
-#pragma unroll
-  for (uint32_t w = 0; w < kStreamThreads / 32; ++w) {
-    base += w < warp ? warp_tot[w] : 0u;
-    total += warp_tot[w];
-  }
-  if (threadIdx.x == 0) {
-    chunk_cnt[gc] = total;
-    if (total) atomicAdd(&seg_cnt[p * g.nseg + s], total);
-    if (total > g.slot) atomicOr(&seg_flag[p * g.nseg + s], 1u);
-  }
-
-  // Phase B: ordered compaction of the warp's candidates into the slot.
-  if (wsum == 0) return;
-  const uint64_t slot0 = (uint64_t)gc * g.slot;
-  uint32_t run = base;
-#pragma unroll
-  for (uint32_t t = 0; t < kRounds; ++t) {
-    const uint32_t bits = (mask >> (4 * t)) & 15u;
+    if (__ballot_sync(0xffffffffu, bits) == 0) continue;  // warp-uniform
     uint32_t tot;
     uint32_t pos = run + warp_excl_small(__popc(bits), &tot);
     run += tot;
-    if (bits) {
-      const uint32_t e0 = 4 * (warp * (kRounds * 32) + t * 32 + lane);
 #pragma unroll
-      for (uint32_t q = 0; q < 4; ++q)
-        if (bits & (1u << q)) {
-          if (pos < g.slot) {
-            cand_idx[slot0 + pos] = start + e0 + q;
-            cand_val[slot0 + pos] = rp[e0 + q];
-          }
-          ++pos;
+    for (uint32_t q = 0; q < 4; ++q)
+      if (bits & (1u << q)) {
+        if (pos < g.slot) {
+          const uint64_t keep = l2_policy_evict_last();
+          st_keep(cand_idx + slot0 + pos, start + e0 + q, keep);
+          st_keep(cand_val + slot0 + pos, av[q], keep);
         }
-    }
+        ++pos;
+      }
+  }
+  if (lane == 0) {
+    sub_cnt[sub] = run;
+    if (run) atomicAdd(&seg_cnt[p * g.nseg + s], run);
+    if (run > g.slot) atomicOr(&seg_flag[p * g.nseg + s], 1u);
   }
 }
 
@@ -335,10 +394,15 @@ topk_stream_kernel(const float* __restrict__ grad, float* __restrict__ residual,
 // cluster owns chunks [ms*r/CS, ms*(r+1)/CS) of the segment.
 // ---------------------------------------------------------------------------
 struct SelectArgs {
+  uint32_t CS;         // CTAs per segment (a thread-block cluster when > 1)
+  uint32_t warp_done;  // topk_select_short_kernel ran: only the segments in `todo` remain
+  uint32_t* todo;      // segments the short kernel left to topk_select_kernel
+  uint32_t* todo_cnt;
   float* residual;
   const uint32_t* seg_cnt;
   const uint32_t* seg_flag;
-  const uint32_t* chunk_cnt;
+  const uint32_t* sub_cnt;  // candidates per warp sub-chunk
+  const uint32_t* guess;    // per-segment lower bound G of the k-th key
   const uint32_t* cand_idx;
   const float* cand_val;
   uint32_t* out_idx;
@@ -350,13 +414,13 @@ struct SelectArgs {
 struct SelectShared {
   uint32_t hist[2048];
   uint32_t tot[2048];
-  uint32_t wpre[kWin + 1];
+  uint32_t wpre[kWin + 1];  // prefix of sub-chunk counts of a window
   uint32_t scratch[34];
   uint32_t res[2];
   uint32_t cnt[2];  // this CTA's (> T, == T) counts, read by higher ranks
 };
 
-// Exclusive prefix of the candidate counts of chunks [c0, c0 + nw) into
+// Exclusive prefix of the candidate counts of nw consecutive sub-chunks into
 // sh.wpre[0..nw]; returns the window total.
 __device__ uint32_t load_window(SelectShared& sh, const uint32_t* cc, uint32_t nw) {
   const uint32_t per = (kWin + kSelectThreads - 1) / kSelectThreads;
@@ -381,7 +445,7 @@ __device__ uint32_t load_window(SelectShared& sh, const uint32_t* cc, uint32_t n
   return total;
 }
 
-// Position v of a window -> its chunk (largest w with wpre[w] <= v).
+// Position v of a window -> its sub-chunk (largest w with wpre[w] <= v).
 __device__ __forceinline__ uint32_t window_chunk(const SelectShared& sh, uint32_t nw, uint32_t v) {
   uint32_t lo = 0, hi = nw;  // invariant: wpre[lo] <= v < wpre[hi]
   while (hi - lo > 1) {
@@ -391,14 +455,207 @@ __device__ __forceinline__ uint32_t window_chunk(const SelectShared& sh, uint32_
   return lo;
 }
 
-__global__ void __launch_bounds__(kSelectThreads)
-topk_select_kernel(SelectArgs a) {
-  __shared__ SelectShared sh;
-  cg::cluster_group cluster = cg::this_cluster();
-  const uint32_t CS = cluster.num_blocks();
-  const uint32_t rank = cluster.block_rank();
+// Select for a layer-sized segment whose candidates were all kept in their
+// sub-slots (at most kShortCands of them, over at most kShortSubs
+// sub-chunks): one warp per segment, no block barrier.
+//  1. lane L copies the contiguous candidate range [L*c, (L+1)*c) into the
+//     warp's shared memory with cp.async (every copy in flight at once),
+//     walking the sub-chunks with a cursor;
+//  2. four radix digits (8, 8, 8, 7 bits) of the k-th key T, each from one
+//     warp-private 256-bin histogram over the shared copy;
+//  3. each lane writes the kept entries of its range in index order at the
+//     offset given by warp scans of the per-lane counts (keys > T, and keys
+//     == T up to tie_take, lowest indices first); indices are resolved and the
+//     residual zeroed in a last batched pass.
+// Segments that do not qualify go to the to-do list of topk_select_kernel.
+constexpr uint32_t kShortSubs = 128;
+constexpr uint32_t kShortCands = 2048;
+constexpr uint32_t kShortWarps = 4;  // warps (segments) per CTA
+constexpr uint32_t kShortWords = kShortSubs + 1 + kShortCands + 256;
+
+__device__ __forceinline__ bool short_select_eligible(const SelectArgs& a, uint32_t gs, uint32_t k,
+                                                      uint32_t ms) {
+  return a.CS == 1 && a.seg_flag[gs] == 0 && a.seg_cnt[gs] >= k &&
+         ms * kWarpsPerChunk <= kShortSubs && a.seg_cnt[gs] <= kShortCands;
+}
+
+__device__ __forceinline__ uint32_t warp_excl_sum(uint32_t v, uint32_t* total) {
+  const uint32_t incl = warp_incl_sum(v);
+  *total = __shfl_sync(0xffffffffu, incl, 31);
+  return incl - v;
+}
+
+__global__ void __launch_bounds__(kShortWarps * 32)
+topk_select_short_kernel(SelectArgs a) {
+  extern __shared__ uint32_t dsm[];
   const Geo& g = a.g;
-  const uint32_t gs = blockIdx.x / CS;
+  const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+  const uint32_t gs = blockIdx.x * kShortWarps + warp;
+  if (gs >= (uint32_t)g.P * g.nseg) return;  // warp-uniform
+  const uint32_t p = gs / g.nseg, s = gs % g.nseg;
+  const uint32_t k = seg_k(g, s), ms = seg_chunks(g, s);
+  if (k == 0) return;
+  if (!short_select_eligible(a, gs, k, ms)) {  // hand it to topk_select_kernel
+    if (lane == 0) a.todo[atomicAdd(a.todo_cnt, 1u)] = gs;
+    return;
+  }
+  uint32_t* wpre = dsm + warp * kShortWords;
+  float* vals = reinterpret_cast<float*>(wpre + kShortSubs + 1);
+  uint32_t* hist = wpre + kShortSubs + 1 + kShortCands;
+  const uint32_t nsub = ms * kWarpsPerChunk;
+  const uint64_t sub0 = ((uint64_t)p * g.nchunk + (uint64_t)s * g.m) * kWarpsPerChunk;
+  const uint32_t* cidx = a.cand_idx + sub0 * g.slot;
+  const float* cval = a.cand_val + sub0 * g.slot;
+  // prefix of the sub-chunk counts (4 per lane)
+  {
+    uint32_t c4[4], sum = 0;
+#pragma unroll
+    for (uint32_t i = 0; i < 4; ++i) {
+      const uint32_t w = lane * 4 + i;
+      c4[i] = w < nsub ? a.sub_cnt[sub0 + w] : 0u;
+      sum += c4[i];
+    }
+    uint32_t tot;
+    uint32_t ex = warp_excl_sum(sum, &tot);
+#pragma unroll
+    for (uint32_t i = 0; i < 4; ++i) {
+      const uint32_t w = lane * 4 + i;
+      if (w < nsub) wpre[w] = ex;
+      ex += c4[i];
+    }
+    if (lane == 0) wpre[nsub] = tot;
+  }
+  __syncwarp();
+  const uint32_t M = wpre[nsub];
+  // 1. this lane's candidates [v_lo, v_hi) -> shared memory.
+  const uint32_t per = (M + 31) / 32;
+  const uint32_t v_lo = min(lane * per, M), v_hi = min(v_lo + per, M);
+  uint32_t w0 = 0;
+  for (uint32_t step = kShortSubs / 2; step > 0; step >>= 1)
+    if (w0 + step <= nsub && wpre[w0 + step] <= v_lo) w0 += step;
+  {
+    uint32_t w = w0;
+    for (uint32_t v = v_lo; v < v_hi; ++v) {
+      while (wpre[w + 1] <= v) ++w;
+      cp_async4(vals + v, cval + w * g.slot + (v - wpre[w]));
+    }
+  }
+  cp_async_wait_all();
+  __syncwarp();
+  // 2. radix digits of T (bits 30..23, 22..15, 14..7, 6..0).
+  uint32_t prefix = 0, rem = k;
+  for (int d = 0; d < 4; ++d) {
+    const uint32_t shift = d == 3 ? 0 : 23 - 8 * d;
+    const uint32_t wbits = d == 3 ? 7 : 8, hi_shift = shift + wbits;
+    for (uint32_t i = lane; i < 256; i += 32) hist[i] = 0;
+    __syncwarp();
+    for (uint32_t v0 = 0; v0 < M; v0 += 32) {
+      const uint32_t v = v0 + lane;
+      const uint32_t key = v < M ? mag_key(vals[v]) : 0u;
+      const bool match = v < M && (d == 0 || (key >> hi_shift) == prefix);
+      hist_add(hist, (key >> shift) & ((1u << wbits) - 1u), match);
+    }
+    __syncwarp();
+    // bins from high to low: lane covers 8 of them
+    uint32_t hb[8], sum = 0;
+#pragma unroll
+    for (uint32_t i = 0; i < 8; ++i) {
+      hb[i] = hist[255 - (8 * lane + i)];
+      sum += hb[i];
+    }
+    uint32_t tot;
+    const uint32_t excl = warp_excl_sum(sum, &tot);
+    uint32_t b = 0xffffffffu, ab = 0;
+    if (excl < rem && rem <= excl + sum) {
+      uint32_t acc = excl;
+#pragma unroll
+      for (uint32_t i = 0; i < 8; ++i) {
+        if (b == 0xffffffffu && acc + hb[i] >= rem) {
+          b = 255 - (8 * lane + i);
+          ab = acc;
+        }
+        acc += hb[i];
+      }
+    }
+    const uint32_t found = __ballot_sync(0xffffffffu, b != 0xffffffffu);
+    if (!found) {
+      if (lane == 0) set_status(a.status, SPARCML_ERR_BAD_STREAM);
+      b = 0;
+    } else {
+      const uint32_t src = __ffs(found) - 1;
+      b = __shfl_sync(0xffffffffu, b, src);
+      rem -= __shfl_sync(0xffffffffu, ab, src);
+    }
+    prefix = (prefix << wbits) | b;
+    __syncwarp();
+  }
+  const uint32_t T = prefix, tie_take = rem;  // keys == T to keep, lowest indices first
+  // 3. ordered write of this lane's range.
+  uint32_t n_gt = 0, n_eq = 0;
+  for (uint32_t v = v_lo; v < v_hi; ++v) {
+    const uint32_t key = mag_key(vals[v]);
+    n_gt += key > T ? 1u : 0u;
+    n_eq += key == T ? 1u : 0u;
+  }
+  uint32_t t_gt, t_eq;
+  uint32_t e_gt = warp_excl_sum(n_gt, &t_gt), e_eq = warp_excl_sum(n_eq, &t_eq);
+  float* rp = a.residual + (uint64_t)p * g.N;
+  const uint64_t out0 = (uint64_t)p * g.cap + (uint64_t)s * g.k_full;
+  uint32_t* oi = a.out_idx + out0;
+  const uint64_t keep = l2_policy_evict_last();
+  {
+    uint32_t w = w0;
+    for (uint32_t v = v_lo; v < v_hi; ++v) {
+      const float x = vals[v];
+      const uint32_t key = mag_key(x);
+      const bool gt = key > T, eq = key == T;
+      if (gt || (eq && e_eq < tie_take)) {
+        const uint32_t pos = e_gt + min(e_eq, tie_take);
+        while (wpre[w + 1] <= v) ++w;
+        if (pos < k) {
+          oi[pos] = w * g.slot + (v - wpre[w]);  // slot offset for now
+          st_keep(a.out_val + out0 + pos, x, keep);
+        } else {
+          set_status(a.status, SPARCML_ERR_BAD_STREAM);
+        }
+      }
+      e_gt += gt ? 1u : 0u;
+      e_eq += eq ? 1u : 0u;
+    }
+  }
+  __syncwarp();
+  // offsets -> indices; the residual is zeroed at each kept index.
+  constexpr uint32_t kB = 4;
+  for (uint32_t j0 = 0; j0 < k; j0 += 32 * kB) {
+    uint32_t off[kB], idx[kB];
+#pragma unroll
+    for (uint32_t q = 0; q < kB; ++q) {
+      const uint32_t j = j0 + q * 32 + lane;
+      off[q] = j < k ? oi[j] : 0u;
+    }
+#pragma unroll
+    for (uint32_t q = 0; q < kB; ++q) {
+      const uint32_t j = j0 + q * 32 + lane;
+      idx[q] = j < k ? cidx[off[q]] : 0u;
+    }
+#pragma unroll
+    for (uint32_t q = 0; q < kB; ++q) {
+      const uint32_t j = j0 + q * 32 + lane;
+      if (j < k) {
+        st_keep(oi + j, idx[q], keep);
+        rp[idx[q]] = 0.0f;
+      }
+    }
+  }
+}
+
+// Select for segment gs by CTA `rank` of the CS CTAs (a cluster when CS > 1)
+// that share it. Every CTA of a cluster calls this for the same segment.
+__device__ __forceinline__ void select_segment(const SelectArgs& a, SelectShared& sh,
+                                               cg::cluster_group& cluster, uint32_t gs,
+                                               uint32_t rank) {
+  const uint32_t CS = a.CS;
+  const Geo& g = a.g;
   const uint32_t p = gs / g.nseg, s = gs % g.nseg;
   const uint32_t n = seg_n(g, s), k = seg_k(g, s);
   if (k == 0) return;  // uniform over the cluster
@@ -415,29 +672,51 @@ topk_select_kernel(SelectArgs a) {
   const uint32_t raw_hi =
       (uint32_t)min((uint64_t)seg_start + (uint64_t)(cb - c_first) * kChunk, seg_end);
   float* rp = a.residual + (uint64_t)p * g.N;
-  const uint64_t node_chunk0 = (uint64_t)p * g.nchunk;
+  const uint64_t node_sub0 = (uint64_t)p * g.nchunk * kWarpsPerChunk;
+  const uint32_t sa = ca * kWarpsPerChunk, sb = cb * kWarpsPerChunk;  // this CTA's sub-chunks
 
   // Fast path: one CTA owns the segment and all its candidates fit in shared
   // memory. They are read from global memory once, in index order; the
   // radix select and the ordered compaction then run on the shared copy.
-  if (CS == 1 && !raw && ms <= kWin && a.seg_cnt[gs] <= kSmallCands) {
+  if (CS == 1 && !raw && ms * kWarpsPerChunk <= kWin && a.seg_cnt[gs] <= kSmallCands) {
     extern __shared__ uint32_t dsm[];
     uint32_t* s_idx = dsm;
     float* s_val = reinterpret_cast<float*>(dsm + kSmallCands);
-    const uint32_t M = load_window(sh, a.chunk_cnt + node_chunk0 + c_first, ms);
-    for (uint32_t v = t; v < M; v += blockDim.x) {
-      const uint32_t w = window_chunk(sh, ms, v);
-      const uint64_t slot = (node_chunk0 + c_first + w) * g.slot + (v - sh.wpre[w]);
-      s_idx[v] = a.cand_idx[slot];
-      s_val[v] = a.cand_val[slot];
+    const uint32_t nsub = ms * kWarpsPerChunk;
+    const uint32_t M = load_window(sh, a.sub_cnt + node_sub0 + sa, nsub);
+    constexpr uint32_t kLoadBatch = 4;  // candidate loads in flight per thread
+    for (uint32_t v0 = 0; v0 < M; v0 += blockDim.x * kLoadBatch) {
+      uint32_t li[kLoadBatch];
+      float lv[kLoadBatch];
+#pragma unroll
+      for (uint32_t u = 0; u < kLoadBatch; ++u) {
+        const uint32_t v = v0 + u * blockDim.x + t;
+        li[u] = 0;
+        lv[u] = 0.0f;
+        if (v < M) {
+          const uint32_t w = window_chunk(sh, nsub, v);
+          const uint64_t slot = (node_sub0 + sa + w) * g.slot + (v - sh.wpre[w]);
+          li[u] = a.cand_idx[slot];
+          lv[u] = a.cand_val[slot];
+        }
+      }
+#pragma unroll
+      for (uint32_t u = 0; u < kLoadBatch; ++u) {
+        const uint32_t v = v0 + u * blockDim.x + t;
+        if (v < M) {
+          s_idx[v] = li[u];
+          s_val[v] = lv[u];
+        }
+      }
     }
     __syncthreads();
-    const uint32_t shifts[3] = {20, 9, 0};
-    const uint32_t widths[3] = {11, 11, 9};
+    // Four 8-bit digits (bits 30..23, 22..15, 14..7, 6..0): 256 bins, one
+    // per thread, so zeroing and scanning a histogram costs one step.
     uint32_t prefix = 0, rem = k;
-    for (int d = 0; d < 3; ++d) {
-      const uint32_t shift = shifts[d], nb = 1u << widths[d], hi_shift = shift + widths[d];
-      for (uint32_t b = t; b < nb; b += blockDim.x) sh.hist[b] = 0;
+    for (int d = 0; d < 4; ++d) {
+      const uint32_t shift = d == 3 ? 0 : 23 - 8 * d;
+      const uint32_t nb = d == 3 ? 128 : 256, hi_shift = d == 0 ? 31 : shift + (d == 3 ? 7 : 8);
+      for (uint32_t b = t; b < 256; b += blockDim.x) sh.hist[b] = 0;
       __syncthreads();
       for (uint32_t v0 = 0; v0 < M; v0 += blockDim.x) {
         const uint32_t v = v0 + t;
@@ -446,7 +725,7 @@ topk_select_kernel(SelectArgs a) {
         hist_add(sh.hist, (key >> shift) & (nb - 1), match);
       }
       __syncthreads();
-      find_from_top(sh.hist, nb, rem, sh.scratch, sh.res);
+      find_from_top(sh.hist, 256, rem, sh.scratch, sh.res);
       uint32_t b = sh.res[0];
       if (b == kNone) {
         set_status(a.status, SPARCML_ERR_BAD_STREAM);
@@ -454,7 +733,7 @@ topk_select_kernel(SelectArgs a) {
       } else {
         rem -= sh.res[1];
       }
-      prefix = (prefix << widths[d]) | b;
+      prefix = (prefix << (d == 3 ? 7 : 8)) | b;
     }
     const uint32_t T = prefix, tie_take = rem;
     const uint64_t out0 = (uint64_t)p * g.cap + (uint64_t)s * g.k_full;
@@ -499,9 +778,9 @@ topk_select_kernel(SelectArgs a) {
         body(valid, i, valid ? rp[i] : 0.0f);
       }
     } else {
-      for (uint32_t w0 = ca; w0 < cb; w0 += kWin) {
-        const uint32_t nw = min(kWin, cb - w0);
-        const uint32_t total = load_window(sh, a.chunk_cnt + node_chunk0 + w0, nw);
+      for (uint32_t w0 = sa; w0 < sb; w0 += kWin) {
+        const uint32_t nw = min(kWin, sb - w0);
+        const uint32_t total = load_window(sh, a.sub_cnt + node_sub0 + w0, nw);
         for (uint32_t v0 = 0; v0 < total; v0 += blockDim.x) {
           const uint32_t v = v0 + t;
           const bool valid = v < total;
@@ -509,7 +788,7 @@ topk_select_kernel(SelectArgs a) {
           float x = 0.0f;
           if (valid) {
             const uint32_t w = window_chunk(sh, nw, v);
-            const uint64_t slot = (node_chunk0 + w0 + w) * g.slot + (v - sh.wpre[w]);
+            const uint64_t slot = (node_sub0 + w0 + w) * g.slot + (v - sh.wpre[w]);
             i = a.cand_idx[slot];
             x = a.cand_val[slot];
           }
@@ -521,11 +800,10 @@ topk_select_kernel(SelectArgs a) {
   };
 
   // Radix select of the k-th largest key: digits of 11, 11 and 9 bits.
-  const uint32_t shifts[3] = {20, 9, 0};
-  const uint32_t widths[3] = {11, 11, 9};
   uint32_t prefix = 0, rem = k;
   for (int d = 0; d < 3; ++d) {
-    const uint32_t shift = shifts[d], nb = 1u << widths[d], hi_shift = shift + widths[d];
+    const uint32_t width = d < 2 ? 11 : 9, shift = d == 0 ? 20 : (d == 1 ? 9 : 0);
+    const uint32_t nb = 1u << width, hi_shift = shift + width;
     for (uint32_t b = t; b < 2048; b += blockDim.x) sh.hist[b] = 0;
     __syncthreads();
     for_each([&](bool valid, uint32_t, float x) {
@@ -534,10 +812,14 @@ topk_select_kernel(SelectArgs a) {
       hist_add(sh.hist, (key >> shift) & (nb - 1), match);
     });
     __syncthreads();
-    cluster.sync();
+    if (CS > 1) cluster.sync();
     for (uint32_t b = t; b < nb; b += blockDim.x) {
       uint32_t sum = 0;
-      for (uint32_t q = 0; q < CS; ++q) sum += cluster.map_shared_rank(sh.hist, q)[b];
+      if (CS > 1) {
+        for (uint32_t q = 0; q < CS; ++q) sum += cluster.map_shared_rank(sh.hist, q)[b];
+      } else {
+        sum = sh.hist[b];
+      }
       sh.tot[b] = sum;
     }
     __syncthreads();
@@ -549,8 +831,8 @@ topk_select_kernel(SelectArgs a) {
     } else {
       rem -= sh.res[1];
     }
-    prefix = (prefix << widths[d]) | b;
-    cluster.sync();  // every CTA is done reading this CTA's histogram
+    prefix = (prefix << width) | b;
+    if (CS > 1) cluster.sync();  // every CTA is done reading this CTA's histogram
   }
   const uint32_t T = prefix;     // exact k-th largest key
   const uint32_t tie_take = rem;  // keys == T to keep, lowest indices first
@@ -571,14 +853,16 @@ topk_select_kernel(SelectArgs a) {
     if (t == 0) sh.cnt[1] = tot;
     __syncthreads();
   }
-  cluster.sync();
   uint32_t gt_pre = 0, eq_pre = 0;
-  for (uint32_t q = 0; q < rank; ++q) {
-    const uint32_t* rc = cluster.map_shared_rank(sh.cnt, q);
-    gt_pre += rc[0];
-    eq_pre += rc[1];
+  if (CS > 1) {
+    cluster.sync();
+    for (uint32_t q = 0; q < rank; ++q) {
+      const uint32_t* rc = cluster.map_shared_rank(sh.cnt, q);
+      gt_pre += rc[0];
+      eq_pre += rc[1];
+    }
+    cluster.sync();  // peers may exit or reuse their shared memory after this
   }
-  cluster.sync();  // peers may exit or reuse their shared memory after this
 
   // Ordered compaction of the kept entries.
   const uint64_t out0 = (uint64_t)p * g.cap + (uint64_t)s * g.k_full;
@@ -606,8 +890,23 @@ topk_select_kernel(SelectArgs a) {
   });
 }
 
+__global__ void __launch_bounds__(kSelectThreads)
+topk_select_kernel(SelectArgs a) {
+  __shared__ SelectShared sh;
+  cg::cluster_group cluster = cg::this_cluster();
+  if (a.warp_done) {  // only the segments the short kernel handed over
+    const uint32_t n_todo = *a.todo_cnt;
+    for (uint32_t i = blockIdx.x; i < n_todo; i += gridDim.x) {
+      select_segment(a, sh, cluster, a.todo[i], 0);
+      __syncthreads();
+    }
+  } else {
+    select_segment(a, sh, cluster, blockIdx.x / a.CS, a.CS > 1 ? cluster.block_rank() : 0u);
+  }
+}
+
 struct Layout {
-  size_t guess, seg_cnt, seg_flag, chunk_cnt, cand_idx, cand_val, total;
+  size_t todo_cnt, guess, seg_cnt, seg_flag, todo, chunk_cnt, cand_idx, cand_val, total;
 };
 
 bool make_geo(int32_t P, uint64_t N, uint64_t seg_len, uint32_t k_num, uint32_t k_den, Geo* g) {
@@ -630,8 +929,8 @@ bool make_geo(int32_t P, uint64_t N, uint64_t seg_len, uint32_t k_num, uint32_t 
   g->k_last = (uint32_t)((uint64_t)g->L_last * k_num / k_den);
   // Expected candidates are about d + a few per cent of a chunk; the slot
   // holds 2d + 1/8 of it (or all of it), and overflow falls back safely.
-  const double want = (double)kChunk * (2.0 * k_num / k_den) + kChunk / 8.0;
-  uint32_t slot = (uint32_t)std::min<double>(kChunk, std::ceil(want / 32.0) * 32.0);
+  const double want = (double)kSub * (2.0 * k_num / k_den) + kSub / 8.0;
+  uint32_t slot = (uint32_t)std::min<double>(kSub, std::ceil(want / 32.0) * 32.0);
   g->slot = std::max<uint32_t>(slot, 32);
   g->P = P;
   return true;
@@ -640,8 +939,10 @@ bool make_geo(int32_t P, uint64_t N, uint64_t seg_len, uint32_t k_num, uint32_t 
 Layout make_layout(const Geo& g) {
   Layout l;
   size_t o = 256;  // status word and padding
-  const size_t nsegs = (size_t)g.P * g.nseg, nch = (size_t)g.P * g.nchunk;
+  const size_t nsegs = (size_t)g.P * g.nseg, nch = (size_t)g.P * g.nchunk * kWarpsPerChunk;
+  l.todo_cnt = 64;
   l.guess = o; o = align_up(o + 4 * nsegs, 256);
+  l.todo = o; o = align_up(o + 4 * nsegs, 256);
   l.seg_cnt = o; o = align_up(o + 4 * nsegs, 256);
   l.seg_flag = o; o = align_up(o + 4 * nsegs, 256);
   l.chunk_cnt = o; o = align_up(o + 4 * nch, 256);
@@ -686,14 +987,33 @@ extern "C" int sparcml_topk_ef_traced(const float* grad, float* residual, int32_
   uint32_t* cand_idx = reinterpret_cast<uint32_t*>(w + l.cand_idx);
   float* cand_val = reinterpret_cast<float*>(w + l.cand_val);
   int32_t* status = reinterpret_cast<int32_t*>(w);
+  uint32_t* todo = reinterpret_cast<uint32_t*>(w + l.todo);
+  uint32_t* todo_cnt = reinterpret_cast<uint32_t*>(w + l.todo_cnt);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   auto mark = [&](int i) {
     if (events && events[i]) cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s);
   };
 
   mark(0);
-  topk_guess_kernel<<<(unsigned)(P * g.nseg), kGuessThreads, 0, s>>>(
-      grad, residual, g, guess, seg_cnt, seg_flag, out_nnz, (uint32_t)total_k);
+  const uint32_t nsegs = (uint32_t)P * g.nseg;
+  if (g.L > kSampleMax && g.L <= kShortSegment && g.L_last > kSampleMax) {
+    // layer-sized segments: one warp each
+    const uint32_t wpc = kGuessThreads / 32;
+    topk_guess_warp_kernel<<<(nsegs + wpc - 1) / wpc, kGuessThreads, 0, s>>>(
+        grad, residual, g, guess, seg_cnt, seg_flag, out_nnz, (uint32_t)total_k, todo_cnt);
+  } else {
+    // Keys per guess thread: the largest sample of any segment / kGuessThreads.
+    auto sample_size = [](uint32_t n) {
+      return n <= kSampleMax ? n : (n <= kShortSegment ? kSampleShort : kSampleMax);
+    };
+    const uint32_t smax = std::max(sample_size(g.L), sample_size(g.L_last));
+    if (smax <= 16 * kGuessThreads)
+      topk_guess_kernel<16><<<nsegs, kGuessThreads, 0, s>>>(
+          grad, residual, g, guess, seg_cnt, seg_flag, out_nnz, (uint32_t)total_k, todo_cnt);
+    else
+      topk_guess_kernel<kSampleMax / kGuessThreads><<<nsegs, kGuessThreads, 0, s>>>(
+          grad, residual, g, guess, seg_cnt, seg_flag, out_nnz, (uint32_t)total_k, todo_cnt);
+  }
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   mark(1);
   topk_stream_kernel<<<(unsigned)((uint64_t)P * g.nchunk), kStreamThreads, 0, s>>>(
@@ -704,10 +1024,20 @@ extern "C" int sparcml_topk_ef_traced(const float* grad, float* residual, int32_
   // Cluster size: enough CTAs per segment to spread its chunks (<= 8).
   uint32_t CS = 1;
   while (CS < 8 && (uint64_t)g.m / (CS * 2) >= 64) CS *= 2;
-  SelectArgs a{residual, seg_cnt, seg_flag, chunk_cnt, cand_idx, cand_val,
-               out_idx, out_val, status, g};
+  SelectArgs a{CS, CS == 1 ? 1u : 0u, todo, todo_cnt, residual, seg_cnt, seg_flag, chunk_cnt,
+               guess, cand_idx, cand_val, out_idx, out_val, status, g};
+  if (CS == 1) {  // layer-sized segments: one warp each
+    const size_t smem = (size_t)kShortWarps * kShortWords * sizeof(uint32_t);
+    if (!ensure_smem(reinterpret_cast<const void*>(topk_select_short_kernel), smem))
+      return SPARCML_ERR_CUDA;
+    topk_select_short_kernel<<<(nsegs + kShortWarps - 1) / kShortWarps, kShortWarps * 32, smem,
+                               s>>>(a);
+    if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
+  }
+  // CS == 1: a small grid walks the segments the short kernel handed over.
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((uint64_t)P * g.nseg * CS), 1, 1);
+  cfg.gridDim = dim3(CS == 1 ? std::min<unsigned>(nsegs, 2 * 152)
+                             : (unsigned)((uint64_t)P * g.nseg * CS), 1, 1);
   cfg.blockDim = dim3(kSelectThreads, 1, 1);
   cfg.dynamicSmemBytes = 2 * kSmallCands * sizeof(uint32_t);
   cfg.stream = s;
@@ -718,12 +1048,16 @@ extern "C" int sparcml_topk_ef_traced(const float* grad, float* residual, int32_
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)cfg.dynamicSmemBytes) != cudaSuccess)
+  if (!ensure_smem(reinterpret_cast<const void*>(topk_select_kernel), cfg.dynamicSmemBytes))
     return SPARCML_ERR_CUDA;
-  if (cudaLaunchKernelEx(&cfg, topk_select_kernel, a) != cudaSuccess) return SPARCML_ERR_CUDA;
+  if (CS == 1) {
+    topk_select_kernel<<<cfg.gridDim, cfg.blockDim, cfg.dynamicSmemBytes, s>>>(a);
+    if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
+  } else if (cudaLaunchKernelEx(&cfg, topk_select_kernel, a) != cudaSuccess) {
+    return SPARCML_ERR_CUDA;
+  }
   mark(3);
-  note_launches(3);
+  note_launches(CS == 1 ? 4 : 3);
   return SPARCML_OK;
 }
 
