@@ -198,3 +198,19 @@ def test_reduce_q4_equals_dequantize_then_reduce(k, dense):
     else:
         assert np.array_equal(u32(out.idx[:U]), ref["idx"])
         assert np.array_equal(bits(out.val[:U].cpu().numpy()), bits(ref["val"]))
+
+
+def test_reduce_sparse_regime_skewed_tile():
+    """Sparse inputs take wide tiles with a compact accumulator; a tile that
+    still receives many thousand entries (skew) is accumulated in several slot
+    windows from re-read entries. Checked bit for bit against the oracle."""
+    rng = np.random.default_rng(12)
+    P, N, cap = 3, 4_194_304, 20_000
+    idx = np.zeros((P, cap), np.uint32)
+    val = rng.standard_normal((P, cap)).astype(np.float32)
+    nnz = np.full(P, cap, np.uint32)
+    idx[0] = np.arange(cap, dtype=np.uint32) * 3            # 20,000 entries in the first wide tile
+    idx[1] = np.sort(rng.choice(60_000, cap, replace=False))  # overlapping the same tile
+    idx[2] = np.sort(rng.choice(N, cap, replace=False))       # spread out
+    r = check_reduce(idx, val, nnz, N, repeat=2)
+    assert not r["is_dense"] and r["nnz"] > 8192

@@ -57,6 +57,7 @@ struct ReduceArgs {
   int32_t P;
   uint32_t N;
   uint32_t ntiles;
+  uint32_t tile_w;      // indices per tile: kTile (dense regime) or a wider power of two
   uint32_t cap_sparse;  // floor(N * num / den): largest sparse result
   uint32_t* out_idx;
   float* out_val;
@@ -95,6 +96,50 @@ __device__ __forceinline__ float load_value(const ReduceArgs& a, uint32_t p, uin
   }
 }
 
+// Decoupled look-back (Merrill and Garland, 2016), one warp wide: the tile
+// publishes its count, then reads the states of the 32 nearest predecessors
+// at once and sums back to the nearest inclusive prefix; it publishes its own
+// inclusive prefix and leaves its exclusive offset in *out. Every wait is
+// bounded (SPARCML_ERR_TIMEOUT, then it carries on). Called by the whole
+// CTA; only warp 0 works.
+__device__ void tile_lookback(const ReduceArgs& a, uint32_t tile, uint32_t count, uint32_t* out) {
+  const uint32_t t = threadIdx.x, lane = lane_id();
+  if (t >= 32) return;
+  unsigned long long* st = a.tile_state;
+  uint32_t excl = 0;
+  if (tile == 0) {
+    if (t == 0) atomicExch(&st[0], kFlagInc | count);
+  } else {
+    if (t == 0) atomicExch(&st[tile], kFlagAgg | count);
+    int64_t base = (int64_t)tile - 1;
+    uint32_t spins = 0, backoff = 32;
+    while (true) {
+      const int64_t j = base - (int64_t)lane;
+      const unsigned long long sv =
+          j >= 0 ? *reinterpret_cast<volatile unsigned long long*>(&st[j]) : (2ull << 62);
+      const unsigned long long flag = sv & (3ull << 62);
+      const uint32_t inc = __ballot_sync(0xffffffffu, flag == kFlagInc);
+      const uint32_t notready = __ballot_sync(0xffffffffu, flag == 0);
+      const uint32_t upto = inc ? (uint32_t)(__ffs(inc) - 1) : 31u;  // lanes 0..upto count
+      const uint32_t need = upto == 31 ? 0xffffffffu : ((2u << upto) - 1u);
+      if (notready & need) {
+        if (++spins > kSpinLimit) {
+          if (t == 0) set_status(a.status, SPARCML_ERR_TIMEOUT);
+          break;
+        }
+        __nanosleep(backoff);
+        backoff = min(backoff * 2, 1024u);
+        continue;
+      }
+      excl += warp_sum(lane <= upto ? (uint32_t)sv : 0u);
+      if (inc) break;
+      base -= 32;
+    }
+    if (t == 0) atomicExch(&st[tile], kFlagInc | (excl + count));
+  }
+  if (t == 0) *out = excl;
+}
+
 // Where each node's entries for tile t start: split[t * P + p] =
 // lower_bound(idx_p, t * kTile) for t < ntiles and lower_bound(idx_p, N) for
 // t = ntiles. One warp per (tile boundary, node): each round probes 32
@@ -102,14 +147,14 @@ __device__ __forceinline__ float load_value(const ReduceArgs& a, uint32_t p, uin
 // per memory round trip instead of 2-fold.
 __global__ void __launch_bounds__(256)
 reduce_split_kernel(const uint32_t* __restrict__ idx, const uint32_t* __restrict__ nnz,
-                    int32_t P, uint64_t cap, uint32_t N, uint32_t ntiles,
+                    int32_t P, uint64_t cap, uint32_t N, uint32_t ntiles, uint32_t tile_w,
                     uint32_t* __restrict__ split) {
   const uint64_t w = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (w >= (uint64_t)(ntiles + 1) * P) return;  // warp-uniform
   const uint32_t lane = lane_id();
   const uint32_t t = (uint32_t)(w / P), p = (uint32_t)(w % P);
   const uint32_t n = (uint32_t)min((uint64_t)nnz[p], cap);
-  const uint32_t x = t == ntiles ? N : t * kTile;
+  const uint32_t x = t == ntiles ? N : t * tile_w;
   const uint32_t* a = idx + (uint64_t)p * cap;
   uint32_t lo = 0, hi = n;  // the answer lies in [lo, hi]
   while (hi - lo > 32) {
@@ -264,44 +309,8 @@ reduce_tile_kernel(ReduceArgs a) {
   uint32_t count;
   block_excl_scan(c, scratch, &count);
 
-  // Decoupled look-back for the tile's exclusive offset, one warp wide: each
-  // round reads the states of the 32 nearest predecessors at once and sums
-  // back to the nearest inclusive prefix.
-  if (t < 32) {
-    unsigned long long* st = a.tile_state;
-    uint32_t excl = 0;
-    if (tile == 0) {
-      if (t == 0) atomicExch(&st[0], kFlagInc | count);
-    } else {
-      if (t == 0) atomicExch(&st[tile], kFlagAgg | count);
-      int64_t base = (int64_t)tile - 1;
-      uint32_t spins = 0, backoff = 32;
-      while (true) {
-        const int64_t j = base - (int64_t)lane;
-        const unsigned long long sv =
-            j >= 0 ? *reinterpret_cast<volatile unsigned long long*>(&st[j]) : (2ull << 62);
-        const unsigned long long flag = sv & (3ull << 62);
-        const uint32_t inc = __ballot_sync(0xffffffffu, flag == kFlagInc);
-        const uint32_t notready = __ballot_sync(0xffffffffu, flag == 0);
-        const uint32_t upto = inc ? (uint32_t)(__ffs(inc) - 1) : 31u;  // lanes 0..upto count
-        const uint32_t need = upto == 31 ? 0xffffffffu : ((2u << upto) - 1u);
-        if (notready & need) {
-          if (++spins > kSpinLimit) {
-            if (t == 0) set_status(a.status, SPARCML_ERR_TIMEOUT);
-            break;
-          }
-          __nanosleep(backoff);
-          backoff = min(backoff * 2, 1024u);
-          continue;
-        }
-        excl += warp_sum(lane <= upto ? (uint32_t)sv : 0u);
-        if (inc) break;
-        base -= 32;
-      }
-      if (t == 0) atomicExch(&st[tile], kFlagInc | (excl + count));
-    }
-    if (t == 0) bc[2] = excl;
-  }
+  // Decoupled look-back for the tile's exclusive offset.
+  tile_lookback(a, tile, count, &bc[2]);
   __syncthreads();
   const uint32_t excl = bc[2];
   const uint32_t incl = excl + count;
@@ -338,16 +347,223 @@ reduce_tile_kernel(ReduceArgs a) {
   }
 }
 
+// Sparse regime: tiles of a.tile_w indices (up to kMaxTileW), chosen so a
+// tile holds about two thousand entries. Shared memory scales with the
+// tile's union, not its width: a presence bitmap is built first, its prefix
+// popcounts give every present index a slot (its rank in the tile), and the
+// sums go to a compact fp32 array of slots. Accumulation keeps ascending node
+// order (barrier after each node with entries in a batch), so the bits equal
+// the dense-accumulator kernel's. Tiles whose union exceeds kAccCap are
+// accumulated in several slot windows.
+constexpr uint32_t kMaxTileW = 1u << 17;
+constexpr uint32_t kMaxWords = kMaxTileW / 32;
+constexpr uint32_t kAccCap = 8192;
+constexpr int32_t kMaxSparseP = 1024;
+
+template <bool Q4>
+__global__ void __launch_bounds__(kReduceThreads)
+reduce_sparse_tile_kernel(ReduceArgs a) {
+  extern __shared__ __align__(16) uint32_t dyn[];
+  const uint32_t W = a.tile_w / 32;
+  uint32_t* bm = dyn;                                    // [W] presence bits
+  uint32_t* woff = bm + W;                               // [W] slots before each word
+  float* acc = reinterpret_cast<float*>(woff + W);       // [kAccCap] compact sums
+  uint32_t* lo = reinterpret_cast<uint32_t*>(acc + kAccCap);  // [P]
+  uint32_t* pre = lo + a.P;                              // [P + 1]
+  __shared__ uint32_t scratch[34];
+  __shared__ uint32_t bc[4];
+  const uint32_t t = threadIdx.x, lane = lane_id();
+
+  if (t == 0) {
+    bc[0] = atomicAdd(a.ticket, 1u);
+    bc[1] = 0;
+  }
+  for (uint32_t w = t; w < W; w += blockDim.x) bm[w] = 0;
+  __syncthreads();
+  const uint32_t tile = bc[0];
+  const uint32_t tile_lo = tile * a.tile_w;
+  const uint32_t tile_n = min(a.tile_w, a.N - tile_lo);
+  const bool last = tile == a.ntiles - 1;
+  for (int32_t p = t; p < a.P; p += blockDim.x) {
+    uint32_t n = a.nnz[p];
+    if (n > a.cap) {
+      set_status(a.status, SPARCML_ERR_CAPACITY);
+      n = (uint32_t)a.cap;
+    }
+    const uint32_t l = a.split[(uint64_t)tile * a.P + p];
+    uint32_t h = a.split[(uint64_t)(tile + 1) * a.P + p];
+    if (last && h < n) set_status(a.status, SPARCML_ERR_BAD_STREAM);  // idx >= N
+    if (h < l) {
+      set_status(a.status, SPARCML_ERR_BAD_STREAM);
+      h = l;
+    }
+    lo[p] = l;
+    pre[p] = h - l;
+    atomicMax(&bc[1], n);
+  }
+  __syncthreads();
+  uint32_t E = 0;
+  for (int32_t base = 0; base < a.P; base += blockDim.x) {
+    const int32_t p = base + (int32_t)t;
+    const uint32_t c = p < a.P ? pre[p] : 0u;
+    uint32_t tot;
+    const uint32_t ex = block_excl_scan(c, scratch, &tot);
+    if (p < a.P) pre[p] = E + ex;
+    E += tot;
+    __syncthreads();
+  }
+  if (t == 0) pre[a.P] = E;
+  __syncthreads();
+  const bool dense_certain = bc[1] > a.cap_sparse;
+  auto node_of = [&](uint32_t v) {
+    uint32_t l = 0, h = (uint32_t)a.P;
+    while (h - l > 1) {
+      const uint32_t m = (l + h) >> 1;
+      if (pre[m] <= v) l = m; else h = m;
+    }
+    return l;
+  };
+  const uint32_t batch = blockDim.x * kUnroll;
+  const bool resident = E <= batch;  // all entries stay in registers
+  uint32_t iv[kUnroll], pv[kUnroll];
+  float vv[kUnroll];
+  // Load batch c0 into registers; entries that fail the stream checks get
+  // pv = kNoNode and are skipped.
+  constexpr uint32_t kNoNode = 0xffffffffu;
+  auto load_batch = [&](uint32_t c0) {
+#pragma unroll
+    for (uint32_t u = 0; u < kUnroll; ++u) {
+      const uint32_t v = c0 + u * blockDim.x + t;
+      iv[u] = 0;
+      vv[u] = 0.0f;
+      pv[u] = kNoNode;
+      if (v < E) {
+        const uint32_t p = node_of(v);
+        const uint32_t j = lo[p] + (v - pre[p]);
+        iv[u] = a.idx[(uint64_t)p * a.cap + j];
+        vv[u] = load_value<Q4>(a, p, j);
+        pv[u] = p;
+      }
+    }
+#pragma unroll
+    for (uint32_t u = 0; u < kUnroll; ++u) {
+      const uint32_t v = c0 + u * blockDim.x + t;
+      uint32_t prev = __shfl_up_sync(0xffffffffu, iv[u], 1);
+      if (v < E) {
+        const uint32_t p = pv[u];
+        const uint32_t j = lo[p] + (v - pre[p]);
+        if ((lane == 0 || v == pre[p]) && j > 0) prev = a.idx[(uint64_t)p * a.cap + j - 1];
+        if (!((j == 0 || prev < iv[u]) && iv[u] - tile_lo < tile_n)) {
+          set_status(a.status, SPARCML_ERR_BAD_STREAM);
+          pv[u] = kNoNode;
+        }
+      }
+    }
+  };
+  // 1. presence bits
+  for (uint32_t c0 = 0; c0 < E; c0 += batch) {
+    load_batch(c0);
+#pragma unroll
+    for (uint32_t u = 0; u < kUnroll; ++u)
+      if (pv[u] != kNoNode) {
+        const uint32_t off = iv[u] - tile_lo;
+        atomicOr(&bm[off >> 5], 1u << (off & 31));
+      }
+  }
+  __syncthreads();
+  // 2. slots: exclusive prefix of the words' popcounts (consecutive words per thread)
+  const uint32_t wpt = (W + blockDim.x - 1) / blockDim.x;
+  uint32_t cnt = 0;
+  for (uint32_t i = 0; i < wpt; ++i) {
+    const uint32_t w = t * wpt + i;
+    cnt += w < W ? __popc(bm[w]) : 0u;
+  }
+  uint32_t U;
+  uint32_t run = block_excl_scan(cnt, scratch, &U);
+  for (uint32_t i = 0; i < wpt; ++i) {
+    const uint32_t w = t * wpt + i;
+    if (w < W) {
+      woff[w] = run;
+      run += __popc(bm[w]);
+    }
+  }
+  // 3. the tile's output offset
+  tile_lookback(a, tile, U, &bc[2]);
+  __syncthreads();
+  const uint32_t excl = bc[2];
+  const uint32_t incl = excl + U;
+  const bool dense = dense_certain || incl > a.cap_sparse;
+  // 4. accumulate and emit, slot window by slot window
+  for (uint32_t s0 = 0; s0 < U || (s0 == 0 && dense); s0 += kAccCap) {
+    const uint32_t win = min(kAccCap, U - min(U, s0));
+    for (uint32_t i = t; i < win; i += blockDim.x) acc[i] = 0.0f;
+    __syncthreads();
+    for (uint32_t c0 = 0; c0 < E; c0 += batch) {
+      if (!resident) load_batch(c0);
+      const uint32_t c1 = min(c0 + batch, E);
+      const uint32_t p_first = node_of(c0), p_last = node_of(c1 - 1);
+      for (uint32_t p = p_first; p <= p_last; ++p) {
+        if (pre[p + 1] == pre[p]) continue;  // no entries: no barrier needed
+#pragma unroll
+        for (uint32_t u = 0; u < kUnroll; ++u) {
+          if (pv[u] == p) {
+            const uint32_t off = iv[u] - tile_lo, w = off >> 5;
+            const uint32_t slot = woff[w] + __popc(bm[w] & ((1u << (off & 31)) - 1u));
+            if (slot - s0 < win) acc[slot - s0] = __fadd_rn(acc[slot - s0], vv[u]);
+          }
+        }
+        __syncthreads();
+      }
+    }
+    if (dense) {
+      // every index of the tile once: present ones in the window of their slot,
+      // absent ones (+0.0f) in the first window
+      float* od = a.out_dense + tile_lo;
+      for (uint32_t x = t; x < tile_n; x += blockDim.x) {
+        const uint32_t w = x >> 5, bit = 1u << (x & 31);
+        if (bm[w] & bit) {
+          const uint32_t slot = woff[w] + __popc(bm[w] & (bit - 1u));
+          if (slot - s0 < win) od[x] = acc[slot - s0];
+        } else if (s0 == 0) {
+          od[x] = 0.0f;
+        }
+      }
+    } else {
+      for (uint32_t w = t; w < W; w += blockDim.x) {
+        uint32_t bits = bm[w];
+        uint32_t slot = woff[w];
+        while (bits) {
+          const uint32_t b = __ffs(bits) - 1;
+          bits &= bits - 1;
+          if (slot - s0 < win) {
+            a.out_idx[excl + slot] = tile_lo + w * 32 + b;
+            a.out_val[excl + slot] = acc[slot - s0];
+          }
+          ++slot;
+        }
+      }
+    }
+    __syncthreads();
+  }
+  if (t == 0) {
+    a.tile_info[tile] = make_uint2(excl, U | (dense ? 0x80000000u : 0u));
+    if (last) {
+      *a.out_nnz = incl;
+      *a.out_is_dense = dense ? 1 : 0;
+    }
+  }
+}
+
 // Dense result: rewrite the leading tiles that were emitted sparse.
 __global__ void __launch_bounds__(256)
 reduce_fixup_kernel(const int32_t* __restrict__ is_dense, const uint2* __restrict__ tile_info,
                     const uint32_t* __restrict__ out_idx, const float* __restrict__ out_val,
-                    float* __restrict__ out_dense, uint32_t N) {
+                    float* __restrict__ out_dense, uint32_t N, uint32_t tile_w) {
   if (*is_dense == 0) return;
   const uint2 info = tile_info[blockIdx.x];
   if (info.y & 0x80000000u) return;
-  const uint32_t tile_lo = blockIdx.x * kTile;
-  const uint32_t tile_n = min(kTile, N - tile_lo);
+  const uint32_t tile_lo = blockIdx.x * tile_w;
+  const uint32_t tile_n = min(tile_w, N - tile_lo);
   for (uint32_t x = threadIdx.x; x < tile_n; x += blockDim.x) out_dense[tile_lo + x] = 0.0f;
   __syncthreads();
   for (uint32_t e = threadIdx.x; e < info.y; e += blockDim.x) {
@@ -389,19 +605,38 @@ int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
   // Clear the ticket and the look-back states (the status word is kept).
   if (cudaMemsetAsync(w + l.ticket, 0, l.info - l.ticket, s) != cudaSuccess)
     return SPARCML_ERR_CUDA;
-  const size_t smem = (kTile + kWords + 2 * (size_t)a.P + 1) * sizeof(uint32_t);
-  if (!ensure_smem(reinterpret_cast<const void*>(reduce_tile_kernel<Q4, true>), smem))
-    return SPARCML_ERR_CUDA;
+  // Regime: the entries of an 8,192-index tile are at most P * cap * 8192 / N.
+  // Sparse inputs take wide tiles (about 2,048 entries each) with a compact
+  // accumulator; denser ones the dense-accumulator tile of kTile indices.
+  const double est = (double)a.P * (double)a.cap * kTile / (double)a.N;
+  uint32_t tile_w = kTile;
+  if (a.P <= kMaxSparseP && est <= 512.0) {
+    while (tile_w < kMaxTileW && est * (2.0 * tile_w / kTile) <= 2048.0 && tile_w < a.N)
+      tile_w *= 2;
+  }
+  a.tile_w = tile_w;
+  a.ntiles = (uint32_t)((a.N + tile_w - 1) / tile_w);
   mark(0);
   const uint64_t nsplit = (uint64_t)(a.ntiles + 1) * a.P;  // one warp each
   reduce_split_kernel<<<(unsigned)((nsplit * 32 + 255) / 256), 256, 0, s>>>(
-      a.idx, a.nnz, a.P, a.cap, a.N, a.ntiles, split);
+      a.idx, a.nnz, a.P, a.cap, a.N, a.ntiles, a.tile_w, split);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
-  reduce_tile_kernel<Q4, true><<<a.ntiles, kReduceThreads, smem, s>>>(a);
+  if (tile_w > kTile) {
+    const size_t smem =
+        (2 * (size_t)(tile_w / 32) + kAccCap + 2 * (size_t)a.P + 1) * sizeof(uint32_t);
+    if (!ensure_smem(reinterpret_cast<const void*>(reduce_sparse_tile_kernel<Q4>), smem))
+      return SPARCML_ERR_CUDA;
+    reduce_sparse_tile_kernel<Q4><<<a.ntiles, kReduceThreads, smem, s>>>(a);
+  } else {
+    const size_t smem = (kTile + kWords + 2 * (size_t)a.P + 1) * sizeof(uint32_t);
+    if (!ensure_smem(reinterpret_cast<const void*>(reduce_tile_kernel<Q4, true>), smem))
+      return SPARCML_ERR_CUDA;
+    reduce_tile_kernel<Q4, true><<<a.ntiles, kReduceThreads, smem, s>>>(a);
+  }
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   mark(1);
   reduce_fixup_kernel<<<a.ntiles, 256, 0, s>>>(a.out_is_dense, a.tile_info, a.out_idx,
-                                               a.out_val, a.out_dense, a.N);
+                                               a.out_val, a.out_dense, a.N, a.tile_w);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   mark(2);
   note_launches(3);
@@ -580,6 +815,7 @@ extern "C" int sparcml_sparse_reduce_noalloc(const uint32_t* idx, const float* v
   a.P = P;
   a.N = (uint32_t)N;
   a.ntiles = (uint32_t)((N + kTile - 1) / kTile);
+  a.tile_w = kTile;
   a.cap_sparse = (uint32_t)(N * dens_num / dens_den);
   a.out_idx = out_idx;
   a.out_val = out_val;
@@ -600,7 +836,7 @@ extern "C" int sparcml_sparse_reduce_noalloc(const uint32_t* idx, const float* v
   reduce_tile_kernel<false><<<a.ntiles, kReduceThreads, smem, s>>>(a);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   reduce_fixup_kernel<<<a.ntiles, 256, 0, s>>>(a.out_is_dense, a.tile_info, a.out_idx,
-                                               a.out_val, a.out_dense, a.N);
+                                               a.out_val, a.out_dense, a.N, a.tile_w);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   note_launches(2);
   return SPARCML_OK;
