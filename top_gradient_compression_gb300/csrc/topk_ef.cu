@@ -396,6 +396,7 @@ topk_stream_kernel(const float* __restrict__ grad, float* __restrict__ residual,
 struct SelectArgs {
   uint32_t CS;         // CTAs per segment (a thread-block cluster when > 1)
   uint32_t warp_done;  // topk_select_short_kernel ran: only the segments in `todo` remain
+  uint32_t raw_only;   // the long-segment passes ran: only fallback segments remain
   uint32_t* todo;      // segments the short kernel left to topk_select_kernel
   uint32_t* todo_cnt;
   float* residual;
@@ -661,6 +662,7 @@ __device__ __forceinline__ void select_segment(const SelectArgs& a, SelectShared
   if (k == 0) return;  // uniform over the cluster
   const uint32_t t = threadIdx.x;
   const bool raw = a.seg_flag[gs] != 0 || a.seg_cnt[gs] < k;
+  if (a.raw_only && !raw) return;  // done by the long-segment passes
   const uint32_t ms = seg_chunks(g, s);
   const uint32_t c_first = s * g.m;  // node-local id of the segment's first chunk
   const uint32_t ca = c_first + (uint32_t)((uint64_t)ms * rank / CS);
@@ -890,6 +892,249 @@ __device__ __forceinline__ void select_segment(const SelectArgs& a, SelectShared
   });
 }
 
+// ---------------------------------------------------------------------------
+// Long segments (thousands of chunks): the exact select as a sequence of
+// grid-wide passes, each CTA owning a range of kRangeSubs warp sub-chunks of
+// one segment (a few hundred candidates), so the whole GPU works on every
+// pass:
+//   long_hist  x3  histogram of one radix digit (11, 11, 9 bits) of the keys
+//                  that match the prefix so far, per CTA in shared memory,
+//                  flushed into the segment's global histogram;
+//   long_find  x3  one CTA per segment: the boundary bin -> prefix, rank left;
+//   long_count     per range: keys > T and keys == T;
+//   long_scan      one CTA per segment: exclusive prefix over its ranges;
+//   long_write     per range: the kept entries in index order, residual = 0.
+// Segments whose candidates do not cover k (or overflowed a slot) are left to
+// topk_select_kernel, which reads their acc directly.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kRangeSubs = 256;
+constexpr uint32_t kHistWords = 2048 + 2048 + 512;  // per segment: the three digits
+
+struct LongArgs {
+  Geo g;
+  const uint32_t* seg_cnt;
+  const uint32_t* seg_flag;
+  const uint32_t* sub_cnt;
+  const uint32_t* cand_idx;
+  const float* cand_val;
+  float* residual;
+  uint32_t* out_idx;
+  float* out_val;
+  int32_t* status;
+  uint32_t* hist;       // [P * nseg][kHistWords]
+  uint32_t* sel;        // [P * nseg][2]: prefix so far, rank left (then T, tie_take)
+  uint32_t* range_cnt;  // [P * nseg][nr][2]: keys > T, keys == T (then their prefixes)
+  uint32_t nr;          // ranges of a full segment
+};
+
+__device__ __forceinline__ bool long_eligible(const LongArgs& a, uint32_t gs, uint32_t k) {
+  return k > 0 && a.seg_flag[gs] == 0 && a.seg_cnt[gs] >= k;
+}
+
+// The candidates of range r of segment gs: per-sub-chunk prefix in spre,
+// returns their count (0 if the range is empty or the segment is not handled).
+__device__ uint32_t long_range_setup(const LongArgs& a, uint32_t gs, uint32_t r, uint32_t* spre,
+                                     uint32_t* scratch, uint64_t* sub_base) {
+  const Geo& g = a.g;
+  const uint32_t s = gs % g.nseg, p = gs / g.nseg;
+  const uint32_t nsub = seg_chunks(g, s) * kWarpsPerChunk;
+  const uint32_t sa = r * kRangeSubs;
+  if (sa >= nsub || !long_eligible(a, gs, seg_k(g, s))) return 0;  // CTA-uniform
+  const uint32_t nr = min(kRangeSubs, nsub - sa);
+  *sub_base = ((uint64_t)p * g.nchunk + (uint64_t)s * g.m) * kWarpsPerChunk + sa;
+  const uint32_t c = threadIdx.x < nr ? a.sub_cnt[*sub_base + threadIdx.x] : 0u;
+  uint32_t tot;
+  const uint32_t ex = block_excl_scan(c, scratch, &tot);
+  if (threadIdx.x < nr) spre[threadIdx.x] = ex;
+  if (threadIdx.x == 0) spre[nr] = tot;
+  for (uint32_t i = nr + 1 + threadIdx.x; i <= kRangeSubs; i += blockDim.x) spre[i] = tot;
+  __syncthreads();
+  return tot;
+}
+
+__device__ __forceinline__ uint64_t long_slot(const LongArgs& a, const uint32_t* spre,
+                                              uint64_t sub_base, uint32_t v) {
+  uint32_t w = 0;
+#pragma unroll
+  for (uint32_t step = kRangeSubs / 2; step > 0; step >>= 1)
+    if (spre[w + step] <= v) w += step;
+  return (sub_base + w) * a.g.slot + (v - spre[w]);
+}
+
+__global__ void __launch_bounds__(kSelectThreads)
+long_hist_kernel(LongArgs a, int d) {
+  __shared__ uint32_t spre[kRangeSubs + 1];
+  __shared__ uint32_t scratch[34];
+  __shared__ uint32_t hist[2048];
+  const uint32_t gs = blockIdx.x / a.nr, r = blockIdx.x % a.nr;
+  uint64_t sub_base = 0;
+  const uint32_t M = long_range_setup(a, gs, r, spre, scratch, &sub_base);
+  if (M == 0) return;
+  const uint32_t width = d < 2 ? 11 : 9, shift = d == 0 ? 20 : (d == 1 ? 9 : 0);
+  const uint32_t nb = 1u << width, hi_shift = shift + width;
+  const uint32_t prefix = d == 0 ? 0u : a.sel[2 * gs];
+  for (uint32_t b = threadIdx.x; b < nb; b += blockDim.x) hist[b] = 0;
+  __syncthreads();
+  constexpr uint32_t kB = 4;
+  for (uint32_t v0 = 0; v0 < M; v0 += blockDim.x * kB) {
+    float x[kB];
+#pragma unroll
+    for (uint32_t q = 0; q < kB; ++q) {
+      const uint32_t v = v0 + q * blockDim.x + threadIdx.x;
+      x[q] = v < M ? a.cand_val[long_slot(a, spre, sub_base, v)] : 0.0f;
+    }
+#pragma unroll
+    for (uint32_t q = 0; q < kB; ++q) {
+      const uint32_t v = v0 + q * blockDim.x + threadIdx.x;
+      const uint32_t key = mag_key(x[q]);
+      hist_add(hist, (key >> shift) & (nb - 1),
+               v < M && (d == 0 || (key >> hi_shift) == prefix));
+    }
+  }
+  __syncthreads();
+  uint32_t* gh = a.hist + (uint64_t)gs * kHistWords + (d == 0 ? 0 : (d == 1 ? 2048 : 4096));
+  for (uint32_t b = threadIdx.x; b < nb; b += blockDim.x)
+    if (hist[b]) atomicAdd(&gh[b], hist[b]);
+}
+
+__global__ void __launch_bounds__(kSelectThreads)
+long_find_kernel(LongArgs a, int d) {
+  __shared__ uint32_t scratch[34];
+  __shared__ uint32_t res[2];
+  const uint32_t gs = blockIdx.x;
+  const Geo& g = a.g;
+  const uint32_t k = seg_k(g, gs % g.nseg);
+  if (!long_eligible(a, gs, k)) return;
+  const uint32_t width = d < 2 ? 11 : 9, nb = 1u << width;
+  const uint32_t* gh = a.hist + (uint64_t)gs * kHistWords + (d == 0 ? 0 : (d == 1 ? 2048 : 4096));
+  const uint32_t prefix = d == 0 ? 0u : a.sel[2 * gs];
+  const uint32_t rem = d == 0 ? k : a.sel[2 * gs + 1];
+  find_from_top(gh, nb, rem, scratch, res);
+  if (threadIdx.x == 0) {
+    uint32_t b = res[0], above = res[1];
+    if (b == kNone) {  // cannot happen for consistent counts
+      set_status(a.status, SPARCML_ERR_BAD_STREAM);
+      b = 0;
+      above = 0;
+    }
+    a.sel[2 * gs] = (prefix << width) | b;
+    a.sel[2 * gs + 1] = rem - above;
+  }
+}
+
+__global__ void __launch_bounds__(kSelectThreads)
+long_count_kernel(LongArgs a) {
+  __shared__ uint32_t spre[kRangeSubs + 1];
+  __shared__ uint32_t scratch[34];
+  const uint32_t gs = blockIdx.x / a.nr, r = blockIdx.x % a.nr;
+  uint64_t sub_base = 0;
+  const uint32_t M = long_range_setup(a, gs, r, spre, scratch, &sub_base);
+  if (M == 0) {
+    if (threadIdx.x == 0) {
+      a.range_cnt[2 * ((uint64_t)gs * a.nr + r)] = 0;
+      a.range_cnt[2 * ((uint64_t)gs * a.nr + r) + 1] = 0;
+    }
+    return;
+  }
+  const uint32_t T = a.sel[2 * gs];
+  uint32_t n_gt = 0, n_eq = 0;
+  constexpr uint32_t kB = 4;
+  for (uint32_t v0 = 0; v0 < M; v0 += blockDim.x * kB) {
+    float x[kB];
+#pragma unroll
+    for (uint32_t q = 0; q < kB; ++q) {
+      const uint32_t v = v0 + q * blockDim.x + threadIdx.x;
+      x[q] = v < M ? a.cand_val[long_slot(a, spre, sub_base, v)] : 0.0f;
+    }
+#pragma unroll
+    for (uint32_t q = 0; q < kB; ++q) {
+      const uint32_t v = v0 + q * blockDim.x + threadIdx.x;
+      const uint32_t key = mag_key(x[q]);
+      n_gt += (v < M && key > T) ? 1u : 0u;
+      n_eq += (v < M && key == T) ? 1u : 0u;
+    }
+  }
+  uint32_t tg, te;
+  block_excl_scan(n_gt, scratch, &tg);
+  __syncthreads();
+  block_excl_scan(n_eq, scratch, &te);
+  if (threadIdx.x == 0) {
+    a.range_cnt[2 * ((uint64_t)gs * a.nr + r)] = tg;
+    a.range_cnt[2 * ((uint64_t)gs * a.nr + r) + 1] = te;
+  }
+}
+
+__global__ void __launch_bounds__(1024)
+long_scan_kernel(LongArgs a) {
+  __shared__ uint32_t scratch[34];
+  const uint32_t gs = blockIdx.x;
+  const Geo& g = a.g;
+  if (!long_eligible(a, gs, seg_k(g, gs % g.nseg))) return;
+  uint32_t* rc = a.range_cnt + 2 * (uint64_t)gs * a.nr;
+  uint32_t run_gt = 0, run_eq = 0;
+  for (uint32_t r0 = 0; r0 < a.nr; r0 += blockDim.x) {
+    const uint32_t r = r0 + threadIdx.x;
+    const uint32_t cg_ = r < a.nr ? rc[2 * r] : 0u, ce = r < a.nr ? rc[2 * r + 1] : 0u;
+    uint32_t tg, te;
+    const uint32_t eg = block_excl_scan(cg_, scratch, &tg);
+    __syncthreads();
+    const uint32_t ee = block_excl_scan(ce, scratch, &te);
+    if (r < a.nr) {
+      rc[2 * r] = run_gt + eg;
+      rc[2 * r + 1] = run_eq + ee;
+    }
+    run_gt += tg;
+    run_eq += te;
+    __syncthreads();
+  }
+}
+
+__global__ void __launch_bounds__(kSelectThreads)
+long_write_kernel(LongArgs a) {
+  __shared__ uint32_t spre[kRangeSubs + 1];
+  __shared__ uint32_t scratch[34];
+  const uint32_t gs = blockIdx.x / a.nr, r = blockIdx.x % a.nr;
+  uint64_t sub_base = 0;
+  const uint32_t M = long_range_setup(a, gs, r, spre, scratch, &sub_base);
+  if (M == 0) return;
+  const Geo& g = a.g;
+  const uint32_t p = gs / g.nseg, s = gs % g.nseg, k = seg_k(g, s);
+  const uint32_t T = a.sel[2 * gs], tie_take = a.sel[2 * gs + 1];
+  uint32_t run_gt = a.range_cnt[2 * ((uint64_t)gs * a.nr + r)];
+  uint32_t run_eq = a.range_cnt[2 * ((uint64_t)gs * a.nr + r) + 1];
+  float* rp = a.residual + (uint64_t)p * g.N;
+  const uint64_t out0 = (uint64_t)p * g.cap + (uint64_t)s * g.k_full;
+  const uint64_t keep = l2_policy_evict_last();
+  for (uint32_t v0 = 0; v0 < M; v0 += blockDim.x) {
+    const uint32_t v = v0 + threadIdx.x;
+    uint64_t slot = 0;
+    float x = 0.0f;
+    if (v < M) {
+      slot = long_slot(a, spre, sub_base, v);
+      x = a.cand_val[slot];
+    }
+    const uint32_t key = mag_key(x);
+    const bool gt = v < M && key > T, eq = v < M && key == T;
+    uint32_t tot;
+    const uint32_t ex = block_excl_scan((gt ? 1u : 0u) | (eq ? 0x10000u : 0u), scratch, &tot);
+    const uint32_t e_gt = run_gt + (ex & 0xffffu), e_eq = run_eq + (ex >> 16);
+    if (gt || (eq && e_eq < tie_take)) {
+      const uint32_t pos = e_gt + min(e_eq, tie_take);
+      if (pos < k) {
+        const uint32_t i = a.cand_idx[slot];
+        st_keep(a.out_idx + out0 + pos, i, keep);
+        st_keep(a.out_val + out0 + pos, x, keep);
+        rp[i] = 0.0f;
+      } else {
+        set_status(a.status, SPARCML_ERR_BAD_STREAM);
+      }
+    }
+    run_gt += tot & 0xffffu;
+    run_eq += tot >> 16;
+    __syncthreads();
+  }
+}
+
 __global__ void __launch_bounds__(kSelectThreads)
 topk_select_kernel(SelectArgs a) {
   __shared__ SelectShared sh;
@@ -906,7 +1151,9 @@ topk_select_kernel(SelectArgs a) {
 }
 
 struct Layout {
-  size_t todo_cnt, guess, seg_cnt, seg_flag, todo, chunk_cnt, cand_idx, cand_val, total;
+  size_t todo_cnt, guess, seg_cnt, seg_flag, todo, chunk_cnt, cand_idx, cand_val;
+  size_t lhist, lsel, lrange, total;
+  uint32_t nr;  // long-segment ranges of a full segment
 };
 
 bool make_geo(int32_t P, uint64_t N, uint64_t seg_len, uint32_t k_num, uint32_t k_den, Geo* g) {
@@ -948,6 +1195,10 @@ Layout make_layout(const Geo& g) {
   l.chunk_cnt = o; o = align_up(o + 4 * nch, 256);
   l.cand_idx = o; o = align_up(o + 4 * nch * g.slot, 256);
   l.cand_val = o; o = align_up(o + 4 * nch * g.slot, 256);
+  l.nr = (uint32_t)(((uint64_t)g.m * kWarpsPerChunk + kRangeSubs - 1) / kRangeSubs);
+  l.lhist = o; o = align_up(o + 4 * nsegs * kHistWords, 256);
+  l.lsel = o; o = align_up(o + 8 * nsegs, 256);
+  l.lrange = o; o = align_up(o + 8 * nsegs * l.nr, 256);
   l.total = o;
   return l;
 }
@@ -1024,14 +1275,30 @@ extern "C" int sparcml_topk_ef_traced(const float* grad, float* residual, int32_
   // Cluster size: enough CTAs per segment to spread its chunks (<= 8).
   uint32_t CS = 1;
   while (CS < 8 && (uint64_t)g.m / (CS * 2) >= 64) CS *= 2;
-  SelectArgs a{CS, CS == 1 ? 1u : 0u, todo, todo_cnt, residual, seg_cnt, seg_flag, chunk_cnt,
-               guess, cand_idx, cand_val, out_idx, out_val, status, g};
+  SelectArgs a{CS, CS == 1 ? 1u : 0u, CS > 1 ? 1u : 0u, todo, todo_cnt, residual, seg_cnt,
+               seg_flag, chunk_cnt, guess, cand_idx, cand_val, out_idx, out_val, status, g};
   if (CS == 1) {  // layer-sized segments: one warp each
     const size_t smem = (size_t)kShortWarps * kShortWords * sizeof(uint32_t);
     if (!ensure_smem(reinterpret_cast<const void*>(topk_select_short_kernel), smem))
       return SPARCML_ERR_CUDA;
     topk_select_short_kernel<<<(nsegs + kShortWarps - 1) / kShortWarps, kShortWarps * 32, smem,
                                s>>>(a);
+    if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
+  } else {  // long segments: grid-wide passes
+    LongArgs la{g, seg_cnt, seg_flag, chunk_cnt, cand_idx, cand_val, residual, out_idx, out_val,
+                status, reinterpret_cast<uint32_t*>(w + l.lhist),
+                reinterpret_cast<uint32_t*>(w + l.lsel),
+                reinterpret_cast<uint32_t*>(w + l.lrange), l.nr};
+    if (cudaMemsetAsync(la.hist, 0, 4 * (size_t)nsegs * kHistWords, s) != cudaSuccess)
+      return SPARCML_ERR_CUDA;
+    const unsigned ranges = nsegs * l.nr;
+    for (int d = 0; d < 3; ++d) {
+      long_hist_kernel<<<ranges, kSelectThreads, 0, s>>>(la, d);
+      long_find_kernel<<<nsegs, kSelectThreads, 0, s>>>(la, d);
+    }
+    long_count_kernel<<<ranges, kSelectThreads, 0, s>>>(la);
+    long_scan_kernel<<<nsegs, 1024, 0, s>>>(la);
+    long_write_kernel<<<ranges, kSelectThreads, 0, s>>>(la);
     if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   }
   // CS == 1: a small grid walks the segments the short kernel handed over.
@@ -1057,7 +1324,7 @@ extern "C" int sparcml_topk_ef_traced(const float* grad, float* residual, int32_
     return SPARCML_ERR_CUDA;
   }
   mark(3);
-  note_launches(CS == 1 ? 4 : 3);
+  note_launches(CS == 1 ? 4 : 3 + 9);
   return SPARCML_OK;
 }
 
