@@ -45,7 +45,12 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["resnet50", "asr"], default="resnet50")
+    ap.add_argument("--workload", choices=["resnet50", "asr", "sweep", "logreg"], default="resnet50",
+                    help="resnet50/asr: the whole EF step; sweep/logreg: the sparse reduce alone "
+                         "on given streams (density-sweep cell / Zipf logistic regression)")
+    ap.add_argument("--sweep-p", type=int, default=64)
+    ap.add_argument("--sweep-d", type=float, default=10,
+                    help="per-node density in percent: 0.1, 1, 5 or 10")
     ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--nodes", type=int, default=0,
@@ -280,6 +285,76 @@ def run_reference(args, ranks):
 
 
 # ---------------------------------------------------------------------------
+# reduce-only workloads (streams given): density sweep cell, logreg
+# ---------------------------------------------------------------------------
+def run_reduce_only(args, ranks):
+    """Times the sparse sum-reduce with the dense switch alone on seeded
+    streams. value = stream input bytes (8 per entry) per second."""
+    from top_gradient_compression_gb300 import api, workloads as W
+    dev = ranks.device()
+    torch.cuda.set_device(dev)
+    if args.workload == "sweep":
+        P, N, dpct = args.sweep_p, W.SWEEP_N, args.sweep_d
+        cell = [(a, b) for a, b in W.SWEEP_D if abs(100.0 * a / b - dpct) < 1e-9]
+        if not cell:
+            raise SystemExit(f"--sweep-d must be one of {[100.0 * a / b for a, b in W.SWEEP_D]}")
+        idx, val, nnz = W.sweep_streams(P, *cell[0])
+        desc = (f"density-sweep cell: P={P} streams of {int(nnz[0]):,} uniform distinct indices "
+                f"(d={dpct}%) over N={N:,}, N(0,1) values")
+    else:
+        idx, val, nnz = W.logreg_streams()
+        P, N = idx.shape[0], W.LOGREG["N"]
+        desc = (f"logistic-regression gradients: P={P} streams of 40,000 Zipf(1.1) features over "
+                f"N={N:,}, N(0,1e-2) values")
+    di = torch.from_numpy(idx.view(np.int32)).to(dev)
+    dv = torch.from_numpy(val).to(dev)
+    dn = torch.from_numpy(nnz.view(np.int32)).to(dev)
+    ws = api.workspace(api.reduce_workspace_size(P, N), dev)
+    out = api.reduce_out(N, dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)  # 256 MB > L2
+    K, Wm = args.steps, args.warmup
+    evs = [api.make_events(3) for _ in range(K)]
+    for i in range(Wm):
+        api.sparse_reduce(di, dv, dn, N, out=out, ws=ws)
+    torch.cuda.synchronize()
+    launches0 = api.launch_count()
+    tot = 0.0
+    for i in range(K):
+        flush.fill_(float(i))  # inputs do not stay in L2 between timed runs
+        api.sparse_reduce(di, dv, dn, N, out=out, ws=ws, events=evs[i])
+    torch.cuda.synchronize()
+    launches = api.launch_count() - launches0
+    if api.get_status(ws) != 0:
+        raise RuntimeError("device status set after the timed reduces")
+    t_tile = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    t_fix = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
+    ms = ranks.max(t_tile + t_fix)
+    sum_nnz = int(nnz.astype(np.int64).sum())
+    U, dense = int(out.nnz.item()), bool(out.is_dense.item())
+    in_bytes = 8 * sum_nnz
+    out_bytes = 4 * N if dense else 8 * U
+    peak, peak_kind = hbm_peak()
+    achieved = (in_bytes + out_bytes) / (t_tile * 1e-3) / 1e9
+    if ranks.rank != 0:
+        return
+    print(json.dumps({
+        "metric": METRIC, "value": ranks.world * in_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s",
+        "elems_per_s": ranks.world * sum_nnz / (ms * 1e-3), "n_gpus": ranks.world, "steps": K,
+        "warmup": Wm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded numpy index sets)",
+        "config": {"workload": desc, "P": P, "N": N, "sum_nnz": sum_nnz,
+                   "units": "value = 8 B per input entry / (split+tile+fixup time)",
+                   "l2": "256 MB buffer written between timed runs (L2 flushed)"},
+        "roofline": {"bound": "hbm", "kernel": "reduce split + tile",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": peak_kind, "algorithmic_bytes_per_launch": in_bytes + out_bytes,
+                     "traffic": None, "launch_ms": t_tile},
+        "kernels_ms": {"reduce_split_tile": t_tile, "reduce_fixup": t_fix},
+        "reduce": {"U": U, "is_dense": dense},
+        "gpu_launches": launches}), flush=True)
+
+
+# ---------------------------------------------------------------------------
 # our path
 # ---------------------------------------------------------------------------
 def run_ours(args, ranks):
@@ -505,6 +580,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, ranks)
+        elif args.workload in ("sweep", "logreg"):
+            run_reduce_only(args, ranks)
         else:
             run_ours(args, ranks)
     finally:

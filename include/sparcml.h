@@ -176,7 +176,8 @@ int sparcml_dequantize4(const uint8_t* codes, const float* scales, const uint32_
  *              that hold i, in ascending node order (fp32 RN adds).
  * U = number of distinct indices. The result is dense iff
  *     U * dens_den > N * dens_num          (dens_num/dens_den = 1/4: > 25%)
- * Sparse result: out_idx/out_val [0, U) ascending; out_dense untouched.
+ * Sparse result: out_idx/out_val [0, U) ascending; out_dense holds
+ * unspecified values (it may be used as scratch).
  * Dense result: out_dense [N] holds out[i], +0.0f where no node has i;
  * out_idx/out_val hold unspecified values.
  * *out_nnz = U and *out_is_dense = 0/1 in both cases (device scalars).

@@ -214,3 +214,57 @@ def test_reduce_sparse_regime_skewed_tile():
     idx[2] = np.sort(rng.choice(N, cap, replace=False))       # spread out
     r = check_reduce(idx, val, nnz, N, repeat=2)
     assert not r["is_dense"] and r["nnz"] > 8192
+
+
+def test_reduce_dense_regime_sparse_result_is_compacted():
+    """Inputs that cover the index space (P * cap >= N) take the dense-first
+    tiles; when the streams overlap so much that the union stays under 25%, the
+    sparse result is rebuilt from the dense slices. Bit for bit vs the oracle."""
+    rng = np.random.default_rng(21)
+    P, N, k = 24, 200_000, 10_000  # P * k = 1.2 N
+    base = np.sort(rng.choice(N, 12_000, replace=False)).astype(np.uint32)
+    idx = np.zeros((P, k), np.uint32)
+    for p in range(P):
+        idx[p] = np.sort(rng.choice(base, k, replace=False))
+    val = rng.standard_normal((P, k)).astype(np.float32)
+    r = check_reduce(idx, val, np.full(P, k, np.uint32), N, repeat=2)
+    assert not r["is_dense"] and r["nnz"] <= 12_000
+
+
+@pytest.mark.parametrize("P,N,maxk,note", [
+    (64, 100_003, 3_000, "warp-per-1,024-index tiles, 64 nodes, ragged last tile, dense result"),
+    (33, 50_001, 400, "warp-per-1,024-index tiles, nodes 32.., result near the switch"),
+    (5, 700, 200, "one ragged warp tile shorter than 1,024 indices"),
+    (40, 30_000, 1_500, "rounds spanning several nodes, some nodes empty"),
+    (4, 10_000, 1_001, "rows not 16-byte aligned (cap = 1,001): quad split pass with a lead"),
+    (7, 20_001, 1_001, "P * cap not a multiple of 4: scalar split pass"),
+    (80, 100_000, 2_000, "more than 64 nodes covering the index space: staged CTA tiles"),
+    (100, 200_000, 1_000, "more than 64 nodes, union crosses 25% part-way: look-back + fix-up"),
+    (8, 200_000, 4_000, "P * cap between N/16 and N/4: look-back tiles, sparse result"),
+])
+def test_reduce_each_regime_exact(P, N, maxk, note):
+    """Every tiling regime of the reduce, bit for bit against the oracle; node
+    sizes vary from 0 to maxk so tiles see empty and short per-node runs."""
+    rng = np.random.default_rng(P * 1000 + maxk)
+    idx, val, nnz = rand_streams(rng, P, N, maxk)
+    nnz[P // 2] = 0  # an empty node in the middle of the order
+    check_reduce(idx, val, nnz, N, repeat=2)
+
+
+@pytest.mark.parametrize("k", [1100, 1101])  # quad / scalar split pass
+def test_reduce_detects_bad_streams_in_warp_tiles(k):
+    """Streams that cover a quarter of the index space take the warp-per-tile
+    path; a step down, a repeat or an index past N is flagged there too."""
+    N = 4096
+    rng = np.random.default_rng(4)
+    good = np.sort(rng.choice(N - 1, size=k, replace=False)).astype(np.uint32)
+    bad = [good.copy(), good.copy(), good.copy()]
+    bad[0][500], bad[0][501] = bad[0][501], bad[0][500]  # step down inside a tile
+    bad[1][700] = bad[1][699]                              # repeated index
+    bad[2][-1] = N                                         # index past the end
+    for b in bad:
+        idx = np.stack([good, b])
+        di, dv, dn = streams_to_dev(idx, np.ones((2, k), np.float32), np.full(2, k, np.uint32))
+        ws = api.workspace(api.reduce_workspace_size(2, N), DEV)
+        api.sparse_reduce(di, dv, dn, N, ws=ws)
+        assert api.get_status(ws) == api.STATUS_CODE["SPARCML_ERR_BAD_STREAM"]

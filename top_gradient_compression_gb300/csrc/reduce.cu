@@ -30,6 +30,8 @@
 // Every wait on a predecessor is bounded; on expiry the kernel records
 // SPARCML_ERR_TIMEOUT and carries on, so a bad input can never hang the GPU.
 
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace sparcml {
@@ -68,6 +70,8 @@ struct ReduceArgs {
   unsigned long long* tile_state;
   uint2* tile_info;  // (offset, count | dense << 31)
   const uint32_t* split;  // [(ntiles + 1) * P] node sub-range starts per tile
+  uint32_t* tile_bm;      // dense-first mode: [ntiles][kWords] presence bits per tile
+  uint32_t* u_total;      // warp-tile mode: union size, summed by atomics
   int32_t* status;
 };
 
@@ -347,6 +351,598 @@ reduce_tile_kernel(ReduceArgs a) {
   }
 }
 
+// Dense regime: tiles of kTile indices with a dense fp32 shared accumulator.
+// The tile's entries are taken node by node in work items of at most
+// kStageEntries, copied global -> shared with cp.async through a kStages-deep
+// ring, so the next items' loads are in flight while this one is added. A
+// barrier after each item keeps ascending node order (and frees its stage).
+// DENSE_FIRST (chosen when P * cap >= N, so the result is almost surely
+// dense): the tile writes its dense slice and its count straight away, with
+// no look-back; reduce_finalize_kernel and reduce_compact_kernel produce U,
+// the dense flag and, if the result is sparse after all, the sparse output.
+constexpr uint32_t kStages = 4;
+constexpr uint32_t kStageEntries = 1024;
+constexpr uint32_t kNoPrev = 0xffffffffu;
+
+template <bool Q4, bool DENSE_FIRST>
+__global__ void __launch_bounds__(kReduceThreads)
+reduce_dense_tile_kernel(ReduceArgs a) {
+  extern __shared__ __align__(16) uint32_t dyn[];
+  float* acc = reinterpret_cast<float*>(dyn);                       // [kTile]
+  uint32_t* bm = dyn + kTile;                                        // [kWords]
+  uint32_t* sidx = bm + kWords;                                      // [kStages][kStageEntries]
+  float* sval = reinterpret_cast<float*>(sidx + kStages * kStageEntries);
+  uint32_t* lo = reinterpret_cast<uint32_t*>(sval + kStages * kStageEntries);  // [P]
+  uint32_t* hi = lo + a.P;                                           // [P]
+  uint32_t* ipre = hi + a.P;                                         // [P + 1] items per node, prefix
+  __shared__ uint32_t sprev[kStages];
+  __shared__ uint32_t scratch[34];
+  __shared__ uint32_t bc[4];
+  const uint32_t t = threadIdx.x;
+
+  if (t == 0) {
+    bc[0] = atomicAdd(a.ticket, 1u);
+    bc[1] = 0;
+  }
+  for (uint32_t w = t; w < kTile / 4; w += blockDim.x)
+    reinterpret_cast<float4*>(acc)[w] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (uint32_t w = t; w < kWords; w += blockDim.x) bm[w] = 0;
+  __syncthreads();
+  const uint32_t tile = bc[0];
+  const uint32_t tile_lo = tile * kTile;
+  const uint32_t tile_n = min(kTile, a.N - tile_lo);
+  const bool last = tile == a.ntiles - 1;
+  for (int32_t p = t; p < a.P; p += blockDim.x) {
+    uint32_t n = a.nnz[p];
+    if (n > a.cap) {
+      set_status(a.status, SPARCML_ERR_CAPACITY);
+      n = (uint32_t)a.cap;
+    }
+    const uint32_t l = a.split[(uint64_t)tile * a.P + p];
+    uint32_t h = a.split[(uint64_t)(tile + 1) * a.P + p];
+    if (last && h < n) set_status(a.status, SPARCML_ERR_BAD_STREAM);  // idx >= N
+    if (h < l) {
+      set_status(a.status, SPARCML_ERR_BAD_STREAM);
+      h = l;
+    }
+    lo[p] = l;
+    hi[p] = h;
+    ipre[p] = (h - l + kStageEntries - 1) / kStageEntries;
+    atomicMax(&bc[1], n);
+  }
+  __syncthreads();
+  uint32_t n_items = 0;
+  for (int32_t base = 0; base < a.P; base += blockDim.x) {
+    const int32_t p = base + (int32_t)t;
+    const uint32_t c = p < a.P ? ipre[p] : 0u;
+    uint32_t tot;
+    const uint32_t ex = block_excl_scan(c, scratch, &tot);
+    if (p < a.P) ipre[p] = n_items + ex;
+    n_items += tot;
+    __syncthreads();
+  }
+  if (t == 0) ipre[a.P] = n_items;
+  __syncthreads();
+  const bool dense_certain = bc[1] > a.cap_sparse;
+
+  // work item i -> node p and entries [j0, j1) of that node's stream
+  auto item = [&](uint32_t i, uint32_t* p, uint32_t* j0, uint32_t* j1) {
+    uint32_t l = 0, h = (uint32_t)a.P;  // ipre[l] <= i < ipre[h]
+    while (h - l > 1) {
+      const uint32_t m = (l + h) >> 1;
+      if (ipre[m] <= i) l = m; else h = m;
+    }
+    *p = l;
+    *j0 = lo[l] + (i - ipre[l]) * kStageEntries;
+    *j1 = min(*j0 + kStageEntries, hi[l]);
+  };
+  auto issue = [&](uint32_t i) {
+    if (i < n_items) {
+      uint32_t p, j0, j1;
+      item(i, &p, &j0, &j1);
+      const uint32_t st = i % kStages;
+      const uint32_t* ip = a.idx + (uint64_t)p * a.cap;
+      for (uint32_t j = j0 + t; j < j1; j += blockDim.x) {
+        cp_async4(sidx + st * kStageEntries + (j - j0), ip + j);
+        if constexpr (!Q4) cp_async4(sval + st * kStageEntries + (j - j0), a.val + (uint64_t)p * a.cap + j);
+      }
+      if (t == 0) {
+        if (j0 > 0) cp_async4(&sprev[st], ip + j0 - 1);
+        else sprev[st] = kNoPrev;
+      }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  for (uint32_t i = 0; i + 1 < kStages; ++i) issue(i);
+  for (uint32_t i = 0; i < n_items; ++i) {
+    issue(i + kStages - 1);  // refills the stage item i - 1 used
+    asm volatile("cp.async.wait_group %0;" ::"n"(kStages - 1) : "memory");
+    __syncthreads();
+    uint32_t p, j0, j1;
+    item(i, &p, &j0, &j1);
+    const uint32_t st = i % kStages;
+    const uint32_t* si = sidx + st * kStageEntries;
+    for (uint32_t j = j0 + t; j < j1; j += blockDim.x) {
+      const uint32_t e = j - j0;
+      const uint32_t iv = si[e];
+      const uint32_t prev = e > 0 ? si[e - 1] : sprev[st];
+      const uint32_t off = iv - tile_lo;
+      if ((j == 0 || (prev != kNoPrev && prev < iv)) && off < tile_n) {
+        float v;
+        if constexpr (Q4) v = load_value<Q4>(a, p, j);
+        else v = sval[st * kStageEntries + e];
+        acc[off] = __fadd_rn(acc[off], v);
+        atomicOr(&bm[off >> 5], 1u << (off & 31));
+      } else {
+        set_status(a.status, SPARCML_ERR_BAD_STREAM);
+      }
+    }
+    __syncthreads();  // ascending node order; the stage may be refilled
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+
+  uint32_t c = 0;
+  for (uint32_t w = t; w < kWords; w += blockDim.x) c += __popc(bm[w]);
+  uint32_t count;
+  block_excl_scan(c, scratch, &count);
+  if constexpr (DENSE_FIRST) {
+    float* od = a.out_dense + tile_lo;
+    const bool vec = (reinterpret_cast<uintptr_t>(od) & 15) == 0;
+    const uint32_t nv = vec ? tile_n / 4 : 0;
+    for (uint32_t w = t; w < nv; w += blockDim.x)
+      reinterpret_cast<float4*>(od)[w] = reinterpret_cast<const float4*>(acc)[w];
+    for (uint32_t x = nv * 4 + t; x < tile_n; x += blockDim.x) od[x] = acc[x];
+    uint32_t* tb = a.tile_bm + (uint64_t)tile * kWords;
+    for (uint32_t w = t; w < kWords; w += blockDim.x) tb[w] = bm[w];
+    if (t == 0) a.tile_info[tile] = make_uint2(0, count);
+    (void)dense_certain;
+    return;
+  }
+  tile_lookback(a, tile, count, &bc[2]);
+  __syncthreads();
+  const uint32_t excl = bc[2];
+  const uint32_t incl = excl + count;
+  const bool dense = dense_certain || incl > a.cap_sparse;
+  if (dense) {
+    float* od = a.out_dense + tile_lo;
+    const bool vec = (reinterpret_cast<uintptr_t>(od) & 15) == 0;
+    const uint32_t nv = vec ? tile_n / 4 : 0;
+    for (uint32_t w = t; w < nv; w += blockDim.x)
+      reinterpret_cast<float4*>(od)[w] = reinterpret_cast<const float4*>(acc)[w];
+    for (uint32_t x = nv * 4 + t; x < tile_n; x += blockDim.x) od[x] = acc[x];
+  } else {
+    const uint32_t word = t < kWords ? bm[t] : 0u;
+    uint32_t tot;
+    uint32_t pos = excl + block_excl_scan(__popc(word), scratch, &tot);
+    uint32_t bits = word;
+    while (bits) {
+      const uint32_t b = __ffs(bits) - 1;
+      bits &= bits - 1;
+      const uint32_t off = t * 32 + b;
+      a.out_idx[pos] = tile_lo + off;
+      a.out_val[pos] = acc[off];
+      ++pos;
+    }
+  }
+  if (t == 0) {
+    a.tile_info[tile] = make_uint2(excl, count | (dense ? 0x80000000u : 0u));
+    if (last) {
+      *a.out_nnz = incl;
+      *a.out_is_dense = dense ? 1 : 0;
+    }
+  }
+}
+
+// Heavy coverage (P <= kMiniMaxP, P * cap >= N / 4): one warp per mini-tile
+// of kMini indices, no block barrier and no shared-memory staging. The
+// warp's entries of the mini-tile are numbered in ascending node order
+// ("positions"); lane l takes positions l, l + 32, ... so one round of 32
+// positions covers one node, or a few at node changes. A round loads its
+// indices and values straight into registers (kMiniRounds rounds in
+// flight), then adds them into the warp's shared accumulator; rounds, and the
+// nodes within a round, are applied in order, so every index is summed in
+// ascending node order. The streams were validated by the split pass; here
+// every access is only kept in bounds. Output: the dense slice, the presence
+// bitmap and the union size (reduce_mini_compact_kernel finishes).
+constexpr uint32_t kMini = 1024;
+constexpr uint32_t kMiniShift = 10;
+constexpr uint32_t kMiniWords = kMini / 32;
+constexpr uint32_t kMiniRounds = 8;
+constexpr int32_t kMiniMaxP = 64;
+constexpr uint32_t kMiniWarps = 4;  // mini-tiles per CTA
+// per-warp region, a multiple of 16 bytes: acc is accessed as uint4
+constexpr uint32_t kMiniWarpWords = (kMini + 2 * kMiniMaxP + 1 + 31) / 32 * 32;
+static_assert(kMiniWarpWords % 4 == 0, "uint4 access to each warp's accumulator");
+constexpr uint32_t kAbsent = 0xffffffffu;
+
+// Split table of the warp tiles by one streaming pass over every node's
+// indices (grid: x over entries, y = node): entry j of node p is the first of
+// node p at or past every tile boundary between its predecessor's and its own
+// (boundary t is t * kMini, and N for t = ntiles); the closing run (entry
+// nnz, boundaries past the last index) is written by warp 0 of CTA x = 0.
+// Validates the streams on the way: strictly ascending, every index < N.
+__device__ __forceinline__ uint32_t mini_tiles_at_or_below(uint32_t v, uint32_t N, uint32_t ntiles) {
+  return v >= N ? ntiles + 1 : (v >> kMiniShift) + 1;
+}
+
+// Write split[t][p] = j for t in [t0, t1): short runs by the lane itself,
+// long ones (sparse nodes) by the whole warp. Called by all 32 lanes.
+__device__ __forceinline__ void split_fill(uint32_t* split, int32_t P, uint32_t p, uint32_t t0,
+                                           uint32_t t1, uint32_t j) {
+  const bool wide = t1 - t0 > 4;
+  if (!wide)
+    for (uint32_t t = t0; t < t1; ++t) split[(uint64_t)t * P + p] = j;
+  uint32_t todo = __ballot_sync(0xffffffffu, wide);
+  while (todo) {
+    const uint32_t src = __ffs(todo) - 1;
+    todo &= todo - 1;
+    const uint32_t a0 = __shfl_sync(0xffffffffu, t0, src);
+    const uint32_t a1 = __shfl_sync(0xffffffffu, t1, src);
+    const uint32_t jj = __shfl_sync(0xffffffffu, j, src);
+    for (uint32_t t = a0 + lane_id(); t < a1; t += 32) split[(uint64_t)t * P + p] = jj;
+  }
+}
+
+__device__ __forceinline__ void split_close(const uint32_t* row, uint32_t n, int32_t P, uint32_t p,
+                                            uint32_t N, uint32_t ntiles, uint32_t* split) {
+  if (blockIdx.x != 0 || threadIdx.x >= 32) return;  // warp-uniform
+  const uint32_t t0 = n > 0 ? mini_tiles_at_or_below(row[n - 1], N, ntiles) : 0u;
+  for (uint32_t t = t0 + lane_id(); t <= ntiles; t += 32) split[(uint64_t)t * P + p] = n;
+}
+
+constexpr uint32_t kSplitBatch = 8;  // scalar pass: entries per thread, loaded together
+constexpr uint32_t kSplitQuads = 4;  // vector pass: 16-byte quads per thread
+
+// Scalar pass: any alignment.
+__global__ void __launch_bounds__(256)
+reduce_split_stream_kernel(const uint32_t* __restrict__ idx, const uint32_t* __restrict__ nnz,
+                           int32_t P, uint64_t cap, uint32_t N, uint32_t ntiles,
+                           uint32_t* __restrict__ split, int32_t* status) {
+  const uint32_t p = blockIdx.y, lane = lane_id();
+  uint32_t n = nnz[p];
+  if (n > cap) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) set_status(status, SPARCML_ERR_CAPACITY);
+    n = (uint32_t)cap;
+  }
+  const uint32_t* row = idx + (uint64_t)p * cap;
+  split_close(row, n, P, p, N, ntiles, split);
+  const uint64_t span = (uint64_t)blockDim.x * kSplitBatch;
+  bool bad = false;
+  for (uint64_t j0 = (uint64_t)blockIdx.x * span; j0 < n; j0 += (uint64_t)gridDim.x * span) {
+    // batch u covers entries j0 + u * blockDim + threadIdx.x: coalesced per u
+    uint32_t cur[kSplitBatch], before[kSplitBatch];
+#pragma unroll
+    for (uint32_t u = 0; u < kSplitBatch; ++u) {
+      const uint64_t j = j0 + (uint64_t)u * blockDim.x + threadIdx.x;
+      cur[u] = j < n ? ld_stream(row + j) : 0u;
+      before[u] = (lane == 0 && j > 0 && j < n) ? row[j - 1] : 0u;
+    }
+#pragma unroll
+    for (uint32_t u = 0; u < kSplitBatch; ++u) {
+      const uint64_t j = j0 + (uint64_t)u * blockDim.x + threadIdx.x;
+      uint32_t prev = __shfl_up_sync(0xffffffffu, cur[u], 1);
+      if (lane == 0) prev = before[u];
+      const bool entry = j < n, head = j == 0;
+      bad |= entry && (cur[u] >= N || (!head && cur[u] <= prev));
+      // no boundary between prev and cur: the common case, nothing to write
+      const bool inner =
+          !entry || (!head && cur[u] < N && (cur[u] >> kMiniShift) == (prev >> kMiniShift));
+      if (__all_sync(0xffffffffu, inner)) continue;
+      uint32_t t0 = 0, t1 = 0;
+      if (!inner) {
+        t0 = head ? 0u : mini_tiles_at_or_below(prev, N, ntiles);
+        t1 = max(t0, mini_tiles_at_or_below(cur[u], N, ntiles));  // a step down writes nothing
+      }
+      split_fill(split, P, p, t0, t1, (uint32_t)j);
+    }
+  }
+  if (bad) set_status(status, SPARCML_ERR_BAD_STREAM);
+}
+
+// Vector pass: idx 16-byte aligned and P * cap a multiple of 4, so every
+// 16-byte quad that overlaps a row lies inside the buffer. Quad k of node p
+// holds entries j = 4k - lead .. 4k - lead + 3 (lead = (p * cap) mod 4); a
+// quad whose four entries are valid and stay in one tile needs four compares.
+__global__ void __launch_bounds__(256)
+reduce_split_quad_kernel(const uint32_t* __restrict__ idx, const uint32_t* __restrict__ nnz,
+                         int32_t P, uint64_t cap, uint32_t N, uint32_t ntiles,
+                         uint32_t* __restrict__ split, int32_t* status) {
+  const uint32_t p = blockIdx.y, lane = lane_id();
+  uint32_t n = nnz[p];
+  if (n > cap) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) set_status(status, SPARCML_ERR_CAPACITY);
+    n = (uint32_t)cap;
+  }
+  const uint64_t e0 = (uint64_t)p * cap;
+  const uint32_t lead = (uint32_t)(e0 & 3u);
+  const uint32_t* row = idx + e0;
+  const uint4* quads = reinterpret_cast<const uint4*>(idx + (e0 - lead));
+  const uint64_t nq = ((uint64_t)lead + n + 3) / 4;
+  split_close(row, n, P, p, N, ntiles, split);
+  const uint64_t span = (uint64_t)blockDim.x * kSplitQuads;
+  bool bad = false;
+  for (uint64_t k0 = (uint64_t)blockIdx.x * span; k0 < nq; k0 += (uint64_t)gridDim.x * span) {
+    uint4 v[kSplitQuads];
+    uint32_t before[kSplitQuads];
+#pragma unroll
+    for (uint32_t u = 0; u < kSplitQuads; ++u) {
+      const uint64_t k = k0 + (uint64_t)u * blockDim.x + threadIdx.x;
+      v[u] = k < nq ? ld_stream(quads + k) : make_uint4(0, 0, 0, 0);
+      // entry before the quad: idx[e0 - lead + 4k - 1], inside the buffer when 4k > lead
+      before[u] = (lane == 0 && k < nq && 4 * k > lead) ? idx[e0 - lead + 4 * k - 1] : 0u;
+    }
+#pragma unroll
+    for (uint32_t u = 0; u < kSplitQuads; ++u) {
+      const uint64_t k = k0 + (uint64_t)u * blockDim.x + threadIdx.x;
+      uint32_t prev = __shfl_up_sync(0xffffffffu, v[u].w, 1);
+      if (lane == 0) prev = before[u];
+      const uint4 q = v[u];
+      const uint64_t jq = 4 * k;  // j + lead of the quad's first entry
+      const bool live = k < nq;
+      const bool full = live && jq >= (uint64_t)lead + 1 && jq + 4 <= (uint64_t)lead + n;
+      const uint32_t jf = (uint32_t)(jq - lead);
+      // A full quad of a valid stream crosses the boundaries t * kMini for t
+      // in [t0, t1), all in (prev, q.w]; the first entry at or past one is
+      // found by three compares. A bad quad writes nothing (flagged).
+      uint32_t t0 = 0, t1 = 0;
+      if (full) {
+        const bool ok = prev < q.x && q.x < q.y && q.y < q.z && q.z < q.w && q.w < N;
+        bad |= !ok;
+        if (ok) {
+          t0 = (prev >> kMiniShift) + 1;
+          t1 = (q.w >> kMiniShift) + 1;
+        }
+      }
+      const bool wide = t1 - t0 > 4;
+      if (!wide) {
+        for (uint32_t t = t0; t < t1; ++t) {
+          const uint32_t b = t << kMiniShift;
+          split[(uint64_t)t * P + p] = jf + (q.x < b) + (q.y < b) + (q.z < b);
+        }
+      }
+      uint32_t todo = __ballot_sync(0xffffffffu, wide);
+      while (todo) {
+        const uint32_t src = __ffs(todo) - 1;
+        todo &= todo - 1;
+        const uint32_t a0 = __shfl_sync(0xffffffffu, t0, src);
+        const uint32_t a1 = __shfl_sync(0xffffffffu, t1, src);
+        const uint32_t sj = __shfl_sync(0xffffffffu, jf, src);
+        const uint32_t sx = __shfl_sync(0xffffffffu, q.x, src);
+        const uint32_t sy = __shfl_sync(0xffffffffu, q.y, src);
+        const uint32_t sz = __shfl_sync(0xffffffffu, q.z, src);
+        for (uint32_t t = a0 + lane; t < a1; t += 32) {
+          const uint32_t b = t << kMiniShift;
+          split[(uint64_t)t * P + p] = sj + (sx < b) + (sy < b) + (sz < b);
+        }
+      }
+      // quads cut by the row's ends: entry by entry
+      const bool part = live && !full;
+      if (!__any_sync(0xffffffffu, part)) continue;
+      const uint32_t e[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (uint32_t i = 0; i < 4; ++i) {
+        const uint64_t jj = jq + i;  // j + lead
+        const bool ent = part && jj >= lead && jj < (uint64_t)lead + n;
+        const uint32_t j = (uint32_t)(jj - lead);
+        const uint32_t pv = i == 0 ? prev : e[i - 1];
+        uint32_t s0 = 0, s1 = 0;
+        if (ent) {
+          bad |= e[i] >= N || (j > 0 && e[i] <= pv);
+          s0 = j > 0 ? mini_tiles_at_or_below(pv, N, ntiles) : 0u;
+          s1 = max(s0, mini_tiles_at_or_below(e[i], N, ntiles));
+        }
+        split_fill(split, P, p, s0, s1, j);
+      }
+    }
+  }
+  if (bad) set_status(status, SPARCML_ERR_BAD_STREAM);
+}
+
+template <bool Q4>
+__global__ void __launch_bounds__(kMiniWarps * 32)
+reduce_mini_kernel(ReduceArgs a) {
+  extern __shared__ __align__(16) uint32_t dyn[];
+  const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+  const uint32_t m = blockIdx.x * kMiniWarps + warp;  // mini-tile
+  if (m >= a.ntiles) return;                          // warp-uniform
+  uint32_t* acc = dyn + warp * kMiniWarpWords;        // [kMini] float bits
+  uint32_t* lo = acc + kMini;                          // [P] first entry in the tile
+  uint32_t* cpre = lo + kMiniMaxP;                     // [P + 1] first position
+  const uint32_t tile_lo = m * kMini;
+  const uint32_t tile_n = min(kMini, a.N - tile_lo);
+  // Absent indices hold kAbsent, a NaN that fp32 arithmetic never returns
+  // (the GPU's NaN results are 0x7fffffff): presence needs no bitmap.
+#pragma unroll
+  for (uint32_t i = 0; i < kMini / 128; ++i)
+    reinterpret_cast<uint4*>(acc)[i * 32 + lane] = make_uint4(kAbsent, kAbsent, kAbsent, kAbsent);
+  uint32_t c[2] = {0, 0};
+#pragma unroll
+  for (uint32_t q = 0; q < 2; ++q) {
+    const int32_t p = (int32_t)(lane + 32 * q);
+    if (p < a.P) {
+      const uint32_t n = (uint32_t)min((uint64_t)a.nnz[p], a.cap);
+      const uint32_t l = min(a.split[(uint64_t)m * a.P + p], n);
+      const uint32_t h = min(a.split[(uint64_t)(m + 1) * a.P + p], n);
+      lo[p] = l;
+      c[q] = h > l ? h - l : 0u;
+    }
+  }
+  {
+    const uint32_t i0 = warp_incl_sum(c[0]), t0 = __shfl_sync(0xffffffffu, i0, 31);
+    const uint32_t i1 = warp_incl_sum(c[1]);
+    if (lane < (uint32_t)a.P) cpre[lane] = i0 - c[0];
+    if (lane + 32 < (uint32_t)a.P) cpre[lane + 32] = t0 + i1 - c[1];
+    if (lane == 31) cpre[a.P] = t0 + i1;
+  }
+  __syncwarp();
+  const uint32_t total = cpre[a.P];
+  // Each lane walks its positions x = lane, lane + 32, ...: it finds its node
+  // again only when x leaves the current node's range, and otherwise steps its
+  // entry pointers by 32.
+  uint32_t x = lane, p = 0, pend = 0, j = 0;
+  const uint32_t* ip = a.idx;
+  const float* vp = a.val;
+  for (uint32_t r0 = 0; r0 < total; r0 += 32 * kMiniRounds) {
+    uint32_t ix[kMiniRounds], pn[kMiniRounds];
+    float vx[kMiniRounds];
+#pragma unroll
+    for (uint32_t u = 0; u < kMiniRounds; ++u) {
+      pn[u] = kMiniMaxP;  // no entry
+      ix[u] = 0;
+      vx[u] = 0.0f;
+      if (x < total) {
+        if (x >= pend) {
+          while (cpre[p + 1] <= x) ++p;
+          pend = cpre[p + 1];
+          j = lo[p] + (x - cpre[p]);
+          ip = a.idx + (uint64_t)p * a.cap + j;
+          if constexpr (!Q4) vp = a.val + (uint64_t)p * a.cap + j;
+        }
+        pn[u] = p;
+        ix[u] = ld_stream(ip);
+        if constexpr (Q4) vx[u] = load_value<Q4>(a, p, j);
+        else vx[u] = ld_stream(vp);
+      }
+      x += 32;
+      j += 32;
+      ip += 32;
+      if constexpr (!Q4) vp += 32;
+    }
+#pragma unroll
+    for (uint32_t u = 0; u < kMiniRounds; ++u) {
+      // live lanes are a prefix: lane 0 is live in every non-empty round
+      const uint32_t first = __shfl_sync(0xffffffffu, pn[u], 0);
+      if (first == kMiniMaxP) break;  // warp-uniform: later rounds are empty too
+      const bool live = pn[u] != kMiniMaxP;
+      const uint32_t off = ix[u] - tile_lo;
+      const bool mine = live && off < tile_n;
+      if (__all_sync(0xffffffffu, pn[u] == first || !live)) {  // one node: distinct indices
+        if (mine) {
+          const uint32_t old = acc[off];
+          acc[off] = __float_as_uint(__fadd_rn(old == kAbsent ? 0.0f : __uint_as_float(old), vx[u]));
+        }
+      } else {
+        const uint32_t last = __reduce_max_sync(0xffffffffu, live ? pn[u] : 0u);
+        for (uint32_t q = first; q <= last; ++q) {  // node changes: one node at a time
+          if (mine && pn[u] == q) {
+            const uint32_t old = acc[off];
+            acc[off] =
+                __float_as_uint(__fadd_rn(old == kAbsent ? 0.0f : __uint_as_float(old), vx[u]));
+          }
+          __syncwarp();
+        }
+      }
+      __syncwarp();
+    }
+  }
+  // presence bitmap: word i covers indices 32i..32i+31 and ends up in lane i
+  uint32_t word = 0;
+#pragma unroll 8
+  for (uint32_t i = 0; i < kMiniWords; ++i) {
+    const uint32_t b = __ballot_sync(0xffffffffu, acc[i * 32 + lane] != kAbsent);
+    if (lane == i) word = b;
+  }
+  const uint32_t count = warp_sum(__popc(word));
+  float* od = a.out_dense + tile_lo;
+  auto fix = [](uint32_t b) { return b == kAbsent ? 0.0f : __uint_as_float(b); };
+  if (tile_n == kMini && (reinterpret_cast<uintptr_t>(od) & 15) == 0) {
+#pragma unroll
+    for (uint32_t i = 0; i < kMini / 128; ++i) {
+      const uint4 q = reinterpret_cast<const uint4*>(acc)[i * 32 + lane];
+      reinterpret_cast<float4*>(od)[i * 32 + lane] = make_float4(fix(q.x), fix(q.y), fix(q.z), fix(q.w));
+    }
+  } else {
+    for (uint32_t x = lane; x < tile_n; x += 32) od[x] = fix(acc[x]);
+  }
+  a.tile_bm[(uint64_t)m * kMiniWords + lane] = word;
+  if (lane == 0 && count) atomicAdd(a.u_total, count);
+}
+
+// Warp-tile mode, last pass: the union size U decides dense or sparse; a
+// sparse result is compacted from the dense slices and bitmaps, groups of 8
+// warp tiles per CTA taking their offsets by decoupled look-back.
+__global__ void __launch_bounds__(kReduceThreads)
+reduce_mini_compact_kernel(ReduceArgs a) {
+  __shared__ uint32_t scratch[34];
+  __shared__ uint32_t bc[3];
+  const uint32_t U = *a.u_total;
+  const bool dense = U > a.cap_sparse;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    *a.out_nnz = U;
+    *a.out_is_dense = dense ? 1 : 0;
+  }
+  if (dense) return;
+  if (threadIdx.x == 0) bc[0] = atomicAdd(a.ticket, 1u);
+  __syncthreads();
+  const uint32_t g = bc[0];  // group of kReduceThreads bitmap words
+  const uint64_t wi = (uint64_t)g * kReduceThreads + threadIdx.x;
+  const uint64_t nwords = (uint64_t)a.ntiles * kMiniWords;
+  const uint32_t word = wi < nwords ? a.tile_bm[wi] : 0u;
+  uint32_t tot;
+  const uint32_t ex = block_excl_scan(__popc(word), scratch, &tot);
+  tile_lookback(a, g, tot, &bc[2]);
+  __syncthreads();
+  uint32_t pos = bc[2] + ex;
+  uint32_t bits = word;
+  while (bits) {
+    const uint32_t b = __ffs(bits) - 1;
+    bits &= bits - 1;
+    const uint32_t i = (uint32_t)(wi * 32 + b);
+    if (pos < a.cap_sparse) {
+      a.out_idx[pos] = i;
+      a.out_val[pos] = a.out_dense[i];
+    }
+    ++pos;
+  }
+}
+
+// Dense-first mode: U = sum of the tiles' counts, the dense flag, and each
+// tile's exclusive offset (one CTA).
+__global__ void __launch_bounds__(1024)
+reduce_finalize_kernel(uint2* __restrict__ tile_info, uint32_t ntiles, uint32_t cap_sparse,
+                       uint32_t* __restrict__ out_nnz, int32_t* __restrict__ out_is_dense) {
+  __shared__ uint32_t scratch[34];
+  uint32_t run = 0;
+  for (uint32_t t0 = 0; t0 < ntiles; t0 += blockDim.x) {
+    const uint32_t i = t0 + threadIdx.x;
+    const uint32_t c = i < ntiles ? tile_info[i].y : 0u;
+    uint32_t tot;
+    const uint32_t ex = block_excl_scan(c, scratch, &tot);
+    if (i < ntiles) tile_info[i].x = run + ex;
+    run += tot;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    *out_nnz = run;
+    *out_is_dense = run > cap_sparse ? 1 : 0;
+  }
+}
+
+// Dense-first mode, sparse result after all: the tile's present entries,
+// ascending, from its dense slice and saved bitmap (words_per_tile <= blockDim).
+__global__ void __launch_bounds__(kReduceThreads)
+reduce_compact_kernel(const int32_t* __restrict__ is_dense, const uint2* __restrict__ tile_info,
+                      const uint32_t* __restrict__ tile_bm, const float* __restrict__ out_dense,
+                      uint32_t* __restrict__ out_idx, float* __restrict__ out_val,
+                      uint32_t words_per_tile) {
+  __shared__ uint32_t scratch[34];
+  if (*is_dense) return;
+  const uint32_t tile = blockIdx.x, tile_lo = tile * words_per_tile * 32;
+  const uint32_t word = threadIdx.x < words_per_tile
+                            ? tile_bm[(uint64_t)tile * words_per_tile + threadIdx.x] : 0u;
+  uint32_t tot;
+  uint32_t pos = tile_info[tile].x + block_excl_scan(__popc(word), scratch, &tot);
+  uint32_t bits = word;
+  while (bits) {
+    const uint32_t b = __ffs(bits) - 1;
+    bits &= bits - 1;
+    const uint32_t i = tile_lo + threadIdx.x * 32 + b;
+    out_idx[pos] = i;
+    out_val[pos] = out_dense[i];
+    ++pos;
+  }
+}
+
 // Sparse regime: tiles of a.tile_w indices (up to kMaxTileW), chosen so a
 // tile holds about two thousand entries. Shared memory scales with the
 // tile's union, not its width: a presence bitmap is built first, its prefix
@@ -573,17 +1169,20 @@ reduce_fixup_kernel(const int32_t* __restrict__ is_dense, const uint2* __restric
 }
 
 struct ReduceLayout {
-  size_t ticket, state, info, split, total;
+  size_t ticket, state, info, split, bm, total;
 };
 
 ReduceLayout reduce_layout(int32_t P, uint64_t N) {
-  const size_t ntiles = (N + kTile - 1) / kTile;
+  // sized for the finest tiling any regime uses (kMini-index tiles)
+  const size_t ntiles = (N + kMini - 1) / kMini;
   ReduceLayout l;
   l.ticket = 64;
   l.state = 256;
   l.info = align_up(l.state + 8 * ntiles, 256);
   l.split = align_up(l.info + 8 * ntiles, 256);
-  l.total = align_up(l.split + 4 * (ntiles + 1) * (size_t)P, 256);
+  l.bm = align_up(l.split + 4 * (ntiles + 1) * (size_t)P, 256);
+  const size_t bm_words = std::max((N + kTile - 1) / kTile * (size_t)kWords, ntiles * 32);
+  l.total = align_up(l.bm + 4 * bm_words, 256);
   return l;
 }
 
@@ -602,6 +1201,8 @@ int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
   a.tile_info = reinterpret_cast<uint2*>(w + l.info);
   uint32_t* split = reinterpret_cast<uint32_t*>(w + l.split);
   a.split = split;
+  a.tile_bm = reinterpret_cast<uint32_t*>(w + l.bm);
+  a.u_total = reinterpret_cast<uint32_t*>(w + 128);  // cleared with the ticket below
   // Clear the ticket and the look-back states (the status word is kept).
   if (cudaMemsetAsync(w + l.ticket, 0, l.info - l.ticket, s) != cudaSuccess)
     return SPARCML_ERR_CUDA;
@@ -614,9 +1215,39 @@ int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
     while (tile_w < kMaxTileW && est * (2.0 * tile_w / kTile) <= 2048.0 && tile_w < a.N)
       tile_w *= 2;
   }
+  // Heavy coverage with few nodes: warp-per-mini-tile, dense-first.
+  const bool mini =
+      tile_w == kTile && a.P <= kMiniMaxP && 4.0 * (double)a.P * (double)a.cap >= (double)a.N;
+  if (mini) tile_w = kMini;
   a.tile_w = tile_w;
   a.ntiles = (uint32_t)((a.N + tile_w - 1) / tile_w);
   mark(0);
+  if (mini) {
+    // split table by one streaming pass (also validates the streams)
+    const bool quads = (reinterpret_cast<uintptr_t>(a.idx) & 15) == 0 && ((uint64_t)a.P * a.cap) % 4 == 0;
+    const uint64_t per_block = quads ? 256 * 4 * kSplitQuads : 256 * kSplitBatch;
+    const uint32_t gx = (uint32_t)std::max<uint64_t>(
+        1, std::min<uint64_t>((a.cap + per_block - 1) / per_block, 2432 / (uint64_t)a.P));
+    if (quads)
+      reduce_split_quad_kernel<<<dim3(gx, (unsigned)a.P), 256, 0, s>>>(
+          a.idx, a.nnz, a.P, a.cap, a.N, a.ntiles, split, a.status);
+    else
+      reduce_split_stream_kernel<<<dim3(gx, (unsigned)a.P), 256, 0, s>>>(
+          a.idx, a.nnz, a.P, a.cap, a.N, a.ntiles, split, a.status);
+    if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
+    const size_t smem = (size_t)kMiniWarps * kMiniWarpWords * sizeof(uint32_t);
+    if (!ensure_smem(reinterpret_cast<const void*>(reduce_mini_kernel<Q4>), smem))
+      return SPARCML_ERR_CUDA;
+    reduce_mini_kernel<Q4><<<(a.ntiles + kMiniWarps - 1) / kMiniWarps, kMiniWarps * 32, smem, s>>>(a);
+    if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
+    mark(1);
+    const uint64_t groups = ((uint64_t)a.ntiles * kMiniWords + kReduceThreads - 1) / kReduceThreads;
+    reduce_mini_compact_kernel<<<(unsigned)groups, kReduceThreads, 0, s>>>(a);
+    if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
+    mark(2);
+    note_launches(3);
+    return SPARCML_OK;
+  }
   const uint64_t nsplit = (uint64_t)(a.ntiles + 1) * a.P;  // one warp each
   reduce_split_kernel<<<(unsigned)((nsplit * 32 + 255) / 256), 256, 0, s>>>(
       a.idx, a.nnz, a.P, a.cap, a.N, a.ntiles, a.tile_w, split);
@@ -628,10 +1259,27 @@ int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
       return SPARCML_ERR_CUDA;
     reduce_sparse_tile_kernel<Q4><<<a.ntiles, kReduceThreads, smem, s>>>(a);
   } else {
-    const size_t smem = (kTile + kWords + 2 * (size_t)a.P + 1) * sizeof(uint32_t);
-    if (!ensure_smem(reinterpret_cast<const void*>(reduce_tile_kernel<Q4, true>), smem))
+    const size_t smem = (kTile + kWords + 2 * kStages * kStageEntries + 3 * (size_t)a.P + 1) *
+                        sizeof(uint32_t);
+    if ((double)a.P * (double)a.cap >= (double)a.N) {
+      // dense-first: no look-back; U and the flag come from the finalize pass
+      if (!ensure_smem(reinterpret_cast<const void*>(reduce_dense_tile_kernel<Q4, true>), smem))
+        return SPARCML_ERR_CUDA;
+      reduce_dense_tile_kernel<Q4, true><<<a.ntiles, kReduceThreads, smem, s>>>(a);
+      if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
+      mark(1);
+      reduce_finalize_kernel<<<1, 1024, 0, s>>>(a.tile_info, a.ntiles, a.cap_sparse, a.out_nnz,
+                                               a.out_is_dense);
+      reduce_compact_kernel<<<a.ntiles, kReduceThreads, 0, s>>>(
+          a.out_is_dense, a.tile_info, a.tile_bm, a.out_dense, a.out_idx, a.out_val, kWords);
+      if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
+      mark(2);
+      note_launches(4);
+      return SPARCML_OK;
+    }
+    if (!ensure_smem(reinterpret_cast<const void*>(reduce_dense_tile_kernel<Q4, false>), smem))
       return SPARCML_ERR_CUDA;
-    reduce_tile_kernel<Q4, true><<<a.ntiles, kReduceThreads, smem, s>>>(a);
+    reduce_dense_tile_kernel<Q4, false><<<a.ntiles, kReduceThreads, smem, s>>>(a);
   }
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   mark(1);
