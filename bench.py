@@ -94,6 +94,12 @@ class Ranks:
             dist.destroy_process_group()
 
 
+def job_rate(world: int, units_per_rank: float, seconds: float) -> float:
+    """Whole-job throughput: every rank processes the same units (weak
+    scaling), and the job takes as long as its slowest rank."""
+    return world * units_per_rank / seconds
+
+
 def reduce_max(x: float, pg: bool, device) -> float:
     """Max of a float over all ranks (identity without a process group)."""
     if not pg:
@@ -338,8 +344,8 @@ def run_reduce_only(args, ranks):
     if ranks.rank != 0:
         return
     print(json.dumps({
-        "metric": METRIC, "value": ranks.world * in_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s",
-        "elems_per_s": ranks.world * sum_nnz / (ms * 1e-3), "n_gpus": ranks.world, "steps": K,
+        "metric": METRIC, "value": job_rate(ranks.world, in_bytes, ms * 1e-3) / 1e9, "unit": "GB/s",
+        "elems_per_s": job_rate(ranks.world, sum_nnz, ms * 1e-3), "n_gpus": ranks.world, "steps": K,
         "warmup": Wm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded numpy index sets)",
         "config": {"workload": desc, "P": P, "N": N, "sum_nnz": sum_nnz,
@@ -448,7 +454,7 @@ def run_ours(args, ranks):
     is_dense = bool(rd_out.is_dense.item())
     sum_nnz = int(tk_out[2].sum().item())
     in_bytes_step = P * N * 4
-    value = ranks.world * in_bytes_step / (ms * 1e-3) / 1e9
+    value = job_rate(ranks.world, in_bytes_step, ms * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
     stream_bytes = 12 * P * N  # read grad + residual, write residual
     achieved = stream_bytes / (kern["topk_stream"] * 1e-3) / 1e9
@@ -524,7 +530,7 @@ def run_ours(args, ranks):
             d2h += read_result()
         torch.cuda.synchronize()
         dt = ranks.max(time.perf_counter() - t0)
-        e2e = {"value": ranks.world * in_bytes_step * E / dt / 1e9, "unit": "GB/s",
+        e2e = {"value": job_rate(ranks.world, in_bytes_step * E, dt) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": in_bytes_step, "d2h_bytes_per_step": d2h // E,
                "ms_per_step": dt / E * 1e3, "steps": E,
                "note": "next step's host->device copy overlaps this step's kernels"}
@@ -546,7 +552,7 @@ def run_ours(args, ranks):
         return
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s",
-        "elems_per_s": ranks.world * P * N / (ms * 1e-3),
+        "elems_per_s": job_rate(ranks.world, P * N, ms * 1e-3),
         "n_gpus": ranks.world, "steps": K, "warmup": Wm, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": spec["data"],
