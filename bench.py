@@ -395,7 +395,7 @@ def run_ours(args, ranks):
     K, Wm = args.steps, args.warmup
     ev_tk = [api.make_events(4) for _ in range(K)]
     ev_rd = [api.make_events(3) for _ in range(K)]
-    ev_q = [api.make_events(2) for _ in range(K)] if spec["quant"] else None
+    ev_q = [api.make_events(3) for _ in range(K)] if spec["quant"] else None
 
     def step(i, grad, timed=False):
         api.topk_ef(grad, res, L, kn, kd, out=tk_out, ws=tk_ws,
@@ -409,6 +409,8 @@ def run_ours(args, ranks):
                 ev_q[i][1].record()
             api.sparse_reduce_q4(tk_out[0], codes, scales, tk_out[2], bucket, N, out=rd_out,
                                  ws=rd_ws)
+            if timed:
+                ev_q[i][2].record()
         else:
             api.sparse_reduce(tk_out[0], tk_out[1], tk_out[2], N, out=rd_out, ws=rd_ws,
                               events=ev_rd[i] if timed else None)
@@ -446,6 +448,7 @@ def run_ours(args, ranks):
             "topk_select": mean_ms(ev_tk, 2, 3)}
     if spec["quant"]:
         kern["quantize4"] = mean_ms(ev_q, 0, 1)
+        kern["reduce_q4"] = mean_ms(ev_q, 1, 2)
     else:
         kern["reduce_split_tile"] = mean_ms(ev_rd, 0, 1)
         kern["reduce_fixup"] = mean_ms(ev_rd, 1, 2)

@@ -178,9 +178,10 @@ def test_quantize_dequantize_parity():
             assert np.array_equal(bits(gd[p, :n]), bits(od[p, :n]))
 
 
-@pytest.mark.parametrize("k,dense", [(5_000, False), (20_000, True)])
-def test_reduce_q4_equals_dequantize_then_reduce(k, dense):
-    P, N, bucket = 6, 300_000, 512
+@pytest.mark.parametrize("k,dense,bucket", [(1_000, False, 512), (5_000, False, 96),
+                                             (20_000, True, 512), (30_000, True, 6)])
+def test_reduce_q4_equals_dequantize_then_reduce(k, dense, bucket):
+    P, N = 6, 300_000
     idx, val, nnz = W.uniform_streams(P, N, k, 31, std=1e-3)
     nnz[2] = k // 2 + 345
     seed = W.quant_seed(0)
@@ -240,7 +241,10 @@ def test_reduce_dense_regime_sparse_result_is_compacted():
     (7, 20_001, 1_001, "P * cap not a multiple of 4: scalar split pass"),
     (80, 100_000, 2_000, "more than 64 nodes covering the index space: staged CTA tiles"),
     (100, 200_000, 1_000, "more than 64 nodes, union crosses 25% part-way: look-back + fix-up"),
-    (8, 200_000, 4_000, "P * cap between N/16 and N/4: look-back tiles, sparse result"),
+    (8, 200_000, 4_000, "P * cap between N/16 and N/2: sparse-first warp tiles, look-back"),
+    (16, 100_000, 2_800, "sparse-first warp tiles, union crosses 25% part-way: fix-up"),
+    (200, 1_000_000, 500, "more than 64 nodes, P * cap below N/4: compact-accumulator tiles"),
+    (1100, 100_000, 60, "more than 1,024 nodes: staged CTA tiles with look-back"),
 ])
 def test_reduce_each_regime_exact(P, N, maxk, note):
     """Every tiling regime of the reduce, bit for bit against the oracle; node
@@ -268,3 +272,29 @@ def test_reduce_detects_bad_streams_in_warp_tiles(k):
         ws = api.workspace(api.reduce_workspace_size(2, N), DEV)
         api.sparse_reduce(di, dv, dn, N, ws=ws)
         assert api.get_status(ws) == api.STATUS_CODE["SPARCML_ERR_BAD_STREAM"]
+
+
+@pytest.mark.parametrize("P,N,k", [(6, 30_000, 2_000), (64, 65_536, 3_001)])
+def test_reduce_warp_tiles_with_unaligned_buffers(P, N, k):
+    """Warp tiles read 16-byte quads only from 16-byte aligned buffers; stream
+    buffers that start 4 bytes off a 16-byte boundary take the entry-by-entry
+    loads. Same bits as the oracle either way."""
+    idx, val, nnz = W.uniform_streams(P, N, k, 40 + P)
+    ref = oracle.sparse_reduce(idx, val, nnz, N)
+    flat_i = torch.zeros(P * k + 1, dtype=torch.int32, device=DEV)
+    flat_v = torch.zeros(P * k + 1, dtype=torch.float32, device=DEV)
+    flat_i[1:] = torch.from_numpy(idx.view(np.int32).reshape(-1)).to(DEV)
+    flat_v[1:] = torch.from_numpy(val.reshape(-1)).to(DEV)
+    di, dv = flat_i[1:].view(P, k), flat_v[1:].view(P, k)
+    assert di.data_ptr() % 16 == 4 and dv.data_ptr() % 16 == 4
+    dn = torch.from_numpy(nnz.view(np.int32)).to(DEV)
+    ws = api.workspace(api.reduce_workspace_size(P, N), DEV)
+    out = api.sparse_reduce(di, dv, dn, N, ws=ws)
+    assert api.get_status(ws) == 0
+    U = int(out.nnz.item())
+    assert U == ref["nnz"] and bool(out.is_dense.item()) == ref["is_dense"]
+    if ref["is_dense"]:
+        assert np.array_equal(bits(out.dense.cpu().numpy()), bits(ref["dense"]))
+    else:
+        assert np.array_equal(u32(out.idx[:U]), ref["idx"])
+        assert np.array_equal(bits(out.val[:U].cpu().numpy()), bits(ref["val"]))

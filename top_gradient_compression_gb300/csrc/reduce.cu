@@ -56,6 +56,7 @@ struct ReduceArgs {
   uint64_t code_stride;
   uint64_t scale_stride;
   uint32_t bucket;
+  uint32_t bucket_shift;  // log2(bucket) when a power of two, else 32
   int32_t P;
   uint32_t N;
   uint32_t ntiles;
@@ -84,6 +85,18 @@ __device__ __forceinline__ uint32_t lower_bound_u32(const uint32_t* a, uint32_t 
   return lo;
 }
 
+// level / 7 for a 4-bit level 1..7: the correctly rounded fp32 quotient (the
+// constant expressions are IEEE divisions, as __fdiv_rn would give), picked by
+// selects on the level's bits rather than an indexed table, which lanes with
+// different levels would serialise on.
+__device__ __forceinline__ float level_over_7(uint32_t level) {
+  const float lo = (level & 2u) ? ((level & 1u) ? 3.0f / 7.0f : 2.0f / 7.0f)
+                                : ((level & 1u) ? 1.0f / 7.0f : 0.0f);
+  const float hi = (level & 2u) ? ((level & 1u) ? 7.0f / 7.0f : 6.0f / 7.0f)
+                                : ((level & 1u) ? 5.0f / 7.0f : 4.0f / 7.0f);
+  return (level & 4u) ? hi : lo;
+}
+
 // Value of entry j of node p: fp32 as stored, or decoded from 4 bits.
 template <bool Q4>
 __device__ __forceinline__ float load_value(const ReduceArgs& a, uint32_t p, uint32_t j) {
@@ -94,8 +107,9 @@ __device__ __forceinline__ float load_value(const ReduceArgs& a, uint32_t p, uin
     const uint32_t code = (j & 1) ? (byte >> 4) : (byte & 15u);
     const uint32_t level = code & 7u;
     if (level == 0) return 0.0f;
-    const float scale = a.scales[(uint64_t)p * a.scale_stride + j / a.bucket];
-    const float v = __fmul_rn(__fdiv_rn((float)level, 7.0f), scale);
+    const uint32_t b = a.bucket_shift < 32 ? j >> a.bucket_shift : j / a.bucket;
+    const float scale = a.scales[(uint64_t)p * a.scale_stride + b];
+    const float v = __fmul_rn(level_over_7(level), scale);
     return (code & 8u) ? -v : v;
   }
 }
@@ -551,7 +565,8 @@ constexpr uint32_t kMiniRounds = 8;
 constexpr int32_t kMiniMaxP = 64;
 constexpr uint32_t kMiniWarps = 4;  // mini-tiles per CTA
 // per-warp region, a multiple of 16 bytes: acc is accessed as uint4
-constexpr uint32_t kMiniWarpWords = (kMini + 2 * kMiniMaxP + 1 + 31) / 32 * 32;
+constexpr uint32_t kAccWords = kMini;
+constexpr uint32_t kMiniWarpWords = (kAccWords + 3 * kMiniMaxP + 1 + 31) / 32 * 32;
 static_assert(kMiniWarpWords % 4 == 0, "uint4 access to each warp's accumulator");
 constexpr uint32_t kAbsent = 0xffffffffu;
 
@@ -657,30 +672,31 @@ reduce_split_quad_kernel(const uint32_t* __restrict__ idx, const uint32_t* __res
   const uint32_t lead = (uint32_t)(e0 & 3u);
   const uint32_t* row = idx + e0;
   const uint4* quads = reinterpret_cast<const uint4*>(idx + (e0 - lead));
-  const uint64_t nq = ((uint64_t)lead + n + 3) / 4;
+  // 32-bit positions: the host sends rows of at most 2^31 entries here
+  const uint32_t nq = (lead + n + 3) / 4;
   split_close(row, n, P, p, N, ntiles, split);
-  const uint64_t span = (uint64_t)blockDim.x * kSplitQuads;
+  const uint32_t span = blockDim.x * kSplitQuads;
   bool bad = false;
-  for (uint64_t k0 = (uint64_t)blockIdx.x * span; k0 < nq; k0 += (uint64_t)gridDim.x * span) {
+  for (uint32_t k0 = blockIdx.x * span; k0 < nq; k0 += gridDim.x * span) {
     uint4 v[kSplitQuads];
     uint32_t before[kSplitQuads];
 #pragma unroll
     for (uint32_t u = 0; u < kSplitQuads; ++u) {
-      const uint64_t k = k0 + (uint64_t)u * blockDim.x + threadIdx.x;
+      const uint32_t k = k0 + u * blockDim.x + threadIdx.x;
       v[u] = k < nq ? ld_stream(quads + k) : make_uint4(0, 0, 0, 0);
-      // entry before the quad: idx[e0 - lead + 4k - 1], inside the buffer when 4k > lead
-      before[u] = (lane == 0 && k < nq && 4 * k > lead) ? idx[e0 - lead + 4 * k - 1] : 0u;
+      // entry before the quad: row[4k - lead - 1], inside the buffer when 4k > lead
+      before[u] = (lane == 0 && k < nq && 4 * k > lead) ? row[4 * k - lead - 1] : 0u;
     }
 #pragma unroll
     for (uint32_t u = 0; u < kSplitQuads; ++u) {
-      const uint64_t k = k0 + (uint64_t)u * blockDim.x + threadIdx.x;
+      const uint32_t k = k0 + u * blockDim.x + threadIdx.x;
       uint32_t prev = __shfl_up_sync(0xffffffffu, v[u].w, 1);
       if (lane == 0) prev = before[u];
       const uint4 q = v[u];
-      const uint64_t jq = 4 * k;  // j + lead of the quad's first entry
+      const uint32_t jq = 4 * k;  // j + lead of the quad's first entry
       const bool live = k < nq;
-      const bool full = live && jq >= (uint64_t)lead + 1 && jq + 4 <= (uint64_t)lead + n;
-      const uint32_t jf = (uint32_t)(jq - lead);
+      const bool full = live && jq > lead && n >= 4 && jq - lead <= n - 4;
+      const uint32_t jf = jq - lead;
       // A full quad of a valid stream crosses the boundaries t * kMini for t
       // in [t0, t1), all in (prev, q.w]; the first entry at or past one is
       // found by three compares. A bad quad writes nothing (flagged).
@@ -721,9 +737,9 @@ reduce_split_quad_kernel(const uint32_t* __restrict__ idx, const uint32_t* __res
       const uint32_t e[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
       for (uint32_t i = 0; i < 4; ++i) {
-        const uint64_t jj = jq + i;  // j + lead
-        const bool ent = part && jj >= lead && jj < (uint64_t)lead + n;
-        const uint32_t j = (uint32_t)(jj - lead);
+        const uint32_t jj = jq + i;  // j + lead
+        const bool ent = part && jj >= lead && jj - lead < n;
+        const uint32_t j = jj - lead;
         const uint32_t pv = i == 0 ? prev : e[i - 1];
         uint32_t s0 = 0, s1 = 0;
         if (ent) {
@@ -738,15 +754,162 @@ reduce_split_quad_kernel(const uint32_t* __restrict__ idx, const uint32_t* __res
   if (bad) set_status(status, SPARCML_ERR_BAD_STREAM);
 }
 
-template <bool Q4>
+// Decoupled look-back for one warp's tile (the calling warp, all 32 lanes):
+// publish the count, sum predecessors back to the nearest inclusive prefix,
+// publish the inclusive prefix, return the exclusive offset. Tiles are
+// claimed in ticket order, so every tile waited on is already running. Each
+// wait is bounded (SPARCML_ERR_TIMEOUT, then it carries on).
+__device__ uint32_t warp_lookback(const ReduceArgs& a, uint32_t tile, uint32_t count) {
+  const uint32_t lane = lane_id();
+  unsigned long long* st = a.tile_state;
+  if (tile == 0) {
+    if (lane == 0) atomicExch(&st[0], kFlagInc | count);
+    return 0;
+  }
+  if (lane == 0) atomicExch(&st[tile], kFlagAgg | count);
+  uint32_t excl = 0;
+  int64_t base = (int64_t)tile - 1;
+  uint32_t spins = 0, backoff = 32;
+  while (true) {
+    const int64_t j = base - (int64_t)lane;
+    const unsigned long long sv =
+        j >= 0 ? *reinterpret_cast<volatile unsigned long long*>(&st[j]) : (2ull << 62);
+    const unsigned long long flag = sv & (3ull << 62);
+    const uint32_t inc = __ballot_sync(0xffffffffu, flag == kFlagInc);
+    const uint32_t notready = __ballot_sync(0xffffffffu, flag == 0);
+    const uint32_t upto = inc ? (uint32_t)(__ffs(inc) - 1) : 31u;  // lanes 0..upto count
+    const uint32_t need = upto == 31 ? 0xffffffffu : ((2u << upto) - 1u);
+    if (notready & need) {
+      if (++spins > kSpinLimit) {
+        if (lane == 0) set_status(a.status, SPARCML_ERR_TIMEOUT);
+        break;
+      }
+      __nanosleep(backoff);
+      backoff = min(backoff * 2, 1024u);
+      continue;
+    }
+    excl += warp_sum(lane <= upto ? (uint32_t)sv : 0u);
+    if (inc) break;
+    base -= 32;
+  }
+  if (lane == 0) atomicExch(&st[tile], kFlagInc | (excl + count));
+  return excl;
+}
+
+// Warp tile epilogue, sparse-first: the CTA's kMiniWarps tiles take one
+// offset by look-back (their counts summed), each tile its share in tile
+// order. While the running union stays within cap_sparse a tile emits its
+// present indices ascending (each lane the indices of its bitmap word), past
+// it the dense slice. tile_info records which, for the fix-up pass; the last
+// tile writes U. Called by every warp of the CTA (inactive ones add nothing).
+__device__ __forceinline__ void mini_epilogue_lookback(const ReduceArgs& a, uint32_t m,
+                                                       const uint32_t* acc, bool active,
+                                                       uint32_t* sh /* [kMiniWarps + 1] */) {
+  const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+  uint32_t word = 0;
+  if (active) {
+#pragma unroll 8
+    for (uint32_t i = 0; i < kMiniWords; ++i) {
+      const uint32_t b = __ballot_sync(0xffffffffu, acc[i * 32 + lane] != kAbsent);
+      if (lane == i) word = b;
+    }
+  }
+  const uint32_t wincl = warp_incl_sum(__popc(word));
+  const uint32_t count = __shfl_sync(0xffffffffu, wincl, 31);
+  if (lane == 0) sh[warp] = count;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t total = warp_sum(lane < kMiniWarps ? sh[lane] : 0u);
+    const uint32_t gexcl = warp_lookback(a, m / kMiniWarps, total);
+    __syncwarp();
+    if (lane == 0) sh[kMiniWarps] = gexcl;
+  }
+  __syncthreads();
+  if (!active) return;
+  uint32_t excl = sh[kMiniWarps];
+  for (uint32_t w = 0; w < warp; ++w) excl += sh[w];
+  const uint32_t tile_lo = m * kMini;
+  const uint32_t tile_n = min(kMini, a.N - tile_lo);
+  const uint32_t incl = excl + count;
+  const bool dense = incl > a.cap_sparse;
+  if (dense) {
+    float* od = a.out_dense + tile_lo;
+    for (uint32_t x = lane; x < tile_n; x += 32)
+      od[x] = acc[x] == kAbsent ? 0.0f : __uint_as_float(acc[x]);
+  } else {
+    uint32_t pos = excl + wincl - __popc(word);  // entries before word `lane`
+    uint32_t bits = word;
+    while (bits) {
+      const uint32_t x = lane * 32 + (__ffs(bits) - 1);
+      bits &= bits - 1;
+      a.out_idx[pos] = tile_lo + x;
+      a.out_val[pos] = __uint_as_float(acc[x]);
+      ++pos;
+    }
+  }
+  if (lane == 0) {
+    a.tile_info[m] = make_uint2(excl, count | (dense ? 0x80000000u : 0u));
+    if (m == a.ntiles - 1) {
+      *a.out_nnz = incl;
+      *a.out_is_dense = dense ? 1 : 0;
+    }
+  }
+}
+
+// Warp tile epilogue: presence bitmap (absent = kAbsent), dense slice with
+// absent indices as +0.0f, and the tile's count added to the union size.
+__device__ __forceinline__ void mini_epilogue(const ReduceArgs& a, uint32_t m, const uint32_t* acc) {
+  const uint32_t lane = lane_id();
+  const uint32_t tile_lo = m * kMini;
+  const uint32_t tile_n = min(kMini, a.N - tile_lo);
+  // presence bitmap: word i covers indices 32i..32i+31 and ends up in lane i
+  uint32_t word = 0;
+#pragma unroll 8
+  for (uint32_t i = 0; i < kMiniWords; ++i) {
+    const uint32_t b = __ballot_sync(0xffffffffu, acc[i * 32 + lane] != kAbsent);
+    if (lane == i) word = b;
+  }
+  const uint32_t count = warp_sum(__popc(word));
+  float* od = a.out_dense + tile_lo;
+  auto fix = [](uint32_t b) { return b == kAbsent ? 0.0f : __uint_as_float(b); };
+  if (tile_n == kMini && (reinterpret_cast<uintptr_t>(od) & 15) == 0) {
+#pragma unroll
+    for (uint32_t i = 0; i < kMini / 128; ++i) {
+      const uint4 q = reinterpret_cast<const uint4*>(acc)[i * 32 + lane];
+      reinterpret_cast<float4*>(od)[i * 32 + lane] = make_float4(fix(q.x), fix(q.y), fix(q.z), fix(q.w));
+    }
+  } else {
+    for (uint32_t x = lane; x < tile_n; x += 32) od[x] = fix(acc[x]);
+  }
+  a.tile_bm[(uint64_t)m * kMiniWords + lane] = word;
+  if (lane == 0 && count) atomicAdd(a.u_total, count);
+}
+
+// LB: sparse-first output with look-back, the CTA's group of tiles claimed by
+// ticket (so every group waited on is already running); else dense-first
+// (slice, bitmap and union size; the tile is the warp's grid position).
+__device__ __forceinline__ uint32_t mini_tile_of_warp(const ReduceArgs& a, bool lb, uint32_t* sh) {
+  if (!lb) return blockIdx.x * kMiniWarps + (threadIdx.x >> 5);
+  if (threadIdx.x == 0) sh[0] = atomicAdd(a.ticket, 1u);
+  __syncthreads();
+  const uint32_t m = sh[0] * kMiniWarps + (threadIdx.x >> 5);
+  __syncthreads();  // sh is reused by the epilogue
+  return m;
+}
+
+template <bool Q4, bool LB>
 __global__ void __launch_bounds__(kMiniWarps * 32)
 reduce_mini_kernel(ReduceArgs a) {
   extern __shared__ __align__(16) uint32_t dyn[];
   const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
-  const uint32_t m = blockIdx.x * kMiniWarps + warp;  // mini-tile
-  if (m >= a.ntiles) return;                          // warp-uniform
+  __shared__ uint32_t sh[kMiniWarps + 1];
+  const uint32_t m = mini_tile_of_warp(a, LB, sh);
+  if constexpr (!LB) {
+    if (m >= a.ntiles) return;  // warp-uniform
+  }
+  const bool active = m < a.ntiles;
   uint32_t* acc = dyn + warp * kMiniWarpWords;        // [kMini] float bits
-  uint32_t* lo = acc + kMini;                          // [P] first entry in the tile
+  uint32_t* lo = acc + kAccWords;                      // [P] first entry in the tile
   uint32_t* cpre = lo + kMiniMaxP;                     // [P + 1] first position
   const uint32_t tile_lo = m * kMini;
   const uint32_t tile_n = min(kMini, a.N - tile_lo);
@@ -759,7 +922,7 @@ reduce_mini_kernel(ReduceArgs a) {
 #pragma unroll
   for (uint32_t q = 0; q < 2; ++q) {
     const int32_t p = (int32_t)(lane + 32 * q);
-    if (p < a.P) {
+    if (active && p < a.P) {  // a tile past the end (last CTA group) has no entries
       const uint32_t n = (uint32_t)min((uint64_t)a.nnz[p], a.cap);
       const uint32_t l = min(a.split[(uint64_t)m * a.P + p], n);
       const uint32_t h = min(a.split[(uint64_t)(m + 1) * a.P + p], n);
@@ -835,27 +998,146 @@ reduce_mini_kernel(ReduceArgs a) {
       __syncwarp();
     }
   }
-  // presence bitmap: word i covers indices 32i..32i+31 and ends up in lane i
-  uint32_t word = 0;
-#pragma unroll 8
-  for (uint32_t i = 0; i < kMiniWords; ++i) {
-    const uint32_t b = __ballot_sync(0xffffffffu, acc[i * 32 + lane] != kAbsent);
-    if (lane == i) word = b;
+  if constexpr (LB) mini_epilogue_lookback(a, m, acc, active, sh);
+  else mini_epilogue(a, m, acc);
+}
+
+// Vector form of the warp tile (fp32 values, idx and val 16-byte aligned):
+// each node's entries of the tile are read as the 16-byte quads of the
+// buffer that hold them, so a lane takes 4 entries per round with two
+// 128-bit loads. The first and last quad of a node are masked to the node's
+// range; a quad that would run past the end of the buffer is read entry by
+// entry. A round of 32 quads spans a few nodes: their entries are added one
+// node at a time, in ascending order.
+constexpr uint32_t kQuadRounds = 4;
+
+template <bool LB>
+__global__ void __launch_bounds__(kMiniWarps * 32)
+reduce_mini_quad_kernel(ReduceArgs a) {
+  extern __shared__ __align__(16) uint32_t dyn[];
+  const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+  __shared__ uint32_t sh[kMiniWarps + 1];
+  const uint32_t m = mini_tile_of_warp(a, LB, sh);
+  if constexpr (!LB) {
+    if (m >= a.ntiles) return;  // warp-uniform
   }
-  const uint32_t count = warp_sum(__popc(word));
-  float* od = a.out_dense + tile_lo;
-  auto fix = [](uint32_t b) { return b == kAbsent ? 0.0f : __uint_as_float(b); };
-  if (tile_n == kMini && (reinterpret_cast<uintptr_t>(od) & 15) == 0) {
+  const bool active = m < a.ntiles;
+  uint32_t* acc = dyn + warp * kMiniWarpWords;        // [kMini] float bits
+  uint32_t* lo = acc + kAccWords;                      // [P] first entry in the tile
+  uint32_t* qpre = lo + kMiniMaxP;                     // [P + 1] first quad position
+  uint32_t* hi = qpre + kMiniMaxP + 1;                 // [P] end entry in the tile
+  const uint32_t tile_lo = m * kMini;
+  const uint32_t tile_n = min(kMini, a.N - tile_lo);
 #pragma unroll
-    for (uint32_t i = 0; i < kMini / 128; ++i) {
-      const uint4 q = reinterpret_cast<const uint4*>(acc)[i * 32 + lane];
-      reinterpret_cast<float4*>(od)[i * 32 + lane] = make_float4(fix(q.x), fix(q.y), fix(q.z), fix(q.w));
+  for (uint32_t i = 0; i < kMini / 128; ++i)
+    reinterpret_cast<uint4*>(acc)[i * 32 + lane] = make_uint4(kAbsent, kAbsent, kAbsent, kAbsent);
+  uint32_t c[2] = {0, 0};
+#pragma unroll
+  for (uint32_t q = 0; q < 2; ++q) {
+    const int32_t p = (int32_t)(lane + 32 * q);
+    if (active && p < a.P) {  // a tile past the end (last CTA group) has no entries
+      const uint32_t n = (uint32_t)min((uint64_t)a.nnz[p], a.cap);
+      const uint32_t l = min(a.split[(uint64_t)m * a.P + p], n);
+      const uint32_t h = min(a.split[(uint64_t)(m + 1) * a.P + p], n);
+      lo[p] = l;
+      hi[p] = h;
+      if (h > l) {  // quads of the buffer holding entries [row + l, row + h)
+        const uint64_t row = (uint64_t)p * a.cap;
+        c[q] = (uint32_t)(((row + h + 3) >> 2) - ((row + l) >> 2));
+      }
     }
-  } else {
-    for (uint32_t x = lane; x < tile_n; x += 32) od[x] = fix(acc[x]);
   }
-  a.tile_bm[(uint64_t)m * kMiniWords + lane] = word;
-  if (lane == 0 && count) atomicAdd(a.u_total, count);
+  {
+    const uint32_t i0 = warp_incl_sum(c[0]), t0 = __shfl_sync(0xffffffffu, i0, 31);
+    const uint32_t i1 = warp_incl_sum(c[1]);
+    if (lane < (uint32_t)a.P) qpre[lane] = i0 - c[0];
+    if (lane + 32 < (uint32_t)a.P) qpre[lane + 32] = t0 + i1 - c[1];
+    if (lane == 31) qpre[a.P] = t0 + i1;
+  }
+  __syncwarp();
+  const uint32_t total = qpre[a.P];
+  const uint64_t buf_end = (uint64_t)a.P * a.cap;  // entries in the buffer
+  const uint4* idx4 = reinterpret_cast<const uint4*>(a.idx);
+  const float4* val4 = reinterpret_cast<const float4*>(a.val);
+  // lane state for its current node: quad range and the masks of its ends
+  uint32_t x = lane, p = 0, qend = 0, y = 0, nq = 0, head = 0xfu, tail = 0xfu;
+  uint64_t g = 0;  // buffer quad of position x
+  for (uint32_t r0 = 0; r0 < total; r0 += 32 * kQuadRounds) {
+    uint4 ix[kQuadRounds];
+    float4 vx[kQuadRounds];
+    uint32_t pn[kQuadRounds], mk[kQuadRounds];
+#pragma unroll
+    for (uint32_t u = 0; u < kQuadRounds; ++u) {
+      pn[u] = kMiniMaxP;  // no entry
+      mk[u] = 0;
+      ix[u] = make_uint4(0, 0, 0, 0);
+      vx[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (x < total) {
+        if (x >= qend) {
+          while (qpre[p + 1] <= x) ++p;
+          qend = qpre[p + 1];
+          const uint64_t e0 = (uint64_t)p * a.cap + lo[p], e1 = (uint64_t)p * a.cap + hi[p];
+          nq = qend - qpre[p];
+          y = x - qpre[p];
+          g = (e0 >> 2) + y;
+          head = (0xfu << (uint32_t)(e0 & 3)) & 0xfu;
+          tail = (1u << (uint32_t)(((e1 - 1) & 3) + 1)) - 1u;
+        }
+        uint32_t mask = 0xfu;
+        if (y == 0) mask &= head;
+        if (y == nq - 1) mask &= tail;
+        pn[u] = p;
+        mk[u] = mask;
+        if (4 * g + 4 <= buf_end) {
+          ix[u] = ld_stream(idx4 + g);
+          const uint4 vb = ld_stream(reinterpret_cast<const uint4*>(val4 + g));
+          vx[u] = make_float4(__uint_as_float(vb.x), __uint_as_float(vb.y), __uint_as_float(vb.z),
+                              __uint_as_float(vb.w));
+        } else {  // the buffer's last, partial quad: its valid entries only
+          const uint32_t* ie = a.idx + 4 * g;
+          const float* ve = a.val + 4 * g;
+          if (mask & 1u) { ix[u].x = ie[0]; vx[u].x = ve[0]; }
+          if (mask & 2u) { ix[u].y = ie[1]; vx[u].y = ve[1]; }
+          if (mask & 4u) { ix[u].z = ie[2]; vx[u].z = ve[2]; }
+          if (mask & 8u) { ix[u].w = ie[3]; vx[u].w = ve[3]; }
+        }
+      }
+      x += 32;
+      y += 32;
+      g += 32;
+    }
+    auto add = [&](uint32_t iv, float v) {
+      const uint32_t off = iv - tile_lo;
+      if (off < tile_n) {
+        const uint32_t old = acc[off];
+        acc[off] = __float_as_uint(__fadd_rn(old == kAbsent ? 0.0f : __uint_as_float(old), v));
+      }
+    };
+    auto add_quad = [&](uint32_t u) {
+      if (mk[u] & 1u) add(ix[u].x, vx[u].x);
+      if (mk[u] & 2u) add(ix[u].y, vx[u].y);
+      if (mk[u] & 4u) add(ix[u].z, vx[u].z);
+      if (mk[u] & 8u) add(ix[u].w, vx[u].w);
+    };
+#pragma unroll
+    for (uint32_t u = 0; u < kQuadRounds; ++u) {
+      const uint32_t first = __shfl_sync(0xffffffffu, pn[u], 0);
+      if (first == kMiniMaxP) break;  // warp-uniform: later rounds are empty too
+      const bool live = pn[u] != kMiniMaxP;
+      if (__all_sync(0xffffffffu, pn[u] == first || !live)) {  // one node: distinct indices
+        if (live) add_quad(u);
+      } else {
+        const uint32_t last = __reduce_max_sync(0xffffffffu, live ? pn[u] : 0u);
+        for (uint32_t q = first; q <= last; ++q) {  // one node at a time
+          if (live && pn[u] == q) add_quad(u);
+          __syncwarp();
+        }
+      }
+      __syncwarp();
+    }
+  }
+  if constexpr (LB) mini_epilogue_lookback(a, m, acc, active, sh);
+  else mini_epilogue(a, m, acc);
 }
 
 // Warp-tile mode, last pass: the union size U decides dense or sparse; a
@@ -952,7 +1234,6 @@ reduce_compact_kernel(const int32_t* __restrict__ is_dense, const uint2* __restr
 // the dense-accumulator kernel's. Tiles whose union exceeds kAccCap are
 // accumulated in several slot windows.
 constexpr uint32_t kMaxTileW = 1u << 17;
-constexpr uint32_t kMaxWords = kMaxTileW / 32;
 constexpr uint32_t kAccCap = 8192;
 constexpr int32_t kMaxSparseP = 1024;
 
@@ -1154,19 +1435,25 @@ reduce_sparse_tile_kernel(ReduceArgs a) {
 __global__ void __launch_bounds__(256)
 reduce_fixup_kernel(const int32_t* __restrict__ is_dense, const uint2* __restrict__ tile_info,
                     const uint32_t* __restrict__ out_idx, const float* __restrict__ out_val,
-                    float* __restrict__ out_dense, uint32_t N, uint32_t tile_w) {
+                    float* __restrict__ out_dense, uint32_t N, uint32_t tile_w, uint32_t ntiles) {
   if (*is_dense == 0) return;
-  const uint2 info = tile_info[blockIdx.x];
-  if (info.y & 0x80000000u) return;
-  const uint32_t tile_lo = blockIdx.x * tile_w;
-  const uint32_t tile_n = min(tile_w, N - tile_lo);
-  for (uint32_t x = threadIdx.x; x < tile_n; x += blockDim.x) out_dense[tile_lo + x] = 0.0f;
-  __syncthreads();
-  for (uint32_t e = threadIdx.x; e < info.y; e += blockDim.x) {
-    const uint32_t i = out_idx[info.x + e];
-    if (i - tile_lo < tile_n) out_dense[i] = out_val[info.x + e];
+  for (uint32_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {  // block-uniform
+    const uint2 info = tile_info[tile];
+    if (info.y & 0x80000000u) continue;
+    const uint32_t tile_lo = tile * tile_w;
+    const uint32_t tile_n = min(tile_w, N - tile_lo);
+    for (uint32_t x = threadIdx.x; x < tile_n; x += blockDim.x) out_dense[tile_lo + x] = 0.0f;
+    __syncthreads();
+    for (uint32_t e = threadIdx.x; e < info.y; e += blockDim.x) {
+      const uint32_t i = out_idx[info.x + e];
+      if (i - tile_lo < tile_n) out_dense[i] = out_val[info.x + e];
+    }
+    __syncthreads();
   }
 }
+
+// Blocks of the fix-up pass: each walks tiles; a sparse result exits at once.
+inline unsigned fixup_grid(uint32_t ntiles) { return std::min<uint32_t>(ntiles, 1216u); }
 
 struct ReduceLayout {
   size_t ticket, state, info, split, bm, total;
@@ -1211,20 +1498,21 @@ int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
   // accumulator; denser ones the dense-accumulator tile of kTile indices.
   const double est = (double)a.P * (double)a.cap * kTile / (double)a.N;
   uint32_t tile_w = kTile;
-  if (a.P <= kMaxSparseP && est <= 512.0) {
+  // Few nodes covering at least N/16 indices: one warp per kMini-index tile.
+  const bool mini = a.P <= kMiniMaxP && 16.0 * (double)a.P * (double)a.cap >= (double)a.N;
+  const bool sparse = !mini && a.P <= kMaxSparseP && est <= 2048.0;
+  if (sparse) {
     while (tile_w < kMaxTileW && est * (2.0 * tile_w / kTile) <= 2048.0 && tile_w < a.N)
       tile_w *= 2;
   }
-  // Heavy coverage with few nodes: warp-per-mini-tile, dense-first.
-  const bool mini =
-      tile_w == kTile && a.P <= kMiniMaxP && 4.0 * (double)a.P * (double)a.cap >= (double)a.N;
   if (mini) tile_w = kMini;
   a.tile_w = tile_w;
   a.ntiles = (uint32_t)((a.N + tile_w - 1) / tile_w);
   mark(0);
   if (mini) {
     // split table by one streaming pass (also validates the streams)
-    const bool quads = (reinterpret_cast<uintptr_t>(a.idx) & 15) == 0 && ((uint64_t)a.P * a.cap) % 4 == 0;
+    const bool quads = (reinterpret_cast<uintptr_t>(a.idx) & 15) == 0 &&
+                       ((uint64_t)a.P * a.cap) % 4 == 0 && a.cap <= (1ull << 31);
     const uint64_t per_block = quads ? 256 * 4 * kSplitQuads : 256 * kSplitBatch;
     const uint32_t gx = (uint32_t)std::max<uint64_t>(
         1, std::min<uint64_t>((a.cap + per_block - 1) / per_block, 2432 / (uint64_t)a.P));
@@ -1236,11 +1524,35 @@ int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
           a.idx, a.nnz, a.P, a.cap, a.N, a.ntiles, split, a.status);
     if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
     const size_t smem = (size_t)kMiniWarps * kMiniWarpWords * sizeof(uint32_t);
-    if (!ensure_smem(reinterpret_cast<const void*>(reduce_mini_kernel<Q4>), smem))
-      return SPARCML_ERR_CUDA;
-    reduce_mini_kernel<Q4><<<(a.ntiles + kMiniWarps - 1) / kMiniWarps, kMiniWarps * 32, smem, s>>>(a);
+    const unsigned grid = (a.ntiles + kMiniWarps - 1) / kMiniWarps;
+    const bool vec = !Q4 && (reinterpret_cast<uintptr_t>(a.idx) & 15) == 0 &&
+                     (reinterpret_cast<uintptr_t>(a.val) & 15) == 0;
+    // A possibly dense result (P * cap >= N / 4) is written dense-first; else
+    // sparse-first with look-back and a fix-up if the union crosses after all.
+    const bool lb = 4.0 * (double)a.P * (double)a.cap < (double)a.N;
+    const void* fn;
+    if (vec) fn = lb ? reinterpret_cast<const void*>(reduce_mini_quad_kernel<true>)
+                     : reinterpret_cast<const void*>(reduce_mini_quad_kernel<false>);
+    else fn = lb ? reinterpret_cast<const void*>(reduce_mini_kernel<Q4, true>)
+                 : reinterpret_cast<const void*>(reduce_mini_kernel<Q4, false>);
+    if (!ensure_smem(fn, smem)) return SPARCML_ERR_CUDA;
+    if (vec) {
+      if (lb) reduce_mini_quad_kernel<true><<<grid, kMiniWarps * 32, smem, s>>>(a);
+      else reduce_mini_quad_kernel<false><<<grid, kMiniWarps * 32, smem, s>>>(a);
+    } else {
+      if (lb) reduce_mini_kernel<Q4, true><<<grid, kMiniWarps * 32, smem, s>>>(a);
+      else reduce_mini_kernel<Q4, false><<<grid, kMiniWarps * 32, smem, s>>>(a);
+    }
     if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
     mark(1);
+    if (lb) {
+      reduce_fixup_kernel<<<fixup_grid(a.ntiles), 256, 0, s>>>(a.out_is_dense, a.tile_info, a.out_idx,
+                                                   a.out_val, a.out_dense, a.N, a.tile_w, a.ntiles);
+      if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
+      mark(2);
+      note_launches(3);
+      return SPARCML_OK;
+    }
     const uint64_t groups = ((uint64_t)a.ntiles * kMiniWords + kReduceThreads - 1) / kReduceThreads;
     reduce_mini_compact_kernel<<<(unsigned)groups, kReduceThreads, 0, s>>>(a);
     if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
@@ -1252,7 +1564,7 @@ int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
   reduce_split_kernel<<<(unsigned)((nsplit * 32 + 255) / 256), 256, 0, s>>>(
       a.idx, a.nnz, a.P, a.cap, a.N, a.ntiles, a.tile_w, split);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
-  if (tile_w > kTile) {
+  if (sparse) {
     const size_t smem =
         (2 * (size_t)(tile_w / 32) + kAccCap + 2 * (size_t)a.P + 1) * sizeof(uint32_t);
     if (!ensure_smem(reinterpret_cast<const void*>(reduce_sparse_tile_kernel<Q4>), smem))
@@ -1283,8 +1595,8 @@ int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
   }
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   mark(1);
-  reduce_fixup_kernel<<<a.ntiles, 256, 0, s>>>(a.out_is_dense, a.tile_info, a.out_idx,
-                                               a.out_val, a.out_dense, a.N, a.tile_w);
+  reduce_fixup_kernel<<<fixup_grid(a.ntiles), 256, 0, s>>>(a.out_is_dense, a.tile_info, a.out_idx,
+                                               a.out_val, a.out_dense, a.N, a.tile_w, a.ntiles);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   mark(2);
   note_launches(3);
@@ -1374,6 +1686,7 @@ extern "C" int sparcml_sparse_reduce_q4(const uint32_t* idx, const uint8_t* code
   a.code_stride = (cap + 1) / 2;
   a.scale_stride = (cap + bucket - 1) / bucket;
   a.bucket = bucket;
+  a.bucket_shift = (bucket & (bucket - 1)) == 0 ? (uint32_t)__builtin_ctz(bucket) : 32u;
   a.P = P;
   a.N = (uint32_t)N;
   a.ntiles = (uint32_t)((N + kTile - 1) / kTile);
@@ -1483,8 +1796,8 @@ extern "C" int sparcml_sparse_reduce_noalloc(const uint32_t* idx, const float* v
     return SPARCML_ERR_CUDA;
   reduce_tile_kernel<false><<<a.ntiles, kReduceThreads, smem, s>>>(a);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
-  reduce_fixup_kernel<<<a.ntiles, 256, 0, s>>>(a.out_is_dense, a.tile_info, a.out_idx,
-                                               a.out_val, a.out_dense, a.N, a.tile_w);
+  reduce_fixup_kernel<<<fixup_grid(a.ntiles), 256, 0, s>>>(a.out_is_dense, a.tile_info, a.out_idx,
+                                               a.out_val, a.out_dense, a.N, a.tile_w, a.ntiles);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   note_launches(2);
   return SPARCML_OK;
