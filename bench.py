@@ -341,6 +341,11 @@ def run_reduce_only(args, ranks):
     out_bytes = 4 * N if dense else 8 * U
     peak, peak_kind = hbm_peak()
     achieved = (in_bytes + out_bytes) / (t_tile * 1e-3) / 1e9
+    traffic = None
+    if args.workload == "sweep":  # counters committed for the largest cell only
+        e = load_traffic(f"reduce_sweep_P{P}_d{dpct:g}",
+                         os.path.join(ROOT, "top_gradient_compression_gb300", "csrc", "reduce.cu"))
+        traffic = None if e is None else e["dram_bytes_per_launch"]
     if ranks.rank != 0:
         return
     print(json.dumps({
@@ -354,7 +359,7 @@ def run_reduce_only(args, ranks):
         "roofline": {"bound": "hbm", "kernel": "reduce split + tile",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": peak_kind, "algorithmic_bytes_per_launch": in_bytes + out_bytes,
-                     "traffic": None, "launch_ms": t_tile},
+                     "traffic": traffic, "launch_ms": t_tile},
         "kernels_ms": {"reduce_split_tile": t_tile, "reduce_fixup": t_fix},
         "reduce": {"U": U, "is_dense": dense},
         "gpu_launches": launches}), flush=True)
