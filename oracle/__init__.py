@@ -53,6 +53,11 @@ def _load():
                                              C.c_uint32, C.c_uint64, u8p, f32p]
             lib.oracle_dequantize4.argtypes = [u8p, f32p, u32p, C.c_int32, C.c_uint64,
                                                C.c_uint32, f32p]
+            lib.oracle_quantize.argtypes = [C.c_void_p, f32p, C.c_void_p, C.c_int32, C.c_uint64,
+                                            C.c_uint32, C.c_uint32, C.c_uint64, u8p, f32p,
+                                            C.c_void_p]
+            lib.oracle_dequantize.argtypes = [u8p, f32p, C.c_void_p, C.c_int32, C.c_uint64,
+                                              C.c_uint32, C.c_uint32, f32p]
             lib.oracle_sparse_reduce.argtypes = [u32p, f32p, u32p, C.c_int32, C.c_uint64,
                                                  C.c_uint64, C.c_uint32, C.c_uint32, u32p, f32p,
                                                  C.c_uint64, f32p, C.POINTER(C.c_uint64),
@@ -149,6 +154,42 @@ def dequantize4(codes, scales, nnz, cap, bucket):
     out = np.zeros((P, cap), np.float32)
     _check("oracle_dequantize4", _load().oracle_dequantize4(codes, scales, nnz, P, cap, bucket,
                                                             out))
+    return out
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(C.c_void_p)
+
+
+def quantize(val, bucket, bits, seed, idx=None, nnz=None, with_error=False):
+    """b-bit stochastic quantisation, b in {2, 4, 8} (SparCML §2.2, §6), of
+    stream values (idx, nnz given) or dense rows (idx None: the position is
+    the rounding key; nnz None: full rows). Returns (codes, scales) or, with
+    with_error, (codes, scales, v - dequantised v)."""
+    val = _f32(val)
+    if val.ndim == 1:
+        val = val[None]
+    P, cap = val.shape
+    idx = None if idx is None else _u32(idx)
+    nnz = None if nnz is None else _u32(nnz)
+    per_byte = 8 // bits
+    codes = np.zeros((P, (cap + per_byte - 1) // per_byte), np.uint8)
+    scales = np.zeros((P, (cap + bucket - 1) // bucket), np.float32)
+    err = np.zeros((P, cap), np.float32) if with_error else None
+    _check("oracle_quantize", _load().oracle_quantize(
+        _ptr(idx), val, _ptr(nnz), P, cap, bucket, bits, C.c_uint64(seed & (2**64 - 1)),
+        codes, scales, _ptr(err)))
+    return (codes, scales, err) if with_error else (codes, scales)
+
+
+def dequantize(codes, scales, cap, bucket, bits, nnz=None):
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = _f32(scales)
+    nnz = None if nnz is None else _u32(nnz)
+    P = codes.shape[0]
+    out = np.zeros((P, cap), np.float32)
+    _check("oracle_dequantize", _load().oracle_dequantize(codes, scales, _ptr(nnz), P, cap,
+                                                          bucket, bits, out))
     return out
 
 

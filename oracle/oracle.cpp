@@ -229,6 +229,98 @@ int oracle_dequantize4(const uint8_t* codes, const float* scales, const uint32_t
   return OK;
 }
 
+// b-bit stochastic quantisation (§6: QSGD-style buckets with one fp32 scale,
+// 2-, 4- and 8-bit outputs), of stream values or of dense rows. With
+// s = 2^(b-1) - 1 levels: scale = max |v| over the bucket, r = (|v| / scale)
+// * s in fp32, level = floor(r) rounded up with probability frac(r) (the
+// same SplitMix64 draw as the 4-bit form, keyed by (seed, node, index)), code
+// = (v < 0) << (b-1) | level. 8/b codes per byte, the earliest entry in the
+// lowest bits. Dense rows (idx == nullptr) use the position j as the index;
+// nnz == nullptr means every row holds cap entries. If err_out is given it
+// receives v - dequantised(v) per entry (quantisation-error feedback).
+// codes: [P][ceil(cap / (8/b))], scales: [P][ceil(cap / bucket)].
+int oracle_quantize(const uint32_t* idx, const float* val, const uint32_t* nnz, int32_t P,
+                    uint64_t cap, uint32_t bucket, uint32_t bits, uint64_t seed,
+                    uint8_t* codes, float* scales, float* err_out) {
+  if (P <= 0 || cap == 0 || (bits != 2 && bits != 4 && bits != 8)) return INVALID;
+  const uint32_t per_byte = 8 / bits;
+  if (bucket == 0 || bucket % per_byte != 0) return INVALID;
+  const uint32_t s = (1u << (bits - 1)) - 1;
+  const uint64_t code_stride = (cap + per_byte - 1) / per_byte;
+  const uint64_t scale_stride = (cap + bucket - 1) / bucket;
+  const uint64_t seed_mix = splitmix64(seed);
+  for (int32_t p = 0; p < P; ++p) {
+    const uint64_t n = nnz ? nnz[p] : cap;
+    if (n > cap) return INVALID;
+    const uint64_t node_mix = splitmix64(seed_mix ^ (uint64_t)(uint32_t)p);
+    const float* vp = val + (uint64_t)p * cap;
+    uint8_t* cp = codes + (uint64_t)p * code_stride;
+    for (uint64_t b0 = 0; b0 < n; b0 += bucket) {
+      const uint64_t b1 = std::min<uint64_t>(b0 + bucket, n);
+      float scale = 0.0f;
+      for (uint64_t j = b0; j < b1; ++j) scale = std::max(scale, std::fabs(vp[j]));
+      scales[(uint64_t)p * scale_stride + b0 / bucket] = scale;
+      for (uint64_t j = b0; j < b1; ++j) {
+        const float v = vp[j];
+        const uint64_t index = idx ? idx[(uint64_t)p * cap + j] : j;
+        uint32_t level = 0;
+        if (scale > 0.0f) {
+          const float r = (std::fabs(v) / scale) * (float)s;
+          const float f = std::floor(r);
+          const float frac = r - f;
+          const uint64_t h = splitmix64(node_mix ^ index);
+          const float u = (float)(h >> 40) * (1.0f / 16777216.0f);
+          level = (uint32_t)f + (u < frac ? 1u : 0u);
+          if (level > s) level = s;
+        }
+        const uint32_t sign = v < 0.0f ? 1u : 0u;
+        const uint32_t code = (sign << (bits - 1)) | level;
+        const uint32_t shift = (uint32_t)(j % per_byte) * bits;
+        uint8_t& byte = cp[j / per_byte];
+        const uint32_t mask = ((1u << bits) - 1u) << shift;
+        byte = (uint8_t)((byte & ~mask) | (code << shift));
+        if (err_out) {
+          float q = 0.0f;
+          if (level != 0) {
+            q = ((float)level / (float)s) * scale;
+            if (sign) q = -q;
+          }
+          err_out[(uint64_t)p * cap + j] = v - q;
+        }
+      }
+    }
+  }
+  return OK;
+}
+
+// Inverse of the b-bit code: v = +-(level / s) * scale, level 0 -> +0.0f.
+int oracle_dequantize(const uint8_t* codes, const float* scales, const uint32_t* nnz,
+                      int32_t P, uint64_t cap, uint32_t bucket, uint32_t bits, float* val_out) {
+  if (P <= 0 || cap == 0 || (bits != 2 && bits != 4 && bits != 8)) return INVALID;
+  const uint32_t per_byte = 8 / bits;
+  if (bucket == 0 || bucket % per_byte != 0) return INVALID;
+  const uint32_t s = (1u << (bits - 1)) - 1;
+  const uint64_t code_stride = (cap + per_byte - 1) / per_byte;
+  const uint64_t scale_stride = (cap + bucket - 1) / bucket;
+  for (int32_t p = 0; p < P; ++p) {
+    const uint64_t n = nnz ? nnz[p] : cap;
+    if (n > cap) return INVALID;
+    for (uint64_t j = 0; j < n; ++j) {
+      const uint8_t byte = codes[(uint64_t)p * code_stride + j / per_byte];
+      const uint32_t code = (byte >> ((j % per_byte) * bits)) & ((1u << bits) - 1u);
+      const uint32_t level = code & s;
+      const float scale = scales[(uint64_t)p * scale_stride + j / bucket];
+      float v = 0.0f;
+      if (level != 0) {
+        v = ((float)level / (float)s) * scale;
+        if (code >> (bits - 1)) v = -v;
+      }
+      val_out[(uint64_t)p * cap + j] = v;
+    }
+  }
+  return OK;
+}
+
 // Sum-reduction of P sparse streams (§5.2) with the dense switch (§5.1,
 // §5.3.3). The sum for an index runs over the nodes that hold it, in
 // ascending node order, starting from +0.0f. U = size of the index union.

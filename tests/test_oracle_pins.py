@@ -359,6 +359,121 @@ def test_quantizer_draw_depends_only_on_seed_node_index():
     assert not np.array_equal(unpack(c4, n)[1], l1[0])
 
 
+def unpack_bits(codes, n, bits):
+    """codes [P][ceil(n / (8/b))] -> [P][n], the earliest entry in the lowest bits."""
+    per = 8 // bits
+    out = np.empty(codes.shape[:-1] + (codes.shape[-1] * per,), np.uint8)
+    for k in range(per):
+        out[..., k::per] = (codes >> (k * bits)) & ((1 << bits) - 1)
+    return out[..., :n]
+
+
+def test_general_quantizer_at_4_bits_is_the_4bit_form():
+    rng = np.random.default_rng(21)
+    P, cap = 3, 1300
+    val = (rng.laplace(size=(P, cap)) * 1e-3).astype(np.float32)
+    idx = np.tile(np.arange(cap, dtype=np.uint32) * 5, (P, 1))
+    nnz = np.array([1300, 1025, 7], np.uint32)
+    c4, s4 = oracle.quantize4(idx, val, nnz, 512, seed=3)
+    c, sc = oracle.quantize(val, 512, 4, 3, idx=idx, nnz=nnz)
+    assert np.array_equal(c, c4) and np.array_equal(sc.view(np.uint32), s4.view(np.uint32))
+    d4 = oracle.dequantize4(c4, s4, nnz, cap, 512)
+    d = oracle.dequantize(c, sc, cap, 512, 4, nnz=nnz)
+    assert np.array_equal(d.view(np.uint32), d4.view(np.uint32))
+
+
+@pytest.mark.parametrize("bits", [2, 8])
+def test_b_bit_quantizer_bounds_levels_signs_and_max_entry(bits):
+    """§6, 2- and 8-bit outputs: s = 2^(b-1) - 1 levels of the bucket max."""
+    rng = np.random.default_rng(bits)
+    s_lv = (1 << (bits - 1)) - 1
+    P, cap, bucket = 2, 1000, 256
+    val = rng.standard_normal((P, cap)).astype(np.float32)
+    idx = np.tile(np.arange(cap, dtype=np.uint32) * 2, (P, 1))
+    nnz = np.array([1000, 513], np.uint32)
+    codes, scales = oracle.quantize(val, bucket, bits, 77, idx=idx, nnz=nnz)
+    deq = oracle.dequantize(codes, scales, cap, bucket, bits, nnz=nnz)
+    cl = unpack_bits(codes, cap, bits)
+    for p in range(P):
+        n = int(nnz[p])
+        for b0 in range(0, n, bucket):
+            b1 = min(b0 + bucket, n)
+            v = val[p, b0:b1]
+            s = scales[p, b0 // bucket]
+            assert s == np.abs(v).max()
+            lv = cl[p, b0:b1] & s_lv
+            assert np.array_equal(cl[p, b0:b1] >> (bits - 1), (v < 0).astype(np.uint8))
+            for j in range(len(v)):
+                r = Fraction(float(abs(v[j]))) / Fraction(float(s)) * s_lv
+                assert math.floor(r - Fraction(1, 10**5)) <= lv[j] <= math.ceil(r + Fraction(1, 10**5))
+            assert np.all(np.abs(deq[p, b0:b1].astype(np.float64) - v) <= s / s_lv * (1 + 1e-6))
+            m = int(np.argmax(np.abs(v)))
+            assert deq[p, b0 + m] == v[m]  # level s: the bucket maximum is exact
+
+
+@pytest.mark.parametrize("bits,r", [(2, 0.3), (8, 40.75)])
+def test_b_bit_quantizer_rounds_up_with_probability_frac(bits, r):
+    s_lv = (1 << (bits - 1)) - 1
+    n = 40000
+    val = np.full((1, n), r, np.float32)
+    val[0, 0] = float(s_lv)  # scale s => r = |v| exactly
+    codes, _ = oracle.quantize(val, n, bits, 13)  # dense row: the position is the key
+    lv = unpack_bits(codes, n, bits)[0, 1:] & s_lv
+    f = r - math.floor(r)
+    assert set(np.unique(lv).tolist()) <= {math.floor(r), math.floor(r) + 1}
+    assert abs(np.mean(lv == math.floor(r) + 1) - f) <= 6 * math.sqrt(f * (1 - f) / (n - 1))
+
+
+@pytest.mark.parametrize("bits", [2, 8])
+def test_b_bit_quantizer_is_unbiased_over_seeds(bits):
+    """§2.2: zero-mean quantisation noise at every width."""
+    rng = np.random.default_rng(5)
+    s_lv = (1 << (bits - 1)) - 1
+    n, M = 64, 2000
+    val = rng.standard_normal((1, n)).astype(np.float32)
+    acc = np.zeros(n)
+    for k in range(M):
+        c, sc = oracle.quantize(val, n, bits, k * 104729 + 3)
+        acc += oracle.dequantize(c, sc, n, n, bits)[0]
+    sd = np.abs(val).max() / s_lv / 2
+    assert np.all(np.abs(acc / M - val[0]) <= 6 * sd / math.sqrt(M) + 1e-7)
+
+
+def test_dense_rows_quantise_like_a_stream_of_every_position():
+    """A dense row is the stream idx = 0..n-1 of all its entries."""
+    rng = np.random.default_rng(8)
+    P, n = 3, 3000
+    val = rng.standard_normal((P, n)).astype(np.float32)
+    for bits in (2, 4, 8):
+        cd, sd = oracle.quantize(val, 1024, bits, 99)
+        cs, ss = oracle.quantize(val, 1024, bits, 99,
+                                 idx=np.tile(np.arange(n, dtype=np.uint32), (P, 1)),
+                                 nnz=np.full(P, n, np.uint32))
+        assert np.array_equal(cd, cs) and np.array_equal(sd, ss)
+
+
+def test_quantisation_error_output_completes_the_value():
+    """Error feedback option: dequantised value + error gives the value back
+    up to the one rounding of v - q, and the error is bounded by one level."""
+    rng = np.random.default_rng(9)
+    val = rng.standard_normal((2, 700)).astype(np.float32)
+    for bits in (2, 4, 8):
+        s_lv = (1 << (bits - 1)) - 1
+        c, sc, err = oracle.quantize(val, 128, bits, 4, with_error=True)
+        deq = oracle.dequantize(c, sc, 700, 128, bits)
+        back = deq.astype(np.float64) + err.astype(np.float64)
+        ulp = np.spacing(np.maximum(np.abs(val), np.abs(deq))).astype(np.float64)
+        assert np.all(np.abs(back - val) <= ulp / 2)  # one rounding of v - q
+        bmax = np.repeat(sc, 128, axis=1)[:, :700]
+        assert np.all(np.abs(err) <= bmax / s_lv * (1 + 1e-6))
+
+
+def test_quantizer_rejects_bucket_not_whole_bytes():
+    val = np.ones((1, 8), np.float32)
+    with pytest.raises(RuntimeError):
+        oracle.quantize(val, 6, 2, 1)  # 2-bit codes pack 4 per byte
+
+
 # --------------------------------------------------------------------------
 # Pack and densify (§5.1).
 # --------------------------------------------------------------------------
