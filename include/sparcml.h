@@ -167,6 +167,40 @@ int sparcml_dequantize4(const uint8_t* codes, const float* scales, const uint32_
                         int32_t* status, void* stream);
 
 /* ------------------------------------------------------------------------
+ * b-bit stochastic quantisation, b in {2, 4, 8} (§6: QSGD with 2-, 4- and
+ * 8-bit outputs; §2.2 zero-mean noise), of stream values or of dense rows
+ * (for example the dense reduced result, quantised before it is shared as
+ * in the second half of DSAR, §6). The 4-bit form of sparcml_quantize4
+ * with s = 2^(b-1) - 1 levels (1, 7, 127):
+ *     r     = (|v| / scale) * s            (fp32, RN, no contraction)
+ *     level = floor(r) + (u < r - floor(r)),  clamped to s;  0 if scale == 0
+ *     code  = (v < 0) << (b-1) | level,  8/b codes per byte, the earliest
+ *             entry of the byte in its lowest bits
+ * with u and the SplitMix64 key as in sparcml_quantize4.
+ *   idx      [P][cap] stream indices, or NULL for dense rows: the rounding
+ *            key of entry j is then j itself.
+ *   val      [P][cap] values.
+ *   nnz      [P] entries per row, or NULL: every row holds cap entries.
+ *   bucket   entries per bucket, >= 1, a multiple of 8/b.
+ *   codes    [P][ceil(cap / (8/b))] bytes; scales [P][ceil(cap/bucket)].
+ *   err_out  [P][cap] or NULL: receives v - dequantised(v) (one fp32 RN
+ *            subtraction) per entry, for quantisation-error feedback.
+ *   status   as for sparcml_quantize4.
+ * SPARCML_ERR_INVALID_ARG for another b or a bucket that splits a byte.
+ * ------------------------------------------------------------------------ */
+int sparcml_quantize(const uint32_t* idx, const float* val, const uint32_t* nnz, int32_t P,
+                     uint64_t cap, uint32_t bucket, uint32_t bits, uint64_t seed,
+                     uint8_t* codes, float* scales, float* err_out, int32_t* status,
+                     void* stream);
+
+/* Inverse map of sparcml_quantize: val_out[p][j] = +-(level / s) * scale,
+ * level / s rounded to fp32 first, level 0 giving +0.0f. nnz may be NULL
+ * (full rows). Entries past nnz[p] untouched. */
+int sparcml_dequantize(const uint8_t* codes, const float* scales, const uint32_t* nnz,
+                       int32_t P, uint64_t cap, uint32_t bucket, uint32_t bits, float* val_out,
+                       int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------
  * Sparse sum-reduction of P streams with the adaptive dense switch
  * (§5.2 sum with neutral element 0; §5.1 / §5.3.3 switch to dense; the
  * result size U is the size of the index union, App. B).
@@ -212,6 +246,17 @@ int sparcml_sparse_reduce_traced(const uint32_t* idx, const float* val, const ui
 int sparcml_sparse_reduce_q4(const uint32_t* idx, const uint8_t* codes, const float* scales,
                              const uint32_t* nnz, int32_t P, uint64_t cap, uint32_t bucket,
                              uint64_t N, uint32_t dens_num, uint32_t dens_den,
+                             uint32_t* out_idx, float* out_val, uint64_t out_cap,
+                             float* out_dense, uint32_t* out_nnz, int32_t* out_is_dense,
+                             void* ws, size_t ws_bytes, void* stream);
+
+/* Same reduction with values in the b-bit form of sparcml_quantize (b in
+ * {2, 4, 8}; codes, scales, bucket as there), decoded on load exactly as
+ * sparcml_dequantize does: bit-identical to sparcml_dequantize followed by
+ * sparcml_sparse_reduce. bits = 4 is sparcml_sparse_reduce_q4. */
+int sparcml_sparse_reduce_qb(const uint32_t* idx, const uint8_t* codes, const float* scales,
+                             const uint32_t* nnz, int32_t P, uint64_t cap, uint32_t bucket,
+                             uint32_t bits, uint64_t N, uint32_t dens_num, uint32_t dens_den,
                              uint32_t* out_idx, float* out_val, uint64_t out_cap,
                              float* out_dense, uint32_t* out_nnz, int32_t* out_is_dense,
                              void* ws, size_t ws_bytes, void* stream);

@@ -98,6 +98,14 @@ def test_reduce_and_other_host_validation():
     assert lib.sparcml_pack(FAKE, 2, 100, C.c_float(float("nan")), FAKE, FAKE, FAKE, 10, FAKE,
                             4096, None) == 1
     assert lib.sparcml_get_status(None, None) == 1
+    q = lib.sparcml_quantize
+    assert q(None, FAKE, None, 1, 16, 8, 3, 0, FAKE, FAKE, None, None, None) == 1  # bits
+    assert q(None, FAKE, None, 1, 16, 6, 2, 0, FAKE, FAKE, None, None, None) == 1  # bucket
+    assert q(None, None, None, 1, 16, 8, 4, 0, FAKE, FAKE, None, None, None) == 1  # val
+    assert lib.sparcml_dequantize(FAKE, FAKE, None, 1, 16, 8, 5, FAKE, None, None) == 1
+    ws = lib.sparcml_sparse_reduce_workspace_size(2, 1000)
+    assert lib.sparcml_sparse_reduce_qb(FAKE, FAKE, FAKE, FAKE, 2, 10, 6, 2, 1000, 1, 4, FAKE,
+                                        FAKE, 250, FAKE, FAKE, FAKE, FAKE, ws, None) == 1
 
 
 def test_segment_k_total_matches_the_oracle_rule():

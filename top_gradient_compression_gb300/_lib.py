@@ -36,6 +36,13 @@ SIGNATURES = {
                                     vp, vp, vp, vp]),
     "sparcml_dequantize4": (C.c_int, [vp, vp, vp, C.c_int32, C.c_uint64, C.c_uint32, vp, vp,
                                       vp]),
+    "sparcml_quantize": (C.c_int, [vp, vp, vp, C.c_int32, C.c_uint64, C.c_uint32, C.c_uint32,
+                                   C.c_uint64, vp, vp, vp, vp, vp]),
+    "sparcml_dequantize": (C.c_int, [vp, vp, vp, C.c_int32, C.c_uint64, C.c_uint32, C.c_uint32,
+                                     vp, vp, vp]),
+    "sparcml_sparse_reduce_qb": (C.c_int, [vp, vp, vp, vp, C.c_int32, C.c_uint64, C.c_uint32,
+                                           C.c_uint32, C.c_uint64, C.c_uint32, C.c_uint32, vp,
+                                           vp, C.c_uint64, vp, vp, vp, vp, C.c_size_t, vp]),
     "sparcml_sparse_reduce_workspace_size": (C.c_size_t, [C.c_int32, C.c_uint64]),
     "sparcml_sparse_reduce": (C.c_int, [vp, vp, vp, C.c_int32, C.c_uint64, C.c_uint64,
                                         C.c_uint32, C.c_uint32, vp, vp, C.c_uint64, vp, vp, vp,

@@ -195,6 +195,44 @@ def dequantize4(codes, scales, nnz, cap: int, bucket: int, out=None, status=None
     return out
 
 
+def quantize(val, bucket: int, bits: int, seed: int, idx=None, nnz=None, codes=None,
+             scales=None, err=None, status=None, stream=None):
+    """b-bit stochastic quantisation (b in {2, 4, 8}) of stream values (idx,
+    nnz given) or of dense rows (idx None: positions are the rounding keys;
+    nnz None: full rows). val may be 1-D (one row). err, if given, receives
+    v - dequantised(v). Returns (codes, scales)."""
+    if val.dim() == 1:
+        val = val.view(1, -1)
+    P, cap = val.shape
+    per = 8 // bits
+    if codes is None:
+        codes = torch.zeros((P, (cap + per - 1) // per), dtype=torch.uint8, device=val.device)
+    if scales is None:
+        scales = torch.zeros((P, (cap + bucket - 1) // bucket), dtype=torch.float32,
+                             device=val.device)
+    _check("sparcml_quantize", _lib.load().sparcml_quantize(
+        None if idx is None else _cuda(idx, torch.int32, "idx", 2),
+        _cuda(val, torch.float32, "val", 2),
+        None if nnz is None else _cuda(nnz, torch.int32, "nnz", 1), P, cap, bucket, bits,
+        seed & (2**64 - 1), _cuda(codes, torch.uint8, "codes", 2),
+        _cuda(scales, torch.float32, "scales", 2),
+        None if err is None else _cuda(err.view(P, cap), torch.float32, "err", 2),
+        _opt_ptr(status), _stream(stream)))
+    return codes, scales
+
+
+def dequantize(codes, scales, cap: int, bucket: int, bits: int, nnz=None, out=None, status=None,
+               stream=None):
+    P = codes.shape[0]
+    if out is None:
+        out = torch.zeros((P, cap), dtype=torch.float32, device=codes.device)
+    _check("sparcml_dequantize", _lib.load().sparcml_dequantize(
+        _cuda(codes, torch.uint8, "codes", 2), _cuda(scales, torch.float32, "scales", 2),
+        None if nnz is None else _cuda(nnz, torch.int32, "nnz", 1), P, cap, bucket, bits,
+        _cuda(out, torch.float32, "val_out", 2), _opt_ptr(status), _stream(stream)))
+    return out
+
+
 # ---------------------------------------------------------------------------
 # Sparse sum-reduce with the dense switch (§5.1-§5.3).
 # ---------------------------------------------------------------------------
@@ -262,6 +300,23 @@ def sparse_reduce_q4(idx, codes, scales, nnz, bucket: int, N: int, dens_num: int
         _cuda(scales, torch.float32, "scales", 2), _cuda(nnz, torch.int32, "nnz", 1), P, cap,
         bucket, N, dens_num, dens_den, oi, ov, ocap, od, on, odn, ws.data_ptr(), ws.numel(),
         _stream(stream)))
+    return out
+
+
+def sparse_reduce_qb(idx, codes, scales, nnz, bucket: int, bits: int, N: int, dens_num: int = 1,
+                     dens_den: int = 4, out: ReduceOut | None = None, ws=None,
+                     stream=None) -> ReduceOut:
+    P, cap = idx.shape
+    if out is None:
+        out = reduce_out(N, idx.device, dens_num, dens_den)
+    if ws is None:
+        ws = workspace(reduce_workspace_size(P, N), idx.device)
+    oi, ov, ocap, od, on, odn = _reduce_out_ptrs(out)
+    _check("sparcml_sparse_reduce_qb", _lib.load().sparcml_sparse_reduce_qb(
+        _cuda(idx, torch.int32, "idx", 2), _cuda(codes, torch.uint8, "codes", 2),
+        _cuda(scales, torch.float32, "scales", 2), _cuda(nnz, torch.int32, "nnz", 1), P, cap,
+        bucket, bits, N, dens_num, dens_den, oi, ov, ocap, od, on, odn, ws.data_ptr(),
+        ws.numel(), _stream(stream)))
     return out
 
 

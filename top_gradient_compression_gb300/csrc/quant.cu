@@ -1,14 +1,16 @@
-// 4-bit stochastic quantisation of stream values and its inverse, sm_103a.
+// b-bit (2, 4, 8) stochastic quantisation of stream values or dense rows and
+// its inverse, sm_103a.
 //
 // "SparCML: High-Performance Sparse Communication for Machine Learning",
 // §2.2 (quantisation Q is an element-wise stochastic operator whose noise
 // has zero mean) and §6 (QSGD: buckets of entries quantised independently,
 // packed low-precision items plus one full-precision scale per bucket; 2-,
-// 4- and 8-bit outputs). This file provides the 4-bit form: sign bit plus a
-// 3-bit level in 0..7 of the bucket's max |v|.
+// 4- and 8-bit outputs). Code: sign bit plus a (b-1)-bit level in 0..s,
+// s = 2^(b-1) - 1 (1, 7, 127), of the bucket's max |v|; 8/b codes per byte,
+// the earliest entry in the lowest bits.
 //
 // One warp per bucket: a warp max-reduction gives the scale, then each lane
-// encodes pairs of entries into one byte (even entry in the low nibble).
+// encodes the 8/b entries of one byte.
 // The rounding draw for an entry is SplitMix64 keyed by (seed, node, index),
 // so it does not depend on which thread or launch handles the entry.
 
@@ -21,31 +23,67 @@ namespace {
 
 constexpr uint32_t kQuantThreads = 256;
 
-__device__ __forceinline__ uint32_t encode4(float v, uint32_t i, float scale, uint64_t node_mix) {
-  uint32_t level = 0;
-  if (scale > 0.0f) {
-    const float r = __fmul_rn(__fdiv_rn(fabsf(v), scale), 7.0f);
-    const float f = floorf(r);
-    const float frac = __fsub_rn(r, f);
-    const uint64_t h = splitmix64(node_mix ^ (uint64_t)i);
-    const float u = __fmul_rn((float)(uint32_t)(h >> 40), 1.0f / 16777216.0f);
-    level = (uint32_t)f + (u < frac ? 1u : 0u);
-    level = min(level, 7u);
+// level / s as the correctly rounded fp32 quotient: selects on constant
+// quotients for s = 7, the level itself for s = 1, an IEEE division else.
+template <int BITS>
+__device__ __forceinline__ float level_over_s(uint32_t level) {
+  if constexpr (BITS == 2) {
+    return (float)level;
+  } else if constexpr (BITS == 4) {
+    const float lo = (level & 2u) ? ((level & 1u) ? 3.0f / 7.0f : 2.0f / 7.0f)
+                                  : ((level & 1u) ? 1.0f / 7.0f : 0.0f);
+    const float hi = (level & 2u) ? ((level & 1u) ? 7.0f / 7.0f : 6.0f / 7.0f)
+                                  : ((level & 1u) ? 5.0f / 7.0f : 4.0f / 7.0f);
+    return (level & 4u) ? hi : lo;
+  } else {
+    return __fdiv_rn((float)level, 127.0f);
   }
-  return (v < 0.0f ? 8u : 0u) | level;
 }
 
+template <int BITS>
+__device__ __forceinline__ float decode(uint32_t code, float scale) {
+  constexpr uint32_t kS = (1u << (BITS - 1)) - 1u;
+  const uint32_t level = code & kS;
+  if (level == 0) return 0.0f;
+  const float v = __fmul_rn(level_over_s<BITS>(level), scale);
+  return (code >> (BITS - 1)) ? -v : v;
+}
+
+// Code of v: sign << (BITS-1) | level, level = floor(r) rounded up with
+// probability frac(r), r = (|v| / scale) * s, the draw keyed by the index.
+template <int BITS>
+__device__ __forceinline__ uint32_t encode(float v, uint64_t index, float scale,
+                                           uint64_t node_mix) {
+  constexpr uint32_t kS = (1u << (BITS - 1)) - 1u;
+  uint32_t level = 0;
+  if (scale > 0.0f) {
+    const float r = __fmul_rn(__fdiv_rn(fabsf(v), scale), (float)kS);
+    const float f = floorf(r);
+    const float frac = __fsub_rn(r, f);
+    const uint64_t h = splitmix64(node_mix ^ index);
+    const float u = __fmul_rn((float)(uint32_t)(h >> 40), 1.0f / 16777216.0f);
+    level = (uint32_t)f + (u < frac ? 1u : 0u);
+    level = min(level, kS);
+  }
+  return (v < 0.0f ? 1u << (BITS - 1) : 0u) | level;
+}
+
+// One warp per bucket: warp max of |v| -> scale; then each lane packs the
+// codes of 8/BITS consecutive entries into one byte. idx == nullptr: dense
+// rows (the position is the rounding key); nnz == nullptr: full rows.
+template <int BITS>
 __global__ void __launch_bounds__(kQuantThreads)
-quantize4_kernel(const uint32_t* __restrict__ idx, const float* __restrict__ val,
-                 const uint32_t* __restrict__ nnz, int32_t P, uint64_t cap, uint32_t bucket,
-                 uint32_t nbk, uint64_t seed, uint8_t* __restrict__ codes,
-                 float* __restrict__ scales, uint64_t code_stride, uint64_t scale_stride,
-                 int32_t* status) {
+quantize_kernel(const uint32_t* __restrict__ idx, const float* __restrict__ val,
+                const uint32_t* __restrict__ nnz, int32_t P, uint64_t cap, uint32_t bucket,
+                uint32_t nbk, uint64_t seed, uint8_t* __restrict__ codes,
+                float* __restrict__ scales, float* __restrict__ err_out, uint64_t code_stride,
+                uint64_t scale_stride, int32_t* status) {
+  constexpr uint32_t kPer = 8 / BITS;
   const uint64_t gw = (uint64_t)blockIdx.x * (kQuantThreads / 32) + (threadIdx.x >> 5);
   if (gw >= (uint64_t)P * nbk) return;  // warp-uniform
   const uint32_t p = (uint32_t)(gw / nbk), b = (uint32_t)(gw % nbk);
   const uint32_t lane = lane_id();
-  uint64_t n = nnz[p];
+  uint64_t n = nnz ? (uint64_t)nnz[p] : cap;
   if (n > cap) {
     if (lane == 0 && b == 0) set_status(status, SPARCML_ERR_CAPACITY);
     n = cap;
@@ -54,7 +92,7 @@ quantize4_kernel(const uint32_t* __restrict__ idx, const float* __restrict__ val
   if (b0 >= n) return;
   const uint64_t b1 = min(b0 + bucket, n);
   const float* vp = val + (uint64_t)p * cap;
-  const uint32_t* ip = idx + (uint64_t)p * cap;
+  const uint32_t* ip = idx ? idx + (uint64_t)p * cap : nullptr;
   float m = 0.0f;
   for (uint64_t j = b0 + lane; j < b1; j += 32) m = fmaxf(m, fabsf(vp[j]));
 #pragma unroll
@@ -62,42 +100,114 @@ quantize4_kernel(const uint32_t* __restrict__ idx, const float* __restrict__ val
   if (lane == 0) scales[(uint64_t)p * scale_stride + b] = m;
   const uint64_t node_mix = splitmix64(splitmix64(seed) ^ (uint64_t)p);
   uint8_t* cp = codes + (uint64_t)p * code_stride;
-  for (uint64_t j = b0 + 2 * lane; j < b1; j += 64) {
-    const uint32_t c0 = encode4(vp[j], ip[j], m, node_mix);
-    const uint32_t c1 = j + 1 < b1 ? encode4(vp[j + 1], ip[j + 1], m, node_mix) : 0u;
-    cp[j >> 1] = (uint8_t)(c0 | (c1 << 4));
+  float* ep = err_out ? err_out + (uint64_t)p * cap : nullptr;
+  for (uint64_t j0 = b0 + (uint64_t)kPer * lane; j0 < b1; j0 += 32ull * kPer) {
+    uint32_t byte = 0;
+#pragma unroll
+    for (uint32_t k = 0; k < kPer; ++k) {
+      const uint64_t j = j0 + k;
+      if (j < b1) {
+        const float v = vp[j];
+        const uint32_t c = encode<BITS>(v, ip ? (uint64_t)ip[j] : j, m, node_mix);
+        byte |= c << (k * BITS);
+        if (ep) ep[j] = __fsub_rn(v, decode<BITS>(c, m));
+      }
+    }
+    cp[j0 / kPer] = (uint8_t)byte;
   }
 }
 
-__device__ __forceinline__ float decode4(uint32_t code, float scale) {
-  const uint32_t level = code & 7u;
-  if (level == 0) return 0.0f;
-  const float v = __fmul_rn(__fdiv_rn((float)level, 7.0f), scale);
-  return (code & 8u) ? -v : v;
-}
-
+template <int BITS>
 __global__ void __launch_bounds__(kQuantThreads)
-dequantize4_kernel(const uint8_t* __restrict__ codes, const float* __restrict__ scales,
-                   const uint32_t* __restrict__ nnz, int32_t P, uint64_t cap, uint32_t bucket,
-                   uint64_t code_stride, uint64_t scale_stride, float* __restrict__ out,
-                   int32_t* status) {
+dequantize_kernel(const uint8_t* __restrict__ codes, const float* __restrict__ scales,
+                  const uint32_t* __restrict__ nnz, int32_t P, uint64_t cap, uint32_t bucket,
+                  uint64_t code_stride, uint64_t scale_stride, float* __restrict__ out,
+                  int32_t* status) {
+  constexpr uint32_t kPer = 8 / BITS;
   const uint64_t total = (uint64_t)P * code_stride;
   for (uint64_t q = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; q < total;
        q += (uint64_t)gridDim.x * blockDim.x) {
     const uint32_t p = (uint32_t)(q / code_stride);
-    const uint64_t j = (q % code_stride) * 2;
-    uint64_t n = nnz[p];
+    const uint64_t j0 = (q % code_stride) * kPer;
+    uint64_t n = nnz ? (uint64_t)nnz[p] : cap;
     if (n > cap) {
-      if (j == 0) set_status(status, SPARCML_ERR_CAPACITY);
+      if (j0 == 0) set_status(status, SPARCML_ERR_CAPACITY);
       n = cap;
     }
-    if (j >= n) continue;
-    const uint8_t byte = codes[q];
+    if (j0 >= n) continue;
+    const uint32_t byte = codes[q];
     const float* sp = scales + (uint64_t)p * scale_stride;
     float* op = out + (uint64_t)p * cap;
-    op[j] = decode4(byte & 15u, sp[j / bucket]);
-    if (j + 1 < n) op[j + 1] = decode4(byte >> 4, sp[(j + 1) / bucket]);
+#pragma unroll
+    for (uint32_t k = 0; k < kPer; ++k) {
+      const uint64_t j = j0 + k;
+      if (j < n) op[j] = decode<BITS>((byte >> (k * BITS)) & ((1u << BITS) - 1u), sp[j / bucket]);
+    }
   }
+}
+
+bool valid_width(uint32_t bits, uint32_t bucket) {
+  if (bits != 2 && bits != 4 && bits != 8) return false;
+  return bucket >= 1 && bucket % (8 / bits) == 0;
+}
+
+int launch_quantize(const uint32_t* idx, const float* val, const uint32_t* nnz, int32_t P,
+                    uint64_t cap, uint32_t bucket, uint32_t bits, uint64_t seed, uint8_t* codes,
+                    float* scales, float* err_out, int32_t* status, void* stream) {
+  if (!val || !codes || !scales || P < 1 || P > 65535 || cap < 1 || cap > 0xffffffffull ||
+      !valid_width(bits, bucket))
+    return SPARCML_ERR_INVALID_ARG;
+  const uint64_t nbk = (cap + bucket - 1) / bucket;
+  const uint64_t warps = (uint64_t)P * nbk;
+  const uint64_t blocks = (warps + kQuantThreads / 32 - 1) / (kQuantThreads / 32);
+  if (nbk > 0xffffffffull || blocks > 0x7fffffffull) return SPARCML_ERR_INVALID_ARG;
+  const uint64_t per = 8 / bits, code_stride = (cap + per - 1) / per;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const unsigned g = (unsigned)blocks;
+  if (bits == 2)
+    quantize_kernel<2><<<g, kQuantThreads, 0, s>>>(idx, val, nnz, P, cap, bucket, (uint32_t)nbk,
+                                                   seed, codes, scales, err_out, code_stride,
+                                                   nbk, status);
+  else if (bits == 4)
+    quantize_kernel<4><<<g, kQuantThreads, 0, s>>>(idx, val, nnz, P, cap, bucket, (uint32_t)nbk,
+                                                   seed, codes, scales, err_out, code_stride,
+                                                   nbk, status);
+  else
+    quantize_kernel<8><<<g, kQuantThreads, 0, s>>>(idx, val, nnz, P, cap, bucket, (uint32_t)nbk,
+                                                   seed, codes, scales, err_out, code_stride,
+                                                   nbk, status);
+  if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
+  note_launches(1);
+  return SPARCML_OK;
+}
+
+int launch_dequantize(const uint8_t* codes, const float* scales, const uint32_t* nnz,
+                      int32_t P, uint64_t cap, uint32_t bucket, uint32_t bits, float* val_out,
+                      int32_t* status, void* stream) {
+  if (!codes || !scales || !val_out || P < 1 || P > 65535 || cap < 1 ||
+      cap > 0xffffffffull || !valid_width(bits, bucket))
+    return SPARCML_ERR_INVALID_ARG;
+  const uint64_t per = 8 / bits, code_stride = (cap + per - 1) / per;
+  const uint64_t total = (uint64_t)P * code_stride;
+  const unsigned blocks =
+      (unsigned)std::min<uint64_t>((total + kQuantThreads - 1) / kQuantThreads, 152u * 32u);
+  const uint64_t scale_stride = (cap + bucket - 1) / bucket;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (bits == 2)
+    dequantize_kernel<2><<<blocks, kQuantThreads, 0, s>>>(codes, scales, nnz, P, cap, bucket,
+                                                          code_stride, scale_stride, val_out,
+                                                          status);
+  else if (bits == 4)
+    dequantize_kernel<4><<<blocks, kQuantThreads, 0, s>>>(codes, scales, nnz, P, cap, bucket,
+                                                          code_stride, scale_stride, val_out,
+                                                          status);
+  else
+    dequantize_kernel<8><<<blocks, kQuantThreads, 0, s>>>(codes, scales, nnz, P, cap, bucket,
+                                                          code_stride, scale_stride, val_out,
+                                                          status);
+  if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
+  note_launches(1);
+  return SPARCML_OK;
 }
 
 }  // namespace
@@ -108,34 +218,28 @@ using namespace sparcml;
 extern "C" int sparcml_quantize4(const uint32_t* idx, const float* val, const uint32_t* nnz,
                                  int32_t P, uint64_t cap, uint32_t bucket, uint64_t seed,
                                  uint8_t* codes, float* scales, int32_t* status, void* stream) {
-  if (!idx || !val || !nnz || !codes || !scales || P < 1 || P > 65535 || cap < 1 ||
-      cap > 0xffffffffull || bucket < 2 || (bucket & 1))
-    return SPARCML_ERR_INVALID_ARG;
-  const uint64_t nbk = (cap + bucket - 1) / bucket;
-  const uint64_t warps = (uint64_t)P * nbk;
-  const uint64_t blocks = (warps + kQuantThreads / 32 - 1) / (kQuantThreads / 32);
-  if (nbk > 0xffffffffull || blocks > 0x7fffffffull) return SPARCML_ERR_INVALID_ARG;
-  quantize4_kernel<<<(unsigned)blocks, kQuantThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-      idx, val, nnz, P, cap, bucket, (uint32_t)nbk, seed, codes, scales, (cap + 1) / 2, nbk,
-      status);
-  if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
-  note_launches(1);
-  return SPARCML_OK;
+  if (!idx || !nnz || bucket < 2 || (bucket & 1)) return SPARCML_ERR_INVALID_ARG;
+  return launch_quantize(idx, val, nnz, P, cap, bucket, 4, seed, codes, scales, nullptr, status,
+                         stream);
 }
 
 extern "C" int sparcml_dequantize4(const uint8_t* codes, const float* scales, const uint32_t* nnz,
                                    int32_t P, uint64_t cap, uint32_t bucket, float* val_out,
                                    int32_t* status, void* stream) {
-  if (!codes || !scales || !nnz || !val_out || P < 1 || P > 65535 || cap < 1 ||
-      cap > 0xffffffffull || bucket < 2 || (bucket & 1))
-    return SPARCML_ERR_INVALID_ARG;
-  const uint64_t code_stride = (cap + 1) / 2;
-  const uint64_t total = (uint64_t)P * code_stride;
-  const uint64_t blocks = std::min<uint64_t>((total + kQuantThreads - 1) / kQuantThreads, 152u * 32u);
-  dequantize4_kernel<<<(unsigned)blocks, kQuantThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-      codes, scales, nnz, P, cap, bucket, code_stride, (cap + bucket - 1) / bucket, val_out,
-      status);
-  if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
-  note_launches(1);
-  return SPARCML_OK;
+  if (!nnz || bucket < 2 || (bucket & 1)) return SPARCML_ERR_INVALID_ARG;
+  return launch_dequantize(codes, scales, nnz, P, cap, bucket, 4, val_out, status, stream);
+}
+
+extern "C" int sparcml_quantize(const uint32_t* idx, const float* val, const uint32_t* nnz,
+                                int32_t P, uint64_t cap, uint32_t bucket, uint32_t bits,
+                                uint64_t seed, uint8_t* codes, float* scales, float* err_out,
+                                int32_t* status, void* stream) {
+  return launch_quantize(idx, val, nnz, P, cap, bucket, bits, seed, codes, scales, err_out,
+                         status, stream);
+}
+
+extern "C" int sparcml_dequantize(const uint8_t* codes, const float* scales, const uint32_t* nnz,
+                                  int32_t P, uint64_t cap, uint32_t bucket, uint32_t bits,
+                                  float* val_out, int32_t* status, void* stream) {
+  return launch_dequantize(codes, scales, nnz, P, cap, bucket, bits, val_out, status, stream);
 }

@@ -57,6 +57,7 @@ struct ReduceArgs {
   uint64_t scale_stride;
   uint32_t bucket;
   uint32_t bucket_shift;  // log2(bucket) when a power of two, else 32
+  uint32_t bits;          // width of the quantised codes: 2, 4 or 8
   int32_t P;
   uint32_t N;
   uint32_t ntiles;
@@ -97,20 +98,36 @@ __device__ __forceinline__ float level_over_7(uint32_t level) {
   return (level & 4u) ? hi : lo;
 }
 
-// Value of entry j of node p: fp32 as stored, or decoded from 4 bits.
+// Value of entry j of node p: fp32 as stored, or decoded from its b-bit code
+// (sign bit over a level of s = 2^(b-1) - 1; v = +-(level / s) * scale).
 template <bool Q4>
 __device__ __forceinline__ float load_value(const ReduceArgs& a, uint32_t p, uint32_t j) {
   if constexpr (!Q4) {
     return a.val[(uint64_t)p * a.cap + j];
   } else {
-    const uint8_t byte = a.codes[(uint64_t)p * a.code_stride + (j >> 1)];
-    const uint32_t code = (j & 1) ? (byte >> 4) : (byte & 15u);
-    const uint32_t level = code & 7u;
+    // a.bits is the same for the whole launch: a uniform branch
+    uint32_t code, level;
+    float q;
+    const uint8_t* cp = a.codes + (uint64_t)p * a.code_stride;
+    if (a.bits == 4) {
+      const uint8_t byte = cp[j >> 1];
+      code = (j & 1) ? (byte >> 4) : (byte & 15u);
+      level = code & 7u;
+      q = level_over_7(level);
+    } else if (a.bits == 8) {
+      code = cp[j];
+      level = code & 127u;
+      q = __fdiv_rn((float)level, 127.0f);
+    } else {
+      code = (cp[j >> 2] >> ((j & 3) * 2)) & 3u;
+      level = code & 1u;
+      q = (float)level;
+    }
     if (level == 0) return 0.0f;
     const uint32_t b = a.bucket_shift < 32 ? j >> a.bucket_shift : j / a.bucket;
     const float scale = a.scales[(uint64_t)p * a.scale_stride + b];
-    const float v = __fmul_rn(level_over_7(level), scale);
-    return (code & 8u) ? -v : v;
+    const float v = __fmul_rn(q, scale);
+    return (code >> (a.bits - 1)) ? -v : v;
   }
 }
 
@@ -1666,27 +1683,31 @@ extern "C" int sparcml_sparse_reduce(const uint32_t* idx, const float* val, cons
                                       ws_bytes, stream, nullptr);
 }
 
-extern "C" int sparcml_sparse_reduce_q4(const uint32_t* idx, const uint8_t* codes,
-                                        const float* scales, const uint32_t* nnz, int32_t P,
-                                        uint64_t cap, uint32_t bucket, uint64_t N,
-                                        uint32_t dens_num, uint32_t dens_den, uint32_t* out_idx,
-                                        float* out_val, uint64_t out_cap, float* out_dense,
-                                        uint32_t* out_nnz, int32_t* out_is_dense, void* ws,
-                                        size_t ws_bytes, void* stream) {
+namespace sparcml {
+namespace {
+int reduce_quantised(const uint32_t* idx, const uint8_t* codes, const float* scales,
+                     const uint32_t* nnz, int32_t P, uint64_t cap, uint32_t bucket, uint32_t bits,
+                     uint64_t N, uint32_t dens_num, uint32_t dens_den, uint32_t* out_idx,
+                     float* out_val, uint64_t out_cap, float* out_dense, uint32_t* out_nnz,
+                     int32_t* out_is_dense, void* ws, size_t ws_bytes, void* stream) {
   const int st = check_reduce_args(idx, nnz, P, cap, N, dens_num, dens_den, out_idx, out_val,
                                    out_cap, out_dense, out_nnz, out_is_dense, ws);
   if (st != SPARCML_OK) return st;
-  if (!codes || !scales || bucket < 2 || (bucket & 1) || cap < 1) return SPARCML_ERR_INVALID_ARG;
+  if (bits != 2 && bits != 4 && bits != 8) return SPARCML_ERR_INVALID_ARG;
+  const uint32_t per = 8 / bits;
+  if (!codes || !scales || bucket < 1 || bucket % per != 0 || cap < 1)
+    return SPARCML_ERR_INVALID_ARG;
   ReduceArgs a = {};
   a.idx = idx;
   a.codes = codes;
   a.scales = scales;
   a.nnz = nnz;
   a.cap = cap;
-  a.code_stride = (cap + 1) / 2;
+  a.code_stride = (cap + per - 1) / per;
   a.scale_stride = (cap + bucket - 1) / bucket;
   a.bucket = bucket;
   a.bucket_shift = (bucket & (bucket - 1)) == 0 ? (uint32_t)__builtin_ctz(bucket) : 32u;
+  a.bits = bits;
   a.P = P;
   a.N = (uint32_t)N;
   a.ntiles = (uint32_t)((N + kTile - 1) / kTile);
@@ -1697,6 +1718,33 @@ extern "C" int sparcml_sparse_reduce_q4(const uint32_t* idx, const uint8_t* code
   a.out_nnz = out_nnz;
   a.out_is_dense = out_is_dense;
   return launch_reduce<true>(a, ws, ws_bytes, static_cast<cudaStream_t>(stream), nullptr);
+}
+}  // namespace
+}  // namespace sparcml
+
+extern "C" int sparcml_sparse_reduce_q4(const uint32_t* idx, const uint8_t* codes,
+                                        const float* scales, const uint32_t* nnz, int32_t P,
+                                        uint64_t cap, uint32_t bucket, uint64_t N,
+                                        uint32_t dens_num, uint32_t dens_den, uint32_t* out_idx,
+                                        float* out_val, uint64_t out_cap, float* out_dense,
+                                        uint32_t* out_nnz, int32_t* out_is_dense, void* ws,
+                                        size_t ws_bytes, void* stream) {
+  if (bucket < 2 || (bucket & 1)) return SPARCML_ERR_INVALID_ARG;
+  return reduce_quantised(idx, codes, scales, nnz, P, cap, bucket, 4, N, dens_num, dens_den,
+                          out_idx, out_val, out_cap, out_dense, out_nnz, out_is_dense, ws,
+                          ws_bytes, stream);
+}
+
+extern "C" int sparcml_sparse_reduce_qb(const uint32_t* idx, const uint8_t* codes,
+                                        const float* scales, const uint32_t* nnz, int32_t P,
+                                        uint64_t cap, uint32_t bucket, uint32_t bits, uint64_t N,
+                                        uint32_t dens_num, uint32_t dens_den, uint32_t* out_idx,
+                                        float* out_val, uint64_t out_cap, float* out_dense,
+                                        uint32_t* out_nnz, int32_t* out_is_dense, void* ws,
+                                        size_t ws_bytes, void* stream) {
+  return reduce_quantised(idx, codes, scales, nnz, P, cap, bucket, bits, N, dens_num, dens_den,
+                          out_idx, out_val, out_cap, out_dense, out_nnz, out_is_dense, ws,
+                          ws_bytes, stream);
 }
 
 // ---------------------------------------------------------------------------
