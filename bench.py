@@ -45,9 +45,13 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["resnet50", "asr", "sweep", "logreg"], default="resnet50",
+    ap.add_argument("--workload", choices=["resnet50", "asr", "sweep", "logreg", "qsgd"],
+                    default="resnet50",
                     help="resnet50/asr: the whole EF step; sweep/logreg: the sparse reduce alone "
-                         "on given streams (density-sweep cell / Zipf logistic regression)")
+                         "on given streams (density-sweep cell / Zipf logistic regression); "
+                         "qsgd: b-bit quantisation of a dense reduced result")
+    ap.add_argument("--bits", type=int, default=4, choices=[2, 4, 8],
+                    help="asr / qsgd: width of the quantised codes")
     ap.add_argument("--sweep-p", type=int, default=64)
     ap.add_argument("--sweep-d", type=float, default=10,
                     help="per-node density in percent: 0.1, 1, 5 or 10")
@@ -92,6 +96,13 @@ class Ranks:
         if self.pg:
             import torch.distributed as dist
             dist.destroy_process_group()
+
+
+def gpu_head_start(calls: int, us_per_call: float = 60.0):
+    """Hold the GPU in a short spin before a loop of small timed calls, so the
+    host queues the calls ahead of the GPU and no timed interval includes host
+    launch latency (each call's interval is bracketed by its own events)."""
+    torch.cuda._sleep(int(min(calls * us_per_call, 200_000.0) * 2_000))  # ~2 GHz cycles
 
 
 def job_rate(world: int, units_per_rank: float, seconds: float) -> float:
@@ -189,6 +200,8 @@ def workload_spec(name):
                     gen=lambda t, dev: W.resnet50_grads(t, device=dev),
                     data="synthetic: N(0, sigma_b^2), sigma_b log-uniform in [1e-4, 1e-1] per "
                          "100k-entry block (seeded torch generator on device)")
+    if name != "asr":
+        raise ValueError(f"workload {name!r} has no EF-step spec")
     c = W.ASR
     return dict(name="asr", P=c["P"], N=c["N"], seg_len=c["seg_len"], k_num=c["k_num"],
                 k_den=c["k_den"], quant=True, bucket=c["bucket"],
@@ -242,8 +255,9 @@ def cpu_sample_run(spec, grads_host, nseg, steps):
         oi, ov, on = oracle.topk_ef(g, res, L, spec["k_num"], spec["k_den"])
         if spec["quant"]:
             from top_gradient_compression_gb300 import workloads as W
-            codes, scales = oracle.quantize4(oi, ov, on, spec["bucket"], W.quant_seed(s))
-            ov = oracle.dequantize4(codes, scales, on, oi.shape[1], spec["bucket"])
+            b = spec.get("bits", 4)
+            codes, scales = oracle.quantize(ov, spec["bucket"], b, W.quant_seed(s), idx=oi, nnz=on)
+            ov = oracle.dequantize(codes, scales, oi.shape[1], spec["bucket"], b, nnz=on)
         oracle.sparse_reduce(oi, ov, on, n)
     dt = time.perf_counter() - t0
     return dt, P * n * 4 * steps, n
@@ -254,7 +268,10 @@ def run_reference(args, ranks):
     if ranks.rank != 0:
         return
     from top_gradient_compression_gb300 import workloads as W
+    if args.workload in ("sweep", "logreg", "qsgd"):
+        return run_reference_op(args)
     spec = workload_spec(args.workload)
+    spec["bits"] = args.bits
     P, L = spec["P"], spec["seg_len"]
     nseg = 1
     n = min(spec["N"], nseg * L)
@@ -265,8 +282,9 @@ def run_reference(args, ranks):
     def step(s):
         oi, ov, on = oracle.topk_ef(grads[0], res, L, spec["k_num"], spec["k_den"])
         if spec["quant"]:
-            c, sc = oracle.quantize4(oi, ov, on, spec["bucket"], W.quant_seed(s))
-            ov = oracle.dequantize4(c, sc, on, oi.shape[1], spec["bucket"])
+            b = spec.get("bits", 4)
+            c, sc = oracle.quantize(ov, spec["bucket"], b, W.quant_seed(s), idx=oi, nnz=on)
+            ov = oracle.dequantize(c, sc, oi.shape[1], spec["bucket"], b, nnz=on)
         oracle.sparse_reduce(oi, ov, on, n)
 
     for s in range(args.warmup):
@@ -288,6 +306,50 @@ def run_reference(args, ranks):
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def run_reference_op(args):
+    """--impl reference for the single-operation workloads: the oracle's reduce
+    (sweep, logreg) or quantiser (qsgd) on the same inputs, one host core."""
+    import oracle
+    from top_gradient_compression_gb300 import workloads as W
+    if args.workload == "logreg":
+        idx, val, nnz = W.logreg_streams()
+        N = W.LOGREG["N"]
+    else:
+        P = args.sweep_p if args.workload == "sweep" else 64
+        dpct = args.sweep_d if args.workload == "sweep" else 10
+        cell = [(a, b) for a, b in W.SWEEP_D if abs(100.0 * a / b - dpct) < 1e-9][0]
+        idx, val, nnz = W.sweep_streams(P, *cell)
+        N = W.SWEEP_N
+    if args.workload == "qsgd":
+        x = oracle.sparse_reduce(idx, val, nnz, N)["dense"]
+        op = lambda s: oracle.quantize(x, 1024, args.bits, W.quant_seed(s))  # noqa: E731
+        units, nbytes = N, 4 * N
+        desc = f"QSGD {args.bits}-bit on a dense reduced vector, N={N:,}, buckets of 1024"
+    else:
+        op = lambda s: oracle.sparse_reduce(idx, val, nnz, N)  # noqa: E731
+        units = int(nnz.astype(np.int64).sum())
+        nbytes = 8 * units
+        desc = f"sparse reduce of {idx.shape[0]} streams, N={N:,} ({args.workload})"
+    for s in range(args.warmup):
+        op(s)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        op(s)
+    dt = time.perf_counter() - t0
+    v = nbytes * args.steps / dt / 1e9
+    sample = f"oracle (1 thread): the whole workload, {args.steps} calls"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s",
+        "elems_per_s": units * args.steps / dt, "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": desc, "sample": sample},
+        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+        flush=True)
 
 
 # ---------------------------------------------------------------------------
@@ -325,6 +387,7 @@ def run_reduce_only(args, ranks):
     torch.cuda.synchronize()
     launches0 = api.launch_count()
     tot = 0.0
+    gpu_head_start(K)
     for i in range(K):
         flush.fill_(float(i))  # inputs do not stay in L2 between timed runs
         api.sparse_reduce(di, dv, dn, N, out=out, ws=ws, events=evs[i])
@@ -375,6 +438,7 @@ def run_ours(args, ranks):
         raise RuntimeError("bench.py --impl ours needs a CUDA device")
     torch.cuda.set_device(dev)
     spec = workload_spec(args.workload)
+    spec["bits"] = args.bits
     if args.nodes:
         spec["P"] = args.nodes
         spec["desc"] += f" [P overridden to {args.nodes}]"
@@ -392,8 +456,11 @@ def run_ours(args, ranks):
     rd_ws = api.workspace(api.reduce_workspace_size(P, N), dev)
     rd_out = api.reduce_out(N, dev)
     if spec["quant"]:
-        bucket = spec["bucket"]
-        codes = torch.zeros((P, (cap + 1) // 2), dtype=torch.uint8, device=dev)
+        bucket, qbits = spec["bucket"], args.bits
+        codes = torch.zeros((P, (cap + 8 // qbits - 1) // (8 // qbits)), dtype=torch.uint8,
+                            device=dev)
+        if qbits != 4:
+            spec["desc"] = spec["desc"].replace("4-bit", f"{qbits}-bit")
         scales = torch.zeros((P, (cap + bucket - 1) // bucket), device=dev)
         qstat = api.status_word(dev)
 
@@ -408,11 +475,11 @@ def run_ours(args, ranks):
         if spec["quant"]:
             if timed:
                 ev_q[i][0].record()
-            api.quantize4(tk_out[0], tk_out[1], tk_out[2], bucket, W.quant_seed(i), codes=codes,
-                          scales=scales, status=qstat)
+            api.quantize(tk_out[1], bucket, qbits, W.quant_seed(i), idx=tk_out[0], nnz=tk_out[2],
+                         codes=codes, scales=scales, status=qstat)
             if timed:
                 ev_q[i][1].record()
-            api.sparse_reduce_q4(tk_out[0], codes, scales, tk_out[2], bucket, N, out=rd_out,
+            api.sparse_reduce_qb(tk_out[0], codes, scales, tk_out[2], bucket, qbits, N, out=rd_out,
                                  ws=rd_ws)
             if timed:
                 ev_q[i][2].record()
@@ -452,8 +519,8 @@ def run_ours(args, ranks):
     kern = {"topk_guess": mean_ms(ev_tk, 0, 1), "topk_stream": mean_ms(ev_tk, 1, 2),
             "topk_select": mean_ms(ev_tk, 2, 3)}
     if spec["quant"]:
-        kern["quantize4"] = mean_ms(ev_q, 0, 1)
-        kern["reduce_q4"] = mean_ms(ev_q, 1, 2)
+        kern[f"quantize{qbits}"] = mean_ms(ev_q, 0, 1)
+        kern[f"reduce_q{qbits}"] = mean_ms(ev_q, 1, 2)
     else:
         kern["reduce_split_tile"] = mean_ms(ev_rd, 0, 1)
         kern["reduce_fixup"] = mean_ms(ev_rd, 1, 2)
@@ -469,7 +536,8 @@ def run_ours(args, ranks):
     traffic = load_traffic("topk_stream_kernel",
                            os.path.join(ROOT, "top_gradient_compression_gb300", "csrc",
                                         "topk_ef.cu"))
-    reduce_in = 8 * sum_nnz if not spec["quant"] else sum_nnz // 2 + 4 * P * ((cap + 511) // 512) + 4 * sum_nnz
+    reduce_in = (8 * sum_nnz if not spec["quant"] else
+                 sum_nnz * qbits // 8 + 4 * P * ((cap + bucket - 1) // bucket) + 4 * sum_nnz)
 
     # ---- end to end: pinned host gradients in, reduced result out, every step.
     # Step i+1's gradients are copied on a second stream into the other device
@@ -588,6 +656,78 @@ def run_ours(args, ranks):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# QSGD on the dense reduced result (DSAR's quantised second half, §6)
+# ---------------------------------------------------------------------------
+def run_qsgd(args, ranks):
+    """b-bit stochastic quantisation of a dense reduced vector: the dense result
+    of the largest density-sweep cell (P=64, d=10%), buckets of 1,024. One step
+    = one quantise call. value = 4 B per input entry / time."""
+    from top_gradient_compression_gb300 import api, workloads as W
+    dev = ranks.device()
+    torch.cuda.set_device(dev)
+    N, bits_, bucket = W.SWEEP_N, args.bits, 1024
+    idx, val, nnz = W.sweep_streams(64, 10, 100)
+    di = torch.from_numpy(idx.view(np.int32)).to(dev)
+    dv = torch.from_numpy(val).to(dev)
+    dn = torch.from_numpy(nnz.view(np.int32)).to(dev)
+    out = api.sparse_reduce(di, dv, dn, N)
+    if not bool(out.is_dense.item()):
+        raise RuntimeError("the sweep cell's reduced result is expected dense")
+    x = out.dense.view(1, N)
+    del di, dv, dn
+    per = 8 // bits_
+    codes = torch.zeros((1, (N + per - 1) // per), dtype=torch.uint8, device=dev)
+    scales = torch.zeros((1, (N + bucket - 1) // bucket), device=dev)
+    status = api.status_word(dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)  # 256 MB > L2
+    K, Wm = args.steps, args.warmup
+    for i in range(Wm):
+        api.quantize(x, bucket, bits_, W.quant_seed(i), codes=codes, scales=scales, status=status)
+    torch.cuda.synchronize()
+    launches0 = api.launch_count()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    clocks = ClockSampler(dev)
+    time.sleep(1.0)
+    t_host0 = time.time()
+    gpu_head_start(K)
+    for i in range(K):
+        flush.fill_(float(i))  # the 16.8 MB input does not stay in L2 between calls
+        evs[i][0].record()
+        api.quantize(x, bucket, bits_, W.quant_seed(i), codes=codes, scales=scales, status=status)
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    clk = clocks.summary(t_host0, t_host1)
+    clocks.stop()
+    launches = api.launch_count() - launches0
+    if api.get_status(status) != 0:
+        raise RuntimeError("device status set after the timed quantise calls")
+    ms = ranks.max(float(np.mean([a.elapsed_time(b) for a, b in evs])))
+    in_bytes = 4 * N
+    out_bytes = codes.numel() + 4 * scales.numel()
+    peak, peak_kind = hbm_peak()
+    achieved = (in_bytes + out_bytes) / (ms * 1e-3) / 1e9
+    if ranks.rank != 0:
+        return
+    print(json.dumps({
+        "metric": METRIC, "value": job_rate(ranks.world, in_bytes, ms * 1e-3) / 1e9,
+        "unit": "GB/s", "elems_per_s": job_rate(ranks.world, N, ms * 1e-3),
+        "n_gpus": ranks.world, "steps": K, "warmup": Wm, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (dense result of the P=64, d=10% density-sweep reduce)",
+        "config": {"workload": f"QSGD {bits_}-bit on a dense reduced vector, N={N:,}, buckets of "
+                               f"{bucket}", "N": N, "bits": bits_, "bucket": bucket,
+                   "units": "value = 4 B per input entry / quantise time",
+                   "l2": "256 MB buffer written between timed calls (L2 flushed)"},
+        "roofline": {"bound": "hbm", "kernel": f"quantize_kernel<{bits_}>", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": in_bytes + out_bytes, "traffic": None,
+                     "launch_ms": ms},
+        "cpu_baseline": None, "e2e": None, "gpu_launches": launches, "clocks": clk}), flush=True)
+
+
 def main():
     args = parse_args()
     ranks = Ranks()
@@ -596,6 +736,8 @@ def main():
             run_reference(args, ranks)
         elif args.workload in ("sweep", "logreg"):
             run_reduce_only(args, ranks)
+        elif args.workload == "qsgd":
+            run_qsgd(args, ranks)
         else:
             run_ours(args, ranks)
     finally:

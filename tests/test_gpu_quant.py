@@ -15,10 +15,14 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("b", [2, 4, 8])
-@pytest.mark.parametrize("bucket", [512, 96])
-def test_stream_quantise_dequantise_and_error(b, bucket):
+@pytest.mark.parametrize("bucket,cap", [(512, 3_001), (96, 3_004), (512, 3_004), (1024, 3_004)])
+def test_stream_quantise_dequantise_and_error(b, bucket, cap):
+    """cap % 4 == 0 with buckets of 512 / 1,024 takes the register-resident
+    vector kernel (rows ending inside a float4 included); the rest the
+    entry-by-entry one."""
     P, N, k = 5, 400_000, 3_001
-    idx, val, nnz = W.uniform_streams(P, N, k, 61, std=1e-3)
+    idx, val, nnz = W.uniform_streams(P, N, k, 61, std=1e-3, cap=cap)
+    k = cap
     nnz[1] = 1_237
     nnz[3] = 0
     seed = W.quant_seed(4)
@@ -42,11 +46,12 @@ def test_stream_quantise_dequantise_and_error(b, bucket):
 
 
 @pytest.mark.parametrize("b", [2, 4, 8])
-def test_dense_rows_quantise_like_the_oracle(b):
+@pytest.mark.parametrize("N", [1_000_003, 1_049_088])
+def test_dense_rows_quantise_like_the_oracle(b, N):
     """QSGD on a dense vector (the reduced result of a dense reduce), buckets of
-    1,024, positions as rounding keys; a ragged last bucket."""
+    1,024, positions as rounding keys; a ragged last bucket (the second size
+    takes the vector kernel)."""
     rng = np.random.default_rng(b)
-    N = 1_000_003 - (1_000_003 % (8 // b))
     x = rng.standard_normal((1, N)).astype(np.float32)
     x[0, 5000:6024] = 0.0  # an all-zero bucket
     oc, osc = oracle.quantize(x, 1024, b, 12345)

@@ -9,8 +9,8 @@
 // s = 2^(b-1) - 1 (1, 7, 127), of the bucket's max |v|; 8/b codes per byte,
 // the earliest entry in the lowest bits.
 //
-// One warp per bucket: a warp max-reduction gives the scale, then each lane
-// encodes the 8/b entries of one byte.
+// Two passes: one warp per bucket takes the scale (a warp max-reduction),
+// then one thread per code byte encodes its 8/b entries.
 // The rounding draw for an entry is SplitMix64 keyed by (seed, node, index),
 // so it does not depend on which thread or launch handles the entry.
 
@@ -68,17 +68,11 @@ __device__ __forceinline__ uint32_t encode(float v, uint64_t index, float scale,
   return (v < 0.0f ? 1u << (BITS - 1) : 0u) | level;
 }
 
-// One warp per bucket: warp max of |v| -> scale; then each lane packs the
-// codes of 8/BITS consecutive entries into one byte. idx == nullptr: dense
-// rows (the position is the rounding key); nnz == nullptr: full rows.
-template <int BITS>
+// Pass 1, one warp per bucket: scale = max |v| over the bucket.
 __global__ void __launch_bounds__(kQuantThreads)
-quantize_kernel(const uint32_t* __restrict__ idx, const float* __restrict__ val,
-                const uint32_t* __restrict__ nnz, int32_t P, uint64_t cap, uint32_t bucket,
-                uint32_t nbk, uint64_t seed, uint8_t* __restrict__ codes,
-                float* __restrict__ scales, float* __restrict__ err_out, uint64_t code_stride,
-                uint64_t scale_stride, int32_t* status) {
-  constexpr uint32_t kPer = 8 / BITS;
+quantize_scale_kernel(const float* __restrict__ val, const uint32_t* __restrict__ nnz, int32_t P,
+                      uint64_t cap, uint32_t bucket, uint32_t nbk, float* __restrict__ scales,
+                      uint64_t scale_stride, int32_t* status) {
   const uint64_t gw = (uint64_t)blockIdx.x * (kQuantThreads / 32) + (threadIdx.x >> 5);
   if (gw >= (uint64_t)P * nbk) return;  // warp-uniform
   const uint32_t p = (uint32_t)(gw / nbk), b = (uint32_t)(gw % nbk);
@@ -92,28 +86,90 @@ quantize_kernel(const uint32_t* __restrict__ idx, const float* __restrict__ val,
   if (b0 >= n) return;
   const uint64_t b1 = min(b0 + bucket, n);
   const float* vp = val + (uint64_t)p * cap;
-  const uint32_t* ip = idx ? idx + (uint64_t)p * cap : nullptr;
   float m = 0.0f;
   for (uint64_t j = b0 + lane; j < b1; j += 32) m = fmaxf(m, fabsf(vp[j]));
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
   if (lane == 0) scales[(uint64_t)p * scale_stride + b] = m;
+}
+
+// Pass 1 for aligned rows and buckets of 128 * VPL entries: each lane issues
+// its VPL float4 loads together (a latency chain of one load, not 32).
+template <int VPL>
+__global__ void __launch_bounds__(kQuantThreads)
+quantize_scale_vec_kernel(const float* __restrict__ val, const uint32_t* __restrict__ nnz,
+                          int32_t P, uint64_t cap, uint32_t nbk, float* __restrict__ scales,
+                          uint64_t scale_stride, int32_t* status) {
+  constexpr uint32_t kBucket = 128 * VPL;
+  const uint64_t gw = (uint64_t)blockIdx.x * (kQuantThreads / 32) + (threadIdx.x >> 5);
+  if (gw >= (uint64_t)P * nbk) return;  // warp-uniform
+  const uint32_t p = (uint32_t)(gw / nbk), b = (uint32_t)(gw % nbk);
+  const uint32_t lane = lane_id();
+  uint64_t n = nnz ? (uint64_t)nnz[p] : cap;
+  if (n > cap) {
+    if (lane == 0 && b == 0) set_status(status, SPARCML_ERR_CAPACITY);
+    n = cap;
+  }
+  const uint64_t b0 = (uint64_t)b * kBucket;
+  if (b0 >= n) return;
+  const uint64_t b1 = min(b0 + kBucket, n);
+  const float4* vp = reinterpret_cast<const float4*>(val + (uint64_t)p * cap + b0);
+  float4 v[VPL];
+#pragma unroll
+  for (int k = 0; k < VPL; ++k) {
+    const uint64_t j = b0 + 4ull * (lane + 32u * k);
+    v[k] = j < b1 ? vp[lane + 32 * k] : make_float4(0.f, 0.f, 0.f, 0.f);  // inside the row
+  }
+  float m = 0.0f;
+#pragma unroll
+  for (int k = 0; k < VPL; ++k) {
+    const uint64_t j = b0 + 4ull * (lane + 32u * k);
+    // entries past the row's end (the float4 holding its last entry) do not count
+    const float e[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      if (j + t < b1) m = fmaxf(m, fabsf(e[t]));
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+  if (lane == 0) scales[(uint64_t)p * scale_stride + b] = m;
+}
+
+// Pass 2, one thread per code byte (8/BITS entries of one bucket, since a
+// bucket is a whole number of bytes): encode against the bucket's scale.
+// idx == nullptr: dense rows (the position is the rounding key); nnz ==
+// nullptr: full rows.
+template <int BITS>
+__global__ void __launch_bounds__(kQuantThreads)
+quantize_encode_kernel(const uint32_t* __restrict__ idx, const float* __restrict__ val,
+                       const uint32_t* __restrict__ nnz, uint64_t cap, uint32_t bucket_shift,
+                       uint32_t bucket, uint64_t seed, uint8_t* __restrict__ codes,
+                       const float* __restrict__ scales, float* __restrict__ err_out,
+                       uint32_t code_stride, uint64_t scale_stride) {
+  constexpr uint32_t kPer = 8 / BITS;
+  const uint32_t p = blockIdx.y;  // grid: (bytes of a row, node)
+  const uint32_t n = nnz ? (uint32_t)min((uint64_t)nnz[p], cap) : (uint32_t)cap;
   const uint64_t node_mix = splitmix64(splitmix64(seed) ^ (uint64_t)p);
+  const uint64_t row = (uint64_t)p * cap;
+  const float* sp = scales + (uint64_t)p * scale_stride;
   uint8_t* cp = codes + (uint64_t)p * code_stride;
-  float* ep = err_out ? err_out + (uint64_t)p * cap : nullptr;
-  for (uint64_t j0 = b0 + (uint64_t)kPer * lane; j0 < b1; j0 += 32ull * kPer) {
+  for (uint32_t q = blockIdx.x * blockDim.x + threadIdx.x; q < code_stride;
+       q += gridDim.x * blockDim.x) {
+    const uint32_t j0 = q * kPer;
+    if (j0 >= n) break;  // bytes past the row's entries stay untouched
+    const float m = sp[bucket_shift < 32 ? j0 >> bucket_shift : j0 / bucket];
     uint32_t byte = 0;
 #pragma unroll
     for (uint32_t k = 0; k < kPer; ++k) {
-      const uint64_t j = j0 + k;
-      if (j < b1) {
-        const float v = vp[j];
-        const uint32_t c = encode<BITS>(v, ip ? (uint64_t)ip[j] : j, m, node_mix);
+      const uint32_t j = j0 + k;
+      if (j < n) {
+        const float v = val[row + j];
+        const uint32_t c = encode<BITS>(v, idx ? (uint64_t)idx[row + j] : (uint64_t)j, m, node_mix);
         byte |= c << (k * BITS);
-        if (ep) ep[j] = __fsub_rn(v, decode<BITS>(c, m));
+        if (err_out) err_out[row + j] = __fsub_rn(v, decode<BITS>(c, m));
       }
     }
-    cp[j0 / kPer] = (uint8_t)byte;
+    cp[q] = (uint8_t)byte;
   }
 }
 
@@ -163,21 +219,34 @@ int launch_quantize(const uint32_t* idx, const float* val, const uint32_t* nnz, 
   if (nbk > 0xffffffffull || blocks > 0x7fffffffull) return SPARCML_ERR_INVALID_ARG;
   const uint64_t per = 8 / bits, code_stride = (cap + per - 1) / per;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const unsigned g = (unsigned)blocks;
-  if (bits == 2)
-    quantize_kernel<2><<<g, kQuantThreads, 0, s>>>(idx, val, nnz, P, cap, bucket, (uint32_t)nbk,
-                                                   seed, codes, scales, err_out, code_stride,
-                                                   nbk, status);
-  else if (bits == 4)
-    quantize_kernel<4><<<g, kQuantThreads, 0, s>>>(idx, val, nnz, P, cap, bucket, (uint32_t)nbk,
-                                                   seed, codes, scales, err_out, code_stride,
-                                                   nbk, status);
+  const bool vec = (bucket == 512 || bucket == 1024) && cap % 4 == 0 &&
+                   (reinterpret_cast<uintptr_t>(val) & 15) == 0;
+  if (vec && bucket == 512)
+    quantize_scale_vec_kernel<4><<<(unsigned)blocks, kQuantThreads, 0, s>>>(
+        val, nnz, P, cap, (uint32_t)nbk, scales, nbk, status);
+  else if (vec)
+    quantize_scale_vec_kernel<8><<<(unsigned)blocks, kQuantThreads, 0, s>>>(
+        val, nnz, P, cap, (uint32_t)nbk, scales, nbk, status);
   else
-    quantize_kernel<8><<<g, kQuantThreads, 0, s>>>(idx, val, nnz, P, cap, bucket, (uint32_t)nbk,
-                                                   seed, codes, scales, err_out, code_stride,
-                                                   nbk, status);
+    quantize_scale_kernel<<<(unsigned)blocks, kQuantThreads, 0, s>>>(
+        val, nnz, P, cap, bucket, (uint32_t)nbk, scales, nbk, status);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
-  note_launches(1);
+  const uint32_t shift = (bucket & (bucket - 1)) == 0 ? (uint32_t)__builtin_ctz(bucket) : 32u;
+  const dim3 eg((unsigned)std::min<uint64_t>((code_stride + kQuantThreads - 1) / kQuantThreads,
+                                             std::max<uint64_t>(1, 152u * 64u / (uint64_t)P)),
+                (unsigned)P);
+  const uint32_t cs = (uint32_t)code_stride;
+  if (bits == 2)
+    quantize_encode_kernel<2><<<eg, kQuantThreads, 0, s>>>(idx, val, nnz, cap, shift, bucket,
+                                                            seed, codes, scales, err_out, cs, nbk);
+  else if (bits == 4)
+    quantize_encode_kernel<4><<<eg, kQuantThreads, 0, s>>>(idx, val, nnz, cap, shift, bucket,
+                                                            seed, codes, scales, err_out, cs, nbk);
+  else
+    quantize_encode_kernel<8><<<eg, kQuantThreads, 0, s>>>(idx, val, nnz, cap, shift, bucket,
+                                                            seed, codes, scales, err_out, cs, nbk);
+  if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
+  note_launches(2);
   return SPARCML_OK;
 }
 
