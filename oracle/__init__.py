@@ -62,6 +62,10 @@ def _load():
                                                  C.c_uint64, C.c_uint32, C.c_uint32, u32p, f32p,
                                                  C.c_uint64, f32p, C.POINTER(C.c_uint64),
                                                  C.POINTER(C.c_int32)]
+            lib.oracle_sparse_reduce_op.argtypes = [u32p, f32p, u32p, C.c_int32, C.c_uint64,
+                                                    C.c_uint64, C.c_int32, C.c_uint32,
+                                                    C.c_uint32, u32p, f32p, C.c_uint64, f32p,
+                                                    C.POINTER(C.c_uint64), C.POINTER(C.c_int32)]
             lib.oracle_densify.argtypes = [u32p, f32p, u32p, C.c_int32, C.c_uint64, C.c_uint64,
                                            f32p]
             for f in ("oracle_topk_ef", "oracle_pack", "oracle_quantize4", "oracle_dequantize4",
@@ -191,6 +195,30 @@ def dequantize(codes, scales, cap, bucket, bits, nnz=None):
     _check("oracle_dequantize", _load().oracle_dequantize(codes, scales, _ptr(nnz), P, cap,
                                                           bucket, bits, out))
     return out
+
+
+OPS = {"sum": 0, "max": 1, "min": 2, "or": 3}
+
+
+def sparse_reduce_op(idx, val, nnz, N, op, dens_num=1, dens_den=4):
+    """Reduction of P sparse streams with sum, max, min or bitwise or, each
+    with its neutral element for unlisted coordinates (SparCML §5.2). Same
+    result dict as sparse_reduce."""
+    idx, val, nnz = _u32(idx), _f32(val), _u32(nnz)
+    P, cap = idx.shape
+    out_cap = max(N * dens_num // dens_den, 1)
+    oi = np.zeros(out_cap, np.uint32)
+    ov = np.zeros(out_cap, np.float32)
+    od = np.zeros(N, np.float32)
+    u = C.c_uint64(0)
+    d = C.c_int32(0)
+    _check("oracle_sparse_reduce_op", _load().oracle_sparse_reduce_op(
+        idx, val, nnz, P, cap, N, OPS[op], dens_num, dens_den, oi, ov, out_cap, od,
+        C.byref(u), C.byref(d)))
+    U = int(u.value)
+    if d.value:
+        return dict(nnz=U, is_dense=True, idx=None, val=None, dense=od)
+    return dict(nnz=U, is_dense=False, idx=oi[:U].copy(), val=ov[:U].copy(), dense=None)
 
 
 def sparse_reduce(idx, val, nnz, N, dens_num=1, dens_den=4):

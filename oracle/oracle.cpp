@@ -36,6 +36,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <limits>
 #include <map>
 #include <utility>
 #include <vector>
@@ -359,6 +360,82 @@ int oracle_sparse_reduce(const uint32_t* idx, const float* val, const uint32_t* 
     if (U > out_cap) return CAPACITY;
     uint64_t j = 0;
     for (const auto& kv : sum) {
+      out_idx[j] = kv.first;
+      out_val[j] = kv.second;
+      ++j;
+    }
+  }
+  return OK;
+}
+
+// Reduction of P sparse streams with another coordinate-wise associative
+// operation that has a neutral element (§5.2): a stream stands for the
+// vector whose unlisted coordinates hold the neutral element, and
+//   op 0 sum: a + b,                          neutral +0.0f
+//   op 1 max: b if b > a else a (fp32 order),  neutral -inf
+//   op 2 min: b if b < a else a,               neutral +inf
+//   op 3 or:  bitwise or of the fp32 bit patterns, neutral +0.0f (all bits 0)
+// applied over the nodes that hold an index in ascending node order,
+// starting from the neutral element. Union size, dense switch and output
+// layout as in oracle_sparse_reduce; a dense result holds the neutral element
+// where no node has the index. op 0 is oracle_sparse_reduce.
+static float fold(int32_t op, float a, float b) {
+  switch (op) {
+    case 0: return a + b;
+    case 1: return b > a ? b : a;
+    case 2: return b < a ? b : a;
+    default: {
+      uint32_t x, y;
+      std::memcpy(&x, &a, 4);
+      std::memcpy(&y, &b, 4);
+      x |= y;
+      float r;
+      std::memcpy(&r, &x, 4);
+      return r;
+    }
+  }
+}
+
+static float neutral(int32_t op) {
+  if (op == 1) return -std::numeric_limits<float>::infinity();
+  if (op == 2) return std::numeric_limits<float>::infinity();
+  return 0.0f;
+}
+
+int oracle_sparse_reduce_op(const uint32_t* idx, const float* val, const uint32_t* nnz,
+                            int32_t P, uint64_t cap, uint64_t N, int32_t op, uint32_t dens_num,
+                            uint32_t dens_den, uint32_t* out_idx, float* out_val,
+                            uint64_t out_cap, float* out_dense, uint64_t* out_nnz,
+                            int32_t* out_is_dense) {
+  if (P <= 0 || N == 0 || N > 0xffffffffULL || dens_den == 0 || op < 0 || op > 3)
+    return INVALID;
+  const float e = neutral(op);
+  std::map<uint32_t, float> acc;
+  for (int32_t p = 0; p < P; ++p) {
+    if (nnz[p] > cap) return INVALID;
+    for (uint64_t j = 0; j < nnz[p]; ++j) {
+      const uint32_t i = idx[(uint64_t)p * cap + j];
+      if (i >= N) return BAD_STREAM;
+      if (j > 0 && i <= idx[(uint64_t)p * cap + j - 1]) return BAD_STREAM;
+      const float v = val[(uint64_t)p * cap + j];
+      auto it = acc.find(i);
+      if (it == acc.end())
+        acc.emplace(i, fold(op, e, v));
+      else
+        it->second = fold(op, it->second, v);
+    }
+  }
+  const uint64_t U = acc.size();
+  const bool dense = U * (uint64_t)dens_den > N * (uint64_t)dens_num;
+  *out_nnz = U;
+  *out_is_dense = dense ? 1 : 0;
+  if (dense) {
+    for (uint64_t i = 0; i < N; ++i) out_dense[i] = e;
+    for (const auto& kv : acc) out_dense[kv.first] = kv.second;
+  } else {
+    if (U > out_cap) return CAPACITY;
+    uint64_t j = 0;
+    for (const auto& kv : acc) {
       out_idx[j] = kv.first;
       out_val[j] = kv.second;
       ++j;

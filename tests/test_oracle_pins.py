@@ -475,6 +475,88 @@ def test_quantizer_rejects_bucket_not_whole_bytes():
 
 
 # --------------------------------------------------------------------------
+# Other associative reductions with a neutral element (§5.2).
+# --------------------------------------------------------------------------
+NEUTRAL = {"sum": 0.0, "max": -np.inf, "min": np.inf, "or": 0.0}
+
+
+def dense_fold(dense_rows, op):
+    """Fold [P][N] rows over nodes in order with numpy's own elementwise ops."""
+    if op == "or":
+        r = np.bitwise_or.reduce(dense_rows.view(np.uint32), axis=0)
+        return r.view(np.float32)
+    if op == "sum":
+        acc = np.zeros(dense_rows.shape[1], np.float32)
+        for row in dense_rows:
+            acc = acc + row
+        return acc
+    f = np.maximum if op == "max" else np.minimum
+    return f.reduce(dense_rows, axis=0)
+
+
+@pytest.mark.parametrize("op", ["max", "min", "or"])
+@pytest.mark.parametrize("seed", range(3))
+def test_reduce_op_equals_brute_force_dense_fold(op, seed):
+    """Each stream is the vector with the neutral element at unlisted indices;
+    the reduced vector is the elementwise fold, and U the union's size."""
+    rng = np.random.default_rng(100 + seed)
+    P, N = 5, 300
+    k = int(rng.integers(10, 120))
+    idx = np.zeros((P, k), np.uint32)
+    val = rng.standard_normal((P, k)).astype(np.float32)
+    nnz = rng.integers(0, k + 1, size=P).astype(np.uint32)
+    dense = np.full((P, N), NEUTRAL[op], np.float32)
+    union = set()
+    for p in range(P):
+        sel = np.sort(rng.choice(N, size=int(nnz[p]), replace=False)).astype(np.uint32)
+        idx[p, :nnz[p]] = sel
+        dense[p, sel] = val[p, :nnz[p]]
+        union |= set(sel.tolist())
+    want = dense_fold(dense, op)
+    r = oracle.sparse_reduce_op(idx, val, nnz, N, op, 1, 1000)  # forced dense
+    assert r["is_dense"] and r["nnz"] == len(union)
+    assert np.array_equal(r["dense"].view(np.uint32), want.view(np.uint32))
+    r = oracle.sparse_reduce_op(idx, val, nnz, N, op, 1, 1)  # never dense
+    assert np.array_equal(r["idx"], np.array(sorted(union), np.uint32))
+    assert np.array_equal(r["val"].view(np.uint32), want[r["idx"]].view(np.uint32))
+
+
+def test_reduce_op_sum_is_the_sum_reduce_and_idempotent_ops_keep_a_stream():
+    rng = np.random.default_rng(7)
+    P, N, k = 4, 5000, 900
+    idx, val, nnz = (np.zeros((P, k), np.uint32), rng.standard_normal((P, k)).astype(np.float32),
+                     np.full(P, k, np.uint32))
+    for p in range(P):
+        idx[p] = np.sort(rng.choice(N, k, replace=False))
+    a = oracle.sparse_reduce(idx, val, nnz, N, 1, 1)  # sparse output either way
+    b = oracle.sparse_reduce_op(idx, val, nnz, N, "sum", 1, 1)
+    assert a["nnz"] == b["nnz"] and np.array_equal(a["idx"], b["idx"])
+    assert np.array_equal(a["val"].view(np.uint32), b["val"].view(np.uint32))
+    same_i = np.tile(idx[:1], (3, 1))
+    same_v = np.tile(val[:1], (3, 1))
+    for op in ("max", "min", "or"):  # x op x = x: three copies reduce to the stream
+        r = oracle.sparse_reduce_op(same_i, same_v, np.full(3, k, np.uint32), N, op)
+        assert np.array_equal(r["idx"], idx[0])
+        assert np.array_equal(r["val"].view(np.uint32), val[0].view(np.uint32))
+
+
+def test_reduce_op_ties_keep_the_lower_node_and_dense_absent_is_neutral():
+    idx = np.array([[3], [3]], np.uint32)
+    nnz = np.array([1, 1], np.uint32)
+    pz_nz = np.array([[0.0], [-0.0]], np.float32)
+    r = oracle.sparse_reduce_op(idx, pz_nz, nnz, 4, "max", 1, 8)
+    assert r["dense"][3].view(np.uint32) == np.float32(0.0).view(np.uint32)  # +0 kept
+    r = oracle.sparse_reduce_op(idx, pz_nz[::-1].copy(), nnz, 4, "min", 1, 8)
+    assert r["dense"][3].view(np.uint32) == np.float32(-0.0).view(np.uint32)  # -0 kept
+    for op in ("max", "min", "or"):
+        r = oracle.sparse_reduce_op(idx, pz_nz, nnz, 4, op, 1, 8)
+        assert r["is_dense"] and r["nnz"] == 1
+        rest = np.delete(r["dense"], 3)
+        assert np.array_equal(rest.view(np.uint32),
+                              np.full(3, NEUTRAL[op], np.float32).view(np.uint32))
+
+
+# --------------------------------------------------------------------------
 # Pack and densify (§5.1).
 # --------------------------------------------------------------------------
 def test_pack_and_densify_round_trip():
