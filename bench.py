@@ -52,6 +52,8 @@ def parse_args():
                          "qsgd: b-bit quantisation of a dense reduced result")
     ap.add_argument("--bits", type=int, default=4, choices=[2, 4, 8],
                     help="asr / qsgd: width of the quantised codes")
+    ap.add_argument("--op", default="sum", choices=["sum", "max", "min", "or"],
+                    help="sweep / logreg: the reduction (each with its neutral element)")
     ap.add_argument("--sweep-p", type=int, default=64)
     ap.add_argument("--sweep-d", type=float, default=10,
                     help="per-node density in percent: 0.1, 1, 5 or 10")
@@ -382,15 +384,25 @@ def run_reduce_only(args, ranks):
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)  # 256 MB > L2
     K, Wm = args.steps, args.warmup
     evs = [api.make_events(3) for _ in range(K)]
+    def call(i, timed):
+        if args.op == "sum":
+            api.sparse_reduce(di, dv, dn, N, out=out, ws=ws, events=evs[i] if timed else None)
+        else:  # timed as one interval: split + tile + finish
+            if timed:
+                evs[i][0].record()
+            api.sparse_reduce_op(di, dv, dn, N, args.op, out=out, ws=ws)
+            if timed:
+                evs[i][1].record()
+                evs[i][2].record()
+
     for i in range(Wm):
-        api.sparse_reduce(di, dv, dn, N, out=out, ws=ws)
+        call(i, False)
     torch.cuda.synchronize()
     launches0 = api.launch_count()
-    tot = 0.0
     gpu_head_start(K)
     for i in range(K):
         flush.fill_(float(i))  # inputs do not stay in L2 between timed runs
-        api.sparse_reduce(di, dv, dn, N, out=out, ws=ws, events=evs[i])
+        call(i, True)
     torch.cuda.synchronize()
     launches = api.launch_count() - launches0
     if api.get_status(ws) != 0:
@@ -416,7 +428,7 @@ def run_reduce_only(args, ranks):
         "elems_per_s": job_rate(ranks.world, sum_nnz, ms * 1e-3), "n_gpus": ranks.world, "steps": K,
         "warmup": Wm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded numpy index sets)",
-        "config": {"workload": desc, "P": P, "N": N, "sum_nnz": sum_nnz,
+        "config": {"workload": desc, "P": P, "N": N, "sum_nnz": sum_nnz, "op": args.op,
                    "units": "value = 8 B per input entry / (split+tile+fixup time)",
                    "l2": "256 MB buffer written between timed runs (L2 flushed)"},
         "roofline": {"bound": "hbm", "kernel": "reduce split + tile",

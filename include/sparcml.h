@@ -239,6 +239,29 @@ int sparcml_sparse_reduce_traced(const uint32_t* idx, const float* val, const ui
                                  int32_t* out_is_dense, void* ws, size_t ws_bytes, void* stream,
                                  void* const* events);
 
+/* Same reduction with another coordinate-wise associative operation that
+ * has a neutral element (§5.2). A stream stands for the vector holding the
+ * neutral element at its unlisted indices; for every index in the union,
+ *     out[i] = e op v_p0 op v_p1 op ...   (nodes p0 < p1 < ... holding i)
+ * with
+ *     SPARCML_OP_SUM 0  a + b (fp32 RN)                       e = +0.0f
+ *     SPARCML_OP_MAX 1  b if b > a else a (ties keep a)       e = -inf
+ *     SPARCML_OP_MIN 2  b if b < a else a (ties keep a)       e = +inf
+ *     SPARCML_OP_OR  3  bitwise or of the fp32 bit patterns   e = +0.0f
+ * U, the dense switch, layouts and error behaviour as in
+ * sparcml_sparse_reduce; a dense result holds e where no node has the
+ * index. op = SPARCML_OP_SUM is sparcml_sparse_reduce. Another op value:
+ * SPARCML_ERR_INVALID_ARG. */
+#define SPARCML_OP_SUM 0
+#define SPARCML_OP_MAX 1
+#define SPARCML_OP_MIN 2
+#define SPARCML_OP_OR 3
+int sparcml_sparse_reduce_op(const uint32_t* idx, const float* val, const uint32_t* nnz,
+                             int32_t P, uint64_t cap, uint64_t N, int32_t op, uint32_t dens_num,
+                             uint32_t dens_den, uint32_t* out_idx, float* out_val,
+                             uint64_t out_cap, float* out_dense, uint32_t* out_nnz,
+                             int32_t* out_is_dense, void* ws, size_t ws_bytes, void* stream);
+
 /* Same reduction, with each stream's values given in the 4-bit form of
  * sparcml_quantize4 (codes, scales, bucket) and decoded on load exactly as
  * sparcml_dequantize4 does. Bit-identical to dequantize4 followed by

@@ -106,6 +106,8 @@ def test_reduce_and_other_host_validation():
     ws = lib.sparcml_sparse_reduce_workspace_size(2, 1000)
     assert lib.sparcml_sparse_reduce_qb(FAKE, FAKE, FAKE, FAKE, 2, 10, 6, 2, 1000, 1, 4, FAKE,
                                         FAKE, 250, FAKE, FAKE, FAKE, FAKE, ws, None) == 1
+    assert lib.sparcml_sparse_reduce_op(FAKE, FAKE, FAKE, 2, 10, 1000, 4, 1, 4, FAKE, FAKE, 250,
+                                        FAKE, FAKE, FAKE, FAKE, ws, None) == 1  # unknown op
 
 
 def test_segment_k_total_matches_the_oracle_rule():

@@ -50,6 +50,9 @@ SIGNATURES = {
     "sparcml_sparse_reduce_traced": (C.c_int, [vp, vp, vp, C.c_int32, C.c_uint64, C.c_uint64,
                                                C.c_uint32, C.c_uint32, vp, vp, C.c_uint64, vp,
                                                vp, vp, vp, C.c_size_t, vp, vp]),
+    "sparcml_sparse_reduce_op": (C.c_int, [vp, vp, vp, C.c_int32, C.c_uint64, C.c_uint64,
+                                           C.c_int32, C.c_uint32, C.c_uint32, vp, vp, C.c_uint64,
+                                           vp, vp, vp, vp, C.c_size_t, vp]),
     "sparcml_sparse_reduce_q4": (C.c_int, [vp, vp, vp, vp, C.c_int32, C.c_uint64, C.c_uint32,
                                            C.c_uint64, C.c_uint32, C.c_uint32, vp, vp,
                                            C.c_uint64, vp, vp, vp, vp, C.c_size_t, vp]),

@@ -303,6 +303,26 @@ def sparse_reduce_q4(idx, codes, scales, nnz, bucket: int, N: int, dens_num: int
     return out
 
 
+OPS = {"sum": 0, "max": 1, "min": 2, "or": 3}
+
+
+def sparse_reduce_op(idx, val, nnz, N: int, op: str, dens_num: int = 1, dens_den: int = 4,
+                     out: ReduceOut | None = None, ws=None, stream=None) -> ReduceOut:
+    """Reduction with sum, max, min or bitwise or (§5.2), neutral element at
+    unlisted indices; same outputs as sparse_reduce."""
+    P, cap = idx.shape
+    if out is None:
+        out = reduce_out(N, idx.device, dens_num, dens_den)
+    if ws is None:
+        ws = workspace(reduce_workspace_size(P, N), idx.device)
+    oi, ov, ocap, od, on, odn = _reduce_out_ptrs(out)
+    _check("sparcml_sparse_reduce_op", _lib.load().sparcml_sparse_reduce_op(
+        _cuda(idx, torch.int32, "idx", 2), _cuda(val, torch.float32, "val", 2),
+        _cuda(nnz, torch.int32, "nnz", 1), P, cap, N, OPS[op], dens_num, dens_den, oi, ov, ocap,
+        od, on, odn, ws.data_ptr(), ws.numel(), _stream(stream)))
+    return out
+
+
 def sparse_reduce_qb(idx, codes, scales, nnz, bucket: int, bits: int, N: int, dens_num: int = 1,
                      dens_den: int = 4, out: ReduceOut | None = None, ws=None,
                      stream=None) -> ReduceOut:

@@ -58,6 +58,7 @@ struct ReduceArgs {
   uint32_t bucket;
   uint32_t bucket_shift;  // log2(bucket) when a power of two, else 32
   uint32_t bits;          // width of the quantised codes: 2, 4 or 8
+  int32_t op;             // kOpSum, kOpMax, kOpMin or kOpOr
   int32_t P;
   uint32_t N;
   uint32_t ntiles;
@@ -84,6 +85,26 @@ __device__ __forceinline__ uint32_t lower_bound_u32(const uint32_t* a, uint32_t 
     if (a[mid] < x) lo = mid + 1; else hi = mid;
   }
   return lo;
+}
+
+// The reduction (§5.2: any coordinate-wise associative operation with a
+// neutral element): a stream stands for the vector holding the neutral
+// element at unlisted indices; an index's result folds its nodes' values in
+// ascending node order starting from the neutral element.
+enum : int32_t { kOpSum = 0, kOpMax = 1, kOpMin = 2, kOpOr = 3 };
+
+__device__ __forceinline__ float op_neutral(int32_t op) {
+  return op == kOpMax ? -INFINITY : op == kOpMin ? INFINITY : 0.0f;
+}
+
+// The fold of one value into a partial result. max/min take the new value
+// only when it is strictly greater / smaller (ties keep the lower node's); or
+// works on the fp32 bit patterns. op is the same for the whole launch.
+__device__ __forceinline__ float op_fold(int32_t op, float acc, float v) {
+  if (op == kOpSum) return __fadd_rn(acc, v);
+  if (op == kOpMax) return v > acc ? v : acc;
+  if (op == kOpMin) return v < acc ? v : acc;
+  return __uint_as_float(__float_as_uint(acc) | __float_as_uint(v));
 }
 
 // level / 7 for a 4-bit level 1..7: the correctly rounded fp32 quotient (the
@@ -224,8 +245,9 @@ reduce_tile_kernel(ReduceArgs a) {
     bc[0] = atomicAdd(a.ticket, 1u);
     bc[1] = 0;
   }
+  const float e = op_neutral(a.op);  // +0.0f for the sum
   for (uint32_t w = t; w < kTile / 4; w += blockDim.x)
-    reinterpret_cast<float4*>(acc)[w] = make_float4(0.f, 0.f, 0.f, 0.f);
+    reinterpret_cast<float4*>(acc)[w] = make_float4(e, e, e, e);
   for (uint32_t w = t; w < kWords; w += blockDim.x) bm[w] = 0;
   __syncthreads();
   const uint32_t tile = bc[0];
@@ -395,10 +417,11 @@ constexpr uint32_t kStages = 4;
 constexpr uint32_t kStageEntries = 1024;
 constexpr uint32_t kNoPrev = 0xffffffffu;
 
-template <bool Q4, bool DENSE_FIRST>
+template <bool Q4, bool DENSE_FIRST, bool ANY>
 __global__ void __launch_bounds__(kReduceThreads)
 reduce_dense_tile_kernel(ReduceArgs a) {
   extern __shared__ __align__(16) uint32_t dyn[];
+  const int32_t kop = ANY ? a.op : kOpSum;  // sum-only launches fold the branch away
   float* acc = reinterpret_cast<float*>(dyn);                       // [kTile]
   uint32_t* bm = dyn + kTile;                                        // [kWords]
   uint32_t* sidx = bm + kWords;                                      // [kStages][kStageEntries]
@@ -415,8 +438,9 @@ reduce_dense_tile_kernel(ReduceArgs a) {
     bc[0] = atomicAdd(a.ticket, 1u);
     bc[1] = 0;
   }
+  const float e = op_neutral(kop);  // +0.0f for the sum
   for (uint32_t w = t; w < kTile / 4; w += blockDim.x)
-    reinterpret_cast<float4*>(acc)[w] = make_float4(0.f, 0.f, 0.f, 0.f);
+    reinterpret_cast<float4*>(acc)[w] = make_float4(e, e, e, e);
   for (uint32_t w = t; w < kWords; w += blockDim.x) bm[w] = 0;
   __syncthreads();
   const uint32_t tile = bc[0];
@@ -502,7 +526,7 @@ reduce_dense_tile_kernel(ReduceArgs a) {
         float v;
         if constexpr (Q4) v = load_value<Q4>(a, p, j);
         else v = sval[st * kStageEntries + e];
-        acc[off] = __fadd_rn(acc[off], v);
+        acc[off] = op_fold(kop, acc[off], v);
         atomicOr(&bm[off >> 5], 1u << (off & 31));
       } else {
         set_status(a.status, SPARCML_ERR_BAD_STREAM);
@@ -852,7 +876,7 @@ __device__ __forceinline__ void mini_epilogue_lookback(const ReduceArgs& a, uint
   if (dense) {
     float* od = a.out_dense + tile_lo;
     for (uint32_t x = lane; x < tile_n; x += 32)
-      od[x] = acc[x] == kAbsent ? 0.0f : __uint_as_float(acc[x]);
+      od[x] = acc[x] == kAbsent ? op_neutral(a.op) : __uint_as_float(acc[x]);
   } else {
     uint32_t pos = excl + wincl - __popc(word);  // entries before word `lane`
     uint32_t bits = word;
@@ -888,7 +912,8 @@ __device__ __forceinline__ void mini_epilogue(const ReduceArgs& a, uint32_t m, c
   }
   const uint32_t count = warp_sum(__popc(word));
   float* od = a.out_dense + tile_lo;
-  auto fix = [](uint32_t b) { return b == kAbsent ? 0.0f : __uint_as_float(b); };
+  const float e = op_neutral(a.op);
+  auto fix = [e](uint32_t b) { return b == kAbsent ? e : __uint_as_float(b); };
   if (tile_n == kMini && (reinterpret_cast<uintptr_t>(od) & 15) == 0) {
 #pragma unroll
     for (uint32_t i = 0; i < kMini / 128; ++i) {
@@ -914,10 +939,11 @@ __device__ __forceinline__ uint32_t mini_tile_of_warp(const ReduceArgs& a, bool 
   return m;
 }
 
-template <bool Q4, bool LB>
+template <bool Q4, bool LB, bool ANY>
 __global__ void __launch_bounds__(kMiniWarps * 32)
 reduce_mini_kernel(ReduceArgs a) {
   extern __shared__ __align__(16) uint32_t dyn[];
+  const int32_t kop = ANY ? a.op : kOpSum;  // sum-only launches fold the branch away
   const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
   __shared__ uint32_t sh[kMiniWarps + 1];
   const uint32_t m = mini_tile_of_warp(a, LB, sh);
@@ -930,8 +956,11 @@ reduce_mini_kernel(ReduceArgs a) {
   uint32_t* cpre = lo + kMiniMaxP;                     // [P + 1] first position
   const uint32_t tile_lo = m * kMini;
   const uint32_t tile_n = min(kMini, a.N - tile_lo);
-  // Absent indices hold kAbsent, a NaN that fp32 arithmetic never returns
-  // (the GPU's NaN results are 0x7fffffff): presence needs no bitmap.
+  const float e = op_neutral(kop);
+  // Absent indices hold kAbsent, a NaN that neither the sum (the GPU's NaN
+  // results are 0x7fffffff) nor max/min (a NaN value never replaces the
+  // partial result) ever leaves there: presence needs no bitmap. Bitwise or
+  // can produce any pattern and is not run here.
 #pragma unroll
   for (uint32_t i = 0; i < kMini / 128; ++i)
     reinterpret_cast<uint4*>(acc)[i * 32 + lane] = make_uint4(kAbsent, kAbsent, kAbsent, kAbsent);
@@ -999,7 +1028,7 @@ reduce_mini_kernel(ReduceArgs a) {
       if (__all_sync(0xffffffffu, pn[u] == first || !live)) {  // one node: distinct indices
         if (mine) {
           const uint32_t old = acc[off];
-          acc[off] = __float_as_uint(__fadd_rn(old == kAbsent ? 0.0f : __uint_as_float(old), vx[u]));
+          acc[off] = __float_as_uint(op_fold(kop, old == kAbsent ? e : __uint_as_float(old), vx[u]));
         }
       } else {
         const uint32_t last = __reduce_max_sync(0xffffffffu, live ? pn[u] : 0u);
@@ -1007,7 +1036,7 @@ reduce_mini_kernel(ReduceArgs a) {
           if (mine && pn[u] == q) {
             const uint32_t old = acc[off];
             acc[off] =
-                __float_as_uint(__fadd_rn(old == kAbsent ? 0.0f : __uint_as_float(old), vx[u]));
+                __float_as_uint(op_fold(kop, old == kAbsent ? e : __uint_as_float(old), vx[u]));
           }
           __syncwarp();
         }
@@ -1028,10 +1057,11 @@ reduce_mini_kernel(ReduceArgs a) {
 // node at a time, in ascending order.
 constexpr uint32_t kQuadRounds = 4;
 
-template <bool LB>
+template <bool LB, bool ANY>
 __global__ void __launch_bounds__(kMiniWarps * 32)
 reduce_mini_quad_kernel(ReduceArgs a) {
   extern __shared__ __align__(16) uint32_t dyn[];
+  const int32_t kop = ANY ? a.op : kOpSum;  // sum-only launches fold the branch away
   const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
   __shared__ uint32_t sh[kMiniWarps + 1];
   const uint32_t m = mini_tile_of_warp(a, LB, sh);
@@ -1045,6 +1075,7 @@ reduce_mini_quad_kernel(ReduceArgs a) {
   uint32_t* hi = qpre + kMiniMaxP + 1;                 // [P] end entry in the tile
   const uint32_t tile_lo = m * kMini;
   const uint32_t tile_n = min(kMini, a.N - tile_lo);
+  const float e = op_neutral(kop);
 #pragma unroll
   for (uint32_t i = 0; i < kMini / 128; ++i)
     reinterpret_cast<uint4*>(acc)[i * 32 + lane] = make_uint4(kAbsent, kAbsent, kAbsent, kAbsent);
@@ -1127,7 +1158,7 @@ reduce_mini_quad_kernel(ReduceArgs a) {
       const uint32_t off = iv - tile_lo;
       if (off < tile_n) {
         const uint32_t old = acc[off];
-        acc[off] = __float_as_uint(__fadd_rn(old == kAbsent ? 0.0f : __uint_as_float(old), v));
+        acc[off] = __float_as_uint(op_fold(kop, old == kAbsent ? e : __uint_as_float(old), v));
       }
     };
     auto add_quad = [&](uint32_t u) {
@@ -1254,10 +1285,11 @@ constexpr uint32_t kMaxTileW = 1u << 17;
 constexpr uint32_t kAccCap = 8192;
 constexpr int32_t kMaxSparseP = 1024;
 
-template <bool Q4>
+template <bool Q4, bool ANY>
 __global__ void __launch_bounds__(kReduceThreads)
 reduce_sparse_tile_kernel(ReduceArgs a) {
   extern __shared__ __align__(16) uint32_t dyn[];
+  const int32_t kop = ANY ? a.op : kOpSum;  // sum-only launches fold the branch away
   const uint32_t W = a.tile_w / 32;
   uint32_t* bm = dyn;                                    // [W] presence bits
   uint32_t* woff = bm + W;                               // [W] slots before each word
@@ -1390,7 +1422,7 @@ reduce_sparse_tile_kernel(ReduceArgs a) {
   // 4. accumulate and emit, slot window by slot window
   for (uint32_t s0 = 0; s0 < U || (s0 == 0 && dense); s0 += kAccCap) {
     const uint32_t win = min(kAccCap, U - min(U, s0));
-    for (uint32_t i = t; i < win; i += blockDim.x) acc[i] = 0.0f;
+    for (uint32_t i = t; i < win; i += blockDim.x) acc[i] = op_neutral(kop);
     __syncthreads();
     for (uint32_t c0 = 0; c0 < E; c0 += batch) {
       if (!resident) load_batch(c0);
@@ -1403,7 +1435,7 @@ reduce_sparse_tile_kernel(ReduceArgs a) {
           if (pv[u] == p) {
             const uint32_t off = iv[u] - tile_lo, w = off >> 5;
             const uint32_t slot = woff[w] + __popc(bm[w] & ((1u << (off & 31)) - 1u));
-            if (slot - s0 < win) acc[slot - s0] = __fadd_rn(acc[slot - s0], vv[u]);
+            if (slot - s0 < win) acc[slot - s0] = op_fold(kop, acc[slot - s0], vv[u]);
           }
         }
         __syncthreads();
@@ -1419,7 +1451,7 @@ reduce_sparse_tile_kernel(ReduceArgs a) {
           const uint32_t slot = woff[w] + __popc(bm[w] & (bit - 1u));
           if (slot - s0 < win) od[x] = acc[slot - s0];
         } else if (s0 == 0) {
-          od[x] = 0.0f;
+          od[x] = op_neutral(kop);
         }
       }
     } else {
@@ -1452,14 +1484,15 @@ reduce_sparse_tile_kernel(ReduceArgs a) {
 __global__ void __launch_bounds__(256)
 reduce_fixup_kernel(const int32_t* __restrict__ is_dense, const uint2* __restrict__ tile_info,
                     const uint32_t* __restrict__ out_idx, const float* __restrict__ out_val,
-                    float* __restrict__ out_dense, uint32_t N, uint32_t tile_w, uint32_t ntiles) {
+                    float* __restrict__ out_dense, uint32_t N, uint32_t tile_w, uint32_t ntiles,
+                    float neutral) {
   if (*is_dense == 0) return;
   for (uint32_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {  // block-uniform
     const uint2 info = tile_info[tile];
     if (info.y & 0x80000000u) continue;
     const uint32_t tile_lo = tile * tile_w;
     const uint32_t tile_n = min(tile_w, N - tile_lo);
-    for (uint32_t x = threadIdx.x; x < tile_n; x += blockDim.x) out_dense[tile_lo + x] = 0.0f;
+    for (uint32_t x = threadIdx.x; x < tile_n; x += blockDim.x) out_dense[tile_lo + x] = neutral;
     __syncthreads();
     for (uint32_t e = threadIdx.x; e < info.y; e += blockDim.x) {
       const uint32_t i = out_idx[info.x + e];
@@ -1516,7 +1549,8 @@ int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
   const double est = (double)a.P * (double)a.cap * kTile / (double)a.N;
   uint32_t tile_w = kTile;
   // Few nodes covering at least N/16 indices: one warp per kMini-index tile.
-  const bool mini = a.P <= kMiniMaxP && 16.0 * (double)a.P * (double)a.cap >= (double)a.N;
+  const bool mini = a.P <= kMiniMaxP && 16.0 * (double)a.P * (double)a.cap >= (double)a.N &&
+                    a.op != kOpOr;  // warp tiles mark absent indices with a NaN pattern
   const bool sparse = !mini && a.P <= kMaxSparseP && est <= 2048.0;
   if (sparse) {
     while (tile_w < kMaxTileW && est * (2.0 * tile_w / kTile) <= 2048.0 && tile_w < a.N)
@@ -1547,24 +1581,26 @@ int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
     // A possibly dense result (P * cap >= N / 4) is written dense-first; else
     // sparse-first with look-back and a fix-up if the union crosses after all.
     const bool lb = 4.0 * (double)a.P * (double)a.cap < (double)a.N;
-    const void* fn;
-    if (vec) fn = lb ? reinterpret_cast<const void*>(reduce_mini_quad_kernel<true>)
-                     : reinterpret_cast<const void*>(reduce_mini_quad_kernel<false>);
-    else fn = lb ? reinterpret_cast<const void*>(reduce_mini_kernel<Q4, true>)
-                 : reinterpret_cast<const void*>(reduce_mini_kernel<Q4, false>);
-    if (!ensure_smem(fn, smem)) return SPARCML_ERR_CUDA;
-    if (vec) {
-      if (lb) reduce_mini_quad_kernel<true><<<grid, kMiniWarps * 32, smem, s>>>(a);
-      else reduce_mini_quad_kernel<false><<<grid, kMiniWarps * 32, smem, s>>>(a);
-    } else {
-      if (lb) reduce_mini_kernel<Q4, true><<<grid, kMiniWarps * 32, smem, s>>>(a);
-      else reduce_mini_kernel<Q4, false><<<grid, kMiniWarps * 32, smem, s>>>(a);
-    }
+    const bool any = a.op != kOpSum;
+    auto go = [&](auto kernel) {
+      if (!ensure_smem(reinterpret_cast<const void*>(kernel), smem)) return false;
+      kernel<<<grid, kMiniWarps * 32, smem, s>>>(a);
+      return true;
+    };
+    bool ok;
+    if (vec)
+      ok = lb ? (any ? go(reduce_mini_quad_kernel<true, true>) : go(reduce_mini_quad_kernel<true, false>))
+              : (any ? go(reduce_mini_quad_kernel<false, true>) : go(reduce_mini_quad_kernel<false, false>));
+    else
+      ok = lb ? (any ? go(reduce_mini_kernel<Q4, true, true>) : go(reduce_mini_kernel<Q4, true, false>))
+              : (any ? go(reduce_mini_kernel<Q4, false, true>) : go(reduce_mini_kernel<Q4, false, false>));
+    if (!ok) return SPARCML_ERR_CUDA;
     if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
     mark(1);
     if (lb) {
       reduce_fixup_kernel<<<fixup_grid(a.ntiles), 256, 0, s>>>(a.out_is_dense, a.tile_info, a.out_idx,
-                                                   a.out_val, a.out_dense, a.N, a.tile_w, a.ntiles);
+                                                   a.out_val, a.out_dense, a.N, a.tile_w, a.ntiles,
+        a.op == kOpMax ? -INFINITY : a.op == kOpMin ? INFINITY : 0.0f);
       if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
       mark(2);
       note_launches(3);
@@ -1584,17 +1620,27 @@ int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
   if (sparse) {
     const size_t smem =
         (2 * (size_t)(tile_w / 32) + kAccCap + 2 * (size_t)a.P + 1) * sizeof(uint32_t);
-    if (!ensure_smem(reinterpret_cast<const void*>(reduce_sparse_tile_kernel<Q4>), smem))
+    auto go = [&](auto kernel) {
+      if (!ensure_smem(reinterpret_cast<const void*>(kernel), smem)) return false;
+      kernel<<<a.ntiles, kReduceThreads, smem, s>>>(a);
+      return true;
+    };
+    if (!(a.op != kOpSum ? go(reduce_sparse_tile_kernel<Q4, true>)
+                         : go(reduce_sparse_tile_kernel<Q4, false>)))
       return SPARCML_ERR_CUDA;
-    reduce_sparse_tile_kernel<Q4><<<a.ntiles, kReduceThreads, smem, s>>>(a);
   } else {
     const size_t smem = (kTile + kWords + 2 * kStages * kStageEntries + 3 * (size_t)a.P + 1) *
                         sizeof(uint32_t);
+    auto go_dense = [&](auto kernel) {
+      if (!ensure_smem(reinterpret_cast<const void*>(kernel), smem)) return false;
+      kernel<<<a.ntiles, kReduceThreads, smem, s>>>(a);
+      return true;
+    };
     if ((double)a.P * (double)a.cap >= (double)a.N) {
       // dense-first: no look-back; U and the flag come from the finalize pass
-      if (!ensure_smem(reinterpret_cast<const void*>(reduce_dense_tile_kernel<Q4, true>), smem))
+      if (!(a.op != kOpSum ? go_dense(reduce_dense_tile_kernel<Q4, true, true>)
+                           : go_dense(reduce_dense_tile_kernel<Q4, true, false>)))
         return SPARCML_ERR_CUDA;
-      reduce_dense_tile_kernel<Q4, true><<<a.ntiles, kReduceThreads, smem, s>>>(a);
       if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
       mark(1);
       reduce_finalize_kernel<<<1, 1024, 0, s>>>(a.tile_info, a.ntiles, a.cap_sparse, a.out_nnz,
@@ -1606,14 +1652,15 @@ int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
       note_launches(4);
       return SPARCML_OK;
     }
-    if (!ensure_smem(reinterpret_cast<const void*>(reduce_dense_tile_kernel<Q4, false>), smem))
+    if (!(a.op != kOpSum ? go_dense(reduce_dense_tile_kernel<Q4, false, true>)
+                         : go_dense(reduce_dense_tile_kernel<Q4, false, false>)))
       return SPARCML_ERR_CUDA;
-    reduce_dense_tile_kernel<Q4, false><<<a.ntiles, kReduceThreads, smem, s>>>(a);
   }
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   mark(1);
   reduce_fixup_kernel<<<fixup_grid(a.ntiles), 256, 0, s>>>(a.out_is_dense, a.tile_info, a.out_idx,
-                                               a.out_val, a.out_dense, a.N, a.tile_w, a.ntiles);
+                                               a.out_val, a.out_dense, a.N, a.tile_w, a.ntiles,
+        a.op == kOpMax ? -INFINITY : a.op == kOpMin ? INFINITY : 0.0f);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   mark(2);
   note_launches(3);
@@ -1644,18 +1691,19 @@ extern "C" size_t sparcml_sparse_reduce_workspace_size(int32_t P, uint64_t N) {
   return reduce_layout(P, N).total;
 }
 
-extern "C" int sparcml_sparse_reduce_traced(const uint32_t* idx, const float* val,
-                                            const uint32_t* nnz, int32_t P, uint64_t cap,
-                                            uint64_t N, uint32_t dens_num, uint32_t dens_den,
-                                            uint32_t* out_idx, float* out_val, uint64_t out_cap,
-                                            float* out_dense, uint32_t* out_nnz,
-                                            int32_t* out_is_dense, void* ws, size_t ws_bytes,
-                                            void* stream, void* const* events) {
+namespace sparcml {
+namespace {
+int reduce_fp32(const uint32_t* idx, const float* val, const uint32_t* nnz, int32_t P,
+                uint64_t cap, uint64_t N, int32_t op, uint32_t dens_num, uint32_t dens_den,
+                uint32_t* out_idx, float* out_val, uint64_t out_cap, float* out_dense,
+                uint32_t* out_nnz, int32_t* out_is_dense, void* ws, size_t ws_bytes,
+                void* stream, void* const* events) {
   const int st = check_reduce_args(idx, nnz, P, cap, N, dens_num, dens_den, out_idx, out_val,
                                    out_cap, out_dense, out_nnz, out_is_dense, ws);
   if (st != SPARCML_OK) return st;
-  if (!val) return SPARCML_ERR_INVALID_ARG;
+  if (!val || op < kOpSum || op > kOpOr) return SPARCML_ERR_INVALID_ARG;
   ReduceArgs a = {};
+  a.op = op;
   a.idx = idx;
   a.val = val;
   a.nnz = nnz;
@@ -1670,6 +1718,30 @@ extern "C" int sparcml_sparse_reduce_traced(const uint32_t* idx, const float* va
   a.out_nnz = out_nnz;
   a.out_is_dense = out_is_dense;
   return launch_reduce<false>(a, ws, ws_bytes, static_cast<cudaStream_t>(stream), events);
+}
+}  // namespace
+}  // namespace sparcml
+
+extern "C" int sparcml_sparse_reduce_traced(const uint32_t* idx, const float* val,
+                                            const uint32_t* nnz, int32_t P, uint64_t cap,
+                                            uint64_t N, uint32_t dens_num, uint32_t dens_den,
+                                            uint32_t* out_idx, float* out_val, uint64_t out_cap,
+                                            float* out_dense, uint32_t* out_nnz,
+                                            int32_t* out_is_dense, void* ws, size_t ws_bytes,
+                                            void* stream, void* const* events) {
+  return reduce_fp32(idx, val, nnz, P, cap, N, kOpSum, dens_num, dens_den, out_idx, out_val,
+                     out_cap, out_dense, out_nnz, out_is_dense, ws, ws_bytes, stream, events);
+}
+
+extern "C" int sparcml_sparse_reduce_op(const uint32_t* idx, const float* val,
+                                        const uint32_t* nnz, int32_t P, uint64_t cap, uint64_t N,
+                                        int32_t op, uint32_t dens_num, uint32_t dens_den,
+                                        uint32_t* out_idx, float* out_val, uint64_t out_cap,
+                                        float* out_dense, uint32_t* out_nnz,
+                                        int32_t* out_is_dense, void* ws, size_t ws_bytes,
+                                        void* stream) {
+  return reduce_fp32(idx, val, nnz, P, cap, N, op, dens_num, dens_den, out_idx, out_val,
+                     out_cap, out_dense, out_nnz, out_is_dense, ws, ws_bytes, stream, nullptr);
 }
 
 extern "C" int sparcml_sparse_reduce(const uint32_t* idx, const float* val, const uint32_t* nnz,
@@ -1845,7 +1917,8 @@ extern "C" int sparcml_sparse_reduce_noalloc(const uint32_t* idx, const float* v
   reduce_tile_kernel<false><<<a.ntiles, kReduceThreads, smem, s>>>(a);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   reduce_fixup_kernel<<<fixup_grid(a.ntiles), 256, 0, s>>>(a.out_is_dense, a.tile_info, a.out_idx,
-                                               a.out_val, a.out_dense, a.N, a.tile_w, a.ntiles);
+                                               a.out_val, a.out_dense, a.N, a.tile_w, a.ntiles,
+        a.op == kOpMax ? -INFINITY : a.op == kOpMin ? INFINITY : 0.0f);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   note_launches(2);
   return SPARCML_OK;
