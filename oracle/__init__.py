@@ -66,6 +66,9 @@ def _load():
                                                     C.c_uint64, C.c_int32, C.c_uint32,
                                                     C.c_uint32, u32p, f32p, C.c_uint64, f32p,
                                                     C.POINTER(C.c_uint64), C.POINTER(C.c_int32)]
+            u64p = np.ctypeslib.ndpointer(dtype=np.uint64, flags="C_CONTIGUOUS")
+            lib.oracle_ssar.argtypes = [u32p, f32p, u32p, C.c_int32, C.c_uint64, C.c_uint64,
+                                        u32p, f32p, C.c_uint64, C.POINTER(C.c_uint64), u64p]
             lib.oracle_densify.argtypes = [u32p, f32p, u32p, C.c_int32, C.c_uint64, C.c_uint64,
                                            f32p]
             for f in ("oracle_topk_ef", "oracle_pack", "oracle_quantize4", "oracle_dequantize4",
@@ -219,6 +222,22 @@ def sparse_reduce_op(idx, val, nnz, N, op, dens_num=1, dens_den=4):
     if d.value:
         return dict(nnz=U, is_dense=True, idx=None, val=None, dense=od)
     return dict(nnz=U, is_dense=False, idx=oi[:U].copy(), val=ov[:U].copy(), dense=None)
+
+
+def ssar(idx, val, nnz, N):
+    """Static sparse allreduce by recursive doubling (SparCML §5.3.1): log2(P)
+    stages of pairwise two-stream sum reduces. Returns (idx, val, stage_nnz)."""
+    idx, val, nnz = _u32(idx), _f32(val), _u32(nnz)
+    P, cap = idx.shape
+    out_cap = int(min(N, P * cap))
+    oi = np.zeros(max(out_cap, 1), np.uint32)
+    ov = np.zeros(max(out_cap, 1), np.float32)
+    stages = np.zeros(max(P.bit_length() - 1, 1), np.uint64)
+    u = C.c_uint64(0)
+    _check("oracle_ssar", _load().oracle_ssar(idx, val, nnz, P, cap, N, oi, ov, out_cap,
+                                              C.byref(u), stages))
+    U = int(u.value)
+    return oi[:U].copy(), ov[:U].copy(), stages[:P.bit_length() - 1].copy()
 
 
 def sparse_reduce(idx, val, nnz, N, dens_num=1, dens_den=4):

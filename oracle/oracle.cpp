@@ -444,6 +444,64 @@ int oracle_sparse_reduce_op(const uint32_t* idx, const float* val, const uint32_
   return OK;
 }
 
+// Static sparse allreduce by recursive doubling (SSAR, §5.3.1), emulated on
+// one host: at stage s = 0 .. log2(P) - 1 every node i combines its current
+// sparse partial result with the one of node i XOR 2^s; both obtain the same
+// result, so a stage keeps one result per group of 2^(s+1) nodes. Combining
+// two partial results A (lower group) and B is the two-stream sum reduce:
+// for every index of A ∪ B, (+0.0f + a) + b, or +0.0f + the single value.
+// The result never switches to dense (static sparse). out gets the final
+// result (ascending, out_nnz entries); stage_nnz[s] the total number of
+// entries held after stage s over the distinct partial results (fill-in).
+// P must be a power of two >= 2.
+int oracle_ssar(const uint32_t* idx, const float* val, const uint32_t* nnz, int32_t P,
+                uint64_t cap, uint64_t N, uint32_t* out_idx, float* out_val, uint64_t out_cap,
+                uint64_t* out_nnz, uint64_t* stage_nnz) {
+  if (P < 2 || (P & (P - 1)) != 0 || N == 0 || N > 0xffffffffULL) return INVALID;
+  std::vector<std::map<uint32_t, float>> part((size_t)P);
+  for (int32_t p = 0; p < P; ++p) {
+    if (nnz[p] > cap) return INVALID;
+    for (uint64_t j = 0; j < nnz[p]; ++j) {
+      const uint32_t i = idx[(uint64_t)p * cap + j];
+      if (i >= N) return BAD_STREAM;
+      if (j > 0 && i <= idx[(uint64_t)p * cap + j - 1]) return BAD_STREAM;
+      part[(size_t)p].emplace(i, val[(uint64_t)p * cap + j]);
+    }
+  }
+  // group g of a stage holds the partial result of nodes [g * 2^s, (g + 1) * 2^s)
+  int stage = 0;
+  while (part.size() > 1) {
+    std::vector<std::map<uint32_t, float>> next(part.size() / 2);
+    uint64_t fill = 0;
+    for (size_t g = 0; g < next.size(); ++g) {
+      const auto& A = part[2 * g];
+      const auto& B = part[2 * g + 1];
+      auto& C = next[g];
+      for (const auto& kv : A) C.emplace(kv.first, 0.0f + kv.second);
+      for (const auto& kv : B) {
+        auto it = C.find(kv.first);
+        if (it == C.end())
+          C.emplace(kv.first, 0.0f + kv.second);
+        else
+          it->second = it->second + kv.second;
+      }
+      fill += C.size();
+    }
+    stage_nnz[stage++] = fill;
+    part.swap(next);
+  }
+  const auto& R = part[0];
+  *out_nnz = R.size();
+  if (R.size() > out_cap) return CAPACITY;
+  uint64_t j = 0;
+  for (const auto& kv : R) {
+    out_idx[j] = kv.first;
+    out_val[j] = kv.second;
+    ++j;
+  }
+  return OK;
+}
+
 // Scatter each node's stream into a dense [P][N] vector, +0.0f elsewhere.
 int oracle_densify(const uint32_t* idx, const float* val, const uint32_t* nnz, int32_t P,
                    uint64_t cap, uint64_t N, float* dense) {

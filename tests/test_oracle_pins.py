@@ -557,6 +557,64 @@ def test_reduce_op_ties_keep_the_lower_node_and_dense_absent_is_neutral():
 
 
 # --------------------------------------------------------------------------
+# Static sparse allreduce by recursive doubling (§5.3.1).
+# --------------------------------------------------------------------------
+def disjoint_or_same(P, k, N, same, rng):
+    if same:
+        base = np.sort(rng.choice(N, k, replace=False)).astype(np.uint32)
+        idx = np.tile(base, (P, 1))
+    else:
+        perm = rng.permutation(N)[:P * k].reshape(P, k)
+        idx = np.sort(perm, axis=1).astype(np.uint32)
+    return idx, rng.standard_normal((P, k)).astype(np.float32), np.full(P, k, np.uint32)
+
+
+@pytest.mark.parametrize("P", [2, 4, 8, 16])
+def test_ssar_fill_in_identical_and_disjoint_sets(P):
+    """§5.3.1: fully overlapping indices keep every intermediate result at k
+    items; disjoint indices double them at each stage (App. B: union of
+    disjoint sets = sum of sizes)."""
+    rng = np.random.default_rng(P)
+    k, N = 300, 100_000
+    stages = P.bit_length() - 1
+    idx, val, nnz = disjoint_or_same(P, k, N, True, rng)
+    _, _, fill = oracle.ssar(idx, val, nnz, N)
+    assert fill.tolist() == [(P >> (s + 1)) * k for s in range(stages)]
+    idx, val, nnz = disjoint_or_same(P, k, N, False, rng)
+    oi, _, fill = oracle.ssar(idx, val, nnz, N)
+    assert fill.tolist() == [P * k] * stages
+    assert np.array_equal(oi, np.sort(idx.reshape(-1)))
+
+
+@pytest.mark.parametrize("P", [2, 8, 32])
+def test_ssar_equals_the_sequential_reduce_when_sums_are_exact(P):
+    """With small integer values every sum is exact, so the recursive-doubling
+    order gives the sequential reduce's result bit for bit; with P = 2 it is
+    that reduce for any values."""
+    rng = np.random.default_rng(40 + P)
+    N, k = 5000, 700
+    idx = np.zeros((P, k), np.uint32)
+    for p in range(P):
+        idx[p] = np.sort(rng.choice(N, k, replace=False))
+    val = rng.integers(-1000, 1000, size=(P, k)).astype(np.float32)
+    nnz = rng.integers(0, k + 1, size=P).astype(np.uint32)
+    oi, ov, _ = oracle.ssar(idx, val, nnz, N)
+    ref = oracle.sparse_reduce(idx, val, nnz, N, 1, 1)
+    assert np.array_equal(oi, ref["idx"]) and np.array_equal(ov.view(np.uint32), ref["val"].view(np.uint32))
+    if P == 2:
+        val2 = rng.standard_normal((2, k)).astype(np.float32)
+        oi, ov, _ = oracle.ssar(idx, val2, nnz, N)
+        ref = oracle.sparse_reduce(idx, val2, nnz, N, 1, 1)
+        assert np.array_equal(ov.view(np.uint32), ref["val"].view(np.uint32))
+
+
+def test_ssar_needs_a_power_of_two():
+    with pytest.raises(RuntimeError):
+        oracle.ssar(np.zeros((3, 1), np.uint32), np.zeros((3, 1), np.float32),
+                    np.zeros(3, np.uint32), 10)
+
+
+# --------------------------------------------------------------------------
 # Pack and densify (§5.1).
 # --------------------------------------------------------------------------
 def test_pack_and_densify_round_trip():
