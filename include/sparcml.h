@@ -285,6 +285,39 @@ int sparcml_sparse_reduce_qb(const uint32_t* idx, const uint8_t* codes, const fl
                              void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Static sparse allreduce by recursive doubling (SSAR, §5.3.1), emulated on
+ * one GPU. In stage s = 0 .. log2(P) - 1 each node combines its sparse
+ * partial result with that of node i XOR 2^s; both get the same result, so
+ * stage s keeps one partial result per group of 2^(s+1) nodes. Combining the
+ * lower group's A with the upper group's B is the two-stream sum reduce:
+ *     out[i] = (+0.0f + a) + b   if i is in both,   +0.0f + v otherwise.
+ * The result stays sparse at every stage (no dense switch).
+ *   idx, val, nnz  P input streams [P][cap] (strictly ascending, < N).
+ *   P        a power of two, 2 .. 65,536; cap <= 2^31 - 1.
+ *   out_idx/out_val  the final result, ascending; out_cap >=
+ *            min(N, P * cap); *out_nnz = its size (device scalar).
+ *   stage_nnz  device [log2 P] or NULL: entries held after each stage over
+ *            its distinct partial results (the fill-in).
+ *   ws       >= sparcml_ssar_workspace_size(P, cap, N) bytes, 256-aligned.
+ * Device-side errors (bad stream, an expired bounded wait) go to the
+ * workspace's status word (sparcml_get_status(ws, stream)).
+ * ------------------------------------------------------------------------ */
+size_t sparcml_ssar_workspace_size(int32_t P, uint64_t cap, uint64_t N);
+int sparcml_ssar_allreduce(const uint32_t* idx, const float* val, const uint32_t* nnz, int32_t P,
+                           uint64_t cap, uint64_t N, uint32_t* out_idx, float* out_val,
+                           uint64_t out_cap, uint32_t* out_nnz, unsigned long long* stage_nnz,
+                           void* ws, size_t ws_bytes, void* stream);
+
+/* Same, plus a profiling hook: `events` is a host array of log2(P) + 1
+ * cudaEvent_t (entries may be NULL), recorded on `stream` before each stage
+ * and after the last. */
+int sparcml_ssar_allreduce_traced(const uint32_t* idx, const float* val, const uint32_t* nnz,
+                                  int32_t P, uint64_t cap, uint64_t N, uint32_t* out_idx,
+                                  float* out_val, uint64_t out_cap, uint32_t* out_nnz,
+                                  unsigned long long* stage_nnz, void* ws, size_t ws_bytes,
+                                  void* stream, void* const* events);
+
+/* ------------------------------------------------------------------------
  * Allocation-free sparse reduce. The paper has no counterpart: this entry
  * point exists for callers of this library that cannot allocate device
  * memory where they reduce (a plug-in inside a host framework that owns all

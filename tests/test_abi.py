@@ -108,6 +108,13 @@ def test_reduce_and_other_host_validation():
                                         FAKE, 250, FAKE, FAKE, FAKE, FAKE, ws, None) == 1
     assert lib.sparcml_sparse_reduce_op(FAKE, FAKE, FAKE, 2, 10, 1000, 4, 1, 4, FAKE, FAKE, 250,
                                         FAKE, FAKE, FAKE, FAKE, ws, None) == 1  # unknown op
+    sw = lib.sparcml_ssar_workspace_size(4, 100, 1000)
+    assert sw > 0 and lib.sparcml_ssar_workspace_size(3, 100, 1000) == 0  # P not a power of 2
+    ss = lib.sparcml_ssar_allreduce
+    assert ss(FAKE, FAKE, FAKE, 6, 100, 1000, FAKE, FAKE, 600, FAKE, None, FAKE, sw, None) == 1
+    assert ss(FAKE, FAKE, FAKE, 4, 100, 1000, FAKE, FAKE, 399, FAKE, None, FAKE, sw, None) == 3
+    assert ss(FAKE, FAKE, FAKE, 4, 100, 1000, FAKE, FAKE, 400, FAKE, None, FAKE, sw - 1,
+              None) == 2
 
 
 def test_segment_k_total_matches_the_oracle_rule():

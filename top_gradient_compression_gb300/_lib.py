@@ -59,6 +59,12 @@ SIGNATURES = {
     "sparcml_sparse_reduce_noalloc": (C.c_int, [vp, vp, vp, C.c_int32, C.c_uint64, C.c_uint64,
                                                 C.c_uint32, C.c_uint32, vp, vp, C.c_uint64, vp,
                                                 vp, vp, vp, vp]),
+    "sparcml_ssar_workspace_size": (C.c_size_t, [C.c_int32, C.c_uint64, C.c_uint64]),
+    "sparcml_ssar_allreduce": (C.c_int, [vp, vp, vp, C.c_int32, C.c_uint64, C.c_uint64, vp, vp,
+                                         C.c_uint64, vp, vp, vp, C.c_size_t, vp]),
+    "sparcml_ssar_allreduce_traced": (C.c_int, [vp, vp, vp, C.c_int32, C.c_uint64, C.c_uint64,
+                                                vp, vp, C.c_uint64, vp, vp, vp, C.c_size_t, vp,
+                                                vp]),
     "sparcml_densify": (C.c_int, [vp, vp, vp, C.c_int32, C.c_uint64, C.c_uint64, vp, vp, vp]),
 }
 

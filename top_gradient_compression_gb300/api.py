@@ -340,6 +340,38 @@ def sparse_reduce_qb(idx, codes, scales, nnz, bucket: int, bits: int, N: int, de
     return out
 
 
+def ssar_workspace_size(P: int, cap: int, N: int) -> int:
+    return int(_lib.load().sparcml_ssar_workspace_size(P, cap, N))
+
+
+def ssar_allreduce(idx, val, nnz, N: int, ws=None, stream=None, events=None):
+    """Static sparse allreduce by recursive doubling (§5.3.1), emulated: returns
+    (out_idx int32 [min(N, P*cap)], out_val, out_nnz int32 [1], stage_nnz
+    int64 [log2 P]); the first out_nnz entries are the result. `events`
+    (log2 P + 1 CUDA events) are recorded around the stages."""
+    P, cap = idx.shape
+    dev = idx.device
+    out_cap = min(N, P * cap)
+    out_idx = torch.empty(out_cap, dtype=torch.int32, device=dev)
+    out_val = torch.empty(out_cap, dtype=torch.float32, device=dev)
+    out_nnz = torch.zeros(1, dtype=torch.int32, device=dev)
+    stages = P.bit_length() - 1
+    stage_nnz = torch.zeros(max(stages, 1), dtype=torch.int64, device=dev)
+    if ws is None:
+        ws = workspace(ssar_workspace_size(P, cap, N), dev)
+    lib = _lib.load()
+    args = (_cuda(idx, torch.int32, "idx", 2), _cuda(val, torch.float32, "val", 2),
+            _cuda(nnz, torch.int32, "nnz", 1), P, cap, N, out_idx.data_ptr(), out_val.data_ptr(),
+            out_cap, out_nnz.data_ptr(), stage_nnz.data_ptr(), ws.data_ptr(), ws.numel(),
+            _stream(stream))
+    if events is None:
+        _check("sparcml_ssar_allreduce", lib.sparcml_ssar_allreduce(*args))
+    else:
+        arr = (C.c_void_p * len(events))(*[e.cuda_event for e in events])
+        _check("sparcml_ssar_allreduce_traced", lib.sparcml_ssar_allreduce_traced(*args, arr))
+    return out_idx, out_val, out_nnz, stage_nnz[:stages]
+
+
 def densify(idx, val, nnz, N: int, out=None, status=None, stream=None):
     P, cap = idx.shape
     if out is None:
