@@ -45,11 +45,12 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["resnet50", "asr", "sweep", "logreg", "qsgd"],
+    ap.add_argument("--workload", choices=["resnet50", "asr", "sweep", "logreg", "qsgd", "ssar"],
                     default="resnet50",
                     help="resnet50/asr: the whole EF step; sweep/logreg: the sparse reduce alone "
                          "on given streams (density-sweep cell / Zipf logistic regression); "
-                         "qsgd: b-bit quantisation of a dense reduced result")
+                         "qsgd: b-bit quantisation of a dense reduced result; "
+                         "ssar: recursive-doubling sparse allreduce of a density-sweep cell")
     ap.add_argument("--bits", type=int, default=4, choices=[2, 4, 8],
                     help="asr / qsgd: width of the quantised codes")
     ap.add_argument("--op", default="sum", choices=["sum", "max", "min", "or"],
@@ -270,7 +271,7 @@ def run_reference(args, ranks):
     if ranks.rank != 0:
         return
     from top_gradient_compression_gb300 import workloads as W
-    if args.workload in ("sweep", "logreg", "qsgd"):
+    if args.workload in ("sweep", "logreg", "qsgd", "ssar"):
         return run_reference_op(args)
     spec = workload_spec(args.workload)
     spec["bits"] = args.bits
@@ -319,12 +320,17 @@ def run_reference_op(args):
         idx, val, nnz = W.logreg_streams()
         N = W.LOGREG["N"]
     else:
-        P = args.sweep_p if args.workload == "sweep" else 64
-        dpct = args.sweep_d if args.workload == "sweep" else 10
+        P = args.sweep_p if args.workload in ("sweep", "ssar") else 64
+        dpct = args.sweep_d if args.workload in ("sweep", "ssar") else 10
         cell = [(a, b) for a, b in W.SWEEP_D if abs(100.0 * a / b - dpct) < 1e-9][0]
         idx, val, nnz = W.sweep_streams(P, *cell)
         N = W.SWEEP_N
-    if args.workload == "qsgd":
+    if args.workload == "ssar":
+        op = lambda s: oracle.ssar(idx, val, nnz, N)  # noqa: E731
+        units = int(nnz.astype(np.int64).sum())
+        nbytes = 8 * units
+        desc = f"SSAR recursive doubling of {idx.shape[0]} streams, N={N:,}"
+    elif args.workload == "qsgd":
         x = oracle.sparse_reduce(idx, val, nnz, N)["dense"]
         op = lambda s: oracle.quantize(x, 1024, args.bits, W.quant_seed(s))  # noqa: E731
         units, nbytes = N, 4 * N
@@ -740,6 +746,80 @@ def run_qsgd(args, ranks):
         "cpu_baseline": None, "e2e": None, "gpu_launches": launches, "clocks": clk}), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# SSAR recursive doubling, emulated (§5.3.1): fill-in and GB/s per stage
+# ---------------------------------------------------------------------------
+def run_ssar(args, ranks):
+    """The static sparse allreduce by recursive doubling over the streams of a
+    density-sweep cell (--sweep-p, --sweep-d). value = stream input bytes (8
+    per entry) / time of all stages; per stage: fill-in and GB/s of that
+    stage's own input + output bytes."""
+    from top_gradient_compression_gb300 import api, workloads as W
+    dev = ranks.device()
+    torch.cuda.set_device(dev)
+    P, N, dpct = args.sweep_p, W.SWEEP_N, args.sweep_d
+    cell = [(a, b) for a, b in W.SWEEP_D if abs(100.0 * a / b - dpct) < 1e-9]
+    if not cell or P & (P - 1):
+        raise SystemExit("--workload ssar needs a power-of-two --sweep-p and a sweep density")
+    idx, val, nnz = W.sweep_streams(P, *cell[0])
+    di = torch.from_numpy(idx.view(np.int32)).to(dev)
+    dv = torch.from_numpy(val).to(dev)
+    dn = torch.from_numpy(nnz.view(np.int32)).to(dev)
+    cap = idx.shape[1]
+    ws = api.workspace(api.ssar_workspace_size(P, cap, N), dev)
+    stages = P.bit_length() - 1
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    K, Wm = args.steps, args.warmup
+    evs = [api.make_events(stages + 1) for _ in range(K)]
+    for i in range(Wm):
+        api.ssar_allreduce(di, dv, dn, N, ws=ws)
+    torch.cuda.synchronize()
+    launches0 = api.launch_count()
+    clocks = ClockSampler(dev)
+    time.sleep(1.0)
+    t_host0 = time.time()
+    gpu_head_start(K)
+    for i in range(K):
+        flush.fill_(float(i))
+        _, _, out_nnz, fill = api.ssar_allreduce(di, dv, dn, N, ws=ws, events=evs[i])
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    clk = clocks.summary(t_host0, t_host1)
+    clocks.stop()
+    launches = api.launch_count() - launches0
+    if api.get_status(ws) != 0:
+        raise RuntimeError("device status set after the timed calls")
+    st_ms = [float(np.mean([e[s].elapsed_time(e[s + 1]) for e in evs])) for s in range(stages)]
+    ms = ranks.max(sum(st_ms))
+    fill = [int(x) for x in fill.cpu().numpy()]
+    sum_nnz = int(nnz.astype(np.int64).sum())
+    ins = [sum_nnz] + fill[:-1]
+    per_stage = [{"stage": s, "partial_results": P >> (s + 1), "entries_in": ins[s],
+                  "entries_out": fill[s], "fill_in_density": fill[s] / ((P >> (s + 1)) * N),
+                  "ms": st_ms[s], "GBps": 8 * (ins[s] + fill[s]) / (st_ms[s] * 1e-3) / 1e9}
+                 for s in range(stages)]
+    in_bytes = 8 * sum_nnz
+    moved = sum(8 * (ins[s] + fill[s]) for s in range(stages))
+    peak, peak_kind = hbm_peak()
+    if ranks.rank != 0:
+        return
+    print(json.dumps({
+        "metric": METRIC, "value": job_rate(ranks.world, in_bytes, ms * 1e-3) / 1e9, "unit": "GB/s",
+        "elems_per_s": job_rate(ranks.world, sum_nnz, ms * 1e-3), "n_gpus": ranks.world,
+        "steps": K, "warmup": Wm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded numpy index sets)",
+        "config": {"workload": f"SSAR recursive doubling, P={P} streams of {int(nnz[0]):,} "
+                               f"uniform indices (d={dpct:g}%) over N={N:,}",
+                   "P": P, "N": N, "units": "value = 8 B per input entry / time of all stages",
+                   "l2": "256 MB buffer written between timed runs (L2 flushed)"},
+        "stages": per_stage, "result_nnz": int(out_nnz.item()),
+        "roofline": {"bound": "hbm", "kernel": "ssar stages (partition + merge)",
+                     "achieved": moved / (ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
+                     "frac": moved / (ms * 1e-3) / 1e9 / peak, "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": moved, "traffic": None, "launch_ms": ms},
+        "cpu_baseline": None, "e2e": None, "gpu_launches": launches, "clocks": clk}), flush=True)
+
+
 def main():
     args = parse_args()
     ranks = Ranks()
@@ -750,6 +830,8 @@ def main():
             run_reduce_only(args, ranks)
         elif args.workload == "qsgd":
             run_qsgd(args, ranks)
+        elif args.workload == "ssar":
+            run_ssar(args, ranks)
         else:
             run_ours(args, ranks)
     finally:
