@@ -298,3 +298,52 @@ def test_reduce_warp_tiles_with_unaligned_buffers(P, N, k):
     else:
         assert np.array_equal(u32(out.idx[:U]), ref["idx"])
         assert np.array_equal(bits(out.val[:U].cpu().numpy()), bits(ref["val"]))
+
+
+def hot_head_streams(P, N, head, k, seed):
+    """Every node holds all of [0, head) plus k - head random others: the
+    first tiles hold P * 1,024 entries each (a skewed, Zipf-like head)."""
+    rng = np.random.default_rng(seed)
+    idx = np.zeros((P, k), np.uint32)
+    for p in range(P):
+        rest = rng.choice(np.arange(head, N), size=k - head, replace=False)
+        idx[p] = np.sort(np.concatenate([np.arange(head), rest])).astype(np.uint32)
+    val = rng.standard_normal((P, k)).astype(np.float32)
+    return idx, val, np.full(P, k, np.uint32)
+
+
+@pytest.mark.parametrize("P,k", [(16, 6_000), (17, 6_001)])  # quad / entry-by-entry warp tiles
+def test_reduce_hot_head_tiles(P, k):
+    """A skewed head: the first tiles hold P * 1,024 entries each (every node
+    has every index there). Bit for bit against the oracle (sum, and max)."""
+    N = 100_000
+    idx, val, nnz = hot_head_streams(P, N, 3_100, k, P)
+    r = check_reduce(idx, val, nnz, N, repeat=2)
+    assert r["nnz"] >= 3_100
+    ref = oracle.sparse_reduce_op(idx, val, nnz, N, "max")
+    di, dv, dn = streams_to_dev(idx, val, nnz)
+    out = api.sparse_reduce_op(di, dv, dn, N, "max")
+    assert int(out.nnz.item()) == ref["nnz"] and bool(out.is_dense.item()) == ref["is_dense"]
+    got = out.dense if ref["is_dense"] else out.val[:ref["nnz"]]
+    want = ref["dense"] if ref["is_dense"] else ref["val"]
+    assert np.array_equal(bits(got.cpu().numpy()), bits(want))
+
+
+def test_reduce_hot_head_tiles_with_4bit_values():
+    P, N, k, bucket = 16, 100_000, 6_000, 512
+    idx, val, nnz = hot_head_streams(P, N, 3_100, k, 5)
+    val *= 1e-2
+    seed = W.quant_seed(2)
+    oc, osc = oracle.quantize4(idx, val, nnz, bucket, seed)
+    deq = oracle.dequantize4(oc, osc, nnz, k, bucket)
+    ref = oracle.sparse_reduce(idx, deq, nnz, N)
+    di, dv, dn = streams_to_dev(idx, val, nnz)
+    codes, scales = api.quantize4(di, dv, dn, bucket, seed)
+    out = api.sparse_reduce_q4(di, codes, scales, dn, bucket, N)
+    U = int(out.nnz.item())
+    assert U == ref["nnz"] and bool(out.is_dense.item()) == ref["is_dense"]
+    if ref["is_dense"]:
+        assert np.array_equal(bits(out.dense.cpu().numpy()), bits(ref["dense"]))
+    else:
+        assert np.array_equal(u32(out.idx[:U]), ref["idx"])
+        assert np.array_equal(bits(out.val[:U].cpu().numpy()), bits(ref["val"]))
