@@ -182,14 +182,16 @@ __global__ void __launch_bounds__(kMergeThreads) ssar_merge_kernel(StageArgs s) 
   const uint32_t j0 = s.split_b[(uint64_t)g * per + c], j1 = s.split_b[(uint64_t)g * per + c + 1];
   const uint32_t la = i1 > i0 ? min(i1 - i0, kChunk + 1) : 0u;  // bounds kept for bad streams
   const uint32_t lb = j1 > j0 ? min(j1 - j0, kChunk + 1) : 0u;
+  // stage both sub-ranges with asynchronous copies: every load in flight at once
   for (uint32_t x = t; x < la; x += blockDim.x) {
-    sa_idx[x] = q.a_idx[i0 + x];
-    sa_val[x] = q.a_val[i0 + x];
+    cp_async4(&sa_idx[x], q.a_idx + i0 + x);
+    cp_async4(&sa_val[x], q.a_val + i0 + x);
   }
   for (uint32_t x = t; x < lb; x += blockDim.x) {
-    sb_idx[x] = q.b_idx[j0 + x];
-    sb_val[x] = q.b_val[j0 + x];
+    cp_async4(&sb_idx[x], q.b_idx + j0 + x);
+    cp_async4(&sb_val[x], q.b_val + j0 + x);
   }
+  cp_async_wait_all();
   __syncthreads();
   if (s.validate) {  // strictly ascending streams with indices < N
     for (uint32_t x = t; x < la; x += blockDim.x) {
@@ -220,27 +222,28 @@ __global__ void __launch_bounds__(kMergeThreads) ssar_merge_kernel(StageArgs s) 
   local_split(min(t * kPerThread, L), &a0, &b0);
   local_split(min((t + 1) * kPerThread, L), &a1, &b1);
   if (b0 > b1) b0 = b1;  // a tie moved the start past a short range
-  uint32_t oidx[kPerThread + 1];
-  float oval[kPerThread + 1];
-  uint32_t n = 0;
-  uint32_t ia = a0, ib = b0;
-  while ((ia < a1 || ib < b1) && n <= kPerThread) {
-    if (ib >= b1 || (ia < a1 && sa_idx[ia] < sb_idx[ib])) {
-      oidx[n] = sa_idx[ia];
-      oval[n] = __fadd_rn(0.0f, sa_val[ia]);
-      ++ia;
-    } else if (ia >= a1 || sb_idx[ib] < sa_idx[ia]) {
-      oidx[n] = sb_idx[ib];
-      oval[n] = __fadd_rn(0.0f, sb_val[ib]);
-      ++ib;
-    } else {  // the same index in A and B: (+0 + a) + b
-      oidx[n] = sa_idx[ia];
-      oval[n] = __fadd_rn(__fadd_rn(0.0f, sa_val[ia]), sb_val[ib]);
-      ++ia;
-      ++ib;
+  // Two walks over the thread's positions in shared memory: the first counts
+  // the merged entries, the second (after the offsets are known) writes them,
+  // so nothing is held in per-thread arrays.
+  auto walk = [&](auto emit) {
+    uint32_t n = 0, ia = a0, ib = b0;
+    while ((ia < a1 || ib < b1) && n <= kPerThread) {
+      if (ib >= b1 || (ia < a1 && sa_idx[ia] < sb_idx[ib])) {
+        emit(n, sa_idx[ia], __fadd_rn(0.0f, sa_val[ia]));
+        ++ia;
+      } else if (ia >= a1 || sb_idx[ib] < sa_idx[ia]) {
+        emit(n, sb_idx[ib], __fadd_rn(0.0f, sb_val[ib]));
+        ++ib;
+      } else {  // the same index in A and B: (+0 + a) + b
+        emit(n, sa_idx[ia], __fadd_rn(__fadd_rn(0.0f, sa_val[ia]), sb_val[ib]));
+        ++ia;
+        ++ib;
+      }
+      ++n;
     }
-    ++n;
-  }
+    return n;
+  };
+  const uint32_t n = walk([](uint32_t, uint32_t, float) {});
   uint32_t count;
   const uint32_t ex = block_excl_scan(n, scratch, &count);
   if (t < 32) {
@@ -248,15 +251,16 @@ __global__ void __launch_bounds__(kMergeThreads) ssar_merge_kernel(StageArgs s) 
     if (t == 0) bc[1] = excl;
   }
   __syncthreads();
-  const uint64_t base = (uint64_t)g * s.cap_out + bc[1] + ex;
-  for (uint32_t x = 0; x < n; ++x) {
-    if (bc[1] + ex + x < s.cap_out) {
-      s.out_idx[base + x] = oidx[x];
-      s.out_val[base + x] = oval[x];
+  const uint64_t pos0 = (uint64_t)bc[1] + ex;
+  const uint64_t base = (uint64_t)g * s.cap_out;
+  walk([&](uint32_t x, uint32_t key, float v) {
+    if (pos0 + x < s.cap_out) {
+      s.out_idx[base + pos0 + x] = key;
+      s.out_val[base + pos0 + x] = v;
     } else {
       set_status(s.status, SPARCML_ERR_CAPACITY);
     }
-  }
+  });
   const bool last = (uint64_t)(c + 1) * kChunk >= total;
   if (t == 0 && last) {
     const uint32_t u = bc[1] + count;
