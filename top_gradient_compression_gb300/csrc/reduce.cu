@@ -2,30 +2,40 @@
 //
 // "SparCML: High-Performance Sparse Communication for Machine Learning",
 // §5.2 (allreduce of sparse vectors with a coordinate-wise associative op
-// that has a neutral element: here fp32 sum, neutral +0.0), §5.3.2 (the
-// split phase routes index ranges to owners: here each CTA owns a tile of
-// the index space), §5.1 / §5.3.3 (switch to a dense representation once
-// fill-in passes the threshold delta), App. B (the result size is the size
-// of the union of the contributed index sets).
+// that has a neutral element: fp32 sum with neutral +0.0, and max, min,
+// bitwise or), §5.3.2 (the split phase routes index ranges to owners: here
+// a warp or CTA owns each tile of the index space), §5.1 / §5.3.3 (switch to
+// a dense representation once fill-in passes the threshold delta), App. B
+// (the result size is the size of the union of the contributed index sets).
 //
-// One pass over the input, no sort, no floating-point atomics:
+// No sort and no floating-point atomics: the index space is cut into tiles,
+// each tile is reduced by one owner (a warp or a CTA) that adds its nodes'
+// entries in ascending node order, so every result is bit-exact. The host
+// picks the tiling from P, cap and N (no device read):
 //
-//  tile kernel   (one CTA per tile of kTile consecutive indices, tiles taken
-//                in index order through a ticket). The CTA binary-searches
-//                each node's sub-range for its tile, then adds the nodes'
-//                entries into a shared-memory fp32 accumulator node by node
-//                in ascending node order (indices are unique within a node,
-//                so no two threads of one node touch the same word) and sets
-//                a presence bitmap. Its union count is chained to the
-//                previous tiles with a decoupled look-back (Merrill and
-//                Garland, 2016) to get the tile's output offset. A tile whose
-//                inclusive count still fits the sparse capacity writes its
-//                entries ascending (bitmap + prefix popcount); once the
-//                running count passes floor(N * num / den) the result is
-//                certainly dense and the tile writes its dense slice.
-//  fix-up kernel (one CTA per tile) runs only if the final result is dense:
-//                the leading tiles that were written sparse are turned into
-//                their dense slices (zeros, then a scatter of their entries).
+//  warp tiles (P <= 64, P * cap >= N / 16): a streaming split pass
+//      (reduce_split_quad_kernel / reduce_split_stream_kernel) finds where
+//      every node's entries enter every 1,024-index tile and validates the
+//      streams; one warp per tile (reduce_mini_quad_kernel with 16-byte
+//      quads, or reduce_mini_kernel) sums into a shared accumulator.
+//      P * cap >= N / 4: dense-first (slice + bitmap + union size, then
+//      reduce_mini_compact_kernel if the result is sparse after all);
+//      otherwise sparse-first with a decoupled look-back per CTA group
+//      (Merrill and Garland, 2016) and reduce_fixup_kernel if the union
+//      crosses the dense threshold after all.
+//  compact-accumulator CTA tiles (P * cap < N / 4 when P > 64, or
+//      P * cap < N / 16): reduce_split_kernel (33-ary search per (tile,
+//      node)), reduce_sparse_tile_kernel (tiles of 8,192..131,072 indices,
+//      bitmap + prefix-popcount slots, look-back), fix-up.
+//  staged CTA tiles (P > 64 with P * cap >= N / 4, or P > 1,024):
+//      reduce_dense_tile_kernel (8,192-index tiles, per-node items through a
+//      cp.async ring), dense-first with reduce_finalize_kernel and
+//      reduce_compact_kernel, or look-back + fix-up.
+//
+// Tiles past the sparse capacity floor(N * num / den) write dense slices;
+// a dense result holds the operation's neutral element (+0.0f for the sum)
+// where no node has the index. The same kernels serve max, min and bitwise
+// or (sparcml_sparse_reduce_op) and 2/4/8-bit values decoded on load.
 //
 // Every wait on a predecessor is bounded; on expiry the kernel records
 // SPARCML_ERR_TIMEOUT and carries on, so a bad input can never hang the GPU.
@@ -1553,7 +1563,7 @@ int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
                     a.op != kOpOr;  // warp tiles mark absent indices with a NaN pattern
   const bool sparse = !mini && a.P <= kMaxSparseP && est <= 2048.0;
   if (sparse) {
-    while (tile_w < kMaxTileW && est * (2.0 * tile_w / kTile) <= 2048.0 && tile_w < a.N)
+    while (tile_w < kMaxTileW && est * (2.0 * tile_w / kTile) <= 1024.0 && tile_w < a.N)
       tile_w *= 2;
   }
   if (mini) tile_w = kMini;

@@ -458,21 +458,21 @@ __device__ __forceinline__ uint32_t window_chunk(const SelectShared& sh, uint32_
 
 // Select for a layer-sized segment whose candidates were all kept in their
 // sub-slots (at most kShortCands of them, over at most kShortSubs
-// sub-chunks): one warp per segment, no block barrier.
-//  1. lane L copies the contiguous candidate range [L*c, (L+1)*c) into the
-//     warp's shared memory with cp.async (every copy in flight at once),
-//     walking the sub-chunks with a cursor;
+// sub-chunks): one CTA of kSegThreads per segment (4 warps share the work of
+// each phase, so a segment's chain of phases is short):
+//  1. thread t copies sub-chunk t's candidates into shared memory with
+//     cp.async (every copy in flight at once), at the sub-chunk's offset;
 //  2. four radix digits (8, 8, 8, 7 bits) of the k-th key T, each from one
-//     warp-private 256-bin histogram over the shared copy;
-//  3. each lane writes the kept entries of its range in index order at the
-//     offset given by warp scans of the per-lane counts (keys > T, and keys
-//     == T up to tie_take, lowest indices first); indices are resolved and the
-//     residual zeroed in a last batched pass.
+//     256-bin histogram over the shared copy (warp-aggregated adds), its
+//     bins scanned from the top by warp 0;
+//  3. thread t writes the kept entries of its contiguous candidate range in
+//     index order at the offset given by a block scan of its counts (keys
+//     > T, and keys == T up to tie_take, lowest indices first); then the
+//     offsets are resolved to indices and the residual is zeroed there.
 // Segments that do not qualify go to the to-do list of topk_select_kernel.
 constexpr uint32_t kShortSubs = 128;
 constexpr uint32_t kShortCands = 2048;
-constexpr uint32_t kShortWarps = 4;  // warps (segments) per CTA
-constexpr uint32_t kShortWords = kShortSubs + 1 + kShortCands + 256;
+constexpr uint32_t kSegThreads = 128;  // = kShortSubs: one sub-chunk per thread in phase 1
 
 __device__ __forceinline__ bool short_select_eligible(const SelectArgs& a, uint32_t gs, uint32_t k,
                                                       uint32_t ms) {
@@ -486,167 +486,131 @@ __device__ __forceinline__ uint32_t warp_excl_sum(uint32_t v, uint32_t* total) {
   return incl - v;
 }
 
-__global__ void __launch_bounds__(kShortWarps * 32)
+__global__ void __launch_bounds__(kSegThreads)
 topk_select_short_kernel(SelectArgs a) {
-  extern __shared__ uint32_t dsm[];
+  __shared__ uint32_t wpre[kShortSubs + 1];
+  __shared__ float vals[kShortCands];
+  __shared__ uint32_t hist[256];
+  __shared__ uint32_t scratch[34];
+  __shared__ uint32_t dig[2];
   const Geo& g = a.g;
-  const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
-  const uint32_t gs = blockIdx.x * kShortWarps + warp;
-  if (gs >= (uint32_t)g.P * g.nseg) return;  // warp-uniform
+  const uint32_t t = threadIdx.x, lane = lane_id(), warp = t >> 5;
+  const uint32_t gs = blockIdx.x;
   const uint32_t p = gs / g.nseg, s = gs % g.nseg;
   const uint32_t k = seg_k(g, s), ms = seg_chunks(g, s);
-  if (k == 0) return;
-  if (!short_select_eligible(a, gs, k, ms)) {  // hand it to topk_select_kernel
-    if (lane == 0) a.todo[atomicAdd(a.todo_cnt, 1u)] = gs;
+  if (k == 0) return;                                // CTA-uniform
+  if (!short_select_eligible(a, gs, k, ms)) {        // CTA-uniform: to topk_select_kernel
+    if (t == 0) a.todo[atomicAdd(a.todo_cnt, 1u)] = gs;
     return;
   }
-  uint32_t* wpre = dsm + warp * kShortWords;
-  float* vals = reinterpret_cast<float*>(wpre + kShortSubs + 1);
-  uint32_t* hist = wpre + kShortSubs + 1 + kShortCands;
   const uint32_t nsub = ms * kWarpsPerChunk;
   const uint64_t sub0 = ((uint64_t)p * g.nchunk + (uint64_t)s * g.m) * kWarpsPerChunk;
   const uint32_t* cidx = a.cand_idx + sub0 * g.slot;
   const float* cval = a.cand_val + sub0 * g.slot;
-  // prefix of the sub-chunk counts (4 per lane)
-  {
-    uint32_t c4[4], sum = 0;
-#pragma unroll
-    for (uint32_t i = 0; i < 4; ++i) {
-      const uint32_t w = lane * 4 + i;
-      c4[i] = w < nsub ? a.sub_cnt[sub0 + w] : 0u;
-      sum += c4[i];
-    }
-    uint32_t tot;
-    uint32_t ex = warp_excl_sum(sum, &tot);
-#pragma unroll
-    for (uint32_t i = 0; i < 4; ++i) {
-      const uint32_t w = lane * 4 + i;
-      if (w < nsub) wpre[w] = ex;
-      ex += c4[i];
-    }
-    if (lane == 0) wpre[nsub] = tot;
-  }
-  __syncwarp();
-  const uint32_t M = wpre[nsub];
-  // 1. this lane's candidates [v_lo, v_hi) -> shared memory.
-  const uint32_t per = (M + 31) / 32;
-  const uint32_t v_lo = min(lane * per, M), v_hi = min(v_lo + per, M);
-  uint32_t w0 = 0;
-  for (uint32_t step = kShortSubs / 2; step > 0; step >>= 1)
-    if (w0 + step <= nsub && wpre[w0 + step] <= v_lo) w0 += step;
-  {
-    uint32_t w = w0;
-    for (uint32_t v = v_lo; v < v_hi; ++v) {
-      while (wpre[w + 1] <= v) ++w;
-      cp_async4(vals + v, cval + w * g.slot + (v - wpre[w]));
-    }
-  }
+  // 1. offsets of the sub-chunks' candidates, then the copies
+  const uint32_t c = t < nsub ? a.sub_cnt[sub0 + t] : 0u;
+  uint32_t M;
+  const uint32_t off = block_excl_scan(c, scratch, &M);
+  if (t < nsub) wpre[t] = off;
+  if (t == 0) wpre[nsub] = M;
+  for (uint32_t i = 0; i < c; ++i) cp_async4(vals + off + i, cval + (uint64_t)t * g.slot + i);
   cp_async_wait_all();
-  __syncwarp();
-  // 2. radix digits of T (bits 30..23, 22..15, 14..7, 6..0).
+  __syncthreads();
+  // 2. radix digits of T (bits 30..23, 22..15, 14..7, 6..0)
   uint32_t prefix = 0, rem = k;
   for (int d = 0; d < 4; ++d) {
     const uint32_t shift = d == 3 ? 0 : 23 - 8 * d;
     const uint32_t wbits = d == 3 ? 7 : 8, hi_shift = shift + wbits;
-    for (uint32_t i = lane; i < 256; i += 32) hist[i] = 0;
-    __syncwarp();
-    for (uint32_t v0 = 0; v0 < M; v0 += 32) {
-      const uint32_t v = v0 + lane;
+    for (uint32_t i = t; i < 256; i += kSegThreads) hist[i] = 0;
+    __syncthreads();
+    for (uint32_t v0 = 0; v0 < M; v0 += kSegThreads) {
+      const uint32_t v = v0 + t;
       const uint32_t key = v < M ? mag_key(vals[v]) : 0u;
       const bool match = v < M && (d == 0 || (key >> hi_shift) == prefix);
       hist_add(hist, (key >> shift) & ((1u << wbits) - 1u), match);
     }
-    __syncwarp();
-    // bins from high to low: lane covers 8 of them
-    uint32_t hb[8], sum = 0;
-#pragma unroll
-    for (uint32_t i = 0; i < 8; ++i) {
-      hb[i] = hist[255 - (8 * lane + i)];
-      sum += hb[i];
-    }
-    uint32_t tot;
-    const uint32_t excl = warp_excl_sum(sum, &tot);
-    uint32_t b = 0xffffffffu, ab = 0;
-    if (excl < rem && rem <= excl + sum) {
-      uint32_t acc = excl;
+    __syncthreads();
+    if (warp == 0) {  // bins from high to low: lane covers 8 of them
+      uint32_t hb[8], sum = 0;
 #pragma unroll
       for (uint32_t i = 0; i < 8; ++i) {
-        if (b == 0xffffffffu && acc + hb[i] >= rem) {
-          b = 255 - (8 * lane + i);
-          ab = acc;
+        hb[i] = hist[255 - (8 * lane + i)];
+        sum += hb[i];
+      }
+      uint32_t tot;
+      const uint32_t excl = warp_excl_sum(sum, &tot);
+      uint32_t b = 0xffffffffu, ab = 0;
+      if (excl < rem && rem <= excl + sum) {
+        uint32_t acc = excl;
+#pragma unroll
+        for (uint32_t i = 0; i < 8; ++i) {
+          if (b == 0xffffffffu && acc + hb[i] >= rem) {
+            b = 255 - (8 * lane + i);
+            ab = acc;
+          }
+          acc += hb[i];
         }
-        acc += hb[i];
+      }
+      const uint32_t found = __ballot_sync(0xffffffffu, b != 0xffffffffu);
+      if (lane == 0) {
+        if (!found) {
+          set_status(a.status, SPARCML_ERR_BAD_STREAM);
+          dig[0] = 0;
+          dig[1] = rem;
+        }
+      }
+      if (found && lane == __ffs(found) - 1) {
+        dig[0] = b;
+        dig[1] = rem - ab;
       }
     }
-    const uint32_t found = __ballot_sync(0xffffffffu, b != 0xffffffffu);
-    if (!found) {
-      if (lane == 0) set_status(a.status, SPARCML_ERR_BAD_STREAM);
-      b = 0;
-    } else {
-      const uint32_t src = __ffs(found) - 1;
-      b = __shfl_sync(0xffffffffu, b, src);
-      rem -= __shfl_sync(0xffffffffu, ab, src);
-    }
-    prefix = (prefix << wbits) | b;
-    __syncwarp();
+    __syncthreads();
+    prefix = (prefix << wbits) | dig[0];
+    rem = dig[1];
   }
   const uint32_t T = prefix, tie_take = rem;  // keys == T to keep, lowest indices first
-  // 3. ordered write of this lane's range.
+  // 3. ordered write of this thread's contiguous range
+  const uint32_t per = (M + kSegThreads - 1) / kSegThreads;
+  const uint32_t v_lo = min(t * per, M), v_hi = min(v_lo + per, M);
   uint32_t n_gt = 0, n_eq = 0;
   for (uint32_t v = v_lo; v < v_hi; ++v) {
     const uint32_t key = mag_key(vals[v]);
     n_gt += key > T ? 1u : 0u;
     n_eq += key == T ? 1u : 0u;
   }
-  uint32_t t_gt, t_eq;
-  uint32_t e_gt = warp_excl_sum(n_gt, &t_gt), e_eq = warp_excl_sum(n_eq, &t_eq);
+  uint32_t tot;  // both counts in one scan: M <= kShortCands < 2^16
+  const uint32_t ex = block_excl_scan((n_gt << 16) | n_eq, scratch, &tot);
+  uint32_t e_gt = ex >> 16, e_eq = ex & 0xffffu;
   float* rp = a.residual + (uint64_t)p * g.N;
   const uint64_t out0 = (uint64_t)p * g.cap + (uint64_t)s * g.k_full;
   uint32_t* oi = a.out_idx + out0;
   const uint64_t keep = l2_policy_evict_last();
-  {
-    uint32_t w = w0;
-    for (uint32_t v = v_lo; v < v_hi; ++v) {
-      const float x = vals[v];
-      const uint32_t key = mag_key(x);
-      const bool gt = key > T, eq = key == T;
-      if (gt || (eq && e_eq < tie_take)) {
-        const uint32_t pos = e_gt + min(e_eq, tie_take);
-        while (wpre[w + 1] <= v) ++w;
-        if (pos < k) {
-          oi[pos] = w * g.slot + (v - wpre[w]);  // slot offset for now
-          st_keep(a.out_val + out0 + pos, x, keep);
-        } else {
-          set_status(a.status, SPARCML_ERR_BAD_STREAM);
-        }
+  uint32_t w = 0;  // sub-chunk of v_lo: the largest w with wpre[w] <= v_lo
+  for (uint32_t step = kShortSubs / 2; step > 0; step >>= 1)
+    if (w + step <= nsub && wpre[w + step] <= v_lo) w += step;
+  for (uint32_t v = v_lo; v < v_hi; ++v) {
+    const float x = vals[v];
+    const uint32_t key = mag_key(x);
+    const bool gt = key > T, eq = key == T;
+    if (gt || (eq && e_eq < tie_take)) {
+      const uint32_t pos = e_gt + min(e_eq, tie_take);
+      while (wpre[w + 1] <= v) ++w;
+      if (pos < k) {
+        oi[pos] = w * g.slot + (v - wpre[w]);  // slot offset for now
+        st_keep(a.out_val + out0 + pos, x, keep);
+      } else {
+        set_status(a.status, SPARCML_ERR_BAD_STREAM);
       }
-      e_gt += gt ? 1u : 0u;
-      e_eq += eq ? 1u : 0u;
     }
+    e_gt += gt ? 1u : 0u;
+    e_eq += eq ? 1u : 0u;
   }
-  __syncwarp();
+  __syncthreads();  // the offsets written above are visible to the whole CTA
   // offsets -> indices; the residual is zeroed at each kept index.
-  constexpr uint32_t kB = 4;
-  for (uint32_t j0 = 0; j0 < k; j0 += 32 * kB) {
-    uint32_t off[kB], idx[kB];
-#pragma unroll
-    for (uint32_t q = 0; q < kB; ++q) {
-      const uint32_t j = j0 + q * 32 + lane;
-      off[q] = j < k ? oi[j] : 0u;
-    }
-#pragma unroll
-    for (uint32_t q = 0; q < kB; ++q) {
-      const uint32_t j = j0 + q * 32 + lane;
-      idx[q] = j < k ? cidx[off[q]] : 0u;
-    }
-#pragma unroll
-    for (uint32_t q = 0; q < kB; ++q) {
-      const uint32_t j = j0 + q * 32 + lane;
-      if (j < k) {
-        st_keep(oi + j, idx[q], keep);
-        rp[idx[q]] = 0.0f;
-      }
-    }
+  for (uint32_t j = t; j < k; j += kSegThreads) {
+    const uint32_t idx = cidx[oi[j]];
+    st_keep(oi + j, idx, keep);
+    rp[idx] = 0.0f;
   }
 }
 
@@ -1277,12 +1241,8 @@ extern "C" int sparcml_topk_ef_traced(const float* grad, float* residual, int32_
   while (CS < 8 && (uint64_t)g.m / (CS * 2) >= 64) CS *= 2;
   SelectArgs a{CS, CS == 1 ? 1u : 0u, CS > 1 ? 1u : 0u, todo, todo_cnt, residual, seg_cnt,
                seg_flag, chunk_cnt, guess, cand_idx, cand_val, out_idx, out_val, status, g};
-  if (CS == 1) {  // layer-sized segments: one warp each
-    const size_t smem = (size_t)kShortWarps * kShortWords * sizeof(uint32_t);
-    if (!ensure_smem(reinterpret_cast<const void*>(topk_select_short_kernel), smem))
-      return SPARCML_ERR_CUDA;
-    topk_select_short_kernel<<<(nsegs + kShortWarps - 1) / kShortWarps, kShortWarps * 32, smem,
-                               s>>>(a);
+  if (CS == 1) {  // layer-sized segments: one CTA each
+    topk_select_short_kernel<<<nsegs, kSegThreads, 0, s>>>(a);
     if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   } else {  // long segments: grid-wide passes
     LongArgs la{g, seg_cnt, seg_flag, chunk_cnt, cand_idx, cand_val, residual, out_idx, out_val,
