@@ -73,6 +73,9 @@ struct Geo {
   uint32_t k_last;   // k of the last segment
   uint32_t slot;     // candidate slot capacity per warp sub-chunk
   int32_t P;
+  // rank r of the guess in a sample (see sample_rank), per segment kind:
+  // the warp guess's sample and the CTA guess's sample
+  uint32_t r_warp_full, r_warp_last, r_cta_full, r_cta_last;
 };
 
 __device__ __forceinline__ uint32_t seg_n(const Geo& g, uint32_t s) {
@@ -165,14 +168,7 @@ topk_guess_kernel(const float* __restrict__ grad, const float* __restrict__ resi
   // layer-sized segments whose candidate sets are small anyway.
   const bool exact = n <= kSampleMax;
   const uint32_t S = exact ? n : (n <= kShortSegment ? kSampleShort : kSampleMax);
-  uint32_t r;
-  if (exact) {
-    r = k;
-  } else {
-    const double lam = (double)k * (double)S / (double)n;
-    const double rr = ceil(lam + 4.0 * sqrt(lam) + 8.0);
-    r = rr >= (double)S ? S : (uint32_t)rr;
-  }
+  const uint32_t r = exact ? k : (s == g.nseg - 1 ? g.r_cta_last : g.r_cta_full);
   // All sample loads are issued before any is used.
   uint32_t pos[KPT];
   bool ok[KPT];
@@ -264,24 +260,46 @@ topk_guess_warp_kernel(const float* __restrict__ grad, const float* __restrict__
   const float* gp = grad + base;
   const float* rp = residual + base;
   constexpr uint32_t nruns = kWarpSample / kRun, kLines = kRun / 32, kBatchRuns = 2;
-  const double lam = (double)k * (double)kWarpSample / (double)n;
-  const double rr = ceil(lam + 4.0 * sqrt(lam) + 8.0);
-  const uint32_t r = rr >= (double)kWarpSample ? kWarpSample : (uint32_t)rr;
+  const uint32_t r = s == g.nseg - 1 ? g.r_warp_last : g.r_warp_full;
   uint32_t key[kWarpKeys];
+  // run start (n <= kShortSegment, so run * (n - kRun) fits in 32 bits)
+  auto run_at = [&](uint32_t run) { return (run * (n - kRun) / (nruns - 1)) & ~(kRun - 1); };
+  if (((reinterpret_cast<uintptr_t>(gp) | reinterpret_cast<uintptr_t>(rp)) & 15) == 0) {
+    // 16-byte aligned segment: a run is 64 float4, two per lane; four runs'
+    // loads (16 of them) in flight at once
+    constexpr uint32_t kVecRuns = 4, kVecPer = kRun / 128;  // float4 per lane per run
 #pragma unroll
-  for (uint32_t r0 = 0; r0 < nruns; r0 += kBatchRuns) {
-    float a[kBatchRuns * kLines], b[kBatchRuns * kLines];
+    for (uint32_t r0 = 0; r0 < nruns; r0 += kVecRuns) {
+      float4 a[kVecRuns * kVecPer], b[kVecRuns * kVecPer];
 #pragma unroll
-    for (uint32_t q = 0; q < kBatchRuns * kLines; ++q) {
-      const uint32_t run = r0 + q / kLines;
-      // n <= kShortSegment, so run * (n - kRun) fits in 32 bits
-      const uint32_t i = ((run * (n - kRun) / (nruns - 1)) & ~(kRun - 1)) + (q % kLines) * 32 + lane;
-      a[q] = rp[i];
-      b[q] = gp[i];
+      for (uint32_t q = 0; q < kVecRuns * kVecPer; ++q) {
+        const uint32_t i = run_at(r0 + q / kVecPer) + ((q % kVecPer) * 32 + lane) * 4;
+        a[q] = *reinterpret_cast<const float4*>(rp + i);
+        b[q] = *reinterpret_cast<const float4*>(gp + i);
+      }
+#pragma unroll
+      for (uint32_t q = 0; q < kVecRuns * kVecPer; ++q) {
+        uint32_t* kq = key + (r0 * kVecPer + q) * 4;
+        kq[0] = mag_key(__fadd_rn(a[q].x, b[q].x));
+        kq[1] = mag_key(__fadd_rn(a[q].y, b[q].y));
+        kq[2] = mag_key(__fadd_rn(a[q].z, b[q].z));
+        kq[3] = mag_key(__fadd_rn(a[q].w, b[q].w));
+      }
     }
+  } else {
 #pragma unroll
-    for (uint32_t q = 0; q < kBatchRuns * kLines; ++q)
-      key[r0 * kLines + q] = mag_key(__fadd_rn(a[q], b[q]));
+    for (uint32_t r0 = 0; r0 < nruns; r0 += kBatchRuns) {
+      float a[kBatchRuns * kLines], b[kBatchRuns * kLines];
+#pragma unroll
+      for (uint32_t q = 0; q < kBatchRuns * kLines; ++q) {
+        const uint32_t i = run_at(r0 + q / kLines) + (q % kLines) * 32 + lane;
+        a[q] = rp[i];
+        b[q] = gp[i];
+      }
+#pragma unroll
+      for (uint32_t q = 0; q < kBatchRuns * kLines; ++q)
+        key[r0 * kLines + q] = mag_key(__fadd_rn(a[q], b[q]));
+    }
   }
   uint32_t G = 0;
 #pragma unroll 1
@@ -1120,6 +1138,19 @@ struct Layout {
   uint32_t nr;  // long-segment ranges of a full segment
 };
 
+// Rank of the guess in a sample of S of a segment's n entries with k kept:
+// r = ceil(lambda + 4 sqrt(lambda) + 8) with lambda = k S / n, the expected
+// number of sampled keys among the top k plus four standard deviations and a
+// margin, so the r-th largest sample key is very likely at or below the k-th
+// key of the segment. Computed once on the host (double precision is slow on
+// this GPU's cores).
+uint32_t sample_rank(uint32_t k, uint32_t n, uint32_t S) {
+  if (n == 0) return 0;
+  const double lam = (double)k * (double)S / (double)n;
+  const double rr = std::ceil(lam + 4.0 * std::sqrt(lam) + 8.0);
+  return rr >= (double)S ? S : (uint32_t)rr;
+}
+
 bool make_geo(int32_t P, uint64_t N, uint64_t seg_len, uint32_t k_num, uint32_t k_den, Geo* g) {
   if (P < 1 || P > 65535 || N < 1 || N > 0xffffffffull || seg_len < 1 || k_den < 1 ||
       k_num > k_den)
@@ -1144,6 +1175,11 @@ bool make_geo(int32_t P, uint64_t N, uint64_t seg_len, uint32_t k_num, uint32_t 
   uint32_t slot = (uint32_t)std::min<double>(kSub, std::ceil(want / 32.0) * 32.0);
   g->slot = std::max<uint32_t>(slot, 32);
   g->P = P;
+  auto cta_sample = [](uint32_t n) { return n <= kShortSegment ? kSampleShort : kSampleMax; };
+  g->r_warp_full = sample_rank(g->k_full, g->L, kWarpSample);
+  g->r_warp_last = sample_rank(g->k_last, g->L_last, kWarpSample);
+  g->r_cta_full = sample_rank(g->k_full, g->L, cta_sample(g->L));
+  g->r_cta_last = sample_rank(g->k_last, g->L_last, cta_sample(g->L_last));
   return true;
 }
 
