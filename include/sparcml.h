@@ -231,7 +231,8 @@ int sparcml_sparse_reduce(const uint32_t* idx, const float* val, const uint32_t*
 
 /* Same as sparcml_sparse_reduce, plus a profiling hook: `events` is a host
  * array of 3 cudaEvent_t (entries may be NULL), recorded on `stream` before
- * the tile kernel, between it and the dense fix-up kernel, and after. */
+ * the split and tile kernels, between them and the finishing kernel (dense
+ * fix-up or compaction), and after it. */
 int sparcml_sparse_reduce_traced(const uint32_t* idx, const float* val, const uint32_t* nnz,
                                  int32_t P, uint64_t cap, uint64_t N, uint32_t dens_num,
                                  uint32_t dens_den, uint32_t* out_idx, float* out_val,
