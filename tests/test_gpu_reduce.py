@@ -255,23 +255,74 @@ def test_reduce_each_regime_exact(P, N, maxk, note):
     check_reduce(idx, val, nnz, N, repeat=2)
 
 
-@pytest.mark.parametrize("k", [1100, 1101])  # quad / scalar split pass
-def test_reduce_detects_bad_streams_in_warp_tiles(k):
-    """Streams that cover a quarter of the index space take the warp-per-tile
-    path; a step down, a repeat or an index past N is flagged there too."""
-    N = 4096
+@pytest.mark.parametrize("N,k", [
+    (4_096, 1_100), (4_096, 1_101),     # dense-first warp tiles: quad / scalar split pass
+    (65_536, 3_000), (65_536, 3_001),   # sparse-first warp tiles: quad / scalar split pass
+])
+def test_reduce_detects_bad_streams_in_warp_tiles(N, k):
+    """Streams that cover a large share of the index space take the
+    warp-per-tile path; a step down, a repeat, an index past N or two entries
+    swapped across tiles is flagged there too, by either form of the split
+    pass and with either output order."""
     rng = np.random.default_rng(4)
     good = np.sort(rng.choice(N - 1, size=k, replace=False)).astype(np.uint32)
-    bad = [good.copy(), good.copy(), good.copy()]
+    bad = [good.copy() for _ in range(4)]
     bad[0][500], bad[0][501] = bad[0][501], bad[0][500]  # step down inside a tile
     bad[1][700] = bad[1][699]                              # repeated index
     bad[2][-1] = N                                         # index past the end
+    bad[3][100], bad[3][900] = bad[3][900], bad[3][100]    # out of order across tiles
     for b in bad:
         idx = np.stack([good, b])
         di, dv, dn = streams_to_dev(idx, np.ones((2, k), np.float32), np.full(2, k, np.uint32))
         ws = api.workspace(api.reduce_workspace_size(2, N), DEV)
         api.sparse_reduce(di, dv, dn, N, ws=ws)
         assert api.get_status(ws) == api.STATUS_CODE["SPARCML_ERR_BAD_STREAM"]
+
+
+@pytest.mark.parametrize("P,N,k,note", [
+    (64, 65_536, 6_553, "64 nodes at 10 %, the largest sweep cell's per-tile load"),
+    (64, 70_001, 7_000, "ragged last tile"),
+    (8, 50_000, 5_001, "rows not 16-byte aligned (cap = 5,001)"),
+    (3, 100_000, 8_000, "sparse-first with look-back"),
+])
+def test_reduce_warp_tiles_heavy_nodes_exact(P, N, k, note):
+    """About a hundred entries per node and 1,024-index tile: a round of 32
+    quads holds one node's tail and the next node's head, so nearly every
+    round is added one node at a time. Bit for bit against the oracle."""
+    idx, val, nnz = W.uniform_streams(P, N, k, 70 + P)
+    nnz[P // 2] = 2 * k // 3  # a shorter node among full ones
+    check_reduce(idx, val, nnz, N, repeat=2)
+
+
+def test_reduce_largest_sweep_cell_sampled():
+    """P = 64, d = 10 % at N = 4,194,304, launched as the benchmark does: the
+    union size against a count of the distinct indices, and the values at
+    two whole tiles plus 2,048 random indices against the oracle run on the
+    streams restricted to those indices (each index sums independently)."""
+    P, N = 64, W.SWEEP_N
+    idx, val, nnz = W.sweep_streams(P, 10, 100)
+    di, dv, dn = streams_to_dev(idx, val, nnz)
+    ws = api.workspace(api.reduce_workspace_size(P, N), DEV)
+    out = api.sparse_reduce(di, dv, dn, N, ws=ws)
+    assert api.get_status(ws) == 0
+    U = int(out.nnz.item())
+    assert U == np.unique(idx.reshape(-1)).size
+    assert bool(out.is_dense.item()) == (4 * U > N) and 4 * U > N
+    rng = np.random.default_rng(12)
+    sample = np.union1d(np.arange(7 * 1024, 9 * 1024), rng.choice(N, 2_048, replace=False))
+    keep = np.isin(idx, sample)
+    cnt = keep.sum(axis=1)
+    sub_i = np.zeros((P, int(cnt.max())), np.uint32)
+    sub_v = np.zeros((P, int(cnt.max())), np.float32)
+    for p in range(P):
+        sub_i[p, :cnt[p]] = idx[p][keep[p]]
+        sub_v[p, :cnt[p]] = val[p][keep[p]]
+    ref = oracle.sparse_reduce(sub_i, sub_v, cnt.astype(np.uint32), N)
+    assert not ref["is_dense"]
+    want = np.zeros(N, np.float32)
+    want[ref["idx"]] = ref["val"]
+    got = out.dense.cpu().numpy()
+    assert np.array_equal(bits(got[sample]), bits(want[sample]))
 
 
 @pytest.mark.parametrize("P,N,k", [(6, 30_000, 2_000), (64, 65_536, 3_001)])

@@ -35,6 +35,8 @@ def check_op(idx, val, nnz, N, op, repeat=2):
     (3, 4_194_304, 2_000),     # compact-accumulator CTA tiles
     (8, 200_000, 4_000),       # sparse-first warp tiles (or: CTA tiles)
     (16, 200_000, 12_000),     # dense-first warp tiles, dense result
+    (4, 100_000, 8_000),       # ~80 entries per node and tile: dense-first warp tiles
+    (3, 100_000, 8_000),       # the same load, sparse-first warp tiles with look-back
     (80, 100_000, 2_000),      # more than 64 nodes: staged CTA tiles, dense-first
     (100, 200_000, 1_000),     # staged CTA tiles, look-back, dense by fix-up
 ])
