@@ -608,6 +608,37 @@ def test_ssar_equals_the_sequential_reduce_when_sums_are_exact(P):
         assert np.array_equal(ov.view(np.uint32), ref["val"].view(np.uint32))
 
 
+@pytest.mark.parametrize("P", [4, 8, 16])
+def test_ssar_equals_a_dense_pairwise_tree_brute_force(P):
+    """Recursive doubling (§5.3.1) written out densely with numpy: at stage s
+    group g adds (+0 + lower half) + upper half element-wise, absent entries
+    being +0.0, and the support is the union of the halves' supports. With
+    N(0, 1) values the sums round, so this pins the tree order bit for bit,
+    and the stage sizes are the unions' sizes (App. B)."""
+    rng = np.random.default_rng(70 + P)
+    N, k = 3000, 400
+    idx = np.zeros((P, k), np.uint32)
+    for p in range(P):
+        idx[p] = np.sort(rng.choice(N, k, replace=False))
+    val = rng.standard_normal((P, k)).astype(np.float32)
+    val[:, ::11] = -0.0
+    nnz = rng.integers(0, k + 1, size=P).astype(np.uint32)
+    dense = np.zeros((P, N), np.float32)
+    here = np.zeros((P, N), bool)
+    for p in range(P):
+        dense[p, idx[p, :nnz[p]]] = val[p, :nnz[p]]
+        here[p, idx[p, :nnz[p]]] = True
+    fill = []
+    while dense.shape[0] > 1:
+        dense = (np.float32(0.0) + dense[0::2]) + dense[1::2]
+        here = here[0::2] | here[1::2]
+        fill.append(int(here.sum()))
+    oi, ov, of = oracle.ssar(idx, val, nnz, N)
+    assert of.tolist() == fill
+    assert np.array_equal(oi, np.flatnonzero(here[0]).astype(np.uint32))
+    assert np.array_equal(ov.view(np.uint32), dense[0, oi].view(np.uint32))
+
+
 def test_ssar_needs_a_power_of_two():
     with pytest.raises(RuntimeError):
         oracle.ssar(np.zeros((3, 1), np.uint32), np.zeros((3, 1), np.float32),
