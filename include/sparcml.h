@@ -35,7 +35,8 @@
  *     fit, a wait that ran out) never trap: the first one is recorded in a
  *     device status word (the first 4 bytes of the workspace, or the
  *     explicit `status` pointer) and read back by sparcml_get_status.
- *   - Limits. 1 <= P <= 65535, 1 <= N <= 2^32 - 1 (indices are uint32).
+ *   - Limits. 1 <= P <= 65535, 1 <= N <= 2^32 - 1 (indices are uint32),
+ *     unless an entry point states its own bound on P.
  *
  * Results are deterministic: the same inputs give the same bits on every
  * run (fixed summation order, no floating-point atomics).
@@ -215,6 +216,8 @@ int sparcml_dequantize(const uint8_t* codes, const float* scales, const uint32_t
  * Dense result: out_dense [N] holds out[i], +0.0f where no node has i;
  * out_idx/out_val hold unspecified values.
  * *out_nnz = U and *out_is_dense = 0/1 in both cases (device scalars).
+ *   P        1 .. 4,096 (above: SPARCML_ERR_INVALID_ARG, and the workspace
+ *            size function returns 0); cap < 2^32.
  *   out_cap  capacity of out_idx/out_val, >= floor(N * dens_num / dens_den)
  *            (enough for any sparse result).
  *   ws       >= sparcml_sparse_reduce_workspace_size(P, N) bytes.

@@ -90,6 +90,11 @@ def test_reduce_and_other_host_validation():
              None) == 1
     assert r(FAKE, FAKE, FAKE, 4, 10, 1000, 1, 4, FAKE, FAKE, 250, FAKE, FAKE, FAKE, FAKE, ws - 1,
              None) == 2
+    assert lib.sparcml_sparse_reduce_workspace_size(4097, 1000) == 0  # P above 4,096
+    assert r(FAKE, FAKE, FAKE, 4097, 10, 1000, 1, 4, FAKE, FAKE, 250, FAKE, FAKE, FAKE, FAKE,
+             1 << 30, None) == 1
+    assert r(FAKE, FAKE, FAKE, 4, 1 << 32, 1000, 1, 4, FAKE, FAKE, 250, FAKE, FAKE, FAKE, FAKE,
+             ws, None) == 1  # cap of 2^32 entries
     assert lib.sparcml_quantize4(FAKE, FAKE, FAKE, 2, 100, 3, 0, FAKE, FAKE, None, None) == 1
     assert lib.sparcml_dequantize4(FAKE, FAKE, FAKE, 2, 0, 512, FAKE, None, None) == 1
     assert lib.sparcml_densify(FAKE, FAKE, FAKE, 2, 10, 0, FAKE, None, None) == 1
