@@ -163,3 +163,34 @@ def test_asr_workload_node0_three_steps_then_quantised_reduce():
     assert U == ref["nnz"] and not ref["is_dense"] and not bool(out.is_dense.item())
     assert np.array_equal(u32(out.idx[:U]), ref["idx"])
     assert np.array_equal(bits(out.val[:U].cpu().numpy()), bits(ref["val"]))
+
+
+def test_ef_state_checkpoint_and_resume_is_bitwise():
+    """The error-feedback residual is the only state carried between steps:
+    ten steps in one go equal five steps, a torch.save / torch.load round
+    trip of the residual through host memory, and five more, bit for bit
+    (every step's streams and the final residual)."""
+    import io
+    P, N, L = 4, 300_000, 100_000
+    grads = [torch.from_numpy(make("normal", P, N, 100 + s)).to(DEV) for s in range(10)]
+
+    def run(res, steps):
+        outs = []
+        for g in steps:
+            idx, val, nnz = api.topk_ef(g, res, L, 1, 100)
+            outs.append((idx.clone(), val.clone(), nnz.clone()))
+        return outs
+
+    res_a = torch.zeros((P, N), device=DEV)
+    a = run(res_a, grads)
+    res_b = torch.zeros((P, N), device=DEV)
+    b = run(res_b, grads[:5])
+    buf = io.BytesIO()
+    torch.save(res_b.cpu(), buf)
+    buf.seek(0)
+    res_c = torch.load(buf).to(DEV)
+    b += run(res_c, grads[5:])
+    for (ia, va, na), (ib, vb, nb) in zip(a, b):
+        assert torch.equal(na, nb) and torch.equal(ia, ib)
+        assert torch.equal(va.view(torch.int32), vb.view(torch.int32))
+    assert torch.equal(res_a.view(torch.int32), res_c.view(torch.int32))
