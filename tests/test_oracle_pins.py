@@ -77,6 +77,24 @@ def test_topk_brute_force_all_k_tiny(seed):
             assert np.array_equal(val[p, :k].view(np.uint32), acc[p, want].view(np.uint32))
 
 
+def test_topk_orders_non_finite_magnitudes_by_bit_pattern():
+    """Non-finite inputs are not rejected; the magnitude key is the bit
+    pattern of |x|, so any NaN ranks above +-inf, which ranks above every
+    finite value; among NaNs the larger payload wins, and +inf and -inf have
+    one key, so the lower index wins between them."""
+    f = np.float32
+    qnan, big_nan = np.uint32(0x7FC00000).view(f), np.uint32(0x7FC00001).view(f)
+    grad = np.array([[1.0, -np.inf, 3.0e38, qnan, -2.0, np.inf, big_nan, 0.0]], f)
+    for k, want in [(1, [6]), (2, [3, 6]), (3, [1, 3, 6]), (4, [1, 3, 5, 6]), (5, [1, 2, 3, 5, 6])]:
+        res = np.zeros_like(grad)
+        idx, val, nnz = oracle.topk_ef(grad, res, seg_len=8, k_num=k, k_den=8, cap=8)
+        assert nnz[0] == k and list(idx[0, :k]) == want
+        kept = np.zeros(8, bool)
+        kept[want] = True
+        assert np.array_equal(res[0, ~kept].view(np.uint32), grad[0, ~kept].view(np.uint32))
+        assert (res[0, kept].view(np.uint32) == 0).all()
+
+
 @pytest.mark.parametrize("N,seg_len,k_num,k_den", [(50, 16, 3, 8), (37, 5, 2, 5), (64, 64, 1, 100),
                                                     (33, 1, 1, 1), (40, 7, 0, 3)])
 def test_topk_segments_brute_force(N, seg_len, k_num, k_den):
