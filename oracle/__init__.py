@@ -30,7 +30,7 @@ def build(force: bool = False) -> str:
     """Compile oracle.cpp into liboracle.so next to it (no fast-math, no FMA contraction)."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.check_call(["g++", "-O2", "-std=c++17", "-fPIC", "-shared",
+        subprocess.check_call(["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-pthread",
                                "-ffp-contract=off", "-fno-fast-math", "-o", tmp, _SRC])
         os.replace(tmp, _LIB)
     return _LIB
@@ -47,6 +47,18 @@ def _load():
             lib.oracle_splitmix64.restype = C.c_uint64
             lib.oracle_topk_ef.argtypes = [f32p, f32p, C.c_int32, C.c_uint64, C.c_uint64,
                                            C.c_uint64, C.c_uint64, u32p, f32p, u32p, C.c_uint64]
+            u64p_ = np.ctypeslib.ndpointer(dtype=np.uint64, flags="C_CONTIGUOUS")
+            lib.oracle_topk_ef_segments.argtypes = [f32p, f32p, C.c_int32, C.c_uint64, u64p_,
+                                                    u64p_, C.c_uint64, u32p, f32p, u32p,
+                                                    C.c_uint64]
+            lib.oracle_topk_ef_segments_mt.argtypes = [f32p, f32p, C.c_int32, C.c_uint64, u64p_,
+                                                       u64p_, C.c_uint64, u32p, f32p, u32p,
+                                                       C.c_uint64, C.c_int32]
+            lib.oracle_sparse_reduce_mt.argtypes = [u32p, f32p, u32p, C.c_int32, C.c_uint64,
+                                                    C.c_uint64, C.c_uint32, C.c_uint32, u32p,
+                                                    f32p, C.c_uint64, f32p,
+                                                    C.POINTER(C.c_uint64), C.POINTER(C.c_int32),
+                                                    C.c_int32]
             lib.oracle_pack.argtypes = [f32p, C.c_int32, C.c_uint64, C.c_float, u32p, f32p,
                                         u32p, C.c_uint64]
             lib.oracle_quantize4.argtypes = [u32p, f32p, u32p, C.c_int32, C.c_uint64,
@@ -71,8 +83,11 @@ def _load():
                                         u32p, f32p, C.c_uint64, C.POINTER(C.c_uint64), u64p]
             lib.oracle_densify.argtypes = [u32p, f32p, u32p, C.c_int32, C.c_uint64, C.c_uint64,
                                            f32p]
-            for f in ("oracle_topk_ef", "oracle_pack", "oracle_quantize4", "oracle_dequantize4",
-                      "oracle_sparse_reduce", "oracle_densify"):
+            for f in ("oracle_topk_ef", "oracle_topk_ef_segments", "oracle_topk_ef_segments_mt",
+                      "oracle_pack", "oracle_quantize4", "oracle_dequantize4",
+                      "oracle_quantize", "oracle_dequantize", "oracle_sparse_reduce",
+                      "oracle_sparse_reduce_op", "oracle_sparse_reduce_mt", "oracle_ssar",
+                      "oracle_densify"):
                 getattr(lib, f).restype = C.c_int
             _lib = lib
     return _lib
@@ -125,6 +140,46 @@ def topk_ef(grad, residual, seg_len, k_num, k_den, cap=None):
     nnz = np.zeros((P,), np.uint32)
     _check("oracle_topk_ef", _load().oracle_topk_ef(g, residual, P, N, seg_len, k_num, k_den,
                                                     idx, val, nnz, cap))
+    return idx, val, nnz
+
+
+def uniform_segments(N: int, seg_len: int, k_num: int, k_den: int):
+    """The equal-segment table: begins [0, L, 2L, ..., N] and k_s = floor(n_s * k_num / k_den)
+    (the last segment takes the remainder, App. A)."""
+    begin = list(range(0, N, seg_len)) + [N]
+    return begin, segment_ks(N, seg_len, k_num, k_den)
+
+
+def _seg_arrays(seg_begin, seg_k):
+    b = np.ascontiguousarray(np.asarray(seg_begin, dtype=np.uint64))
+    k = np.ascontiguousarray(np.asarray(seg_k, dtype=np.uint64))
+    if b.ndim != 1 or k.ndim != 1 or b.size != k.size + 1:
+        raise ValueError("seg_begin needs nseg + 1 entries and seg_k nseg")
+    return b, k
+
+
+def topk_ef_segments(grad, residual, seg_begin, seg_k, cap=None, threads: int = 1):
+    """Top-k with error feedback over an arbitrary segment table (SparCML §2.2,
+    §4; layer-wise sparsification, §8.4): segment s = [seg_begin[s],
+    seg_begin[s+1]) keeps seg_k[s] entries. residual is updated IN PLACE.
+    threads > 1 spreads the (node, segment) pairs over host threads (same
+    results). Returns (idx [P, cap] uint32, val [P, cap] float32, nnz [P] uint32)."""
+    g = _f32(grad)
+    assert isinstance(residual, np.ndarray) and residual.dtype == np.float32 \
+        and residual.flags.c_contiguous and residual.shape == g.shape
+    P, N = g.shape
+    b, k = _seg_arrays(seg_begin, seg_k)
+    total = int(k.sum())
+    cap = max(total, 1) if cap is None else cap
+    idx = np.zeros((P, cap), np.uint32)
+    val = np.zeros((P, cap), np.float32)
+    nnz = np.zeros((P,), np.uint32)
+    if threads > 1:
+        _check("oracle_topk_ef_segments_mt", _load().oracle_topk_ef_segments_mt(
+            g, residual, P, N, b, k, k.size, idx, val, nnz, cap, threads))
+    else:
+        _check("oracle_topk_ef_segments", _load().oracle_topk_ef_segments(
+            g, residual, P, N, b, k, k.size, idx, val, nnz, cap))
     return idx, val, nnz
 
 
@@ -240,8 +295,10 @@ def ssar(idx, val, nnz, N):
     return oi[:U].copy(), ov[:U].copy(), stages[:P.bit_length() - 1].copy()
 
 
-def sparse_reduce(idx, val, nnz, N, dens_num=1, dens_den=4):
+def sparse_reduce(idx, val, nnz, N, dens_num=1, dens_den=4, threads: int = 1):
     """Sum-reduction of P sparse streams with the dense switch (SparCML §5.1-§5.3).
+    threads > 1 cuts the index space into that many ranges reduced on host
+    threads (same results).
 
     Returns dict(nnz=U, is_dense=bool, idx=uint32[U] | None, val=float32[U] | None,
     dense=float32[N] | None)."""
@@ -253,9 +310,14 @@ def sparse_reduce(idx, val, nnz, N, dens_num=1, dens_den=4):
     od = np.zeros(N, np.float32)
     u = C.c_uint64(0)
     d = C.c_int32(0)
-    _check("oracle_sparse_reduce", _load().oracle_sparse_reduce(
-        idx, val, nnz, P, cap, N, dens_num, dens_den, oi, ov, out_cap, od,
-        C.byref(u), C.byref(d)))
+    if threads > 1:
+        _check("oracle_sparse_reduce_mt", _load().oracle_sparse_reduce_mt(
+            idx, val, nnz, P, cap, N, dens_num, dens_den, oi, ov, out_cap, od,
+            C.byref(u), C.byref(d), threads))
+    else:
+        _check("oracle_sparse_reduce", _load().oracle_sparse_reduce(
+            idx, val, nnz, P, cap, N, dens_num, dens_den, oi, ov, out_cap, od,
+            C.byref(u), C.byref(d)))
     U = int(u.value)
     if d.value:
         return dict(nnz=U, is_dense=True, idx=None, val=None, dense=od)

@@ -37,7 +37,9 @@
 #include <cstdint>
 #include <cstring>
 #include <limits>
+#include <atomic>
 #include <map>
+#include <thread>
 #include <utility>
 #include <vector>
 
@@ -67,18 +69,107 @@ uint64_t segment_k(uint64_t n_s, uint64_t k_num, uint64_t k_den) {
   return n_s * k_num / k_den;  // floor(d * n_s) with d = k_num / k_den
 }
 
+// One fp32 addition, round to nearest even. IEEE 754 leaves the payload of a
+// NaN result open; the reading used throughout is that every NaN produced by
+// an addition is the quiet NaN with all payload bits set (0x7fffffff), so
+// that the bits of a result do not depend on which input NaN a machine
+// propagates.
+float add_f32(float a, float b) {
+  float r = a + b;
+  if (r != r) {
+    const uint32_t canonical = 0x7fffffffu;
+    std::memcpy(&r, &canonical, sizeof r);
+  }
+  return r;
+}
+
 }  // namespace
 
 extern "C" {
 
 uint64_t oracle_splitmix64(uint64_t x) { return splitmix64(x); }
 
-// Per-node Top-k with error feedback (§2.2, §4), segment by segment.
+// Top-k with error feedback (§2.2, §4) of one segment [b, e) of one node,
+// keeping k_s entries: acc = residual + grad over the segment; the k_s
+// entries with the largest magnitude key (ties: lower index first) go to
+// out_idx/out_val in ascending index order; the residual becomes acc with
+// the kept positions set to +0.0f.
+static void topk_segment(const float* g, float* r, uint64_t b, uint64_t e, uint64_t k_s,
+                         uint32_t* out_idx, float* out_val) {
+  const uint64_t n_s = e - b;
+  std::vector<float> acc(n_s);
+  // Error feedback: the accumulated gradient is residual + new gradient.
+  for (uint64_t i = 0; i < n_s; ++i) acc[i] = add_f32(r[b + i], g[b + i]);
+  std::vector<std::pair<uint32_t, uint32_t>> keyed;  // (key, index)
+  keyed.reserve(n_s);
+  for (uint64_t i = 0; i < n_s; ++i)
+    keyed.emplace_back(magnitude_key(acc[i]), (uint32_t)(b + i));
+  // Largest magnitude first; among equal magnitudes the lower index first.
+  std::sort(keyed.begin(), keyed.end(),
+            [](const std::pair<uint32_t, uint32_t>& x, const std::pair<uint32_t, uint32_t>& y) {
+              if (x.first != y.first) return x.first > y.first;
+              return x.second < y.second;
+            });
+  std::vector<uint32_t> chosen;
+  for (uint64_t j = 0; j < k_s; ++j) chosen.push_back(keyed[j].second);
+  std::sort(chosen.begin(), chosen.end());
+  for (uint64_t j = 0; j < chosen.size(); ++j) {
+    out_idx[j] = chosen[j];
+    out_val[j] = acc[chosen[j] - b];
+  }
+  // Transmitted components leave the residual; the rest stay in it.
+  for (uint32_t i : chosen) acc[i - b] = 0.0f;
+  for (uint64_t i = 0; i < n_s; ++i) r[b + i] = acc[i];
+}
+
+// Checks a segment table: seg_begin[0] = 0 < seg_begin[1] < ... <
+// seg_begin[nseg] = N and seg_k[s] <= n_s; returns the sum of the k_s in
+// *total_k.
+static int check_segments(uint64_t N, const uint64_t* seg_begin, const uint64_t* seg_k,
+                          uint64_t nseg, uint64_t* total_k) {
+  if (nseg == 0 || seg_begin[0] != 0 || seg_begin[nseg] != N) return INVALID;
+  uint64_t t = 0;
+  for (uint64_t s = 0; s < nseg; ++s) {
+    if (seg_begin[s + 1] <= seg_begin[s]) return INVALID;
+    if (seg_k[s] > seg_begin[s + 1] - seg_begin[s]) return INVALID;
+    t += seg_k[s];
+  }
+  *total_k = t;
+  return OK;
+}
+
+// Per-node Top-k with error feedback over an arbitrary segment table, the
+// layer-wise sparsification of §8.4: segment s of every node is
+// [seg_begin[s], seg_begin[s + 1]) and keeps seg_k[s] entries.
 //   grad, residual: [P][N] fp32 row-major; residual is updated in place.
-//   Segments of one node: [s*seg_len, min((s+1)*seg_len, N)).
-//   k_s = floor(n_s * k_num / k_den).
-//   out_idx/out_val: [P][cap]; node p's stream is written ascending at
-//   p*cap; out_nnz[p] = sum of k_s.
+//   out_idx/out_val: [P][cap]; node p's stream holds the segments' kept
+//   entries one segment after the other (so ascending), starting at p*cap;
+//   out_nnz[p] = sum of seg_k.
+int oracle_topk_ef_segments(const float* grad, float* residual, int32_t P, uint64_t N,
+                            const uint64_t* seg_begin, const uint64_t* seg_k, uint64_t nseg,
+                            uint32_t* out_idx, float* out_val, uint32_t* out_nnz,
+                            uint64_t cap) {
+  if (P <= 0 || N == 0 || N > 0xffffffffULL) return INVALID;
+  uint64_t total_k = 0;
+  const int st = check_segments(N, seg_begin, seg_k, nseg, &total_k);
+  if (st != OK) return st;
+  if (total_k > cap) return CAPACITY;
+  for (int32_t p = 0; p < P; ++p) {
+    uint64_t written = 0;
+    for (uint64_t s = 0; s < nseg; ++s) {
+      topk_segment(grad + (uint64_t)p * N, residual + (uint64_t)p * N, seg_begin[s],
+                   seg_begin[s + 1], seg_k[s], out_idx + (uint64_t)p * cap + written,
+                   out_val + (uint64_t)p * cap + written);
+      written += seg_k[s];
+    }
+    out_nnz[p] = (uint32_t)written;
+  }
+  return OK;
+}
+
+// Per-node Top-k with error feedback (§2.2, §4) over equal segments: segment
+// s is [s*seg_len, min((s+1)*seg_len, N)) (the last one takes the remainder,
+// App. A) and keeps k_s = floor(n_s * k_num / k_den) entries.
 int oracle_topk_ef(const float* grad, float* residual, int32_t P, uint64_t N,
                    uint64_t seg_len, uint64_t k_num, uint64_t k_den,
                    uint32_t* out_idx, float* out_val, uint32_t* out_nnz,
@@ -86,48 +177,14 @@ int oracle_topk_ef(const float* grad, float* residual, int32_t P, uint64_t N,
   if (P <= 0 || N == 0 || N > 0xffffffffULL || seg_len == 0 || k_den == 0 ||
       k_num > k_den || k_den > 0xffffffffULL)
     return INVALID;
-  uint64_t total_k = 0;
-  for (uint64_t b = 0; b < N; b += seg_len)
-    total_k += segment_k(std::min(seg_len, N - b), k_num, k_den);
-  if (total_k > cap) return CAPACITY;
-
-  std::vector<float> acc(N);
-  std::vector<std::pair<uint32_t, uint32_t>> keyed;  // (key, index)
-  std::vector<uint32_t> chosen;
-  for (int32_t p = 0; p < P; ++p) {
-    const float* g = grad + (uint64_t)p * N;
-    float* r = residual + (uint64_t)p * N;
-    // Error feedback: the accumulated gradient is residual + new gradient.
-    for (uint64_t i = 0; i < N; ++i) acc[i] = r[i] + g[i];
-    uint64_t written = 0;
-    for (uint64_t b = 0; b < N; b += seg_len) {
-      const uint64_t n_s = std::min(seg_len, N - b);
-      const uint64_t k_s = segment_k(n_s, k_num, k_den);
-      keyed.clear();
-      for (uint64_t i = b; i < b + n_s; ++i)
-        keyed.emplace_back(magnitude_key(acc[i]), (uint32_t)i);
-      // Largest magnitude first; among equal magnitudes the lower index first.
-      std::sort(keyed.begin(), keyed.end(),
-                [](const std::pair<uint32_t, uint32_t>& a,
-                   const std::pair<uint32_t, uint32_t>& c) {
-                  if (a.first != c.first) return a.first > c.first;
-                  return a.second < c.second;
-                });
-      chosen.clear();
-      for (uint64_t j = 0; j < k_s; ++j) chosen.push_back(keyed[j].second);
-      std::sort(chosen.begin(), chosen.end());
-      for (uint32_t i : chosen) {
-        out_idx[(uint64_t)p * cap + written] = i;
-        out_val[(uint64_t)p * cap + written] = acc[i];
-        ++written;
-      }
-      // Transmitted components leave the residual; the rest stay in it.
-      for (uint32_t i : chosen) acc[i] = 0.0f;
-    }
-    for (uint64_t i = 0; i < N; ++i) r[i] = acc[i];
-    out_nnz[p] = (uint32_t)written;
+  std::vector<uint64_t> begin, ks;
+  for (uint64_t b = 0; b < N; b += seg_len) {
+    begin.push_back(b);
+    ks.push_back(segment_k(std::min(seg_len, N - b), k_num, k_den));
   }
-  return OK;
+  begin.push_back(N);
+  return oracle_topk_ef_segments(grad, residual, P, N, begin.data(), ks.data(), ks.size(),
+                                 out_idx, out_val, out_nnz, cap);
 }
 
 // Select entries with |x| > thr (thr = 0 keeps the nonzeros), ascending.
@@ -344,9 +401,9 @@ int oracle_sparse_reduce(const uint32_t* idx, const float* val, const uint32_t* 
       const float v = val[(uint64_t)p * cap + j];
       auto it = sum.find(i);
       if (it == sum.end())
-        sum.emplace(i, 0.0f + v);
+        sum.emplace(i, add_f32(0.0f, v));
       else
-        it->second = it->second + v;
+        it->second = add_f32(it->second, v);
     }
   }
   const uint64_t U = sum.size();
@@ -381,7 +438,7 @@ int oracle_sparse_reduce(const uint32_t* idx, const float* val, const uint32_t* 
 // where no node has the index. op 0 is oracle_sparse_reduce.
 static float fold(int32_t op, float a, float b) {
   switch (op) {
-    case 0: return a + b;
+    case 0: return add_f32(a, b);
     case 1: return b > a ? b : a;
     case 2: return b < a ? b : a;
     default: {
@@ -477,13 +534,13 @@ int oracle_ssar(const uint32_t* idx, const float* val, const uint32_t* nnz, int3
       const auto& A = part[2 * g];
       const auto& B = part[2 * g + 1];
       auto& C = next[g];
-      for (const auto& kv : A) C.emplace(kv.first, 0.0f + kv.second);
+      for (const auto& kv : A) C.emplace(kv.first, add_f32(0.0f, kv.second));
       for (const auto& kv : B) {
         auto it = C.find(kv.first);
         if (it == C.end())
-          C.emplace(kv.first, 0.0f + kv.second);
+          C.emplace(kv.first, add_f32(0.0f, kv.second));
         else
-          it->second = it->second + kv.second;
+          it->second = add_f32(it->second, kv.second);
       }
       fill += C.size();
     }
@@ -515,6 +572,112 @@ int oracle_densify(const uint32_t* idx, const float* val, const uint32_t* nnz, i
       if (i >= N) return BAD_STREAM;
       d[i] = val[(uint64_t)p * cap + j];
     }
+  }
+  return OK;
+}
+
+// ---------------------------------------------------------------------------
+// Host-core timing drivers: the CPU baseline on every core. They split the
+// work into pieces that do not interact and run each piece with the same
+// code as the sequential functions above, so the results are identical.
+// ---------------------------------------------------------------------------
+
+// oracle_topk_ef_segments with the (node, segment) pairs spread over
+// nthreads threads (each pair is independent: its own slice of residual,
+// grad and output stream).
+int oracle_topk_ef_segments_mt(const float* grad, float* residual, int32_t P, uint64_t N,
+                               const uint64_t* seg_begin, const uint64_t* seg_k, uint64_t nseg,
+                               uint32_t* out_idx, float* out_val, uint32_t* out_nnz,
+                               uint64_t cap, int32_t nthreads) {
+  if (P <= 0 || N == 0 || N > 0xffffffffULL || nthreads < 1) return INVALID;
+  uint64_t total_k = 0;
+  const int st = check_segments(N, seg_begin, seg_k, nseg, &total_k);
+  if (st != OK) return st;
+  if (total_k > cap) return CAPACITY;
+  std::vector<uint64_t> out0(nseg + 1, 0);
+  for (uint64_t s = 0; s < nseg; ++s) out0[s + 1] = out0[s] + seg_k[s];
+  const uint64_t tasks = (uint64_t)P * nseg;
+  std::atomic<uint64_t> next{0};
+  auto work = [&]() {
+    for (uint64_t t = next++; t < tasks; t = next++) {
+      const uint64_t p = t / nseg, s = t % nseg;
+      topk_segment(grad + p * N, residual + p * N, seg_begin[s], seg_begin[s + 1], seg_k[s],
+                   out_idx + p * cap + out0[s], out_val + p * cap + out0[s]);
+    }
+  };
+  std::vector<std::thread> pool;
+  for (int32_t i = 1; i < nthreads; ++i) pool.emplace_back(work);
+  work();
+  for (auto& th : pool) th.join();
+  for (int32_t p = 0; p < P; ++p) out_nnz[p] = (uint32_t)total_k;
+  return OK;
+}
+
+// oracle_sparse_reduce with the index space cut into nthreads ranges: each
+// thread owns [N t / T, N (t + 1) / T), walks every node's entries in that
+// range in ascending node order into its own std::map, so every index gets
+// the same sum in the same order as in the sequential function.
+int oracle_sparse_reduce_mt(const uint32_t* idx, const float* val, const uint32_t* nnz,
+                            int32_t P, uint64_t cap, uint64_t N, uint32_t dens_num,
+                            uint32_t dens_den, uint32_t* out_idx, float* out_val,
+                            uint64_t out_cap, float* out_dense, uint64_t* out_nnz,
+                            int32_t* out_is_dense, int32_t nthreads) {
+  if (P <= 0 || N == 0 || N > 0xffffffffULL || dens_den == 0 || nthreads < 1) return INVALID;
+  for (int32_t p = 0; p < P; ++p)
+    if (nnz[p] > cap) return INVALID;
+  const int32_t T = nthreads;
+  std::vector<int> bad(T, 0);
+  std::vector<std::map<uint32_t, float>> part(T);
+  auto work = [&](int32_t t) {
+    // streams: strictly ascending and below N (each thread checks a slice)
+    for (int32_t p = 0; p < P; ++p) {
+      const uint32_t* row = idx + (uint64_t)p * cap;
+      const uint64_t n = nnz[p], j0 = n * t / T, j1 = n * (t + 1) / T;
+      for (uint64_t j = j0; j < j1; ++j)
+        if (row[j] >= N || (j > 0 && row[j] <= row[j - 1])) bad[t] = 1;
+    }
+    const uint64_t r0 = N * t / T, r1 = N * (t + 1) / T;
+    auto& sum = part[t];
+    for (int32_t p = 0; p < P; ++p) {
+      const uint32_t* row = idx + (uint64_t)p * cap;
+      const uint32_t* lo = std::lower_bound(row, row + nnz[p], (uint32_t)r0);
+      // the last range also takes any entry >= N (rejected above anyway)
+      const uint32_t* hi =
+          t == T - 1 ? row + nnz[p] : std::lower_bound(row, row + nnz[p], (uint32_t)r1);
+      for (const uint32_t* q = lo; q < hi; ++q) {
+        const float v = val[(uint64_t)p * cap + (uint64_t)(q - row)];
+        auto it = sum.find(*q);
+        if (it == sum.end())
+          sum.emplace(*q, add_f32(0.0f, v));
+        else
+          it->second = add_f32(it->second, v);
+      }
+    }
+  };
+  std::vector<std::thread> pool;
+  for (int32_t t = 1; t < T; ++t) pool.emplace_back(work, t);
+  work(0);
+  for (auto& th : pool) th.join();
+  for (int32_t t = 0; t < T; ++t)
+    if (bad[t]) return BAD_STREAM;
+  uint64_t U = 0;
+  for (int32_t t = 0; t < T; ++t) U += part[t].size();
+  const bool dense = U * (uint64_t)dens_den > N * (uint64_t)dens_num;
+  *out_nnz = U;
+  *out_is_dense = dense ? 1 : 0;
+  if (dense) {
+    for (uint64_t i = 0; i < N; ++i) out_dense[i] = 0.0f;
+    for (int32_t t = 0; t < T; ++t)
+      for (const auto& kv : part[t]) out_dense[kv.first] = kv.second;
+  } else {
+    if (U > out_cap) return CAPACITY;
+    uint64_t j = 0;
+    for (int32_t t = 0; t < T; ++t)
+      for (const auto& kv : part[t]) {
+        out_idx[j] = kv.first;
+        out_val[j] = kv.second;
+        ++j;
+      }
   }
   return OK;
 }

@@ -77,22 +77,146 @@ def test_topk_brute_force_all_k_tiny(seed):
             assert np.array_equal(val[p, :k].view(np.uint32), acc[p, want].view(np.uint32))
 
 
+CANON_NAN = np.uint32(0x7FFFFFFF)
+
+
 def test_topk_orders_non_finite_magnitudes_by_bit_pattern():
     """Non-finite inputs are not rejected; the magnitude key is the bit
-    pattern of |x|, so any NaN ranks above +-inf, which ranks above every
-    finite value; among NaNs the larger payload wins, and +inf and -inf have
-    one key, so the lower index wins between them."""
+    pattern of |x|, so a NaN ranks above +-inf, which ranks above every
+    finite value. Every NaN that the error-feedback add produces is the
+    canonical NaN 0x7fffffff (IEEE 754 leaves a NaN result's payload open),
+    so NaNs of any payload tie and the lower index wins; +inf and -inf have
+    one key, so the lower index wins between them too."""
     f = np.float32
-    qnan, big_nan = np.uint32(0x7FC00000).view(f), np.uint32(0x7FC00001).view(f)
+    qnan, big_nan = np.uint32(0x7FC00000).view(f), np.uint32(0xFFC00001).view(f)
     grad = np.array([[1.0, -np.inf, 3.0e38, qnan, -2.0, np.inf, big_nan, 0.0]], f)
-    for k, want in [(1, [6]), (2, [3, 6]), (3, [1, 3, 6]), (4, [1, 3, 5, 6]), (5, [1, 2, 3, 5, 6])]:
+    acc_bits = grad.view(np.uint32).copy()
+    acc_bits[0, [3, 6]] = CANON_NAN
+    for k, want in [(1, [3]), (2, [3, 6]), (3, [1, 3, 6]), (4, [1, 3, 5, 6]), (5, [1, 2, 3, 5, 6])]:
         res = np.zeros_like(grad)
         idx, val, nnz = oracle.topk_ef(grad, res, seg_len=8, k_num=k, k_den=8, cap=8)
         assert nnz[0] == k and list(idx[0, :k]) == want
+        assert np.array_equal(val[0, :k].view(np.uint32), acc_bits[0, want])
         kept = np.zeros(8, bool)
         kept[want] = True
-        assert np.array_equal(res[0, ~kept].view(np.uint32), grad[0, ~kept].view(np.uint32))
+        assert np.array_equal(res[0, ~kept].view(np.uint32), acc_bits[0, ~kept])
         assert (res[0, kept].view(np.uint32) == 0).all()
+
+
+def test_fp32_additions_give_the_canonical_nan():
+    """Every NaN an addition produces is 0x7fffffff whatever the input
+    payloads (the EF add, the sum reduce and SSAR's pairwise sums), while
+    finite sums and the signs of infinities are untouched."""
+    f = np.float32
+    pay = [np.uint32(x).view(f) for x in (0x7FC00000, 0xFFC00001, 0x7F800001, 0x7FFFFFFF)]
+    for a in pay:
+        g = np.array([[a, np.inf, 1.5]], f)
+        r = np.array([[0.0, -np.inf, 2.25]], f)
+        oracle.topk_ef(g, r, 3, 0, 1)  # k = 0: residual = acc everywhere
+        assert list(r.view(np.uint32)[0]) == [CANON_NAN, CANON_NAN, np.float32(3.75).view(np.uint32)]
+    idx = np.array([[0, 1, 2], [0, 1, 3]], np.uint32)
+    val = np.array([[pay[1], np.inf, 1.0], [1.0, -np.inf, np.inf]], f)
+    out = oracle.sparse_reduce(idx, val, np.array([3, 3], np.uint32), 16)
+    assert list(out["idx"]) == [0, 1, 2, 3]
+    assert list(out["val"].view(np.uint32)) == [CANON_NAN, CANON_NAN,
+                                                 np.float32(1.0).view(np.uint32),
+                                                 np.float32(np.inf).view(np.uint32)]
+    ri, rv, _ = oracle.ssar(idx, val, np.array([3, 3], np.uint32), 16)
+    assert np.array_equal(rv.view(np.uint32), out["val"].view(np.uint32))
+
+
+def brute_table(grad_row, seg_begin, seg_k):
+    want = []
+    for s in range(len(seg_k)):
+        b, e = seg_begin[s], seg_begin[s + 1]
+        want += [b + i for i in brute_topk(grad_row[b:e], seg_k[s])]
+    return want
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_topk_ragged_segment_table_brute_force(seed):
+    """Layer-wise sparsification (§8.4) over an arbitrary segment table:
+    segments of 1, 2, 7 and more entries, each with its own k_s from 0 to n_s,
+    against the O(n^2) definition segment by segment; the EF invariant holds
+    bitwise and nnz is the sum of the k_s."""
+    rng = np.random.default_rng(100 + seed)
+    lens = [1, 7, 2, 40, 1, 13, 64, 3] if seed % 2 else [5, 1, 1, 29, 7, 70]
+    seg_begin = [0] + list(np.cumsum(lens))
+    N = seg_begin[-1]
+    seg_k = [int(rng.integers(0, n + 1)) for n in lens]
+    seg_k[0], seg_k[-1] = 0, lens[-1]  # both ends of the k range
+    P = 3
+    grad = tie_heavy(rng, (P, N)) if seed < 2 else rng.standard_normal((P, N)).astype(np.float32)
+    res0 = tie_heavy(rng, (P, N)) * np.float32(0.5)
+    res = res0.copy()
+    idx, val, nnz = oracle.topk_ef_segments(grad, res, seg_begin, seg_k)
+    acc = res0 + grad
+    K = sum(seg_k)
+    for p in range(P):
+        want = brute_table(acc[p], seg_begin, seg_k)
+        assert int(nnz[p]) == K == len(want)
+        assert list(idx[p, :K]) == want
+        assert np.array_equal(val[p, :K].view(np.uint32), acc[p, want].view(np.uint32))
+        rebuilt = res[p].copy()
+        rebuilt[want] = val[p, :K]
+        assert np.array_equal(rebuilt.view(np.uint32), acc[p].view(np.uint32))
+        assert (res[p, want].view(np.uint32) == 0).all()
+
+
+def test_topk_uniform_form_is_the_equal_segment_table():
+    rng = np.random.default_rng(9)
+    P, N, L = 2, 1000, 300
+    g = rng.standard_normal((P, N)).astype(np.float32)
+    r1, r2 = np.zeros_like(g), np.zeros_like(g)
+    a = oracle.topk_ef(g, r1, L, 3, 100)
+    b, k = oracle.uniform_segments(N, L, 3, 100)
+    assert b == [0, 300, 600, 900, 1000] and k == [9, 9, 9, 3]
+    c = oracle.topk_ef_segments(g, r2, b, k)
+    for x, y in zip(a, c):
+        assert np.array_equal(x, y)
+    assert np.array_equal(r1, r2)
+
+
+def test_topk_segment_table_is_checked():
+    g = np.zeros((1, 10), np.float32)
+    for b, k in [([0, 5, 5, 10], [1, 0, 1]),  # empty segment
+                 ([0, 5, 9], [1, 1]),         # does not end at N
+                 ([1, 5, 10], [1, 1]),        # does not start at 0
+                 ([0, 5, 10], [6, 1])]:       # k_s > n_s
+        with pytest.raises(oracle.OracleError):
+            oracle.topk_ef_segments(g, np.zeros_like(g), b, k)
+
+
+def test_threaded_drivers_give_the_sequential_results():
+    """The all-core timing drivers (pairs (node, segment) on threads; the
+    reduce cut into index ranges) reproduce the sequential oracle bit for bit,
+    for sparse and dense results and for bad streams."""
+    rng = np.random.default_rng(4)
+    P, N = 5, 20_011
+    g = rng.standard_normal((P, N)).astype(np.float32)
+    lens = [1, 999, 7, 5000, 14_004]
+    b = [0] + list(np.cumsum(lens))
+    k = [1, 20, 0, 50, 1300]
+    r1, r2 = np.zeros_like(g), np.zeros_like(g)
+    a = oracle.topk_ef_segments(g, r1, b, k)
+    c = oracle.topk_ef_segments(g, r2, b, k, threads=7)
+    for x, y in zip(a, c):
+        assert np.array_equal(x, y)
+    assert np.array_equal(r1.view(np.uint32), r2.view(np.uint32))
+    for kk, dense in [(400, False), (6000, True)]:
+        idx, val, nnz = W.uniform_streams(P, N, kk, 77 + kk)
+        s1 = oracle.sparse_reduce(idx, val, nnz, N)
+        s2 = oracle.sparse_reduce(idx, val, nnz, N, threads=6)
+        assert s1["nnz"] == s2["nnz"] and s1["is_dense"] == s2["is_dense"] == dense
+        for key in ("idx", "val", "dense"):
+            if s1[key] is not None:
+                assert np.array_equal(np.asarray(s1[key]).view(np.uint32),
+                                      np.asarray(s2[key]).view(np.uint32))
+    idx, val, nnz = W.uniform_streams(2, 100, 10, 5)
+    idx[1, 4] = idx[1, 3]  # not strictly ascending
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.sparse_reduce(idx, val, nnz, 100, threads=3)
+    assert e.value.code == oracle.BAD_STREAM
 
 
 @pytest.mark.parametrize("N,seg_len,k_num,k_den", [(50, 16, 3, 8), (37, 5, 2, 5), (64, 64, 1, 100),
@@ -375,6 +499,73 @@ def test_quantizer_draw_depends_only_on_seed_node_index():
     # a different node key changes some draws
     c4, _ = oracle.quantize4(idx[::-1].copy(), val[::-1].copy(), nnz, n, seed=5)
     assert not np.array_equal(unpack(c4, n)[1], l1[0])
+
+
+def sm64_py(x):
+    """SplitMix64 output for state x in Python integers, written from the
+    published algorithm (Steele, Lea and Flood 2014, with Vigna's 64-bit
+    finaliser): add the golden gamma, then two xor-shift-multiply rounds and a
+    last xor-shift."""
+    z = (x + GOLDEN_RATIO_INC) & M64
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & M64
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & M64
+    return z ^ (z >> 31)
+
+
+def test_python_splitmix64_matches_the_published_vector():
+    with open(os.path.join(GOLDEN, "splitmix64_seed1234567.txt")) as f:
+        expect = [int(l) for l in f if l.strip() and not l.startswith("#")]
+    state = 1234567
+    for e in expect:
+        assert sm64_py(state) == e
+        state = (state + GOLDEN_RATIO_INC) & M64
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("seed", [5, 0x0123456789ABCDEF])
+def test_quantizer_draw_key_known_answers(bits, seed):
+    """Known answers for the rounding draw u = (h >> 40) 2^-24 with
+    h = sm(sm(sm(seed) ^ node) ^ index): each case puts frac(r) a hair above
+    or below the u of its (seed, node, index), computed here with the
+    independent Python SplitMix64, so the level (floor(r) or floor(r) + 1)
+    pins the whole key. A slip in the key (a dropped sm(seed), node and index
+    folded into one state, a swapped pair) draws another u and flips about
+    half of the 24 decisions."""
+    s = (1 << (bits - 1)) - 1
+    base = {2: 0, 4: 3, 8: 60}[bits]
+    rng = np.random.default_rng(seed & 0xFFFF)
+    P, per_row = 4, 6
+    f32 = np.float32
+    cap = 2 * per_row
+    idx = np.zeros((P, cap), np.uint32)
+    val = np.zeros((P, cap), f32)
+    expect = np.zeros((P, per_row), np.int64)
+    for p in range(P):
+        ix = np.sort(rng.choice(1 << 32, size=cap, replace=False)).astype(np.uint64)
+        for c in range(per_row):
+            i0, i = int(ix[2 * c]), int(ix[2 * c + 1])
+            h = sm64_py(sm64_py(sm64_py(seed) ^ p) ^ i)
+            u = f32(h >> 40) * f32(1.0 / 16777216.0)
+            up = (c + p) % 2 == 0  # half the cases just above u, half just below
+            target = float(base) + float(u) + (3e-6 if up else -3e-6)
+            if not (0.0 < target - base < 1.0):
+                target = float(base) + 0.5
+            v = f32(target / s)
+            r = f32(f32(v / f32(1.0)) * f32(s))
+            frac = r - np.floor(r)
+            assert abs(float(frac) - float(u)) < 1e-5 or target == base + 0.5
+            expect[p, c] = int(np.floor(r)) + (1 if u < frac else 0)
+            idx[p, 2 * c], idx[p, 2 * c + 1] = i0, i
+            val[p, 2 * c], val[p, 2 * c + 1] = 1.0, v
+    nnz = np.full(P, cap, np.uint32)
+    codes, scales = oracle.quantize(val, 4, bits, seed, idx=idx, nnz=nnz)  # scale 1 per bucket
+    lv = unpack_bits(codes, cap, bits) & s
+    assert (scales == 1.0).all()
+    assert (lv[:, 0::2] == s).all()  # the bucket maximum: r = s exactly
+    assert np.array_equal(lv[:, 1::2], expect)
+    if bits == 4:
+        c4, _ = oracle.quantize4(idx, val, nnz, 4, seed)
+        assert np.array_equal(c4, codes)
 
 
 def unpack_bits(codes, n, bits):
