@@ -3,13 +3,16 @@
 
 One step = one error-feedback step of the whole path for P emulated nodes:
 Top-k with residual (guess, stream and select kernels), packing into
-{uint32 index, fp32 value} streams, and the sparse sum-reduce with the dense
-switch (tile and fix-up kernels). The default workload is the ResNet-50-sized
-one: P=8 nodes of N=25,557,032 fp32 gradients, Top-k 0.1% per 100,000-entry
-layer block. ``value`` is the gradient input consumed per second
-(P * N * 4 bytes per step) with inputs resident in HBM; ``e2e`` is the same
-metric with every step's gradients copied in from pinned host memory and the
-reduced result copied back.
+{uint32 index, fp32 value} streams, b-bit stochastic quantisation where the
+workload has it, and the sparse sum-reduce with the dense switch. The default
+workload is the largest one, LSTM/ASR-like: P=16 nodes of N=67,108,864 fp32
+gradients, Top-k 1% per node, 4-bit quantisation in buckets of 512, fused
+dequantise + sparse reduce. ``value`` is the gradient input the sparse-reduce
+step consumes per second (P * N * 4 bytes per step) with inputs resident in
+HBM; the reduce's own input rate (8 B per stream entry, or the quantised
+form's bytes) and roofline are reported beside it in ``reduce``; ``e2e`` is
+the step with every step's gradients copied in from pinned host memory and
+the reduced result copied back.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun each rank runs an independent replica on its own GPU (the
@@ -47,7 +50,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["resnet50", "asr", "sweep", "logreg", "qsgd", "ssar"],
-                    default="resnet50",
+                    default="asr",
                     help="resnet50/asr: the whole EF step; sweep/logreg: the sparse reduce alone "
                          "on given streams (density-sweep cell / Zipf logistic regression); "
                          "qsgd: b-bit quantisation of a dense reduced result; "
@@ -64,7 +67,9 @@ def parse_args():
     ap.add_argument("--nodes", type=int, default=0,
                     help="override P (smaller device footprint for profiling captures)")
     ap.add_argument("--cpu-segments", type=int, default=48,
-                    help="segments per node in the bounded CPU-baseline sample")
+                    help="resnet50: layer segments per node in the bounded CPU-baseline sample")
+    ap.add_argument("--cpu-entries", type=int, default=1 << 21,
+                    help="asr: entries per node (one segment) in the bounded CPU-baseline sample")
     return ap.parse_args()
 
 
@@ -129,58 +134,107 @@ def reduce_max(x: float, pg: bool, device) -> float:
 # clocks during the timed region
 # ---------------------------------------------------------------------------
 class ClockSampler:
-    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
-              "clocks_event_reasons.hw_thermal_slowdown",
-              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
-    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    """Samples the SM clock, its maximum, the board power and the active
+    clock-event reasons of the benchmarked GPU from a background thread,
+    every few milliseconds, through NVML (the driver's management library,
+    read-only queries), or every 50 ms through nvidia-smi if NVML cannot be
+    loaded. summary(t0, t1) reports the samples inside [t0, t1] (host
+    time.time()); if none fell there it reports the whole sampling run and
+    says so in "window"."""
+    REASONS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+               "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
 
-    def __init__(self, device):
-        self.samples = []
+    def __init__(self, device, period_s: float = 0.002):
+        import ctypes as C
+        self.samples = []  # (time, sm_mhz, max_mhz, power_w, reason bits)
+        self.stop_flag = threading.Event()
         self.proc = None
+        self.source = None
+        uuid = None
         try:
-            ident = str(device.index)
-            try:
-                u = torch.cuda.get_device_properties(device).uuid
-                ident = "GPU-" + str(u) if not str(u).startswith("GPU-") else str(u)
-            except Exception:
-                pass
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
-                 "-i", ident, "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
-                text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
+            u = str(torch.cuda.get_device_properties(device).uuid)
+            uuid = u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            pass
+        try:
+            nv = C.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            h = C.c_void_p()
+            if uuid is None or nv.nvmlDeviceGetHandleByUUID(uuid.encode(), C.byref(h)) != 0:
+                raise OSError("no NVML handle")
+            get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.nv, self.h, self.get_reasons, self.period = nv, h, get_reasons, period_s
+            self.source = "nvml"
+            self.thread = threading.Thread(target=self._poll_nvml, daemon=True)
             self.thread.start()
         except Exception:
+            self._start_smi(uuid if uuid else str(device.index))
+
+    def _poll_nvml(self):
+        import ctypes as C
+        sm, mx, pw, rs = C.c_uint(), C.c_uint(), C.c_uint(), C.c_ulonglong()
+        while not self.stop_flag.is_set():
+            ok = (self.nv.nvmlDeviceGetClockInfo(self.h, 1, C.byref(sm)) == 0 and
+                  self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, C.byref(mx)) == 0)
+            pok = self.nv.nvmlDeviceGetPowerUsage(self.h, C.byref(pw)) == 0
+            rok = self.get_reasons(self.h, C.byref(rs)) == 0
+            if ok:
+                self.samples.append((time.time(), float(sm.value), float(mx.value),
+                                     pw.value / 1000.0 if pok else None,
+                                     int(rs.value) if rok else 0))
+            time.sleep(self.period)
+
+    def _start_smi(self, ident):
+        fields = ["clocks.sm", "clocks.max.sm", "power.draw",
+                  "clocks_event_reasons.sw_power_cap", "clocks_event_reasons.hw_slowdown",
+                  "clocks_event_reasons.sw_thermal_slowdown",
+                  "clocks_event_reasons.hw_thermal_slowdown"]
+        bits = [0x4, 0x8, 0x20, 0x40]
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + ",".join(fields), "--format=csv,noheader,nounits",
+                 "-i", ident, "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except Exception:
             self.proc = None
+            return
+        self.source = "nvidia-smi"
 
-    def _read(self):
-        for line in self.proc.stdout:
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) == len(self.FIELDS):
-                self.samples.append((time.time(), parts))
-
-    def window(self, t0, t1):
-        return [p for (t, p) in self.samples if t0 <= t <= t1]
+        def read():
+            def num(x):
+                try:
+                    return float(x)
+                except ValueError:
+                    return None
+            for line in self.proc.stdout:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) != len(fields) or num(p[0]) is None:
+                    continue
+                r = sum(b for b, x in zip(bits, p[3:]) if x.lower().startswith("active"))
+                self.samples.append((time.time(), num(p[0]), num(p[1]), num(p[2]), r))
+        self.thread = threading.Thread(target=read, daemon=True)
+        self.thread.start()
 
     def summary(self, t0, t1):
-        w = self.window(t0, t1)
+        w = [x for x in self.samples if t0 <= x[0] <= t1]
+        window = "timed region"
         if not w:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        def num(x):
-            try:
-                return float(x)
-            except ValueError:
-                return None
-        sm = [num(p[0]) for p in w if num(p[0]) is not None]
-        mx = [num(p[1]) for p in w if num(p[1]) is not None]
-        reasons = sorted({self.REASONS[i] for p in w for i in range(4)
-                          if p[3 + i].lower().startswith("active")})
-        pw = [num(p[2]) for p in w if num(p[2]) is not None]
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(w),
-                "power_w_max": max(pw) if pw else None}
+            w, window = list(self.samples), "whole run (no sample inside the timed region)"
+        if not w:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "source": self.source}
+        sm = [x[1] for x in w]
+        mx = [x[2] for x in w]
+        pw = [x[3] for x in w if x[3] is not None]
+        reasons = sorted(n for n, b in self.REASONS.items() if any(x[4] & b for x in w))
+        return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm), "sm_max_mhz": max(mx),
+                "reasons": reasons, "samples": len(w), "window": window,
+                "power_w_max": max(pw) if pw else None, "source": self.source}
 
     def stop(self):
+        self.stop_flag.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -202,6 +256,7 @@ def workload_spec(name):
                           "100,000-entry layer block with error feedback, sparse sum-reduce with "
                           "dense switch at 25%"),
                     gen=lambda t, dev: W.resnet50_grads(t, device=dev),
+                    gen_sample=lambda t, n: W.resnet50_grads(t, N=n),
                     data="synthetic: N(0, sigma_b^2), sigma_b log-uniform in [1e-4, 1e-1] per "
                          "100k-entry block (seeded torch generator on device)")
     if name != "asr":
@@ -212,6 +267,7 @@ def workload_spec(name):
                 desc=("LSTM/ASR-like EF step: P=16 x N=67,108,864 fp32, Top-k 1%, 4-bit "
                       "stochastic quantisation in buckets of 512, fused dequantise + sparse reduce"),
                 gen=lambda t, dev: W.asr_grads(t, device=dev),
+                gen_sample=lambda t, n: W.asr_grads(t, N=n),
                 data="synthetic: Laplace(0, 1e-3) (seeded torch generator on device)")
 
 
@@ -220,13 +276,17 @@ def file_sha(path):
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def load_traffic(kernel, src):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current source of the kernel (else None)."""
+CSRC = os.path.join(ROOT, "top_gradient_compression_gb300", "csrc")
+
+
+def load_traffic(kernel, workload, src):
+    """DRAM bytes per launch of `kernel` on `workload` from a committed ncu
+    summary (profiles/traffic.json, keyed "kernel@workload"), if it was taken
+    on the current source of the kernel (else None)."""
     try:
         with open(TRAFFIC_FILE) as f:
             t = json.load(f)
-        e = t[kernel]
+        e = t[f"{kernel}@{workload}"]
         if e.get("source_sha") != file_sha(src):
             return None
         return e
@@ -242,71 +302,103 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
 # ---------------------------------------------------------------------------
 # CPU baseline: the oracle as it stands, on a bounded sample
 # ---------------------------------------------------------------------------
-def cpu_sample_run(spec, grads_host, nseg, steps):
-    """Oracle Top-k+EF and reduce over the first nseg segments of every node for
-    `steps` EF steps. Returns (seconds, bytes of gradient input processed)."""
+def cpu_sample(spec, args, reference=False):
+    """The bounded slice of the workload the oracle is timed on: (entries per
+    node n, segment table of that slice, description). resnet50: the first
+    --cpu-segments layer blocks of every node; asr: the first --cpu-entries
+    entries of every node as one segment at the workload's density (half as
+    many for the per-step reference arm)."""
     import oracle
-    P, L = spec["P"], spec["seg_len"]
-    n = min(spec["N"], nseg * L)
-    res = np.zeros((P, n), np.float32)
-    t0 = time.perf_counter()
-    for s in range(steps):
-        g = grads_host[s % len(grads_host)][:, :n]
-        g = np.ascontiguousarray(g)
-        oi, ov, on = oracle.topk_ef(g, res, L, spec["k_num"], spec["k_den"])
-        if spec["quant"]:
-            from top_gradient_compression_gb300 import workloads as W
-            b = spec.get("bits", 4)
-            codes, scales = oracle.quantize(ov, spec["bucket"], b, W.quant_seed(s), idx=oi, nnz=on)
-            ov = oracle.dequantize(codes, scales, oi.shape[1], spec["bucket"], b, nnz=on)
-        oracle.sparse_reduce(oi, ov, on, n)
-    dt = time.perf_counter() - t0
-    return dt, P * n * 4 * steps, n
+    P, N, L = spec["P"], spec["N"], spec["seg_len"]
+    if spec["name"] == "resnet50":
+        nseg = min(args.cpu_segments if not reference else 8, (N + L - 1) // L)
+        n = min(N, nseg * L)
+        desc = f"the first {nseg} layer blocks ({n:,} entries) of each of the {P} nodes"
+    else:
+        n = min(N, args.cpu_entries if not reference else args.cpu_entries // 2)
+        desc = f"the first {n:,} entries of each of the {P} nodes as one segment"
+    b, k = oracle.uniform_segments(n, min(L, n), spec["k_num"], spec["k_den"])
+    return n, (b, k), desc
+
+
+def cpu_step(spec, g, res, table, step, threads):
+    """One oracle EF step on the sample: Top-k + EF, quantise + dequantise
+    where the workload has it, and the sparse reduce."""
+    import oracle
+    from top_gradient_compression_gb300 import workloads as W
+    oi, ov, on = oracle.topk_ef_segments(g, res, table[0], table[1], threads=threads)
+    if spec["quant"]:
+        b = spec.get("bits", 4)
+        c, sc = oracle.quantize(ov, spec["bucket"], b, W.quant_seed(step), idx=oi, nnz=on)
+        ov = oracle.dequantize(c, sc, oi.shape[1], spec["bucket"], b, nnz=on)
+    oracle.sparse_reduce(oi, ov, on, g.shape[1], threads=threads)
+
+
+def cpu_baseline_run(spec, args, grads_dev):
+    """Times the oracle on the bounded sample, on one host core and on every
+    host core (the same results either way). Returns the cpu_baseline object."""
+    n, table, desc = cpu_sample(spec, args)
+    gh = [grads_dev[b][:, :n].cpu().numpy() for b in range(min(2, len(grads_dev)))]
+    cores = os.cpu_count() or 1
+    out = {}
+    for label, threads in (("one_core", 1), ("all_cores", cores)):
+        res = np.zeros_like(gh[0])
+        t0 = time.perf_counter()
+        for st in range(2):
+            cpu_step(spec, gh[st % len(gh)], res, table, st, threads)
+        dt = time.perf_counter() - t0
+        out[label] = {"GBps": spec["P"] * n * 4 * 2 / dt / 1e9, "seconds": dt, "threads": threads}
+    return {"value": out["all_cores"]["GBps"], "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "cpu_model": cpu_model(), "one_core_value": out["one_core"]["GBps"],
+            "sample": (f"{desc}, 2 EF steps of Top-k + EF" +
+                       (" + quantise/dequantise" if spec["quant"] else "") +
+                       f" + reduce; gradient bytes / time. All {cores} cores: "
+                       f"{out['all_cores']['seconds']:.1f} s; one core: "
+                       f"{out['one_core']['seconds']:.1f} s")}
 
 
 def run_reference(args, ranks):
-    """--impl reference: the CPU oracle timed on host cores (rank 0 only)."""
+    """--impl reference: the CPU oracle timed on every host core (rank 0 only)."""
     if ranks.rank != 0:
         return
-    from top_gradient_compression_gb300 import workloads as W
     if args.workload in ("sweep", "logreg", "qsgd", "ssar"):
         return run_reference_op(args)
     spec = workload_spec(args.workload)
     spec["bits"] = args.bits
-    P, L = spec["P"], spec["seg_len"]
-    nseg = 1
-    n = min(spec["N"], nseg * L)
-    grads = [spec["gen"](0, "cpu")[:, :n].numpy().copy()]
-    import oracle
-    res = np.zeros((P, n), np.float32)
-
-    def step(s):
-        oi, ov, on = oracle.topk_ef(grads[0], res, L, spec["k_num"], spec["k_den"])
-        if spec["quant"]:
-            b = spec.get("bits", 4)
-            c, sc = oracle.quantize(ov, spec["bucket"], b, W.quant_seed(s), idx=oi, nnz=on)
-            ov = oracle.dequantize(c, sc, oi.shape[1], spec["bucket"], b, nnz=on)
-        oracle.sparse_reduce(oi, ov, on, n)
-
-    for s in range(args.warmup):
-        step(s)
+    n, table, desc = cpu_sample(spec, args, reference=True)
+    g = spec["gen_sample"](0, n).numpy()
+    res = np.zeros_like(g)
+    cores = os.cpu_count() or 1
+    for st in range(args.warmup):
+        cpu_step(spec, g, res, table, st, cores)
     t0 = time.perf_counter()
-    for s in range(args.steps):
-        step(s)
+    for st in range(args.steps):
+        cpu_step(spec, g, res, table, st, cores)
     dt = time.perf_counter() - t0
+    P = spec["P"]
     v = P * n * 4 * args.steps / dt / 1e9
-    sample = (f"oracle (1 thread): {nseg} segment(s) of {L} entries per node x {P} nodes "
-              f"= {P * n:,} gradient entries per step")
+    sample = f"oracle on {cores} host threads: {desc} per step"
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s",
             "elems_per_s": P * n * args.steps / dt, "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": spec["data"], "config": {"workload": spec["desc"], "sample": sample},
-            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "cpu_model": cpu_model(), "sample": sample},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -314,9 +406,10 @@ def run_reference(args, ranks):
 
 def run_reference_op(args):
     """--impl reference for the single-operation workloads: the oracle's reduce
-    (sweep, logreg) or quantiser (qsgd) on the same inputs, one host core."""
+    (sweep, logreg), quantiser (qsgd) or SSAR on the same inputs."""
     import oracle
     from top_gradient_compression_gb300 import workloads as W
+    cores = os.cpu_count() or 1
     if args.workload == "logreg":
         idx, val, nnz = W.logreg_streams()
         N = W.LOGREG["N"]
@@ -326,6 +419,7 @@ def run_reference_op(args):
         cell = [(a, b) for a, b in W.SWEEP_D if abs(100.0 * a / b - dpct) < 1e-9][0]
         idx, val, nnz = W.sweep_streams(P, *cell)
         N = W.SWEEP_N
+    threads = 1
     if args.workload == "ssar":
         op = lambda s: oracle.ssar(idx, val, nnz, N)  # noqa: E731
         units = int(nnz.astype(np.int64).sum())
@@ -337,7 +431,8 @@ def run_reference_op(args):
         units, nbytes = N, 4 * N
         desc = f"QSGD {args.bits}-bit on a dense reduced vector, N={N:,}, buckets of 1024"
     else:
-        op = lambda s: oracle.sparse_reduce(idx, val, nnz, N)  # noqa: E731
+        threads = cores
+        op = lambda s: oracle.sparse_reduce(idx, val, nnz, N, threads=cores)  # noqa: E731
         units = int(nnz.astype(np.int64).sum())
         nbytes = 8 * units
         desc = f"sparse reduce of {idx.shape[0]} streams, N={N:,} ({args.workload})"
@@ -348,14 +443,14 @@ def run_reference_op(args):
         op(s)
     dt = time.perf_counter() - t0
     v = nbytes * args.steps / dt / 1e9
-    sample = f"oracle (1 thread): the whole workload, {args.steps} calls"
+    sample = f"oracle ({threads} host thread(s)): the whole workload, {args.steps} calls"
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s",
         "elems_per_s": units * args.steps / dt, "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": desc, "sample": sample},
-        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
         flush=True)
@@ -402,16 +497,21 @@ def run_reduce_only(args, ranks):
                 evs[i][1].record()
                 evs[i][2].record()
 
+    clocks = ClockSampler(dev)
     for i in range(Wm):
         call(i, False)
     torch.cuda.synchronize()
     launches0 = api.launch_count()
+    t_host0 = time.time()
     gpu_head_start(K)
     for i in range(K):
         flush.fill_(float(i))  # inputs do not stay in L2 between timed runs
         call(i, True)
     torch.cuda.synchronize()
+    t_host1 = time.time()
     launches = api.launch_count() - launches0
+    clk = clocks.summary(t_host0, t_host1)
+    clocks.stop()
     if api.get_status(ws) != 0:
         raise RuntimeError("device status set after the timed reduces")
     t_tile = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
@@ -425,8 +525,7 @@ def run_reduce_only(args, ranks):
     achieved = (in_bytes + out_bytes) / (t_tile * 1e-3) / 1e9
     traffic = None
     if args.workload == "sweep":  # counters committed for the largest cell only
-        e = load_traffic(f"reduce_sweep_P{P}_d{dpct:g}",
-                         os.path.join(ROOT, "top_gradient_compression_gb300", "csrc", "reduce.cu"))
+        e = load_traffic("reduce", f"sweep_P{P}_d{dpct:g}", os.path.join(CSRC, "reduce.cu"))
         traffic = None if e is None else e["dram_bytes_per_launch"]
     if ranks.rank != 0:
         return
@@ -445,7 +544,7 @@ def run_reduce_only(args, ranks):
                      "traffic": traffic, "launch_ms": t_tile},
         "kernels_ms": {"reduce_split_tile": t_tile, "reduce_fixup": t_fix},
         "reduce": {"U": U, "is_dense": dense},
-        "gpu_launches": launches}), flush=True)
+        "gpu_launches": launches, "clocks": clk}), flush=True)
 
 
 # ---------------------------------------------------------------------------
@@ -475,7 +574,8 @@ def run_ours(args, ranks):
     tk_ws = api.workspace(api.topk_ef_workspace_size(P, N, L, kn, kd), dev)
     rd_ws = api.workspace(api.reduce_workspace_size(P, N), dev)
     rd_out = api.reduce_out(N, dev)
-    if spec["quant"]:
+    quant = spec["quant"]
+    if quant:
         bucket, qbits = spec["bucket"], args.bits
         codes = torch.zeros((P, (cap + 8 // qbits - 1) // (8 // qbits)), dtype=torch.uint8,
                             device=dev)
@@ -486,32 +586,33 @@ def run_ours(args, ranks):
 
     K, Wm = args.steps, args.warmup
     ev_tk = [api.make_events(4) for _ in range(K)]
-    ev_rd = [api.make_events(3) for _ in range(K)]
-    ev_q = [api.make_events(3) for _ in range(K)] if spec["quant"] else None
+    ev_rd = [api.make_events(3) for _ in range(K)]  # reduce: before, split+tile | finish, after
+    ev_q = [api.make_events(2) for _ in range(K)] if quant else None  # around the quantiser
 
     def step(i, grad, timed=False):
         api.topk_ef(grad, res, L, kn, kd, out=tk_out, ws=tk_ws,
                     events=ev_tk[i] if timed else None)
-        if spec["quant"]:
+        if quant:
             if timed:
                 ev_q[i][0].record()
             api.quantize(tk_out[1], bucket, qbits, W.quant_seed(i), idx=tk_out[0], nnz=tk_out[2],
                          codes=codes, scales=scales, status=qstat)
             if timed:
                 ev_q[i][1].record()
+                ev_rd[i][0].record()
             api.sparse_reduce_qb(tk_out[0], codes, scales, tk_out[2], bucket, qbits, N, out=rd_out,
                                  ws=rd_ws)
             if timed:
-                ev_q[i][2].record()
+                ev_rd[i][1].record()
+                ev_rd[i][2].record()
         else:
             api.sparse_reduce(tk_out[0], tk_out[1], tk_out[2], N, out=rd_out, ws=rd_ws,
                               events=ev_rd[i] if timed else None)
 
+    clocks = ClockSampler(dev)  # samples from before the warm-up to after the timed steps
     for i in range(Wm):
         step(i, grads[i % NB])
     torch.cuda.synchronize()
-    clocks = ClockSampler(dev)
-    time.sleep(1.0)  # let nvidia-smi start sampling
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = api.launch_count()
     ranks.barrier()
@@ -526,9 +627,10 @@ def run_ours(args, ranks):
     ranks.barrier()
     launches = api.launch_count() - launches0
     ms_local = ev0.elapsed_time(ev1) / K
+    time.sleep(0.02)
     clk = clocks.summary(t_host0, t_host1)
     clocks.stop()
-    for word in (tk_ws, rd_ws):
+    for word in (tk_ws, rd_ws) + ((qstat,) if quant else ()):
         st = api.get_status(word)
         if st != 0:
             raise RuntimeError(f"device status {api.STATUS.get(st, st)} after the timed steps")
@@ -538,26 +640,34 @@ def run_ours(args, ranks):
         return float(np.mean([e[a].elapsed_time(e[b]) for e in evs]))
     kern = {"topk_guess": mean_ms(ev_tk, 0, 1), "topk_stream": mean_ms(ev_tk, 1, 2),
             "topk_select": mean_ms(ev_tk, 2, 3)}
-    if spec["quant"]:
+    if quant:
         kern[f"quantize{qbits}"] = mean_ms(ev_q, 0, 1)
-        kern[f"reduce_q{qbits}"] = mean_ms(ev_q, 1, 2)
+        kern[f"reduce_q{qbits}"] = mean_ms(ev_rd, 0, 2)
     else:
         kern["reduce_split_tile"] = mean_ms(ev_rd, 0, 1)
-        kern["reduce_fixup"] = mean_ms(ev_rd, 1, 2)
+        kern["reduce_finish"] = mean_ms(ev_rd, 1, 2)
+    reduce_ms = mean_ms(ev_rd, 0, 2)
 
     U = int(rd_out.nnz.item())
     is_dense = bool(rd_out.is_dense.item())
-    sum_nnz = int(tk_out[2].sum().item())
+    nnz_h = tk_out[2].cpu().numpy().astype(np.int64)
+    sum_nnz = int(nnz_h.sum())
     in_bytes_step = P * N * 4
     value = job_rate(ranks.world, in_bytes_step, ms * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
     stream_bytes = 12 * P * N  # read grad + residual, write residual
     achieved = stream_bytes / (kern["topk_stream"] * 1e-3) / 1e9
-    traffic = load_traffic("topk_stream_kernel",
-                           os.path.join(ROOT, "top_gradient_compression_gb300", "csrc",
-                                        "topk_ef.cu"))
-    reduce_in = (8 * sum_nnz if not spec["quant"] else
-                 sum_nnz * qbits // 8 + 4 * P * ((cap + bucket - 1) // bucket) + 4 * sum_nnz)
+    traffic = load_traffic("topk_stream_kernel", spec["name"], os.path.join(CSRC, "topk_ef.cu"))
+    # the reduce's input (the metric's unit): 8 B per stream entry, or 4 B of
+    # index + b/8 B of code per entry + 4 B per bucket scale when quantised
+    if quant:
+        reduce_in = (4 * sum_nnz + sum(-(-int(n) * qbits // 8) for n in nnz_h) +
+                     4 * sum(-(-int(n) // bucket) for n in nnz_h))
+    else:
+        reduce_in = 8 * sum_nnz
+    reduce_out_bytes = 4 * N if is_dense else 8 * U
+    reduce_achieved = (reduce_in + reduce_out_bytes) / (reduce_ms * 1e-3) / 1e9
+    rtraffic = load_traffic("reduce", spec["name"], os.path.join(CSRC, "reduce.cu"))
 
     # ---- end to end: pinned host gradients in, reduced result out, every step.
     # Step i+1's gradients are copied on a second stream into the other device
@@ -635,14 +745,7 @@ def run_ours(args, ranks):
     # ---- CPU baseline (rank 0, single GPU only)
     cpu = None
     if not args.no_cpu_baseline and ranks.world == 1:
-        nseg = min(args.cpu_segments, (N + L - 1) // L)
-        n = min(N, nseg * L)
-        gh = [grads[b][:, :n].cpu().numpy() for b in range(min(2, NB))]
-        dt, nbytes, _ = cpu_sample_run(spec, gh, nseg, 2)
-        cpu = {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": (f"first {nseg} segments ({n:,} entries) of each of the {P} nodes, 2 EF "
-                          f"steps of Top-k + reduce; {nbytes / 4:,.0f} gradient entries in "
-                          f"{dt:.1f} s on one host core")}
+        cpu = cpu_baseline_run(spec, args, grads)
 
     if ranks.rank != 0:
         return
@@ -653,9 +756,13 @@ def run_ours(args, ranks):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": spec["data"],
         "config": {"workload": spec["desc"], "P": P, "N": N, "seg_len": L,
-                   "k_per_node": cap, "units": "value = P*N*4 gradient bytes per step / time",
-                   "l2": "inputs larger than L2 (3 x 818 MB gradient batches + 818 MB residual), "
-                         "no flush",
+                   "k_per_node": cap,
+                   "units": ("value = P*N*4 gradient bytes entering the sparse-reduce step per "
+                             "second of whole-step time; elems_per_s = gradient entries per "
+                             "second; the reduce's own input rate (the stream bytes it reads) is "
+                             "reduce.input_GBps"),
+                   "l2": (f"inputs larger than L2 ({NB} x {P * N * 4 / 1e6:,.0f} MB gradient "
+                          f"batches + the residual), no flush"),
                    "parallelism": f"replicas x{ranks.world} (no cross-GPU exchange)"},
         "roofline": {"bound": "hbm", "kernel": "topk_stream_kernel",
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -665,10 +772,19 @@ def run_ours(args, ranks):
                      "traffic": None if traffic is None else traffic["dram_bytes_per_launch"],
                      "launch_ms": kern["topk_stream"]},
         "kernels_ms": kern,
-        "reduce": {"input_bytes": reduce_in, "sum_nnz": sum_nnz, "U": U, "is_dense": is_dense,
-                   "input_GBps": reduce_in / ((kern.get("reduce_split_tile", 0) +
-                                               kern.get("reduce_fixup", 0)) * 1e-3) / 1e9
-                   if not spec["quant"] else None},
+        "reduce": {"input_bytes": reduce_in, "output_bytes": reduce_out_bytes,
+                   "sum_nnz": sum_nnz, "U": U, "is_dense": is_dense, "ms": reduce_ms,
+                   "input_GBps": reduce_in / (reduce_ms * 1e-3) / 1e9,
+                   "elems_per_s": sum_nnz / (reduce_ms * 1e-3),
+                   "roofline": {"bound": "hbm",
+                                "kernel": ("fused dequantise + sparse reduce" if quant
+                                           else "sparse reduce") + " (all its launches)",
+                                "achieved": reduce_achieved, "peak": peak, "unit": "GB/s",
+                                "frac": reduce_achieved / peak, "peak_kind": peak_kind,
+                                "algorithmic_bytes_per_launch": reduce_in + reduce_out_bytes,
+                                "traffic": None if rtraffic is None
+                                else rtraffic["dram_bytes_per_launch"],
+                                "launch_ms": reduce_ms}},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,
@@ -710,7 +826,6 @@ def run_qsgd(args, ranks):
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(K)]
     clocks = ClockSampler(dev)
-    time.sleep(1.0)
     t_host0 = time.time()
     gpu_head_start(K)
     for i in range(K):
@@ -780,7 +895,6 @@ def run_ssar(args, ranks):
     torch.cuda.synchronize()
     launches0 = api.launch_count()
     clocks = ClockSampler(dev)
-    time.sleep(1.0)
     t_host0 = time.time()
     gpu_head_start(K)
     for i in range(K):

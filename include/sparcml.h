@@ -28,6 +28,10 @@
  *     All work is enqueued on it and the call returns without waiting:
  *     the calls are non-blocking in the sense of §7 (MPI-3 style
  *     non-blocking collectives). Only sparcml_get_status synchronises.
+ *   - Workspace header. The first 256 bytes of every workspace hold the
+ *     device status word (bytes 0..3) and the fault-injection word (bytes
+ *     32..35, see sparcml_set_fault_injection). Zero the first 64 bytes when
+ *     a workspace is created; the library keeps them from then on.
  *   - Errors. A return value other than SPARCML_OK means nothing was
  *     enqueued (bad argument, workspace too small, capacity too small) or
  *     a CUDA launch failed (SPARCML_ERR_CUDA). Problems found on the device
@@ -68,6 +72,25 @@ const char* sparcml_status_string(int status);
  * (all devices, all threads). Lets a caller count the kernels inside a
  * timed region. */
 uint64_t sparcml_launch_count(void);
+
+/* Testing hook for the failure-detection path (the pages describe no fault
+ * tolerance; this exercises the library's own bounded waits). Writes the
+ * fault-injection word of a workspace (bytes 32..35) on `stream`:
+ *   mode SPARCML_INJECT_WITHHOLD_FIRST: in later sparse-reduce and SSAR
+ *     calls made with this workspace, the first tile (reduce) or each
+ *     pair's first chunk (SSAR) of every decoupled look-back chain withholds
+ *     its published prefix, and every bounded wait gives up after a few
+ *     thousand polls (milliseconds) instead of about two million. The
+ *     waiting tiles record SPARCML_ERR_TIMEOUT in the status word and carry
+ *     on; the outputs of such a call are unspecified, but every memory
+ *     access stays in bounds and the call always completes.
+ *   mode 0: clears it (later calls are normal again).
+ * The word stays as written across calls. A workspace whose first 64 bytes
+ * were zeroed when it was created has no fault armed.
+ * Returns SPARCML_ERR_INVALID_ARG for another mode or a workspace pointer
+ * that is NULL or not 256-byte aligned. */
+#define SPARCML_INJECT_WITHHOLD_FIRST 1
+int sparcml_set_fault_injection(void* ws, int32_t mode, void* stream);
 
 /* Synchronises `stream`, then returns the first device-detected error
  * recorded in the status word at `status_word` (a workspace pointer, or the
@@ -338,7 +361,9 @@ int sparcml_ssar_allreduce_traced(const uint32_t* idx, const float* val, const u
  *   - Device-side errors go to *status (device int32, may be NULL).
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture. The address is kept with the id of the
+ *     context it belongs to: a call in a new context of that device (after
+ *     cudaDeviceReset, say) looks it up again.
  *   - All calls share the array: calls whose work can overlap on the GPU
  *     (different streams, different host threads) race and must be
  *     serialised by the caller. Each call clears what must start at zero.

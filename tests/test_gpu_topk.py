@@ -101,7 +101,9 @@ def test_resnet50_workload_sampled_segments_ten_steps():
     (node, segment) pairs over all 10 EF steps (segments are independent)."""
     c = W.RESNET50
     P, N, L = c["P"], c["N"], c["seg_len"]
-    picks = [(0, 0), (0, 137), (5, 1), (7, 255), (3, 200)]
+    # one segment on every node, node 7's ragged last segment, and a few more
+    picks = [(0, 0), (1, 37), (2, 74), (3, 111), (4, 148), (5, 185), (6, 222), (7, 255),
+             (0, 137), (5, 1), (3, 200)]
     res_g = torch.zeros((P, N), device=DEV)
     ws = api.workspace(api.topk_ef_workspace_size(P, N, L, c["k_num"], c["k_den"]), DEV)
     res_o = {pk: np.zeros((1, min(L, N - pk[1] * L)), np.float32) for pk in picks}
@@ -127,29 +129,34 @@ def test_resnet50_workload_sampled_segments_ten_steps():
 
 
 @pytest.mark.slow
-def test_asr_workload_node0_three_steps_then_quantised_reduce():
+def test_asr_workload_nodes_0_8_15_three_steps_then_quantised_reduce():
     """Full LSTM/ASR-like workload (P=16, N=67,108,864, one segment per node,
-    k=1%, Laplace(0, 1e-3)): node 0's Top-k+EF is checked against the oracle for
-    all 3 steps; then every node's stream is 4-bit quantised (buckets of 512)
-    and reduced with the fused dequantising reduce, checked against the oracle
-    quantiser, dequantiser and map-based sum on the same streams."""
+    k=1%, Laplace(0, 1e-3)): nodes 0, 8 and 15 (whose rows start at byte 0,
+    2^31 and 4.03e9 of the batch) are checked against the oracle on all 3 EF
+    steps, streams and residual; then every node's stream is 4-bit quantised
+    (buckets of 512) and reduced with the fused dequantising reduce, checked
+    against the oracle quantiser, dequantiser and map-based sum."""
     c = W.ASR
     P, N, L = c["P"], c["N"], c["seg_len"]
+    nodes = [0, 8, 15]
     res_g = torch.zeros((P, N), device=DEV)
-    res_o = np.zeros((1, N), np.float32)
+    res_o = np.zeros((len(nodes), N), np.float32)
     ws = api.workspace(api.topk_ef_workspace_size(P, N, L, c["k_num"], c["k_den"]), DEV)
+    seg_b, seg_k = oracle.uniform_segments(N, L, c["k_num"], c["k_den"])
     for t in range(c["steps"]):
         g = W.asr_grads(t, device=DEV)
         idx, val, nnz = api.topk_ef(g, res_g, L, c["k_num"], c["k_den"], ws=ws)
         assert api.get_status(ws) == 0
-        g0 = g[0:1].cpu().numpy()
+        gh = np.stack([g[p].cpu().numpy() for p in nodes])
         del g
-        oi, ov, on = oracle.topk_ef(g0, res_o, L, c["k_num"], c["k_den"])
+        oi, ov, on = oracle.topk_ef_segments(gh, res_o, seg_b, seg_k, threads=len(nodes))
         k = int(on[0])
         assert k == N // 100 and (u32(nnz) == k).all()
-        assert np.array_equal(u32(idx[0]), oi[0, :k])
-        assert np.array_equal(bits(val[0].cpu().numpy()), bits(ov[0, :k]))
-        assert np.array_equal(bits(res_g[0].cpu().numpy()), bits(res_o[0]))
+        for q, p in enumerate(nodes):
+            assert np.array_equal(u32(idx[p]), oi[q, :k]), f"node {p} step {t}: indices"
+            assert np.array_equal(bits(val[p].cpu().numpy()), bits(ov[q, :k])), f"node {p}: values"
+            assert np.array_equal(bits(res_g[p].cpu().numpy()), bits(res_o[q])), f"node {p}: residual"
+    del res_o
     bucket, seed = c["bucket"], W.quant_seed(c["steps"] - 1)
     codes, scales = api.quantize4(idx, val, nnz, bucket, seed)
     hi, hv, hn = u32(idx), val.cpu().numpy(), u32(nnz)
@@ -157,7 +164,7 @@ def test_asr_workload_node0_three_steps_then_quantised_reduce():
     assert np.array_equal(codes.cpu().numpy(), oc)  # k is even: every nibble is valid
     assert np.array_equal(bits(scales.cpu().numpy()), bits(osc))
     deq = oracle.dequantize4(oc, osc, hn, hi.shape[1], bucket)
-    ref = oracle.sparse_reduce(hi, deq, hn, N)
+    ref = oracle.sparse_reduce(hi, deq, hn, N, threads=8)
     out = api.sparse_reduce_q4(idx, codes, scales, nnz, bucket, N)
     U = int(out.nnz.item())
     assert U == ref["nnz"] and not ref["is_dense"] and not bool(out.is_dense.item())

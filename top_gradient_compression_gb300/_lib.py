@@ -21,6 +21,7 @@ vp = C.c_void_p
 SIGNATURES = {
     "sparcml_status_string": (C.c_char_p, [C.c_int]),
     "sparcml_launch_count": (C.c_uint64, []),
+    "sparcml_set_fault_injection": (C.c_int, [vp, C.c_int32, vp]),
     "sparcml_get_status": (C.c_int, [vp, vp]),
     "sparcml_topk_ef_workspace_size": (C.c_size_t, [C.c_int32, C.c_uint64, C.c_uint64,
                                                     C.c_uint32, C.c_uint32]),

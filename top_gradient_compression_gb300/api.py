@@ -60,7 +60,7 @@ def workspace(nbytes: int, device) -> torch.Tensor:
     """Caller-owned scratch for one library call (256-byte aligned by torch's allocator)."""
     ws = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
     assert ws.data_ptr() % 256 == 0
-    ws[:4].zero_()  # status word
+    ws[:64].zero_()  # header: status word, fault-injection word
     return ws
 
 
@@ -83,6 +83,17 @@ def _event_array(events):
         return None
     arr = (C.c_void_p * len(events))(*[e.cuda_event for e in events])
     return arr
+
+
+INJECT_WITHHOLD_FIRST = 1
+
+
+def set_fault_injection(ws: torch.Tensor, mode: int, stream=None):
+    """Arm (mode INJECT_WITHHOLD_FIRST) or clear (0) the workspace's fault
+    injection: later reduce / SSAR calls with ws see their look-back waits run
+    out and record SPARCML_ERR_TIMEOUT (include/sparcml.h)."""
+    _check("sparcml_set_fault_injection",
+           _lib.load().sparcml_set_fault_injection(ws.data_ptr(), int(mode), _stream(stream)))
 
 
 def launch_count() -> int:

@@ -15,6 +15,23 @@ void note_launches(uint64_t n);
 // current device; the runtime call is made once per (device, kernel, size).
 bool ensure_smem(const void* func, size_t bytes);
 
+// Workspace header: the status word at byte 0, the fault-injection word at
+// byte kInjectOffset (written by sparcml_set_fault_injection, kept across
+// calls). The word arms the injection only when it holds kInjectArmed, a
+// pattern that a workspace left uninitialised is very unlikely to contain.
+constexpr size_t kInjectOffset = 32;
+constexpr uint8_t kInjectByte = 0xa5;
+constexpr uint32_t kInjectArmed = 0xa5a5a5a5u;
+// Polls of a bounded wait, normally and while a fault is injected (then a
+// wait that nothing will end gives up within milliseconds).
+constexpr uint32_t kSpinLimit = 1u << 21;
+constexpr uint32_t kInjectSpinLimit = 1u << 12;
+
+// Whether a fault is injected through this workspace word (nullptr: none).
+__device__ __forceinline__ bool injected(const uint32_t* inject) {
+  return inject != nullptr && *reinterpret_cast<const volatile uint32_t*>(inject) == kInjectArmed;
+}
+
 // Record the first device-side error in a status word (never traps).
 __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
   if (status != nullptr) atomicCAS(status, 0, code);

@@ -199,6 +199,17 @@ extern "C" int sparcml_get_status(void* status_word, void* stream) {
   return h;
 }
 
+extern "C" int sparcml_set_fault_injection(void* ws, int32_t mode, void* stream) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255) != 0 || mode < 0 ||
+      mode > SPARCML_INJECT_WITHHOLD_FIRST)
+    return SPARCML_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(static_cast<char*>(ws) + kInjectOffset, mode ? kInjectByte : 0, 4, s) !=
+      cudaSuccess)
+    return SPARCML_ERR_CUDA;
+  return SPARCML_OK;
+}
+
 extern "C" size_t sparcml_pack_workspace_size(int32_t P, uint64_t N) {
   if (P < 1 || P > 65535 || N < 1 || N > 0xffffffffull) return 0;
   return 256 + 2 * pack_chunk_array_bytes(P, N);

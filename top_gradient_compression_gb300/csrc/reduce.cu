@@ -54,7 +54,6 @@ constexpr uint32_t kUnroll = 8;
 constexpr int32_t kMaxReduceP = 4096;
 constexpr unsigned long long kFlagAgg = 1ull << 62;
 constexpr unsigned long long kFlagInc = 2ull << 62;
-constexpr uint32_t kSpinLimit = 1u << 21;
 
 struct ReduceArgs {
   const uint32_t* idx;
@@ -86,6 +85,7 @@ struct ReduceArgs {
   uint32_t* tile_bm;      // dense-first mode: [ntiles][kWords] presence bits per tile
   uint32_t* u_total;      // warp-tile mode: union size, summed by atomics
   int32_t* status;
+  const uint32_t* inject;  // the workspace's fault-injection word (or nullptr)
 };
 
 __device__ __forceinline__ uint32_t lower_bound_u32(const uint32_t* a, uint32_t n, uint32_t x) {
@@ -173,8 +173,12 @@ __device__ void tile_lookback(const ReduceArgs& a, uint32_t tile, uint32_t count
   if (t >= 32) return;
   unsigned long long* st = a.tile_state;
   uint32_t excl = 0;
+  // an injected fault: the chain's first tile withholds its flag and every
+  // wait gives up early (SPARCML_ERR_TIMEOUT)
+  const bool inject = injected(a.inject);
+  const uint32_t limit = inject ? kInjectSpinLimit : kSpinLimit;
   if (tile == 0) {
-    if (t == 0) atomicExch(&st[0], kFlagInc | count);
+    if (t == 0 && !inject) atomicExch(&st[0], kFlagInc | count);
   } else {
     if (t == 0) atomicExch(&st[tile], kFlagAgg | count);
     int64_t base = (int64_t)tile - 1;
@@ -189,7 +193,7 @@ __device__ void tile_lookback(const ReduceArgs& a, uint32_t tile, uint32_t count
       const uint32_t upto = inc ? (uint32_t)(__ffs(inc) - 1) : 31u;  // lanes 0..upto count
       const uint32_t need = upto == 31 ? 0xffffffffu : ((2u << upto) - 1u);
       if (notready & need) {
-        if (++spins > kSpinLimit) {
+        if (++spins > limit) {
           if (t == 0) set_status(a.status, SPARCML_ERR_TIMEOUT);
           break;
         }
@@ -813,8 +817,10 @@ reduce_split_quad_kernel(const uint32_t* __restrict__ idx, const uint32_t* __res
 __device__ uint32_t warp_lookback(const ReduceArgs& a, uint32_t tile, uint32_t count) {
   const uint32_t lane = lane_id();
   unsigned long long* st = a.tile_state;
+  const bool inject = injected(a.inject);
+  const uint32_t limit = inject ? kInjectSpinLimit : kSpinLimit;
   if (tile == 0) {
-    if (lane == 0) atomicExch(&st[0], kFlagInc | count);
+    if (lane == 0 && !inject) atomicExch(&st[0], kFlagInc | count);
     return 0;
   }
   if (lane == 0) atomicExch(&st[tile], kFlagAgg | count);
@@ -831,7 +837,7 @@ __device__ uint32_t warp_lookback(const ReduceArgs& a, uint32_t tile, uint32_t c
     const uint32_t upto = inc ? (uint32_t)(__ffs(inc) - 1) : 31u;  // lanes 0..upto count
     const uint32_t need = upto == 31 ? 0xffffffffu : ((2u << upto) - 1u);
     if (notready & need) {
-      if (++spins > kSpinLimit) {
+      if (++spins > limit) {
         if (lane == 0) set_status(a.status, SPARCML_ERR_TIMEOUT);
         break;
       }
@@ -1550,6 +1556,7 @@ int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
   a.split = split;
   a.tile_bm = reinterpret_cast<uint32_t*>(w + l.bm);
   a.u_total = reinterpret_cast<uint32_t*>(w + 128);  // cleared with the ticket below
+  a.inject = reinterpret_cast<const uint32_t*>(w + kInjectOffset);
   // Clear the ticket and the look-back states (the status word is kept).
   if (cudaMemsetAsync(w + l.ticket, 0, l.info - l.ticket, s) != cudaSuccess)
     return SPARCML_ERR_CUDA;
@@ -1841,6 +1848,8 @@ extern "C" int sparcml_sparse_reduce_qb(const uint32_t* idx, const uint8_t* code
 // calls whose work overlaps on the GPU race; the array keeps the last call's
 // contents and each call clears the words that must start at zero.
 // ---------------------------------------------------------------------------
+#include <cuda.h>
+
 #include <mutex>
 
 namespace sparcml {
@@ -1859,22 +1868,60 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[sparcml::kNoAll
 namespace sparcml {
 namespace {
 std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+struct NoAllocSlot {
+  unsigned long long ctx_id;  // context the address belongs to (0: none yet)
+  void* ptr;
+};
+NoAllocSlot g_noalloc[kNoAllocMaxDevices] = {};
 
-// Device address of the scratch array on the current device. The first call
-// on a device looks it up (cudaGetSymbolAddress, no allocation) and keeps it.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context (0 if none or unknown).
+// The driver functions come through the runtime's entry-point query, so the
+// library does not link the driver library itself.
+unsigned long long current_ctx_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(f);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the scratch array in the current device's context. The
+// first call on a device looks it up (cudaGetSymbolAddress: no allocation)
+// and keeps it with the id of the context it belongs to; a later call in
+// another context (after cudaDeviceReset, say) looks it up again. If the
+// context id cannot be read, the address is looked up on every call.
 int noalloc_scratch(char** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices)
     return SPARCML_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_ptr[dev] == nullptr) {
+  NoAllocSlot& slot = g_noalloc[dev];
+  unsigned long long id = current_ctx_id();
+  if (id == 0 || slot.ctx_id != id || slot.ptr == nullptr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
       return SPARCML_ERR_CUDA;
-    g_noalloc_ptr[dev] = p;
+    slot.ptr = p;
+    slot.ctx_id = current_ctx_id();  // the lookup made the context current if it was not
   }
-  *out = static_cast<char*>(g_noalloc_ptr[dev]);
+  *out = static_cast<char*>(slot.ptr);
   return SPARCML_OK;
 }
 }  // namespace

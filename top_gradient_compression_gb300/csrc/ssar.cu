@@ -35,7 +35,6 @@ constexpr uint32_t kMergeThreads = 256;  // kChunk / kMergeThreads positions per
 constexpr uint32_t kPerThread = kChunk / kMergeThreads;
 constexpr unsigned long long kAggFlag = 1ull << 62;
 constexpr unsigned long long kIncFlag = 2ull << 62;
-constexpr uint32_t kWaitLimit = 1u << 21;
 
 struct Pair {
   const uint32_t* a_idx;
@@ -63,6 +62,7 @@ struct StageArgs {
   uint32_t* ticket;
   unsigned long long* fill;   // stage fill-in (may be null)
   int32_t* status;
+  const uint32_t* inject;    // the workspace's fault-injection word
   bool validate;            // stage 0: check the caller's streams
 };
 
@@ -129,8 +129,12 @@ __global__ void __launch_bounds__(256) ssar_partition_kernel(StageArgs s) {
 __device__ uint32_t chunk_lookback(const StageArgs& s, uint64_t slot0, uint32_t c, uint32_t count) {
   const uint32_t lane = lane_id();
   unsigned long long* st = s.state + slot0;
+  // an injected fault: each pair's first chunk withholds its flag and every
+  // wait gives up early (SPARCML_ERR_TIMEOUT)
+  const bool inject = injected(s.inject);
+  const uint32_t limit = inject ? kInjectSpinLimit : kSpinLimit;
   if (c == 0) {
-    if (lane == 0) atomicExch(&st[0], kIncFlag | count);
+    if (lane == 0 && !inject) atomicExch(&st[0], kIncFlag | count);
     return 0;
   }
   if (lane == 0) atomicExch(&st[c], kAggFlag | count);
@@ -147,7 +151,7 @@ __device__ uint32_t chunk_lookback(const StageArgs& s, uint64_t slot0, uint32_t 
     const uint32_t upto = inc ? (uint32_t)(__ffs(inc) - 1) : 31u;
     const uint32_t need = upto == 31 ? 0xffffffffu : ((2u << upto) - 1u);
     if (notready & need) {
-      if (++spins > kWaitLimit) {
+      if (++spins > limit) {
         if (lane == 0) set_status(s.status, SPARCML_ERR_TIMEOUT);
         break;
       }
@@ -365,6 +369,7 @@ extern "C" int sparcml_ssar_allreduce_traced(const uint32_t* idx, const float* v
     a.ticket = reinterpret_cast<uint32_t*>(w + l.ticket);
     a.fill = stage_nnz ? stage_nnz + st : nullptr;
     a.status = reinterpret_cast<int32_t*>(w);
+    a.inject = reinterpret_cast<const uint32_t*>(w + kInjectOffset);
     a.validate = st == 0;
     if ((uint64_t)G * a.chunks > (uint64_t)P / 2 * l.chunks0) return SPARCML_ERR_WORKSPACE;
     // the ticket and this stage's look-back words start at zero
