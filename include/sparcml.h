@@ -99,47 +99,90 @@ int sparcml_set_fault_injection(void* ws, int32_t mode, void* stream);
 int sparcml_get_status(void* status_word, void* stream);
 
 /* ------------------------------------------------------------------------
- * Top-k selection with error feedback, fused with packing (§2.2, §4, §5.1;
- * layer-wise sparsification of §8.4 via segments; last segment takes the
- * remainder as in App. A).
+ * Top-k selection with error feedback, fused with packing (§2.2, §4, §5.1),
+ * over a table of segments: the layer-wise sparsification of §8.4, where
+ * every layer of the model keeps its own number of components.
  *
  * For every node p and every element i:
- *     acc = residual[p][i] + grad[p][i]            (one fp32 add, RN)
- * Each node is cut into segments [s*seg_len, min((s+1)*seg_len, N)) of
- * length n_s; segment s keeps exactly k_s = floor(n_s * k_num / k_den)
- * entries: those with the largest |acc|, comparing the bit patterns of
- * |acc| as unsigned integers, ties going to the lowest index. The kept
- * entries are written to node p's stream in ascending index order
- * (segment after segment), with val = acc; out_nnz[p] = sum of k_s.
- * residual[p][i] becomes +0.0f at kept entries and acc everywhere else.
+ *     acc = residual[p][i] + grad[p][i]            (one fp32 add, RN; a NaN
+ *                                                   result is 0x7fffffff)
+ * Segment s of every node is [seg_begin[s], seg_begin[s+1]) and keeps
+ * exactly seg_k[s] entries: those with the largest |acc|, comparing the bit
+ * patterns of |acc| as unsigned integers (so any NaN ranks above +-inf, which
+ * rank above every finite value), ties going to the lowest index. Node p's
+ * stream holds the kept entries of segment 0, then segment 1, ..., each in
+ * ascending index order (so the stream is ascending), with val = acc;
+ * out_nnz[p] = sum of seg_k. residual[p][i] becomes +0.0f at kept entries
+ * and acc everywhere else.
  *
  *   grad      [P][N] fp32, read only.
  *   residual  [P][N] fp32, read and overwritten in place (the EF state).
- *   seg_len   segment length, >= 1 (values >= N mean one segment per node).
- *   k_num, k_den  density d = k_num / k_den, 0 <= k_num <= k_den < 2^32.
- *   out_idx, out_val  [P][cap]; out_nnz [P].  cap >= sum of k_s, else
- *             SPARCML_ERR_CAPACITY.
- *   ws        >= sparcml_topk_ef_workspace_size(P, N, seg_len, k_num, k_den)
- *             bytes, 256-byte aligned.
- * Non-finite inputs are not rejected; NaN has the largest magnitude key.
+ *   seg_begin HOST array of nseg + 1 entries: seg_begin[0] = 0 <
+ *             seg_begin[1] < ... < seg_begin[nseg] = N (no empty segment).
+ *   seg_k     HOST array of nseg entries, seg_k[s] <= seg_begin[s+1] -
+ *             seg_begin[s] (0 keeps nothing, the length keeps everything).
+ *             Both host arrays are read during the call only; the library
+ *             copies what the GPU needs into the workspace on `stream`
+ *             through kernel parameters (no host-side staging buffer, no
+ *             synchronisation).
+ *   out_idx, out_val  [P][cap]; out_nnz [P]. cap >= sparcml_topk_total_k,
+ *             else SPARCML_ERR_CAPACITY.
+ *   ws        >= sparcml_topk_ef_workspace_size(P, N, seg_begin, seg_k, nseg)
+ *             bytes, 256-byte aligned; the same table must be passed to both.
+ * A table that breaks the rules above returns SPARCML_ERR_INVALID_ARG.
+ * 128-bit loads are used when grad and residual are 16-byte aligned
+ * (whatever the segment offsets); other pointers take a slower scalar path.
  * ------------------------------------------------------------------------ */
-size_t sparcml_topk_ef_workspace_size(int32_t P, uint64_t N, uint64_t seg_len,
-                                      uint32_t k_num, uint32_t k_den);
+size_t sparcml_topk_ef_workspace_size(int32_t P, uint64_t N, const uint64_t* seg_begin,
+                                      const uint32_t* seg_k, uint32_t nseg);
 int sparcml_topk_ef(const float* grad, float* residual, int32_t P, uint64_t N,
-                    uint64_t seg_len, uint32_t k_num, uint32_t k_den,
-                    uint32_t* out_idx, float* out_val, uint32_t* out_nnz,
-                    uint64_t cap, void* ws, size_t ws_bytes, void* stream);
+                    const uint64_t* seg_begin, const uint32_t* seg_k, uint32_t nseg,
+                    uint32_t* out_idx, float* out_val, uint32_t* out_nnz, uint64_t cap,
+                    void* ws, size_t ws_bytes, void* stream);
 
 /* Same as sparcml_topk_ef, plus a profiling hook: `events` is a host array
  * of 4 cudaEvent_t (entries may be NULL; the array itself may be NULL),
- * recorded on `stream` before the guess kernel, before the stream kernel,
- * before the select kernel and after it, so a caller can time each kernel
- * with CUDA events on the launching stream. */
+ * recorded on `stream` before the table upload and guess kernels, before the
+ * stream kernel, before the select kernels and after them, so a caller can
+ * time each phase with CUDA events on the launching stream. */
 int sparcml_topk_ef_traced(const float* grad, float* residual, int32_t P, uint64_t N,
-                           uint64_t seg_len, uint32_t k_num, uint32_t k_den,
-                           uint32_t* out_idx, float* out_val, uint32_t* out_nnz,
-                           uint64_t cap, void* ws, size_t ws_bytes, void* stream,
-                           void* const* events);
+                           const uint64_t* seg_begin, const uint32_t* seg_k, uint32_t nseg,
+                           uint32_t* out_idx, float* out_val, uint32_t* out_nnz, uint64_t cap,
+                           void* ws, size_t ws_bytes, void* stream, void* const* events);
+
+/* Diagnostic: synchronises `stream`, then returns how many (node, segment)
+ * pairs the last sparcml_topk_ef call made with workspace `ws` decided by
+ * re-reading the segment (the raw select), because its sampled guess did not
+ * leave enough candidates, a candidate sub-slot overflowed or the boundary
+ * bin was too large; -1 on a CUDA error. The results are the same either
+ * way; a count above zero on ordinary data means lost speed, not accuracy. */
+int64_t sparcml_topk_ef_fallbacks(const void* ws, void* stream);
+
+/* Capacity a stream needs for a table: the sum of seg_k (0 for NULL). */
+uint64_t sparcml_topk_total_k(const uint32_t* seg_k, uint32_t nseg);
+
+/* The equal-segment table (App. A: the last segment takes the remainder):
+ * segment s = [s*L, min((s+1)*L, N)) with L = min(seg_len, N), keeping
+ * k_s = floor(n_s * k_num / k_den) entries (density d = k_num / k_den).
+ * Returns nseg (0 for N = 0, N >= 2^32, seg_len = 0, k_den = 0 or
+ * k_num > k_den) and, where the host pointers are not NULL, writes
+ * seg_begin[0 .. nseg] and seg_k[0 .. nseg - 1]. */
+uint32_t sparcml_topk_uniform_segments(uint64_t N, uint64_t seg_len, uint32_t k_num,
+                                       uint32_t k_den, uint64_t* seg_begin, uint32_t* seg_k);
+
+/* Convenience forms over the equal-segment table above: identical to
+ * sparcml_topk_ef(_traced) called with that table. */
+size_t sparcml_topk_ef_uniform_workspace_size(int32_t P, uint64_t N, uint64_t seg_len,
+                                              uint32_t k_num, uint32_t k_den);
+int sparcml_topk_ef_uniform(const float* grad, float* residual, int32_t P, uint64_t N,
+                            uint64_t seg_len, uint32_t k_num, uint32_t k_den,
+                            uint32_t* out_idx, float* out_val, uint32_t* out_nnz, uint64_t cap,
+                            void* ws, size_t ws_bytes, void* stream);
+int sparcml_topk_ef_uniform_traced(const float* grad, float* residual, int32_t P, uint64_t N,
+                                   uint64_t seg_len, uint32_t k_num, uint32_t k_den,
+                                   uint32_t* out_idx, float* out_val, uint32_t* out_nnz,
+                                   uint64_t cap, void* ws, size_t ws_bytes, void* stream,
+                                   void* const* events);
 
 /* ------------------------------------------------------------------------
  * Pack a naturally sparse dense batch into streams (§5.1): node p's stream

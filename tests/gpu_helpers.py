@@ -23,7 +23,15 @@ def streams_to_dev(idx, val, nnz):
             torch.from_numpy(np.ascontiguousarray(nnz).view(np.int32)).to(DEV))
 
 
-def check_topk_steps(grads, seg_len, k_num, k_den, res0=None):
+def check_fallbacks(ws, fallback):
+    """fallback False: no (node, segment) was decided by the raw select; True:
+    at least one was; None: either."""
+    n = api.topk_fallbacks(ws)
+    if fallback is not None:
+        assert (n > 0) == fallback, f"raw-select fallbacks: {n}"
+
+
+def check_topk_steps(grads, seg_len, k_num, k_den, res0=None, fallback=None):
     """Run the EF steps on GPU and oracle side by side; everything must match bitwise."""
     P, N = grads[0].shape
     res_o = np.zeros((P, N), np.float32) if res0 is None else res0.copy()
@@ -34,9 +42,35 @@ def check_topk_steps(grads, seg_len, k_num, k_den, res0=None):
         idx, val, nnz = api.topk_ef(gg, res_g, seg_len, k_num, k_den, ws=ws)
         st = api.get_status(ws)
         assert st == 0, api.STATUS[st]
+        check_fallbacks(ws, fallback)
         oi, ov, on = oracle.topk_ef(g, res_o, seg_len, k_num, k_den, cap=idx.shape[1])
         gn = u32(nnz)
         assert np.array_equal(gn, on)
+        gi, gv = u32(idx), bits(val.cpu().numpy())
+        for p in range(P):
+            n = int(on[p])
+            assert np.array_equal(gi[p, :n], oi[p, :n]), f"node {p}: indices differ"
+            assert np.array_equal(gv[p, :n], bits(ov[p, :n])), f"node {p}: values differ"
+        assert np.array_equal(bits(res_g.cpu().numpy()), bits(res_o)), "residual differs"
+    return res_o
+
+
+def check_topk_table_steps(grads, seg_begin, seg_k, res0=None, fallback=None):
+    """The segment-table form over several EF steps against the oracle, bitwise:
+    streams, nnz and the residual after every step."""
+    P, N = grads[0].shape
+    res_o = np.zeros((P, N), np.float32) if res0 is None else res0.copy()
+    res_g = torch.from_numpy(res_o.copy()).to(DEV)
+    ws = api.workspace(api.topk_ef_segments_workspace_size(P, N, seg_begin, seg_k), DEV)
+    for g in grads:
+        gg = torch.from_numpy(np.ascontiguousarray(g)).to(DEV)
+        idx, val, nnz = api.topk_ef_segments(gg, res_g, seg_begin, seg_k, ws=ws)
+        st = api.get_status(ws)
+        assert st == 0, api.STATUS[st]
+        check_fallbacks(ws, fallback)
+        oi, ov, on = oracle.topk_ef_segments(g, res_o, seg_begin, seg_k, cap=idx.shape[1],
+                                             threads=4)
+        assert np.array_equal(u32(nnz), on)
         gi, gv = u32(idx), bits(val.cpu().numpy())
         for p in range(P):
             n = int(on[p])

@@ -46,36 +46,52 @@ def test_status_strings_and_launch_counter():
 
 def test_workspace_sizes():
     lib = _lib.load()
-    assert lib.sparcml_topk_ef_workspace_size(0, 10, 10, 1, 100) == 0
-    assert lib.sparcml_topk_ef_workspace_size(1, 10, 10, 2, 1) == 0  # k_num > k_den
-    assert lib.sparcml_topk_ef_workspace_size(1, 1 << 32, 10, 1, 100) == 0  # N too large
-    small = lib.sparcml_topk_ef_workspace_size(4, 65536, 65536, 1, 100)
-    big = lib.sparcml_topk_ef_workspace_size(8, 25_557_032, 100_000, 1, 1000)
+    ws = lib.sparcml_topk_ef_uniform_workspace_size
+    assert ws(0, 10, 10, 1, 100) == 0
+    assert ws(1, 10, 10, 2, 1) == 0  # k_num > k_den
+    assert ws(1, 1 << 32, 10, 1, 100) == 0  # N too large
+    small = ws(4, 65536, 65536, 1, 100)
+    big = ws(8, 25_557_032, 100_000, 1, 1000)
     assert 0 < small < big
     assert small % 256 == 0 and big % 256 == 0
     # candidate slots are bounded by the input size: at most 8 bytes per entry + overhead
     assert big < 8 * 8 * 25_557_032
+    b, k = api.uniform_segments(25_557_032, 100_000, 1, 1000)
+    assert api.topk_ef_segments_workspace_size(8, 25_557_032, b, k) == big
     assert lib.sparcml_sparse_reduce_workspace_size(64, 4_194_304) > 0
     assert lib.sparcml_sparse_reduce_workspace_size(5000, 100) == 0  # P above the limit
     assert lib.sparcml_pack_workspace_size(2, 100) >= 256
 
 
 def test_topk_host_validation_returns_before_launch():
+    import numpy as np
     lib = _lib.load()
-    ws = lib.sparcml_topk_ef_workspace_size(2, 1000, 100, 1, 10)
-    args = dict(grad=FAKE, res=FAKE, P=2, N=1000, L=100, kn=1, kd=10, oi=FAKE, ov=FAKE, on=FAKE,
-                cap=100, ws=FAKE, wsb=ws, s=None)
+    good_b = np.array([0, 1, 8, 500, 1000], np.uint64)
+    good_k = np.array([0, 7, 5, 100], np.uint32)
+    ws = api.topk_ef_segments_workspace_size(2, 1000, good_b, good_k)
+    assert ws > 0
 
-    def call(**kw):
-        a = dict(args, **kw)
-        return lib.sparcml_topk_ef(a["grad"], a["res"], a["P"], a["N"], a["L"], a["kn"], a["kd"],
-                                   a["oi"], a["ov"], a["on"], a["cap"], a["ws"], a["wsb"], a["s"])
-    assert call(grad=None) == api.STATUS_CODE["SPARCML_ERR_INVALID_ARG"]
-    assert call(P=0) == 1 and call(N=0) == 1 and call(L=0) == 1 and call(kd=0) == 1
-    assert call(kn=11) == 1
-    assert call(ws=FAKE + 8) == 1  # workspace must be 256-byte aligned
-    assert call(wsb=ws - 1) == 2
-    assert call(cap=99) == 3  # 10 segments x 10 entries do not fit
+    def call(b=good_b, k=good_k, nseg=None, P=2, N=1000, cap=112, w=FAKE, wsb=ws, grad=FAKE):
+        b = np.ascontiguousarray(b, np.uint64)
+        k = np.ascontiguousarray(k, np.uint32)
+        return lib.sparcml_topk_ef(grad, FAKE, P, N, b.ctypes.data, k.ctypes.data,
+                                   k.size if nseg is None else nseg, FAKE, FAKE, FAKE, cap, w, wsb,
+                                   None)
+    bad = api.STATUS_CODE["SPARCML_ERR_INVALID_ARG"]
+    assert call(grad=None) == bad and call(P=0) == bad and call(N=0) == bad
+    assert call(nseg=0) == bad
+    assert call(b=[1, 8, 500, 1000, 1000]) == bad      # does not start at 0
+    assert call(b=[0, 1, 8, 500, 999]) == bad          # does not end at N
+    assert call(b=[0, 8, 8, 500, 1000]) == bad         # an empty segment
+    assert call(k=[2, 7, 5, 100]) == bad               # k_s > n_s
+    assert call(w=FAKE + 8) == bad                     # workspace must be 256-byte aligned
+    assert call(wsb=ws - 1) == api.STATUS_CODE["SPARCML_ERR_WORKSPACE"]
+    assert call(cap=111) == api.STATUS_CODE["SPARCML_ERR_CAPACITY"]  # 112 entries per node
+    uw = lib.sparcml_topk_ef_uniform_workspace_size(2, 1000, 100, 1, 10)
+    u = lib.sparcml_topk_ef_uniform
+    assert u(FAKE, FAKE, 2, 1000, 0, 1, 10, FAKE, FAKE, FAKE, 100, FAKE, uw, None) == bad
+    assert u(FAKE, FAKE, 2, 1000, 100, 11, 10, FAKE, FAKE, FAKE, 100, FAKE, uw, None) == bad
+    assert u(FAKE, FAKE, 2, 1000, 100, 1, 10, FAKE, FAKE, FAKE, 99, FAKE, uw, None) == 3
 
 
 def test_reduce_and_other_host_validation():
@@ -122,11 +138,21 @@ def test_reduce_and_other_host_validation():
               None) == 2
 
 
-def test_segment_k_total_matches_the_oracle_rule():
+def test_equal_segment_table_matches_the_oracle_rule():
+    """The library's equal-segment table and its k rounding (floor, the last
+    segment takes the remainder) agree with the oracle's."""
     import oracle
     for N, L, kn, kd in [(65_536, 65_536, 1, 100), (25_557_032, 100_000, 1, 1000), (1001, 7, 3, 8),
                          (10, 100, 1, 1), (33, 1, 1, 2)]:
+        b, k = api.uniform_segments(N, L, kn, kd)
+        ob, ok = oracle.uniform_segments(N, L, kn, kd)
+        assert list(b) == ob and list(k) == ok
         assert api.segment_k_total(N, L, kn, kd) == sum(oracle.segment_ks(N, L, kn, kd))
+    lib = _lib.load()
+    assert lib.sparcml_topk_uniform_segments(0, 10, 1, 2, None, None) == 0
+    assert lib.sparcml_topk_uniform_segments(10, 0, 1, 2, None, None) == 0
+    assert lib.sparcml_topk_uniform_segments(10, 3, 3, 2, None, None) == 0
+    assert lib.sparcml_topk_total_k(None, 5) == 0
 
 
 def test_binding_arity_matches_the_header():

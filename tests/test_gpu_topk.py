@@ -7,7 +7,7 @@ import torch
 import oracle
 from top_gradient_compression_gb300 import api, workloads as W
 
-from gpu_helpers import DEV, bits, check_topk_steps, u32
+from gpu_helpers import DEV, bits, check_topk_steps, check_topk_table_steps, u32
 
 pytestmark = pytest.mark.gpu
 
@@ -29,25 +29,80 @@ def make(dist, P, N, seed):
 def test_tiny_workload_three_steps():
     c = W.TINY
     grads = [W.tiny_grads(t).numpy() for t in range(c["steps"])]
-    check_topk_steps(grads, c["seg_len"], c["k_num"], c["k_den"])
+    check_topk_steps(grads, c["seg_len"], c["k_num"], c["k_den"], fallback=False)
 
 
-@pytest.mark.parametrize("P,N,seg_len,k_num,k_den,dist", [
-    (3, 1001, 100, 3, 100, "normal"),          # node bases not 16-byte aligned
-    (2, 50_000, 7_000, 1, 50, "ties"),          # ragged segments, heavy ties
-    (1, 3 * 8192 + 5, 8192, 1, 10, "normal"),   # chunk-sized segments + ragged tail
-    (2, 40, 1, 1, 1, "normal"),                 # segment length 1, k = n
-    (2, 1000, 1000, 0, 1, "normal"),            # k = 0
-    (2, 777, 777, 1, 1, "ties"),                # k = n with ties
-    (1, 1 << 21, 1 << 21, 1, 100, "normal"),    # one long segment: 4-CTA cluster
-    (2, 4_194_304, 4_194_304, 1, 100, "laplace"),  # 8-CTA cluster
-    (2, 300_000, 100_000, 1, 1000, "normal"),   # layer-sized segments, k = 100
-    (4, 65_536, 65_536, 30, 100, "ties"),       # dense selection (30%)
-    (2, 20_000, 20_000, 1, 100, "const"),       # all keys equal: lowest indices win
+@pytest.mark.parametrize("P,N,seg_len,k_num,k_den,dist,fallback", [
+    (3, 1001, 100, 3, 100, "normal", False),         # node bases not 16-byte aligned
+    (2, 50_000, 7_000, 1, 50, "ties", False),         # ragged segments, heavy ties
+    (1, 3 * 8192 + 5, 8192, 1, 10, "normal", False),  # chunk-sized segments + ragged tail
+    (2, 40, 1, 1, 1, "normal", False),                # segment length 1, k = n
+    (2, 1000, 1000, 0, 1, "normal", False),           # k = 0
+    (2, 777, 777, 1, 1, "ties", False),               # k = n with ties
+    (1, 1 << 21, 1 << 21, 1, 100, "normal", False),   # one long segment
+    (2, 4_194_304, 4_194_304, 1, 100, "laplace", False),  # long segments
+    (2, 300_000, 100_000, 1, 1000, "normal", False),  # layer-sized segments, k = 100
+    (4, 65_536, 65_536, 30, 100, "ties", False),      # 30 %: range-parallel select, ties
+    (2, 20_000, 20_000, 1, 100, "const", True),       # all keys equal: sub-slots overflow
 ])
-def test_topk_shapes(P, N, seg_len, k_num, k_den, dist):
+def test_topk_shapes(P, N, seg_len, k_num, k_den, dist, fallback):
     grads = [make(dist, P, N, s) for s in range(2)]
-    check_topk_steps(grads, seg_len, k_num, k_den)
+    check_topk_steps(grads, seg_len, k_num, k_den, fallback=fallback)
+
+
+def table(lens, ks):
+    return [0] + list(np.cumsum(lens).astype(int)), list(ks)
+
+
+def test_topk_segment_table_mixed_sizes():
+    """Layer-wise sparsification over a ragged table in one call (§8.4):
+    segments of 1, 7, 100,000 and more than 2^18 entries, every kind of
+    segment (k = 0, k = n, sampled whole, layer-sized, long), offsets that are
+    not multiples of 4, k_s from 0 to n_s."""
+    lens = [1, 7, 100_000, 300_001, 1, 7, 13, 8_192, 8_193, 262_144, 262_147, 1_100_000, 5]
+    ks = [0, 7, 100, 3_000, 1, 0, 13, 81, 1_000, 2_621, 26_214, 11_000, 2]
+    P = 3
+    b, k = table(lens, ks)
+    grads = [make("normal", P, b[-1], 40 + t) for t in range(3)]
+    check_topk_table_steps(grads, b, k, fallback=False)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_topk_segment_table_random(seed):
+    rng = np.random.default_rng(500 + seed)
+    lens = list(rng.choice([1, 3, 64, 1_000, 9_000, 70_000, 300_000], size=24))
+    ks = [int(rng.integers(0, n + 1)) if rng.random() < 0.3 else max(0, n // 100) for n in lens]
+    b, k = table(lens, ks)
+    P = 2
+    grads = [make("laplace" if seed % 2 else "normal", P, b[-1], 60 + 3 * seed + t)
+             for t in range(2)]
+    check_topk_table_steps(grads, b, k)
+
+
+def test_topk_long_segments_keep_all_none_and_dense():
+    """Long segments (> 2^18) that keep nothing, everything (written straight
+    from the stream pass), 90 % (candidates almost everywhere) and 0.01 %."""
+    lens = [300_000, 400_003, 600_000, 350_000]
+    ks = [0, 400_003, 540_000, 35]
+    b, k = table(lens, ks)
+    grads = [make("normal", 2, b[-1], 70 + t) for t in range(2)]
+    check_topk_table_steps(grads, b, k, fallback=False)
+
+
+@pytest.mark.parametrize("dist", ["ties", "const"])
+def test_topk_long_segment_falls_back_to_the_raw_select(dist):
+    """A long segment whose candidates cannot decide the select (a boundary
+    bin far above its buffer, or sub-slots that overflow): the raw select
+    re-reads the segment's acc and gives the same bits."""
+    P, N = 2, 1 << 21
+    grads = [make(dist, P, N, 80 + t) for t in range(2)]
+    # the first EF step sees the raw tie groups; later steps add the residual,
+    # which splits them, so only the first step is sure to fall back
+    check_topk_steps(grads[:1], N, 1, 100, fallback=True)
+    check_topk_steps(grads, N, 1, 100)
+    b, k = table([N // 2 + 3, N // 2 - 3], [10_000, 5])
+    check_topk_table_steps(grads[:1], b, k, fallback=True)
+    check_topk_table_steps(grads, b, k)
 
 
 def test_topk_const_keeps_lowest_indices():
@@ -69,7 +124,7 @@ def test_topk_sample_overestimates_then_falls_back():
     for i in range(n_runs):
         st = (i * (N - run) // (n_runs - 1)) & ~(run - 1)
         g[0, st:st + run] = 10.0 + i
-    check_topk_steps([g], N, 1, 100)  # k = 10,485 > 8,192 sampled entries
+    check_topk_steps([g], N, 1, 100, fallback=True)  # k = 10,485 > 8,192 sampled entries
 
 
 def test_topk_nonzero_initial_residual():

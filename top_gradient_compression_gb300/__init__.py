@@ -11,10 +11,12 @@ The compute lives in libsparcml.so (CUDA, C ABI in include/sparcml.h);
 """
 from .api import (ReduceOut, SparcmlError, densify, dequantize4, get_status, launch_count,
                   pack, quantize4, reduce_out, reduce_workspace_size, segment_k_total,
-                  sparse_reduce, sparse_reduce_q4, status_word, topk_ef,
-                  topk_ef_workspace_size, workspace)
+                  sparse_reduce, sparse_reduce_q4, status_word, topk_ef, topk_ef_segments,
+                  topk_ef_segments_workspace_size, topk_ef_workspace_size, total_k,
+                  uniform_segments, workspace)
 
 __all__ = ["ReduceOut", "SparcmlError", "densify", "dequantize4", "get_status", "launch_count",
            "pack", "quantize4", "reduce_out", "reduce_workspace_size", "segment_k_total",
-           "sparse_reduce", "sparse_reduce_q4", "status_word", "topk_ef",
-           "topk_ef_workspace_size", "workspace"]
+           "sparse_reduce", "sparse_reduce_q4", "status_word", "topk_ef", "topk_ef_segments",
+           "topk_ef_segments_workspace_size", "topk_ef_workspace_size", "total_k",
+           "uniform_segments", "workspace"]

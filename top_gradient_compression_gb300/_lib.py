@@ -23,13 +23,23 @@ SIGNATURES = {
     "sparcml_launch_count": (C.c_uint64, []),
     "sparcml_set_fault_injection": (C.c_int, [vp, C.c_int32, vp]),
     "sparcml_get_status": (C.c_int, [vp, vp]),
-    "sparcml_topk_ef_workspace_size": (C.c_size_t, [C.c_int32, C.c_uint64, C.c_uint64,
-                                                    C.c_uint32, C.c_uint32]),
-    "sparcml_topk_ef": (C.c_int, [vp, vp, C.c_int32, C.c_uint64, C.c_uint64, C.c_uint32,
-                                  C.c_uint32, vp, vp, vp, C.c_uint64, vp, C.c_size_t, vp]),
-    "sparcml_topk_ef_traced": (C.c_int, [vp, vp, C.c_int32, C.c_uint64, C.c_uint64, C.c_uint32,
-                                         C.c_uint32, vp, vp, vp, C.c_uint64, vp, C.c_size_t, vp,
-                                         vp]),
+    "sparcml_topk_ef_workspace_size": (C.c_size_t, [C.c_int32, C.c_uint64, vp, vp, C.c_uint32]),
+    "sparcml_topk_ef": (C.c_int, [vp, vp, C.c_int32, C.c_uint64, vp, vp, C.c_uint32, vp, vp, vp,
+                                  C.c_uint64, vp, C.c_size_t, vp]),
+    "sparcml_topk_ef_traced": (C.c_int, [vp, vp, C.c_int32, C.c_uint64, vp, vp, C.c_uint32, vp,
+                                         vp, vp, C.c_uint64, vp, C.c_size_t, vp, vp]),
+    "sparcml_topk_ef_fallbacks": (C.c_int64, [vp, vp]),
+    "sparcml_topk_total_k": (C.c_uint64, [vp, C.c_uint32]),
+    "sparcml_topk_uniform_segments": (C.c_uint32, [C.c_uint64, C.c_uint64, C.c_uint32,
+                                                   C.c_uint32, vp, vp]),
+    "sparcml_topk_ef_uniform_workspace_size": (C.c_size_t, [C.c_int32, C.c_uint64, C.c_uint64,
+                                                            C.c_uint32, C.c_uint32]),
+    "sparcml_topk_ef_uniform": (C.c_int, [vp, vp, C.c_int32, C.c_uint64, C.c_uint64, C.c_uint32,
+                                          C.c_uint32, vp, vp, vp, C.c_uint64, vp, C.c_size_t,
+                                          vp]),
+    "sparcml_topk_ef_uniform_traced": (C.c_int, [vp, vp, C.c_int32, C.c_uint64, C.c_uint64,
+                                                 C.c_uint32, C.c_uint32, vp, vp, vp, C.c_uint64,
+                                                 vp, C.c_size_t, vp, vp]),
     "sparcml_pack_workspace_size": (C.c_size_t, [C.c_int32, C.c_uint64]),
     "sparcml_pack": (C.c_int, [vp, C.c_int32, C.c_uint64, C.c_float, vp, vp, vp, C.c_uint64,
                                vp, C.c_size_t, vp]),

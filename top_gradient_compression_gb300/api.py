@@ -13,6 +13,7 @@ from __future__ import annotations
 import ctypes as C
 from dataclasses import dataclass
 
+import numpy as _np
 import torch
 
 from . import _lib
@@ -106,50 +107,122 @@ def get_status(word: torch.Tensor, stream=None) -> int:
 
 
 # ---------------------------------------------------------------------------
-# Top-k with error feedback (§2.2, §4) fused with packing (§5.1).
+# Top-k with error feedback (§2.2, §4) fused with packing (§5.1), over a
+# segment table (layer-wise sparsification, §8.4).
 # ---------------------------------------------------------------------------
-def topk_ef_workspace_size(P: int, N: int, seg_len: int, k_num: int, k_den: int) -> int:
-    return int(_lib.load().sparcml_topk_ef_workspace_size(P, N, seg_len, k_num, k_den))
+def _table(seg_begin, seg_k):
+    """Host arrays of a segment table: (seg_begin uint64 [nseg+1], seg_k uint32 [nseg])."""
+    b = _np.ascontiguousarray(_np.asarray(seg_begin, dtype=_np.uint64))
+    k = _np.ascontiguousarray(_np.asarray(seg_k, dtype=_np.uint32))
+    if b.ndim != 1 or k.ndim != 1 or b.size != k.size + 1:
+        raise ValueError("seg_begin needs nseg + 1 entries and seg_k nseg")
+    return b, k
+
+
+def uniform_segments(N: int, seg_len: int, k_num: int, k_den: int):
+    """The library's equal-segment table: (seg_begin uint64 [nseg+1], seg_k uint32 [nseg])."""
+    lib = _lib.load()
+    n = int(lib.sparcml_topk_uniform_segments(N, seg_len, k_num, k_den, None, None))
+    if n == 0:
+        raise ValueError("invalid equal-segment table parameters")
+    b = _np.zeros(n + 1, _np.uint64)
+    k = _np.zeros(n, _np.uint32)
+    lib.sparcml_topk_uniform_segments(N, seg_len, k_num, k_den, b.ctypes.data, k.ctypes.data)
+    return b, k
+
+
+def total_k(seg_k) -> int:
+    """Entries a node's stream holds for a table (the capacity it needs)."""
+    k = _np.ascontiguousarray(_np.asarray(seg_k, dtype=_np.uint32))
+    return int(_lib.load().sparcml_topk_total_k(k.ctypes.data, k.size))
 
 
 def segment_k_total(N: int, seg_len: int, k_num: int, k_den: int) -> int:
-    L = min(seg_len, N)
-    nseg = (N + L - 1) // L
-    return (nseg - 1) * (L * k_num // k_den) + (N - (nseg - 1) * L) * k_num // k_den
+    return total_k(uniform_segments(N, seg_len, k_num, k_den)[1])
 
 
-def topk_ef(grad: torch.Tensor, residual: torch.Tensor, seg_len: int, k_num: int, k_den: int,
-            out=None, ws: torch.Tensor | None = None, stream=None, events=None):
-    """Returns (idx int32 [P, cap], val float32 [P, cap], nnz int32 [P]); residual is updated.
-    ``events``: optional 4 CUDA events (see make_events) recorded around the three kernels."""
+def topk_fallbacks(ws: torch.Tensor, stream=None) -> int:
+    """(node, segment) pairs the last Top-k call with ws decided by re-reading
+    the segment (same results, slower); synchronises the stream."""
+    n = int(_lib.load().sparcml_topk_ef_fallbacks(ws.data_ptr(), _stream(stream)))
+    if n < 0:
+        raise SparcmlError("sparcml_topk_ef_fallbacks", 7)
+    return n
+
+
+def topk_ef_workspace_size(P: int, N: int, seg_len: int, k_num: int, k_den: int) -> int:
+    return int(_lib.load().sparcml_topk_ef_uniform_workspace_size(P, N, seg_len, k_num, k_den))
+
+
+def topk_ef_segments_workspace_size(P: int, N: int, seg_begin, seg_k) -> int:
+    b, k = _table(seg_begin, seg_k)
+    return int(_lib.load().sparcml_topk_ef_workspace_size(P, N, b.ctypes.data, k.ctypes.data,
+                                                          k.size))
+
+
+def _topk_out(out, P, cap, device):
+    if out is None:
+        out = (torch.empty((P, max(cap, 1)), dtype=torch.int32, device=device),
+               torch.empty((P, max(cap, 1)), dtype=torch.float32, device=device),
+               torch.empty((P,), dtype=torch.int32, device=device))
+    idx, val, nnz = out
+    return out, (_cuda(idx, torch.int32, "out_idx", 2), _cuda(val, torch.float32, "out_val", 2),
+                 _cuda(nnz, torch.int32, "out_nnz", 1), idx.shape[1])
+
+
+def _grad_res(grad, residual):
     gp = _cuda(grad, torch.float32, "grad", 2)
     rp = _cuda(residual, torch.float32, "residual", 2)
     if residual.shape != grad.shape:
         raise ValueError("grad and residual shapes differ")
+    return gp, rp
+
+
+def topk_ef(grad: torch.Tensor, residual: torch.Tensor, seg_len: int, k_num: int, k_den: int,
+            out=None, ws: torch.Tensor | None = None, stream=None, events=None):
+    """Equal segments of seg_len, density k_num/k_den. Returns (idx int32 [P, cap],
+    val float32 [P, cap], nnz int32 [P]); residual is updated. ``events``: optional
+    4 CUDA events (see make_events) recorded around the phases."""
+    gp, rp = _grad_res(grad, residual)
     P, N = grad.shape
-    if out is None:
-        cap = max(segment_k_total(N, seg_len, k_num, k_den), 1)
-        out = (torch.empty((P, cap), dtype=torch.int32, device=grad.device),
-               torch.empty((P, cap), dtype=torch.float32, device=grad.device),
-               torch.empty((P,), dtype=torch.int32, device=grad.device))
-    idx, val, nnz = out
-    ip = _cuda(idx, torch.int32, "out_idx", 2)
-    vp = _cuda(val, torch.float32, "out_val", 2)
-    np_ = _cuda(nnz, torch.int32, "out_nnz", 1)
-    cap = idx.shape[1]
+    out, (ip, vp, np_, cap) = _topk_out(out, P, segment_k_total(N, seg_len, k_num, k_den)
+                                        if out is None else 0, grad.device)
     if ws is None:
         ws = workspace(topk_ef_workspace_size(P, N, seg_len, k_num, k_den), grad.device)
     lib = _lib.load()
     if events is None:
-        _check("sparcml_topk_ef", lib.sparcml_topk_ef(
+        _check("sparcml_topk_ef_uniform", lib.sparcml_topk_ef_uniform(
             gp, rp, P, N, seg_len, k_num, k_den, ip, vp, np_, cap, ws.data_ptr(), ws.numel(),
             _stream(stream)))
     else:
         assert len(events) == 4
-        _check("sparcml_topk_ef_traced", lib.sparcml_topk_ef_traced(
+        _check("sparcml_topk_ef_uniform_traced", lib.sparcml_topk_ef_uniform_traced(
             gp, rp, P, N, seg_len, k_num, k_den, ip, vp, np_, cap, ws.data_ptr(), ws.numel(),
             _stream(stream), _event_array(events)))
-    return idx, val, nnz
+    return out
+
+
+def topk_ef_segments(grad: torch.Tensor, residual: torch.Tensor, seg_begin, seg_k, out=None,
+                     ws: torch.Tensor | None = None, stream=None, events=None):
+    """Segment s = [seg_begin[s], seg_begin[s+1]) keeps seg_k[s] entries (host
+    arrays). Returns (idx, val, nnz) as topk_ef; residual is updated."""
+    gp, rp = _grad_res(grad, residual)
+    P, N = grad.shape
+    b, k = _table(seg_begin, seg_k)
+    out, (ip, vp, np_, cap) = _topk_out(out, P, total_k(k) if out is None else 0, grad.device)
+    if ws is None:
+        ws = workspace(topk_ef_segments_workspace_size(P, N, b, k), grad.device)
+    lib = _lib.load()
+    if events is None:
+        _check("sparcml_topk_ef", lib.sparcml_topk_ef(
+            gp, rp, P, N, b.ctypes.data, k.ctypes.data, k.size, ip, vp, np_, cap, ws.data_ptr(),
+            ws.numel(), _stream(stream)))
+    else:
+        assert len(events) == 4
+        _check("sparcml_topk_ef_traced", lib.sparcml_topk_ef_traced(
+            gp, rp, P, N, b.ctypes.data, k.ctypes.data, k.size, ip, vp, np_, cap, ws.data_ptr(),
+            ws.numel(), _stream(stream), _event_array(events)))
+    return out
 
 
 # ---------------------------------------------------------------------------

@@ -3,40 +3,53 @@
 // "SparCML: High-Performance Sparse Communication for Machine Learning",
 // §2.2 (Top-k SGD: each node sends its k largest-magnitude components and
 // accumulates the rest for the next iteration), §4 (residual error), §5.1
-// (sparse streams of index-value pairs), §8.4 (layer-wise sparsification,
-// here: segments), App. A (the last part takes the remainder).
+// (sparse streams of index-value pairs), §8.4 (layer-wise sparsification:
+// every segment of the caller's layer table keeps its own k_s).
 //
-// Exact selection in three launches, all stream-ordered:
+// The host turns the caller's segment table into per-segment records and
+// hands them to the GPU as the parameters of a small upload kernel (kernel
+// parameters are copied at launch, so this needs no host-side staging, no
+// allocation and no synchronisation). Then, stream-ordered:
 //
-//  1. guess  (one CTA per segment). Computes acc = residual + grad on a
-//     sample of the segment (all of it when it is short, else 256 runs of
-//     32 consecutive entries) and picks a key G low enough that, with
-//     overwhelming probability, at least k_s entries of the whole segment
-//     have |acc| key >= G. For a fully sampled segment G <= the exact k-th
-//     key, so coverage is certain.
+//  1. init     chunk descriptors and the per-(node, segment) state.
+//  2. guess    per (node, segment): acc = residual + grad on a sample (all of
+//              a segment of up to 8,192 entries), and G = the r-th largest
+//              sample key with its low 15 bits cleared, r chosen so that, with
+//              overwhelming probability, at least k_s keys of the whole
+//              segment are >= G (certainly so for a fully sampled segment).
+//              Long segments also get a histogram scale from a second, higher
+//              sample quantile.
+//  3. stream   the HBM-bound pass (one CTA per 8,192-entry chunk of a
+//              segment): reads grad and residual once with 128-bit loads
+//              aligned on the element grid, writes acc back into residual,
+//              and compacts the candidates (key >= G) in index order into the
+//              warp's own sub-slot. A segment that keeps everything (k = n) is
+//              written straight to the stream here; one that keeps nothing
+//              never has candidates. For long segments every candidate is also
+//              counted in a 2,048-bin histogram of (key - G) >> shift.
+//  4. select   layer-sized segments: one CTA per segment selects among its
+//              candidates in shared memory (four 8-bit radix digits) and
+//              writes the kept entries in index order. Long segments: the
+//              histogram's boundary bin; the candidates in that bin collected;
+//              the exact k-th key T and the index cut I_T among keys equal to
+//              T (lowest indices first) from a select in shared memory; an
+//              ordered write of every candidate with key > T, or key == T and
+//              index <= I_T. Whatever the candidates cannot decide (the guess
+//              covered fewer than k_s entries, a sub-slot or the boundary
+//              buffer overflowed) is decided again from the segment's acc
+//              (now in residual) by a raw select: the answer is the same.
 //
-//  2. stream (one CTA per 8192-entry chunk, the HBM-bound pass). Reads grad
-//     and residual once with 128-bit loads, writes acc back into residual
-//     with 128-bit stores, and compacts the chunk's candidates (key >= G)
-//     into a per-chunk slot in index order (warp ballots). Counts go to the
-//     chunk and to its segment.
-//
-//  3. select (one thread-block cluster per segment). If the candidates do
-//     not cover k_s (or a chunk slot overflowed) the cluster falls back to
-//     reading the segment's acc directly; the answer is the same either
-//     way. A three-digit radix select over the candidates, with the
-//     histograms summed through distributed shared memory, gives the exact
-//     k-th key T and how many entries equal to T to keep (lowest indices
-//     first). An ordered compaction then writes the kept entries ascending
-//     and sets residual = +0.0f at each of them.
-//
-// Only the stream pass touches all of grad and residual: 12 bytes per
-// entry plus a few percent for candidates.
+// The kept entries go to the node's stream in ascending index order, at the
+// segment's offset (the sum of the k of the segments before it); the residual
+// becomes +0.0f at every kept entry.
 
 #include <cooperative_groups.h>
 
 #include <algorithm>
 #include <cmath>
+#include <map>
+#include <mutex>
+#include <vector>
 
 #include "common.cuh"
 
@@ -48,56 +61,103 @@ namespace {
 constexpr uint32_t kChunk = 8192;         // entries per stream-pass CTA
 constexpr uint32_t kStreamThreads = 256;  // 8 warps x 1024 entries
 constexpr uint32_t kWarpsPerChunk = kStreamThreads / 32;
-constexpr uint32_t kSub = kChunk / kWarpsPerChunk;            // entries per warp: 1,024
-constexpr uint32_t kRounds = kSub / (32 * 4);                  // float4 rounds per warp
-constexpr uint32_t kSampleMax = 8192;     // sample of a long segment
-constexpr uint32_t kSampleShort = 4096;   // sample of a layer-sized segment
-constexpr uint32_t kShortSegment = 1u << 18;
-constexpr uint32_t kRun = 256;  // consecutive entries per sample run (1 KB per array)
+constexpr uint32_t kSub = kChunk / kWarpsPerChunk;  // entries per warp sub-chunk: 1,024
+constexpr uint32_t kRounds = kSub / (32 * 4);       // float4 rounds per warp
+constexpr uint32_t kExactMax = 8192;      // segments sampled whole
+constexpr uint32_t kLayerMax = 1u << 18;  // layer-sized: warp guess, one-CTA select
+constexpr uint32_t kSampleLong = 8192;    // sample of a long segment
+constexpr uint32_t kWarpSample = 2048;    // sample of a layer-sized segment
+constexpr uint32_t kRun = 256;            // consecutive entries per sample run
 constexpr uint32_t kGuessThreads = 256;
-constexpr uint32_t kSelectThreads = 256;
-constexpr uint32_t kSmallCands = 4096;  // candidates a select CTA keeps in shared memory
-constexpr uint32_t kWin = 1024;  // chunks per window in the select pass
 constexpr uint32_t kNone = 0xffffffffu;
+constexpr uint32_t kBins = 2048;          // histogram of a long segment's candidates
+constexpr uint32_t kRangeSubs = 256;      // sub-chunks per long-select range
+constexpr uint32_t kBoundCap = 16384;     // boundary-bin entries per (node, long segment)
+constexpr uint32_t kMaxRanges = 16384;    // ranges of one long segment (n < 2^32)
+constexpr uint32_t kUploadWords = 7680;   // 30 KB of kernel parameters per upload launch
+constexpr size_t kFallbackOffset = 68;     // workspace header: raw-select count of the last call
 
-struct Geo {
-  uint64_t N;        // entries per node
-  uint64_t cap;      // stream capacity per node
-  uint32_t L;        // segment length (last segment may be shorter)
-  uint32_t L_last;
-  uint32_t nseg;     // segments per node
-  uint32_t m;        // chunks per full segment
-  uint32_t m_last;   // chunks in the last segment
-  uint32_t nchunk;   // chunks per node
-  uint32_t k_full;   // k of a full segment
-  uint32_t k_last;   // k of the last segment
-  uint32_t slot;     // candidate slot capacity per warp sub-chunk
-  int32_t P;
-  // rank r of the guess in a sample (see sample_rank), per segment kind:
-  // the warp guess's sample and the CTA guess's sample
-  uint32_t r_warp_full, r_warp_last, r_cta_full, r_cta_last;
+// Segment kinds (what the guess and select passes do with a segment).
+enum : uint32_t { kKeepNone = 0, kKeepAll = 1, kExact = 2, kLayer = 3, kLong = 4 };
+
+// One segment of the caller's table, identical for every node (12 words).
+struct SegRec {
+  uint32_t begin;   // node-local first entry
+  uint32_t n;       // entries
+  uint32_t k;       // entries kept
+  uint32_t out0;    // offset of the segment's kept entries in a node's stream
+  uint32_t chunk0;  // first node-local chunk
+  uint32_t nchunk;  // chunks: ceil((n + 3) / kChunk) (quads aligned on the element grid)
+  uint32_t slot;    // candidate entries per warp sub-slot, a multiple of 32
+  uint32_t slot32;  // node-local base of the segment's sub-slots, in units of 32 entries
+  uint32_t rank;    // guess rank r (low 16 bits) and histogram anchor rank (high 16 bits)
+  uint32_t kind;
+  uint32_t lidx;    // position among the long segments (kLong), else kNone
+  uint32_t range0;  // first long-select range of the segment (kLong)
+};
+static_assert(sizeof(SegRec) == 48, "segment record layout");
+
+// One chunk of a segment (two 16-byte words, loaded together).
+struct ChunkDesc {
+  uint32_t begin, end, seg, j;    // the segment's node-local range, its id, the chunk's place
+  uint32_t slot, slot32, kind, aux;  // sub-slot size and base/32; kind; out0 (kKeepAll) or lidx
+};
+static_assert(sizeof(ChunkDesc) == 32, "chunk descriptor layout");
+
+// Per (node, long segment): the select's state.
+enum : uint32_t { kModeNormal = 0, kModeFallback = 1 };
+struct LongSel {
+  uint32_t mode, bin, rank, T, cut, overflow, pad0, pad1;
 };
 
-__device__ __forceinline__ uint32_t seg_n(const Geo& g, uint32_t s) {
-  return s == g.nseg - 1 ? g.L_last : g.L;
+struct UploadBatch {
+  uint32_t words[kUploadWords];
+  uint32_t* dst;
+  uint32_t count;
+};
+
+__global__ void __launch_bounds__(256) topk_upload_kernel(const __grid_constant__ UploadBatch b) {
+  for (uint32_t i = threadIdx.x; i < b.count; i += blockDim.x) b.dst[i] = b.words[i];
 }
-__device__ __forceinline__ uint32_t seg_k(const Geo& g, uint32_t s) {
-  return s == g.nseg - 1 ? g.k_last : g.k_full;
-}
-__device__ __forceinline__ uint32_t seg_chunks(const Geo& g, uint32_t s) {
-  return s == g.nseg - 1 ? g.m_last : g.m;
-}
-// Node-local chunk c -> segment s, chunk j inside it.
-__device__ __forceinline__ void chunk_pos(const Geo& g, uint32_t c, uint32_t* s, uint32_t* j) {
-  const uint32_t full = (g.nseg - 1) * g.m;
-  if (c >= full) {
-    *s = g.nseg - 1;
-    *j = c - full;
-  } else {
-    *s = c / g.m;
-    *j = c % g.m;
-  }
-}
+
+struct Args {
+  const float* grad;
+  float* residual;
+  uint32_t* out_idx;
+  float* out_val;
+  uint32_t* out_nnz;
+  int32_t* status;
+  uint64_t N;
+  uint64_t cap;
+  uint64_t node_slots;  // candidate sub-slot entries per node
+  int32_t P;
+  uint32_t nseg, nchunk, nlong, nranges;
+  uint32_t total_k;
+  uint32_t vec;         // grad and residual 16-byte aligned: 128-bit loads on the element grid
+  uint32_t u_L, u_m;    // equal segments of u_L entries and u_m chunks each (0: another table)
+  const SegRec* recs;
+  ChunkDesc* desc;
+  const uint32_t* cta_list;   // segments guessed by one CTA (exact and long kinds)
+  const uint32_t* warp_list;  // segments guessed by one warp (layer kind)
+  const uint32_t* short_list; // segments selected by one CTA (exact and layer kinds)
+  const uint32_t* long_list;  // long segments, by lidx
+  const uint32_t* range_map;  // long-select range -> lidx << 16 | range within the segment
+  uint2* guess;               // [P][nseg] (G, histogram shift)
+  uint32_t* seg_cnt;          // [P][nseg] candidates
+  uint32_t* seg_flag;         // [P][nseg] a sub-slot overflowed
+  uint32_t* sub_cnt;          // [P][nchunk][8] candidates per warp sub-chunk
+  uint32_t* cand_idx;         // [P][node_slots]
+  float* cand_val;
+  uint32_t* todo;             // layer-sized segments left to the raw select: p * nseg + s
+  uint32_t* todo_cnt;
+  uint32_t* fallbacks;        // (node, segment) pairs the raw select decided in this call
+  uint32_t* hist;             // [P][nlong][kBins]
+  LongSel* lsel;              // [P][nlong]
+  uint32_t* bnd_cnt;          // [P][nlong]
+  uint2* bnd;                 // [P][nlong][kBoundCap] (key, index)
+  uint32_t* range_gt;         // [P][nranges]: candidates above the boundary bin
+  uint32_t* range_off;        // [P][nranges]: output offset of the range in its segment
+};
 
 // Among bins ordered from high to low, find b with
 //   above(b) = sum_{b' > b} h[b'] < r <= above(b) + h[b],   r >= 1.
@@ -128,87 +188,77 @@ __device__ void find_from_top(const uint32_t* h, uint32_t nbins, uint32_t r, uin
 }
 
 // ---------------------------------------------------------------------------
-// 1. guess: one CTA per (node, segment). The sample keys stay in registers
-// (KPT per thread); G = the r-th largest sample key with its low 15 bits
-// cleared, found bit by bit (16 block-wide counts, no histogram).
+// 1. init: one grid-stride pass over every item of per-call state: the chunk
+// descriptors (chunk -> segment by a binary search over the records), the
+// per-(node, segment) counters and guesses of the trivial kinds, the
+// long-select state and histograms, and the nodes' stream sizes.
 // ---------------------------------------------------------------------------
-template <uint32_t KPT>
-__global__ void __launch_bounds__(kGuessThreads)
-topk_guess_kernel(const float* __restrict__ grad, const float* __restrict__ residual, Geo g,
-                  uint32_t* __restrict__ guess, uint32_t* __restrict__ seg_cnt,
-                  uint32_t* __restrict__ seg_flag, uint32_t* __restrict__ out_nnz,
-                  uint32_t total_k, uint32_t* __restrict__ todo_cnt) {
-  constexpr uint32_t kWarps = kGuessThreads / 32;
-  __shared__ uint32_t wsum[2][kWarps];
-
-  const uint32_t gs = blockIdx.x;
-  const uint32_t p = gs / g.nseg, s = gs % g.nseg;
-  const uint32_t n = seg_n(g, s), k = seg_k(g, s);
-  const uint32_t t = threadIdx.x, lane = lane_id(), warp = t >> 5;
-  if (t == 0) {
-    if (gs == 0) *todo_cnt = 0;
-    seg_cnt[gs] = 0;
-    seg_flag[gs] = 0;
-    if (s == 0) out_nnz[p] = total_k;
-  }
-  if (k == 0) {
-    if (t == 0) guess[gs] = kNone;  // no key reaches it: no candidates
-    return;
-  }
-  if (k >= n) {
-    if (t == 0) guess[gs] = 0;  // everything is kept
-    return;
-  }
-  const uint64_t base = (uint64_t)p * g.N + (uint64_t)s * g.L;
-  const float* gp = grad + base;
-  const float* rp = residual + base;
-
-  // Sample: all of a segment of at most kSampleMax entries; else runs of kRun
-  // consecutive entries (1 KB per array: whole DRAM bursts), fewer for
-  // layer-sized segments whose candidate sets are small anyway.
-  const bool exact = n <= kSampleMax;
-  const uint32_t S = exact ? n : (n <= kShortSegment ? kSampleShort : kSampleMax);
-  const uint32_t r = exact ? k : (s == g.nseg - 1 ? g.r_cta_last : g.r_cta_full);
-  // All sample loads are issued before any is used.
-  uint32_t pos[KPT];
-  bool ok[KPT];
-  if (exact) {
-#pragma unroll
-    for (uint32_t q = 0; q < KPT; ++q) {
-      pos[q] = t + q * kGuessThreads;
-      ok[q] = pos[q] < S;
-    }
-  } else {
-    // Runs of kRun consecutive entries spread evenly over the segment; warp w
-    // reads runs w * (KPT / kLinesPerRun) + ..., each as kRun / 32 coalesced
-    // 128-byte lines per array.
-    const uint32_t nruns = S / kRun;
-    constexpr uint32_t kLinesPerRun = kRun / 32;
-#pragma unroll
-    for (uint32_t q = 0; q < KPT; q += kLinesPerRun) {
-      const uint32_t run = warp * (KPT / kLinesPerRun) + q / kLinesPerRun;
-      const uint32_t st =
-          run < nruns
-              ? (uint32_t)(((uint64_t)run * (n - kRun) / (nruns - 1)) & ~(uint64_t)(kRun - 1))
-              : 0u;
-#pragma unroll
-      for (uint32_t l = 0; l < kLinesPerRun; ++l) {
-        pos[q + l] = st + l * 32 + lane;
-        ok[q + l] = run < nruns;
+__global__ void __launch_bounds__(256) topk_init_kernel(Args a) {
+  const uint64_t n_desc = a.nchunk, n_seg = (uint64_t)a.P * a.nseg;
+  const uint64_t n_long = (uint64_t)a.P * a.nlong, n_hist = n_long * kBins;
+  const uint64_t total = n_desc + n_seg + n_long + n_hist + (uint64_t)a.P;
+  for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (uint64_t)gridDim.x * blockDim.x) {
+    if (i < n_desc) {
+      const uint32_t c = (uint32_t)i;
+      uint32_t lo = 0, hi = a.nseg;  // the segment s with chunk0[s] <= c < chunk0[s + 1]
+      while (hi - lo > 1) {
+        const uint32_t m = (lo + hi) >> 1;
+        if (a.recs[m].chunk0 <= c) lo = m; else hi = m;
       }
+      const SegRec r = a.recs[lo];
+      const uint32_t j = c - r.chunk0;
+      ChunkDesc d;
+      d.begin = r.begin;
+      d.end = r.begin + r.n;
+      d.seg = lo;
+      d.j = j;
+      d.slot = r.slot;
+      d.slot32 = r.slot32 + j * kWarpsPerChunk * (r.slot / 32);
+      d.kind = r.kind;
+      d.aux = r.kind == kLong ? r.lidx : r.out0;
+      a.desc[c] = d;
+      continue;
+    }
+    uint64_t x = i - n_desc;
+    if (x < n_seg) {
+      const uint32_t s = (uint32_t)(x % a.nseg);
+      const uint32_t kind = a.recs[s].kind;
+      a.seg_cnt[x] = 0;
+      a.seg_flag[x] = 0;
+      if (kind == kKeepNone) a.guess[x] = make_uint2(kNone, 0);
+      if (kind == kKeepAll) a.guess[x] = make_uint2(0, 0);
+      continue;
+    }
+    x -= n_seg;
+    if (x < n_long) {
+      a.bnd_cnt[x] = 0;
+      a.lsel[x].overflow = 0;
+      continue;
+    }
+    x -= n_long;
+    if (x < n_hist) {
+      a.hist[x] = 0;
+      continue;
+    }
+    x -= n_hist;
+    a.out_nnz[x] = a.total_k;
+    if (x == 0) {
+      *a.todo_cnt = 0;
+      *a.fallbacks = 0;
     }
   }
-  float ra[KPT], ga[KPT];
-#pragma unroll
-  for (uint32_t q = 0; q < KPT; ++q) {
-    ra[q] = ok[q] ? rp[pos[q]] : 0.0f;
-    ga[q] = ok[q] ? gp[pos[q]] : 0.0f;
-  }
-  uint32_t key[KPT];
-#pragma unroll
-  for (uint32_t q = 0; q < KPT; ++q) key[q] = ok[q] ? mag_key(__fadd_rn(ra[q], ga[q])) : kNone;
-  // Bitwise radix select on the 2^15 grid: the largest G with at least r
-  // sample keys >= G, i.e. the r-th largest key with its low 15 bits cleared.
+}
+
+// ---------------------------------------------------------------------------
+// 2. guess.
+// ---------------------------------------------------------------------------
+// Largest G on the 2^15 grid with at least r of the block's keys >= G (the
+// r-th largest key with its low 15 bits cleared), keys held KPT per thread.
+template <uint32_t KPT>
+__device__ uint32_t block_rank_key(const uint32_t (&key)[KPT], uint32_t r, uint32_t (*wsum)[8]) {
+  constexpr uint32_t kWarps = kGuessThreads / 32;
+  const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
   uint32_t G = 0;
 #pragma unroll 1
   for (int bit = 30; bit >= 15; --bit) {
@@ -225,82 +275,125 @@ topk_guess_kernel(const float* __restrict__ grad, const float* __restrict__ resi
     for (uint32_t w = 0; w < kWarps; ++w) tot += ws[w];
     if (tot >= r) G = trial;
   }
-  const uint32_t prefix = G >> 15;
-  if (t == 0) guess[gs] = prefix << 15;
+  return G;
 }
 
-// Layer-sized segments (kSampleMax < n <= kShortSegment): one warp per
-// segment, no block barrier. The 2,048-entry sample (8 runs of kRun) sits in
-// registers, 64 keys per lane; G is the same function of the sample as in
-// topk_guess_kernel (the r-th largest key with its low 15 bits cleared).
-constexpr uint32_t kWarpSample = 2048;
+// Histogram scale of a long segment: the smallest shift with
+// (anchor - G) >> shift < kBins.
+__device__ __forceinline__ uint32_t hist_shift(uint32_t G, uint32_t anchor) {
+  if (anchor <= G) return 0;
+  const uint32_t span = anchor - G;
+  const uint32_t bits = 32 - __clz(span);
+  return bits > 11 ? bits - 11 : 0;
+}
+
+// One CTA per (node, segment) of the exact and long kinds. Exact: the whole
+// segment, r = k. Long: 32 runs of kRun consecutive entries spread evenly.
+constexpr uint32_t kGuessKPT = kSampleLong / kGuessThreads;  // 32
+
+__global__ void __launch_bounds__(kGuessThreads) topk_guess_cta_kernel(Args a, uint32_t nlist) {
+  __shared__ uint32_t wsum[2][8];
+  const uint32_t p = blockIdx.x / nlist, s = a.cta_list[blockIdx.x % nlist];
+  const SegRec r = a.recs[s];
+  const uint32_t t = threadIdx.x, lane = lane_id(), warp = t >> 5;
+  const uint64_t base = (uint64_t)p * a.N + r.begin;
+  const float* gp = a.grad + base;
+  const float* rp = a.residual + base;
+  const bool exact = r.kind == kExact;
+  uint32_t pos[kGuessKPT];
+  bool ok[kGuessKPT];
+  if (exact) {
+#pragma unroll
+    for (uint32_t q = 0; q < kGuessKPT; ++q) {
+      pos[q] = t + q * kGuessThreads;
+      ok[q] = pos[q] < r.n;
+    }
+  } else {
+    constexpr uint32_t nruns = kSampleLong / kRun, kLinesPerRun = kRun / 32;
+#pragma unroll
+    for (uint32_t q = 0; q < kGuessKPT; q += kLinesPerRun) {
+      const uint32_t run = warp * (kGuessKPT / kLinesPerRun) + q / kLinesPerRun;
+      const uint32_t st =
+          (uint32_t)(((uint64_t)run * (r.n - kRun) / (nruns - 1)) & ~(uint64_t)(kRun - 1));
+#pragma unroll
+      for (uint32_t l = 0; l < kLinesPerRun; ++l) {
+        pos[q + l] = st + l * 32 + lane;
+        ok[q + l] = true;
+      }
+    }
+  }
+  float ra[kGuessKPT], ga[kGuessKPT];
+#pragma unroll
+  for (uint32_t q = 0; q < kGuessKPT; ++q) {
+    ra[q] = ok[q] ? rp[pos[q]] : 0.0f;
+    ga[q] = ok[q] ? gp[pos[q]] : 0.0f;
+  }
+  uint32_t key[kGuessKPT];
+#pragma unroll
+  for (uint32_t q = 0; q < kGuessKPT; ++q) key[q] = ok[q] ? mag_key(__fadd_rn(ra[q], ga[q])) : kNone;
+  const uint32_t G = block_rank_key<kGuessKPT>(key, exact ? r.k : (r.rank & 0xffffu), wsum);
+  uint32_t shift = 0;
+  if (!exact) shift = hist_shift(G, block_rank_key<kGuessKPT>(key, r.rank >> 16, wsum));
+  if (t == 0) a.guess[(uint64_t)p * a.nseg + s] = make_uint2(G, shift);
+}
+
+// Layer-sized segments: one warp per (node, segment), no block barrier. The
+// 2,048-entry sample (8 runs of kRun) sits in registers, 64 keys per lane.
 constexpr uint32_t kWarpKeys = kWarpSample / 32;
 
-__global__ void __launch_bounds__(kGuessThreads)
-topk_guess_warp_kernel(const float* __restrict__ grad, const float* __restrict__ residual, Geo g,
-                       uint32_t* __restrict__ guess, uint32_t* __restrict__ seg_cnt,
-                       uint32_t* __restrict__ seg_flag, uint32_t* __restrict__ out_nnz,
-                       uint32_t total_k, uint32_t* __restrict__ todo_cnt) {
+__global__ void __launch_bounds__(kGuessThreads) topk_guess_warp_kernel(Args a, uint32_t nlist) {
   const uint32_t lane = lane_id();
-  const uint32_t gs = blockIdx.x * (kGuessThreads / 32) + (threadIdx.x >> 5);
-  if (gs >= (uint32_t)g.P * g.nseg) return;  // warp-uniform
-  const uint32_t p = gs / g.nseg, s = gs % g.nseg;
-  const uint32_t n = seg_n(g, s), k = seg_k(g, s);
-  if (lane == 0) {
-    if (gs == 0) *todo_cnt = 0;
-    seg_cnt[gs] = 0;
-    seg_flag[gs] = 0;
-    if (s == 0) out_nnz[p] = total_k;
-  }
-  if (k == 0 || k >= n) {
-    if (lane == 0) guess[gs] = k == 0 ? kNone : 0u;
-    return;
-  }
-  const uint64_t base = (uint64_t)p * g.N + (uint64_t)s * g.L;
-  const float* gp = grad + base;
-  const float* rp = residual + base;
-  constexpr uint32_t nruns = kWarpSample / kRun, kLines = kRun / 32, kBatchRuns = 2;
-  const uint32_t r = s == g.nseg - 1 ? g.r_warp_last : g.r_warp_full;
+  const uint64_t gw = (uint64_t)blockIdx.x * (kGuessThreads / 32) + (threadIdx.x >> 5);
+  if (gw >= (uint64_t)a.P * nlist) return;  // warp-uniform
+  const uint32_t p = (uint32_t)(gw / nlist), s = a.warp_list[gw % nlist];
+  const SegRec r = a.recs[s];
+  const uint64_t seg0 = (uint64_t)p * a.N + r.begin;
+  // runs start on the element grid's 4-aligned positions inside the segment
+  const uint32_t sh = (uint32_t)((4 - (seg0 & 3)) & 3);
+  const float* gp = a.grad + seg0 + sh;
+  const float* rp = a.residual + seg0 + sh;
+  constexpr uint32_t nruns = kWarpSample / kRun;
+  const uint32_t span = r.n - sh - kRun;  // n > kExactMax: positive
+  auto run_at = [&](uint32_t run) { return (run * span / (nruns - 1)) & ~(kRun - 1); };
   uint32_t key[kWarpKeys];
-  // run start (n <= kShortSegment, so run * (n - kRun) fits in 32 bits)
-  auto run_at = [&](uint32_t run) { return (run * (n - kRun) / (nruns - 1)) & ~(kRun - 1); };
-  if (((reinterpret_cast<uintptr_t>(gp) | reinterpret_cast<uintptr_t>(rp)) & 15) == 0) {
-    // 16-byte aligned segment: a run is 64 float4, two per lane; four runs'
-    // loads (16 of them) in flight at once
-    constexpr uint32_t kVecRuns = 4, kVecPer = kRun / 128;  // float4 per lane per run
+  if (a.vec) {
+    // a run is 64 float4, two per lane; four runs' loads in flight at once
+    constexpr uint32_t kVecRuns = 4, kVecPer = kRun / 128;
 #pragma unroll
     for (uint32_t r0 = 0; r0 < nruns; r0 += kVecRuns) {
-      float4 a[kVecRuns * kVecPer], b[kVecRuns * kVecPer];
+      float4 x[kVecRuns * kVecPer], y[kVecRuns * kVecPer];
 #pragma unroll
       for (uint32_t q = 0; q < kVecRuns * kVecPer; ++q) {
         const uint32_t i = run_at(r0 + q / kVecPer) + ((q % kVecPer) * 32 + lane) * 4;
-        a[q] = *reinterpret_cast<const float4*>(rp + i);
-        b[q] = *reinterpret_cast<const float4*>(gp + i);
+        x[q] = *reinterpret_cast<const float4*>(rp + i);
+        y[q] = *reinterpret_cast<const float4*>(gp + i);
       }
 #pragma unroll
       for (uint32_t q = 0; q < kVecRuns * kVecPer; ++q) {
         uint32_t* kq = key + (r0 * kVecPer + q) * 4;
-        kq[0] = mag_key(__fadd_rn(a[q].x, b[q].x));
-        kq[1] = mag_key(__fadd_rn(a[q].y, b[q].y));
-        kq[2] = mag_key(__fadd_rn(a[q].z, b[q].z));
-        kq[3] = mag_key(__fadd_rn(a[q].w, b[q].w));
+        kq[0] = mag_key(__fadd_rn(x[q].x, y[q].x));
+        kq[1] = mag_key(__fadd_rn(x[q].y, y[q].y));
+        kq[2] = mag_key(__fadd_rn(x[q].z, y[q].z));
+        kq[3] = mag_key(__fadd_rn(x[q].w, y[q].w));
       }
     }
   } else {
+    constexpr uint32_t kLines = kRun / 32, kBatchRuns = 2;
 #pragma unroll
     for (uint32_t r0 = 0; r0 < nruns; r0 += kBatchRuns) {
-      float a[kBatchRuns * kLines], b[kBatchRuns * kLines];
+      float x[kBatchRuns * kLines], y[kBatchRuns * kLines];
 #pragma unroll
       for (uint32_t q = 0; q < kBatchRuns * kLines; ++q) {
         const uint32_t i = run_at(r0 + q / kLines) + (q % kLines) * 32 + lane;
-        a[q] = rp[i];
-        b[q] = gp[i];
+        x[q] = rp[i];
+        y[q] = gp[i];
       }
 #pragma unroll
       for (uint32_t q = 0; q < kBatchRuns * kLines; ++q)
-        key[r0 * kLines + q] = mag_key(__fadd_rn(a[q], b[q]));
+        key[r0 * kLines + q] = mag_key(__fadd_rn(x[q], y[q]));
     }
   }
+  const uint32_t rr = r.rank & 0xffffu;
   uint32_t G = 0;
 #pragma unroll 1
   for (int bit = 30; bit >= 15; --bit) {
@@ -308,79 +401,125 @@ topk_guess_warp_kernel(const float* __restrict__ grad, const float* __restrict__
     uint32_t c = 0;
 #pragma unroll
     for (uint32_t q = 0; q < kWarpKeys; ++q) c += key[q] >= trial ? 1u : 0u;
-    if (warp_sum(c) >= r) G = trial;
+    if (warp_sum(c) >= rr) G = trial;
   }
-  if (lane == 0) guess[gs] = G;
+  if (lane == 0) a.guess[(uint64_t)p * a.nseg + s] = make_uint2(G, 0);
 }
 
 // ---------------------------------------------------------------------------
-// 2. stream: one CTA per chunk of kChunk entries (a chunk never crosses a
-// segment boundary). Warp w owns the contiguous sub-chunk of kSub entries
-// [start + kSub w, start + kSub (w + 1)), read as kRounds rounds of 32 float4,
-// and compacts its candidates in index order straight from registers into its
-// own sub-slot: no barrier, no second read.
+// 3. stream: one CTA per (node, chunk). Warp w owns the 1,024 grid positions
+// [q0, q0 + 1024) with q0 = floor4(segment start) + j * kChunk + w * kSub,
+// restricted to the segment: 8 rounds of one float4 per lane, all 16 loads
+// in flight before the first is used. Quads wholly inside the segment use
+// 128-bit accesses; the segment's ends go entry by entry. UNIFORM (a table of
+// equal segments, the last one possibly shorter): the chunk's segment and
+// place are arithmetic, so the data loads leave at once; otherwise they wait
+// for the chunk's descriptor. The rest of the chunk's description is loaded
+// after the data loads are in flight.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kStreamThreads)
-topk_stream_kernel(const float* __restrict__ grad, float* __restrict__ residual, Geo g,
-                   const uint32_t* __restrict__ guess, uint32_t* __restrict__ seg_cnt,
-                   uint32_t* __restrict__ seg_flag, uint32_t* __restrict__ sub_cnt,
-                   uint32_t* __restrict__ cand_idx, float* __restrict__ cand_val) {
+template <bool UNIFORM>
+__global__ void __launch_bounds__(kStreamThreads, 2) topk_stream_kernel(Args a) {
   const uint32_t gc = blockIdx.x;
-  const uint32_t p = gc / g.nchunk, c = gc % g.nchunk;
-  uint32_t s, j;
-  chunk_pos(g, c, &s, &j);
+  const uint32_t p = gc / a.nchunk, c = gc - p * a.nchunk;
   const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
-  const uint32_t seg_start = s * g.L;
-  const uint64_t start64 = (uint64_t)seg_start + (uint64_t)j * kChunk + warp * kSub;
-  const uint64_t seg_end = (uint64_t)seg_start + seg_n(g, s);
-  const uint32_t nn = start64 < seg_end ? (uint32_t)min((uint64_t)kSub, seg_end - start64) : 0u;
-  const uint32_t start = nn ? (uint32_t)start64 : 0u;  // this warp's first entry
-  const uint32_t G = guess[p * g.nseg + s];
-  const float* gp = grad + (uint64_t)p * g.N + start;
-  float* rp = residual + (uint64_t)p * g.N + start;
-  const bool aligned =
-      ((reinterpret_cast<uintptr_t>(gp) | reinterpret_cast<uintptr_t>(rp)) & 15) == 0;
-
+  uint32_t begin, end, seg, j;
+  uint4 d1 = make_uint4(0, 0, 0, 0);
+  if (UNIFORM) {
+    seg = min(c / a.u_m, a.nseg - 1);
+    j = c - seg * a.u_m;
+    begin = seg * a.u_L;
+    end = (uint32_t)min((uint64_t)begin + a.u_L, a.N);
+  } else {
+    const uint4 d0 = reinterpret_cast<const uint4*>(a.desc + c)[0];
+    begin = d0.x;
+    end = d0.y;
+    seg = d0.z;
+    j = d0.w;
+  }
+  const uint64_t row = (uint64_t)p * a.N;
+  const uint64_t lo = row + begin, hi = row + end;
+  const uint64_t q0 = ((lo & ~(uint64_t)3)) + (uint64_t)j * kChunk + (uint64_t)warp * kSub;
+  // (only whether a position is below lo matters: lo_r is clamped to -1)
+  const int32_t lo_r = (int32_t)max((int64_t)lo - (int64_t)q0, (int64_t)-1);
+  const int32_t hi_r = (int32_t)max(min((int64_t)hi - (int64_t)q0, (int64_t)kSub + 4), (int64_t)-1);
+  const float* gp = a.grad + q0;
+  float* rp = a.residual + q0;
   float4 gv[kRounds], rv[kRounds];
 #pragma unroll
   for (uint32_t t = 0; t < kRounds; ++t) {
-    const uint32_t e0 = 4 * (t * 32 + lane);  // sub-chunk local
-    if (aligned && e0 + 4 <= nn) {
+    const int32_t e0 = (int32_t)(4 * (t * 32 + lane));
+    if (a.vec && e0 >= lo_r && e0 + 4 <= hi_r) {
       gv[t] = __ldcs(reinterpret_cast<const float4*>(gp + e0));
       rv[t] = *reinterpret_cast<const float4*>(rp + e0);
     } else {
-      float a[4] = {0.f, 0.f, 0.f, 0.f}, b[4] = {0.f, 0.f, 0.f, 0.f};
+      float x[4] = {0.f, 0.f, 0.f, 0.f}, y[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (uint32_t q = 0; q < 4; ++q)
-        if (e0 + q < nn) {
-          a[q] = gp[e0 + q];
-          b[q] = rp[e0 + q];
+      for (int32_t q = 0; q < 4; ++q)
+        if (e0 + q >= lo_r && e0 + q < hi_r) {
+          x[q] = gp[e0 + q];
+          y[q] = rp[e0 + q];
         }
-      gv[t] = make_float4(a[0], a[1], a[2], a[3]);
-      rv[t] = make_float4(b[0], b[1], b[2], b[3]);
+      gv[t] = make_float4(x[0], x[1], x[2], x[3]);
+      rv[t] = make_float4(y[0], y[1], y[2], y[3]);
     }
   }
+  // the rest of the description, while the data loads are in flight
+  uint32_t slot, slot32, kind, aux;
+  if (UNIFORM) {
+    const SegRec& r = a.recs[seg];
+    slot = r.slot;
+    kind = r.kind;
+    aux = r.kind == kLong ? r.lidx : r.out0;
+    slot32 = r.slot32 + j * kWarpsPerChunk * (slot / 32);
+  } else {
+    d1 = reinterpret_cast<const uint4*>(a.desc + c)[1];
+    slot = d1.x;
+    slot32 = d1.y;
+    kind = d1.z;
+    aux = d1.w;
+  }
+  const uint64_t gs = (uint64_t)p * a.nseg + seg;
+  const uint32_t G = a.guess[gs].x;
+  const uint32_t base_u = (uint32_t)(q0 - row);  // node-local index of q0, modulo 2^32
+  if (kind == kKeepAll) {  // CTA-uniform. k = n: every entry goes to the stream, residual 0
+    const uint64_t o = (uint64_t)p * a.cap + aux - begin;  // + node-local index
+#pragma unroll
+    for (uint32_t t = 0; t < kRounds; ++t) {
+      const int32_t e0 = (int32_t)(4 * (t * 32 + lane));
+      const float av[4] = {__fadd_rn(rv[t].x, gv[t].x), __fadd_rn(rv[t].y, gv[t].y),
+                           __fadd_rn(rv[t].z, gv[t].z), __fadd_rn(rv[t].w, gv[t].w)};
+#pragma unroll
+      for (int32_t q = 0; q < 4; ++q)
+        if (e0 + q >= lo_r && e0 + q < hi_r) {
+          const uint32_t idx = base_u + (uint32_t)(e0 + q);
+          a.out_idx[o + idx] = idx;
+          a.out_val[o + idx] = av[q];
+          rp[e0 + q] = 0.0f;
+        }
+    }
+    return;
+  }
   const uint64_t sub = (uint64_t)gc * kWarpsPerChunk + warp;
-  const uint64_t slot0 = sub * g.slot;
+  const uint64_t slot0 = (uint64_t)p * a.node_slots + (uint64_t)slot32 * 32 + (uint64_t)warp * slot;
   uint32_t run = 0;  // candidates so far in this sub-chunk (warp-uniform)
 #pragma unroll
   for (uint32_t t = 0; t < kRounds; ++t) {
-    const uint32_t e0 = 4 * (t * 32 + lane);
-    float4 a;
-    a.x = __fadd_rn(rv[t].x, gv[t].x);
-    a.y = __fadd_rn(rv[t].y, gv[t].y);
-    a.z = __fadd_rn(rv[t].z, gv[t].z);
-    a.w = __fadd_rn(rv[t].w, gv[t].w);
-    const float av[4] = {a.x, a.y, a.z, a.w};
+    const int32_t e0 = (int32_t)(4 * (t * 32 + lane));
+    float4 acc;
+    acc.x = __fadd_rn(rv[t].x, gv[t].x);
+    acc.y = __fadd_rn(rv[t].y, gv[t].y);
+    acc.z = __fadd_rn(rv[t].z, gv[t].z);
+    acc.w = __fadd_rn(rv[t].w, gv[t].w);
+    const float av[4] = {acc.x, acc.y, acc.z, acc.w};
     uint32_t bits = 0;
-    if (aligned && e0 + 4 <= nn) {
-      *reinterpret_cast<float4*>(rp + e0) = a;
+    if (a.vec && e0 >= lo_r && e0 + 4 <= hi_r) {
+      *reinterpret_cast<float4*>(rp + e0) = acc;
 #pragma unroll
       for (uint32_t q = 0; q < 4; ++q) bits |= (mag_key(av[q]) >= G ? 1u : 0u) << q;
     } else {
 #pragma unroll
-      for (uint32_t q = 0; q < 4; ++q)
-        if (e0 + q < nn) {
+      for (int32_t q = 0; q < 4; ++q)
+        if (e0 + q >= lo_r && e0 + q < hi_r) {
           rp[e0 + q] = av[q];
           bits |= (mag_key(av[q]) >= G ? 1u : 0u) << q;
         }
@@ -392,94 +531,35 @@ topk_stream_kernel(const float* __restrict__ grad, float* __restrict__ residual,
 #pragma unroll
     for (uint32_t q = 0; q < 4; ++q)
       if (bits & (1u << q)) {
-        if (pos < g.slot) {
+        if (pos < slot) {
           const uint64_t keep = l2_policy_evict_last();
-          st_keep(cand_idx + slot0 + pos, start + e0 + q, keep);
-          st_keep(cand_val + slot0 + pos, av[q], keep);
+          st_keep(a.cand_idx + slot0 + pos, base_u + (uint32_t)e0 + q, keep);
+          st_keep(a.cand_val + slot0 + pos, av[q], keep);
         }
         ++pos;
       }
   }
+  // Pad the sub-slot's last 32-byte sector: every sector of candidates is
+  // written whole, so no later eviction from L2 leaves a half-written sector.
+  const uint32_t pad_end = min((run + 7u) & ~7u, slot);
+  if (run + lane < pad_end) {
+    const uint64_t keep = l2_policy_evict_last();
+    st_keep(a.cand_idx + slot0 + run + lane, kNone, keep);
+    st_keep(a.cand_val + slot0 + run + lane, 0.0f, keep);
+  }
   if (lane == 0) {
-    sub_cnt[sub] = run;
-    if (run) atomicAdd(&seg_cnt[p * g.nseg + s], run);
-    if (run > g.slot) atomicOr(&seg_flag[p * g.nseg + s], 1u);
+    a.sub_cnt[sub] = run;
+    if (run) atomicAdd(&a.seg_cnt[gs], run);
+    if (run > slot) atomicOr(&a.seg_flag[gs], 1u);
   }
 }
 
 // ---------------------------------------------------------------------------
-// 3. select: one cluster of CS CTAs per (node, segment). CTA r of the
-// cluster owns chunks [ms*r/CS, ms*(r+1)/CS) of the segment.
-// ---------------------------------------------------------------------------
-struct SelectArgs {
-  uint32_t CS;         // CTAs per segment (a thread-block cluster when > 1)
-  uint32_t warp_done;  // topk_select_short_kernel ran: only the segments in `todo` remain
-  uint32_t raw_only;   // the long-segment passes ran: only fallback segments remain
-  uint32_t* todo;      // segments the short kernel left to topk_select_kernel
-  uint32_t* todo_cnt;
-  float* residual;
-  const uint32_t* seg_cnt;
-  const uint32_t* seg_flag;
-  const uint32_t* sub_cnt;  // candidates per warp sub-chunk
-  const uint32_t* guess;    // per-segment lower bound G of the k-th key
-  const uint32_t* cand_idx;
-  const float* cand_val;
-  uint32_t* out_idx;
-  float* out_val;
-  int32_t* status;
-  Geo g;
-};
-
-struct SelectShared {
-  uint32_t hist[2048];
-  uint32_t tot[2048];
-  uint32_t wpre[kWin + 1];  // prefix of sub-chunk counts of a window
-  uint32_t scratch[34];
-  uint32_t res[2];
-  uint32_t cnt[2];  // this CTA's (> T, == T) counts, read by higher ranks
-};
-
-// Exclusive prefix of the candidate counts of nw consecutive sub-chunks into
-// sh.wpre[0..nw]; returns the window total.
-__device__ uint32_t load_window(SelectShared& sh, const uint32_t* cc, uint32_t nw) {
-  const uint32_t per = (kWin + kSelectThreads - 1) / kSelectThreads;
-  const uint32_t t = threadIdx.x;
-  uint32_t v[per], sum = 0;
-#pragma unroll
-  for (uint32_t i = 0; i < per; ++i) {
-    const uint32_t w = t * per + i;
-    v[i] = w < nw ? cc[w] : 0u;
-    sum += v[i];
-  }
-  uint32_t total;
-  uint32_t ex = block_excl_scan(sum, sh.scratch, &total);
-#pragma unroll
-  for (uint32_t i = 0; i < per; ++i) {
-    const uint32_t w = t * per + i;
-    if (w < nw) sh.wpre[w] = ex;
-    ex += v[i];
-  }
-  if (t == 0) sh.wpre[nw] = total;
-  __syncthreads();
-  return total;
-}
-
-// Position v of a window -> its sub-chunk (largest w with wpre[w] <= v).
-__device__ __forceinline__ uint32_t window_chunk(const SelectShared& sh, uint32_t nw, uint32_t v) {
-  uint32_t lo = 0, hi = nw;  // invariant: wpre[lo] <= v < wpre[hi]
-  while (hi - lo > 1) {
-    const uint32_t mid = (lo + hi) >> 1;
-    if (sh.wpre[mid] <= v) lo = mid; else hi = mid;
-  }
-  return lo;
-}
-
-// Select for a layer-sized segment whose candidates were all kept in their
-// sub-slots (at most kShortCands of them, over at most kShortSubs
-// sub-chunks): one CTA of kSegThreads per segment (4 warps share the work of
-// each phase, so a segment's chain of phases is short):
-//  1. thread t copies sub-chunk t's candidates into shared memory with
-//     cp.async (every copy in flight at once), at the sub-chunk's offset;
+// 4a. select of a layer-sized segment whose candidates were all kept in
+// their sub-slots (at most kShortCands over at most kShortSubs sub-chunks):
+// one CTA of kSegThreads per (node, segment):
+//  1. each thread copies its sub-chunks' candidates into shared memory with
+//     cp.async (every copy in flight at once), at the sub-chunks' offsets;
 //  2. four radix digits (8, 8, 8, 7 bits) of the k-th key T, each from one
 //     256-bin histogram over the shared copy (warp-aggregated adds), its
 //     bins scanned from the top by warp 0;
@@ -487,16 +567,14 @@ __device__ __forceinline__ uint32_t window_chunk(const SelectShared& sh, uint32_
 //     index order at the offset given by a block scan of its counts (keys
 //     > T, and keys == T up to tie_take, lowest indices first); then the
 //     offsets are resolved to indices and the residual is zeroed there.
-// Segments that do not qualify go to the to-do list of topk_select_kernel.
-constexpr uint32_t kShortSubs = 128;
-constexpr uint32_t kShortCands = 2048;
-constexpr uint32_t kSegThreads = 128;  // = kShortSubs: one sub-chunk per thread in phase 1
-
-__device__ __forceinline__ bool short_select_eligible(const SelectArgs& a, uint32_t gs, uint32_t k,
-                                                      uint32_t ms) {
-  return a.CS == 1 && a.seg_flag[gs] == 0 && a.seg_cnt[gs] >= k &&
-         ms * kWarpsPerChunk <= kShortSubs && a.seg_cnt[gs] <= kShortCands;
-}
+// Segments that do not qualify go to the to-do list of the raw select.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kSegThreads = 128;
+constexpr uint32_t kShortSubs = 3 * kSegThreads;  // 33 chunks of a layer-sized segment fit
+constexpr uint32_t kShortCands = 8192;
+// Layer-sized segments expected to leave more candidates than this go to the
+// range-parallel long select instead (their guess then samples 8,192 entries).
+constexpr uint32_t kShortExpect = 6144;
 
 __device__ __forceinline__ uint32_t warp_excl_sum(uint32_t v, uint32_t* total) {
   const uint32_t incl = warp_incl_sum(v);
@@ -504,34 +582,44 @@ __device__ __forceinline__ uint32_t warp_excl_sum(uint32_t v, uint32_t* total) {
   return incl - v;
 }
 
-__global__ void __launch_bounds__(kSegThreads)
-topk_select_short_kernel(SelectArgs a) {
+__global__ void __launch_bounds__(kSegThreads) topk_select_short_kernel(Args a, uint32_t nlist) {
   __shared__ uint32_t wpre[kShortSubs + 1];
   __shared__ float vals[kShortCands];
   __shared__ uint32_t hist[256];
   __shared__ uint32_t scratch[34];
   __shared__ uint32_t dig[2];
-  const Geo& g = a.g;
   const uint32_t t = threadIdx.x, lane = lane_id(), warp = t >> 5;
-  const uint32_t gs = blockIdx.x;
-  const uint32_t p = gs / g.nseg, s = gs % g.nseg;
-  const uint32_t k = seg_k(g, s), ms = seg_chunks(g, s);
-  if (k == 0) return;                                // CTA-uniform
-  if (!short_select_eligible(a, gs, k, ms)) {        // CTA-uniform: to topk_select_kernel
-    if (t == 0) a.todo[atomicAdd(a.todo_cnt, 1u)] = gs;
+  const uint32_t p = blockIdx.x / nlist, s = a.short_list[blockIdx.x % nlist];
+  const SegRec r = a.recs[s];
+  const uint64_t gs = (uint64_t)p * a.nseg + s;
+  const uint32_t k = r.k, nsub = r.nchunk * kWarpsPerChunk;
+  const uint32_t cnt = a.seg_cnt[gs];
+  if (a.seg_flag[gs] != 0 || cnt < k || cnt > kShortCands || nsub > kShortSubs) {
+    if (t == 0) a.todo[atomicAdd(a.todo_cnt, 1u)] = (uint32_t)gs;  // CTA-uniform
     return;
   }
-  const uint32_t nsub = ms * kWarpsPerChunk;
-  const uint64_t sub0 = ((uint64_t)p * g.nchunk + (uint64_t)s * g.m) * kWarpsPerChunk;
-  const uint32_t* cidx = a.cand_idx + sub0 * g.slot;
-  const float* cval = a.cand_val + sub0 * g.slot;
-  // 1. offsets of the sub-chunks' candidates, then the copies
-  const uint32_t c = t < nsub ? a.sub_cnt[sub0 + t] : 0u;
+  const uint64_t sub0 = ((uint64_t)p * a.nchunk + r.chunk0) * kWarpsPerChunk;
+  const uint64_t slot_base = (uint64_t)p * a.node_slots + (uint64_t)r.slot32 * 32;
+  const uint32_t* cidx = a.cand_idx + slot_base;
+  const float* cval = a.cand_val + slot_base;
+  // 1. offsets of the sub-chunks' candidates (thread t: sub-chunks 3t .. 3t + 2)
+  uint32_t c3[3], csum = 0;
+#pragma unroll
+  for (uint32_t i = 0; i < 3; ++i) {
+    const uint32_t w = 3 * t + i;
+    c3[i] = w < nsub ? a.sub_cnt[sub0 + w] : 0u;
+    csum += c3[i];
+  }
   uint32_t M;
-  const uint32_t off = block_excl_scan(c, scratch, &M);
-  if (t < nsub) wpre[t] = off;
+  uint32_t off = block_excl_scan(csum, scratch, &M);
+#pragma unroll
+  for (uint32_t i = 0; i < 3; ++i) {
+    const uint32_t w = 3 * t + i;
+    if (w < nsub) wpre[w] = off;
+    for (uint32_t e = 0; e < c3[i]; ++e) cp_async4(vals + off + e, cval + (uint64_t)w * r.slot + e);
+    off += c3[i];
+  }
   if (t == 0) wpre[nsub] = M;
-  for (uint32_t i = 0; i < c; ++i) cp_async4(vals + off + i, cval + (uint64_t)t * g.slot + i);
   cp_async_wait_all();
   __syncthreads();
   // 2. radix digits of T (bits 30..23, 22..15, 14..7, 6..0)
@@ -570,12 +658,10 @@ topk_select_short_kernel(SelectArgs a) {
         }
       }
       const uint32_t found = __ballot_sync(0xffffffffu, b != 0xffffffffu);
-      if (lane == 0) {
-        if (!found) {
-          set_status(a.status, SPARCML_ERR_BAD_STREAM);
-          dig[0] = 0;
-          dig[1] = rem;
-        }
+      if (lane == 0 && !found) {  // cannot happen for consistent counts
+        set_status(a.status, SPARCML_ERR_BAD_STREAM);
+        dig[0] = 0;
+        dig[1] = rem;
       }
       if (found && lane == __ffs(found) - 1) {
         dig[0] = b;
@@ -599,12 +685,12 @@ topk_select_short_kernel(SelectArgs a) {
   uint32_t tot;  // both counts in one scan: M <= kShortCands < 2^16
   const uint32_t ex = block_excl_scan((n_gt << 16) | n_eq, scratch, &tot);
   uint32_t e_gt = ex >> 16, e_eq = ex & 0xffffu;
-  float* rp = a.residual + (uint64_t)p * g.N;
-  const uint64_t out0 = (uint64_t)p * g.cap + (uint64_t)s * g.k_full;
+  float* rp = a.residual + (uint64_t)p * a.N;
+  const uint64_t out0 = (uint64_t)p * a.cap + r.out0;
   uint32_t* oi = a.out_idx + out0;
   const uint64_t keep = l2_policy_evict_last();
   uint32_t w = 0;  // sub-chunk of v_lo: the largest w with wpre[w] <= v_lo
-  for (uint32_t step = kShortSubs / 2; step > 0; step >>= 1)
+  for (uint32_t step = 256; step > 0; step >>= 1)
     if (w + step <= nsub && wpre[w + step] <= v_lo) w += step;
   for (uint32_t v = v_lo; v < v_hi; ++v) {
     const float x = vals[v];
@@ -614,7 +700,7 @@ topk_select_short_kernel(SelectArgs a) {
       const uint32_t pos = e_gt + min(e_eq, tie_take);
       while (wpre[w + 1] <= v) ++w;
       if (pos < k) {
-        oi[pos] = w * g.slot + (v - wpre[w]);  // slot offset for now
+        oi[pos] = w * r.slot + (v - wpre[w]);  // slot offset for now
         st_keep(a.out_val + out0 + pos, x, keep);
       } else {
         set_status(a.status, SPARCML_ERR_BAD_STREAM);
@@ -624,166 +710,439 @@ topk_select_short_kernel(SelectArgs a) {
     e_eq += eq ? 1u : 0u;
   }
   __syncthreads();  // the offsets written above are visible to the whole CTA
-  // offsets -> indices; the residual is zeroed at each kept index.
-  for (uint32_t j = t; j < k; j += kSegThreads) {
-    const uint32_t idx = cidx[oi[j]];
-    st_keep(oi + j, idx, keep);
-    rp[idx] = 0.0f;
+  // offsets -> indices; the residual is zeroed at each kept index. (Every
+  // position below k was written above when the counts are consistent; an
+  // offset out of the segment's sub-slots is skipped, not followed.)
+  const uint32_t span = nsub * r.slot;
+  for (uint32_t i = t; i < k; i += kSegThreads) {
+    const uint32_t o = oi[i];
+    if (o >= span) {
+      set_status(a.status, SPARCML_ERR_BAD_STREAM);
+      continue;
+    }
+    const uint32_t idx = cidx[o];
+    st_keep(oi + i, idx, keep);
+    if (idx - r.begin < r.n) rp[idx] = 0.0f;
   }
 }
 
-// Select for segment gs by CTA `rank` of the CS CTAs (a cluster when CS > 1)
-// that share it. Every CTA of a cluster calls this for the same segment.
-__device__ __forceinline__ void select_segment(const SelectArgs& a, SelectShared& sh,
-                                               cg::cluster_group& cluster, uint32_t gs,
-                                               uint32_t rank) {
-  const uint32_t CS = a.CS;
-  const Geo& g = a.g;
-  const uint32_t p = gs / g.nseg, s = gs % g.nseg;
-  const uint32_t n = seg_n(g, s), k = seg_k(g, s);
-  if (k == 0) return;  // uniform over the cluster
-  const uint32_t t = threadIdx.x;
-  const bool raw = a.seg_flag[gs] != 0 || a.seg_cnt[gs] < k;
-  if (a.raw_only && !raw) return;  // done by the long-segment passes
-  const uint32_t ms = seg_chunks(g, s);
-  const uint32_t c_first = s * g.m;  // node-local id of the segment's first chunk
-  const uint32_t ca = c_first + (uint32_t)((uint64_t)ms * rank / CS);
-  const uint32_t cb = c_first + (uint32_t)((uint64_t)ms * (rank + 1) / CS);
-  const uint32_t seg_start = s * g.L;
-  const uint64_t seg_end = (uint64_t)seg_start + n;
-  const uint32_t raw_lo =
-      (uint32_t)min((uint64_t)seg_start + (uint64_t)(ca - c_first) * kChunk, seg_end);
-  const uint32_t raw_hi =
-      (uint32_t)min((uint64_t)seg_start + (uint64_t)(cb - c_first) * kChunk, seg_end);
-  float* rp = a.residual + (uint64_t)p * g.N;
-  const uint64_t node_sub0 = (uint64_t)p * g.nchunk * kWarpsPerChunk;
-  const uint32_t sa = ca * kWarpsPerChunk, sb = cb * kWarpsPerChunk;  // this CTA's sub-chunks
+// ---------------------------------------------------------------------------
+// 4b. select of a long segment from its candidates.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t bin_of(uint32_t key, uint32_t G, uint32_t shift) {
+  return min((key - G) >> shift, kBins - 1);
+}
 
-  // Fast path: one CTA owns the segment and all its candidates fit in shared
-  // memory. They are read from global memory once, in index order; the
-  // radix select and the ordered compaction then run on the shared copy.
-  if (CS == 1 && !raw && ms * kWarpsPerChunk <= kWin && a.seg_cnt[gs] <= kSmallCands) {
-    extern __shared__ uint32_t dsm[];
-    uint32_t* s_idx = dsm;
-    float* s_val = reinterpret_cast<float*>(dsm + kSmallCands);
-    const uint32_t nsub = ms * kWarpsPerChunk;
-    const uint32_t M = load_window(sh, a.sub_cnt + node_sub0 + sa, nsub);
-    constexpr uint32_t kLoadBatch = 4;  // candidate loads in flight per thread
-    for (uint32_t v0 = 0; v0 < M; v0 += blockDim.x * kLoadBatch) {
-      uint32_t li[kLoadBatch];
-      float lv[kLoadBatch];
-#pragma unroll
-      for (uint32_t u = 0; u < kLoadBatch; ++u) {
-        const uint32_t v = v0 + u * blockDim.x + t;
-        li[u] = 0;
-        lv[u] = 0.0f;
-        if (v < M) {
-          const uint32_t w = window_chunk(sh, nsub, v);
-          const uint64_t slot = (node_sub0 + sa + w) * g.slot + (v - sh.wpre[w]);
-          li[u] = a.cand_idx[slot];
-          lv[u] = a.cand_val[slot];
-        }
-      }
-#pragma unroll
-      for (uint32_t u = 0; u < kLoadBatch; ++u) {
-        const uint32_t v = v0 + u * blockDim.x + t;
-        if (v < M) {
-          s_idx[v] = li[u];
-          s_val[v] = lv[u];
-        }
-      }
-    }
-    __syncthreads();
-    // Four 8-bit digits (bits 30..23, 22..15, 14..7, 6..0): 256 bins, one
-    // per thread, so zeroing and scanning a histogram costs one step.
-    uint32_t prefix = 0, rem = k;
-    for (int d = 0; d < 4; ++d) {
-      const uint32_t shift = d == 3 ? 0 : 23 - 8 * d;
-      const uint32_t nb = d == 3 ? 128 : 256, hi_shift = d == 0 ? 31 : shift + (d == 3 ? 7 : 8);
-      for (uint32_t b = t; b < 256; b += blockDim.x) sh.hist[b] = 0;
-      __syncthreads();
-      for (uint32_t v0 = 0; v0 < M; v0 += blockDim.x) {
-        const uint32_t v = v0 + t;
-        const uint32_t key = v < M ? mag_key(s_val[v]) : 0u;
-        const bool match = v < M && (d == 0 || (key >> hi_shift) == prefix);
-        hist_add(sh.hist, (key >> shift) & (nb - 1), match);
-      }
-      __syncthreads();
-      find_from_top(sh.hist, 256, rem, sh.scratch, sh.res);
-      uint32_t b = sh.res[0];
-      if (b == kNone) {
-        set_status(a.status, SPARCML_ERR_BAD_STREAM);
-        b = 0;
-      } else {
-        rem -= sh.res[1];
-      }
-      prefix = (prefix << (d == 3 ? 7 : 8)) | b;
-    }
-    const uint32_t T = prefix, tie_take = rem;
-    const uint64_t out0 = (uint64_t)p * g.cap + (uint64_t)s * g.k_full;
-    uint32_t run_gt = 0, run_eq = 0;
-    for (uint32_t v0 = 0; v0 < M; v0 += blockDim.x) {
-      const uint32_t v = v0 + t;
-      const float x = v < M ? s_val[v] : 0.0f;
-      const uint32_t key = mag_key(x);
-      const bool gt = v < M && key > T;
-      const bool eq = v < M && key == T;
-      uint32_t tot;
-      const uint32_t ex =
-          block_excl_scan((gt ? 1u : 0u) | (eq ? 0x10000u : 0u), sh.scratch, &tot);
-      const uint32_t e_gt = run_gt + (ex & 0xffffu), e_eq = run_eq + (ex >> 16);
-      if (gt || (eq && e_eq < tie_take)) {
-        const uint32_t pos = e_gt + min(e_eq, tie_take);
-        if (pos < k) {
-          const uint32_t i = s_idx[v];
-          a.out_idx[out0 + pos] = i;
-          a.out_val[out0 + pos] = x;
-          rp[i] = 0.0f;
-        } else {
-          set_status(a.status, SPARCML_ERR_BAD_STREAM);
-        }
-      }
-      run_gt += tot & 0xffffu;
-      run_eq += tot >> 16;
-      __syncthreads();
-    }
+// The boundary bin from the histogram the stream pass built; a segment whose
+// candidates cannot decide its select is handed to the raw select.
+__global__ void __launch_bounds__(256) long_find_kernel(Args a) {
+  __shared__ uint32_t scratch[34];
+  __shared__ uint32_t res[2];
+  const uint32_t p = blockIdx.x / a.nlong, ls = blockIdx.x % a.nlong;
+  const uint32_t s = a.long_list[ls];
+  const SegRec r = a.recs[s];
+  const uint64_t gs = (uint64_t)p * a.nseg + s, pl = (uint64_t)p * a.nlong + ls;
+  LongSel& L = a.lsel[pl];
+  if (a.seg_flag[gs] != 0 || a.seg_cnt[gs] < r.k) {  // CTA-uniform
+    if (threadIdx.x == 0) L.mode = kModeFallback;
     return;
   }
-
-  // Visit every candidate of this CTA as (index, value), window by window.
-  // `ordered` passes see them in ascending index order, blockDim at a time.
-  auto for_each = [&](auto&& body) {
-    if (raw) {
-      const uint32_t total = raw_hi > raw_lo ? raw_hi - raw_lo : 0;
-      for (uint32_t v0 = 0; v0 < total; v0 += blockDim.x) {
-        const uint32_t v = v0 + t;
-        const bool valid = v < total;
-        const uint32_t i = raw_lo + v;
-        body(valid, i, valid ? rp[i] : 0.0f);
-      }
+  find_from_top(a.hist + pl * kBins, kBins, r.k, scratch, res);
+  if (threadIdx.x == 0) {
+    if (res[0] == kNone) {  // counts disagree with the candidates: decide it again raw
+      L.mode = kModeFallback;
     } else {
-      for (uint32_t w0 = sa; w0 < sb; w0 += kWin) {
-        const uint32_t nw = min(kWin, sb - w0);
-        const uint32_t total = load_window(sh, a.sub_cnt + node_sub0 + w0, nw);
-        for (uint32_t v0 = 0; v0 < total; v0 += blockDim.x) {
-          const uint32_t v = v0 + t;
-          const bool valid = v < total;
-          uint32_t i = 0;
-          float x = 0.0f;
-          if (valid) {
-            const uint32_t w = window_chunk(sh, nw, v);
-            const uint64_t slot = (node_sub0 + w0 + w) * g.slot + (v - sh.wpre[w]);
-            i = a.cand_idx[slot];
-            x = a.cand_val[slot];
-          }
-          body(valid, i, x);
+      L.mode = kModeNormal;
+      L.bin = res[0];
+      L.rank = r.k - res[1];
+    }
+  }
+}
+
+// The candidates of one range (kRangeSubs sub-chunks) of a long segment,
+// warp w taking its 32 sub-chunks' candidates as one sequence: f(v, idx_ptr,
+// val_ptr) for v = 0 .. its count, in index order, 32 lanes at a time.
+struct RangeView {
+  uint32_t p, ls, s, rr;  // node, long segment, segment id, range within the segment
+  SegRec rec;
+  uint64_t gs, pl;
+  uint32_t excl;          // candidates of this lane's sub-chunk before it in the warp
+  uint32_t count;         // this warp's candidates
+  uint64_t slot_base;     // this warp's first sub-slot
+};
+
+__device__ __forceinline__ bool range_view(const Args& a, RangeView* v) {
+  const uint32_t rid = blockIdx.x % a.nranges;
+  v->p = blockIdx.x / a.nranges;
+  const uint32_t m = a.range_map[rid];
+  v->ls = m >> 16;
+  v->rr = m & 0xffffu;
+  v->s = a.long_list[v->ls];
+  v->rec = a.recs[v->s];
+  v->gs = (uint64_t)v->p * a.nseg + v->s;
+  v->pl = (uint64_t)v->p * a.nlong + v->ls;
+  const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
+  const uint32_t nsub = v->rec.nchunk * kWarpsPerChunk;
+  const uint32_t w0 = v->rr * kRangeSubs + warp * 32;  // the warp's first sub-chunk
+  const uint32_t w = w0 + lane;
+  const uint64_t sub0 = ((uint64_t)v->p * a.nchunk + v->rec.chunk0) * kWarpsPerChunk;
+  const uint32_t c = w < nsub ? min(a.sub_cnt[sub0 + w], v->rec.slot) : 0u;
+  const uint32_t incl = warp_incl_sum(c);
+  v->excl = incl - c;
+  v->count = __shfl_sync(0xffffffffu, incl, 31);
+  v->slot_base = (uint64_t)v->p * a.node_slots + (uint64_t)v->rec.slot32 * 32 +
+                 (uint64_t)w0 * v->rec.slot;
+  return true;
+}
+
+// Offset (from the warp's first sub-slot) of the warp's candidate number x:
+// sub-chunk i = the last lane whose exclusive count is <= x (five shuffles),
+// then x - excl_i into it. Below 32 * 1,024: 32 bits.
+__device__ __forceinline__ uint32_t range_off(const RangeView& v, uint32_t x) {
+  uint32_t i = 0;
+#pragma unroll
+  for (uint32_t step = 16; step > 0; step >>= 1) {
+    const uint32_t cand = i + step;
+    const uint32_t e = __shfl_sync(0xffffffffu, v.excl, cand & 31u);
+    if (cand < 32 && e <= x) i = cand;
+  }
+  const uint32_t e = __shfl_sync(0xffffffffu, v.excl, i);
+  return i * v.rec.slot + (x - e);
+}
+
+// Candidates a lane holds in registers at once: a warp's first 512 are all
+// loaded before any is used (a warp of 32 sub-chunks holds about 500 at 1.5 %
+// density); any beyond are taken in further batches.
+constexpr uint32_t kHold = 16;
+
+// Per range: the candidates' bins, (key - G) >> shift (the top bin takes
+// everything above), counted in shared memory and added to the (node,
+// segment) histogram. A segment whose sub-slots overflowed is skipped: its
+// select falls back to the raw select.
+__global__ void __launch_bounds__(256) long_hist_kernel(Args a) {
+  __shared__ uint32_t h[kBins];
+  for (uint32_t b = threadIdx.x; b < kBins; b += blockDim.x) h[b] = 0;
+  __syncthreads();
+  RangeView v;
+  range_view(a, &v);
+  if (a.seg_flag[v.gs] != 0) return;  // CTA-uniform
+  const uint32_t lane = lane_id();
+  const uint2 gsh = a.guess[v.gs];
+  const float* cv = a.cand_val + v.slot_base;
+  for (uint32_t x0 = 0; x0 < v.count; x0 += 32 * kHold) {
+    float xv[kHold];
+#pragma unroll
+    for (uint32_t u = 0; u < kHold; ++u) {
+      const uint32_t x = x0 + u * 32 + lane;
+      const uint32_t o = range_off(v, min(x, v.count - 1));
+      xv[u] = x < v.count ? cv[o] : 0.0f;
+    }
+#pragma unroll
+    for (uint32_t u = 0; u < kHold; ++u)
+      if (x0 + u * 32 + lane < v.count) atomicAdd(&h[bin_of(mag_key(xv[u]), gsh.x, gsh.y)], 1u);
+  }
+  __syncthreads();
+  uint32_t* gh = a.hist + v.pl * kBins;
+  for (uint32_t b = threadIdx.x; b < kBins; b += blockDim.x)
+    if (h[b]) atomicAdd(gh + b, h[b]);  // result unused: a reduction in L2
+}
+
+// Per range: candidates above the boundary bin are counted; those in it are
+// appended (key, index) to the segment's boundary buffer.
+__global__ void __launch_bounds__(256) long_collect_kernel(Args a) {
+  __shared__ uint32_t wgt[8];
+  RangeView v;
+  range_view(a, &v);
+  if (a.lsel[v.pl].mode != kModeNormal) return;  // CTA-uniform
+  const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+  const uint2 gsh = a.guess[v.gs];
+  const uint32_t bstar = a.lsel[v.pl].bin;
+  uint2* bnd = a.bnd + v.pl * kBoundCap;
+  const float* cv = a.cand_val + v.slot_base;
+  const uint32_t* ci = a.cand_idx + v.slot_base;
+  uint32_t gt = 0;
+  for (uint32_t x0 = 0; x0 < v.count; x0 += 32 * kHold) {
+    float xv[kHold];
+    uint32_t so[kHold];
+#pragma unroll
+    for (uint32_t u = 0; u < kHold; ++u) {
+      const uint32_t x = x0 + u * 32 + lane;
+      so[u] = range_off(v, min(x, v.count - 1));
+      xv[u] = x < v.count ? cv[so[u]] : 0.0f;
+    }
+#pragma unroll
+    for (uint32_t u = 0; u < kHold; ++u) {
+      const uint32_t x = x0 + u * 32 + lane;
+      if (x0 + u * 32 >= v.count) break;  // warp-uniform
+      const uint32_t key = mag_key(xv[u]);
+      const uint32_t b = bin_of(key, gsh.x, gsh.y);
+      gt += (x < v.count && b > bstar) ? 1u : 0u;
+      const bool inb = x < v.count && b == bstar;
+      const uint32_t m = __ballot_sync(0xffffffffu, inb);
+      if (m) {
+        uint32_t base = 0;
+        if (lane == 0) base = atomicAdd(&a.bnd_cnt[v.pl], (uint32_t)__popc(m));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        if (inb) {
+          const uint32_t pos = base + __popc(m & lanemask_lt());
+          if (pos < kBoundCap) bnd[pos] = make_uint2(key, ci[so[u]]);
+          else atomicOr(&a.lsel[v.pl].overflow, 1u);
         }
-        __syncthreads();  // wpre is rewritten by the next window
       }
     }
-  };
+  }
+  gt = warp_sum(gt);
+  if (lane == 0) wgt[warp] = gt;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t sum = 0;
+    for (uint32_t w = 0; w < 8; ++w) sum += wgt[w];
+    a.range_gt[(uint64_t)v.p * a.nranges + blockIdx.x % a.nranges] = sum;
+  }
+}
 
-  // Radix select of the k-th largest key: digits of 11, 11 and 9 bits.
+// Per (node, long segment), one CTA of 1,024 threads: the exact k-th key T
+// among the boundary bin's candidates (three radix digits in shared memory),
+// the index cut I_T (keys equal to T are kept up to the tie_take-th lowest
+// index: four 8-bit digits of the index), the kept boundary entries counted
+// per range, and the output offset of every range (a scan over the ranges).
+constexpr uint32_t kExactThreads = 1024;
+
+__global__ void __launch_bounds__(kExactThreads) long_exact_kernel(Args a) {
+  extern __shared__ __align__(16) uint32_t dyn[];
+  uint32_t* skey = dyn;                     // [kBoundCap]
+  uint32_t* sidx = skey + kBoundCap;        // [kBoundCap]
+  uint32_t* rkeep = sidx + kBoundCap;       // [kMaxRanges] kept boundary entries per range
+  uint32_t* hist = rkeep + kMaxRanges;      // [2048]
+  __shared__ uint32_t scratch[34];
+  __shared__ uint32_t res[2];
+  const uint32_t t = threadIdx.x;
+  const uint32_t p = blockIdx.x / a.nlong, ls = blockIdx.x % a.nlong;
+  const uint32_t s = a.long_list[ls];
+  const SegRec r = a.recs[s];
+  const uint64_t pl = (uint64_t)p * a.nlong + ls;
+  LongSel& L = a.lsel[pl];
+  if (L.mode != kModeNormal) return;  // CTA-uniform
+  const uint32_t M = a.bnd_cnt[pl];
+  if (L.overflow || M > kBoundCap || M < L.rank) {
+    __syncthreads();
+    if (t == 0) L.mode = kModeFallback;
+    return;
+  }
+  const uint2* bnd = a.bnd + pl * kBoundCap;
+  for (uint32_t i = t; i < M; i += kExactThreads) {
+    const uint2 e = bnd[i];
+    skey[i] = e.x;
+    sidx[i] = e.y;
+  }
+  const uint32_t nr = (r.nchunk * kWarpsPerChunk + kRangeSubs - 1) / kRangeSubs;
+  for (uint32_t i = t; i < nr; i += kExactThreads) rkeep[i] = 0;
+  __syncthreads();
+  // the rank-th largest key: digits of 11, 11 and 9 bits
+  uint32_t prefix = 0, rem = L.rank;
+  for (int d = 0; d < 3; ++d) {
+    const uint32_t width = d < 2 ? 11 : 9, shift = d == 0 ? 20 : (d == 1 ? 9 : 0);
+    const uint32_t nb = 1u << width, hi_shift = shift + width;
+    for (uint32_t b = t; b < 2048; b += kExactThreads) hist[b] = 0;
+    __syncthreads();
+    for (uint32_t i = t; i < M; i += kExactThreads) {
+      const uint32_t key = skey[i];
+      if (d == 0 || (key >> hi_shift) == prefix) atomicAdd(&hist[(key >> shift) & (nb - 1)], 1u);
+    }
+    __syncthreads();
+    find_from_top(hist, 2048, rem, scratch, res);  // bins past nb stay zero
+    uint32_t b = res[0];
+    if (b == kNone) {  // cannot happen for consistent counts
+      set_status(a.status, SPARCML_ERR_BAD_STREAM);
+      b = 0;
+    } else {
+      rem -= res[1];
+    }
+    prefix = (prefix << width) | b;
+    __syncthreads();
+  }
+  const uint32_t T = prefix, tie_take = rem;  // keys == T to keep, lowest indices first
+  // index cut among keys == T: the tie_take-th smallest index (4 digits of 8 bits)
+  uint32_t n_eq = 0;
+  for (uint32_t i = t; i < M; i += kExactThreads) n_eq += skey[i] == T ? 1u : 0u;
+  uint32_t eq_total;
+  block_excl_scan(n_eq, scratch, &eq_total);
+  uint32_t cut = 0xffffffffu;
+  if (tie_take < eq_total) {
+    uint32_t ip = 0, irem = tie_take;  // smallest first: count from the bottom
+    for (int d = 0; d < 4; ++d) {
+      const uint32_t shift = 24 - 8 * d;
+      for (uint32_t b = t; b < 2048; b += kExactThreads) hist[b] = 0;
+      __syncthreads();
+      for (uint32_t i = t; i < M; i += kExactThreads) {
+        const uint32_t x = sidx[i];
+        if (skey[i] == T && (d == 0 || (x >> (shift + 8)) == ip))
+          atomicAdd(&hist[2047 - ((x >> shift) & 255u)], 1u);  // reversed: smallest on top
+      }
+      __syncthreads();
+      find_from_top(hist, 2048, irem, scratch, res);
+      uint32_t b = res[0];
+      if (b == kNone) {
+        set_status(a.status, SPARCML_ERR_BAD_STREAM);
+        b = 2047;
+      } else {
+        irem -= res[1];
+      }
+      ip = (ip << 8) | (2047 - b);
+      __syncthreads();
+    }
+    cut = ip;
+  }
+  // kept boundary entries per range
+  const uint64_t row = (uint64_t)p * a.N;
+  const uint64_t A = (row + r.begin) & ~3ull;
+  for (uint32_t i = t; i < M; i += kExactThreads) {
+    const uint32_t key = skey[i], x = sidx[i];
+    if (key > T || (key == T && x <= cut)) {
+      const uint32_t sub = (uint32_t)((row + x - A) / kSub);
+      atomicAdd(&rkeep[sub / kRangeSubs], 1u);
+    }
+  }
+  __syncthreads();
+  // output offsets of the ranges: above-bin counts plus kept boundary entries
+  const uint64_t rg0 = (uint64_t)p * a.nranges + r.range0;
+  uint32_t run = 0;
+  for (uint32_t i0 = 0; i0 < nr; i0 += kExactThreads) {
+    const uint32_t i = i0 + t;
+    const uint32_t c = i < nr ? a.range_gt[rg0 + i] + rkeep[i] : 0u;
+    uint32_t tot;
+    const uint32_t ex = block_excl_scan(c, scratch, &tot);
+    if (i < nr) a.range_off[rg0 + i] = run + ex;
+    run += tot;
+    __syncthreads();
+  }
+  if (t == 0) {
+    if (run != r.k) {  // the counts do not add up: decide the segment again raw
+      L.mode = kModeFallback;
+    } else {
+      L.T = T;
+      L.cut = cut;
+    }
+  }
+}
+
+// Per range: every candidate with key > T, or key == T and index <= I_T, in
+// index order at the range's offset; the residual is zeroed there. Each warp
+// keeps its first 512 candidates (values, offsets, keep bits) in registers
+// between the count and the write; any beyond are read again.
+__global__ void __launch_bounds__(256) long_write_kernel(Args a) {
+  __shared__ uint32_t wcnt[8];
+  __shared__ uint32_t wbase[8];
+  RangeView v;
+  range_view(a, &v);
+  if (a.lsel[v.pl].mode != kModeNormal) return;  // CTA-uniform
+  const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+  const LongSel L = a.lsel[v.pl];
+  const uint32_t T = L.T, cut = L.cut;
+  const float* cv = a.cand_val + v.slot_base;
+  const uint32_t* ci = a.cand_idx + v.slot_base;
+  auto kept = [&](float x, uint32_t o, bool valid) {
+    const uint32_t key = mag_key(x);
+    return valid && (key > T || (key == T && ci[o] <= cut));
+  };
+  // count: the held batch, then any further batches
+  float xv[kHold];
+  uint32_t so[kHold];
+  uint32_t kb = 0, n = 0;
+#pragma unroll
+  for (uint32_t u = 0; u < kHold; ++u) {
+    const uint32_t x = u * 32 + lane;
+    so[u] = range_off(v, min(x, v.count - 1));
+    xv[u] = x < v.count ? cv[so[u]] : 0.0f;
+  }
+#pragma unroll
+  for (uint32_t u = 0; u < kHold; ++u) {
+    const bool k_ = kept(xv[u], so[u], u * 32 + lane < v.count);
+    kb |= (k_ ? 1u : 0u) << u;
+    n += k_ ? 1u : 0u;
+  }
+  for (uint32_t x0 = 32 * kHold; x0 < v.count; x0 += 32) {
+    const uint32_t x = x0 + lane;
+    const uint32_t o = range_off(v, min(x, v.count - 1));
+    n += kept(x < v.count ? cv[o] : 0.0f, o, x < v.count) ? 1u : 0u;
+  }
+  n = warp_sum(n);
+  if (lane == 0) wcnt[warp] = n;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t run = a.range_off[(uint64_t)v.p * a.nranges + blockIdx.x % a.nranges];
+    for (uint32_t w = 0; w < 8; ++w) {
+      wbase[w] = run;
+      run += wcnt[w];
+    }
+  }
+  __syncthreads();
+  uint32_t pos = wbase[warp];
+  const uint64_t out0 = (uint64_t)v.p * a.cap + v.rec.out0;
+  float* rp = a.residual + (uint64_t)v.p * a.N;
+  const uint64_t keep = l2_policy_evict_last();
+  auto emit = [&](bool k_, uint32_t idx, float val) {
+    const uint32_t m = __ballot_sync(0xffffffffu, k_);
+    if (k_) {
+      const uint32_t o = pos + __popc(m & lanemask_lt());
+      if (o < v.rec.k) {
+        st_keep(a.out_idx + out0 + o, idx, keep);
+        st_keep(a.out_val + out0 + o, val, keep);
+        rp[idx] = 0.0f;
+      } else {
+        set_status(a.status, SPARCML_ERR_BAD_STREAM);
+      }
+    }
+    pos += __popc(m);
+  };
+  uint32_t iv[kHold];
+#pragma unroll
+  for (uint32_t u = 0; u < kHold; ++u) iv[u] = (kb >> u) & 1u ? ci[so[u]] : 0u;
+#pragma unroll
+  for (uint32_t u = 0; u < kHold; ++u) emit((kb >> u) & 1u, iv[u], xv[u]);
+  for (uint32_t x0 = 32 * kHold; x0 < v.count; x0 += 32) {
+    const uint32_t x = x0 + lane;
+    const uint32_t o = range_off(v, min(x, v.count - 1));
+    const float val = x < v.count ? cv[o] : 0.0f;
+    const bool k_ = kept(val, o, x < v.count);
+    emit(k_, k_ ? ci[o] : 0u, val);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 4c. raw select: the segment decided from its acc (already in residual), by
+// a cluster of CS CTAs (CTA q owns the q-th of CS equal parts). Three radix
+// digits (11, 11, 9 bits) of the exact k-th key T, the histograms summed
+// through distributed shared memory; then each CTA's counts of keys > T and
+// == T, their prefix over the cluster, and an ordered compaction.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kRawThreads = 256;
+constexpr uint32_t kRawCluster = 8;
+
+struct RawShared {
+  uint32_t hist[2048];
+  uint32_t tot[2048];
+  uint32_t scratch[34];
+  uint32_t res[2];
+  uint32_t cnt[2];  // this CTA's (> T, == T) counts, read by higher ranks
+};
+
+__device__ void select_raw(const Args& a, RawShared& sh, cg::cluster_group& cluster, uint32_t p,
+                           uint32_t s, uint32_t rank, uint32_t CS) {
+  const SegRec r = a.recs[s];
+  const uint32_t t = threadIdx.x, k = r.k;
+  if (t == 0 && rank == 0) atomicAdd(a.fallbacks, 1u);
+  const uint32_t lo = r.begin + (uint32_t)((uint64_t)r.n * rank / CS);
+  const uint32_t hi = r.begin + (uint32_t)((uint64_t)r.n * (rank + 1) / CS);
+  const float* rp0 = a.residual + (uint64_t)p * a.N;
+  float* rp = a.residual + (uint64_t)p * a.N;
+  auto for_each = [&](auto&& body) {
+    for (uint32_t v0 = lo; v0 < hi; v0 += blockDim.x) {
+      const uint32_t i = v0 + t;
+      const bool valid = i < hi;
+      body(valid, i, valid ? rp0[i] : 0.0f);
+    }
+  };
   uint32_t prefix = 0, rem = k;
   for (int d = 0; d < 3; ++d) {
     const uint32_t width = d < 2 ? 11 : 9, shift = d == 0 ? 20 : (d == 1 ? 9 : 0);
@@ -792,22 +1151,23 @@ __device__ __forceinline__ void select_segment(const SelectArgs& a, SelectShared
     __syncthreads();
     for_each([&](bool valid, uint32_t, float x) {
       const uint32_t key = mag_key(x);
-      const bool match = valid && (d == 0 || (key >> hi_shift) == prefix);
-      hist_add(sh.hist, (key >> shift) & (nb - 1), match);
+      hist_add(sh.hist, (key >> shift) & (nb - 1), valid && (d == 0 || (key >> hi_shift) == prefix));
     });
     __syncthreads();
     if (CS > 1) cluster.sync();
-    for (uint32_t b = t; b < nb; b += blockDim.x) {
+    for (uint32_t b = t; b < 2048; b += blockDim.x) {
       uint32_t sum = 0;
-      if (CS > 1) {
-        for (uint32_t q = 0; q < CS; ++q) sum += cluster.map_shared_rank(sh.hist, q)[b];
-      } else {
-        sum = sh.hist[b];
+      if (b < nb) {
+        if (CS > 1) {
+          for (uint32_t q = 0; q < CS; ++q) sum += cluster.map_shared_rank(sh.hist, q)[b];
+        } else {
+          sum = sh.hist[b];
+        }
       }
       sh.tot[b] = sum;
     }
     __syncthreads();
-    find_from_top(sh.tot, nb, rem, sh.scratch, sh.res);
+    find_from_top(sh.tot, 2048, rem, sh.scratch, sh.res);
     uint32_t b = sh.res[0];
     if (b == kNone) {  // cannot happen for consistent counts; keep going safely
       set_status(a.status, SPARCML_ERR_BAD_STREAM);
@@ -818,10 +1178,7 @@ __device__ __forceinline__ void select_segment(const SelectArgs& a, SelectShared
     prefix = (prefix << width) | b;
     if (CS > 1) cluster.sync();  // every CTA is done reading this CTA's histogram
   }
-  const uint32_t T = prefix;     // exact k-th largest key
-  const uint32_t tie_take = rem;  // keys == T to keep, lowest indices first
-
-  // Counts of this CTA: keys > T and keys == T.
+  const uint32_t T = prefix, tie_take = rem;
   uint32_t n_gt = 0, n_eq = 0;
   for_each([&](bool valid, uint32_t, float x) {
     const uint32_t key = mag_key(x);
@@ -847,9 +1204,7 @@ __device__ __forceinline__ void select_segment(const SelectArgs& a, SelectShared
     }
     cluster.sync();  // peers may exit or reuse their shared memory after this
   }
-
-  // Ordered compaction of the kept entries.
-  const uint64_t out0 = (uint64_t)p * g.cap + (uint64_t)s * g.k_full;
+  const uint64_t out0 = (uint64_t)p * a.cap + r.out0;
   uint32_t run_gt = gt_pre, run_eq = eq_pre;
   for_each([&](bool valid, uint32_t i, float x) {
     const uint32_t key = mag_key(x);
@@ -874,276 +1229,35 @@ __device__ __forceinline__ void select_segment(const SelectArgs& a, SelectShared
   });
 }
 
-// ---------------------------------------------------------------------------
-// Long segments (thousands of chunks): the exact select as a sequence of
-// grid-wide passes, each CTA owning a range of kRangeSubs warp sub-chunks of
-// one segment (a few hundred candidates), so the whole GPU works on every
-// pass:
-//   long_hist  x3  histogram of one radix digit (11, 11, 9 bits) of the keys
-//                  that match the prefix so far, per CTA in shared memory,
-//                  flushed into the segment's global histogram;
-//   long_find  x3  one CTA per segment: the boundary bin -> prefix, rank left;
-//   long_count     per range: keys > T and keys == T;
-//   long_scan      one CTA per segment: exclusive prefix over its ranges;
-//   long_write     per range: the kept entries in index order, residual = 0.
-// Segments whose candidates do not cover k (or overflowed a slot) are left to
-// topk_select_kernel, which reads their acc directly.
-// ---------------------------------------------------------------------------
-constexpr uint32_t kRangeSubs = 256;
-constexpr uint32_t kHistWords = 2048 + 2048 + 512;  // per segment: the three digits
-
-struct LongArgs {
-  Geo g;
-  const uint32_t* seg_cnt;
-  const uint32_t* seg_flag;
-  const uint32_t* sub_cnt;
-  const uint32_t* cand_idx;
-  const float* cand_val;
-  float* residual;
-  uint32_t* out_idx;
-  float* out_val;
-  int32_t* status;
-  uint32_t* hist;       // [P * nseg][kHistWords]
-  uint32_t* sel;        // [P * nseg][2]: prefix so far, rank left (then T, tie_take)
-  uint32_t* range_cnt;  // [P * nseg][nr][2]: keys > T, keys == T (then their prefixes)
-  uint32_t nr;          // ranges of a full segment
-};
-
-__device__ __forceinline__ bool long_eligible(const LongArgs& a, uint32_t gs, uint32_t k) {
-  return k > 0 && a.seg_flag[gs] == 0 && a.seg_cnt[gs] >= k;
-}
-
-// The candidates of range r of segment gs: per-sub-chunk prefix in spre,
-// returns their count (0 if the range is empty or the segment is not handled).
-__device__ uint32_t long_range_setup(const LongArgs& a, uint32_t gs, uint32_t r, uint32_t* spre,
-                                     uint32_t* scratch, uint64_t* sub_base) {
-  const Geo& g = a.g;
-  const uint32_t s = gs % g.nseg, p = gs / g.nseg;
-  const uint32_t nsub = seg_chunks(g, s) * kWarpsPerChunk;
-  const uint32_t sa = r * kRangeSubs;
-  if (sa >= nsub || !long_eligible(a, gs, seg_k(g, s))) return 0;  // CTA-uniform
-  const uint32_t nr = min(kRangeSubs, nsub - sa);
-  *sub_base = ((uint64_t)p * g.nchunk + (uint64_t)s * g.m) * kWarpsPerChunk + sa;
-  const uint32_t c = threadIdx.x < nr ? a.sub_cnt[*sub_base + threadIdx.x] : 0u;
-  uint32_t tot;
-  const uint32_t ex = block_excl_scan(c, scratch, &tot);
-  if (threadIdx.x < nr) spre[threadIdx.x] = ex;
-  if (threadIdx.x == 0) spre[nr] = tot;
-  for (uint32_t i = nr + 1 + threadIdx.x; i <= kRangeSubs; i += blockDim.x) spre[i] = tot;
-  __syncthreads();
-  return tot;
-}
-
-__device__ __forceinline__ uint64_t long_slot(const LongArgs& a, const uint32_t* spre,
-                                              uint64_t sub_base, uint32_t v) {
-  uint32_t w = 0;
-#pragma unroll
-  for (uint32_t step = kRangeSubs / 2; step > 0; step >>= 1)
-    if (spre[w + step] <= v) w += step;
-  return (sub_base + w) * a.g.slot + (v - spre[w]);
-}
-
-__global__ void __launch_bounds__(kSelectThreads)
-long_hist_kernel(LongArgs a, int d) {
-  __shared__ uint32_t spre[kRangeSubs + 1];
-  __shared__ uint32_t scratch[34];
-  __shared__ uint32_t hist[2048];
-  const uint32_t gs = blockIdx.x / a.nr, r = blockIdx.x % a.nr;
-  uint64_t sub_base = 0;
-  const uint32_t M = long_range_setup(a, gs, r, spre, scratch, &sub_base);
-  if (M == 0) return;
-  const uint32_t width = d < 2 ? 11 : 9, shift = d == 0 ? 20 : (d == 1 ? 9 : 0);
-  const uint32_t nb = 1u << width, hi_shift = shift + width;
-  const uint32_t prefix = d == 0 ? 0u : a.sel[2 * gs];
-  for (uint32_t b = threadIdx.x; b < nb; b += blockDim.x) hist[b] = 0;
-  __syncthreads();
-  constexpr uint32_t kB = 4;
-  for (uint32_t v0 = 0; v0 < M; v0 += blockDim.x * kB) {
-    float x[kB];
-#pragma unroll
-    for (uint32_t q = 0; q < kB; ++q) {
-      const uint32_t v = v0 + q * blockDim.x + threadIdx.x;
-      x[q] = v < M ? a.cand_val[long_slot(a, spre, sub_base, v)] : 0.0f;
-    }
-#pragma unroll
-    for (uint32_t q = 0; q < kB; ++q) {
-      const uint32_t v = v0 + q * blockDim.x + threadIdx.x;
-      const uint32_t key = mag_key(x[q]);
-      hist_add(hist, (key >> shift) & (nb - 1),
-               v < M && (d == 0 || (key >> hi_shift) == prefix));
-    }
-  }
-  __syncthreads();
-  uint32_t* gh = a.hist + (uint64_t)gs * kHistWords + (d == 0 ? 0 : (d == 1 ? 2048 : 4096));
-  for (uint32_t b = threadIdx.x; b < nb; b += blockDim.x)
-    if (hist[b]) atomicAdd(&gh[b], hist[b]);
-}
-
-__global__ void __launch_bounds__(kSelectThreads)
-long_find_kernel(LongArgs a, int d) {
-  __shared__ uint32_t scratch[34];
-  __shared__ uint32_t res[2];
-  const uint32_t gs = blockIdx.x;
-  const Geo& g = a.g;
-  const uint32_t k = seg_k(g, gs % g.nseg);
-  if (!long_eligible(a, gs, k)) return;
-  const uint32_t width = d < 2 ? 11 : 9, nb = 1u << width;
-  const uint32_t* gh = a.hist + (uint64_t)gs * kHistWords + (d == 0 ? 0 : (d == 1 ? 2048 : 4096));
-  const uint32_t prefix = d == 0 ? 0u : a.sel[2 * gs];
-  const uint32_t rem = d == 0 ? k : a.sel[2 * gs + 1];
-  find_from_top(gh, nb, rem, scratch, res);
-  if (threadIdx.x == 0) {
-    uint32_t b = res[0], above = res[1];
-    if (b == kNone) {  // cannot happen for consistent counts
-      set_status(a.status, SPARCML_ERR_BAD_STREAM);
-      b = 0;
-      above = 0;
-    }
-    a.sel[2 * gs] = (prefix << width) | b;
-    a.sel[2 * gs + 1] = rem - above;
-  }
-}
-
-__global__ void __launch_bounds__(kSelectThreads)
-long_count_kernel(LongArgs a) {
-  __shared__ uint32_t spre[kRangeSubs + 1];
-  __shared__ uint32_t scratch[34];
-  const uint32_t gs = blockIdx.x / a.nr, r = blockIdx.x % a.nr;
-  uint64_t sub_base = 0;
-  const uint32_t M = long_range_setup(a, gs, r, spre, scratch, &sub_base);
-  if (M == 0) {
-    if (threadIdx.x == 0) {
-      a.range_cnt[2 * ((uint64_t)gs * a.nr + r)] = 0;
-      a.range_cnt[2 * ((uint64_t)gs * a.nr + r) + 1] = 0;
+// mode 0: the layer-sized segments on the to-do list, one CTA each (grid-
+// stride); mode 1: the long segments in fallback mode, one cluster each.
+__global__ void __launch_bounds__(kRawThreads) topk_select_raw_kernel(Args a, int mode) {
+  __shared__ RawShared sh;
+  cg::cluster_group cluster = cg::this_cluster();
+  if (mode == 0) {
+    const uint32_t n_todo = *a.todo_cnt;
+    for (uint32_t i = blockIdx.x; i < n_todo; i += gridDim.x) {
+      const uint32_t gs = a.todo[i];
+      select_raw(a, sh, cluster, gs / a.nseg, gs % a.nseg, 0, 1);
+      __syncthreads();
     }
     return;
   }
-  const uint32_t T = a.sel[2 * gs];
-  uint32_t n_gt = 0, n_eq = 0;
-  constexpr uint32_t kB = 4;
-  for (uint32_t v0 = 0; v0 < M; v0 += blockDim.x * kB) {
-    float x[kB];
-#pragma unroll
-    for (uint32_t q = 0; q < kB; ++q) {
-      const uint32_t v = v0 + q * blockDim.x + threadIdx.x;
-      x[q] = v < M ? a.cand_val[long_slot(a, spre, sub_base, v)] : 0.0f;
-    }
-#pragma unroll
-    for (uint32_t q = 0; q < kB; ++q) {
-      const uint32_t v = v0 + q * blockDim.x + threadIdx.x;
-      const uint32_t key = mag_key(x[q]);
-      n_gt += (v < M && key > T) ? 1u : 0u;
-      n_eq += (v < M && key == T) ? 1u : 0u;
-    }
-  }
-  uint32_t tg, te;
-  block_excl_scan(n_gt, scratch, &tg);
-  __syncthreads();
-  block_excl_scan(n_eq, scratch, &te);
-  if (threadIdx.x == 0) {
-    a.range_cnt[2 * ((uint64_t)gs * a.nr + r)] = tg;
-    a.range_cnt[2 * ((uint64_t)gs * a.nr + r) + 1] = te;
-  }
+  const uint32_t CS = cluster.num_blocks();
+  const uint32_t pl = blockIdx.x / CS;
+  const uint32_t p = pl / a.nlong, ls = pl % a.nlong;
+  if (a.lsel[pl].mode != kModeFallback) return;  // uniform over the cluster
+  select_raw(a, sh, cluster, p, a.long_list[ls], cluster.block_rank(), CS);
 }
 
-__global__ void __launch_bounds__(1024)
-long_scan_kernel(LongArgs a) {
-  __shared__ uint32_t scratch[34];
-  const uint32_t gs = blockIdx.x;
-  const Geo& g = a.g;
-  if (!long_eligible(a, gs, seg_k(g, gs % g.nseg))) return;
-  uint32_t* rc = a.range_cnt + 2 * (uint64_t)gs * a.nr;
-  uint32_t run_gt = 0, run_eq = 0;
-  for (uint32_t r0 = 0; r0 < a.nr; r0 += blockDim.x) {
-    const uint32_t r = r0 + threadIdx.x;
-    const uint32_t cg_ = r < a.nr ? rc[2 * r] : 0u, ce = r < a.nr ? rc[2 * r + 1] : 0u;
-    uint32_t tg, te;
-    const uint32_t eg = block_excl_scan(cg_, scratch, &tg);
-    __syncthreads();
-    const uint32_t ee = block_excl_scan(ce, scratch, &te);
-    if (r < a.nr) {
-      rc[2 * r] = run_gt + eg;
-      rc[2 * r + 1] = run_eq + ee;
-    }
-    run_gt += tg;
-    run_eq += te;
-    __syncthreads();
-  }
-}
-
-__global__ void __launch_bounds__(kSelectThreads)
-long_write_kernel(LongArgs a) {
-  __shared__ uint32_t spre[kRangeSubs + 1];
-  __shared__ uint32_t scratch[34];
-  const uint32_t gs = blockIdx.x / a.nr, r = blockIdx.x % a.nr;
-  uint64_t sub_base = 0;
-  const uint32_t M = long_range_setup(a, gs, r, spre, scratch, &sub_base);
-  if (M == 0) return;
-  const Geo& g = a.g;
-  const uint32_t p = gs / g.nseg, s = gs % g.nseg, k = seg_k(g, s);
-  const uint32_t T = a.sel[2 * gs], tie_take = a.sel[2 * gs + 1];
-  uint32_t run_gt = a.range_cnt[2 * ((uint64_t)gs * a.nr + r)];
-  uint32_t run_eq = a.range_cnt[2 * ((uint64_t)gs * a.nr + r) + 1];
-  float* rp = a.residual + (uint64_t)p * g.N;
-  const uint64_t out0 = (uint64_t)p * g.cap + (uint64_t)s * g.k_full;
-  const uint64_t keep = l2_policy_evict_last();
-  for (uint32_t v0 = 0; v0 < M; v0 += blockDim.x) {
-    const uint32_t v = v0 + threadIdx.x;
-    uint64_t slot = 0;
-    float x = 0.0f;
-    if (v < M) {
-      slot = long_slot(a, spre, sub_base, v);
-      x = a.cand_val[slot];
-    }
-    const uint32_t key = mag_key(x);
-    const bool gt = v < M && key > T, eq = v < M && key == T;
-    uint32_t tot;
-    const uint32_t ex = block_excl_scan((gt ? 1u : 0u) | (eq ? 0x10000u : 0u), scratch, &tot);
-    const uint32_t e_gt = run_gt + (ex & 0xffffu), e_eq = run_eq + (ex >> 16);
-    if (gt || (eq && e_eq < tie_take)) {
-      const uint32_t pos = e_gt + min(e_eq, tie_take);
-      if (pos < k) {
-        const uint32_t i = a.cand_idx[slot];
-        st_keep(a.out_idx + out0 + pos, i, keep);
-        st_keep(a.out_val + out0 + pos, x, keep);
-        rp[i] = 0.0f;
-      } else {
-        set_status(a.status, SPARCML_ERR_BAD_STREAM);
-      }
-    }
-    run_gt += tot & 0xffffu;
-    run_eq += tot >> 16;
-    __syncthreads();
-  }
-}
-
-__global__ void __launch_bounds__(kSelectThreads)
-topk_select_kernel(SelectArgs a) {
-  __shared__ SelectShared sh;
-  cg::cluster_group cluster = cg::this_cluster();
-  if (a.warp_done) {  // only the segments the short kernel handed over
-    const uint32_t n_todo = *a.todo_cnt;
-    for (uint32_t i = blockIdx.x; i < n_todo; i += gridDim.x) {
-      select_segment(a, sh, cluster, a.todo[i], 0);
-      __syncthreads();
-    }
-  } else {
-    select_segment(a, sh, cluster, blockIdx.x / a.CS, a.CS > 1 ? cluster.block_rank() : 0u);
-  }
-}
-
-struct Layout {
-  size_t todo_cnt, guess, seg_cnt, seg_flag, todo, chunk_cnt, cand_idx, cand_val;
-  size_t lhist, lsel, lrange, total;
-  uint32_t nr;  // long-segment ranges of a full segment
-};
-
+// ---------------------------------------------------------------------------
+// Host side: the plan of one call.
+// ---------------------------------------------------------------------------
 // Rank of the guess in a sample of S of a segment's n entries with k kept:
 // r = ceil(lambda + 4 sqrt(lambda) + 8) with lambda = k S / n, the expected
 // number of sampled keys among the top k plus four standard deviations and a
 // margin, so the r-th largest sample key is very likely at or below the k-th
-// key of the segment. Computed once on the host (double precision is slow on
-// this GPU's cores).
+// key of the segment.
 uint32_t sample_rank(uint32_t k, uint32_t n, uint32_t S) {
   if (n == 0) return 0;
   const double lam = (double)k * (double)S / (double)n;
@@ -1151,56 +1265,318 @@ uint32_t sample_rank(uint32_t k, uint32_t n, uint32_t S) {
   return rr >= (double)S ? S : (uint32_t)rr;
 }
 
-bool make_geo(int32_t P, uint64_t N, uint64_t seg_len, uint32_t k_num, uint32_t k_den, Geo* g) {
-  if (P < 1 || P > 65535 || N < 1 || N > 0xffffffffull || seg_len < 1 || k_den < 1 ||
-      k_num > k_den)
-    return false;
-  const uint64_t L = std::min<uint64_t>(seg_len, N);
-  g->N = N;
-  g->L = (uint32_t)L;
-  g->nseg = (uint32_t)((N + L - 1) / L);
-  g->L_last = (uint32_t)(N - (uint64_t)(g->nseg - 1) * L);
-  g->m = (uint32_t)((L + kChunk - 1) / kChunk);
-  g->m_last = (g->L_last + kChunk - 1) / kChunk;
-  const uint64_t nchunk = (uint64_t)(g->nseg - 1) * g->m + g->m_last;
-  if (nchunk > 0xffffffffull || (uint64_t)P * g->nseg > 0x7fffffffull ||
-      (uint64_t)P * nchunk > 0x7fffffffull)
-    return false;
-  g->nchunk = (uint32_t)nchunk;
-  g->k_full = (uint32_t)(L * k_num / k_den);
-  g->k_last = (uint32_t)((uint64_t)g->L_last * k_num / k_den);
-  // Expected candidates are about d + a few per cent of a chunk; the slot
-  // holds 2d + 1/8 of it (or all of it), and overflow falls back safely.
-  const double want = (double)kSub * (2.0 * k_num / k_den) + kSub / 8.0;
-  uint32_t slot = (uint32_t)std::min<double>(kSub, std::ceil(want / 32.0) * 32.0);
-  g->slot = std::max<uint32_t>(slot, 32);
-  g->P = P;
-  auto cta_sample = [](uint32_t n) { return n <= kShortSegment ? kSampleShort : kSampleMax; };
-  g->r_warp_full = sample_rank(g->k_full, g->L, kWarpSample);
-  g->r_warp_last = sample_rank(g->k_last, g->L_last, kWarpSample);
-  g->r_cta_full = sample_rank(g->k_full, g->L, cta_sample(g->L));
-  g->r_cta_last = sample_rank(g->k_last, g->L_last, cta_sample(g->L_last));
-  return true;
+// Rank of the histogram's upper anchor: half of the sample count that is
+// very likely still above the k-th key, at least 1.
+uint32_t anchor_rank(uint32_t k, uint32_t n, uint32_t S) {
+  const double lam = (double)k * (double)S / (double)n;
+  const double lo = lam - 4.0 * std::sqrt(lam) - 8.0;
+  return lo >= 2.0 ? (uint32_t)(lo / 2.0) : 1u;
 }
 
-Layout make_layout(const Geo& g) {
-  Layout l;
-  size_t o = 256;  // status word and padding
-  const size_t nsegs = (size_t)g.P * g.nseg, nch = (size_t)g.P * g.nchunk * kWarpsPerChunk;
-  l.todo_cnt = 64;
-  l.guess = o; o = align_up(o + 4 * nsegs, 256);
-  l.todo = o; o = align_up(o + 4 * nsegs, 256);
-  l.seg_cnt = o; o = align_up(o + 4 * nsegs, 256);
-  l.seg_flag = o; o = align_up(o + 4 * nsegs, 256);
-  l.chunk_cnt = o; o = align_up(o + 4 * nch, 256);
-  l.cand_idx = o; o = align_up(o + 4 * nch * g.slot, 256);
-  l.cand_val = o; o = align_up(o + 4 * nch * g.slot, 256);
-  l.nr = (uint32_t)(((uint64_t)g.m * kWarpsPerChunk + kRangeSubs - 1) / kRangeSubs);
-  l.lhist = o; o = align_up(o + 4 * nsegs * kHistWords, 256);
-  l.lsel = o; o = align_up(o + 8 * nsegs, 256);
-  l.lrange = o; o = align_up(o + 8 * nsegs * l.nr, 256);
-  l.total = o;
-  return l;
+struct Plan {
+  int32_t P;
+  uint64_t N;
+  uint32_t nseg, nchunk, nlong, nranges;
+  uint64_t total_k, node_slots;
+  std::vector<uint32_t> blob;  // records, then the lists
+  size_t w_recs, w_cta, w_warp, w_short, w_long, w_rmap;  // word offsets in the blob
+  uint32_t n_cta, n_warp, n_short;
+  uint32_t u_L, u_m;  // equal segments (the last one possibly shorter), else 0
+  // workspace byte offsets
+  size_t o_blob, o_desc, o_guess, o_cnt, o_flag, o_todo, o_sub, o_cidx, o_cval, o_hist, o_lsel,
+      o_bcnt, o_bnd, o_rgt, o_roff, total;
+};
+
+// Builds the plan; returns SPARCML_OK or the error of the arguments.
+int make_plan(int32_t P, uint64_t N, const uint64_t* seg_begin, const uint32_t* seg_k,
+              uint32_t nseg, Plan* pl) {
+  if (P < 1 || P > 65535 || N < 1 || N > 0xffffffffull || !seg_begin || !seg_k || nseg < 1 ||
+      seg_begin[0] != 0 || seg_begin[nseg] != N)
+    return SPARCML_ERR_INVALID_ARG;
+  Plan& q = *pl;
+  q.P = P;
+  q.N = N;
+  q.nseg = nseg;
+  std::vector<SegRec> recs(nseg);
+  std::vector<uint32_t> cta, warp, shrt, lng, rmap;
+  uint64_t chunks = 0, slots = 0, out = 0;
+  for (uint32_t s = 0; s < nseg; ++s) {
+    if (seg_begin[s + 1] <= seg_begin[s]) return SPARCML_ERR_INVALID_ARG;
+    const uint64_t n = seg_begin[s + 1] - seg_begin[s];
+    if (seg_k[s] > n) return SPARCML_ERR_INVALID_ARG;
+    SegRec& r = recs[s];
+    r.begin = (uint32_t)seg_begin[s];
+    r.n = (uint32_t)n;
+    r.k = seg_k[s];
+    r.out0 = (uint32_t)out;
+    out += r.k;
+    if (out > 0xffffffffull) return SPARCML_ERR_CAPACITY;
+    r.chunk0 = (uint32_t)chunks;
+    r.nchunk = (uint32_t)((n + 3 + kChunk - 1) / kChunk);
+    chunks += r.nchunk;
+    r.kind = r.k == 0 ? kKeepNone : r.k == n ? kKeepAll
+             : n <= kExactMax ? kExact : n <= kLayerMax ? kLayer : kLong;
+    if (r.kind == kLayer &&
+        (double)sample_rank(r.k, r.n, kWarpSample) * (double)n / kWarpSample > kShortExpect)
+      r.kind = kLong;
+    // sub-slot: about twice the density plus an eighth of a sub-chunk, at most
+    // what a sub-chunk of the segment can hold; none for the trivial kinds
+    uint32_t slot = 0;
+    if (r.kind != kKeepNone && r.kind != kKeepAll) {
+      const double want = (double)kSub * (2.0 * r.k / (double)n) + kSub / 8.0;
+      const double most = (double)std::min<uint64_t>(kSub, n + 3);
+      slot = (uint32_t)(std::ceil(std::min(want, most) / 32.0) * 32.0);
+      slot = std::max<uint32_t>(slot, 32);
+    }
+    r.slot = slot;
+    r.slot32 = (uint32_t)(slots / 32);
+    slots += (uint64_t)r.nchunk * kWarpsPerChunk * slot;
+    r.lidx = kNone;
+    r.range0 = 0;
+    r.rank = 0;
+    if (r.kind == kExact) {
+      r.rank = r.k;
+      cta.push_back(s);
+      shrt.push_back(s);
+    } else if (r.kind == kLayer) {
+      r.rank = sample_rank(r.k, r.n, kWarpSample);
+      warp.push_back(s);
+      shrt.push_back(s);
+    } else if (r.kind == kLong) {
+      r.rank = sample_rank(r.k, r.n, kSampleLong) | (anchor_rank(r.k, r.n, kSampleLong) << 16);
+      r.lidx = (uint32_t)lng.size();
+      r.range0 = (uint32_t)rmap.size();
+      const uint32_t nr = (r.nchunk * kWarpsPerChunk + kRangeSubs - 1) / kRangeSubs;
+      if (nr > kMaxRanges || r.lidx > 0xffffu) return SPARCML_ERR_INVALID_ARG;
+      for (uint32_t i = 0; i < nr; ++i) rmap.push_back((r.lidx << 16) | i);
+      lng.push_back(s);
+      cta.push_back(s);
+    }
+  }
+  if (chunks > 0xffffffffull || (uint64_t)P * chunks > 0x7fffffffull ||
+      (uint64_t)P * nseg > 0x7fffffffull || slots / 32 > 0xffffffffull ||
+      (uint64_t)P * rmap.size() > 0x7fffffffull)
+    return SPARCML_ERR_INVALID_ARG;
+  q.nchunk = (uint32_t)chunks;
+  q.node_slots = slots;
+  q.u_L = q.u_m = 0;
+  {
+    bool eq = true;
+    for (uint32_t s = 1; s + 1 < nseg && eq; ++s) eq = recs[s].n == recs[0].n;
+    if (eq && recs[nseg - 1].n <= recs[0].n) {
+      q.u_L = recs[0].n;
+      q.u_m = recs[0].nchunk;
+    }
+  }
+  q.total_k = out;
+  q.nlong = (uint32_t)lng.size();
+  q.nranges = (uint32_t)rmap.size();
+  q.n_cta = (uint32_t)cta.size();
+  q.n_warp = (uint32_t)warp.size();
+  q.n_short = (uint32_t)shrt.size();
+  // the blob: records then lists, each list 4-word aligned
+  auto pad4 = [](size_t w) { return (w + 3) / 4 * 4; };
+  q.w_recs = 0;
+  q.w_cta = pad4(q.w_recs + (size_t)nseg * 12);
+  q.w_warp = pad4(q.w_cta + cta.size());
+  q.w_short = pad4(q.w_warp + warp.size());
+  q.w_long = pad4(q.w_short + shrt.size());
+  q.w_rmap = pad4(q.w_long + lng.size());
+  q.blob.assign(pad4(q.w_rmap + rmap.size()), 0u);
+  std::copy(reinterpret_cast<const uint32_t*>(recs.data()),
+            reinterpret_cast<const uint32_t*>(recs.data()) + (size_t)nseg * 12, q.blob.begin());
+  std::copy(cta.begin(), cta.end(), q.blob.begin() + q.w_cta);
+  std::copy(warp.begin(), warp.end(), q.blob.begin() + q.w_warp);
+  std::copy(shrt.begin(), shrt.end(), q.blob.begin() + q.w_short);
+  std::copy(lng.begin(), lng.end(), q.blob.begin() + q.w_long);
+  std::copy(rmap.begin(), rmap.end(), q.blob.begin() + q.w_rmap);
+  // workspace layout
+  const uint64_t pseg = (uint64_t)P * nseg, psub = (uint64_t)P * chunks * kWarpsPerChunk;
+  const uint64_t plong = (uint64_t)P * q.nlong, prng = (uint64_t)P * q.nranges;
+  size_t o = 256;  // status word, fault-injection word, to-do counter
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes, 256);
+    return at;
+  };
+  q.o_blob = take(4 * q.blob.size());
+  q.o_desc = take(sizeof(ChunkDesc) * (size_t)chunks);
+  q.o_guess = take(8 * pseg);
+  q.o_cnt = take(4 * pseg);
+  q.o_flag = take(4 * pseg);
+  q.o_todo = take(4 * pseg);
+  q.o_sub = take(4 * psub);
+  q.o_cidx = take(4 * (uint64_t)P * slots);
+  q.o_cval = take(4 * (uint64_t)P * slots);
+  q.o_hist = take(4 * plong * kBins);
+  q.o_lsel = take(sizeof(LongSel) * plong);
+  q.o_bcnt = take(4 * plong);
+  q.o_bnd = take(8 * plong * kBoundCap);
+  q.o_rgt = take(4 * prng);
+  q.o_roff = take(4 * prng);
+  q.total = o;
+  return SPARCML_OK;
+}
+
+int launch_topk(const Plan& q, const float* grad, float* residual, uint32_t* out_idx,
+                float* out_val, uint32_t* out_nnz, uint64_t cap, void* ws, size_t ws_bytes,
+                cudaStream_t s, void* const* events) {
+  char* w = static_cast<char*>(ws);
+  auto mark = [&](int i) {
+    if (events && events[i]) cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s);
+  };
+  Args a = {};
+  a.grad = grad;
+  a.residual = residual;
+  a.out_idx = out_idx;
+  a.out_val = out_val;
+  a.out_nnz = out_nnz;
+  a.status = reinterpret_cast<int32_t*>(w);
+  a.N = q.N;
+  a.cap = cap;
+  a.node_slots = q.node_slots;
+  a.P = q.P;
+  a.nseg = q.nseg;
+  a.nchunk = q.nchunk;
+  a.nlong = q.nlong;
+  a.nranges = q.nranges;
+  a.total_k = (uint32_t)q.total_k;
+  a.vec = ((reinterpret_cast<uintptr_t>(grad) | reinterpret_cast<uintptr_t>(residual)) & 15) == 0;
+  a.u_L = q.u_L;
+  a.u_m = q.u_m;
+  uint32_t* blob = reinterpret_cast<uint32_t*>(w + q.o_blob);
+  a.recs = reinterpret_cast<const SegRec*>(blob + q.w_recs);
+  a.cta_list = blob + q.w_cta;
+  a.warp_list = blob + q.w_warp;
+  a.short_list = blob + q.w_short;
+  a.long_list = blob + q.w_long;
+  a.range_map = blob + q.w_rmap;
+  a.desc = reinterpret_cast<ChunkDesc*>(w + q.o_desc);
+  a.guess = reinterpret_cast<uint2*>(w + q.o_guess);
+  a.seg_cnt = reinterpret_cast<uint32_t*>(w + q.o_cnt);
+  a.seg_flag = reinterpret_cast<uint32_t*>(w + q.o_flag);
+  a.todo = reinterpret_cast<uint32_t*>(w + q.o_todo);
+  a.todo_cnt = reinterpret_cast<uint32_t*>(w + 64);
+  a.fallbacks = reinterpret_cast<uint32_t*>(w + kFallbackOffset);
+  a.sub_cnt = reinterpret_cast<uint32_t*>(w + q.o_sub);
+  a.cand_idx = reinterpret_cast<uint32_t*>(w + q.o_cidx);
+  a.cand_val = reinterpret_cast<float*>(w + q.o_cval);
+  a.hist = reinterpret_cast<uint32_t*>(w + q.o_hist);
+  a.lsel = reinterpret_cast<LongSel*>(w + q.o_lsel);
+  a.bnd_cnt = reinterpret_cast<uint32_t*>(w + q.o_bcnt);
+  a.bnd = reinterpret_cast<uint2*>(w + q.o_bnd);
+  a.range_gt = reinterpret_cast<uint32_t*>(w + q.o_rgt);
+  a.range_off = reinterpret_cast<uint32_t*>(w + q.o_roff);
+  uint64_t launches = 0;
+
+  mark(0);
+  // the plan's records and lists travel as kernel parameters
+  for (size_t i = 0; i < q.blob.size(); i += kUploadWords) {
+    UploadBatch b;
+    b.count = (uint32_t)std::min<size_t>(kUploadWords, q.blob.size() - i);
+    b.dst = blob + i;
+    std::copy(q.blob.begin() + i, q.blob.begin() + i + b.count, b.words);
+    topk_upload_kernel<<<1, 256, 0, s>>>(b);
+    ++launches;
+  }
+  {
+    const uint64_t items = q.nchunk + (uint64_t)q.P * q.nseg + (uint64_t)q.P * q.nlong * (kBins + 1) +
+                           (uint64_t)q.P;
+    topk_init_kernel<<<(unsigned)std::min<uint64_t>((items + 255) / 256, 4 * 152), 256, 0, s>>>(a);
+    ++launches;
+  }
+  if (q.n_cta) {
+    topk_guess_cta_kernel<<<(unsigned)((uint64_t)q.P * q.n_cta), kGuessThreads, 0, s>>>(a, q.n_cta);
+    ++launches;
+  }
+  if (q.n_warp) {
+    const uint64_t warps = (uint64_t)q.P * q.n_warp, wpc = kGuessThreads / 32;
+    topk_guess_warp_kernel<<<(unsigned)((warps + wpc - 1) / wpc), kGuessThreads, 0, s>>>(a, q.n_warp);
+    ++launches;
+  }
+  if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
+  mark(1);
+  {
+    const unsigned grid = (unsigned)((uint64_t)q.P * q.nchunk);
+    if (q.u_L)
+      topk_stream_kernel<true><<<grid, kStreamThreads, 0, s>>>(a);
+    else
+      topk_stream_kernel<false><<<grid, kStreamThreads, 0, s>>>(a);
+    ++launches;
+  }
+  if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
+  mark(2);
+  if (q.n_short) {
+    topk_select_short_kernel<<<(unsigned)((uint64_t)q.P * q.n_short), kSegThreads, 0, s>>>(
+        a, q.n_short);
+    topk_select_raw_kernel<<<(unsigned)std::min<uint64_t>((uint64_t)q.P * q.n_short, 2 * 152),
+                             kRawThreads, 0, s>>>(a, 0);
+    launches += 2;
+    if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
+  }
+  if (q.nlong) {
+    const unsigned pl = (unsigned)((uint64_t)q.P * q.nlong);
+    const unsigned pr = (unsigned)((uint64_t)q.P * q.nranges);
+    long_hist_kernel<<<pr, 256, 0, s>>>(a);
+    long_find_kernel<<<pl, 256, 0, s>>>(a);
+    long_collect_kernel<<<pr, 256, 0, s>>>(a);
+    const size_t smem = (2 * (size_t)kBoundCap + kMaxRanges + 2048) * sizeof(uint32_t);
+    if (!ensure_smem(reinterpret_cast<const void*>(long_exact_kernel), smem))
+      return SPARCML_ERR_CUDA;
+    long_exact_kernel<<<pl, kExactThreads, smem, s>>>(a);
+    long_write_kernel<<<pr, 256, 0, s>>>(a);
+    launches += 5;
+    if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(pl * kRawCluster, 1, 1);
+    cfg.blockDim = dim3(kRawThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kRawCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, topk_select_raw_kernel, a, 1) != cudaSuccess)
+      return SPARCML_ERR_CUDA;
+    ++launches;
+  }
+  mark(3);
+  note_launches(launches);
+  return SPARCML_OK;
+}
+
+int topk_call(const float* grad, float* residual, int32_t P, uint64_t N, const uint64_t* seg_begin,
+              const uint32_t* seg_k, uint32_t nseg, uint32_t* out_idx, float* out_val,
+              uint32_t* out_nnz, uint64_t cap, void* ws, size_t ws_bytes, void* stream,
+              void* const* events) {
+  if (!grad || !residual || !out_idx || !out_val || !out_nnz || !ws) return SPARCML_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return SPARCML_ERR_INVALID_ARG;
+  Plan q;
+  const int st = make_plan(P, N, seg_begin, seg_k, nseg, &q);
+  if (st != SPARCML_OK) return st;
+  if (ws_bytes < q.total) return SPARCML_ERR_WORKSPACE;
+  if (q.total_k > cap) return SPARCML_ERR_CAPACITY;
+  return launch_topk(q, grad, residual, out_idx, out_val, out_nnz, cap, ws, ws_bytes,
+                     static_cast<cudaStream_t>(stream), events);
+}
+
+// The equal-segment table: segment s = [s L, min((s + 1) L, N)), k_s =
+// floor(n_s k_num / k_den) (the last segment takes the remainder).
+bool uniform_table(uint64_t N, uint64_t seg_len, uint32_t k_num, uint32_t k_den,
+                   std::vector<uint64_t>* begin, std::vector<uint32_t>* ks) {
+  if (N < 1 || N > 0xffffffffull || seg_len < 1 || k_den < 1 || k_num > k_den) return false;
+  const uint64_t L = std::min<uint64_t>(seg_len, N);
+  begin->clear();
+  ks->clear();
+  for (uint64_t b = 0; b < N; b += L) {
+    begin->push_back(b);
+    ks->push_back((uint32_t)(std::min<uint64_t>(L, N - b) * k_num / k_den));
+  }
+  begin->push_back(N);
+  return true;
 }
 
 }  // namespace
@@ -1208,126 +1584,84 @@ Layout make_layout(const Geo& g) {
 
 using namespace sparcml;
 
-extern "C" size_t sparcml_topk_ef_workspace_size(int32_t P, uint64_t N, uint64_t seg_len,
-                                                 uint32_t k_num, uint32_t k_den) {
-  Geo g;
-  if (!make_geo(P, N, seg_len, k_num, k_den, &g)) return 0;
-  return make_layout(g).total;
+extern "C" uint32_t sparcml_topk_uniform_segments(uint64_t N, uint64_t seg_len, uint32_t k_num,
+                                                  uint32_t k_den, uint64_t* seg_begin,
+                                                  uint32_t* seg_k) {
+  std::vector<uint64_t> b;
+  std::vector<uint32_t> k;
+  if (!uniform_table(N, seg_len, k_num, k_den, &b, &k) || k.size() > 0xffffffffull) return 0;
+  if (seg_begin) std::copy(b.begin(), b.end(), seg_begin);
+  if (seg_k) std::copy(k.begin(), k.end(), seg_k);
+  return (uint32_t)k.size();
 }
 
-extern "C" int sparcml_topk_ef_traced(const float* grad, float* residual, int32_t P,
-                                      uint64_t N, uint64_t seg_len, uint32_t k_num,
-                                      uint32_t k_den, uint32_t* out_idx, float* out_val,
+extern "C" uint64_t sparcml_topk_total_k(const uint32_t* seg_k, uint32_t nseg) {
+  uint64_t t = 0;
+  if (seg_k)
+    for (uint32_t s = 0; s < nseg; ++s) t += seg_k[s];
+  return t;
+}
+
+extern "C" size_t sparcml_topk_ef_workspace_size(int32_t P, uint64_t N, const uint64_t* seg_begin,
+                                                 const uint32_t* seg_k, uint32_t nseg) {
+  Plan q;
+  if (make_plan(P, N, seg_begin, seg_k, nseg, &q) != SPARCML_OK) return 0;
+  return q.total;
+}
+
+extern "C" int sparcml_topk_ef_traced(const float* grad, float* residual, int32_t P, uint64_t N,
+                                      const uint64_t* seg_begin, const uint32_t* seg_k,
+                                      uint32_t nseg, uint32_t* out_idx, float* out_val,
                                       uint32_t* out_nnz, uint64_t cap, void* ws, size_t ws_bytes,
                                       void* stream, void* const* events) {
-  Geo g;
-  if (!grad || !residual || !out_idx || !out_val || !out_nnz || !ws ||
-      !make_geo(P, N, seg_len, k_num, k_den, &g))
-    return SPARCML_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return SPARCML_ERR_INVALID_ARG;
-  const Layout l = make_layout(g);
-  if (ws_bytes < l.total) return SPARCML_ERR_WORKSPACE;
-  const uint64_t total_k = (uint64_t)(g.nseg - 1) * g.k_full + g.k_last;
-  if (total_k > cap || total_k > 0xffffffffull) return SPARCML_ERR_CAPACITY;
-  g.cap = cap;
-  char* w = static_cast<char*>(ws);
-  uint32_t* guess = reinterpret_cast<uint32_t*>(w + l.guess);
-  uint32_t* seg_cnt = reinterpret_cast<uint32_t*>(w + l.seg_cnt);
-  uint32_t* seg_flag = reinterpret_cast<uint32_t*>(w + l.seg_flag);
-  uint32_t* chunk_cnt = reinterpret_cast<uint32_t*>(w + l.chunk_cnt);
-  uint32_t* cand_idx = reinterpret_cast<uint32_t*>(w + l.cand_idx);
-  float* cand_val = reinterpret_cast<float*>(w + l.cand_val);
-  int32_t* status = reinterpret_cast<int32_t*>(w);
-  uint32_t* todo = reinterpret_cast<uint32_t*>(w + l.todo);
-  uint32_t* todo_cnt = reinterpret_cast<uint32_t*>(w + l.todo_cnt);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  auto mark = [&](int i) {
-    if (events && events[i]) cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s);
-  };
-
-  mark(0);
-  const uint32_t nsegs = (uint32_t)P * g.nseg;
-  if (g.L > kSampleMax && g.L <= kShortSegment && g.L_last > kSampleMax) {
-    // layer-sized segments: one warp each
-    const uint32_t wpc = kGuessThreads / 32;
-    topk_guess_warp_kernel<<<(nsegs + wpc - 1) / wpc, kGuessThreads, 0, s>>>(
-        grad, residual, g, guess, seg_cnt, seg_flag, out_nnz, (uint32_t)total_k, todo_cnt);
-  } else {
-    // Keys per guess thread: the largest sample of any segment / kGuessThreads.
-    auto sample_size = [](uint32_t n) {
-      return n <= kSampleMax ? n : (n <= kShortSegment ? kSampleShort : kSampleMax);
-    };
-    const uint32_t smax = std::max(sample_size(g.L), sample_size(g.L_last));
-    if (smax <= 16 * kGuessThreads)
-      topk_guess_kernel<16><<<nsegs, kGuessThreads, 0, s>>>(
-          grad, residual, g, guess, seg_cnt, seg_flag, out_nnz, (uint32_t)total_k, todo_cnt);
-    else
-      topk_guess_kernel<kSampleMax / kGuessThreads><<<nsegs, kGuessThreads, 0, s>>>(
-          grad, residual, g, guess, seg_cnt, seg_flag, out_nnz, (uint32_t)total_k, todo_cnt);
-  }
-  if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
-  mark(1);
-  topk_stream_kernel<<<(unsigned)((uint64_t)P * g.nchunk), kStreamThreads, 0, s>>>(
-      grad, residual, g, guess, seg_cnt, seg_flag, chunk_cnt, cand_idx, cand_val);
-  if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
-  mark(2);
-
-  // Cluster size: enough CTAs per segment to spread its chunks (<= 8).
-  uint32_t CS = 1;
-  while (CS < 8 && (uint64_t)g.m / (CS * 2) >= 64) CS *= 2;
-  SelectArgs a{CS, CS == 1 ? 1u : 0u, CS > 1 ? 1u : 0u, todo, todo_cnt, residual, seg_cnt,
-               seg_flag, chunk_cnt, guess, cand_idx, cand_val, out_idx, out_val, status, g};
-  if (CS == 1) {  // layer-sized segments: one CTA each
-    topk_select_short_kernel<<<nsegs, kSegThreads, 0, s>>>(a);
-    if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
-  } else {  // long segments: grid-wide passes
-    LongArgs la{g, seg_cnt, seg_flag, chunk_cnt, cand_idx, cand_val, residual, out_idx, out_val,
-                status, reinterpret_cast<uint32_t*>(w + l.lhist),
-                reinterpret_cast<uint32_t*>(w + l.lsel),
-                reinterpret_cast<uint32_t*>(w + l.lrange), l.nr};
-    if (cudaMemsetAsync(la.hist, 0, 4 * (size_t)nsegs * kHistWords, s) != cudaSuccess)
-      return SPARCML_ERR_CUDA;
-    const unsigned ranges = nsegs * l.nr;
-    for (int d = 0; d < 3; ++d) {
-      long_hist_kernel<<<ranges, kSelectThreads, 0, s>>>(la, d);
-      long_find_kernel<<<nsegs, kSelectThreads, 0, s>>>(la, d);
-    }
-    long_count_kernel<<<ranges, kSelectThreads, 0, s>>>(la);
-    long_scan_kernel<<<nsegs, 1024, 0, s>>>(la);
-    long_write_kernel<<<ranges, kSelectThreads, 0, s>>>(la);
-    if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
-  }
-  // CS == 1: a small grid walks the segments the short kernel handed over.
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(CS == 1 ? std::min<unsigned>(nsegs, 2 * 152)
-                             : (unsigned)((uint64_t)P * g.nseg * CS), 1, 1);
-  cfg.blockDim = dim3(kSelectThreads, 1, 1);
-  cfg.dynamicSmemBytes = 2 * kSmallCands * sizeof(uint32_t);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CS;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (!ensure_smem(reinterpret_cast<const void*>(topk_select_kernel), cfg.dynamicSmemBytes))
-    return SPARCML_ERR_CUDA;
-  if (CS == 1) {
-    topk_select_kernel<<<cfg.gridDim, cfg.blockDim, cfg.dynamicSmemBytes, s>>>(a);
-    if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
-  } else if (cudaLaunchKernelEx(&cfg, topk_select_kernel, a) != cudaSuccess) {
-    return SPARCML_ERR_CUDA;
-  }
-  mark(3);
-  note_launches(CS == 1 ? 4 : 3 + 9);
-  return SPARCML_OK;
+  return topk_call(grad, residual, P, N, seg_begin, seg_k, nseg, out_idx, out_val, out_nnz, cap,
+                   ws, ws_bytes, stream, events);
 }
 
 extern "C" int sparcml_topk_ef(const float* grad, float* residual, int32_t P, uint64_t N,
-                               uint64_t seg_len, uint32_t k_num, uint32_t k_den,
-                               uint32_t* out_idx, float* out_val, uint32_t* out_nnz,
-                               uint64_t cap, void* ws, size_t ws_bytes, void* stream) {
-  return sparcml_topk_ef_traced(grad, residual, P, N, seg_len, k_num, k_den, out_idx, out_val,
-                                out_nnz, cap, ws, ws_bytes, stream, nullptr);
+                               const uint64_t* seg_begin, const uint32_t* seg_k, uint32_t nseg,
+                               uint32_t* out_idx, float* out_val, uint32_t* out_nnz, uint64_t cap,
+                               void* ws, size_t ws_bytes, void* stream) {
+  return topk_call(grad, residual, P, N, seg_begin, seg_k, nseg, out_idx, out_val, out_nnz, cap,
+                   ws, ws_bytes, stream, nullptr);
+}
+
+extern "C" size_t sparcml_topk_ef_uniform_workspace_size(int32_t P, uint64_t N, uint64_t seg_len,
+                                                         uint32_t k_num, uint32_t k_den) {
+  std::vector<uint64_t> b;
+  std::vector<uint32_t> k;
+  if (!uniform_table(N, seg_len, k_num, k_den, &b, &k) || k.size() > 0xffffffffull) return 0;
+  return sparcml_topk_ef_workspace_size(P, N, b.data(), k.data(), (uint32_t)k.size());
+}
+
+extern "C" int sparcml_topk_ef_uniform_traced(const float* grad, float* residual, int32_t P,
+                                              uint64_t N, uint64_t seg_len, uint32_t k_num,
+                                              uint32_t k_den, uint32_t* out_idx, float* out_val,
+                                              uint32_t* out_nnz, uint64_t cap, void* ws,
+                                              size_t ws_bytes, void* stream,
+                                              void* const* events) {
+  std::vector<uint64_t> b;
+  std::vector<uint32_t> k;
+  if (!uniform_table(N, seg_len, k_num, k_den, &b, &k) || k.size() > 0xffffffffull)
+    return SPARCML_ERR_INVALID_ARG;
+  return topk_call(grad, residual, P, N, b.data(), k.data(), (uint32_t)k.size(), out_idx,
+                   out_val, out_nnz, cap, ws, ws_bytes, stream, events);
+}
+
+extern "C" int sparcml_topk_ef_uniform(const float* grad, float* residual, int32_t P, uint64_t N,
+                                       uint64_t seg_len, uint32_t k_num, uint32_t k_den,
+                                       uint32_t* out_idx, float* out_val, uint32_t* out_nnz,
+                                       uint64_t cap, void* ws, size_t ws_bytes, void* stream) {
+  return sparcml_topk_ef_uniform_traced(grad, residual, P, N, seg_len, k_num, k_den, out_idx,
+                                        out_val, out_nnz, cap, ws, ws_bytes, stream, nullptr);
+}
+
+extern "C" int64_t sparcml_topk_ef_fallbacks(const void* ws, void* stream) {
+  if (!ws) return -1;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return -1;
+  uint32_t h = 0;
+  if (cudaMemcpy(&h, static_cast<const char*>(ws) + kFallbackOffset, sizeof h,
+                 cudaMemcpyDeviceToHost) != cudaSuccess)
+    return -1;
+  return h;
 }
