@@ -65,7 +65,9 @@ constexpr uint32_t kSub = kChunk / kWarpsPerChunk;  // entries per warp sub-chun
 constexpr uint32_t kRounds = kSub / (32 * 4);       // float4 rounds per warp
 constexpr uint32_t kExactMax = 8192;      // segments sampled whole
 constexpr uint32_t kLayerMax = 1u << 18;  // layer-sized: warp guess, one-CTA select
-constexpr uint32_t kSampleLong = 8192;    // sample of a long segment
+constexpr uint32_t kSampleLong = 8192;    // sample of one guess CTA
+constexpr uint32_t kGuessCluster = 8;     // guess CTAs of a long segment (a cluster)
+constexpr uint32_t kLongSample = kSampleLong * kGuessCluster;  // sample of a long segment
 constexpr uint32_t kWarpSample = 2048;    // sample of a layer-sized segment
 constexpr uint32_t kRun = 256;            // consecutive entries per sample run
 constexpr uint32_t kGuessThreads = 256;
@@ -255,8 +257,11 @@ __global__ void __launch_bounds__(256) topk_init_kernel(Args a) {
 // ---------------------------------------------------------------------------
 // Largest G on the 2^15 grid with at least r of the block's keys >= G (the
 // r-th largest key with its low 15 bits cleared), keys held KPT per thread.
+// Over a cluster of CS CTAs (CS = 1: the block alone), the counts of each
+// step summed through distributed shared memory.
 template <uint32_t KPT>
-__device__ uint32_t block_rank_key(const uint32_t (&key)[KPT], uint32_t r, uint32_t (*wsum)[8]) {
+__device__ uint32_t block_rank_key(const uint32_t (&key)[KPT], uint32_t r, uint32_t (*wsum)[8],
+                                   cg::cluster_group& cluster, uint32_t CS) {
   constexpr uint32_t kWarps = kGuessThreads / 32;
   const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
   uint32_t G = 0;
@@ -269,12 +274,22 @@ __device__ uint32_t block_rank_key(const uint32_t (&key)[KPT], uint32_t r, uint3
     c = warp_sum(c);
     uint32_t* ws = wsum[bit & 1];  // double-buffered: one barrier per bit
     if (lane == 0) ws[warp] = c;
-    __syncthreads();
     uint32_t tot = 0;
+    if (CS == 1) {
+      __syncthreads();
 #pragma unroll
-    for (uint32_t w = 0; w < kWarps; ++w) tot += ws[w];
+      for (uint32_t w = 0; w < kWarps; ++w) tot += ws[w];
+    } else {
+      cluster.sync();  // every CTA's counts of this bit are in
+      for (uint32_t q = 0; q < CS; ++q) {
+        const uint32_t* rw = cluster.map_shared_rank(ws, q);
+#pragma unroll
+        for (uint32_t w = 0; w < kWarps; ++w) tot += rw[w];
+      }
+    }
     if (tot >= r) G = trial;
   }
+  if (CS > 1) cluster.sync();  // no CTA leaves while its counts may still be read
   return G;
 }
 
@@ -291,8 +306,11 @@ __device__ __forceinline__ uint32_t hist_shift(uint32_t G, uint32_t anchor) {
 // segment, r = k. Long: 32 runs of kRun consecutive entries spread evenly.
 constexpr uint32_t kGuessKPT = kSampleLong / kGuessThreads;  // 32
 
+// Segments sampled whole (the exact kind): one CTA per (node, segment).
 __global__ void __launch_bounds__(kGuessThreads) topk_guess_cta_kernel(Args a, uint32_t nlist) {
   __shared__ uint32_t wsum[2][8];
+  cg::cluster_group cluster = cg::this_cluster();
+  const uint32_t CS = 1, rank = 0;
   const uint32_t p = blockIdx.x / nlist, s = a.cta_list[blockIdx.x % nlist];
   const SegRec r = a.recs[s];
   const uint32_t t = threadIdx.x, lane = lane_id(), warp = t >> 5;
@@ -309,10 +327,12 @@ __global__ void __launch_bounds__(kGuessThreads) topk_guess_cta_kernel(Args a, u
       ok[q] = pos[q] < r.n;
     }
   } else {
-    constexpr uint32_t nruns = kSampleLong / kRun, kLinesPerRun = kRun / 32;
+    constexpr uint32_t kLinesPerRun = kRun / 32;
+    const uint32_t nruns = (kSampleLong / kRun) * CS;
 #pragma unroll
     for (uint32_t q = 0; q < kGuessKPT; q += kLinesPerRun) {
-      const uint32_t run = warp * (kGuessKPT / kLinesPerRun) + q / kLinesPerRun;
+      const uint32_t run =
+          rank * (kSampleLong / kRun) + warp * (kGuessKPT / kLinesPerRun) + q / kLinesPerRun;
       const uint32_t st =
           (uint32_t)(((uint64_t)run * (r.n - kRun) / (nruns - 1)) & ~(uint64_t)(kRun - 1));
 #pragma unroll
@@ -331,10 +351,114 @@ __global__ void __launch_bounds__(kGuessThreads) topk_guess_cta_kernel(Args a, u
   uint32_t key[kGuessKPT];
 #pragma unroll
   for (uint32_t q = 0; q < kGuessKPT; ++q) key[q] = ok[q] ? mag_key(__fadd_rn(ra[q], ga[q])) : kNone;
-  const uint32_t G = block_rank_key<kGuessKPT>(key, exact ? r.k : (r.rank & 0xffffu), wsum);
+  const uint32_t G =
+      block_rank_key<kGuessKPT>(key, exact ? r.k : (r.rank & 0xffffu), wsum, cluster, CS);
   uint32_t shift = 0;
-  if (!exact) shift = hist_shift(G, block_rank_key<kGuessKPT>(key, r.rank >> 16, wsum));
-  if (t == 0) a.guess[(uint64_t)p * a.nseg + s] = make_uint2(G, shift);
+  if (!exact) shift = hist_shift(G, block_rank_key<kGuessKPT>(key, r.rank >> 16, wsum, cluster, CS));
+  if (t == 0 && rank == 0) a.guess[(uint64_t)p * a.nseg + s] = make_uint2(G, shift);
+}
+
+// Long segments: a cluster of CS CTAs per (node, segment), each sampling its
+// own 32 runs of kRun entries (CS * 8,192 sample keys in all). G is the r-th
+// largest sample key with its low 15 bits cleared, found as two radix digits
+// (bits 30..20, then 19..15) from histograms summed over the cluster through
+// distributed shared memory; the histogram anchor likewise with its rank.
+__device__ __forceinline__ void warp_find_from_top32(const uint32_t* tot, uint32_t r,
+                                                     uint32_t* bin) {
+  // lanes hold bins 31 - lane (high to low); the bin where the count from the top reaches r
+  const uint32_t lane = lane_id();
+  const uint32_t v = tot[31 - lane];
+  const uint32_t incl = warp_incl_sum(v);
+  const uint32_t hit = __ballot_sync(0xffffffffu, incl >= r && incl - v < r);
+  if (lane == 0) *bin = hit ? 31 - (__ffs(hit) - 1) : 0;
+}
+
+__global__ void __launch_bounds__(kGuessThreads) topk_guess_long_kernel(Args a) {
+  __shared__ uint32_t h1[2048];
+  __shared__ uint32_t tot[2048];
+  __shared__ uint32_t h2[2][32];
+  __shared__ uint32_t t2[2][32];
+  __shared__ uint32_t scratch[34];
+  __shared__ uint32_t res[2];
+  __shared__ uint32_t pick[4];  // digit-1 bins of G and of the anchor, their ranks left
+  __shared__ uint32_t pick2[2];
+  cg::cluster_group cluster = cg::this_cluster();
+  const uint32_t CS = cluster.num_blocks(), rank = cluster.block_rank();
+  const uint32_t item = blockIdx.x / CS;
+  const uint32_t p = item / a.nlong, s = a.long_list[item % a.nlong];
+  const SegRec r = a.recs[s];
+  const uint32_t t = threadIdx.x, lane = lane_id(), warp = t >> 5;
+  for (uint32_t b = t; b < 2048; b += blockDim.x) h1[b] = 0;
+  if (t < 64) (&h2[0][0])[t] = 0;
+  const uint64_t base = (uint64_t)p * a.N + r.begin;
+  const float* gp = a.grad + base;
+  const float* rp = a.residual + base;
+  constexpr uint32_t kLinesPerRun = kRun / 32;
+  const uint32_t nruns = (kSampleLong / kRun) * CS;
+  uint32_t key[kGuessKPT];
+  {
+    float ra[kGuessKPT], ga[kGuessKPT];
+#pragma unroll
+    for (uint32_t q = 0; q < kGuessKPT; q += kLinesPerRun) {
+      const uint32_t run =
+          rank * (kSampleLong / kRun) + warp * (kGuessKPT / kLinesPerRun) + q / kLinesPerRun;
+      const uint32_t st =
+          (uint32_t)(((uint64_t)run * (r.n - kRun) / (nruns - 1)) & ~(uint64_t)(kRun - 1));
+#pragma unroll
+      for (uint32_t l = 0; l < kLinesPerRun; ++l) {
+        ra[q + l] = rp[st + l * 32 + lane];
+        ga[q + l] = gp[st + l * 32 + lane];
+      }
+    }
+#pragma unroll
+    for (uint32_t q = 0; q < kGuessKPT; ++q) key[q] = mag_key(__fadd_rn(ra[q], ga[q]));
+  }
+  __syncthreads();
+#pragma unroll
+  for (uint32_t q = 0; q < kGuessKPT; ++q) atomicAdd(&h1[key[q] >> 20], 1u);
+  __syncthreads();
+  cluster.sync();  // every CTA's digit-1 histogram is in
+  for (uint32_t b = t; b < 2048; b += blockDim.x) {
+    uint32_t sum = 0;
+    for (uint32_t q = 0; q < CS; ++q) sum += cluster.map_shared_rank(h1, q)[b];
+    tot[b] = sum;
+  }
+  __syncthreads();
+  const uint32_t rG = r.rank & 0xffffu, rA = r.rank >> 16;
+  find_from_top(tot, 2048, rG, scratch, res);
+  if (t == 0) {
+    pick[0] = res[0] == kNone ? 0u : res[0];
+    pick[1] = res[0] == kNone ? 1u : rG - res[1];
+  }
+  __syncthreads();
+  find_from_top(tot, 2048, rA, scratch, res);
+  if (t == 0) {
+    pick[2] = res[0] == kNone ? 0u : res[0];
+    pick[3] = res[0] == kNone ? 1u : rA - res[1];
+  }
+  __syncthreads();
+#pragma unroll
+  for (uint32_t q = 0; q < kGuessKPT; ++q) {
+    if ((key[q] >> 20) == pick[0]) atomicAdd(&h2[0][(key[q] >> 15) & 31u], 1u);
+    if ((key[q] >> 20) == pick[2]) atomicAdd(&h2[1][(key[q] >> 15) & 31u], 1u);
+  }
+  __syncthreads();
+  cluster.sync();  // every CTA's digit-2 histograms are in
+  if (t < 64) {
+    uint32_t sum = 0;
+    for (uint32_t q = 0; q < CS; ++q) sum += cluster.map_shared_rank(&h2[0][0], q)[t];
+    (&t2[0][0])[t] = sum;
+  }
+  __syncthreads();
+  if (warp == 0) warp_find_from_top32(t2[0], pick[1], &pick2[0]);
+  if (warp == 1) warp_find_from_top32(t2[1], pick[3], &pick2[1]);
+  __syncthreads();
+  cluster.sync();  // no CTA leaves while its histograms may still be read
+  if (t == 0 && rank == 0) {
+    const uint32_t G = (pick[0] << 20) | (pick2[0] << 15);
+    const uint32_t anchor = (pick[2] << 20) | (pick2[1] << 15);
+    a.guess[(uint64_t)p * a.nseg + s] = make_uint2(G, hist_shift(G, anchor));
+  }
 }
 
 // Layer-sized segments: one warp per (node, segment), no block barrier. The
@@ -501,6 +625,11 @@ __global__ void __launch_bounds__(kStreamThreads, 2) topk_stream_kernel(Args a) 
   }
   const uint64_t sub = (uint64_t)gc * kWarpsPerChunk + warp;
   const uint64_t slot0 = (uint64_t)p * a.node_slots + (uint64_t)slot32 * 32 + (uint64_t)warp * slot;
+  // Long segments keep more than half of their candidates: the stream pass
+  // writes +0.0f for every candidate it stores, and the select restores acc at
+  // the candidates that are not kept (fewer scattered writes than zeroing the
+  // kept ones afterwards).
+  const bool long_seg = kind == kLong;
   uint32_t run = 0;  // candidates so far in this sub-chunk (warp-uniform)
 #pragma unroll
   for (uint32_t t = 0; t < kRounds; ++t) {
@@ -511,33 +640,43 @@ __global__ void __launch_bounds__(kStreamThreads, 2) topk_stream_kernel(Args a) 
     acc.z = __fadd_rn(rv[t].z, gv[t].z);
     acc.w = __fadd_rn(rv[t].w, gv[t].w);
     const float av[4] = {acc.x, acc.y, acc.z, acc.w};
-    uint32_t bits = 0;
-    if (a.vec && e0 >= lo_r && e0 + 4 <= hi_r) {
-      *reinterpret_cast<float4*>(rp + e0) = acc;
+    const bool full = a.vec && e0 >= lo_r && e0 + 4 <= hi_r;
+    uint32_t in = 0xfu;  // entries of the quad inside the segment
+    if (!full) {
+      in = 0;
 #pragma unroll
-      for (uint32_t q = 0; q < 4; ++q) bits |= (mag_key(av[q]) >= G ? 1u : 0u) << q;
-    } else {
+      for (int32_t q = 0; q < 4; ++q) in |= (e0 + q >= lo_r && e0 + q < hi_r ? 1u : 0u) << q;
+    }
+    uint32_t bits = 0;  // candidates: key >= G
 #pragma unroll
-      for (int32_t q = 0; q < 4; ++q)
-        if (e0 + q >= lo_r && e0 + q < hi_r) {
-          rp[e0 + q] = av[q];
-          bits |= (mag_key(av[q]) >= G ? 1u : 0u) << q;
+    for (uint32_t q = 0; q < 4; ++q) bits |= ((in >> q) & (mag_key(av[q]) >= G ? 1u : 0u)) << q;
+    uint32_t zero = 0;  // long segments: candidates kept in the sub-slot get +0.0f
+    if (__ballot_sync(0xffffffffu, bits) != 0) {  // warp-uniform
+      uint32_t tot;
+      uint32_t pos = run + warp_excl_small(__popc(bits), &tot);
+      run += tot;
+#pragma unroll
+      for (uint32_t q = 0; q < 4; ++q)
+        if (bits & (1u << q)) {
+          if (pos < slot) {
+            const uint64_t keep = l2_policy_evict_last();
+            st_keep(a.cand_idx + slot0 + pos, base_u + (uint32_t)e0 + q, keep);
+            st_keep(a.cand_val + slot0 + pos, av[q], keep);
+            zero |= long_seg ? 1u << q : 0u;
+          }
+          ++pos;
         }
     }
-    if (__ballot_sync(0xffffffffu, bits) == 0) continue;  // warp-uniform
-    uint32_t tot;
-    uint32_t pos = run + warp_excl_small(__popc(bits), &tot);
-    run += tot;
+    const float4 w = make_float4(zero & 1u ? 0.0f : acc.x, zero & 2u ? 0.0f : acc.y,
+                                 zero & 4u ? 0.0f : acc.z, zero & 8u ? 0.0f : acc.w);
+    if (full) {
+      *reinterpret_cast<float4*>(rp + e0) = w;
+    } else {
+      const float wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (uint32_t q = 0; q < 4; ++q)
-      if (bits & (1u << q)) {
-        if (pos < slot) {
-          const uint64_t keep = l2_policy_evict_last();
-          st_keep(a.cand_idx + slot0 + pos, base_u + (uint32_t)e0 + q, keep);
-          st_keep(a.cand_val + slot0 + pos, av[q], keep);
-        }
-        ++pos;
-      }
+      for (int32_t q = 0; q < 4; ++q)
+        if (in & (1u << q)) rp[e0 + q] = wv[q];
+    }
   }
   // Pad the sub-slot's last 32-byte sector: every sector of candidates is
   // written whole, so no later eviction from L2 leaves a half-written sector.
@@ -1081,31 +1220,52 @@ __global__ void __launch_bounds__(256) long_write_kernel(Args a) {
   const uint64_t out0 = (uint64_t)v.p * a.cap + v.rec.out0;
   float* rp = a.residual + (uint64_t)v.p * a.N;
   const uint64_t keep = l2_policy_evict_last();
-  auto emit = [&](bool k_, uint32_t idx, float val) {
+  // kept: to the stream (its residual is already +0.0f); a candidate that is
+  // not kept gets its acc back in the residual
+  auto emit = [&](bool valid, bool k_, uint32_t idx, float val) {
     const uint32_t m = __ballot_sync(0xffffffffu, k_);
     if (k_) {
       const uint32_t o = pos + __popc(m & lanemask_lt());
       if (o < v.rec.k) {
         st_keep(a.out_idx + out0 + o, idx, keep);
         st_keep(a.out_val + out0 + o, val, keep);
-        rp[idx] = 0.0f;
       } else {
         set_status(a.status, SPARCML_ERR_BAD_STREAM);
       }
+    } else if (valid) {
+      rp[idx] = val;
     }
     pos += __popc(m);
   };
   uint32_t iv[kHold];
 #pragma unroll
-  for (uint32_t u = 0; u < kHold; ++u) iv[u] = (kb >> u) & 1u ? ci[so[u]] : 0u;
+  for (uint32_t u = 0; u < kHold; ++u) iv[u] = u * 32 + lane < v.count ? ci[so[u]] : 0u;
 #pragma unroll
-  for (uint32_t u = 0; u < kHold; ++u) emit((kb >> u) & 1u, iv[u], xv[u]);
+  for (uint32_t u = 0; u < kHold; ++u) emit(u * 32 + lane < v.count, (kb >> u) & 1u, iv[u], xv[u]);
   for (uint32_t x0 = 32 * kHold; x0 < v.count; x0 += 32) {
     const uint32_t x = x0 + lane;
     const uint32_t o = range_off(v, min(x, v.count - 1));
     const float val = x < v.count ? cv[o] : 0.0f;
     const bool k_ = kept(val, o, x < v.count);
-    emit(k_, k_ ? ci[o] : 0u, val);
+    emit(x < v.count, k_, x < v.count ? ci[o] : 0u, val);
+  }
+}
+
+// Before the raw select re-reads a long segment that fell back: every
+// candidate the stream pass stored (and zeroed in the residual) gets its acc
+// back, so the residual holds acc over the whole segment again.
+__global__ void __launch_bounds__(256) long_restore_kernel(Args a) {
+  RangeView v;
+  range_view(a, &v);
+  if (a.lsel[v.pl].mode != kModeFallback) return;  // CTA-uniform
+  const uint32_t lane = lane_id();
+  const float* cv = a.cand_val + v.slot_base;
+  const uint32_t* ci = a.cand_idx + v.slot_base;
+  float* rp = a.residual + (uint64_t)v.p * a.N;
+  for (uint32_t x0 = 0; x0 < v.count; x0 += 32) {
+    const uint32_t x = x0 + lane;
+    const uint32_t o = range_off(v, min(x, v.count - 1));
+    if (x < v.count) rp[ci[o]] = cv[o];
   }
 }
 
@@ -1343,14 +1503,17 @@ int make_plan(int32_t P, uint64_t N, const uint64_t* seg_begin, const uint32_t* 
       warp.push_back(s);
       shrt.push_back(s);
     } else if (r.kind == kLong) {
-      r.rank = sample_rank(r.k, r.n, kSampleLong) | (anchor_rank(r.k, r.n, kSampleLong) << 16);
+      // both ranks in 16 bits: a rank of the whole sample becomes the one below
+      // it (a guess slightly higher; too few candidates send the segment to the
+      // raw select)
+      r.rank = std::min<uint32_t>(sample_rank(r.k, r.n, kLongSample), 0xffffu) |
+               (std::min<uint32_t>(anchor_rank(r.k, r.n, kLongSample), 0xffffu) << 16);
       r.lidx = (uint32_t)lng.size();
       r.range0 = (uint32_t)rmap.size();
       const uint32_t nr = (r.nchunk * kWarpsPerChunk + kRangeSubs - 1) / kRangeSubs;
       if (nr > kMaxRanges || r.lidx > 0xffffu) return SPARCML_ERR_INVALID_ARG;
       for (uint32_t i = 0; i < nr; ++i) rmap.push_back((r.lidx << 16) | i);
       lng.push_back(s);
-      cta.push_back(s);
     }
   }
   if (chunks > 0xffffffffull || (uint64_t)P * chunks > 0x7fffffffull ||
@@ -1486,7 +1649,24 @@ int launch_topk(const Plan& q, const float* grad, float* residual, uint32_t* out
     ++launches;
   }
   if (q.n_cta) {
-    topk_guess_cta_kernel<<<(unsigned)((uint64_t)q.P * q.n_cta), kGuessThreads, 0, s>>>(a, q.n_cta);
+    topk_guess_cta_kernel<<<(unsigned)((uint64_t)q.P * q.n_cta), kGuessThreads, 0, s>>>(
+        a, q.n_cta);
+    ++launches;
+  }
+  if (q.nlong) {  // a cluster of kGuessCluster CTAs per (node, long segment)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((uint64_t)q.P * q.nlong * kGuessCluster), 1, 1);
+    cfg.blockDim = dim3(kGuessThreads, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kGuessCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, topk_guess_long_kernel, a) != cudaSuccess)
+      return SPARCML_ERR_CUDA;
     ++launches;
   }
   if (q.n_warp) {
@@ -1525,7 +1705,8 @@ int launch_topk(const Plan& q, const float* grad, float* residual, uint32_t* out
       return SPARCML_ERR_CUDA;
     long_exact_kernel<<<pl, kExactThreads, smem, s>>>(a);
     long_write_kernel<<<pr, 256, 0, s>>>(a);
-    launches += 5;
+    long_restore_kernel<<<pr, 256, 0, s>>>(a);
+    launches += 6;
     if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(pl * kRawCluster, 1, 1);
