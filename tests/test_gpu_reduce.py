@@ -398,3 +398,34 @@ def test_reduce_hot_head_tiles_with_4bit_values():
     else:
         assert np.array_equal(u32(out.idx[:U]), ref["idx"])
         assert np.array_equal(bits(out.val[:U].cpu().numpy()), bits(ref["val"]))
+
+
+def test_reduce_skewed_head_every_warp_tile_path():
+    """A Zipf head puts about a thousand entries per node into each of the first
+    1,024-index tiles: those tiles are spread over a CTA (dense-first warp-tile
+    mode) in every variant, fp32 quads, unaligned fp32, the fused 4-bit decode
+    and max, and the result stays bit-exact."""
+    from test_gpu_reduce_ops import check_op
+    P, N, k = 16, 1 << 20, 30_000
+    idx, val, nnz = W.zipf_streams(P, N, k, 1.1, 1.0, 99)
+    check_reduce(idx, val, nnz, N, repeat=2)  # 16-byte quads
+    wide = k + 1  # rows no longer 16-byte aligned: the scalar warp tiles
+    i2 = np.zeros((P, wide), np.uint32)
+    v2 = np.zeros((P, wide), np.float32)
+    i2[:, :k], v2[:, :k] = idx, val
+    check_reduce(i2, v2, nnz, N, repeat=2)
+    check_op(idx, val, nnz, N, "max")
+    bucket, seed = 512, 1234
+    di, dv, dn = streams_to_dev(idx, val, nnz)
+    codes, scales = api.quantize4(di, dv, dn, bucket, seed)
+    oc, osc = oracle.quantize4(idx, val, nnz, bucket, seed)
+    assert np.array_equal(codes.cpu().numpy(), oc)
+    ref = oracle.sparse_reduce(idx, oracle.dequantize4(oc, osc, nnz, k, bucket), nnz, N)
+    out = api.sparse_reduce_q4(di, codes, scales, dn, bucket, N)
+    U = int(out.nnz.item())
+    assert U == ref["nnz"] and bool(out.is_dense.item()) == ref["is_dense"]
+    if ref["is_dense"]:
+        assert np.array_equal(bits(out.dense.cpu().numpy()), bits(ref["dense"]))
+    else:
+        assert np.array_equal(u32(out.idx[:U]), ref["idx"])
+        assert np.array_equal(bits(out.val[:U].cpu().numpy()), bits(ref["val"]))

@@ -84,6 +84,9 @@ struct ReduceArgs {
   const uint32_t* split;  // [(ntiles + 1) * P] node sub-range starts per tile
   uint32_t* tile_bm;      // dense-first mode: [ntiles][kWords] presence bits per tile
   uint32_t* u_total;      // warp-tile mode: union size, summed by atomics
+  uint32_t hot_thr;       // dense-first warp tiles with more entries go to the hot kernel
+  uint32_t* hot_cnt;      // dense-first warp tiles: tiles left to reduce_hot_tile_kernel
+  uint32_t* hot;          // [ntiles] their ids
   int32_t* status;
   const uint32_t* inject;  // the workspace's fault-injection word (or nullptr)
 };
@@ -619,6 +622,14 @@ constexpr uint32_t kMiniWords = kMini / 32;
 constexpr uint32_t kMiniRounds = 8;
 constexpr int32_t kMiniMaxP = 64;
 constexpr uint32_t kMiniWarps = 4;  // mini-tiles per CTA
+// Dense-first warp tiles with more entries than max(kHot, kHotRatio x the
+// average tile) (a skewed, Zipf-like head) are left to reduce_hot_tile_kernel,
+// which spreads one over a CTA.
+constexpr uint32_t kHot = 1024;
+constexpr uint32_t kHotRatio = 2;
+constexpr uint32_t kHotThreads = 512;
+constexpr uint32_t kHotAhead = 8;  // nodes whose loads are in flight at once
+constexpr uint64_t kHotGrid = 4 * 152;  // CTAs of the hot launch: the GPU's 152 SMs, 4 each
 // per-warp region, a multiple of 16 bytes: acc is accessed as uint4
 constexpr uint32_t kAccWords = kMini;
 constexpr uint32_t kMiniWarpWords = (kAccWords + 3 * kMiniMaxP + 1 + 31) / 32 * 32;
@@ -955,55 +966,21 @@ __device__ __forceinline__ uint32_t mini_tile_of_warp(const ReduceArgs& a, bool 
   return m;
 }
 
-template <bool Q4, bool LB, bool ANY>
-__global__ void __launch_bounds__(kMiniWarps * 32)
-reduce_mini_kernel(ReduceArgs a) {
-  extern __shared__ __align__(16) uint32_t dyn[];
-  const int32_t kop = ANY ? a.op : kOpSum;  // sum-only launches fold the branch away
-  const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
-  __shared__ uint32_t sh[kMiniWarps + 1];
-  const uint32_t m = mini_tile_of_warp(a, LB, sh);
-  if constexpr (!LB) {
-    if (m >= a.ntiles) return;  // warp-uniform
-  }
-  const bool active = m < a.ntiles;
-  uint32_t* acc = dyn + warp * kMiniWarpWords;        // [kMini] float bits
-  uint32_t* lo = acc + kAccWords;                      // [P] first entry in the tile
-  uint32_t* cpre = lo + kMiniMaxP;                     // [P + 1] first position
-  const uint32_t tile_lo = m * kMini;
-  const uint32_t tile_n = min(kMini, a.N - tile_lo);
-  const float e = op_neutral(kop);
-  // Absent indices hold kAbsent, a NaN that neither the sum (the GPU's NaN
-  // results are 0x7fffffff) nor max/min (a NaN value never replaces the
-  // partial result) ever leaves there: presence needs no bitmap. Bitwise or
-  // can produce any pattern and is not run here.
-#pragma unroll
-  for (uint32_t i = 0; i < kMini / 128; ++i)
-    reinterpret_cast<uint4*>(acc)[i * 32 + lane] = make_uint4(kAbsent, kAbsent, kAbsent, kAbsent);
-  uint32_t c[2] = {0, 0};
-#pragma unroll
-  for (uint32_t q = 0; q < 2; ++q) {
-    const int32_t p = (int32_t)(lane + 32 * q);
-    if (active && p < a.P) {  // a tile past the end (last CTA group) has no entries
-      const uint32_t n = (uint32_t)min((uint64_t)a.nnz[p], a.cap);
-      const uint32_t l = min(a.split[(uint64_t)m * a.P + p], n);
-      const uint32_t h = min(a.split[(uint64_t)(m + 1) * a.P + p], n);
-      lo[p] = l;
-      c[q] = h > l ? h - l : 0u;
-    }
-  }
-  {
-    const uint32_t i0 = warp_incl_sum(c[0]), t0 = __shfl_sync(0xffffffffu, i0, 31);
-    const uint32_t i1 = warp_incl_sum(c[1]);
-    if (lane < (uint32_t)a.P) cpre[lane] = i0 - c[0];
-    if (lane + 32 < (uint32_t)a.P) cpre[lane + 32] = t0 + i1 - c[1];
-    if (lane == 31) cpre[a.P] = t0 + i1;
-  }
-  __syncwarp();
-  const uint32_t total = cpre[a.P];
-  // Each lane walks its positions x = lane, lane + 32, ...: it finds its node
-  // again only when x leaves the current node's range, and otherwise steps its
-  // entry pointers by 32.
+// The entries of one node-major run of positions [0, total) into a warp's
+// accumulator (absent = kAbsent): position x is entry lo[p] + (x - cpre[p]) of
+// node p, cpre being the nodes' exclusive prefix. Each lane walks its
+// positions x = lane, lane + 32, ...: it finds its node again only when x
+// leaves the current node's range, and otherwise steps its entry pointers by
+// 32. kMiniRounds rounds of loads are in flight at once. A round is applied
+// at once when its indices are distinct (one node, or no index shared by two
+// nodes); otherwise its nodes are applied one at a time, in order, so every
+// index sees its nodes in ascending order.
+template <bool Q4>
+__device__ __forceinline__ void mini_accumulate(const ReduceArgs& a, int32_t kop, uint32_t* acc,
+                                                uint32_t tile_lo, uint32_t tile_n,
+                                                const uint32_t* lo, const uint32_t* cpre,
+                                                uint32_t total, float e) {
+  const uint32_t lane = lane_id();
   uint32_t x = lane, p = 0, pend = 0, j = 0;
   const uint32_t* ip = a.idx;
   const float* vp = a.val;
@@ -1060,6 +1037,61 @@ reduce_mini_kernel(ReduceArgs a) {
       __syncwarp();
     }
   }
+}
+
+template <bool Q4, bool LB, bool ANY>
+__global__ void __launch_bounds__(kMiniWarps * 32)
+reduce_mini_kernel(ReduceArgs a) {
+  extern __shared__ __align__(16) uint32_t dyn[];
+  const int32_t kop = ANY ? a.op : kOpSum;  // sum-only launches fold the branch away
+  const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+  __shared__ uint32_t sh[kMiniWarps + 1];
+  const uint32_t m = mini_tile_of_warp(a, LB, sh);
+  if constexpr (!LB) {
+    if (m >= a.ntiles) return;  // warp-uniform
+  }
+  const bool active = m < a.ntiles;
+  uint32_t* acc = dyn + warp * kMiniWarpWords;        // [kMini] float bits
+  uint32_t* lo = acc + kAccWords;                      // [P] first entry in the tile
+  uint32_t* cpre = lo + kMiniMaxP;                     // [P + 1] first position
+  const uint32_t tile_lo = m * kMini;
+  const uint32_t tile_n = min(kMini, a.N - tile_lo);
+  const float e = op_neutral(kop);
+  // Absent indices hold kAbsent, a NaN that neither the sum (the GPU's NaN
+  // results are 0x7fffffff) nor max/min (a NaN value never replaces the
+  // partial result) ever leaves there: presence needs no bitmap. Bitwise or
+  // can produce any pattern and is not run here.
+#pragma unroll
+  for (uint32_t i = 0; i < kMini / 128; ++i)
+    reinterpret_cast<uint4*>(acc)[i * 32 + lane] = make_uint4(kAbsent, kAbsent, kAbsent, kAbsent);
+  uint32_t c[2] = {0, 0};
+#pragma unroll
+  for (uint32_t q = 0; q < 2; ++q) {
+    const int32_t p = (int32_t)(lane + 32 * q);
+    if (active && p < a.P) {  // a tile past the end (last CTA group) has no entries
+      const uint32_t n = (uint32_t)min((uint64_t)a.nnz[p], a.cap);
+      const uint32_t l = min(a.split[(uint64_t)m * a.P + p], n);
+      const uint32_t h = min(a.split[(uint64_t)(m + 1) * a.P + p], n);
+      lo[p] = l;
+      c[q] = h > l ? h - l : 0u;
+    }
+  }
+  {
+    const uint32_t i0 = warp_incl_sum(c[0]), t0 = __shfl_sync(0xffffffffu, i0, 31);
+    const uint32_t i1 = warp_incl_sum(c[1]);
+    if (lane < (uint32_t)a.P) cpre[lane] = i0 - c[0];
+    if (lane + 32 < (uint32_t)a.P) cpre[lane + 32] = t0 + i1 - c[1];
+    if (lane == 31) cpre[a.P] = t0 + i1;
+  }
+  __syncwarp();
+  const uint32_t total = cpre[a.P];
+  if constexpr (!LB) {
+    if (total > a.hot_thr) {  // warp-uniform: a Zipf-like head, for a whole CTA later
+      if (lane == 0) a.hot[atomicAdd(a.hot_cnt, 1u)] = m;
+      return;
+    }
+  }
+  mini_accumulate<Q4>(a, kop, acc, tile_lo, tile_n, lo, cpre, total, e);
   if constexpr (LB) mini_epilogue_lookback(a, m, acc, active, sh);
   else mini_epilogue(a, m, acc);
 }
@@ -1120,6 +1152,12 @@ reduce_mini_quad_kernel(ReduceArgs a) {
   }
   __syncwarp();
   const uint32_t total = qpre[a.P];
+  if constexpr (!LB) {
+    if (total > a.hot_thr / 4) {  // warp-uniform (quads): a Zipf-like head, for a CTA later
+      if (lane == 0) a.hot[atomicAdd(a.hot_cnt, 1u)] = m;
+      return;
+    }
+  }
   const uint64_t buf_end = (uint64_t)a.P * a.cap;  // entries in the buffer
   const uint4* idx4 = reinterpret_cast<const uint4*>(a.idx);
   const float4* val4 = reinterpret_cast<const float4*>(a.val);
@@ -1204,6 +1242,75 @@ reduce_mini_quad_kernel(ReduceArgs a) {
   else mini_epilogue(a, m, acc);
 }
 
+// A hot tile (dense-first mode, more entries than hot_thr: a skewed,
+// Zipf-like head): one CTA walks the nodes in ascending order. For node p the
+// CTA takes the node's run of the tile, at most kMini entries with distinct
+// indices, kMini / kHotThreads entries a thread, folds them into the shared
+// accumulator, and a barrier orders node p before node p + 1, so every index
+// is folded in node order. Loads run kHotAhead nodes ahead of the folds. Warp 0
+// then writes the tile's dense slice, bitmap and union count like any warp
+// tile. A CTA takes the hot tiles h, h + grid, ...
+template <bool Q4, bool ANY>
+__global__ void __launch_bounds__(kHotThreads)
+reduce_hot_tile_kernel(ReduceArgs a) {
+  constexpr uint32_t R = kMini / kHotThreads;  // entries of a node's run per thread
+  __shared__ __align__(16) uint32_t acc[kMini];
+  __shared__ uint32_t run_lo[kMiniMaxP], run_n[kMiniMaxP];
+  const uint32_t nhot = *a.hot_cnt;
+  const int32_t kop = ANY ? a.op : kOpSum;
+  const float e = op_neutral(kop);
+  const uint32_t t = threadIdx.x;
+  for (uint32_t h = blockIdx.x; h < nhot; h += gridDim.x) {  // CTA-uniform
+    const uint32_t m = a.hot[h];
+    const uint32_t tile_lo = m * kMini;
+    const uint32_t tile_n = min(kMini, a.N - tile_lo);
+    for (uint32_t i = t; i < kMini / 4; i += kHotThreads)
+      reinterpret_cast<uint4*>(acc)[i] = make_uint4(kAbsent, kAbsent, kAbsent, kAbsent);
+    if (t < (uint32_t)a.P) {
+      const uint32_t n = (uint32_t)min((uint64_t)a.nnz[t], a.cap);
+      const uint32_t l = min(a.split[(uint64_t)m * a.P + t], n);
+      const uint32_t hi = min(a.split[(uint64_t)(m + 1) * a.P + t], n);
+      run_lo[t] = l;
+      run_n[t] = hi > l ? hi - l : 0u;  // beyond kMini only for an invalid stream (flagged)
+    }
+    __syncthreads();
+    for (int32_t p0 = 0; p0 < a.P; p0 += kHotAhead) {
+      uint32_t ix[kHotAhead][R];
+      float vx[kHotAhead][R];
+#pragma unroll
+      for (uint32_t u = 0; u < kHotAhead; ++u) {
+        const int32_t p = p0 + (int32_t)u;
+#pragma unroll
+        for (uint32_t r = 0; r < R; ++r) {
+          ix[u][r] = ~0u;  // no entry: off is never below tile_n
+          vx[u][r] = 0.0f;
+          const uint32_t j = t + r * kHotThreads;
+          if (p < a.P && j < run_n[p]) {
+            const uint32_t jj = run_lo[p] + j;
+            ix[u][r] = ld_stream(a.idx + (uint64_t)p * a.cap + jj);
+            if constexpr (Q4) vx[u][r] = load_value<Q4>(a, (uint32_t)p, jj);
+            else vx[u][r] = ld_stream(a.val + (uint64_t)p * a.cap + jj);
+          }
+        }
+      }
+#pragma unroll
+      for (uint32_t u = 0; u < kHotAhead; ++u) {
+#pragma unroll
+        for (uint32_t r = 0; r < R; ++r) {
+          const uint32_t off = ix[u][r] - tile_lo;
+          if (ix[u][r] != ~0u && off < tile_n) {
+            const uint32_t old = acc[off];
+            acc[off] = __float_as_uint(op_fold(kop, old == kAbsent ? e : __uint_as_float(old), vx[u][r]));
+          }
+        }
+        __syncthreads();  // node p0 + u is folded in before node p0 + u + 1
+      }
+    }
+    if (t < 32) mini_epilogue(a, m, acc);
+    __syncthreads();  // warp 0 has read acc and run_* before the next tile
+  }
+}
+
 // Warp-tile mode, last pass: the union size U decides dense or sparse; a
 // sparse result is compacted from the dense slices and bitmaps, groups of 8
 // warp tiles per CTA taking their offsets by decoupled look-back.
@@ -1228,17 +1335,33 @@ reduce_mini_compact_kernel(ReduceArgs a) {
   const uint32_t ex = block_excl_scan(__popc(word), scratch, &tot);
   tile_lookback(a, g, tot, &bc[2]);
   __syncthreads();
-  uint32_t pos = bc[2] + ex;
-  uint32_t bits = word;
-  while (bits) {
-    const uint32_t b = __ffs(bits) - 1;
-    bits &= bits - 1;
-    const uint32_t i = (uint32_t)(wi * 32 + b);
-    if (pos < a.cap_sparse) {
-      a.out_idx[pos] = i;
-      a.out_val[pos] = a.out_dense[i];
+  // Each warp writes its 32 words, lane b taking bit b of a word: the dense
+  // slice is read in 128-byte rows and a word's entries go out side by side
+  // (a full word, the Zipf head, costs one round). Eight words' values are
+  // loaded before any of them is stored, so the loads overlap.
+  const uint32_t lane = lane_id();
+  const uint32_t pos0 = bc[2] + ex;
+  const uint64_t wbase = (uint64_t)g * kReduceThreads + (threadIdx.x & ~31u);
+  const uint32_t below = (1u << lane) - 1u;
+  for (uint32_t k0 = 0; k0 < 32; k0 += 8) {
+    uint32_t wk[8];
+    float v[8];
+#pragma unroll
+    for (uint32_t u = 0; u < 8; ++u) {
+      wk[u] = __shfl_sync(0xffffffffu, word, k0 + u);
+      v[u] = (wk[u] >> lane) & 1u ? a.out_dense[(wbase + k0 + u) * 32 + lane] : 0.0f;
     }
-    ++pos;
+#pragma unroll
+    for (uint32_t u = 0; u < 8; ++u) {
+      const uint32_t pk = __shfl_sync(0xffffffffu, pos0, k0 + u);
+      if ((wk[u] >> lane) & 1u) {
+        const uint32_t pos = pk + __popc(wk[u] & below);
+        if (pos < a.cap_sparse) {
+          a.out_idx[pos] = (uint32_t)((wbase + k0 + u) * 32 + lane);
+          a.out_val[pos] = v[u];
+        }
+      }
+    }
   }
 }
 
@@ -1522,7 +1645,7 @@ reduce_fixup_kernel(const int32_t* __restrict__ is_dense, const uint2* __restric
 inline unsigned fixup_grid(uint32_t ntiles) { return std::min<uint32_t>(ntiles, 1216u); }
 
 struct ReduceLayout {
-  size_t ticket, state, info, split, bm, total;
+  size_t ticket, state, info, split, bm, hot, total;
 };
 
 ReduceLayout reduce_layout(int32_t P, uint64_t N) {
@@ -1535,7 +1658,8 @@ ReduceLayout reduce_layout(int32_t P, uint64_t N) {
   l.split = align_up(l.info + 8 * ntiles, 256);
   l.bm = align_up(l.split + 4 * (ntiles + 1) * (size_t)P, 256);
   const size_t bm_words = std::max((N + kTile - 1) / kTile * (size_t)kWords, ntiles * 32);
-  l.total = align_up(l.bm + 4 * bm_words, 256);
+  l.hot = align_up(l.bm + 4 * bm_words, 256);
+  l.total = align_up(l.hot + 4 * ntiles, 256);
   return l;
 }
 
@@ -1556,6 +1680,8 @@ int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
   a.split = split;
   a.tile_bm = reinterpret_cast<uint32_t*>(w + l.bm);
   a.u_total = reinterpret_cast<uint32_t*>(w + 128);  // cleared with the ticket below
+  a.hot_cnt = reinterpret_cast<uint32_t*>(w + 192);  // likewise
+  a.hot = reinterpret_cast<uint32_t*>(w + l.hot);
   a.inject = reinterpret_cast<const uint32_t*>(w + kInjectOffset);
   // Clear the ticket and the look-back states (the status word is kept).
   if (cudaMemsetAsync(w + l.ticket, 0, l.info - l.ticket, s) != cudaSuccess)
@@ -1575,6 +1701,9 @@ int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
   }
   if (mini) tile_w = kMini;
   a.tile_w = tile_w;
+  a.hot_thr = (uint32_t)std::min<double>(
+      std::max<double>(kHot, kHotRatio * (double)a.P * (double)a.cap * kMini / (double)a.N),
+      (double)kMini * kMiniMaxP);
   a.ntiles = (uint32_t)((a.N + tile_w - 1) / tile_w);
   mark(0);
   if (mini) {
@@ -1623,11 +1752,23 @@ int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
       note_launches(3);
       return SPARCML_OK;
     }
+    {  // the tiles too hot for one warp, a CTA each. A deferred tile holds more
+       // than hot_thr - 8 P entries (quads cut at the runs' ends): hot_max bounds
+       // how many there can be.
+      const uint64_t least = std::max<uint64_t>(a.hot_thr / 2, 1);
+      const uint64_t hot_max = std::min<uint64_t>(a.ntiles, (uint64_t)a.P * a.cap / least + 1);
+      const unsigned hot_grid = (unsigned)std::min<uint64_t>(hot_max, kHotGrid);
+      if (a.op != kOpSum)
+        reduce_hot_tile_kernel<Q4, true><<<hot_grid, kHotThreads, 0, s>>>(a);
+      else
+        reduce_hot_tile_kernel<Q4, false><<<hot_grid, kHotThreads, 0, s>>>(a);
+      if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
+    }
     const uint64_t groups = ((uint64_t)a.ntiles * kMiniWords + kReduceThreads - 1) / kReduceThreads;
     reduce_mini_compact_kernel<<<(unsigned)groups, kReduceThreads, 0, s>>>(a);
     if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
     mark(2);
-    note_launches(3);
+    note_launches(4);
     return SPARCML_OK;
   }
   const uint64_t nsplit = (uint64_t)(a.ntiles + 1) * a.P;  // one warp each

@@ -541,7 +541,7 @@ __global__ void __launch_bounds__(kGuessThreads) topk_guess_warp_kernel(Args a, 
 // for the chunk's descriptor. The rest of the chunk's description is loaded
 // after the data loads are in flight.
 // ---------------------------------------------------------------------------
-template <bool UNIFORM>
+template <bool UNIFORM, bool ANY_LONG>
 __global__ void __launch_bounds__(kStreamThreads, 2) topk_stream_kernel(Args a) {
   const uint32_t gc = blockIdx.x;
   const uint32_t p = gc / a.nchunk, c = gc - p * a.nchunk;
@@ -629,7 +629,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) topk_stream_kernel(Args a) 
   // writes +0.0f for every candidate it stores, and the select restores acc at
   // the candidates that are not kept (fewer scattered writes than zeroing the
   // kept ones afterwards).
-  const bool long_seg = kind == kLong;
+  const bool long_seg = ANY_LONG && kind == kLong;
   uint32_t run = 0;  // candidates so far in this sub-chunk (warp-uniform)
 #pragma unroll
   for (uint32_t t = 0; t < kRounds; ++t) {
@@ -641,6 +641,36 @@ __global__ void __launch_bounds__(kStreamThreads, 2) topk_stream_kernel(Args a) 
     acc.w = __fadd_rn(rv[t].w, gv[t].w);
     const float av[4] = {acc.x, acc.y, acc.z, acc.w};
     const bool full = a.vec && e0 >= lo_r && e0 + 4 <= hi_r;
+    if (!ANY_LONG) {  // the residual gets acc: stored first, then the candidates
+      uint32_t bits = 0;
+      if (full) {
+        *reinterpret_cast<float4*>(rp + e0) = acc;
+#pragma unroll
+        for (uint32_t q = 0; q < 4; ++q) bits |= (mag_key(av[q]) >= G ? 1u : 0u) << q;
+      } else {
+#pragma unroll
+        for (int32_t q = 0; q < 4; ++q)
+          if (e0 + q >= lo_r && e0 + q < hi_r) {
+            rp[e0 + q] = av[q];
+            bits |= (mag_key(av[q]) >= G ? 1u : 0u) << q;
+          }
+      }
+      if (__ballot_sync(0xffffffffu, bits) == 0) continue;  // warp-uniform
+      uint32_t tot;
+      uint32_t pos = run + warp_excl_small(__popc(bits), &tot);
+      run += tot;
+#pragma unroll
+      for (uint32_t q = 0; q < 4; ++q)
+        if (bits & (1u << q)) {
+          if (pos < slot) {
+            const uint64_t keep = l2_policy_evict_last();
+            st_keep(a.cand_idx + slot0 + pos, base_u + (uint32_t)e0 + q, keep);
+            st_keep(a.cand_val + slot0 + pos, av[q], keep);
+          }
+          ++pos;
+        }
+      continue;
+    }
     uint32_t in = 0xfu;  // entries of the quad inside the segment
     if (!full) {
       in = 0;
@@ -1678,10 +1708,15 @@ int launch_topk(const Plan& q, const float* grad, float* residual, uint32_t* out
   mark(1);
   {
     const unsigned grid = (unsigned)((uint64_t)q.P * q.nchunk);
-    if (q.u_L)
-      topk_stream_kernel<true><<<grid, kStreamThreads, 0, s>>>(a);
+    // (the compiler drops the long-segment path from tables without one)
+    if (q.u_L && q.nlong)
+      topk_stream_kernel<true, true><<<grid, kStreamThreads, 0, s>>>(a);
+    else if (q.u_L)
+      topk_stream_kernel<true, false><<<grid, kStreamThreads, 0, s>>>(a);
+    else if (q.nlong)
+      topk_stream_kernel<false, true><<<grid, kStreamThreads, 0, s>>>(a);
     else
-      topk_stream_kernel<false><<<grid, kStreamThreads, 0, s>>>(a);
+      topk_stream_kernel<false, false><<<grid, kStreamThreads, 0, s>>>(a);
     ++launches;
   }
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
