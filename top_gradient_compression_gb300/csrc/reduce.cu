@@ -975,40 +975,59 @@ __device__ __forceinline__ uint32_t mini_tile_of_warp(const ReduceArgs& a, bool 
 // at once when its indices are distinct (one node, or no index shared by two
 // nodes); otherwise its nodes are applied one at a time, in order, so every
 // index sees its nodes in ascending order.
+// The signed 4-bit levels: lut[c] = +-(c & 7) / 7, negative when c & 8.
+__device__ __forceinline__ void init_level_table(float* lut) {
+  if (threadIdx.x < 16) {
+    const float q = level_over_7(threadIdx.x & 7u);
+    lut[threadIdx.x] = (threadIdx.x & 8u) ? -q : q;
+  }
+}
+
+// load_value<true> with the 4-bit level read from the table above: one shared
+// load in place of the selects, and the same bits (under round-to-nearest a
+// product with the sign moved into a factor is the negated product).
+__device__ __forceinline__ float load_value_lut(const ReduceArgs& a, uint32_t p, uint32_t j,
+                                                const float* lut) {
+  if (a.bits != 4) return load_value<true>(a, p, j);  // uniform branch
+  const uint8_t byte = a.codes[(uint64_t)p * a.code_stride + (j >> 1)];
+  const uint32_t code = (j & 1) ? (byte >> 4) : (byte & 15u);
+  if ((code & 7u) == 0) return 0.0f;
+  const uint32_t b = a.bucket_shift < 32 ? j >> a.bucket_shift : j / a.bucket;
+  return __fmul_rn(lut[code], a.scales[(uint64_t)p * a.scale_stride + b]);
+}
+
 template <bool Q4>
 __device__ __forceinline__ void mini_accumulate(const ReduceArgs& a, int32_t kop, uint32_t* acc,
                                                 uint32_t tile_lo, uint32_t tile_n,
                                                 const uint32_t* lo, const uint32_t* cpre,
-                                                uint32_t total, float e) {
+                                                uint32_t total, float e, const float* lut,
+                                                uint8_t* tag /* [kMini] */) {
   const uint32_t lane = lane_id();
-  uint32_t x = lane, p = 0, pend = 0, j = 0;
-  const uint32_t* ip = a.idx;
-  const float* vp = a.val;
+  // Position x of the tile's flattened entries belongs to the largest node q
+  // with cpre[q] <= x (an empty node starts where its successor does, so the
+  // search passes over it): a binary search per position, independent from
+  // round to round, so a round's loads need not wait for the previous round's.
+  const uint32_t P = (uint32_t)a.P;
+  const uint32_t step0 = P > 1 ? 1u << (31 - __clz(P - 1)) : 0u;
   for (uint32_t r0 = 0; r0 < total; r0 += 32 * kMiniRounds) {
     uint32_t ix[kMiniRounds], pn[kMiniRounds];
     float vx[kMiniRounds];
 #pragma unroll
     for (uint32_t u = 0; u < kMiniRounds; ++u) {
+      const uint32_t x = r0 + 32 * u + lane;
       pn[u] = kMiniMaxP;  // no entry
       ix[u] = 0;
       vx[u] = 0.0f;
       if (x < total) {
-        if (x >= pend) {
-          while (cpre[p + 1] <= x) ++p;
-          pend = cpre[p + 1];
-          j = lo[p] + (x - cpre[p]);
-          ip = a.idx + (uint64_t)p * a.cap + j;
-          if constexpr (!Q4) vp = a.val + (uint64_t)p * a.cap + j;
-        }
-        pn[u] = p;
-        ix[u] = ld_stream(ip);
-        if constexpr (Q4) vx[u] = load_value<Q4>(a, p, j);
-        else vx[u] = ld_stream(vp);
+        uint32_t q = 0;
+        for (uint32_t st = step0; st; st >>= 1)
+          if (q + st < P && cpre[q + st] <= x) q += st;
+        const uint32_t j = lo[q] + (x - cpre[q]);
+        pn[u] = q;
+        ix[u] = ld_stream(a.idx + (uint64_t)q * a.cap + j);
+        if constexpr (Q4) vx[u] = load_value_lut(a, q, j, lut);
+        else vx[u] = ld_stream(a.val + (uint64_t)q * a.cap + j);
       }
-      x += 32;
-      j += 32;
-      ip += 32;
-      if constexpr (!Q4) vp += 32;
     }
 #pragma unroll
     for (uint32_t u = 0; u < kMiniRounds; ++u) {
@@ -1018,7 +1037,17 @@ __device__ __forceinline__ void mini_accumulate(const ReduceArgs& a, int32_t kop
       const bool live = pn[u] != kMiniMaxP;
       const uint32_t off = ix[u] - tile_lo;
       const bool mine = live && off < tile_n;
-      if (__all_sync(0xffffffffu, pn[u] == first || !live)) {  // one node: distinct indices
+      bool at_once = __all_sync(0xffffffffu, pn[u] == first || !live);  // one node: distinct
+      if (!at_once) {
+        // Several nodes: at once unless an index repeats in the round. Every
+        // lane with an entry writes its id at its index and reads it back; a
+        // repeat leaves some lane reading another's id. (The tags need no
+        // clearing: a round reads only what it wrote.)
+        if (mine) tag[off] = (uint8_t)lane;
+        __syncwarp();
+        at_once = !__any_sync(0xffffffffu, mine && tag[off] != lane);
+      }
+      if (at_once) {
         if (mine) {
           const uint32_t old = acc[off];
           acc[off] = __float_as_uint(op_fold(kop, old == kAbsent ? e : __uint_as_float(old), vx[u]));
@@ -1046,6 +1075,12 @@ reduce_mini_kernel(ReduceArgs a) {
   const int32_t kop = ANY ? a.op : kOpSum;  // sum-only launches fold the branch away
   const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
   __shared__ uint32_t sh[kMiniWarps + 1];
+  __shared__ float lut[16];
+  __shared__ uint8_t tags[kMiniWarps][kMini];
+  if constexpr (Q4) {
+    init_level_table(lut);
+    __syncthreads();
+  }
   const uint32_t m = mini_tile_of_warp(a, LB, sh);
   if constexpr (!LB) {
     if (m >= a.ntiles) return;  // warp-uniform
@@ -1091,7 +1126,7 @@ reduce_mini_kernel(ReduceArgs a) {
       return;
     }
   }
-  mini_accumulate<Q4>(a, kop, acc, tile_lo, tile_n, lo, cpre, total, e);
+  mini_accumulate<Q4>(a, kop, acc, tile_lo, tile_n, lo, cpre, total, e, lut, tags[warp]);
   if constexpr (LB) mini_epilogue_lookback(a, m, acc, active, sh);
   else mini_epilogue(a, m, acc);
 }

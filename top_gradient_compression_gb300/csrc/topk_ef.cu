@@ -109,7 +109,9 @@ static_assert(sizeof(ChunkDesc) == 32, "chunk descriptor layout");
 // Per (node, long segment): the select's state.
 enum : uint32_t { kModeNormal = 0, kModeFallback = 1 };
 struct LongSel {
-  uint32_t mode, bin, rank, T, cut, overflow, pad0, pad1;
+  uint32_t mode, bin, rank, T, cut, overflow;
+  uint32_t mid;  // the sample's estimate of T: the stream pass zeroes candidates at or above it
+  uint32_t pad;
 };
 
 struct UploadBatch {
@@ -236,6 +238,7 @@ __global__ void __launch_bounds__(256) topk_init_kernel(Args a) {
     if (x < n_long) {
       a.bnd_cnt[x] = 0;
       a.lsel[x].overflow = 0;
+      a.lsel[x].mid = 0;  // zero everything stored until the long guess sets it
       continue;
     }
     x -= n_long;
@@ -376,12 +379,12 @@ __device__ __forceinline__ void warp_find_from_top32(const uint32_t* tot, uint32
 __global__ void __launch_bounds__(kGuessThreads) topk_guess_long_kernel(Args a) {
   __shared__ uint32_t h1[2048];
   __shared__ uint32_t tot[2048];
-  __shared__ uint32_t h2[2][32];
-  __shared__ uint32_t t2[2][32];
+  __shared__ uint32_t h2[3][32];
+  __shared__ uint32_t t2[3][32];
   __shared__ uint32_t scratch[34];
   __shared__ uint32_t res[2];
-  __shared__ uint32_t pick[4];  // digit-1 bins of G and of the anchor, their ranks left
-  __shared__ uint32_t pick2[2];
+  __shared__ uint32_t pick[6];  // digit-1 bins of G, the anchor and the mid guess, ranks left
+  __shared__ uint32_t pick2[3];
   cg::cluster_group cluster = cg::this_cluster();
   const uint32_t CS = cluster.num_blocks(), rank = cluster.block_rank();
   const uint32_t item = blockIdx.x / CS;
@@ -389,7 +392,7 @@ __global__ void __launch_bounds__(kGuessThreads) topk_guess_long_kernel(Args a) 
   const SegRec r = a.recs[s];
   const uint32_t t = threadIdx.x, lane = lane_id(), warp = t >> 5;
   for (uint32_t b = t; b < 2048; b += blockDim.x) h1[b] = 0;
-  if (t < 64) (&h2[0][0])[t] = 0;
+  if (t < 96) (&h2[0][0])[t] = 0;
   const uint64_t base = (uint64_t)p * a.N + r.begin;
   const float* gp = a.grad + base;
   const float* rp = a.residual + base;
@@ -437,14 +440,25 @@ __global__ void __launch_bounds__(kGuessThreads) topk_guess_long_kernel(Args a) 
     pick[3] = res[0] == kNone ? 1u : rA - res[1];
   }
   __syncthreads();
+  // the mid guess: rank k * S / n of the S sample keys, the sample's estimate of T
+  const uint32_t S = nruns * kRun;
+  const uint64_t rM64 = ((uint64_t)r.k * S + r.n / 2) / r.n;
+  const uint32_t rM = rM64 < 1 ? 1u : (uint32_t)rM64;
+  find_from_top(tot, 2048, rM, scratch, res);
+  if (t == 0) {
+    pick[4] = res[0] == kNone ? 0u : res[0];
+    pick[5] = res[0] == kNone ? 1u : rM - res[1];
+  }
+  __syncthreads();
 #pragma unroll
   for (uint32_t q = 0; q < kGuessKPT; ++q) {
     if ((key[q] >> 20) == pick[0]) atomicAdd(&h2[0][(key[q] >> 15) & 31u], 1u);
     if ((key[q] >> 20) == pick[2]) atomicAdd(&h2[1][(key[q] >> 15) & 31u], 1u);
+    if ((key[q] >> 20) == pick[4]) atomicAdd(&h2[2][(key[q] >> 15) & 31u], 1u);
   }
   __syncthreads();
   cluster.sync();  // every CTA's digit-2 histograms are in
-  if (t < 64) {
+  if (t < 96) {
     uint32_t sum = 0;
     for (uint32_t q = 0; q < CS; ++q) sum += cluster.map_shared_rank(&h2[0][0], q)[t];
     (&t2[0][0])[t] = sum;
@@ -452,12 +466,14 @@ __global__ void __launch_bounds__(kGuessThreads) topk_guess_long_kernel(Args a) 
   __syncthreads();
   if (warp == 0) warp_find_from_top32(t2[0], pick[1], &pick2[0]);
   if (warp == 1) warp_find_from_top32(t2[1], pick[3], &pick2[1]);
+  if (warp == 2) warp_find_from_top32(t2[2], pick[5], &pick2[2]);
   __syncthreads();
   cluster.sync();  // no CTA leaves while its histograms may still be read
   if (t == 0 && rank == 0) {
     const uint32_t G = (pick[0] << 20) | (pick2[0] << 15);
     const uint32_t anchor = (pick[2] << 20) | (pick2[1] << 15);
     a.guess[(uint64_t)p * a.nseg + s] = make_uint2(G, hist_shift(G, anchor));
+    a.lsel[(uint64_t)p * a.nlong + item % a.nlong].mid = (pick[4] << 20) | (pick2[2] << 15);
   }
 }
 
@@ -625,11 +641,13 @@ __global__ void __launch_bounds__(kStreamThreads, 2) topk_stream_kernel(Args a) 
   }
   const uint64_t sub = (uint64_t)gc * kWarpsPerChunk + warp;
   const uint64_t slot0 = (uint64_t)p * a.node_slots + (uint64_t)slot32 * 32 + (uint64_t)warp * slot;
-  // Long segments keep more than half of their candidates: the stream pass
-  // writes +0.0f for every candidate it stores, and the select restores acc at
-  // the candidates that are not kept (fewer scattered writes than zeroing the
-  // kept ones afterwards).
+  // Long segments: the stream pass writes +0.0f for every candidate it stores
+  // at or above the mid guess Gm (the sample's estimate of T), and the select
+  // then zeroes the kept candidates below Gm and restores acc at the stored
+  // ones at or above it that are not kept: few scattered writes, where
+  // zeroing every kept candidate afterwards would scatter k of them.
   const bool long_seg = ANY_LONG && kind == kLong;
+  const uint32_t Gm = long_seg ? a.lsel[(uint64_t)p * a.nlong + aux].mid : 0u;
   uint32_t run = 0;  // candidates so far in this sub-chunk (warp-uniform)
 #pragma unroll
   for (uint32_t t = 0; t < kRounds; ++t) {
@@ -692,7 +710,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) topk_stream_kernel(Args a) 
             const uint64_t keep = l2_policy_evict_last();
             st_keep(a.cand_idx + slot0 + pos, base_u + (uint32_t)e0 + q, keep);
             st_keep(a.cand_val + slot0 + pos, av[q], keep);
-            zero |= long_seg ? 1u << q : 0u;
+            zero |= (long_seg && mag_key(av[q]) >= Gm) ? 1u << q : 0u;
           }
           ++pos;
         }
@@ -1018,7 +1036,7 @@ __global__ void __launch_bounds__(256) long_hist_kernel(Args a) {
 
 // Per range: candidates above the boundary bin are counted; those in it are
 // appended (key, index) to the segment's boundary buffer.
-__global__ void __launch_bounds__(256) long_collect_kernel(Args a) {
+__global__ void __launch_bounds__(256, 4) long_collect_kernel(Args a) {
   __shared__ uint32_t wgt[8];
   RangeView v;
   range_view(a, &v);
@@ -1196,50 +1214,55 @@ __global__ void __launch_bounds__(kExactThreads) long_exact_kernel(Args a) {
 }
 
 // Per range: every candidate with key > T, or key == T and index <= I_T, in
-// index order at the range's offset; the residual is zeroed there. Each warp
-// keeps its first 512 candidates (values, offsets, keep bits) in registers
-// between the count and the write; any beyond are read again.
-__global__ void __launch_bounds__(256) long_write_kernel(Args a) {
+// index order at the range's offset. The residual: the stream pass zeroed the
+// candidates with key >= Gm (the mid guess); a kept one below Gm is zeroed
+// here and a stored one at or above Gm that is not kept gets its acc back. Each warp loads its
+// first 512 candidates' values and indices together (both are needed:
+// the index is the output or the restore address) and holds them between
+// the count and the write; any beyond are read again.
+__global__ void __launch_bounds__(256, 4) long_write_kernel(Args a) {
   __shared__ uint32_t wcnt[8];
   __shared__ uint32_t wbase[8];
+  __shared__ uint32_t roff;
   RangeView v;
   range_view(a, &v);
   if (a.lsel[v.pl].mode != kModeNormal) return;  // CTA-uniform
   const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) roff = a.range_off[(uint64_t)v.p * a.nranges + blockIdx.x % a.nranges];
   const LongSel L = a.lsel[v.pl];
-  const uint32_t T = L.T, cut = L.cut;
+  const uint32_t T = L.T, cut = L.cut, Gm = L.mid;
   const float* cv = a.cand_val + v.slot_base;
   const uint32_t* ci = a.cand_idx + v.slot_base;
-  auto kept = [&](float x, uint32_t o, bool valid) {
+  auto kept = [&](float x, uint32_t idx, bool valid) {
     const uint32_t key = mag_key(x);
-    return valid && (key > T || (key == T && ci[o] <= cut));
+    return valid && (key > T || (key == T && idx <= cut));
   };
-  // count: the held batch, then any further batches
   float xv[kHold];
-  uint32_t so[kHold];
-  uint32_t kb = 0, n = 0;
+  uint32_t iv[kHold];
 #pragma unroll
   for (uint32_t u = 0; u < kHold; ++u) {
     const uint32_t x = u * 32 + lane;
-    so[u] = range_off(v, min(x, v.count - 1));
-    xv[u] = x < v.count ? cv[so[u]] : 0.0f;
+    const uint32_t o = range_off(v, min(x, v.count - 1));
+    xv[u] = x < v.count ? cv[o] : 0.0f;
+    iv[u] = x < v.count ? ci[o] : 0u;
   }
+  uint32_t kb = 0, n = 0;
 #pragma unroll
   for (uint32_t u = 0; u < kHold; ++u) {
-    const bool k_ = kept(xv[u], so[u], u * 32 + lane < v.count);
+    const bool k_ = kept(xv[u], iv[u], u * 32 + lane < v.count);
     kb |= (k_ ? 1u : 0u) << u;
     n += k_ ? 1u : 0u;
   }
   for (uint32_t x0 = 32 * kHold; x0 < v.count; x0 += 32) {
     const uint32_t x = x0 + lane;
     const uint32_t o = range_off(v, min(x, v.count - 1));
-    n += kept(x < v.count ? cv[o] : 0.0f, o, x < v.count) ? 1u : 0u;
+    n += kept(x < v.count ? cv[o] : 0.0f, x < v.count ? ci[o] : 0u, x < v.count) ? 1u : 0u;
   }
   n = warp_sum(n);
   if (lane == 0) wcnt[warp] = n;
   __syncthreads();
   if (threadIdx.x == 0) {
-    uint32_t run = a.range_off[(uint64_t)v.p * a.nranges + blockIdx.x % a.nranges];
+    uint32_t run = roff;
     for (uint32_t w = 0; w < 8; ++w) {
       wbase[w] = run;
       run += wcnt[w];
@@ -1250,10 +1273,9 @@ __global__ void __launch_bounds__(256) long_write_kernel(Args a) {
   const uint64_t out0 = (uint64_t)v.p * a.cap + v.rec.out0;
   float* rp = a.residual + (uint64_t)v.p * a.N;
   const uint64_t keep = l2_policy_evict_last();
-  // kept: to the stream (its residual is already +0.0f); a candidate that is
-  // not kept gets its acc back in the residual
   auto emit = [&](bool valid, bool k_, uint32_t idx, float val) {
     const uint32_t m = __ballot_sync(0xffffffffu, k_);
+    const bool zeroed = mag_key(val) >= Gm;
     if (k_) {
       const uint32_t o = pos + __popc(m & lanemask_lt());
       if (o < v.rec.k) {
@@ -1262,22 +1284,20 @@ __global__ void __launch_bounds__(256) long_write_kernel(Args a) {
       } else {
         set_status(a.status, SPARCML_ERR_BAD_STREAM);
       }
-    } else if (valid) {
+      if (!zeroed) rp[idx] = 0.0f;
+    } else if (valid && zeroed) {
       rp[idx] = val;
     }
     pos += __popc(m);
   };
-  uint32_t iv[kHold];
-#pragma unroll
-  for (uint32_t u = 0; u < kHold; ++u) iv[u] = u * 32 + lane < v.count ? ci[so[u]] : 0u;
 #pragma unroll
   for (uint32_t u = 0; u < kHold; ++u) emit(u * 32 + lane < v.count, (kb >> u) & 1u, iv[u], xv[u]);
   for (uint32_t x0 = 32 * kHold; x0 < v.count; x0 += 32) {
     const uint32_t x = x0 + lane;
     const uint32_t o = range_off(v, min(x, v.count - 1));
     const float val = x < v.count ? cv[o] : 0.0f;
-    const bool k_ = kept(val, o, x < v.count);
-    emit(x < v.count, k_, x < v.count ? ci[o] : 0u, val);
+    const uint32_t idx = x < v.count ? ci[o] : 0u;
+    emit(x < v.count, kept(val, idx, x < v.count), idx, val);
   }
 }
 
