@@ -958,9 +958,11 @@ struct RangeView {
   uint64_t slot_base;     // this warp's first sub-slot
 };
 
-__device__ __forceinline__ bool range_view(const Args& a, RangeView* v) {
-  const uint32_t rid = blockIdx.x % a.nranges;
-  v->p = blockIdx.x / a.nranges;
+// Range gr = p * nranges + rid, seen by warp `warp` (0..7) of its 8 warps.
+__device__ __forceinline__ bool range_view_at(const Args& a, RangeView* v, uint32_t gr,
+                                              uint32_t warp) {
+  const uint32_t rid = gr % a.nranges;
+  v->p = gr / a.nranges;
   const uint32_t m = a.range_map[rid];
   v->ls = m >> 16;
   v->rr = m & 0xffffu;
@@ -968,7 +970,7 @@ __device__ __forceinline__ bool range_view(const Args& a, RangeView* v) {
   v->rec = a.recs[v->s];
   v->gs = (uint64_t)v->p * a.nseg + v->s;
   v->pl = (uint64_t)v->p * a.nlong + v->ls;
-  const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
+  const uint32_t lane = lane_id();
   const uint32_t nsub = v->rec.nchunk * kWarpsPerChunk;
   const uint32_t w0 = v->rr * kRangeSubs + warp * 32;  // the warp's first sub-chunk
   const uint32_t w = w0 + lane;
@@ -980,6 +982,11 @@ __device__ __forceinline__ bool range_view(const Args& a, RangeView* v) {
   v->slot_base = (uint64_t)v->p * a.node_slots + (uint64_t)v->rec.slot32 * 32 +
                  (uint64_t)w0 * v->rec.slot;
   return true;
+}
+
+// The range of a CTA of 256 threads: blockIdx.x.
+__device__ __forceinline__ bool range_view(const Args& a, RangeView* v) {
+  return range_view_at(a, v, blockIdx.x, threadIdx.x >> 5);
 }
 
 // Offset (from the warp's first sub-slot) of the warp's candidate number x:
@@ -1220,7 +1227,7 @@ __global__ void __launch_bounds__(kExactThreads) long_exact_kernel(Args a) {
 // first 512 candidates' values and indices together (both are needed:
 // the index is the output or the restore address) and holds them between
 // the count and the write; any beyond are read again.
-__global__ void __launch_bounds__(256, 4) long_write_kernel(Args a) {
+__global__ void __launch_bounds__(256) long_write_kernel(Args a) {
   __shared__ uint32_t wcnt[8];
   __shared__ uint32_t wbase[8];
   __shared__ uint32_t roff;
@@ -1305,9 +1312,12 @@ __global__ void __launch_bounds__(256, 4) long_write_kernel(Args a) {
 // candidate the stream pass stored (and zeroed in the residual) gets its acc
 // back, so the residual holds acc over the whole segment again.
 __global__ void __launch_bounds__(256) long_restore_kernel(Args a) {
+  {  // most segments did not fall back: look at the mode before the range's records
+    const uint32_t ls = a.range_map[blockIdx.x % a.nranges] >> 16;
+    if (a.lsel[(uint64_t)(blockIdx.x / a.nranges) * a.nlong + ls].mode != kModeFallback) return;
+  }
   RangeView v;
   range_view(a, &v);
-  if (a.lsel[v.pl].mode != kModeFallback) return;  // CTA-uniform
   const uint32_t lane = lane_id();
   const float* cv = a.cand_val + v.slot_base;
   const uint32_t* ci = a.cand_idx + v.slot_base;
