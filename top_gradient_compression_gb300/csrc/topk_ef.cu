@@ -18,23 +18,27 @@
 //              overwhelming probability, at least k_s keys of the whole
 //              segment are >= G (certainly so for a fully sampled segment).
 //              Long segments also get a histogram scale from a second, higher
-//              sample quantile.
+//              sample quantile, and a mid guess Gm: the sample's estimate of
+//              the k-th key itself.
 //  3. stream   the HBM-bound pass (one CTA per 8,192-entry chunk of a
 //              segment): reads grad and residual once with 128-bit loads
 //              aligned on the element grid, writes acc back into residual,
 //              and compacts the candidates (key >= G) in index order into the
 //              warp's own sub-slot. A segment that keeps everything (k = n) is
 //              written straight to the stream here; one that keeps nothing
-//              never has candidates. For long segments every candidate is also
-//              counted in a 2,048-bin histogram of (key - G) >> shift.
+//              never has candidates. In long segments a stored candidate at or
+//              above Gm gets +0.0f in the residual at once.
 //  4. select   layer-sized segments: one CTA per segment selects among its
 //              candidates in shared memory (four 8-bit radix digits) and
-//              writes the kept entries in index order. Long segments: the
-//              histogram's boundary bin; the candidates in that bin collected;
-//              the exact k-th key T and the index cut I_T among keys equal to
-//              T (lowest indices first) from a select in shared memory; an
-//              ordered write of every candidate with key > T, or key == T and
-//              index <= I_T. Whatever the candidates cannot decide (the guess
+//              writes the kept entries in index order. Long segments, in
+//              passes over ranges of sub-slots: a 2,048-bin histogram of
+//              (key - G) >> shift; its boundary bin; the candidates in that
+//              bin collected; the exact k-th key T and the index cut I_T
+//              among keys equal to T (lowest indices first) from a select in
+//              shared memory; an ordered write of every candidate with key >
+//              T, or key == T and index <= I_T, which also zeroes the kept
+//              candidates below Gm and restores acc at the stored ones at or
+//              above Gm that are not kept. Whatever the candidates cannot decide (the guess
 //              covered fewer than k_s entries, a sub-slot or the boundary
 //              buffer overflowed) is decided again from the segment's acc
 //              (now in residual) by a raw select: the answer is the same.
