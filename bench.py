@@ -68,7 +68,7 @@ def parse_args():
                     help="override P (smaller device footprint for profiling captures)")
     ap.add_argument("--cpu-segments", type=int, default=48,
                     help="resnet50: layer segments per node in the bounded CPU-baseline sample")
-    ap.add_argument("--cpu-entries", type=int, default=1 << 21,
+    ap.add_argument("--cpu-entries", type=int, default=1 << 23,
                     help="asr: entries per node (one segment) in the bounded CPU-baseline sample")
     return ap.parse_args()
 
