@@ -746,6 +746,53 @@ reduce_split_quad_kernel(const uint32_t* __restrict__ idx, const uint32_t* __res
   for (uint32_t k0 = blockIdx.x * span; k0 < nq; k0 += gridDim.x * span) {
     uint4 v[kSplitQuads];
     uint32_t before[kSplitQuads];
+    // every quad of this span holds four entries of the row (CTA-uniform):
+    // no per-quad range checks and no partial quads
+    const bool interior = 4 * (uint64_t)k0 > lead && 4 * ((uint64_t)k0 + span) <= (uint64_t)lead + n;
+    if (interior) {
+#pragma unroll
+      for (uint32_t u = 0; u < kSplitQuads; ++u) {
+        const uint32_t k = k0 + u * blockDim.x + threadIdx.x;
+        v[u] = ld_stream(quads + k);
+        before[u] = lane == 0 ? row[4 * k - lead - 1] : 0u;
+      }
+#pragma unroll
+      for (uint32_t u = 0; u < kSplitQuads; ++u) {
+        const uint32_t k = k0 + u * blockDim.x + threadIdx.x;
+        uint32_t prev = __shfl_up_sync(0xffffffffu, v[u].w, 1);
+        if (lane == 0) prev = before[u];
+        const uint4 q = v[u];
+        const uint32_t jf = 4 * k - lead;
+        const bool ok = prev < q.x && q.x < q.y && q.y < q.z && q.z < q.w && q.w < N;
+        bad |= !ok;
+        // tiles whose boundary falls in (prev, q.w]: none for most quads
+        const uint32_t t0 = ok ? (prev >> kMiniShift) + 1 : 0u;
+        const uint32_t t1 = ok ? (q.w >> kMiniShift) + 1 : 0u;
+        const bool wide = t1 - t0 > 4;
+        if (!wide) {
+          for (uint32_t t = t0; t < t1; ++t) {
+            const uint32_t b = t << kMiniShift;
+            split[(uint64_t)t * P + p] = jf + (q.x < b) + (q.y < b) + (q.z < b);
+          }
+        }
+        uint32_t todo = __ballot_sync(0xffffffffu, wide);
+        while (todo) {
+          const uint32_t src = __ffs(todo) - 1;
+          todo &= todo - 1;
+          const uint32_t a0 = __shfl_sync(0xffffffffu, t0, src);
+          const uint32_t a1 = __shfl_sync(0xffffffffu, t1, src);
+          const uint32_t sj = __shfl_sync(0xffffffffu, jf, src);
+          const uint32_t sx = __shfl_sync(0xffffffffu, q.x, src);
+          const uint32_t sy = __shfl_sync(0xffffffffu, q.y, src);
+          const uint32_t sz = __shfl_sync(0xffffffffu, q.z, src);
+          for (uint32_t t = a0 + lane; t < a1; t += 32) {
+            const uint32_t b = t << kMiniShift;
+            split[(uint64_t)t * P + p] = sj + (sx < b) + (sy < b) + (sz < b);
+          }
+        }
+      }
+      continue;
+    }
 #pragma unroll
     for (uint32_t u = 0; u < kSplitQuads; ++u) {
       const uint32_t k = k0 + u * blockDim.x + threadIdx.x;
