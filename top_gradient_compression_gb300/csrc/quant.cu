@@ -10,7 +10,7 @@
 // the earliest entry in the lowest bits.
 //
 // Two passes: one warp per bucket takes the scale (a warp max-reduction),
-// then one thread per code byte encodes its 8/b entries.
+// then one thread per 32-bit word of codes encodes its 4 * 8/b entries.
 // The rounding draw for an entry is SplitMix64 keyed by (seed, node, index),
 // so it does not depend on which thread or launch handles the entry.
 
@@ -135,8 +135,9 @@ quantize_scale_vec_kernel(const float* __restrict__ val, const uint32_t* __restr
   if (lane == 0) scales[(uint64_t)p * scale_stride + b] = m;
 }
 
-// Pass 2, one thread per code byte (8/BITS entries of one bucket, since a
-// bucket is a whole number of bytes): encode against the bucket's scale.
+// Pass 2, one thread per 32-bit word of codes: four bytes, each 8/BITS entries
+// of one bucket (a bucket is a whole number of bytes), encoded against the
+// bucket's scale; the word is stored whole when all four bytes hold entries.
 // idx == nullptr: dense rows (the position is the rounding key); nnz ==
 // nullptr: full rows.
 template <int BITS>
@@ -147,29 +148,49 @@ quantize_encode_kernel(const uint32_t* __restrict__ idx, const float* __restrict
                        const float* __restrict__ scales, float* __restrict__ err_out,
                        uint32_t code_stride, uint64_t scale_stride) {
   constexpr uint32_t kPer = 8 / BITS;
-  const uint32_t p = blockIdx.y;  // grid: (bytes of a row, node)
+  const uint32_t p = blockIdx.y;  // grid: (code words of a row, node)
+  __shared__ uint64_t mix;        // the node's part of the draw key, once per CTA
+  if (threadIdx.x == 0) mix = splitmix64(splitmix64(seed) ^ (uint64_t)p);
+  __syncthreads();
+  const uint64_t node_mix = mix;
   const uint32_t n = nnz ? (uint32_t)min((uint64_t)nnz[p], cap) : (uint32_t)cap;
-  const uint64_t node_mix = splitmix64(splitmix64(seed) ^ (uint64_t)p);
   const uint64_t row = (uint64_t)p * cap;
   const float* sp = scales + (uint64_t)p * scale_stride;
   uint8_t* cp = codes + (uint64_t)p * code_stride;
-  for (uint32_t q = blockIdx.x * blockDim.x + threadIdx.x; q < code_stride;
-       q += gridDim.x * blockDim.x) {
-    const uint32_t j0 = q * kPer;
-    if (j0 >= n) break;  // bytes past the row's entries stay untouched
-    const float m = sp[bucket_shift < 32 ? j0 >> bucket_shift : j0 / bucket];
-    uint32_t byte = 0;
+  const bool aligned = (reinterpret_cast<uintptr_t>(cp) & 3) == 0;
+  const uint32_t nwords = (code_stride + 3) / 4;
+  // each thread: one 32-bit word of codes (4 bytes, 4 * kPer entries)
+  for (uint32_t w = blockIdx.x * blockDim.x + threadIdx.x; w < nwords;
+       w += gridDim.x * blockDim.x) {
+    const uint32_t q0 = 4 * w;
+    if (q0 * kPer >= n) break;  // bytes past the row's entries stay untouched
+    uint32_t word = 0;
 #pragma unroll
-    for (uint32_t k = 0; k < kPer; ++k) {
-      const uint32_t j = j0 + k;
-      if (j < n) {
-        const float v = val[row + j];
-        const uint32_t c = encode<BITS>(v, idx ? (uint64_t)idx[row + j] : (uint64_t)j, m, node_mix);
-        byte |= c << (k * BITS);
-        if (err_out) err_out[row + j] = __fsub_rn(v, decode<BITS>(c, m));
+    for (uint32_t b = 0; b < 4; ++b) {
+      const uint32_t j0 = (q0 + b) * kPer;
+      if (q0 + b < code_stride && j0 < n) {
+        const float m = sp[bucket_shift < 32 ? j0 >> bucket_shift : j0 / bucket];
+        uint32_t byte = 0;
+#pragma unroll
+        for (uint32_t k = 0; k < kPer; ++k) {
+          const uint32_t j = j0 + k;
+          if (j < n) {
+            const float v = val[row + j];
+            const uint32_t c = encode<BITS>(v, idx ? (uint64_t)idx[row + j] : (uint64_t)j, m, node_mix);
+            byte |= c << (k * BITS);
+            if (err_out) err_out[row + j] = __fsub_rn(v, decode<BITS>(c, m));
+          }
+        }
+        word |= byte << (8 * b);
       }
     }
-    cp[q] = (uint8_t)byte;
+    if (aligned && q0 + 4 <= code_stride && (q0 + 3) * kPer < n) {
+      *reinterpret_cast<uint32_t*>(cp + q0) = word;  // all four bytes hold entries
+    } else {
+#pragma unroll
+      for (uint32_t b = 0; b < 4; ++b)
+        if (q0 + b < code_stride && (q0 + b) * kPer < n) cp[q0 + b] = (uint8_t)(word >> (8 * b));
+    }
   }
 }
 
@@ -232,7 +253,8 @@ int launch_quantize(const uint32_t* idx, const float* val, const uint32_t* nnz, 
         val, nnz, P, cap, bucket, (uint32_t)nbk, scales, nbk, status);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   const uint32_t shift = (bucket & (bucket - 1)) == 0 ? (uint32_t)__builtin_ctz(bucket) : 32u;
-  const dim3 eg((unsigned)std::min<uint64_t>((code_stride + kQuantThreads - 1) / kQuantThreads,
+  const uint64_t code_words = (code_stride + 3) / 4;
+  const dim3 eg((unsigned)std::min<uint64_t>((code_words + kQuantThreads - 1) / kQuantThreads,
                                              std::max<uint64_t>(1, 152u * 64u / (uint64_t)P)),
                 (unsigned)P);
   const uint32_t cs = (uint32_t)code_stride;
