@@ -226,45 +226,65 @@ __global__ void __launch_bounds__(kMergeThreads) ssar_merge_kernel(StageArgs s) 
   local_split(min(t * kPerThread, L), &a0, &b0);
   local_split(min((t + 1) * kPerThread, L), &a1, &b1);
   if (b0 > b1) b0 = b1;  // a tie moved the start past a short range
-  // Two walks over the thread's positions in shared memory: the first counts
-  // the merged entries, the second (after the offsets are known) writes them,
-  // so nothing is held in per-thread arrays.
-  auto walk = [&](auto emit) {
-    uint32_t n = 0, ia = a0, ib = b0;
-    while ((ia < a1 || ib < b1) && n <= kPerThread) {
-      if (ib >= b1 || (ia < a1 && sa_idx[ia] < sb_idx[ib])) {
-        emit(n, sa_idx[ia], __fadd_rn(0.0f, sa_val[ia]));
-        ++ia;
-      } else if (ia >= a1 || sb_idx[ib] < sa_idx[ia]) {
-        emit(n, sb_idx[ib], __fadd_rn(0.0f, sb_val[ib]));
-        ++ib;
-      } else {  // the same index in A and B: (+0 + a) + b
-        emit(n, sa_idx[ia], __fadd_rn(__fadd_rn(0.0f, sa_val[ia]), sb_val[ib]));
-        ++ia;
-        ++ib;
+  // One walk over the thread's positions (at most kPerThread + 1 entries: a
+  // pair of equal keys kept whole can add one), its entries held in registers
+  // (the loop is unrolled, so every index is static).
+  uint32_t okey[kPerThread + 1];
+  float oval[kPerThread + 1];
+  uint32_t n = 0;
+  {
+    uint32_t ia = a0, ib = b0;
+#pragma unroll
+    for (uint32_t u = 0; u <= kPerThread; ++u) {
+      okey[u] = 0;
+      oval[u] = 0.0f;
+      if (ia < a1 || ib < b1) {  // once false, false for the rest of the walk
+        if (ib >= b1 || (ia < a1 && sa_idx[ia] < sb_idx[ib])) {
+          okey[u] = sa_idx[ia];
+          oval[u] = __fadd_rn(0.0f, sa_val[ia]);
+          ++ia;
+        } else if (ia >= a1 || sb_idx[ib] < sa_idx[ia]) {
+          okey[u] = sb_idx[ib];
+          oval[u] = __fadd_rn(0.0f, sb_val[ib]);
+          ++ib;
+        } else {  // the same index in A and B: (+0 + a) + b
+          okey[u] = sa_idx[ia];
+          oval[u] = __fadd_rn(__fadd_rn(0.0f, sa_val[ia]), sb_val[ib]);
+          ++ia;
+          ++ib;
+        }
+        n = u + 1;
       }
-      ++n;
     }
-    return n;
-  };
-  const uint32_t n = walk([](uint32_t, uint32_t, float) {});
+  }
   uint32_t count;
-  const uint32_t ex = block_excl_scan(n, scratch, &count);
+  const uint32_t ex = block_excl_scan(n, scratch, &count);  // its barriers end every walk
   if (t < 32) {
     const uint32_t excl = chunk_lookback(s, (uint64_t)g * s.chunks, c, count);
     if (t == 0) bc[1] = excl;
   }
+  // The chunk's merged entries, in order, into the (now free) A staging
+  // arrays, then out with consecutive threads on consecutive positions.
+  // count <= la + lb <= kChunk + 2 fits them.
+#pragma unroll
+  for (uint32_t u = 0; u <= kPerThread; ++u) {
+    if (u < n && ex + u < kChunk + 2) {
+      sa_idx[ex + u] = okey[u];
+      sa_val[ex + u] = oval[u];
+    }
+  }
   __syncthreads();
-  const uint64_t pos0 = (uint64_t)bc[1] + ex;
+  const uint64_t pos0 = bc[1];
   const uint64_t base = (uint64_t)g * s.cap_out;
-  walk([&](uint32_t x, uint32_t key, float v) {
+  const uint32_t cnt = min(count, kChunk + 2);
+  for (uint32_t x = t; x < cnt; x += blockDim.x) {
     if (pos0 + x < s.cap_out) {
-      s.out_idx[base + pos0 + x] = key;
-      s.out_val[base + pos0 + x] = v;
+      s.out_idx[base + pos0 + x] = sa_idx[x];
+      s.out_val[base + pos0 + x] = sa_val[x];
     } else {
       set_status(s.status, SPARCML_ERR_CAPACITY);
     }
-  });
+  }
   const bool last = (uint64_t)(c + 1) * kChunk >= total;
   if (t == 0 && last) {
     const uint32_t u = bc[1] + count;
