@@ -917,18 +917,25 @@ __device__ uint32_t warp_lookback(const ReduceArgs& a, uint32_t tile, uint32_t c
 // present indices ascending (each lane the indices of its bitmap word), past
 // it the dense slice. tile_info records which, for the fix-up pass; the last
 // tile writes U. Called by every warp of the CTA (inactive ones add nothing).
+// Presence word of lane i (indices 32i..32i+31 of the tile) from an
+// accumulator that marks absent indices with kAbsent: 32 ballots.
+__device__ __forceinline__ uint32_t presence_word(const uint32_t* acc) {
+  const uint32_t lane = lane_id();
+  uint32_t word = 0;
+#pragma unroll 8
+  for (uint32_t i = 0; i < kMiniWords; ++i) {
+    const uint32_t b = __ballot_sync(0xffffffffu, acc[i * 32 + lane] != kAbsent);
+    if (lane == i) word = b;
+  }
+  return word;
+}
+
+// `word`: the lane's presence word (0 for a tile past the end).
 __device__ __forceinline__ void mini_epilogue_lookback(const ReduceArgs& a, uint32_t m,
                                                        const uint32_t* acc, bool active,
-                                                       uint32_t* sh /* [kMiniWarps + 1] */) {
+                                                       uint32_t* sh /* [kMiniWarps + 1] */,
+                                                       uint32_t word) {
   const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
-  uint32_t word = 0;
-  if (active) {
-#pragma unroll 8
-    for (uint32_t i = 0; i < kMiniWords; ++i) {
-      const uint32_t b = __ballot_sync(0xffffffffu, acc[i * 32 + lane] != kAbsent);
-      if (lane == i) word = b;
-    }
-  }
   const uint32_t wincl = warp_incl_sum(__popc(word));
   const uint32_t count = __shfl_sync(0xffffffffu, wincl, 31);
   if (lane == 0) sh[warp] = count;
@@ -973,17 +980,12 @@ __device__ __forceinline__ void mini_epilogue_lookback(const ReduceArgs& a, uint
 
 // Warp tile epilogue: presence bitmap (absent = kAbsent), dense slice with
 // absent indices as +0.0f, and the tile's count added to the union size.
-__device__ __forceinline__ void mini_epilogue(const ReduceArgs& a, uint32_t m, const uint32_t* acc) {
+// `word`: the lane's presence word (indices 32 lane .. 32 lane + 31).
+__device__ __forceinline__ void mini_epilogue(const ReduceArgs& a, uint32_t m, const uint32_t* acc,
+                                              uint32_t word) {
   const uint32_t lane = lane_id();
   const uint32_t tile_lo = m * kMini;
   const uint32_t tile_n = min(kMini, a.N - tile_lo);
-  // presence bitmap: word i covers indices 32i..32i+31 and ends up in lane i
-  uint32_t word = 0;
-#pragma unroll 8
-  for (uint32_t i = 0; i < kMiniWords; ++i) {
-    const uint32_t b = __ballot_sync(0xffffffffu, acc[i * 32 + lane] != kAbsent);
-    if (lane == i) word = b;
-  }
   const uint32_t count = warp_sum(__popc(word));
   float* od = a.out_dense + tile_lo;
   const float e = op_neutral(a.op);
@@ -1048,7 +1050,8 @@ __device__ __forceinline__ void mini_accumulate(const ReduceArgs& a, int32_t kop
                                                 uint32_t tile_lo, uint32_t tile_n,
                                                 const uint32_t* lo, const uint32_t* cpre,
                                                 uint32_t total, float e, const float* lut,
-                                                uint8_t* tag /* [kMini] */) {
+                                                uint8_t* tag /* [kMini] */,
+                                                uint32_t* bm /* [kMiniWords] presence bits */) {
   const uint32_t lane = lane_id();
   // Position x of the tile's flattened entries belongs to the largest node q
   // with cpre[q] <= x (an empty node starts where its successor does, so the
@@ -1094,6 +1097,7 @@ __device__ __forceinline__ void mini_accumulate(const ReduceArgs& a, int32_t kop
         __syncwarp();
         at_once = !__any_sync(0xffffffffu, mine && tag[off] != lane);
       }
+      if (mine) atomicOr(&bm[off >> 5], 1u << (off & 31));
       if (at_once) {
         if (mine) {
           const uint32_t old = acc[off];
@@ -1124,6 +1128,7 @@ reduce_mini_kernel(ReduceArgs a) {
   __shared__ uint32_t sh[kMiniWarps + 1];
   __shared__ float lut[16];
   __shared__ uint8_t tags[kMiniWarps][kMini];
+  __shared__ uint32_t bmw[kMiniWarps][kMiniWords];  // presence bits, set as entries are folded
   if constexpr (Q4) {
     init_level_table(lut);
     __syncthreads();
@@ -1146,6 +1151,7 @@ reduce_mini_kernel(ReduceArgs a) {
 #pragma unroll
   for (uint32_t i = 0; i < kMini / 128; ++i)
     reinterpret_cast<uint4*>(acc)[i * 32 + lane] = make_uint4(kAbsent, kAbsent, kAbsent, kAbsent);
+  bmw[warp][lane] = 0;
   uint32_t c[2] = {0, 0};
 #pragma unroll
   for (uint32_t q = 0; q < 2; ++q) {
@@ -1173,9 +1179,11 @@ reduce_mini_kernel(ReduceArgs a) {
       return;
     }
   }
-  mini_accumulate<Q4>(a, kop, acc, tile_lo, tile_n, lo, cpre, total, e, lut, tags[warp]);
-  if constexpr (LB) mini_epilogue_lookback(a, m, acc, active, sh);
-  else mini_epilogue(a, m, acc);
+  mini_accumulate<Q4>(a, kop, acc, tile_lo, tile_n, lo, cpre, total, e, lut, tags[warp],
+                      bmw[warp]);
+  __syncwarp();
+  if constexpr (LB) mini_epilogue_lookback(a, m, acc, active, sh, bmw[warp][lane]);
+  else mini_epilogue(a, m, acc, bmw[warp][lane]);
 }
 
 // Vector form of the warp tile (fp32 values, idx and val 16-byte aligned):
@@ -1320,8 +1328,8 @@ reduce_mini_quad_kernel(ReduceArgs a) {
       __syncwarp();
     }
   }
-  if constexpr (LB) mini_epilogue_lookback(a, m, acc, active, sh);
-  else mini_epilogue(a, m, acc);
+  if constexpr (LB) mini_epilogue_lookback(a, m, acc, active, sh, active ? presence_word(acc) : 0u);
+  else mini_epilogue(a, m, acc, presence_word(acc));
 }
 
 // A hot tile (dense-first mode, more entries than hot_thr: a skewed,
@@ -1388,7 +1396,7 @@ reduce_hot_tile_kernel(ReduceArgs a) {
         __syncthreads();  // node p0 + u is folded in before node p0 + u + 1
       }
     }
-    if (t < 32) mini_epilogue(a, m, acc);
+    if (t < 32) mini_epilogue(a, m, acc, presence_word(acc));
     __syncthreads();  // warp 0 has read acc and run_* before the next tile
   }
 }
