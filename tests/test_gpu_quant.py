@@ -111,3 +111,33 @@ def test_quantiser_rejects_bad_widths_on_the_host():
     for b, bucket in ((3, 8), (2, 6), (8, 0)):
         with pytest.raises(api.SparcmlError):
             api.quantize(x, bucket, b, 1, codes=codes, scales=scales)
+
+
+@pytest.mark.parametrize("b", [2, 4, 8])
+@pytest.mark.parametrize("cap", [3_001, 4_096])
+def test_code_bytes_past_each_row_are_untouched(b, cap):
+    """The encode pass stores a 32-bit word of codes only when all four bytes
+    hold entries: bytes past ceil(nnz / (8/b)) keep what the caller put there,
+    on 4-byte aligned rows (cap = 4,096) and unaligned ones (cap = 3,001), for
+    rows ending at every offset within a word."""
+    P, N = 9, 400_000
+    idx, val, nnz = W.uniform_streams(P, N, cap, 62, std=1e-3, cap=cap)
+    per = 8 // b
+    nnz[:] = [cap, 0, 1, per, per + 1, 2 * per + 1, 3 * per + 2, cap - per, cap - 1]
+    seed = W.quant_seed(5)
+    oc, osc = oracle.quantize(val, 512, b, seed, idx=idx, nnz=nnz)
+    di, dv, dn = streams_to_dev(idx, val, nnz)
+    stride = (cap + per - 1) // per
+    codes = torch.full((P, stride), 0xA5, dtype=torch.uint8, device=DEV)
+    codes, scales = api.quantize(dv, 512, b, seed, idx=di, nnz=dn, codes=codes)
+    gc = codes.cpu().numpy()
+    for p in range(P):
+        n = int(nnz[p])
+        nb = (n + per - 1) // per
+        if n % per:  # the last byte's unused codes are zero
+            assert np.array_equal(gc[p, :nb - 1], oc[p, :nb - 1])
+            mask = (1 << (b * (n % per))) - 1
+            assert gc[p, nb - 1] == (oc[p, nb - 1] & mask)
+        else:
+            assert np.array_equal(gc[p, :nb], oc[p, :nb])
+        assert (gc[p, nb:] == 0xA5).all(), p
