@@ -49,7 +49,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["resnet50", "asr", "sweep", "logreg", "qsgd", "ssar"],
+    ap.add_argument("--workload", choices=["resnet50", "asr", "sweep", "logreg", "qsgd", "ssar",
+                                           "asr_reduce"],
                     default="asr",
                     help="resnet50/asr: the whole EF step; sweep/logreg: the sparse reduce alone "
                          "on given streams (density-sweep cell / Zipf logistic regression); "
@@ -375,7 +376,7 @@ def run_reference(args, ranks):
     """--impl reference: the CPU oracle timed on every host core (rank 0 only)."""
     if ranks.rank != 0:
         return
-    if args.workload in ("sweep", "logreg", "qsgd", "ssar"):
+    if args.workload in ("sweep", "logreg", "qsgd", "ssar", "asr_reduce"):
         return run_reference_op(args)
     spec = workload_spec(args.workload)
     spec["bits"] = args.bits
@@ -413,6 +414,9 @@ def run_reference_op(args):
     if args.workload == "logreg":
         idx, val, nnz = W.logreg_streams()
         N = W.LOGREG["N"]
+    elif args.workload == "asr_reduce":  # a bounded sample: 1/8 of N at the same density
+        N = W.ASR["N"] // 8
+        idx, val, nnz = W.uniform_streams(W.ASR["P"], N, N // 100, W.sub_seed(9, N), std=1e-3)
     else:
         P = args.sweep_p if args.workload in ("sweep", "ssar") else 64
         dpct = args.sweep_d if args.workload in ("sweep", "ssar") else 10
@@ -430,6 +434,18 @@ def run_reference_op(args):
         op = lambda s: oracle.quantize(x, 1024, args.bits, W.quant_seed(s))  # noqa: E731
         units, nbytes = N, 4 * N
         desc = f"QSGD {args.bits}-bit on a dense reduced vector, N={N:,}, buckets of 1024"
+    elif args.workload == "asr_reduce":
+        threads = cores
+        kk = idx.shape[1]
+
+        def op(s):  # decode as the fused reduce does, then the reduce
+            c, sc = oracle.quantize4(idx, val, nnz, 512, W.quant_seed(s))
+            oracle.sparse_reduce(idx, oracle.dequantize4(c, sc, nnz, kk, 512), nnz, N,
+                                 threads=cores)
+        units = int(nnz.astype(np.int64).sum())
+        nbytes = idx.shape[0] * (4 * kk + -(-kk // 2) + 4 * -(-kk // 512))
+        desc = (f"4-bit quantise, decode and sparse reduce of {idx.shape[0]} streams of "
+                f"{kk:,} entries, N={N:,} (1/8 of the LSTM/ASR-like reduce)")
     else:
         threads = cores
         op = lambda s: oracle.sparse_reduce(idx, val, nnz, N, threads=cores)  # noqa: E731
@@ -868,6 +884,72 @@ def run_qsgd(args, ranks):
 # ---------------------------------------------------------------------------
 # SSAR recursive doubling, emulated (§5.3.1): fill-in and GB/s per stage
 # ---------------------------------------------------------------------------
+def run_asr_reduce(args, ranks):
+    """The fused 4-bit dequantise + sparse reduce of the LSTM/ASR-like step
+    alone, on C4-shaped streams built on the device (P=16, N=2^26, 671,088
+    sorted distinct uniform indices per node, Laplace(0, 1e-3) values
+    quantised in buckets of 512). value = the reduce's input bytes (4 B index
+    + 0.5 B code per entry + 4 B per bucket scale) per second."""
+    from top_gradient_compression_gb300 import api, workloads as W
+    dev = ranks.device()
+    torch.cuda.set_device(dev)
+    P, N, bucket = W.ASR["P"], W.ASR["N"], 512
+    di, dv, dn = W.asr_reduce_streams(dev)
+    k = di.shape[1]
+    codes, scales = api.quantize4(di, dv, dn, bucket, W.quant_seed(0))
+    ws = api.workspace(api.reduce_workspace_size(P, N), dev)
+    out = api.reduce_out(N, dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    K, Wm = args.steps, args.warmup
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    clocks = ClockSampler(dev)
+    for _ in range(Wm):
+        api.sparse_reduce_q4(di, codes, scales, dn, bucket, N, out=out, ws=ws)
+    torch.cuda.synchronize()
+    launches0 = api.launch_count()
+    t_host0 = time.time()
+    gpu_head_start(K, 300.0)
+    for i in range(K):
+        flush.fill_(float(i))  # the streams do not stay in L2 between timed runs
+        evs[i][0].record()
+        api.sparse_reduce_q4(di, codes, scales, dn, bucket, N, out=out, ws=ws)
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    launches = api.launch_count() - launches0
+    clk = clocks.summary(t_host0, t_host1)
+    clocks.stop()
+    if api.get_status(ws) != 0:
+        raise RuntimeError("device status set after the timed reduces")
+    ms = ranks.max(float(np.mean([a.elapsed_time(b) for a, b in evs])))
+    U, dense = int(out.nnz.item()), bool(out.is_dense.item())
+    nb = -(-k // bucket)
+    in_bytes = P * (4 * k + -(-k // 2) + 4 * nb)
+    out_bytes = 4 * N if dense else 8 * U
+    peak, peak_kind = hbm_peak()
+    achieved = (in_bytes + out_bytes) / (ms * 1e-3) / 1e9
+    if ranks.rank != 0:
+        return
+    print(json.dumps({
+        "metric": METRIC, "value": job_rate(ranks.world, in_bytes, ms * 1e-3) / 1e9, "unit": "GB/s",
+        "elems_per_s": job_rate(ranks.world, P * k, ms * 1e-3), "n_gpus": ranks.world,
+        "steps": K, "warmup": Wm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u4 codes, f32 sums",
+        "data": "synthetic (seeded torch generator on device)",
+        "config": {"workload": "fused 4-bit dequantise + sparse reduce of the LSTM/ASR-like step: "
+                               f"P={P} x {k:,} entries over N={N:,}, buckets of {bucket}",
+                   "units": "value = 4.5 B per input entry + 4 B per bucket scale / reduce time",
+                   "l2": "256 MB buffer written between timed runs (L2 flushed)"},
+        "roofline": {"bound": "hbm", "kernel": "fused dequantise + sparse reduce (all its launches)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": peak_kind, "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
+                     "algorithmic_bytes_per_launch": in_bytes + out_bytes, "traffic": None,
+                     "launch_ms": ms},
+        "reduce": {"U": U, "is_dense": dense},
+        "gpu_launches": launches, "clocks": clk}), flush=True)
+
+
 def run_ssar(args, ranks):
     """The static sparse allreduce by recursive doubling over the streams of a
     density-sweep cell (--sweep-p, --sweep-d). value = stream input bytes (8
@@ -951,6 +1033,8 @@ def main():
             run_qsgd(args, ranks)
         elif args.workload == "ssar":
             run_ssar(args, ranks)
+        elif args.workload == "asr_reduce":
+            run_asr_reduce(args, ranks)
         else:
             run_ours(args, ranks)
     finally:

@@ -173,6 +173,21 @@ def logreg_streams(P: int = LOGREG["P"], N: int = LOGREG["N"], nnz: int = LOGREG
     return zipf_streams(P, N, nnz, LOGREG["zipf_s"], LOGREG["std"], sub_seed(5, P, N, nnz))
 
 
+def asr_reduce_streams(device, P: int = ASR["P"], N: int = ASR["N"]):
+    """The reduce input of the LSTM/ASR-like step, built on `device`: per node
+    k = N * k_num / k_den sorted distinct uniform indices (the positions 1%
+    Top-k of an i.i.d. gradient keeps are uniform) and Laplace(0, 1e-3)
+    values. Returns int32 idx [P, k], float32 val [P, k], int32 nnz [P]."""
+    k = N * ASR["k_num"] // ASR["k_den"]
+    g = _gen(device, sub_seed(7, P, N, k))
+    idx = torch.empty((P, k), dtype=torch.int32, device=device)
+    for p in range(P):
+        idx[p] = torch.randperm(N, generator=g, device=device)[:k].sort().values.to(torch.int32)
+    val = laplace_grad(P, k, 1e-3, sub_seed(8, P, N, k), device)
+    nnz = torch.full((P,), k, dtype=torch.int32, device=device)
+    return idx, val, nnz
+
+
 def quant_seed(step: int) -> int:
     """Per-step 64-bit key handed to the stochastic quantiser (the quantiser mixes
     it with the node and the index itself)."""
