@@ -56,6 +56,9 @@ def parse_args():
                          "on given streams (density-sweep cell / Zipf logistic regression); "
                          "qsgd: b-bit quantisation of a dense reduced result; "
                          "ssar: recursive-doubling sparse allreduce of a density-sweep cell")
+    ap.add_argument("--overlap", action="store_true",
+                    help="EF-step workloads: the quantise and reduce of step t on a second stream, "
+                         "overlapping step t+1's Top-k (default: every step on one stream)")
     ap.add_argument("--bits", type=int, default=4, choices=[2, 4, 8],
                     help="asr / qsgd: width of the quantised codes")
     ap.add_argument("--op", default="sum", choices=["sum", "max", "min", "or"],
@@ -584,20 +587,23 @@ def run_ours(args, ranks):
     grads = [spec["gen"](t, dev) for t in range(NB)]
     res = torch.zeros((P, N), device=dev)
     cap = api.segment_k_total(N, L, kn, kd)
-    tk_out = (torch.empty((P, cap), dtype=torch.int32, device=dev),
-              torch.empty((P, cap), dtype=torch.float32, device=dev),
-              torch.empty((P,), dtype=torch.int32, device=dev))
+    nbuf = 2 if args.overlap else 1  # Top-k outputs and codes double-buffered when overlapped
+    tk_outs = [(torch.empty((P, cap), dtype=torch.int32, device=dev),
+                torch.empty((P, cap), dtype=torch.float32, device=dev),
+                torch.empty((P,), dtype=torch.int32, device=dev)) for _ in range(nbuf)]
+    tk_out = tk_outs[0]
     tk_ws = api.workspace(api.topk_ef_workspace_size(P, N, L, kn, kd), dev)
     rd_ws = api.workspace(api.reduce_workspace_size(P, N), dev)
     rd_out = api.reduce_out(N, dev)
     quant = spec["quant"]
     if quant:
         bucket, qbits = spec["bucket"], args.bits
-        codes = torch.zeros((P, (cap + 8 // qbits - 1) // (8 // qbits)), dtype=torch.uint8,
-                            device=dev)
+        codes_b = [torch.zeros((P, (cap + 8 // qbits - 1) // (8 // qbits)), dtype=torch.uint8,
+                               device=dev) for _ in range(nbuf)]
         if qbits != 4:
             spec["desc"] = spec["desc"].replace("4-bit", f"{qbits}-bit")
-        scales = torch.zeros((P, (cap + bucket - 1) // bucket), device=dev)
+        scales_b = [torch.zeros((P, (cap + bucket - 1) // bucket), device=dev)
+                    for _ in range(nbuf)]
         qstat = api.status_word(dev)
 
     K, Wm = args.steps, args.warmup
@@ -605,29 +611,65 @@ def run_ours(args, ranks):
     ev_rd = [api.make_events(3) for _ in range(K)]  # reduce: before, split+tile | finish, after
     ev_q = [api.make_events(2) for _ in range(K)] if quant else None  # around the quantiser
 
-    def step(i, grad, timed=False):
-        api.topk_ef(grad, res, L, kn, kd, out=tk_out, ws=tk_ws,
-                    events=ev_tk[i] if timed else None)
+    def exchange(i, b, timed):
+        """Quantise (where the workload has it) and reduce step i's streams,
+        buffer b, on the current stream."""
+        o = tk_outs[b]
         if quant:
             if timed:
                 ev_q[i][0].record()
-            api.quantize(tk_out[1], bucket, qbits, W.quant_seed(i), idx=tk_out[0], nnz=tk_out[2],
-                         codes=codes, scales=scales, status=qstat)
+            api.quantize(o[1], bucket, qbits, W.quant_seed(i), idx=o[0], nnz=o[2],
+                         codes=codes_b[b], scales=scales_b[b], status=qstat)
             if timed:
                 ev_q[i][1].record()
                 ev_rd[i][0].record()
-            api.sparse_reduce_qb(tk_out[0], codes, scales, tk_out[2], bucket, qbits, N, out=rd_out,
-                                 ws=rd_ws)
+            api.sparse_reduce_qb(o[0], codes_b[b], scales_b[b], o[2], bucket, qbits, N,
+                                 out=rd_out, ws=rd_ws)
             if timed:
                 ev_rd[i][1].record()
                 ev_rd[i][2].record()
         else:
-            api.sparse_reduce(tk_out[0], tk_out[1], tk_out[2], N, out=rd_out, ws=rd_ws,
+            api.sparse_reduce(o[0], o[1], o[2], N, out=rd_out, ws=rd_ws,
                               events=ev_rd[i] if timed else None)
+
+    def step(i, grad, timed=False):  # one stream: Top-k, then quantise and reduce
+        api.topk_ef(grad, res, L, kn, kd, out=tk_out, ws=tk_ws,
+                    events=ev_tk[i] if timed else None)
+        exchange(i, 0, timed)
+
+    # Overlapped steps (SparCML's non-blocking collectives, §7): step i's
+    # quantise and reduce run on a second stream while step i + 1's Top-k
+    # runs on the main one. Step i's Top-k output and codes live in buffer
+    # i % 2; the Top-k of step i + 2 waits until the reduce of step i is done
+    # with that buffer, and the residual chain stays on the main stream.
+    main_s = torch.cuda.current_stream()
+    side_s = torch.cuda.Stream(device=dev)
+    ev_ready = [torch.cuda.Event() for _ in range(2)]
+    ev_free = [torch.cuda.Event() for _ in range(2)]
+    for e in ev_free:
+        e.record(main_s)
+
+    def step_overlapped(i, grad, timed=False):
+        b = i % 2
+        main_s.wait_event(ev_free[b])
+        api.topk_ef(grad, res, L, kn, kd, out=tk_outs[b], ws=tk_ws,
+                    events=ev_tk[i] if timed else None)
+        ev_ready[b].record(main_s)
+        with torch.cuda.stream(side_s):
+            side_s.wait_event(ev_ready[b])
+            exchange(i, b, timed)
+            ev_free[b].record(side_s)
+
+    def drain():  # the main stream waits for every reduce issued so far
+        for e in ev_free:
+            main_s.wait_event(e)
+
+    run_step = step_overlapped if args.overlap else step
 
     clocks = ClockSampler(dev)  # samples from before the warm-up to after the timed steps
     for i in range(Wm):
-        step(i, grads[i % NB])
+        run_step(i, grads[i % NB])
+    drain()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = api.launch_count()
@@ -636,7 +678,8 @@ def run_ours(args, ranks):
     t_host0 = time.time()
     ev0.record()
     for i in range(K):
-        step(i, grads[i % NB], timed=True)
+        run_step(i, grads[i % NB], timed=True)
+    drain()  # the timed region ends after the last step's reduce
     ev1.record()
     torch.cuda.synchronize()
     t_host1 = time.time()
@@ -666,7 +709,7 @@ def run_ours(args, ranks):
 
     U = int(rd_out.nnz.item())
     is_dense = bool(rd_out.is_dense.item())
-    nnz_h = tk_out[2].cpu().numpy().astype(np.int64)
+    nnz_h = tk_outs[(K - 1) % nbuf][2].cpu().numpy().astype(np.int64)
     sum_nnz = int(nnz_h.sum())
     in_bytes_step = P * N * 4
     value = job_rate(ranks.world, in_bytes_step, ms * 1e-3) / 1e9
@@ -779,7 +822,11 @@ def run_ours(args, ranks):
                              "reduce.input_GBps"),
                    "l2": (f"inputs larger than L2 ({NB} x {P * N * 4 / 1e6:,.0f} MB gradient "
                           f"batches + the residual), no flush"),
-                   "parallelism": f"replicas x{ranks.world} (no cross-GPU exchange)"},
+                   "parallelism": f"replicas x{ranks.world} (no cross-GPU exchange)",
+                   "pipeline": ("step t's quantise + reduce on a second stream, overlapping "
+                                "step t+1's Top-k (every step does all of its work inside the "
+                                "timed region; per-phase times then overlap)" if args.overlap
+                                else "one stream: Top-k, quantise, reduce per step")},
         "roofline": {"bound": "hbm", "kernel": "topk_stream_kernel",
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
