@@ -561,6 +561,37 @@ __global__ void __launch_bounds__(kGuessThreads) topk_guess_warp_kernel(Args a, 
 // for the chunk's descriptor. The rest of the chunk's description is loaded
 // after the data loads are in flight.
 // ---------------------------------------------------------------------------
+// A lane's candidates of one quad (bit q of `bits`: entry q of acc) into
+// the warp's sub-slot at positions pos, pos + 1, ... in index order; those
+// past the sub-slot's end are dropped (the segment then falls back to the raw
+// select). Only the set bits are visited, and the value is picked by selects
+// so acc stays in registers. Returns the bits of the entries stored.
+__device__ __forceinline__ uint32_t store_candidates(uint32_t bits, uint32_t pos, uint32_t slot,
+                                                     uint32_t* cidx, float* cval, uint32_t idx0,
+                                                     const float4& acc, uint64_t keep) {
+  uint32_t stored = bits;
+  if (pos + __popc(bits) > slot) {  // the sub-slot fills up inside this quad (rare)
+    stored = 0;
+    uint32_t q_pos = pos;
+#pragma unroll
+    for (uint32_t q = 0; q < 4; ++q)
+      if (bits & (1u << q)) {
+        if (q_pos < slot) stored |= 1u << q;
+        ++q_pos;
+      }
+  }
+  uint32_t m = stored;
+  while (m) {
+    const uint32_t q = __ffs(m) - 1;
+    m &= m - 1;
+    const float v = q == 0 ? acc.x : q == 1 ? acc.y : q == 2 ? acc.z : acc.w;
+    st_keep(cidx + pos, idx0 + q, keep);
+    st_keep(cval + pos, v, keep);
+    ++pos;
+  }
+  return stored;
+}
+
 template <bool UNIFORM, bool ANY_LONG>
 __global__ void __launch_bounds__(kStreamThreads, 2) topk_stream_kernel(Args a) {
   const uint32_t gc = blockIdx.x;
@@ -652,6 +683,9 @@ __global__ void __launch_bounds__(kStreamThreads, 2) topk_stream_kernel(Args a) 
   // zeroing every kept candidate afterwards would scatter k of them.
   const bool long_seg = ANY_LONG && kind == kLong;
   const uint32_t Gm = long_seg ? a.lsel[(uint64_t)p * a.nlong + aux].mid : 0u;
+  uint32_t* const cidx = a.cand_idx + slot0;  // the warp's sub-slot
+  float* const cval = a.cand_val + slot0;
+  const uint64_t keep = l2_policy_evict_last();
   uint32_t run = 0;  // candidates so far in this sub-chunk (warp-uniform)
 #pragma unroll
   for (uint32_t t = 0; t < kRounds; ++t) {
@@ -679,18 +713,9 @@ __global__ void __launch_bounds__(kStreamThreads, 2) topk_stream_kernel(Args a) 
       }
       if (__ballot_sync(0xffffffffu, bits) == 0) continue;  // warp-uniform
       uint32_t tot;
-      uint32_t pos = run + warp_excl_small(__popc(bits), &tot);
+      const uint32_t pos = run + warp_excl_small(__popc(bits), &tot);
       run += tot;
-#pragma unroll
-      for (uint32_t q = 0; q < 4; ++q)
-        if (bits & (1u << q)) {
-          if (pos < slot) {
-            const uint64_t keep = l2_policy_evict_last();
-            st_keep(a.cand_idx + slot0 + pos, base_u + (uint32_t)e0 + q, keep);
-            st_keep(a.cand_val + slot0 + pos, av[q], keep);
-          }
-          ++pos;
-        }
+      store_candidates(bits, pos, slot, cidx, cval, base_u + (uint32_t)e0, acc, keep);
       continue;
     }
     uint32_t in = 0xfu;  // entries of the quad inside the segment
@@ -702,22 +727,21 @@ __global__ void __launch_bounds__(kStreamThreads, 2) topk_stream_kernel(Args a) 
     uint32_t bits = 0;  // candidates: key >= G
 #pragma unroll
     for (uint32_t q = 0; q < 4; ++q) bits |= ((in >> q) & (mag_key(av[q]) >= G ? 1u : 0u)) << q;
-    uint32_t zero = 0;  // long segments: candidates kept in the sub-slot get +0.0f
+    uint32_t zero = 0;  // long segments: stored candidates at or above Gm get +0.0f
     if (__ballot_sync(0xffffffffu, bits) != 0) {  // warp-uniform
       uint32_t tot;
-      uint32_t pos = run + warp_excl_small(__popc(bits), &tot);
+      const uint32_t pos = run + warp_excl_small(__popc(bits), &tot);
       run += tot;
+      const uint32_t stored =
+          store_candidates(bits, pos, slot, cidx, cval, base_u + (uint32_t)e0, acc, keep);
+      if constexpr (ANY_LONG) {
+        if (long_seg) {
+          uint32_t hi = 0;
 #pragma unroll
-      for (uint32_t q = 0; q < 4; ++q)
-        if (bits & (1u << q)) {
-          if (pos < slot) {
-            const uint64_t keep = l2_policy_evict_last();
-            st_keep(a.cand_idx + slot0 + pos, base_u + (uint32_t)e0 + q, keep);
-            st_keep(a.cand_val + slot0 + pos, av[q], keep);
-            zero |= (long_seg && mag_key(av[q]) >= Gm) ? 1u << q : 0u;
-          }
-          ++pos;
+          for (uint32_t q = 0; q < 4; ++q) hi |= (mag_key(av[q]) >= Gm ? 1u : 0u) << q;
+          zero = stored & hi;
         }
+      }
     }
     const float4 w = make_float4(zero & 1u ? 0.0f : acc.x, zero & 2u ? 0.0f : acc.y,
                                  zero & 4u ? 0.0f : acc.z, zero & 8u ? 0.0f : acc.w);
@@ -734,9 +758,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2) topk_stream_kernel(Args a) 
   // written whole, so no later eviction from L2 leaves a half-written sector.
   const uint32_t pad_end = min((run + 7u) & ~7u, slot);
   if (run + lane < pad_end) {
-    const uint64_t keep = l2_policy_evict_last();
-    st_keep(a.cand_idx + slot0 + run + lane, kNone, keep);
-    st_keep(a.cand_val + slot0 + run + lane, 0.0f, keep);
+    st_keep(cidx + run + lane, kNone, keep);
+    st_keep(cval + run + lane, 0.0f, keep);
   }
   if (lane == 0) {
     a.sub_cnt[sub] = run;
