@@ -592,8 +592,35 @@ __device__ __forceinline__ uint32_t store_candidates(uint32_t bits, uint32_t pos
   return stored;
 }
 
+// Loads NB rounds, t0 .. t0 + NB - 1, of a warp's 1,024 entries: grad and
+// residual as 128-bit loads inside the segment, entry by entry at its ends
+// (zeros outside). All NB loads are issued before any is used.
+template <uint32_t NB>
+__device__ __forceinline__ void load_rounds(float4 (&gv)[NB], float4 (&rv)[NB], uint32_t t0,
+                                            const float* gp, const float* rp, int32_t lo_r,
+                                            int32_t hi_r, bool vec, uint32_t lane) {
+#pragma unroll
+  for (uint32_t u = 0; u < NB; ++u) {
+    const int32_t e0 = (int32_t)(4 * ((t0 + u) * 32 + lane));
+    if (vec && e0 >= lo_r && e0 + 4 <= hi_r) {
+      gv[u] = __ldcs(reinterpret_cast<const float4*>(gp + e0));
+      rv[u] = *reinterpret_cast<const float4*>(rp + e0);
+    } else {
+      float x[4] = {0.f, 0.f, 0.f, 0.f}, y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int32_t q = 0; q < 4; ++q)
+        if (e0 + q >= lo_r && e0 + q < hi_r) {
+          x[q] = gp[e0 + q];
+          y[q] = rp[e0 + q];
+        }
+      gv[u] = make_float4(x[0], x[1], x[2], x[3]);
+      rv[u] = make_float4(y[0], y[1], y[2], y[3]);
+    }
+  }
+}
+
 template <bool UNIFORM, bool ANY_LONG>
-__global__ void __launch_bounds__(kStreamThreads, 2) topk_stream_kernel(Args a) {
+__global__ void __launch_bounds__(kStreamThreads, ANY_LONG ? 2 : 3) topk_stream_kernel(Args a) {
   const uint32_t gc = blockIdx.x;
   const uint32_t p = gc / a.nchunk, c = gc - p * a.nchunk;
   const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
@@ -619,25 +646,13 @@ __global__ void __launch_bounds__(kStreamThreads, 2) topk_stream_kernel(Args a) 
   const int32_t hi_r = (int32_t)max(min((int64_t)hi - (int64_t)q0, (int64_t)kSub + 4), (int64_t)-1);
   const float* gp = a.grad + q0;
   float* rp = a.residual + q0;
-  float4 gv[kRounds], rv[kRounds];
-#pragma unroll
-  for (uint32_t t = 0; t < kRounds; ++t) {
-    const int32_t e0 = (int32_t)(4 * (t * 32 + lane));
-    if (a.vec && e0 >= lo_r && e0 + 4 <= hi_r) {
-      gv[t] = __ldcs(reinterpret_cast<const float4*>(gp + e0));
-      rv[t] = *reinterpret_cast<const float4*>(rp + e0);
-    } else {
-      float x[4] = {0.f, 0.f, 0.f, 0.f}, y[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int32_t q = 0; q < 4; ++q)
-        if (e0 + q >= lo_r && e0 + q < hi_r) {
-          x[q] = gp[e0 + q];
-          y[q] = rp[e0 + q];
-        }
-      gv[t] = make_float4(x[0], x[1], x[2], x[3]);
-      rv[t] = make_float4(y[0], y[1], y[2], y[3]);
-    }
-  }
+  // The warp's rounds in batches of kBatch whose 128-bit loads are all issued
+  // before any of their entries is used. Tables with long segments keep all
+  // eight rounds in flight (two CTAs per SM); the others take two batches of
+  // four at three CTAs per SM (measured: each is the faster form for its kind).
+  constexpr uint32_t kBatch = ANY_LONG ? kRounds : kRounds / 2;
+  float4 gv[kBatch], rv[kBatch];
+  load_rounds<kBatch>(gv, rv, 0, gp, rp, lo_r, hi_r, a.vec, lane);
   // the rest of the description, while the data loads are in flight
   uint32_t slot, slot32, kind, aux;
   if (UNIFORM) {
@@ -660,9 +675,14 @@ __global__ void __launch_bounds__(kStreamThreads, 2) topk_stream_kernel(Args a) 
     const uint64_t o = (uint64_t)p * a.cap + aux - begin;  // + node-local index
 #pragma unroll
     for (uint32_t t = 0; t < kRounds; ++t) {
+      uint32_t u = t;
+      if constexpr (!ANY_LONG) {
+        u = t % kBatch;
+        if (t > 0 && u == 0) load_rounds<kBatch>(gv, rv, t, gp, rp, lo_r, hi_r, a.vec, lane);
+      }
       const int32_t e0 = (int32_t)(4 * (t * 32 + lane));
-      const float av[4] = {__fadd_rn(rv[t].x, gv[t].x), __fadd_rn(rv[t].y, gv[t].y),
-                           __fadd_rn(rv[t].z, gv[t].z), __fadd_rn(rv[t].w, gv[t].w)};
+      const float av[4] = {__fadd_rn(rv[u].x, gv[u].x), __fadd_rn(rv[u].y, gv[u].y),
+                           __fadd_rn(rv[u].z, gv[u].z), __fadd_rn(rv[u].w, gv[u].w)};
 #pragma unroll
       for (int32_t q = 0; q < 4; ++q)
         if (e0 + q >= lo_r && e0 + q < hi_r) {
@@ -689,12 +709,17 @@ __global__ void __launch_bounds__(kStreamThreads, 2) topk_stream_kernel(Args a) 
   uint32_t run = 0;  // candidates so far in this sub-chunk (warp-uniform)
 #pragma unroll
   for (uint32_t t = 0; t < kRounds; ++t) {
+    uint32_t u = t;
+    if constexpr (!ANY_LONG) {
+      u = t % kBatch;
+      if (t > 0 && u == 0) load_rounds<kBatch>(gv, rv, t, gp, rp, lo_r, hi_r, a.vec, lane);
+    }
     const int32_t e0 = (int32_t)(4 * (t * 32 + lane));
     float4 acc;
-    acc.x = __fadd_rn(rv[t].x, gv[t].x);
-    acc.y = __fadd_rn(rv[t].y, gv[t].y);
-    acc.z = __fadd_rn(rv[t].z, gv[t].z);
-    acc.w = __fadd_rn(rv[t].w, gv[t].w);
+    acc.x = __fadd_rn(rv[u].x, gv[u].x);
+    acc.y = __fadd_rn(rv[u].y, gv[u].y);
+    acc.z = __fadd_rn(rv[u].z, gv[u].z);
+    acc.w = __fadd_rn(rv[u].w, gv[u].w);
     const float av[4] = {acc.x, acc.y, acc.z, acc.w};
     const bool full = a.vec && e0 >= lo_r && e0 + 4 <= hi_r;
     if (!ANY_LONG) {  // the residual gets acc: stored first, then the candidates
