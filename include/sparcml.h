@@ -61,6 +61,7 @@ enum sparcml_status {
   SPARCML_ERR_WORKSPACE = 2,   /* ws_bytes below the *_workspace_size     */
   SPARCML_ERR_CAPACITY = 3,    /* an output does not fit its capacity     */
   SPARCML_ERR_BAD_STREAM = 4,  /* index >= N, or not strictly ascending   */
+  SPARCML_ERR_NONFINITE = 5,   /* a checked input holds a NaN or an inf   */
   SPARCML_ERR_TIMEOUT = 6,     /* a bounded device-side wait ran out      */
   SPARCML_ERR_CUDA = 7         /* a CUDA runtime call or launch failed    */
 };
@@ -426,6 +427,20 @@ int sparcml_sparse_reduce_noalloc(const uint32_t* idx, const float* val, const u
  * ------------------------------------------------------------------------ */
 int sparcml_densify(const uint32_t* idx, const float* val, const uint32_t* nnz, int32_t P,
                     uint64_t cap, uint64_t N, float* dense, int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Checked mode for inputs (the pages define no behaviour for non-finite
+ * gradients or values: every operation above passes NaN and inf through by
+ * its rules, e.g. a NaN key ranks above every finite one in Top-k). A caller
+ * that wants such inputs flagged scans them first: SPARCML_ERR_NONFINITE is
+ * recorded in *status if any of x[0 .. n) is a NaN or +-inf.
+ *   x       device fp32 array, any 4-byte alignment (16-byte aligned arrays
+ *           are read with 128-bit loads); n = 0 checks nothing.
+ *   status  device int32 status word (e.g. a workspace head), required.
+ * Stream-ordered and non-blocking like every other call; read the result
+ * with sparcml_get_status.
+ * ------------------------------------------------------------------------ */
+int sparcml_check_finite(const float* x, uint64_t n, int32_t* status, void* stream);
 
 #ifdef __cplusplus
 }

@@ -83,3 +83,39 @@ def test_a_fresh_workspace_has_no_fault_armed():
     assert api.get_status(clean) == 0
     _reduce_matches_oracle(out, idx, val, nnz, N)
     assert int(armed[32:36].cpu().view(torch.int32).item()) != 0
+
+
+def test_checked_mode_flags_non_finite_inputs():
+    """sparcml_check_finite records SPARCML_ERR_NONFINITE for a NaN or an inf
+    anywhere in the array (head, 16-byte quads, tail; aligned and unaligned
+    starts) and nothing for finite data, however large or small."""
+    NONFINITE = api.STATUS_CODE["SPARCML_ERR_NONFINITE"]
+    status = api.status_word(DEV)
+    g = torch.Generator(device=DEV).manual_seed(11)
+    x = torch.randn(1_000_003, device=DEV, generator=g)
+    x[7] = 3.0e38
+    x[8] = 1.0e-40  # subnormal
+    api.check_finite(x, status)
+    assert api.get_status(status) == 0
+    for pos, v in [(0, float("nan")), (1, float("inf")), (500_000, float("-inf")),
+                   (999_999, float("nan")), (1_000_002, float("inf"))]:
+        y = x.clone()
+        y[pos] = v
+        api.check_finite(y, status)
+        assert api.get_status(status) == NONFINITE, pos
+    for start in (1, 2, 3):  # views starting 4, 8 and 12 bytes past a 16-byte boundary
+        y = x.clone()
+        y[start] = float("nan")
+        api.check_finite(y[start:], status)
+        assert api.get_status(status) == NONFINITE, start
+        api.check_finite(y[start + 1:], status)
+        assert api.get_status(status) == 0, start
+    api.check_finite(x[:0], status)
+    assert api.get_status(status) == 0
+    # the workspace of a reduce is a status word too: the next clean call is clean
+    ws = api.workspace(api.reduce_workspace_size(2, 1000), DEV)
+    y = x.clone()
+    y[123] = float("nan")
+    api.check_finite(y, ws)
+    assert api.get_status(ws) == NONFINITE
+    assert api.get_status(ws) == 0

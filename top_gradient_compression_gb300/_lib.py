@@ -77,6 +77,7 @@ SIGNATURES = {
                                                 vp, vp, C.c_uint64, vp, vp, vp, C.c_size_t, vp,
                                                 vp]),
     "sparcml_densify": (C.c_int, [vp, vp, vp, C.c_int32, C.c_uint64, C.c_uint64, vp, vp, vp]),
+    "sparcml_check_finite": (C.c_int, [vp, C.c_uint64, vp, vp]),
 }
 
 

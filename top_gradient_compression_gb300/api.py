@@ -20,8 +20,8 @@ from . import _lib
 
 OK = 0
 STATUS = {0: "SPARCML_OK", 1: "SPARCML_ERR_INVALID_ARG", 2: "SPARCML_ERR_WORKSPACE",
-          3: "SPARCML_ERR_CAPACITY", 4: "SPARCML_ERR_BAD_STREAM", 6: "SPARCML_ERR_TIMEOUT",
-          7: "SPARCML_ERR_CUDA"}
+          3: "SPARCML_ERR_CAPACITY", 4: "SPARCML_ERR_BAD_STREAM", 5: "SPARCML_ERR_NONFINITE",
+          6: "SPARCML_ERR_TIMEOUT", 7: "SPARCML_ERR_CUDA"}
 STATUS_CODE = {v: k for k, v in STATUS.items()}
 
 
@@ -465,3 +465,13 @@ def densify(idx, val, nnz, N: int, out=None, status=None, stream=None):
         _cuda(nnz, torch.int32, "nnz", 1), P, cap, N, _cuda(out, torch.float32, "dense", 2),
         _opt_ptr(status), _stream(stream)))
     return out
+
+
+def check_finite(x: torch.Tensor, status: torch.Tensor, stream=None) -> None:
+    """Checked mode for an input: records SPARCML_ERR_NONFINITE in `status`
+    (a status word or workspace) if x holds a NaN or an inf. Non-blocking;
+    read it with get_status."""
+    if not x.is_cuda or x.dtype != torch.float32 or not x.is_contiguous():
+        raise ValueError("check_finite: x must be a contiguous float32 CUDA tensor")
+    _check("sparcml_check_finite", _lib.load().sparcml_check_finite(
+        x.data_ptr() if x.numel() else None, x.numel(), status.data_ptr(), _stream(stream)))

@@ -4,9 +4,21 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "sparcml.h"
 
 namespace sparcml {
+
+// A named NVTX range over a C-ABI call: profilers (ncu --nvtx, nsys) group
+// the call's kernels under the entry point's name. Free when no tool is
+// attached (NVTX v3 is header-only).
+struct ApiRange {
+  explicit ApiRange(const char* name) { nvtxRangePushA(name); }
+  ~ApiRange() { nvtxRangePop(); }
+  ApiRange(const ApiRange&) = delete;
+  ApiRange& operator=(const ApiRange&) = delete;
+};
 
 // Count of kernels launched by the library (see sparcml_launch_count).
 void note_launches(uint64_t n);

@@ -178,6 +178,7 @@ extern "C" const char* sparcml_status_string(int status) {
     case SPARCML_ERR_WORKSPACE: return "SPARCML_ERR_WORKSPACE";
     case SPARCML_ERR_CAPACITY: return "SPARCML_ERR_CAPACITY";
     case SPARCML_ERR_BAD_STREAM: return "SPARCML_ERR_BAD_STREAM";
+    case SPARCML_ERR_NONFINITE: return "SPARCML_ERR_NONFINITE";
     case SPARCML_ERR_TIMEOUT: return "SPARCML_ERR_TIMEOUT";
     case SPARCML_ERR_CUDA: return "SPARCML_ERR_CUDA";
     default: return "SPARCML_ERR_UNKNOWN";
@@ -218,6 +219,7 @@ extern "C" size_t sparcml_pack_workspace_size(int32_t P, uint64_t N) {
 extern "C" int sparcml_pack(const float* x, int32_t P, uint64_t N, float thr, uint32_t* out_idx,
                             float* out_val, uint32_t* out_nnz, uint64_t cap, void* ws,
                             size_t ws_bytes, void* stream) {
+  const ApiRange nvtx_range(__func__);
   if (!x || !out_idx || !out_val || !out_nnz || !ws || P < 1 || P > 65535 || N < 1 ||
       N > 0xffffffffull || !(thr >= 0.0f) || cap > 0xffffffffull)
     return SPARCML_ERR_INVALID_ARG;
@@ -244,9 +246,46 @@ extern "C" int sparcml_pack(const float* x, int32_t P, uint64_t N, float thr, ui
   return SPARCML_OK;
 }
 
+// Checked mode for inputs: any NaN or +-inf in x[0 .. n) records
+// SPARCML_ERR_NONFINITE. Grid-stride over 16-byte quads of the aligned part
+// (the unaligned head and the tail entry by entry); one vote per warp.
+__global__ void __launch_bounds__(256) check_finite_kernel(const float* __restrict__ x,
+                                                           uint64_t n, uint64_t head,
+                                                           int32_t* status) {
+  const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  bool bad = false;
+  auto nonfinite = [](float v) { return (__float_as_uint(v) & 0x7f800000u) == 0x7f800000u; };
+  for (uint64_t i = tid; i < head; i += stride) bad |= nonfinite(x[i]);
+  const uint64_t nq = (n - head) / 4;
+  const float4* q4 = reinterpret_cast<const float4*>(x + head);
+  for (uint64_t i = tid; i < nq; i += stride) {
+    const float4 v = q4[i];
+    bad |= nonfinite(v.x) | nonfinite(v.y) | nonfinite(v.z) | nonfinite(v.w);
+  }
+  for (uint64_t i = head + 4 * nq + tid; i < n; i += stride) bad |= nonfinite(x[i]);
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31u) == 0)
+    set_status(status, SPARCML_ERR_NONFINITE);
+}
+
+extern "C" int sparcml_check_finite(const float* x, uint64_t n, int32_t* status, void* stream) {
+  const ApiRange nvtx_range(__func__);
+  if (!status || (n > 0 && !x)) return SPARCML_ERR_INVALID_ARG;
+  if (n == 0) return SPARCML_OK;
+  // entries before the first 16-byte boundary (x is at least 4-byte aligned)
+  const uint64_t mis = (reinterpret_cast<uintptr_t>(x) & 15u) / 4u;
+  const uint64_t head = std::min<uint64_t>(n, mis ? 4 - mis : 0);
+  const unsigned grid = (unsigned)std::min<uint64_t>((n / 4 + 255) / 256 + 1, 152u * 8u);
+  check_finite_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(x, n, head, status);
+  if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
+  note_launches(1);
+  return SPARCML_OK;
+}
+
 extern "C" int sparcml_densify(const uint32_t* idx, const float* val, const uint32_t* nnz,
                                int32_t P, uint64_t cap, uint64_t N, float* dense, int32_t* status,
                                void* stream) {
+  const ApiRange nvtx_range(__func__);
   if (!idx || !val || !nnz || !dense || P < 1 || P > 65535 || N < 1 || N > 0xffffffffull)
     return SPARCML_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

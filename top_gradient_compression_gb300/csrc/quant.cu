@@ -309,6 +309,7 @@ using namespace sparcml;
 extern "C" int sparcml_quantize4(const uint32_t* idx, const float* val, const uint32_t* nnz,
                                  int32_t P, uint64_t cap, uint32_t bucket, uint64_t seed,
                                  uint8_t* codes, float* scales, int32_t* status, void* stream) {
+  const ApiRange nvtx_range(__func__);
   if (!idx || !nnz || bucket < 2 || (bucket & 1)) return SPARCML_ERR_INVALID_ARG;
   return launch_quantize(idx, val, nnz, P, cap, bucket, 4, seed, codes, scales, nullptr, status,
                          stream);
@@ -317,6 +318,7 @@ extern "C" int sparcml_quantize4(const uint32_t* idx, const float* val, const ui
 extern "C" int sparcml_dequantize4(const uint8_t* codes, const float* scales, const uint32_t* nnz,
                                    int32_t P, uint64_t cap, uint32_t bucket, float* val_out,
                                    int32_t* status, void* stream) {
+  const ApiRange nvtx_range(__func__);
   if (!nnz || bucket < 2 || (bucket & 1)) return SPARCML_ERR_INVALID_ARG;
   return launch_dequantize(codes, scales, nnz, P, cap, bucket, 4, val_out, status, stream);
 }
@@ -325,6 +327,7 @@ extern "C" int sparcml_quantize(const uint32_t* idx, const float* val, const uin
                                 int32_t P, uint64_t cap, uint32_t bucket, uint32_t bits,
                                 uint64_t seed, uint8_t* codes, float* scales, float* err_out,
                                 int32_t* status, void* stream) {
+  const ApiRange nvtx_range(__func__);
   return launch_quantize(idx, val, nnz, P, cap, bucket, bits, seed, codes, scales, err_out,
                          status, stream);
 }
@@ -332,5 +335,6 @@ extern "C" int sparcml_quantize(const uint32_t* idx, const float* val, const uin
 extern "C" int sparcml_dequantize(const uint8_t* codes, const float* scales, const uint32_t* nnz,
                                   int32_t P, uint64_t cap, uint32_t bucket, uint32_t bits,
                                   float* val_out, int32_t* status, void* stream) {
+  const ApiRange nvtx_range(__func__);
   return launch_dequantize(codes, scales, nnz, P, cap, bucket, bits, val_out, status, stream);
 }

@@ -1977,6 +1977,7 @@ extern "C" int sparcml_sparse_reduce_traced(const uint32_t* idx, const float* va
                                             float* out_dense, uint32_t* out_nnz,
                                             int32_t* out_is_dense, void* ws, size_t ws_bytes,
                                             void* stream, void* const* events) {
+  const ApiRange nvtx_range(__func__);
   return reduce_fp32(idx, val, nnz, P, cap, N, kOpSum, dens_num, dens_den, out_idx, out_val,
                      out_cap, out_dense, out_nnz, out_is_dense, ws, ws_bytes, stream, events);
 }
@@ -1988,6 +1989,7 @@ extern "C" int sparcml_sparse_reduce_op(const uint32_t* idx, const float* val,
                                         float* out_dense, uint32_t* out_nnz,
                                         int32_t* out_is_dense, void* ws, size_t ws_bytes,
                                         void* stream) {
+  const ApiRange nvtx_range(__func__);
   return reduce_fp32(idx, val, nnz, P, cap, N, op, dens_num, dens_den, out_idx, out_val,
                      out_cap, out_dense, out_nnz, out_is_dense, ws, ws_bytes, stream, nullptr);
 }
@@ -2049,6 +2051,7 @@ extern "C" int sparcml_sparse_reduce_q4(const uint32_t* idx, const uint8_t* code
                                         float* out_val, uint64_t out_cap, float* out_dense,
                                         uint32_t* out_nnz, int32_t* out_is_dense, void* ws,
                                         size_t ws_bytes, void* stream) {
+  const ApiRange nvtx_range(__func__);
   if (bucket < 2 || (bucket & 1)) return SPARCML_ERR_INVALID_ARG;
   return reduce_quantised(idx, codes, scales, nnz, P, cap, bucket, 4, N, dens_num, dens_den,
                           out_idx, out_val, out_cap, out_dense, out_nnz, out_is_dense, ws,
@@ -2062,6 +2065,7 @@ extern "C" int sparcml_sparse_reduce_qb(const uint32_t* idx, const uint8_t* code
                                         float* out_val, uint64_t out_cap, float* out_dense,
                                         uint32_t* out_nnz, int32_t* out_is_dense, void* ws,
                                         size_t ws_bytes, void* stream) {
+  const ApiRange nvtx_range(__func__);
   return reduce_quantised(idx, codes, scales, nnz, P, cap, bucket, bits, N, dens_num, dens_den,
                           out_idx, out_val, out_cap, out_dense, out_nnz, out_is_dense, ws,
                           ws_bytes, stream);
@@ -2165,6 +2169,7 @@ extern "C" int sparcml_sparse_reduce_noalloc(const uint32_t* idx, const float* v
                                              float* out_dense, uint32_t* out_nnz,
                                              int32_t* out_is_dense, int32_t* status,
                                              void* stream) {
+  const ApiRange nvtx_range(__func__);
   if (!idx || !val || !nnz || !out_idx || !out_val || !out_dense || !out_nnz || !out_is_dense)
     return SPARCML_ERR_INVALID_ARG;
   if (P < 1 || P > kMaxReduceP || N < 1 || N > 0xffffffffull || cap > 0xffffffffull ||

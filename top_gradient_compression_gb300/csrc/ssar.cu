@@ -346,6 +346,7 @@ extern "C" int sparcml_ssar_allreduce_traced(const uint32_t* idx, const float* v
                                              unsigned long long* stage_nnz, void* ws,
                                              size_t ws_bytes, void* stream,
                                              void* const* events) {
+  const ApiRange nvtx_range(__func__);
   if (!idx || !val || !nnz || !out_idx || !out_val || !out_nnz || !ws)
     return SPARCML_ERR_INVALID_ARG;
   if (P < 2 || (P & (P - 1)) != 0 || P > 65536 || cap < 1 || cap > 0x7fffffffull || N < 1 ||

@@ -1912,6 +1912,7 @@ extern "C" int sparcml_topk_ef_traced(const float* grad, float* residual, int32_
                                       uint32_t nseg, uint32_t* out_idx, float* out_val,
                                       uint32_t* out_nnz, uint64_t cap, void* ws, size_t ws_bytes,
                                       void* stream, void* const* events) {
+  const ApiRange nvtx_range(__func__);
   return topk_call(grad, residual, P, N, seg_begin, seg_k, nseg, out_idx, out_val, out_nnz, cap,
                    ws, ws_bytes, stream, events);
 }
@@ -1938,6 +1939,7 @@ extern "C" int sparcml_topk_ef_uniform_traced(const float* grad, float* residual
                                               uint32_t* out_nnz, uint64_t cap, void* ws,
                                               size_t ws_bytes, void* stream,
                                               void* const* events) {
+  const ApiRange nvtx_range(__func__);
   std::vector<uint64_t> b;
   std::vector<uint32_t> k;
   if (!uniform_table(N, seg_len, k_num, k_den, &b, &k) || k.size() > 0xffffffffull)
