@@ -6,9 +6,39 @@
 
 #include <nvtx3/nvToolsExt.h>
 
+#include <utility>
+
 #include "sparcml.h"
 
 namespace sparcml {
+
+// Programmatic dependent launch. Kernels are launched with programmatic
+// stream serialisation, so a kernel's grid may be set up while the previous
+// kernel of the stream drains; every kernel's first statement waits for the
+// previous grid to complete and its memory to be visible (a no-op when a
+// kernel was launched without the attribute), so no kernel touches memory
+// before its predecessor is done. No kernel triggers early: a dependent grid
+// starts only once every block of the previous one has exited.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline void launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // a failure is recorded as the runtime's last error, read by launch_status()
+  (void)cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // A named NVTX range over a C-ABI call: profilers (ncu --nvtx, nsys) group
 // the call's kernels under the entry point's name. Free when no tool is

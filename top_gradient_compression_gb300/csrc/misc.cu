@@ -29,6 +29,7 @@ __global__ void __launch_bounds__(kPackThreads)
 pack_chunk_kernel(const float* __restrict__ x, uint64_t N, uint32_t nchunk, float thr,
                   uint32_t* __restrict__ chunk_cnt, const uint32_t* __restrict__ chunk_off,
                   uint32_t* __restrict__ out_idx, float* __restrict__ out_val, uint64_t cap) {
+  griddep_wait();
   __shared__ uint32_t warp_tot[kPackThreads / 32];
   const uint32_t p = blockIdx.x / nchunk, c = blockIdx.x % nchunk;
   const uint64_t start = (uint64_t)c * kPackChunk;
@@ -94,6 +95,7 @@ __global__ void __launch_bounds__(1024)
 pack_scan_kernel(const uint32_t* __restrict__ chunk_cnt, uint32_t nchunk,
                  uint32_t* __restrict__ chunk_off, uint32_t* __restrict__ out_nnz, uint64_t cap,
                  int32_t* status) {
+  griddep_wait();
   __shared__ uint32_t scratch[34];
   const uint32_t p = blockIdx.x;
   const uint32_t* cc = chunk_cnt + (uint64_t)p * nchunk;
@@ -115,6 +117,7 @@ pack_scan_kernel(const uint32_t* __restrict__ chunk_cnt, uint32_t nchunk,
 }
 
 __global__ void densify_zero_kernel(float* __restrict__ dense, uint64_t total) {
+  griddep_wait();
   const bool vec = (reinterpret_cast<uintptr_t>(dense) & 15) == 0;
   const uint64_t nv = vec ? total / 4 : 0;
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
@@ -129,6 +132,7 @@ __global__ void densify_scatter_kernel(const uint32_t* __restrict__ idx,
                                        const float* __restrict__ val,
                                        const uint32_t* __restrict__ nnz, int32_t P, uint64_t cap,
                                        uint64_t N, float* __restrict__ dense, int32_t* status) {
+  griddep_wait();
   const uint64_t total = (uint64_t)P * cap;
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
   for (uint64_t e = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += stride) {
@@ -233,13 +237,13 @@ extern "C" int sparcml_pack(const float* x, int32_t P, uint64_t N, float thr, ui
   uint32_t* chunk_off = reinterpret_cast<uint32_t*>(w + 256 + pack_chunk_array_bytes(P, N));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const unsigned grid = (unsigned)((uint64_t)P * nchunk);
-  pack_chunk_kernel<false><<<grid, kPackThreads, 0, s>>>(x, N, (uint32_t)nchunk, thr, chunk_cnt,
+  launch_pdl(pack_chunk_kernel<false>, grid, kPackThreads, 0, s, x, N, (uint32_t)nchunk, thr, chunk_cnt,
                                                          nullptr, nullptr, nullptr, cap);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
-  pack_scan_kernel<<<(unsigned)P, 1024, 0, s>>>(chunk_cnt, (uint32_t)nchunk, chunk_off, out_nnz,
+  launch_pdl(pack_scan_kernel, (unsigned)P, 1024, 0, s, chunk_cnt, (uint32_t)nchunk, chunk_off, out_nnz,
                                                 cap, status);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
-  pack_chunk_kernel<true><<<grid, kPackThreads, 0, s>>>(x, N, (uint32_t)nchunk, thr, chunk_cnt,
+  launch_pdl(pack_chunk_kernel<true>, grid, kPackThreads, 0, s, x, N, (uint32_t)nchunk, thr, chunk_cnt,
                                                         chunk_off, out_idx, out_val, cap);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   note_launches(3);
@@ -252,6 +256,7 @@ extern "C" int sparcml_pack(const float* x, int32_t P, uint64_t N, float thr, ui
 __global__ void __launch_bounds__(256) check_finite_kernel(const float* __restrict__ x,
                                                            uint64_t n, uint64_t head,
                                                            int32_t* status) {
+  griddep_wait();
   const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
   bool bad = false;
@@ -276,7 +281,7 @@ extern "C" int sparcml_check_finite(const float* x, uint64_t n, int32_t* status,
   const uint64_t mis = (reinterpret_cast<uintptr_t>(x) & 15u) / 4u;
   const uint64_t head = std::min<uint64_t>(n, mis ? 4 - mis : 0);
   const unsigned grid = (unsigned)std::min<uint64_t>((n / 4 + 255) / 256 + 1, 152u * 8u);
-  check_finite_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(x, n, head, status);
+  launch_pdl(check_finite_kernel, grid, 256, 0, static_cast<cudaStream_t>(stream), x, n, head, status);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   note_launches(1);
   return SPARCML_OK;
@@ -291,13 +296,13 @@ extern "C" int sparcml_densify(const uint32_t* idx, const float* val, const uint
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const uint64_t total = (uint64_t)P * N;
   const unsigned zgrid = (unsigned)std::min<uint64_t>((total / 4 + 255) / 256 + 1, 152u * 16u);
-  densify_zero_kernel<<<zgrid, 256, 0, s>>>(dense, total);
+  launch_pdl(densify_zero_kernel, zgrid, 256, 0, s, dense, total);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   note_launches(1);
   if (cap == 0) return SPARCML_OK;
   const uint64_t entries = (uint64_t)P * cap;
   const unsigned sgrid = (unsigned)std::min<uint64_t>((entries + 255) / 256, 152u * 16u);
-  densify_scatter_kernel<<<sgrid, 256, 0, s>>>(idx, val, nnz, P, cap, N, dense, status);
+  launch_pdl(densify_scatter_kernel, sgrid, 256, 0, s, idx, val, nnz, P, cap, N, dense, status);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   note_launches(1);
   return SPARCML_OK;

@@ -73,6 +73,7 @@ __global__ void __launch_bounds__(kQuantThreads)
 quantize_scale_kernel(const float* __restrict__ val, const uint32_t* __restrict__ nnz, int32_t P,
                       uint64_t cap, uint32_t bucket, uint32_t nbk, float* __restrict__ scales,
                       uint64_t scale_stride, int32_t* status) {
+  griddep_wait();
   const uint64_t gw = (uint64_t)blockIdx.x * (kQuantThreads / 32) + (threadIdx.x >> 5);
   if (gw >= (uint64_t)P * nbk) return;  // warp-uniform
   const uint32_t p = (uint32_t)(gw / nbk), b = (uint32_t)(gw % nbk);
@@ -100,6 +101,7 @@ __global__ void __launch_bounds__(kQuantThreads)
 quantize_scale_vec_kernel(const float* __restrict__ val, const uint32_t* __restrict__ nnz,
                           int32_t P, uint64_t cap, uint32_t nbk, float* __restrict__ scales,
                           uint64_t scale_stride, int32_t* status) {
+  griddep_wait();
   constexpr uint32_t kBucket = 128 * VPL;
   const uint64_t gw = (uint64_t)blockIdx.x * (kQuantThreads / 32) + (threadIdx.x >> 5);
   if (gw >= (uint64_t)P * nbk) return;  // warp-uniform
@@ -147,6 +149,7 @@ quantize_encode_kernel(const uint32_t* __restrict__ idx, const float* __restrict
                        uint32_t bucket, uint64_t seed, uint8_t* __restrict__ codes,
                        const float* __restrict__ scales, float* __restrict__ err_out,
                        uint32_t code_stride, uint64_t scale_stride) {
+  griddep_wait();
   constexpr uint32_t kPer = 8 / BITS;
   const uint32_t p = blockIdx.y;  // grid: (code words of a row, node)
   __shared__ uint64_t mix;        // the node's part of the draw key, once per CTA
@@ -200,6 +203,7 @@ dequantize_kernel(const uint8_t* __restrict__ codes, const float* __restrict__ s
                   const uint32_t* __restrict__ nnz, int32_t P, uint64_t cap, uint32_t bucket,
                   uint64_t code_stride, uint64_t scale_stride, float* __restrict__ out,
                   int32_t* status) {
+  griddep_wait();
   constexpr uint32_t kPer = 8 / BITS;
   const uint64_t total = (uint64_t)P * code_stride;
   for (uint64_t q = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; q < total;
@@ -243,13 +247,13 @@ int launch_quantize(const uint32_t* idx, const float* val, const uint32_t* nnz, 
   const bool vec = (bucket == 512 || bucket == 1024) && cap % 4 == 0 &&
                    (reinterpret_cast<uintptr_t>(val) & 15) == 0;
   if (vec && bucket == 512)
-    quantize_scale_vec_kernel<4><<<(unsigned)blocks, kQuantThreads, 0, s>>>(
+    launch_pdl(quantize_scale_vec_kernel<4>, (unsigned)blocks, kQuantThreads, 0, s,
         val, nnz, P, cap, (uint32_t)nbk, scales, nbk, status);
   else if (vec)
-    quantize_scale_vec_kernel<8><<<(unsigned)blocks, kQuantThreads, 0, s>>>(
+    launch_pdl(quantize_scale_vec_kernel<8>, (unsigned)blocks, kQuantThreads, 0, s,
         val, nnz, P, cap, (uint32_t)nbk, scales, nbk, status);
   else
-    quantize_scale_kernel<<<(unsigned)blocks, kQuantThreads, 0, s>>>(
+    launch_pdl(quantize_scale_kernel, (unsigned)blocks, kQuantThreads, 0, s,
         val, nnz, P, cap, bucket, (uint32_t)nbk, scales, nbk, status);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   const uint32_t shift = (bucket & (bucket - 1)) == 0 ? (uint32_t)__builtin_ctz(bucket) : 32u;
@@ -259,13 +263,13 @@ int launch_quantize(const uint32_t* idx, const float* val, const uint32_t* nnz, 
                 (unsigned)P);
   const uint32_t cs = (uint32_t)code_stride;
   if (bits == 2)
-    quantize_encode_kernel<2><<<eg, kQuantThreads, 0, s>>>(idx, val, nnz, cap, shift, bucket,
+    launch_pdl(quantize_encode_kernel<2>, eg, kQuantThreads, 0, s, idx, val, nnz, cap, shift, bucket,
                                                             seed, codes, scales, err_out, cs, nbk);
   else if (bits == 4)
-    quantize_encode_kernel<4><<<eg, kQuantThreads, 0, s>>>(idx, val, nnz, cap, shift, bucket,
+    launch_pdl(quantize_encode_kernel<4>, eg, kQuantThreads, 0, s, idx, val, nnz, cap, shift, bucket,
                                                             seed, codes, scales, err_out, cs, nbk);
   else
-    quantize_encode_kernel<8><<<eg, kQuantThreads, 0, s>>>(idx, val, nnz, cap, shift, bucket,
+    launch_pdl(quantize_encode_kernel<8>, eg, kQuantThreads, 0, s, idx, val, nnz, cap, shift, bucket,
                                                             seed, codes, scales, err_out, cs, nbk);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   note_launches(2);
@@ -285,15 +289,15 @@ int launch_dequantize(const uint8_t* codes, const float* scales, const uint32_t*
   const uint64_t scale_stride = (cap + bucket - 1) / bucket;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (bits == 2)
-    dequantize_kernel<2><<<blocks, kQuantThreads, 0, s>>>(codes, scales, nnz, P, cap, bucket,
+    launch_pdl(dequantize_kernel<2>, blocks, kQuantThreads, 0, s, codes, scales, nnz, P, cap, bucket,
                                                           code_stride, scale_stride, val_out,
                                                           status);
   else if (bits == 4)
-    dequantize_kernel<4><<<blocks, kQuantThreads, 0, s>>>(codes, scales, nnz, P, cap, bucket,
+    launch_pdl(dequantize_kernel<4>, blocks, kQuantThreads, 0, s, codes, scales, nnz, P, cap, bucket,
                                                           code_stride, scale_stride, val_out,
                                                           status);
   else
-    dequantize_kernel<8><<<blocks, kQuantThreads, 0, s>>>(codes, scales, nnz, P, cap, bucket,
+    launch_pdl(dequantize_kernel<8>, blocks, kQuantThreads, 0, s, codes, scales, nnz, P, cap, bucket,
                                                           code_stride, scale_stride, val_out,
                                                           status);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;

@@ -222,6 +222,7 @@ __global__ void __launch_bounds__(256)
 reduce_split_kernel(const uint32_t* __restrict__ idx, const uint32_t* __restrict__ nnz,
                     int32_t P, uint64_t cap, uint32_t N, uint32_t ntiles, uint32_t tile_w,
                     uint32_t* __restrict__ split) {
+  griddep_wait();
   const uint64_t w = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (w >= (uint64_t)(ntiles + 1) * P) return;  // warp-uniform
   const uint32_t lane = lane_id();
@@ -249,6 +250,7 @@ reduce_split_kernel(const uint32_t* __restrict__ idx, const uint32_t* __restrict
 template <bool Q4, bool TABLE = false>
 __global__ void __launch_bounds__(kReduceThreads)
 reduce_tile_kernel(ReduceArgs a) {
+  griddep_wait();
   extern __shared__ __align__(16) uint32_t dyn[];
   float* acc = reinterpret_cast<float*>(dyn);
   uint32_t* bm = dyn + kTile;
@@ -437,6 +439,7 @@ constexpr uint32_t kNoPrev = 0xffffffffu;
 template <bool Q4, bool DENSE_FIRST, bool ANY>
 __global__ void __launch_bounds__(kReduceThreads)
 reduce_dense_tile_kernel(ReduceArgs a) {
+  griddep_wait();
   extern __shared__ __align__(16) uint32_t dyn[];
   const int32_t kop = ANY ? a.op : kOpSum;  // sum-only launches fold the branch away
   float* acc = reinterpret_cast<float*>(dyn);                       // [kTile]
@@ -679,6 +682,7 @@ __global__ void __launch_bounds__(256)
 reduce_split_stream_kernel(const uint32_t* __restrict__ idx, const uint32_t* __restrict__ nnz,
                            int32_t P, uint64_t cap, uint32_t N, uint32_t ntiles,
                            uint32_t* __restrict__ split, int32_t* status) {
+  griddep_wait();
   const uint32_t p = blockIdx.y, lane = lane_id();
   uint32_t n = nnz[p];
   if (n > cap) {
@@ -728,6 +732,7 @@ __global__ void __launch_bounds__(256)
 reduce_split_quad_kernel(const uint32_t* __restrict__ idx, const uint32_t* __restrict__ nnz,
                          int32_t P, uint64_t cap, uint32_t N, uint32_t ntiles,
                          uint32_t* __restrict__ split, int32_t* status) {
+  griddep_wait();
   const uint32_t p = blockIdx.y, lane = lane_id();
   uint32_t n = nnz[p];
   if (n > cap) {
@@ -1122,6 +1127,7 @@ __device__ __forceinline__ void mini_accumulate(const ReduceArgs& a, int32_t kop
 template <bool Q4, bool LB, bool ANY>
 __global__ void __launch_bounds__(kMiniWarps * 32)
 reduce_mini_kernel(ReduceArgs a) {
+  griddep_wait();
   extern __shared__ __align__(16) uint32_t dyn[];
   const int32_t kop = ANY ? a.op : kOpSum;  // sum-only launches fold the branch away
   const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
@@ -1198,6 +1204,7 @@ constexpr uint32_t kQuadRounds = 4;
 template <bool LB, bool ANY>
 __global__ void __launch_bounds__(kMiniWarps * 32)
 reduce_mini_quad_kernel(ReduceArgs a) {
+  griddep_wait();
   extern __shared__ __align__(16) uint32_t dyn[];
   const int32_t kop = ANY ? a.op : kOpSum;  // sum-only launches fold the branch away
   const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
@@ -1343,6 +1350,7 @@ reduce_mini_quad_kernel(ReduceArgs a) {
 template <bool Q4, bool ANY>
 __global__ void __launch_bounds__(kHotThreads)
 reduce_hot_tile_kernel(ReduceArgs a) {
+  griddep_wait();
   constexpr uint32_t R = kMini / kHotThreads;  // entries of a node's run per thread
   __shared__ __align__(16) uint32_t acc[kMini];
   __shared__ uint32_t run_lo[kMiniMaxP], run_n[kMiniMaxP];
@@ -1406,6 +1414,7 @@ reduce_hot_tile_kernel(ReduceArgs a) {
 // warp tiles per CTA taking their offsets by decoupled look-back.
 __global__ void __launch_bounds__(kReduceThreads)
 reduce_mini_compact_kernel(ReduceArgs a) {
+  griddep_wait();
   __shared__ uint32_t scratch[34];
   __shared__ uint32_t bc[3];
   const uint32_t U = *a.u_total;
@@ -1460,6 +1469,7 @@ reduce_mini_compact_kernel(ReduceArgs a) {
 __global__ void __launch_bounds__(1024)
 reduce_finalize_kernel(uint2* __restrict__ tile_info, uint32_t ntiles, uint32_t cap_sparse,
                        uint32_t* __restrict__ out_nnz, int32_t* __restrict__ out_is_dense) {
+  griddep_wait();
   __shared__ uint32_t scratch[34];
   uint32_t run = 0;
   for (uint32_t t0 = 0; t0 < ntiles; t0 += blockDim.x) {
@@ -1484,6 +1494,7 @@ reduce_compact_kernel(const int32_t* __restrict__ is_dense, const uint2* __restr
                       const uint32_t* __restrict__ tile_bm, const float* __restrict__ out_dense,
                       uint32_t* __restrict__ out_idx, float* __restrict__ out_val,
                       uint32_t words_per_tile) {
+  griddep_wait();
   __shared__ uint32_t scratch[34];
   if (*is_dense) return;
   const uint32_t tile = blockIdx.x, tile_lo = tile * words_per_tile * 32;
@@ -1517,6 +1528,7 @@ constexpr int32_t kMaxSparseP = 1024;
 template <bool Q4, bool ANY>
 __global__ void __launch_bounds__(kReduceThreads)
 reduce_sparse_tile_kernel(ReduceArgs a) {
+  griddep_wait();
   extern __shared__ __align__(16) uint32_t dyn[];
   const int32_t kop = ANY ? a.op : kOpSum;  // sum-only launches fold the branch away
   const uint32_t W = a.tile_w / 32;
@@ -1715,6 +1727,7 @@ reduce_fixup_kernel(const int32_t* __restrict__ is_dense, const uint2* __restric
                     const uint32_t* __restrict__ out_idx, const float* __restrict__ out_val,
                     float* __restrict__ out_dense, uint32_t N, uint32_t tile_w, uint32_t ntiles,
                     float neutral) {
+  griddep_wait();
   if (*is_dense == 0) return;
   for (uint32_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {  // block-uniform
     const uint2 info = tile_info[tile];
@@ -1804,10 +1817,10 @@ int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
     const uint32_t gx = (uint32_t)std::max<uint64_t>(
         1, std::min<uint64_t>((a.cap + per_block - 1) / per_block, 2432 / (uint64_t)a.P));
     if (quads)
-      reduce_split_quad_kernel<<<dim3(gx, (unsigned)a.P), 256, 0, s>>>(
+      launch_pdl(reduce_split_quad_kernel, dim3(gx, (unsigned)a.P), 256, 0, s,
           a.idx, a.nnz, a.P, a.cap, a.N, a.ntiles, split, a.status);
     else
-      reduce_split_stream_kernel<<<dim3(gx, (unsigned)a.P), 256, 0, s>>>(
+      launch_pdl(reduce_split_stream_kernel, dim3(gx, (unsigned)a.P), 256, 0, s,
           a.idx, a.nnz, a.P, a.cap, a.N, a.ntiles, split, a.status);
     if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
     const size_t smem = (size_t)kMiniWarps * kMiniWarpWords * sizeof(uint32_t);
@@ -1820,7 +1833,7 @@ int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
     const bool any = a.op != kOpSum;
     auto go = [&](auto kernel) {
       if (!ensure_smem(reinterpret_cast<const void*>(kernel), smem)) return false;
-      kernel<<<grid, kMiniWarps * 32, smem, s>>>(a);
+      launch_pdl(kernel, grid, kMiniWarps * 32, smem, s, a);
       return true;
     };
     bool ok;
@@ -1834,7 +1847,7 @@ int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
     if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
     mark(1);
     if (lb) {
-      reduce_fixup_kernel<<<fixup_grid(a.ntiles), 256, 0, s>>>(a.out_is_dense, a.tile_info, a.out_idx,
+      launch_pdl(reduce_fixup_kernel, fixup_grid(a.ntiles), 256, 0, s, a.out_is_dense, a.tile_info, a.out_idx,
                                                    a.out_val, a.out_dense, a.N, a.tile_w, a.ntiles,
         a.op == kOpMax ? -INFINITY : a.op == kOpMin ? INFINITY : 0.0f);
       if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
@@ -1849,20 +1862,20 @@ int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
       const uint64_t hot_max = std::min<uint64_t>(a.ntiles, (uint64_t)a.P * a.cap / least + 1);
       const unsigned hot_grid = (unsigned)std::min<uint64_t>(hot_max, kHotGrid);
       if (a.op != kOpSum)
-        reduce_hot_tile_kernel<Q4, true><<<hot_grid, kHotThreads, 0, s>>>(a);
+        launch_pdl(reduce_hot_tile_kernel<Q4, true>, hot_grid, kHotThreads, 0, s, a);
       else
-        reduce_hot_tile_kernel<Q4, false><<<hot_grid, kHotThreads, 0, s>>>(a);
+        launch_pdl(reduce_hot_tile_kernel<Q4, false>, hot_grid, kHotThreads, 0, s, a);
       if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
     }
     const uint64_t groups = ((uint64_t)a.ntiles * kMiniWords + kReduceThreads - 1) / kReduceThreads;
-    reduce_mini_compact_kernel<<<(unsigned)groups, kReduceThreads, 0, s>>>(a);
+    launch_pdl(reduce_mini_compact_kernel, (unsigned)groups, kReduceThreads, 0, s, a);
     if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
     mark(2);
     note_launches(4);
     return SPARCML_OK;
   }
   const uint64_t nsplit = (uint64_t)(a.ntiles + 1) * a.P;  // one warp each
-  reduce_split_kernel<<<(unsigned)((nsplit * 32 + 255) / 256), 256, 0, s>>>(
+  launch_pdl(reduce_split_kernel, (unsigned)((nsplit * 32 + 255) / 256), 256, 0, s,
       a.idx, a.nnz, a.P, a.cap, a.N, a.ntiles, a.tile_w, split);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   if (sparse) {
@@ -1870,7 +1883,7 @@ int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
         (2 * (size_t)(tile_w / 32) + kAccCap + 2 * (size_t)a.P + 1) * sizeof(uint32_t);
     auto go = [&](auto kernel) {
       if (!ensure_smem(reinterpret_cast<const void*>(kernel), smem)) return false;
-      kernel<<<a.ntiles, kReduceThreads, smem, s>>>(a);
+      launch_pdl(kernel, a.ntiles, kReduceThreads, smem, s, a);
       return true;
     };
     if (!(a.op != kOpSum ? go(reduce_sparse_tile_kernel<Q4, true>)
@@ -1881,7 +1894,7 @@ int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
                         sizeof(uint32_t);
     auto go_dense = [&](auto kernel) {
       if (!ensure_smem(reinterpret_cast<const void*>(kernel), smem)) return false;
-      kernel<<<a.ntiles, kReduceThreads, smem, s>>>(a);
+      launch_pdl(kernel, a.ntiles, kReduceThreads, smem, s, a);
       return true;
     };
     if ((double)a.P * (double)a.cap >= (double)a.N) {
@@ -1891,9 +1904,9 @@ int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
         return SPARCML_ERR_CUDA;
       if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
       mark(1);
-      reduce_finalize_kernel<<<1, 1024, 0, s>>>(a.tile_info, a.ntiles, a.cap_sparse, a.out_nnz,
+      launch_pdl(reduce_finalize_kernel, 1, 1024, 0, s, a.tile_info, a.ntiles, a.cap_sparse, a.out_nnz,
                                                a.out_is_dense);
-      reduce_compact_kernel<<<a.ntiles, kReduceThreads, 0, s>>>(
+      launch_pdl(reduce_compact_kernel, a.ntiles, kReduceThreads, 0, s,
           a.out_is_dense, a.tile_info, a.tile_bm, a.out_dense, a.out_idx, a.out_val, kWords);
       if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
       mark(2);
@@ -1906,7 +1919,7 @@ int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
   }
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   mark(1);
-  reduce_fixup_kernel<<<fixup_grid(a.ntiles), 256, 0, s>>>(a.out_is_dense, a.tile_info, a.out_idx,
+  launch_pdl(reduce_fixup_kernel, fixup_grid(a.ntiles), 256, 0, s, a.out_is_dense, a.tile_info, a.out_idx,
                                                a.out_val, a.out_dense, a.N, a.tile_w, a.ntiles,
         a.op == kOpMax ? -INFINITY : a.op == kOpMin ? INFINITY : 0.0f);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
@@ -2207,9 +2220,9 @@ extern "C" int sparcml_sparse_reduce_noalloc(const uint32_t* idx, const float* v
   const size_t smem = (kTile + kWords + 2 * (size_t)a.P + 1) * sizeof(uint32_t);
   if (!ensure_smem(reinterpret_cast<const void*>(reduce_tile_kernel<false>), smem))
     return SPARCML_ERR_CUDA;
-  reduce_tile_kernel<false><<<a.ntiles, kReduceThreads, smem, s>>>(a);
+  launch_pdl(reduce_tile_kernel<false>, a.ntiles, kReduceThreads, smem, s, a);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
-  reduce_fixup_kernel<<<fixup_grid(a.ntiles), 256, 0, s>>>(a.out_is_dense, a.tile_info, a.out_idx,
+  launch_pdl(reduce_fixup_kernel, fixup_grid(a.ntiles), 256, 0, s, a.out_is_dense, a.tile_info, a.out_idx,
                                                a.out_val, a.out_dense, a.N, a.tile_w, a.ntiles,
         a.op == kOpMax ? -INFINITY : a.op == kOpMin ? INFINITY : 0.0f);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;

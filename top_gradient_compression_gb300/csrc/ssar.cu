@@ -109,6 +109,7 @@ __device__ void merge_split(const uint32_t* A, uint32_t na, const uint32_t* B, u
 
 // One warp per (pair, boundary c in 0..chunks): split at min(c * kChunk, na + nb).
 __global__ void __launch_bounds__(256) ssar_partition_kernel(StageArgs s) {
+  griddep_wait();
   const uint64_t w = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const uint64_t per = (uint64_t)s.chunks + 1;
   if (w >= (uint64_t)s.G * per) return;  // warp-uniform
@@ -168,6 +169,7 @@ __device__ uint32_t chunk_lookback(const StageArgs& s, uint64_t slot0, uint32_t 
 }
 
 __global__ void __launch_bounds__(kMergeThreads) ssar_merge_kernel(StageArgs s) {
+  griddep_wait();
   __shared__ uint32_t sa_idx[kChunk + 2], sb_idx[kChunk + 2];
   __shared__ float sa_val[kChunk + 2], sb_val[kChunk + 2];
   __shared__ uint32_t scratch[34];
@@ -397,8 +399,8 @@ extern "C" int sparcml_ssar_allreduce_traced(const uint32_t* idx, const float* v
     if (cudaMemsetAsync(w + l.ticket, 0, l.split - l.ticket, s) != cudaSuccess)
       return SPARCML_ERR_CUDA;
     const uint64_t warps = (uint64_t)G * (a.chunks + 1);
-    ssar_partition_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(a);
-    ssar_merge_kernel<<<(unsigned)((uint64_t)G * a.chunks), kMergeThreads, 0, s>>>(a);
+    launch_pdl(ssar_partition_kernel, (unsigned)((warps * 32 + 255) / 256), 256, 0, s, a);
+    launch_pdl(ssar_merge_kernel, (unsigned)((uint64_t)G * a.chunks), kMergeThreads, 0, s, a);
     if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
     note_launches(2);
     in_idx = a.out_idx;

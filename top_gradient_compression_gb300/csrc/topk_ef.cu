@@ -125,6 +125,7 @@ struct UploadBatch {
 };
 
 __global__ void __launch_bounds__(256) topk_upload_kernel(const __grid_constant__ UploadBatch b) {
+  griddep_wait();
   for (uint32_t i = threadIdx.x; i < b.count; i += blockDim.x) b.dst[i] = b.words[i];
 }
 
@@ -202,6 +203,7 @@ __device__ void find_from_top(const uint32_t* h, uint32_t nbins, uint32_t r, uin
 // long-select state and histograms, and the nodes' stream sizes.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) topk_init_kernel(Args a) {
+  griddep_wait();
   const uint64_t n_desc = a.nchunk, n_seg = (uint64_t)a.P * a.nseg;
   const uint64_t n_long = (uint64_t)a.P * a.nlong, n_hist = n_long * kBins;
   const uint64_t total = n_desc + n_seg + n_long + n_hist + (uint64_t)a.P;
@@ -315,6 +317,7 @@ constexpr uint32_t kGuessKPT = kSampleLong / kGuessThreads;  // 32
 
 // Segments sampled whole (the exact kind): one CTA per (node, segment).
 __global__ void __launch_bounds__(kGuessThreads) topk_guess_cta_kernel(Args a, uint32_t nlist) {
+  griddep_wait();
   __shared__ uint32_t wsum[2][8];
   cg::cluster_group cluster = cg::this_cluster();
   const uint32_t CS = 1, rank = 0;
@@ -381,6 +384,7 @@ __device__ __forceinline__ void warp_find_from_top32(const uint32_t* tot, uint32
 }
 
 __global__ void __launch_bounds__(kGuessThreads) topk_guess_long_kernel(Args a) {
+  griddep_wait();
   __shared__ uint32_t h1[2048];
   __shared__ uint32_t tot[2048];
   __shared__ uint32_t h2[3][32];
@@ -486,6 +490,7 @@ __global__ void __launch_bounds__(kGuessThreads) topk_guess_long_kernel(Args a) 
 constexpr uint32_t kWarpKeys = kWarpSample / 32;
 
 __global__ void __launch_bounds__(kGuessThreads) topk_guess_warp_kernel(Args a, uint32_t nlist) {
+  griddep_wait();
   const uint32_t lane = lane_id();
   const uint64_t gw = (uint64_t)blockIdx.x * (kGuessThreads / 32) + (threadIdx.x >> 5);
   if (gw >= (uint64_t)a.P * nlist) return;  // warp-uniform
@@ -621,6 +626,7 @@ __device__ __forceinline__ void load_rounds(float4 (&gv)[NB], float4 (&rv)[NB], 
 
 template <bool UNIFORM, bool ANY_LONG>
 __global__ void __launch_bounds__(kStreamThreads, ANY_LONG ? 2 : 3) topk_stream_kernel(Args a) {
+  griddep_wait();
   const uint32_t gc = blockIdx.x;
   const uint32_t p = gc / a.nchunk, c = gc - p * a.nchunk;
   const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
@@ -822,6 +828,7 @@ __device__ __forceinline__ uint32_t warp_excl_sum(uint32_t v, uint32_t* total) {
 }
 
 __global__ void __launch_bounds__(kSegThreads) topk_select_short_kernel(Args a, uint32_t nlist) {
+  griddep_wait();
   __shared__ uint32_t wpre[kShortSubs + 1];
   __shared__ float vals[kShortCands];
   __shared__ uint32_t hist[256];
@@ -975,6 +982,7 @@ __device__ __forceinline__ uint32_t bin_of(uint32_t key, uint32_t G, uint32_t sh
 // The boundary bin from the histogram the stream pass built; a segment whose
 // candidates cannot decide its select is handed to the raw select.
 __global__ void __launch_bounds__(256) long_find_kernel(Args a) {
+  griddep_wait();
   __shared__ uint32_t scratch[34];
   __shared__ uint32_t res[2];
   const uint32_t p = blockIdx.x / a.nlong, ls = blockIdx.x % a.nlong;
@@ -1066,6 +1074,7 @@ constexpr uint32_t kHold = 16;
 // segment) histogram. A segment whose sub-slots overflowed is skipped: its
 // select falls back to the raw select.
 __global__ void __launch_bounds__(256) long_hist_kernel(Args a) {
+  griddep_wait();
   __shared__ uint32_t h[kBins];
   for (uint32_t b = threadIdx.x; b < kBins; b += blockDim.x) h[b] = 0;
   __syncthreads();
@@ -1096,6 +1105,7 @@ __global__ void __launch_bounds__(256) long_hist_kernel(Args a) {
 // Per range: candidates above the boundary bin are counted; those in it are
 // appended (key, index) to the segment's boundary buffer.
 __global__ void __launch_bounds__(256, 4) long_collect_kernel(Args a) {
+  griddep_wait();
   __shared__ uint32_t wgt[8];
   RangeView v;
   range_view(a, &v);
@@ -1155,6 +1165,7 @@ __global__ void __launch_bounds__(256, 4) long_collect_kernel(Args a) {
 constexpr uint32_t kExactThreads = 1024;
 
 __global__ void __launch_bounds__(kExactThreads) long_exact_kernel(Args a) {
+  griddep_wait();
   extern __shared__ __align__(16) uint32_t dyn[];
   uint32_t* skey = dyn;                     // [kBoundCap]
   uint32_t* sidx = skey + kBoundCap;        // [kBoundCap]
@@ -1280,6 +1291,7 @@ __global__ void __launch_bounds__(kExactThreads) long_exact_kernel(Args a) {
 // the index is the output or the restore address) and holds them between
 // the count and the write; any beyond are read again.
 __global__ void __launch_bounds__(256) long_write_kernel(Args a) {
+  griddep_wait();
   __shared__ uint32_t wcnt[8];
   __shared__ uint32_t wbase[8];
   __shared__ uint32_t roff;
@@ -1364,6 +1376,7 @@ __global__ void __launch_bounds__(256) long_write_kernel(Args a) {
 // candidate the stream pass stored (and zeroed in the residual) gets its acc
 // back, so the residual holds acc over the whole segment again.
 __global__ void __launch_bounds__(256) long_restore_kernel(Args a) {
+  griddep_wait();
   {  // most segments did not fall back: look at the mode before the range's records
     const uint32_t ls = a.range_map[blockIdx.x % a.nranges] >> 16;
     if (a.lsel[(uint64_t)(blockIdx.x / a.nranges) * a.nlong + ls].mode != kModeFallback) return;
@@ -1504,6 +1517,7 @@ __device__ void select_raw(const Args& a, RawShared& sh, cg::cluster_group& clus
 // mode 0: the layer-sized segments on the to-do list, one CTA each (grid-
 // stride); mode 1: the long segments in fallback mode, one cluster each.
 __global__ void __launch_bounds__(kRawThreads) topk_select_raw_kernel(Args a, int mode) {
+  griddep_wait();
   __shared__ RawShared sh;
   cg::cluster_group cluster = cg::this_cluster();
   if (mode == 0) {
@@ -1757,11 +1771,11 @@ int launch_topk(const Plan& q, const float* grad, float* residual, uint32_t* out
   {
     const uint64_t items = q.nchunk + (uint64_t)q.P * q.nseg + (uint64_t)q.P * q.nlong * (kBins + 1) +
                            (uint64_t)q.P;
-    topk_init_kernel<<<(unsigned)std::min<uint64_t>((items + 255) / 256, 4 * 152), 256, 0, s>>>(a);
+    launch_pdl(topk_init_kernel, (unsigned)std::min<uint64_t>((items + 255) / 256, 4 * 152), 256, 0, s, a);
     ++launches;
   }
   if (q.n_cta) {
-    topk_guess_cta_kernel<<<(unsigned)((uint64_t)q.P * q.n_cta), kGuessThreads, 0, s>>>(
+    launch_pdl(topk_guess_cta_kernel, (unsigned)((uint64_t)q.P * q.n_cta), kGuessThreads, 0, s,
         a, q.n_cta);
     ++launches;
   }
@@ -1783,7 +1797,7 @@ int launch_topk(const Plan& q, const float* grad, float* residual, uint32_t* out
   }
   if (q.n_warp) {
     const uint64_t warps = (uint64_t)q.P * q.n_warp, wpc = kGuessThreads / 32;
-    topk_guess_warp_kernel<<<(unsigned)((warps + wpc - 1) / wpc), kGuessThreads, 0, s>>>(a, q.n_warp);
+    launch_pdl(topk_guess_warp_kernel, (unsigned)((warps + wpc - 1) / wpc), kGuessThreads, 0, s, a, q.n_warp);
     ++launches;
   }
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
@@ -1792,37 +1806,37 @@ int launch_topk(const Plan& q, const float* grad, float* residual, uint32_t* out
     const unsigned grid = (unsigned)((uint64_t)q.P * q.nchunk);
     // (the compiler drops the long-segment path from tables without one)
     if (q.u_L && q.nlong)
-      topk_stream_kernel<true, true><<<grid, kStreamThreads, 0, s>>>(a);
+      launch_pdl(topk_stream_kernel<true, true>, grid, kStreamThreads, 0, s, a);
     else if (q.u_L)
-      topk_stream_kernel<true, false><<<grid, kStreamThreads, 0, s>>>(a);
+      launch_pdl(topk_stream_kernel<true, false>, grid, kStreamThreads, 0, s, a);
     else if (q.nlong)
-      topk_stream_kernel<false, true><<<grid, kStreamThreads, 0, s>>>(a);
+      launch_pdl(topk_stream_kernel<false, true>, grid, kStreamThreads, 0, s, a);
     else
-      topk_stream_kernel<false, false><<<grid, kStreamThreads, 0, s>>>(a);
+      launch_pdl(topk_stream_kernel<false, false>, grid, kStreamThreads, 0, s, a);
     ++launches;
   }
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   mark(2);
   if (q.n_short) {
-    topk_select_short_kernel<<<(unsigned)((uint64_t)q.P * q.n_short), kSegThreads, 0, s>>>(
+    launch_pdl(topk_select_short_kernel, (unsigned)((uint64_t)q.P * q.n_short), kSegThreads, 0, s,
         a, q.n_short);
-    topk_select_raw_kernel<<<(unsigned)std::min<uint64_t>((uint64_t)q.P * q.n_short, 2 * 152),
-                             kRawThreads, 0, s>>>(a, 0);
+    launch_pdl(topk_select_raw_kernel, (unsigned)std::min<uint64_t>((uint64_t)q.P * q.n_short, 2 * 152),
+                             kRawThreads, 0, s, a, 0);
     launches += 2;
     if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   }
   if (q.nlong) {
     const unsigned pl = (unsigned)((uint64_t)q.P * q.nlong);
     const unsigned pr = (unsigned)((uint64_t)q.P * q.nranges);
-    long_hist_kernel<<<pr, 256, 0, s>>>(a);
-    long_find_kernel<<<pl, 256, 0, s>>>(a);
-    long_collect_kernel<<<pr, 256, 0, s>>>(a);
+    launch_pdl(long_hist_kernel, pr, 256, 0, s, a);
+    launch_pdl(long_find_kernel, pl, 256, 0, s, a);
+    launch_pdl(long_collect_kernel, pr, 256, 0, s, a);
     const size_t smem = (2 * (size_t)kBoundCap + kMaxRanges + 2048) * sizeof(uint32_t);
     if (!ensure_smem(reinterpret_cast<const void*>(long_exact_kernel), smem))
       return SPARCML_ERR_CUDA;
-    long_exact_kernel<<<pl, kExactThreads, smem, s>>>(a);
-    long_write_kernel<<<pr, 256, 0, s>>>(a);
-    long_restore_kernel<<<pr, 256, 0, s>>>(a);
+    launch_pdl(long_exact_kernel, pl, kExactThreads, smem, s, a);
+    launch_pdl(long_write_kernel, pr, 256, 0, s, a);
+    launch_pdl(long_restore_kernel, pr, 256, 0, s, a);
     launches += 6;
     if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
