@@ -18,8 +18,9 @@
 //              overwhelming probability, at least k_s keys of the whole
 //              segment are >= G (certainly so for a fully sampled segment).
 //              Long segments also get a histogram scale from a second, higher
-//              sample quantile, and a mid guess Gm: the sample's estimate of
-//              the k-th key itself.
+//              sample quantile, and a mid guess Gm of the k-th key itself:
+//              the segment's k-th key in the last call made with the same
+//              workspace, else the sample's estimate.
 //  3. stream   the HBM-bound pass (one CTA per 8,192-entry chunk of a
 //              segment): reads grad and residual once with 128-bit loads
 //              aligned on the element grid, writes acc back into residual,
@@ -114,8 +115,8 @@ static_assert(sizeof(ChunkDesc) == 32, "chunk descriptor layout");
 enum : uint32_t { kModeNormal = 0, kModeFallback = 1 };
 struct LongSel {
   uint32_t mode, bin, rank, T, cut, overflow;
-  uint32_t mid;  // the sample's estimate of T: the stream pass zeroes candidates at or above it
-  uint32_t pad;
+  uint32_t mid;  // the stream pass zeroes stored candidates at or above it
+  uint32_t sig;  // signature of the segment whose T this record holds (kept across calls)
 };
 
 struct UploadBatch {
@@ -373,6 +374,12 @@ __global__ void __launch_bounds__(kGuessThreads) topk_guess_cta_kernel(Args a, u
 // largest sample key with its low 15 bits cleared, found as two radix digits
 // (bits 30..20, then 19..15) from histograms summed over the cluster through
 // distributed shared memory; the histogram anchor likewise with its rank.
+// A long segment's signature (its begin, length and k), kept beside its T so
+// that a later call with the same workspace and segment can start from it.
+__device__ __forceinline__ uint32_t seg_signature(const SegRec& r) {
+  return ((r.begin * 0x85ebca6bu) ^ (r.n * 0xc2b2ae35u) ^ (r.k * 0x27d4eb2fu)) | 1u;
+}
+
 __device__ __forceinline__ void warp_find_from_top32(const uint32_t* tot, uint32_t r,
                                                      uint32_t* bin) {
   // lanes hold bins 31 - lane (high to low); the bin where the count from the top reaches r
@@ -481,7 +488,12 @@ __global__ void __launch_bounds__(kGuessThreads) topk_guess_long_kernel(Args a) 
     const uint32_t G = (pick[0] << 20) | (pick2[0] << 15);
     const uint32_t anchor = (pick[2] << 20) | (pick2[1] << 15);
     a.guess[(uint64_t)p * a.nseg + s] = make_uint2(G, hist_shift(G, anchor));
-    a.lsel[(uint64_t)p * a.nlong + item % a.nlong].mid = (pick[4] << 20) | (pick2[2] << 15);
+    // The zeroing threshold: the k-th key T of this segment in the last call
+    // made with this workspace, if the record holds one (in error-feedback
+    // training T moves little from step to step), else the sample's estimate.
+    // It only decides which candidates the stream pass zeroes early.
+    LongSel& L = a.lsel[(uint64_t)p * a.nlong + item % a.nlong];
+    L.mid = L.sig == seg_signature(r) ? L.T : (pick[4] << 20) | (pick2[2] << 15);
   }
 }
 
@@ -703,7 +715,7 @@ __global__ void __launch_bounds__(kStreamThreads, ANY_LONG ? 2 : 3) topk_stream_
   const uint64_t sub = (uint64_t)gc * kWarpsPerChunk + warp;
   const uint64_t slot0 = (uint64_t)p * a.node_slots + (uint64_t)slot32 * 32 + (uint64_t)warp * slot;
   // Long segments: the stream pass writes +0.0f for every candidate it stores
-  // at or above the mid guess Gm (the sample's estimate of T), and the select
+  // at or above the mid guess Gm (an estimate of T), and the select
   // then zeroes the kept candidates below Gm and restores acc at the stored
   // ones at or above it that are not kept: few scattered writes, where
   // zeroing every kept candidate afterwards would scatter k of them.
@@ -1279,6 +1291,7 @@ __global__ void __launch_bounds__(kExactThreads) long_exact_kernel(Args a) {
     } else {
       L.T = T;
       L.cut = cut;
+      L.sig = seg_signature(r);
     }
   }
 }
