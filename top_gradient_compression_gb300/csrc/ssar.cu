@@ -168,10 +168,47 @@ __device__ uint32_t chunk_lookback(const StageArgs& s, uint64_t slot0, uint32_t 
   return excl;
 }
 
+// Stages entries [off, off + len) of a stage's input (idx and val buffers of
+// `total` entries) into shared memory, 16 bytes at a time from the 16-byte
+// boundary at or below `off` when both buffers are 16-byte aligned (`vec`);
+// a quad that would pass the buffers' end is copied entry by entry. Returns
+// the position in shared memory of entry `off`. Asynchronous: the caller
+// waits for the copies.
+__device__ __forceinline__ uint32_t stage_range(uint32_t* sdst_i, float* sdst_v, const uint32_t* gi,
+                                                const float* gv, uint64_t off, uint32_t len,
+                                                uint64_t total, bool vec) {
+  if (!vec) {
+    for (uint32_t x = threadIdx.x; x < len; x += blockDim.x) {
+      cp_async4(&sdst_i[x], gi + off + x);
+      cp_async4(&sdst_v[x], gv + off + x);
+    }
+    return 0;
+  }
+  const uint32_t head = (uint32_t)(off & 3);
+  const uint64_t q0 = off - head;
+  const uint32_t nq = (head + len + 3) / 4;
+  for (uint32_t k = threadIdx.x; k < nq; k += blockDim.x) {
+    const uint64_t e = q0 + 4ull * k;
+    if (e + 4 <= total) {
+      cp_async16(&sdst_i[4 * k], gi + e);
+      cp_async16(&sdst_v[4 * k], gv + e);
+    } else {
+      for (uint32_t u = 0; u < 4; ++u)
+        if (e + u < total) {
+          cp_async4(&sdst_i[4 * k + u], gi + e + u);
+          cp_async4(&sdst_v[4 * k + u], gv + e + u);
+        }
+    }
+  }
+  return head;
+}
+
 __global__ void __launch_bounds__(kMergeThreads) ssar_merge_kernel(StageArgs s) {
   griddep_wait();
-  __shared__ uint32_t sa_idx[kChunk + 2], sb_idx[kChunk + 2];
-  __shared__ float sa_val[kChunk + 2], sb_val[kChunk + 2];
+  // a range of at most kChunk + 1 entries, staged from the 16-byte boundary
+  // at or below its start (up to 3 entries before it, 3 after)
+  __shared__ __align__(16) uint32_t sa_idx[kChunk + 8], sb_idx[kChunk + 8];
+  __shared__ __align__(16) float sa_val[kChunk + 8], sb_val[kChunk + 8];
   __shared__ uint32_t scratch[34];
   __shared__ uint32_t bc[2];
   const uint32_t t = threadIdx.x;
@@ -189,25 +226,28 @@ __global__ void __launch_bounds__(kMergeThreads) ssar_merge_kernel(StageArgs s) 
   const uint32_t la = i1 > i0 ? min(i1 - i0, kChunk + 1) : 0u;  // bounds kept for bad streams
   const uint32_t lb = j1 > j0 ? min(j1 - j0, kChunk + 1) : 0u;
   // stage both sub-ranges with asynchronous copies: every load in flight at once
-  for (uint32_t x = t; x < la; x += blockDim.x) {
-    cp_async4(&sa_idx[x], q.a_idx + i0 + x);
-    cp_async4(&sa_val[x], q.a_val + i0 + x);
-  }
-  for (uint32_t x = t; x < lb; x += blockDim.x) {
-    cp_async4(&sb_idx[x], q.b_idx + j0 + x);
-    cp_async4(&sb_val[x], q.b_val + j0 + x);
-  }
+  const uint64_t in_total = 2ull * s.G * s.cap_in;  // entries of the stage's input buffers
+  const bool vec = ((reinterpret_cast<uintptr_t>(s.in_idx) | reinterpret_cast<uintptr_t>(s.in_val)) &
+                    15) == 0;
+  const uint32_t ha = stage_range(sa_idx, sa_val, s.in_idx, s.in_val,
+                                  (uint64_t)(2 * g) * s.cap_in + i0, la, in_total, vec);
+  const uint32_t hb = stage_range(sb_idx, sb_val, s.in_idx, s.in_val,
+                                  (uint64_t)(2 * g + 1) * s.cap_in + j0, lb, in_total, vec);
   cp_async_wait_all();
   __syncthreads();
+  const uint32_t* A_idx = sa_idx + ha;  // A_idx[x] = entry i0 + x of A
+  const float* A_val = sa_val + ha;
+  const uint32_t* B_idx = sb_idx + hb;
+  const float* B_val = sb_val + hb;
   if (s.validate) {  // strictly ascending streams with indices < N
     for (uint32_t x = t; x < la; x += blockDim.x) {
-      const uint32_t prev = x > 0 ? sa_idx[x - 1] : (i0 > 0 ? q.a_idx[i0 - 1] : 0u);
-      if (sa_idx[x] >= s.N || ((x > 0 || i0 > 0) && sa_idx[x] <= prev))
+      const uint32_t prev = x > 0 ? A_idx[x - 1] : (i0 > 0 ? q.a_idx[i0 - 1] : 0u);
+      if (A_idx[x] >= s.N || ((x > 0 || i0 > 0) && A_idx[x] <= prev))
         set_status(s.status, SPARCML_ERR_BAD_STREAM);
     }
     for (uint32_t x = t; x < lb; x += blockDim.x) {
-      const uint32_t prev = x > 0 ? sb_idx[x - 1] : (j0 > 0 ? q.b_idx[j0 - 1] : 0u);
-      if (sb_idx[x] >= s.N || ((x > 0 || j0 > 0) && sb_idx[x] <= prev))
+      const uint32_t prev = x > 0 ? B_idx[x - 1] : (j0 > 0 ? q.b_idx[j0 - 1] : 0u);
+      if (B_idx[x] >= s.N || ((x > 0 || j0 > 0) && B_idx[x] <= prev))
         set_status(s.status, SPARCML_ERR_BAD_STREAM);
     }
   }
@@ -217,10 +257,10 @@ __global__ void __launch_bounds__(kMergeThreads) ssar_merge_kernel(StageArgs s) 
     uint32_t lo = d > lb ? d - lb : 0u, hi = min(d, la);
     while (lo < hi) {
       const uint32_t mid = (lo + hi) >> 1;
-      if (sa_idx[mid] <= sb_idx[d - 1 - mid]) lo = mid + 1; else hi = mid;
+      if (A_idx[mid] <= B_idx[d - 1 - mid]) lo = mid + 1; else hi = mid;
     }
     uint32_t b = d - lo;
-    if (lo > 0 && b < lb && sa_idx[lo - 1] == sb_idx[b]) ++b;
+    if (lo > 0 && b < lb && A_idx[lo - 1] == B_idx[b]) ++b;
     *oa = lo;
     *ob = b;
   };
@@ -241,17 +281,17 @@ __global__ void __launch_bounds__(kMergeThreads) ssar_merge_kernel(StageArgs s) 
       okey[u] = 0;
       oval[u] = 0.0f;
       if (ia < a1 || ib < b1) {  // once false, false for the rest of the walk
-        if (ib >= b1 || (ia < a1 && sa_idx[ia] < sb_idx[ib])) {
-          okey[u] = sa_idx[ia];
-          oval[u] = __fadd_rn(0.0f, sa_val[ia]);
+        if (ib >= b1 || (ia < a1 && A_idx[ia] < B_idx[ib])) {
+          okey[u] = A_idx[ia];
+          oval[u] = __fadd_rn(0.0f, A_val[ia]);
           ++ia;
-        } else if (ia >= a1 || sb_idx[ib] < sa_idx[ia]) {
-          okey[u] = sb_idx[ib];
-          oval[u] = __fadd_rn(0.0f, sb_val[ib]);
+        } else if (ia >= a1 || B_idx[ib] < A_idx[ia]) {
+          okey[u] = B_idx[ib];
+          oval[u] = __fadd_rn(0.0f, B_val[ib]);
           ++ib;
         } else {  // the same index in A and B: (+0 + a) + b
-          okey[u] = sa_idx[ia];
-          oval[u] = __fadd_rn(__fadd_rn(0.0f, sa_val[ia]), sb_val[ib]);
+          okey[u] = A_idx[ia];
+          oval[u] = __fadd_rn(__fadd_rn(0.0f, A_val[ia]), B_val[ib]);
           ++ia;
           ++ib;
         }
