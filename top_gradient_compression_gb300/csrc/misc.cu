@@ -237,14 +237,14 @@ extern "C" int sparcml_pack(const float* x, int32_t P, uint64_t N, float thr, ui
   uint32_t* chunk_off = reinterpret_cast<uint32_t*>(w + 256 + pack_chunk_array_bytes(P, N));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const unsigned grid = (unsigned)((uint64_t)P * nchunk);
-  launch_pdl(pack_chunk_kernel<false>, grid, kPackThreads, 0, s, x, N, (uint32_t)nchunk, thr, chunk_cnt,
-                                                         nullptr, nullptr, nullptr, cap);
+  launch_pdl(pack_chunk_kernel<false>, grid, kPackThreads, 0, s, x, N, (uint32_t)nchunk, thr,
+             chunk_cnt, nullptr, nullptr, nullptr, cap);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
-  launch_pdl(pack_scan_kernel, (unsigned)P, 1024, 0, s, chunk_cnt, (uint32_t)nchunk, chunk_off, out_nnz,
-                                                cap, status);
+  launch_pdl(pack_scan_kernel, (unsigned)P, 1024, 0, s, chunk_cnt, (uint32_t)nchunk, chunk_off,
+             out_nnz, cap, status);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
-  launch_pdl(pack_chunk_kernel<true>, grid, kPackThreads, 0, s, x, N, (uint32_t)nchunk, thr, chunk_cnt,
-                                                        chunk_off, out_idx, out_val, cap);
+  launch_pdl(pack_chunk_kernel<true>, grid, kPackThreads, 0, s, x, N, (uint32_t)nchunk, thr,
+             chunk_cnt, chunk_off, out_idx, out_val, cap);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   note_launches(3);
   return SPARCML_OK;
@@ -281,7 +281,8 @@ extern "C" int sparcml_check_finite(const float* x, uint64_t n, int32_t* status,
   const uint64_t mis = (reinterpret_cast<uintptr_t>(x) & 15u) / 4u;
   const uint64_t head = std::min<uint64_t>(n, mis ? 4 - mis : 0);
   const unsigned grid = (unsigned)std::min<uint64_t>((n / 4 + 255) / 256 + 1, 152u * 8u);
-  launch_pdl(check_finite_kernel, grid, 256, 0, static_cast<cudaStream_t>(stream), x, n, head, status);
+  launch_pdl(check_finite_kernel, grid, 256, 0, static_cast<cudaStream_t>(stream), x, n, head,
+             status);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   note_launches(1);
   return SPARCML_OK;

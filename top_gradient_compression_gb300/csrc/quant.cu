@@ -247,14 +247,14 @@ int launch_quantize(const uint32_t* idx, const float* val, const uint32_t* nnz, 
   const bool vec = (bucket == 512 || bucket == 1024) && cap % 4 == 0 &&
                    (reinterpret_cast<uintptr_t>(val) & 15) == 0;
   if (vec && bucket == 512)
-    launch_pdl(quantize_scale_vec_kernel<4>, (unsigned)blocks, kQuantThreads, 0, s,
-        val, nnz, P, cap, (uint32_t)nbk, scales, nbk, status);
+    launch_pdl(quantize_scale_vec_kernel<4>, (unsigned)blocks, kQuantThreads, 0, s, val, nnz, P,
+               cap, (uint32_t)nbk, scales, nbk, status);
   else if (vec)
-    launch_pdl(quantize_scale_vec_kernel<8>, (unsigned)blocks, kQuantThreads, 0, s,
-        val, nnz, P, cap, (uint32_t)nbk, scales, nbk, status);
+    launch_pdl(quantize_scale_vec_kernel<8>, (unsigned)blocks, kQuantThreads, 0, s, val, nnz, P,
+               cap, (uint32_t)nbk, scales, nbk, status);
   else
-    launch_pdl(quantize_scale_kernel, (unsigned)blocks, kQuantThreads, 0, s,
-        val, nnz, P, cap, bucket, (uint32_t)nbk, scales, nbk, status);
+    launch_pdl(quantize_scale_kernel, (unsigned)blocks, kQuantThreads, 0, s, val, nnz, P, cap,
+               bucket, (uint32_t)nbk, scales, nbk, status);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   const uint32_t shift = (bucket & (bucket - 1)) == 0 ? (uint32_t)__builtin_ctz(bucket) : 32u;
   const uint64_t code_words = (code_stride + 3) / 4;
@@ -263,14 +263,14 @@ int launch_quantize(const uint32_t* idx, const float* val, const uint32_t* nnz, 
                 (unsigned)P);
   const uint32_t cs = (uint32_t)code_stride;
   if (bits == 2)
-    launch_pdl(quantize_encode_kernel<2>, eg, kQuantThreads, 0, s, idx, val, nnz, cap, shift, bucket,
-                                                            seed, codes, scales, err_out, cs, nbk);
+    launch_pdl(quantize_encode_kernel<2>, eg, kQuantThreads, 0, s, idx, val, nnz, cap, shift,
+               bucket, seed, codes, scales, err_out, cs, nbk);
   else if (bits == 4)
-    launch_pdl(quantize_encode_kernel<4>, eg, kQuantThreads, 0, s, idx, val, nnz, cap, shift, bucket,
-                                                            seed, codes, scales, err_out, cs, nbk);
+    launch_pdl(quantize_encode_kernel<4>, eg, kQuantThreads, 0, s, idx, val, nnz, cap, shift,
+               bucket, seed, codes, scales, err_out, cs, nbk);
   else
-    launch_pdl(quantize_encode_kernel<8>, eg, kQuantThreads, 0, s, idx, val, nnz, cap, shift, bucket,
-                                                            seed, codes, scales, err_out, cs, nbk);
+    launch_pdl(quantize_encode_kernel<8>, eg, kQuantThreads, 0, s, idx, val, nnz, cap, shift,
+               bucket, seed, codes, scales, err_out, cs, nbk);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   note_launches(2);
   return SPARCML_OK;
@@ -289,17 +289,14 @@ int launch_dequantize(const uint8_t* codes, const float* scales, const uint32_t*
   const uint64_t scale_stride = (cap + bucket - 1) / bucket;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (bits == 2)
-    launch_pdl(dequantize_kernel<2>, blocks, kQuantThreads, 0, s, codes, scales, nnz, P, cap, bucket,
-                                                          code_stride, scale_stride, val_out,
-                                                          status);
+    launch_pdl(dequantize_kernel<2>, blocks, kQuantThreads, 0, s, codes, scales, nnz, P, cap,
+               bucket, code_stride, scale_stride, val_out, status);
   else if (bits == 4)
-    launch_pdl(dequantize_kernel<4>, blocks, kQuantThreads, 0, s, codes, scales, nnz, P, cap, bucket,
-                                                          code_stride, scale_stride, val_out,
-                                                          status);
+    launch_pdl(dequantize_kernel<4>, blocks, kQuantThreads, 0, s, codes, scales, nnz, P, cap,
+               bucket, code_stride, scale_stride, val_out, status);
   else
-    launch_pdl(dequantize_kernel<8>, blocks, kQuantThreads, 0, s, codes, scales, nnz, P, cap, bucket,
-                                                          code_stride, scale_stride, val_out,
-                                                          status);
+    launch_pdl(dequantize_kernel<8>, blocks, kQuantThreads, 0, s, codes, scales, nnz, P, cap,
+               bucket, code_stride, scale_stride, val_out, status);
   if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
   note_launches(1);
   return SPARCML_OK;
