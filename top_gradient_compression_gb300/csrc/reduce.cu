@@ -157,11 +157,13 @@ __device__ __forceinline__ float load_value(const ReduceArgs& a, uint32_t p, uin
       level = code & 1u;
       q = (float)level;
     }
-    if (level == 0) return 0.0f;
+    // The scale is read whatever the level (j < cap keeps it inside the
+    // node's ceil(cap / bucket) scales), so its load does not wait for the
+    // code's; a zero level then gives +0.0f by a select.
     const uint32_t b = a.bucket_shift < 32 ? j >> a.bucket_shift : j / a.bucket;
     const float scale = a.scales[(uint64_t)p * a.scale_stride + b];
     const float v = __fmul_rn(q, scale);
-    return (code >> (a.bits - 1)) ? -v : v;
+    return level == 0 ? 0.0f : (code >> (a.bits - 1)) ? -v : v;
   }
 }
 
@@ -622,7 +624,7 @@ reduce_dense_tile_kernel(ReduceArgs a) {
 constexpr uint32_t kMini = 1024;
 constexpr uint32_t kMiniShift = 10;
 constexpr uint32_t kMiniWords = kMini / 32;
-constexpr uint32_t kMiniRounds = 8;
+constexpr uint32_t kMiniRounds = 6;
 constexpr int32_t kMiniMaxP = 64;
 constexpr uint32_t kMiniWarps = 4;  // mini-tiles per CTA
 // Dense-first warp tiles with more entries than max(kHot, kHotRatio x the
@@ -637,6 +639,12 @@ constexpr uint64_t kHotGrid = 4 * 152;  // CTAs of the hot launch: the GPU's 152
 constexpr uint32_t kAccWords = kMini;
 constexpr uint32_t kMiniWarpWords = (kAccWords + 3 * kMiniMaxP + 1 + 31) / 32 * 32;
 static_assert(kMiniWarpWords % 4 == 0, "uint4 access to each warp's accumulator");
+// The scalar warp tile's per-warp region sized for the launch's P (the
+// accumulator, lo[P] and cpre[P + 1], a multiple of 4 words): at P = 16 ten
+// CTAs fit an SM's shared memory, against nine at the largest P.
+__host__ __device__ __forceinline__ uint32_t mini_warp_words(int32_t P) {
+  return kAccWords + ((2u * (uint32_t)P + 1u + 3u) & ~3u);
+}
 constexpr uint32_t kAbsent = 0xffffffffu;
 
 // Split table of the warp tiles by one streaming pass over every node's
@@ -1044,10 +1052,11 @@ __device__ __forceinline__ float load_value_lut(const ReduceArgs& a, uint32_t p,
                                                 const float* lut) {
   if (a.bits != 4) return load_value<true>(a, p, j);  // uniform branch
   const uint8_t byte = a.codes[(uint64_t)p * a.code_stride + (j >> 1)];
-  const uint32_t code = (j & 1) ? (byte >> 4) : (byte & 15u);
-  if ((code & 7u) == 0) return 0.0f;
   const uint32_t b = a.bucket_shift < 32 ? j >> a.bucket_shift : j / a.bucket;
-  return __fmul_rn(lut[code], a.scales[(uint64_t)p * a.scale_stride + b]);
+  const float scale = a.scales[(uint64_t)p * a.scale_stride + b];  // not behind the code
+  const uint32_t code = (j & 1) ? (byte >> 4) : (byte & 15u);
+  const float v = __fmul_rn(lut[code], scale);
+  return (code & 7u) == 0 ? 0.0f : v;
 }
 
 template <bool Q4>
@@ -1135,21 +1144,17 @@ reduce_mini_kernel(ReduceArgs a) {
   __shared__ float lut[16];
   __shared__ uint8_t tags[kMiniWarps][kMini];
   __shared__ uint32_t bmw[kMiniWarps][kMiniWords];  // presence bits, set as entries are folded
-  if constexpr (Q4) {
-    init_level_table(lut);
-    __syncthreads();
-  }
-  const uint32_t m = mini_tile_of_warp(a, LB, sh);
-  if constexpr (!LB) {
-    if (m >= a.ntiles) return;  // warp-uniform
-  }
-  const bool active = m < a.ntiles;
-  uint32_t* acc = dyn + warp * kMiniWarpWords;        // [kMini] float bits
+  __shared__ uint32_t tk;                            // the CTA's ticket (sparse-first)
+  // Sparse-first: the CTA's group of tiles is claimed by ticket (so every
+  // group waited on is already running); the ticket is in flight while the
+  // level table and the accumulators are initialised. Dense-first: the tile
+  // is the warp's grid position.
+  uint32_t ticket = 0;
+  if (LB && threadIdx.x == 0) ticket = atomicAdd(a.ticket, 1u);
+  if constexpr (Q4) init_level_table(lut);
+  uint32_t* acc = dyn + warp * mini_warp_words(a.P);  // [kMini] float bits
   uint32_t* lo = acc + kAccWords;                      // [P] first entry in the tile
-  uint32_t* cpre = lo + kMiniMaxP;                     // [P + 1] first position
-  const uint32_t tile_lo = m * kMini;
-  const uint32_t tile_n = min(kMini, a.N - tile_lo);
-  const float e = op_neutral(kop);
+  uint32_t* cpre = lo + a.P;                           // [P + 1] first position
   // Absent indices hold kAbsent, a NaN that neither the sum (the GPU's NaN
   // results are 0x7fffffff) nor max/min (a NaN value never replaces the
   // partial result) ever leaves there: presence needs no bitmap. Bitwise or
@@ -1158,6 +1163,16 @@ reduce_mini_kernel(ReduceArgs a) {
   for (uint32_t i = 0; i < kMini / 128; ++i)
     reinterpret_cast<uint4*>(acc)[i * 32 + lane] = make_uint4(kAbsent, kAbsent, kAbsent, kAbsent);
   bmw[warp][lane] = 0;
+  if (LB && threadIdx.x == 0) tk = ticket;
+  if (LB || Q4) __syncthreads();
+  const uint32_t m = (LB ? tk : blockIdx.x) * kMiniWarps + warp;
+  if constexpr (!LB) {
+    if (m >= a.ntiles) return;  // warp-uniform
+  }
+  const bool active = m < a.ntiles;
+  const uint32_t tile_lo = m * kMini;
+  const uint32_t tile_n = min(kMini, a.N - tile_lo);
+  const float e = op_neutral(kop);
   uint32_t c[2] = {0, 0};
 #pragma unroll
   for (uint32_t q = 0; q < 2; ++q) {
@@ -1823,10 +1838,11 @@ int launch_reduce(ReduceArgs a, void* ws, size_t ws_bytes, cudaStream_t s,
       launch_pdl(reduce_split_stream_kernel, dim3(gx, (unsigned)a.P), 256, 0, s,
           a.idx, a.nnz, a.P, a.cap, a.N, a.ntiles, split, a.status);
     if (launch_status() != SPARCML_OK) return SPARCML_ERR_CUDA;
-    const size_t smem = (size_t)kMiniWarps * kMiniWarpWords * sizeof(uint32_t);
     const unsigned grid = (a.ntiles + kMiniWarps - 1) / kMiniWarps;
     const bool vec = !Q4 && (reinterpret_cast<uintptr_t>(a.idx) & 15) == 0 &&
                      (reinterpret_cast<uintptr_t>(a.val) & 15) == 0;
+    const size_t smem =
+        (size_t)kMiniWarps * (vec ? kMiniWarpWords : mini_warp_words(a.P)) * sizeof(uint32_t);
     // A possibly dense result (P * cap >= N / 4) is written dense-first; else
     // sparse-first with look-back and a fix-up if the union crosses after all.
     const bool lb = 4.0 * (double)a.P * (double)a.cap < (double)a.N;
