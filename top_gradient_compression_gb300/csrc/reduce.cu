@@ -943,11 +943,16 @@ __device__ __forceinline__ uint32_t presence_word(const uint32_t* acc) {
   return word;
 }
 
-// `word`: the lane's presence word (0 for a tile past the end).
+// `word`: the lane's presence word (0 for a tile past the end). `stage`
+// (optional, kMini / 2 entries of the warp's own shared memory): a sparse
+// tile of at most that many entries stages its offsets in order there and
+// is written 32 consecutive entries at a time; otherwise each lane writes
+// its word's entries.
 __device__ __forceinline__ void mini_epilogue_lookback(const ReduceArgs& a, uint32_t m,
                                                        const uint32_t* acc, bool active,
                                                        uint32_t* sh /* [kMiniWarps + 1] */,
-                                                       uint32_t word) {
+                                                       uint32_t word,
+                                                       uint16_t* stage = nullptr) {
   const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
   const uint32_t wincl = warp_incl_sum(__popc(word));
   const uint32_t count = __shfl_sync(0xffffffffu, wincl, 31);
@@ -971,6 +976,19 @@ __device__ __forceinline__ void mini_epilogue_lookback(const ReduceArgs& a, uint
     float* od = a.out_dense + tile_lo;
     for (uint32_t x = lane; x < tile_n; x += 32)
       od[x] = acc[x] == kAbsent ? op_neutral(a.op) : __uint_as_float(acc[x]);
+  } else if (stage != nullptr && count <= kMini / 2) {  // warp-uniform
+    uint32_t pos = wincl - __popc(word);
+    uint32_t bits = word;
+    while (bits) {
+      stage[pos++] = (uint16_t)(lane * 32 + (__ffs(bits) - 1));
+      bits &= bits - 1;
+    }
+    __syncwarp();
+    for (uint32_t o = lane; o < count; o += 32) {
+      const uint32_t x = stage[o];
+      a.out_idx[excl + o] = tile_lo + x;
+      a.out_val[excl + o] = __uint_as_float(acc[x]);
+    }
   } else {
     uint32_t pos = excl + wincl - __popc(word);  // entries before word `lane`
     uint32_t bits = word;
@@ -1142,7 +1160,8 @@ reduce_mini_kernel(ReduceArgs a) {
   const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
   __shared__ uint32_t sh[kMiniWarps + 1];
   __shared__ float lut[16];
-  __shared__ uint8_t tags[kMiniWarps][kMini];
+  // repeat tags while folding; then the staged offsets of a sparse tile
+  __shared__ __align__(16) uint8_t tags[kMiniWarps][kMini];
   __shared__ uint32_t bmw[kMiniWarps][kMiniWords];  // presence bits, set as entries are folded
   __shared__ uint32_t tk;                            // the CTA's ticket (sparse-first)
   // Sparse-first: the CTA's group of tiles is claimed by ticket (so every
@@ -1203,7 +1222,9 @@ reduce_mini_kernel(ReduceArgs a) {
   mini_accumulate<Q4>(a, kop, acc, tile_lo, tile_n, lo, cpre, total, e, lut, tags[warp],
                       bmw[warp]);
   __syncwarp();
-  if constexpr (LB) mini_epilogue_lookback(a, m, acc, active, sh, bmw[warp][lane]);
+  if constexpr (LB)
+    mini_epilogue_lookback(a, m, acc, active, sh, bmw[warp][lane],
+                           reinterpret_cast<uint16_t*>(tags[warp]));
   else mini_epilogue(a, m, acc, bmw[warp][lane]);
 }
 
