@@ -1026,6 +1026,7 @@ struct RangeView {
   SegRec rec;
   uint64_t gs, pl;
   uint32_t excl;          // candidates of this lane's sub-chunk before it in the warp
+  uint32_t own;           // candidates of this lane's sub-chunk
   uint32_t count;         // this warp's candidates
   uint64_t slot_base;     // this warp's first sub-slot
 };
@@ -1050,6 +1051,7 @@ __device__ __forceinline__ bool range_view_at(const Args& a, RangeView* v, uint3
   const uint32_t c = w < nsub ? min(a.sub_cnt[sub0 + w], v->rec.slot) : 0u;
   const uint32_t incl = warp_incl_sum(c);
   v->excl = incl - c;
+  v->own = c;
   v->count = __shfl_sync(0xffffffffu, incl, 31);
   v->slot_base = (uint64_t)v->p * a.node_slots + (uint64_t)v->rec.slot32 * 32 +
                  (uint64_t)w0 * v->rec.slot;
@@ -1076,10 +1078,23 @@ __device__ __forceinline__ uint32_t range_off(const RangeView& v, uint32_t x) {
   return i * v.rec.slot + (x - e);
 }
 
+// The same offsets for the warp's first kTab candidates, as a table in
+// shared memory that each lane fills for its own sub-chunk: a candidate
+// x < kTab then takes one shared load instead of the search above.
+constexpr uint32_t kTab = 512;
+__device__ __forceinline__ void range_table(const RangeView& v, uint32_t* tab /* [kTab] */) {
+  const uint32_t lane = lane_id();
+  const uint32_t end = min(v.excl + v.own, kTab);
+  const uint32_t base = lane * v.rec.slot - v.excl;  // offset of x is base + x (mod 2^32)
+  for (uint32_t x = v.excl; x < end; ++x) tab[x] = base + x;
+  __syncwarp();
+}
+
 // Candidates a lane holds in registers at once: a warp's first 512 are all
 // loaded before any is used (a warp of 32 sub-chunks holds about 500 at 1.5 %
 // density); any beyond are taken in further batches.
 constexpr uint32_t kHold = 16;
+static_assert(kTab == 32 * kHold, "the held candidates are the tabled ones");
 
 // Per range: the candidates' bins, (key - G) >> shift (the top bin takes
 // everything above), counted in shared memory and added to the (node,
@@ -1096,12 +1111,16 @@ __global__ void __launch_bounds__(256) long_hist_kernel(Args a) {
   const uint32_t lane = lane_id();
   const uint2 gsh = a.guess[v.gs];
   const float* cv = a.cand_val + v.slot_base;
+  __shared__ uint32_t tabs[kStreamThreads / 32][kTab];
+  uint32_t* tab = tabs[threadIdx.x >> 5];
+  range_table(v, tab);
   for (uint32_t x0 = 0; x0 < v.count; x0 += 32 * kHold) {
     float xv[kHold];
 #pragma unroll
     for (uint32_t u = 0; u < kHold; ++u) {
       const uint32_t x = x0 + u * 32 + lane;
-      const uint32_t o = range_off(v, min(x, v.count - 1));
+      const uint32_t xm = min(x, v.count - 1);
+      const uint32_t o = x0 == 0 ? tab[xm] : range_off(v, xm);  // x0: warp-uniform
       xv[u] = x < v.count ? cv[o] : 0.0f;
     }
 #pragma unroll
@@ -1128,15 +1147,18 @@ __global__ void __launch_bounds__(256, 4) long_collect_kernel(Args a) {
   uint2* bnd = a.bnd + v.pl * kBoundCap;
   const float* cv = a.cand_val + v.slot_base;
   const uint32_t* ci = a.cand_idx + v.slot_base;
+  __shared__ uint32_t tabs[kStreamThreads / 32][kTab];
+  uint32_t* tab = tabs[warp];
+  range_table(v, tab);
   uint32_t gt = 0;
   for (uint32_t x0 = 0; x0 < v.count; x0 += 32 * kHold) {
     float xv[kHold];
-    uint32_t so[kHold];
 #pragma unroll
     for (uint32_t u = 0; u < kHold; ++u) {
       const uint32_t x = x0 + u * 32 + lane;
-      so[u] = range_off(v, min(x, v.count - 1));
-      xv[u] = x < v.count ? cv[so[u]] : 0.0f;
+      const uint32_t xm = min(x, v.count - 1);
+      const uint32_t o = x0 == 0 ? tab[xm] : range_off(v, xm);  // x0: warp-uniform
+      xv[u] = x < v.count ? cv[o] : 0.0f;
     }
 #pragma unroll
     for (uint32_t u = 0; u < kHold; ++u) {
@@ -1148,12 +1170,14 @@ __global__ void __launch_bounds__(256, 4) long_collect_kernel(Args a) {
       const bool inb = x < v.count && b == bstar;
       const uint32_t m = __ballot_sync(0xffffffffu, inb);
       if (m) {
+        const uint32_t xm = min(x, v.count - 1);
+        const uint32_t o = x0 == 0 ? tab[xm] : range_off(v, xm);  // the whole warp
         uint32_t base = 0;
         if (lane == 0) base = atomicAdd(&a.bnd_cnt[v.pl], (uint32_t)__popc(m));
         base = __shfl_sync(0xffffffffu, base, 0);
         if (inb) {
           const uint32_t pos = base + __popc(m & lanemask_lt());
-          if (pos < kBoundCap) bnd[pos] = make_uint2(key, ci[so[u]]);
+          if (pos < kBoundCap) bnd[pos] = make_uint2(key, ci[o]);
           else atomicOr(&a.lsel[v.pl].overflow, 1u);
         }
       }
@@ -1321,12 +1345,14 @@ __global__ void __launch_bounds__(256) long_write_kernel(Args a) {
     const uint32_t key = mag_key(x);
     return valid && (key > T || (key == T && idx <= cut));
   };
+  __shared__ uint32_t tabs[kStreamThreads / 32][kTab];
+  range_table(v, tabs[warp]);
   float xv[kHold];
   uint32_t iv[kHold];
 #pragma unroll
   for (uint32_t u = 0; u < kHold; ++u) {
     const uint32_t x = u * 32 + lane;
-    const uint32_t o = range_off(v, min(x, v.count - 1));
+    const uint32_t o = tabs[warp][min(x, v.count - 1)];
     xv[u] = x < v.count ? cv[o] : 0.0f;
     iv[u] = x < v.count ? ci[o] : 0u;
   }
