@@ -570,8 +570,8 @@ __global__ void __launch_bounds__(kGuessThreads) topk_guess_warp_kernel(Args a, 
 // ---------------------------------------------------------------------------
 // 3. stream: one CTA per (node, chunk). Warp w owns the 1,024 grid positions
 // [q0, q0 + 1024) with q0 = floor4(segment start) + j * kChunk + w * kSub,
-// restricted to the segment: 8 rounds of one float4 per lane, all 16 loads
-// in flight before the first is used. Quads wholly inside the segment use
+// restricted to the segment: 8 rounds of one float4 per lane, in two
+// batches of four whose 8 loads are in flight before the first is used. Quads wholly inside the segment use
 // 128-bit accesses; the segment's ends go entry by entry. UNIFORM (a table of
 // equal segments, the last one possibly shorter): the chunk's segment and
 // place are arithmetic, so the data loads leave at once; otherwise they wait
@@ -637,7 +637,7 @@ __device__ __forceinline__ void load_rounds(float4 (&gv)[NB], float4 (&rv)[NB], 
 }
 
 template <bool UNIFORM, bool ANY_LONG>
-__global__ void __launch_bounds__(kStreamThreads, ANY_LONG ? 2 : 3) topk_stream_kernel(Args a) {
+__global__ void __launch_bounds__(kStreamThreads, 3) topk_stream_kernel(Args a) {
   griddep_wait();
   const uint32_t gc = blockIdx.x;
   const uint32_t p = gc / a.nchunk, c = gc - p * a.nchunk;
@@ -664,11 +664,9 @@ __global__ void __launch_bounds__(kStreamThreads, ANY_LONG ? 2 : 3) topk_stream_
   const int32_t hi_r = (int32_t)max(min((int64_t)hi - (int64_t)q0, (int64_t)kSub + 4), (int64_t)-1);
   const float* gp = a.grad + q0;
   float* rp = a.residual + q0;
-  // The warp's rounds in batches of kBatch whose 128-bit loads are all issued
-  // before any of their entries is used. Tables with long segments keep all
-  // eight rounds in flight (two CTAs per SM); the others take two batches of
-  // four at three CTAs per SM (measured: each is the faster form for its kind).
-  constexpr uint32_t kBatch = ANY_LONG ? kRounds : kRounds / 2;
+  // The warp's rounds in two batches of four whose 128-bit loads are all
+  // issued before any of their entries is used, at three CTAs per SM.
+  constexpr uint32_t kBatch = kRounds / 2;
   float4 gv[kBatch], rv[kBatch];
   load_rounds<kBatch>(gv, rv, 0, gp, rp, lo_r, hi_r, a.vec, lane);
   // the rest of the description, while the data loads are in flight
@@ -693,11 +691,8 @@ __global__ void __launch_bounds__(kStreamThreads, ANY_LONG ? 2 : 3) topk_stream_
     const uint64_t o = (uint64_t)p * a.cap + aux - begin;  // + node-local index
 #pragma unroll
     for (uint32_t t = 0; t < kRounds; ++t) {
-      uint32_t u = t;
-      if constexpr (!ANY_LONG) {
-        u = t % kBatch;
-        if (t > 0 && u == 0) load_rounds<kBatch>(gv, rv, t, gp, rp, lo_r, hi_r, a.vec, lane);
-      }
+      const uint32_t u = t % kBatch;
+      if (t > 0 && u == 0) load_rounds<kBatch>(gv, rv, t, gp, rp, lo_r, hi_r, a.vec, lane);
       const int32_t e0 = (int32_t)(4 * (t * 32 + lane));
       const float av[4] = {__fadd_rn(rv[u].x, gv[u].x), __fadd_rn(rv[u].y, gv[u].y),
                            __fadd_rn(rv[u].z, gv[u].z), __fadd_rn(rv[u].w, gv[u].w)};
@@ -714,11 +709,12 @@ __global__ void __launch_bounds__(kStreamThreads, ANY_LONG ? 2 : 3) topk_stream_
   }
   const uint64_t sub = (uint64_t)gc * kWarpsPerChunk + warp;
   const uint64_t slot0 = (uint64_t)p * a.node_slots + (uint64_t)slot32 * 32 + (uint64_t)warp * slot;
-  // Long segments: the stream pass writes +0.0f for every candidate it stores
-  // at or above the mid guess Gm (an estimate of T), and the select
-  // then zeroes the kept candidates below Gm and restores acc at the stored
-  // ones at or above it that are not kept: few scattered writes, where
-  // zeroing every kept candidate afterwards would scatter k of them.
+  // Long segments: the stream pass writes +0.0f (over the acc just stored)
+  // for every candidate it stores at or above the mid guess Gm (an estimate
+  // of T), and the select then zeroes the kept candidates below Gm and
+  // restores acc at the stored ones at or above it that are not kept: few
+  // scattered writes, where zeroing every kept candidate afterwards would
+  // scatter k of them.
   const bool long_seg = ANY_LONG && kind == kLong;
   const uint32_t Gm = long_seg ? a.lsel[(uint64_t)p * a.nlong + aux].mid : 0u;
   uint32_t* const cidx = a.cand_idx + slot0;  // the warp's sub-slot
@@ -727,11 +723,8 @@ __global__ void __launch_bounds__(kStreamThreads, ANY_LONG ? 2 : 3) topk_stream_
   uint32_t run = 0;  // candidates so far in this sub-chunk (warp-uniform)
 #pragma unroll
   for (uint32_t t = 0; t < kRounds; ++t) {
-    uint32_t u = t;
-    if constexpr (!ANY_LONG) {
-      u = t % kBatch;
-      if (t > 0 && u == 0) load_rounds<kBatch>(gv, rv, t, gp, rp, lo_r, hi_r, a.vec, lane);
-    }
+    const uint32_t u = t % kBatch;
+    if (t > 0 && u == 0) load_rounds<kBatch>(gv, rv, t, gp, rp, lo_r, hi_r, a.vec, lane);
     const int32_t e0 = (int32_t)(4 * (t * 32 + lane));
     float4 acc;
     acc.x = __fadd_rn(rv[u].x, gv[u].x);
@@ -740,61 +733,32 @@ __global__ void __launch_bounds__(kStreamThreads, ANY_LONG ? 2 : 3) topk_stream_
     acc.w = __fadd_rn(rv[u].w, gv[u].w);
     const float av[4] = {acc.x, acc.y, acc.z, acc.w};
     const bool full = a.vec && e0 >= lo_r && e0 + 4 <= hi_r;
-    if (!ANY_LONG) {  // the residual gets acc: stored first, then the candidates
-      uint32_t bits = 0;
-      if (full) {
-        *reinterpret_cast<float4*>(rp + e0) = acc;
-#pragma unroll
-        for (uint32_t q = 0; q < 4; ++q) bits |= (mag_key(av[q]) >= G ? 1u : 0u) << q;
-      } else {
-#pragma unroll
-        for (int32_t q = 0; q < 4; ++q)
-          if (e0 + q >= lo_r && e0 + q < hi_r) {
-            rp[e0 + q] = av[q];
-            bits |= (mag_key(av[q]) >= G ? 1u : 0u) << q;
-          }
-      }
-      if (__ballot_sync(0xffffffffu, bits) == 0) continue;  // warp-uniform
-      uint32_t tot;
-      const uint32_t pos = run + warp_excl_small(__popc(bits), &tot);
-      run += tot;
-      store_candidates(bits, pos, slot, cidx, cval, base_u + (uint32_t)e0, acc, keep);
-      continue;
-    }
-    uint32_t in = 0xfu;  // entries of the quad inside the segment
-    if (!full) {
-      in = 0;
-#pragma unroll
-      for (int32_t q = 0; q < 4; ++q) in |= (e0 + q >= lo_r && e0 + q < hi_r ? 1u : 0u) << q;
-    }
-    uint32_t bits = 0;  // candidates: key >= G
-#pragma unroll
-    for (uint32_t q = 0; q < 4; ++q) bits |= ((in >> q) & (mag_key(av[q]) >= G ? 1u : 0u)) << q;
-    uint32_t zero = 0;  // long segments: stored candidates at or above Gm get +0.0f
-    if (__ballot_sync(0xffffffffu, bits) != 0) {  // warp-uniform
-      uint32_t tot;
-      const uint32_t pos = run + warp_excl_small(__popc(bits), &tot);
-      run += tot;
-      const uint32_t stored =
-          store_candidates(bits, pos, slot, cidx, cval, base_u + (uint32_t)e0, acc, keep);
-      if constexpr (ANY_LONG) {
-        if (long_seg) {
-          uint32_t hi = 0;
-#pragma unroll
-          for (uint32_t q = 0; q < 4; ++q) hi |= (mag_key(av[q]) >= Gm ? 1u : 0u) << q;
-          zero = stored & hi;
-        }
-      }
-    }
-    const float4 w = make_float4(zero & 1u ? 0.0f : acc.x, zero & 2u ? 0.0f : acc.y,
-                                 zero & 4u ? 0.0f : acc.z, zero & 8u ? 0.0f : acc.w);
+    // the residual gets acc: stored first, then the candidates
+    uint32_t bits = 0;
     if (full) {
-      *reinterpret_cast<float4*>(rp + e0) = w;
+      *reinterpret_cast<float4*>(rp + e0) = acc;
+#pragma unroll
+      for (uint32_t q = 0; q < 4; ++q) bits |= (mag_key(av[q]) >= G ? 1u : 0u) << q;
     } else {
-      const float wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
       for (int32_t q = 0; q < 4; ++q)
-        if (in & (1u << q)) rp[e0 + q] = wv[q];
+        if (e0 + q >= lo_r && e0 + q < hi_r) {
+          rp[e0 + q] = av[q];
+          bits |= (mag_key(av[q]) >= G ? 1u : 0u) << q;
+        }
+    }
+    if (__ballot_sync(0xffffffffu, bits) == 0) continue;  // warp-uniform
+    uint32_t tot;
+    const uint32_t pos = run + warp_excl_small(__popc(bits), &tot);
+    run += tot;
+    const uint32_t stored =
+        store_candidates(bits, pos, slot, cidx, cval, base_u + (uint32_t)e0, acc, keep);
+    if constexpr (ANY_LONG) {
+      if (long_seg) {
+#pragma unroll
+        for (uint32_t q = 0; q < 4; ++q)
+          if (((stored >> q) & 1u) && mag_key(av[q]) >= Gm) rp[e0 + q] = 0.0f;
+      }
     }
   }
   // Pad the sub-slot's last 32-byte sector: every sector of candidates is
@@ -806,8 +770,23 @@ __global__ void __launch_bounds__(kStreamThreads, ANY_LONG ? 2 : 3) topk_stream_
   }
   if (lane == 0) {
     a.sub_cnt[sub] = run;
-    if (run) atomicAdd(&a.seg_cnt[gs], run);
     if (run > slot) atomicOr(&a.seg_flag[gs], 1u);
+  }
+  if constexpr (ANY_LONG) {
+    // A long segment's chunks all add to one counter: one add per CTA (the
+    // chunk's warps summed in shared memory), not per warp, keeps that L2
+    // sector from serialising the launch.
+    __shared__ uint32_t cta_run[kWarpsPerChunk];
+    if (lane == 0) cta_run[warp] = run;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint32_t sum = 0;
+#pragma unroll
+      for (uint32_t w = 0; w < kWarpsPerChunk; ++w) sum += cta_run[w];
+      if (sum) atomicAdd(&a.seg_cnt[gs], sum);
+    }
+  } else {
+    if (lane == 0 && run) atomicAdd(&a.seg_cnt[gs], run);
   }
 }
 
