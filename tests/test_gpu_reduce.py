@@ -400,6 +400,35 @@ def test_reduce_hot_head_tiles_with_4bit_values():
         assert np.array_equal(bits(out.val[:U].cpu().numpy()), bits(ref["val"]))
 
 
+def test_reduce_sparse_first_head_tiles_past_staging():
+    """Sparse-first warp tiles (P * cap < N / 4) whose first tiles hold every
+    index: 1,024 union entries, more than the 512 a tile stages for its
+    coalesced output, and 16,384 entries, several load batches. Those tiles
+    take the per-lane output; 4-bit values and unaligned fp32 rows (the
+    scalar warp tiles), bit for bit."""
+    P, N, k, bucket = 16, 1 << 22, 50_000, 512
+    idx, val, nnz = hot_head_streams(P, N, 3_100, k, 11)
+    assert 4 * P * k < N  # the sparse-first form
+    val *= 1e-2
+    seed = W.quant_seed(3)
+    oc, osc = oracle.quantize4(idx, val, nnz, bucket, seed)
+    ref = oracle.sparse_reduce(idx, oracle.dequantize4(oc, osc, nnz, k, bucket), nnz, N)
+    assert not ref["is_dense"]
+    di, dv, dn = streams_to_dev(idx, val, nnz)
+    codes, scales = api.quantize4(di, dv, dn, bucket, seed)
+    out = api.sparse_reduce_q4(di, codes, scales, dn, bucket, N)
+    U = int(out.nnz.item())
+    assert U == ref["nnz"] and not bool(out.is_dense.item())
+    assert np.array_equal(u32(out.idx[:U]), ref["idx"])
+    assert np.array_equal(bits(out.val[:U].cpu().numpy()), bits(ref["val"]))
+    wide = k + 1  # rows no longer 16-byte aligned: the scalar warp tiles
+    i2 = np.zeros((P, wide), np.uint32)
+    v2 = np.zeros((P, wide), np.float32)
+    i2[:, :k], v2[:, :k] = idx, val
+    r = check_reduce(i2, v2, nnz, N, repeat=2)
+    assert not r["is_dense"]
+
+
 def test_reduce_skewed_head_every_warp_tile_path():
     """A Zipf head puts about a thousand entries per node into each of the first
     1,024-index tiles: those tiles are spread over a CTA (dense-first warp-tile
