@@ -637,7 +637,7 @@ __device__ __forceinline__ void load_rounds(float4 (&gv)[NB], float4 (&rv)[NB], 
 }
 
 template <bool UNIFORM, bool ANY_LONG>
-__global__ void __launch_bounds__(kStreamThreads, 3) topk_stream_kernel(Args a) {
+__global__ void __launch_bounds__(kStreamThreads, 4) topk_stream_kernel(Args a) {
   griddep_wait();
   const uint32_t gc = blockIdx.x;
   const uint32_t p = gc / a.nchunk, c = gc - p * a.nchunk;
@@ -665,7 +665,8 @@ __global__ void __launch_bounds__(kStreamThreads, 3) topk_stream_kernel(Args a) 
   const float* gp = a.grad + q0;
   float* rp = a.residual + q0;
   // The warp's rounds in two batches of four whose 128-bit loads are all
-  // issued before any of their entries is used, at three CTAs per SM.
+  // issued before any of their entries is used, at four CTAs per SM (64
+  // registers; five would spill).
   constexpr uint32_t kBatch = kRounds / 2;
   float4 gv[kBatch], rv[kBatch];
   load_rounds<kBatch>(gv, rv, 0, gp, rp, lo_r, hi_r, a.vec, lane);
