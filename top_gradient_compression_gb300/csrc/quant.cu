@@ -161,12 +161,51 @@ quantize_encode_kernel(const uint32_t* __restrict__ idx, const float* __restrict
   const float* sp = scales + (uint64_t)p * scale_stride;
   uint8_t* cp = codes + (uint64_t)p * code_stride;
   const bool aligned = (reinterpret_cast<uintptr_t>(cp) & 3) == 0;
+  // 128-bit loads of a word's entries: rows 16-byte aligned, power-of-two
+  // buckets, no error output
+  const bool vrow = aligned && err_out == nullptr && bucket_shift < 32 &&
+                    ((reinterpret_cast<uintptr_t>(val + row) |
+                      (idx ? reinterpret_cast<uintptr_t>(idx + row) : 0)) & 15) == 0;
+  constexpr uint32_t kE = 4 * kPer;  // entries of one word of codes
   const uint32_t nwords = (code_stride + 3) / 4;
   // each thread: one 32-bit word of codes (4 bytes, 4 * kPer entries)
   for (uint32_t w = blockIdx.x * blockDim.x + threadIdx.x; w < nwords;
        w += gridDim.x * blockDim.x) {
     const uint32_t q0 = 4 * w;
     if (q0 * kPer >= n) break;  // bytes past the row's entries stay untouched
+    const uint32_t j0 = q0 * kPer;  // a multiple of 4
+    if (vrow && q0 + 4 <= code_stride && j0 + kE <= n &&
+        (j0 >> bucket_shift) == ((j0 + kE - 1) >> bucket_shift)) {
+      // The word's entries all lie in the row and in one bucket: one scale,
+      // 128-bit loads, no per-entry checks; the same codes as below.
+      const float m = sp[j0 >> bucket_shift];
+      float v[kE];
+      uint32_t key[kE];
+#pragma unroll
+      for (uint32_t i = 0; i < kE / 4; ++i) {
+        const float4 f = *reinterpret_cast<const float4*>(val + row + j0 + 4 * i);
+        v[4 * i] = f.x;
+        v[4 * i + 1] = f.y;
+        v[4 * i + 2] = f.z;
+        v[4 * i + 3] = f.w;
+        if (idx) {
+          const uint4 q = *reinterpret_cast<const uint4*>(idx + row + j0 + 4 * i);
+          key[4 * i] = q.x;
+          key[4 * i + 1] = q.y;
+          key[4 * i + 2] = q.z;
+          key[4 * i + 3] = q.w;
+        } else {
+#pragma unroll
+          for (uint32_t c = 0; c < 4; ++c) key[4 * i + c] = j0 + 4 * i + c;
+        }
+      }
+      uint32_t word = 0;
+#pragma unroll
+      for (uint32_t e = 0; e < kE; ++e)
+        word |= encode<BITS>(v[e], (uint64_t)key[e], m, node_mix) << (e * BITS);
+      *reinterpret_cast<uint32_t*>(cp + q0) = word;
+      continue;
+    }
     uint32_t word = 0;
 #pragma unroll
     for (uint32_t b = 0; b < 4; ++b) {
